@@ -1,0 +1,97 @@
+"""Smooth-K and 1x16 NVFP4 group quantisation, in float32 as the scheme fixes.
+
+Passages:
+* Page "GPU kernel porting with AI agents", section "Sage Attention 3": the
+  quantisation group is limited to 1x16 (NVFP4) with FP8 e4m3 scale factors;
+  values are FP4 e2m1.
+* Page "kernel overview", SageAttention evolution chain and strengths table:
+  the first technique of the chain is smooth-K -- subtract the mean of K over
+  tokens, per channel, before quantising K; softmax is unchanged by it.
+
+Readings (the pages give no formulas):
+* scale rule: s = e4m3_rne_sat(fl32(max|x| / 6)); codes = e2m1_rne_sat(fl32(x / s));
+  a group whose scale encodes to 0 gets all-(+0) codes.
+* Q and K groups run along the head dimension d; V groups run along tokens
+  (the contraction axis of P.V).
+* the K mean is an FP32 sum in a fixed order -- 128-token chunks summed
+  token by token, then the chunk sums summed chunk by chunk, then divided by
+  L -- so that a kernel following the same order reproduces it bit for bit.
+"""
+
+import numpy as np
+
+from .formats import e2m1_encode, e4m3_encode, e4m3_decode
+
+GROUP = 16
+KMEAN_CHUNK = 128
+
+
+def k_mean(k):
+    """Per-channel mean of K over tokens, FP32, fixed summation order.
+
+    k: float32 array [B, Hkv, L, d] (exact bf16 values).  Returns float32
+    [B, Hkv, d].  Chunk c holds tokens [128c, 128c+128); each chunk is summed
+    token by token from 0.0, the chunk sums are then summed in chunk order
+    from 0.0, and the total is divided by L (IEEE float32 division)."""
+    k = np.asarray(k, dtype=np.float32)
+    B, H, L, d = k.shape
+    nchunk = (L + KMEAN_CHUNK - 1) // KMEAN_CHUNK
+    total = np.zeros((B, H, d), dtype=np.float32)
+    for c in range(nchunk):
+        part = np.zeros((B, H, d), dtype=np.float32)
+        for t in range(c * KMEAN_CHUNK, min(L, (c + 1) * KMEAN_CHUNK)):
+            part = part + k[:, :, t, :]
+        total = total + part
+    return (total / np.float32(L)).astype(np.float32)
+
+
+def quantize_groups(x):
+    """1x16 NVFP4 quantisation along the last axis.
+
+    x: float32 array [..., n] with n % 16 == 0.  Returns (codes, scales):
+    codes uint8 [..., n] e2m1 nibbles, scales uint8 [..., n/16] e4m3 bytes."""
+    x = np.asarray(x, dtype=np.float32)
+    n = x.shape[-1]
+    assert n % GROUP == 0, "group axis must be a multiple of 16"
+    g = x.reshape(x.shape[:-1] + (n // GROUP, GROUP))
+    amax = np.max(np.abs(g), axis=-1)                             # exact
+    s = (amax / np.float32(6.0)).astype(np.float32)               # fl32(a / 6)
+    s8 = e4m3_encode(s)
+    sf = e4m3_decode(s8).astype(np.float32)                       # exact
+    safe = np.where(sf == 0, np.float32(1.0), sf).astype(np.float32)
+    q = (g / safe[..., None]).astype(np.float32)                  # fl32(x / s)
+    codes = e2m1_encode(q)
+    codes = np.where((s8 == 0)[..., None], np.uint8(0), codes).astype(np.uint8)
+    return codes.reshape(x.shape), s8
+
+
+def dequantize_groups(codes, scales):
+    """Inverse of ``quantize_groups`` (exact, float64)."""
+    from .formats import e2m1_decode
+    codes = np.asarray(codes)
+    n = codes.shape[-1]
+    vals = e2m1_decode(codes).reshape(codes.shape[:-1] + (n // GROUP, GROUP))
+    sf = e4m3_decode(scales)
+    return (vals * sf[..., None]).reshape(codes.shape)
+
+
+def quantize_q(q):
+    """Q [B,H,L,d] float32 -> (codes [B,H,L,d], scales [B,H,L,d/16]), groups along d."""
+    return quantize_groups(q)
+
+
+def quantize_k(k, mu):
+    """Smooth-K then quantise: K' = fl32(k - mu[c]); groups along d.
+
+    k [B,Hkv,L,d] float32, mu [B,Hkv,d] float32 (from ``k_mean``)."""
+    kp = (np.asarray(k, np.float32) - np.asarray(mu, np.float32)[:, :, None, :]).astype(np.float32)
+    return quantize_groups(kp)
+
+
+def quantize_v(v):
+    """V [B,Hkv,L,d] -> groups of 16 consecutive tokens per channel.
+
+    Returns codes [B,Hkv,d,L] (channel-major, i.e. V transposed) and
+    scales [B,Hkv,d,L/16]."""
+    vt = np.ascontiguousarray(np.swapaxes(np.asarray(v, np.float32), -1, -2))
+    return quantize_groups(vt)

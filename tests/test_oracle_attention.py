@@ -1,0 +1,227 @@
+"""Pins for the oracle's exact attention and SA3 emulation.
+
+Pinned against: pure-Python brute-force softmax attention on tiny inputs,
+closed forms (L=1, Q=0, a dominant key), invariants (rows of P sum to 1,
+smooth-K shift invariance), hand-worked two-level P cases in
+tests/golden/two_level_p.txt, and reduction to exact attention when every
+quantiser is the identity.
+"""
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import attention as A
+from oracle import formats, quant
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def brute_attention(q, k, v, causal, scale):
+    """Plain loops, math.exp; q [Lq,d], k/v [Lk,d] nested lists."""
+    out = []
+    for i, qi in enumerate(q):
+        s = []
+        for j, kj in enumerate(k):
+            if causal and j > i:
+                continue
+            s.append((j, sum(a * b for a, b in zip(qi, kj)) * scale))
+        mx = max(x for _, x in s)
+        w = [(j, math.exp(x - mx)) for j, x in s]
+        tot = sum(x for _, x in w)
+        out.append([sum(x * v[j][c] for j, x in w) / tot for c in range(len(v[0]))])
+    return out
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_exact_matches_brute_force(causal):
+    rng = np.random.default_rng(11)
+    B, H, Hkv, L, d = 1, 4, 2, 9, 5
+    q = rng.standard_normal((B, H, L, d))
+    k = rng.standard_normal((B, Hkv, L, d))
+    v = rng.standard_normal((B, Hkv, L, d))
+    o = A.exact_attention(q, k, v, causal)
+    for h in range(H):
+        ref = brute_attention(q[0, h].tolist(), k[0, h // 2].tolist(), v[0, h // 2].tolist(),
+                              causal, 1 / math.sqrt(d))
+        assert np.allclose(o[0, h], ref, rtol=0, atol=1e-13)
+
+
+def test_exact_row_subset_and_blocking():
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((1, 2, 70, 8))
+    k = rng.standard_normal((1, 2, 70, 8))
+    v = rng.standard_normal((1, 2, 70, 8))
+    full = A.exact_attention(q, k, v, True, block=16)
+    rows = np.array([0, 5, 33, 69])
+    sub = A.exact_attention(q, k, v, True, rows=rows)
+    assert np.allclose(full[:, :, rows], sub, atol=1e-14)
+
+
+def test_closed_forms():
+    rng = np.random.default_rng(4)
+    d = 16
+    v = rng.standard_normal((1, 1, 1, d))
+    q1 = rng.standard_normal((1, 1, 1, d))
+    k1 = rng.standard_normal((1, 1, 1, d))
+    assert np.allclose(A.exact_attention(q1, k1, v, False), v, atol=1e-15)      # L=1 -> O=V
+    L = 40
+    q0 = np.zeros((1, 1, L, d))
+    k = rng.standard_normal((1, 1, L, d))
+    v = rng.standard_normal((1, 1, L, d))
+    assert np.allclose(A.exact_attention(q0, k, v, False)[0, 0], v[0, 0].mean(0), atol=1e-14)
+    pref = np.cumsum(v[0, 0], axis=0) / np.arange(1, L + 1)[:, None]
+    assert np.allclose(A.exact_attention(q0, k, v, True)[0, 0], pref, atol=1e-14)
+    # one dominant key: O ~ V_j
+    q = np.zeros((1, 1, 1, d)); q[..., 0] = 60.0
+    kk = np.zeros((1, 1, L, d)); kk[0, 0, 17, 0] = 60.0
+    assert np.allclose(A.exact_attention(q, kk, v, False)[0, 0, 0], v[0, 0, 17], atol=1e-12)
+
+
+def test_rows_of_p_sum_to_one():
+    # feed V = ones: O = sum_j P_ij * 1 = 1 for every row
+    rng = np.random.default_rng(9)
+    q = rng.standard_normal((1, 2, 50, 8)) * 3
+    k = rng.standard_normal((1, 2, 50, 8)) * 3
+    v = np.ones((1, 2, 50, 8))
+    for causal in (False, True):
+        assert np.allclose(A.exact_attention(q, k, v, causal), 1.0, atol=1e-14)
+        assert np.allclose(A.sa3_emulated_attention(q, k, v, causal, bc=16, quantize_p=False), 1.0,
+                           atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_smooth_k_shift_invariance(causal):
+    rng = np.random.default_rng(6)
+    q = rng.standard_normal((1, 2, 64, 16))
+    k = rng.standard_normal((1, 2, 64, 16))
+    v = rng.standard_normal((1, 2, 64, 16))
+    mu = rng.standard_normal((1, 2, 1, 16)) * 5
+    a = A.exact_attention(q, k, v, causal)
+    b = A.exact_attention(q, k - mu, v, causal)
+    assert np.allclose(a, b, atol=1e-12)
+
+
+@pytest.mark.parametrize("bc", [16, 32, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_emulation_without_quantisers_is_exact(bc, causal):
+    rng = np.random.default_rng(8)
+    B, H, Hkv, L, d = 1, 4, 2, 96, 16
+    q = rng.standard_normal((B, H, L, d)) * 2
+    k = rng.standard_normal((B, Hkv, L, d)) * 2
+    v = rng.standard_normal((B, Hkv, L, d))
+    e = A.sa3_emulated_attention(q, k, v, causal, bc=bc, quantize_p=False)
+    x = A.exact_attention(q, k, v, causal)
+    assert np.allclose(e, x, atol=1e-12)
+
+
+def test_emulation_q_zero_gives_mean_of_vhat():
+    # Q = 0: every logit is 0, P2 = 2688 everywhere, every P code is 6 (0x7) with
+    # scale 448 (0x7E), so O = mean of the (dequantised) V^ rows, or the prefix
+    # mean under the causal mask.
+    rng = np.random.default_rng(12)
+    L, d = 64, 16
+    vc, vs = quant.quantize_groups(rng.standard_normal((1, 1, d, L)).astype(np.float32))
+    vhat = np.swapaxes(quant.dequantize_groups(vc, vs), -1, -2)      # on the FP4 grid
+    q = np.zeros((1, 1, L, d))
+    k = rng.standard_normal((1, 1, L, d))
+    dbg = []
+    o = A.sa3_tile_rows(q[0, 0], k[0, 0], vhat[0, 0], np.arange(L), False, bc=32, debug=dbg)
+    assert np.allclose(o, vhat[0, 0].mean(0), rtol=0, atol=1e-14)
+    for t in dbg:
+        assert np.all(t["scales"] == 0x7E)
+        assert np.all(t["p2"] == np.float32(2688.0))
+    oc = A.sa3_tile_rows(q[0, 0], k[0, 0], vhat[0, 0], np.arange(L), True, bc=32)
+    pref = np.cumsum(vhat[0, 0], axis=0) / np.arange(1, L + 1)[:, None]
+    assert np.allclose(oc, pref, rtol=0, atol=1e-14)
+
+
+def test_max_group_scale_is_448():
+    # the 1x16 group holding a tile's row maximum always gets s2 = 448 (0x7E)
+    rng = np.random.default_rng(21)
+    L, d = 256, 32
+    q = rng.standard_normal((8, d)) * 2
+    k = rng.standard_normal((L, d)) * 2
+    v = rng.standard_normal((L, d))
+    dbg = []
+    A.sa3_tile_rows(q, k, v, np.arange(8) + 200, True, bc=64, debug=dbg)
+    for t in dbg:
+        live = np.isfinite(t["m_t"])
+        arg = np.argmax(t["p2"], axis=1)
+        for r in np.flatnonzero(live):
+            assert t["scales"][r, arg[r] // 16] == 0x7E
+            assert t["p2"][r, arg[r]] == np.float32(2688.0)
+
+
+def _gold_p():
+    g = {}
+    cases = []
+    with open(os.path.join(GOLD, "two_level_p.txt")) as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            if key == "case":
+                cases.append((vals[0], [int(t) for t in vals[2:]]))
+            else:
+                g[key] = vals
+    return g, cases
+
+
+@pytest.mark.parametrize("case", [c[0] for c in _gold_p()[1]])
+def test_two_level_p_hand_worked(case):
+    g, cases = _gold_p()
+    tiles = dict(cases)[case]
+    w = np.array([float(Fraction(x)) for x in g["w"]])
+    l0 = 2.0 - 2.0 ** -15
+    n = len(tiles)
+    L, d = 16 * n, 16
+    # one query row; q = e0, key k of tile i = (t_i - k) e0 so the raw score is t_i - k;
+    # the scale 1/log2(e) makes the base-2 logit equal the raw score.
+    q = np.zeros((1, d)); q[0, 0] = 1.0
+    kk = np.zeros((L, d))
+    for i, t in enumerate(tiles):
+        kk[16 * i:16 * i + 16, 0] = t - np.arange(16)
+    rng = np.random.default_rng(31)
+    v = rng.standard_normal((L, d))
+    dbg = []
+    o = A.sa3_tile_rows(q, kk, v, np.array([L - 1]), False, bc=16, scale=1.0 / A.LOG2E, debug=dbg)
+    tmax = max(tiles)
+    f = np.array([2.0 ** (t - tmax) for t in tiles])
+    num = sum(f[i] * (w @ v[16 * i:16 * i + 16]) for i in range(n))
+    expect = num / (f.sum() * l0)
+    assert np.allclose(o[0], expect, rtol=0, atol=1e-13)
+    for t in dbg:
+        assert int(t["scales"][0, 0]) == int(g["group_scale"][0], 16)
+        codes, _ = quant.quantize_groups(t["p2"])
+        assert [int(c) for c in codes[0]] == [int(c, 16) for c in g["group_codes"]]
+
+
+def test_gqa_head_mapping():
+    rng = np.random.default_rng(14)
+    q = rng.standard_normal((1, 6, 20, 8))
+    k = rng.standard_normal((1, 2, 20, 8))
+    v = rng.standard_normal((1, 2, 20, 8))
+    o = A.exact_attention(q, k, v, False)
+    kr = np.repeat(k, 3, axis=1)
+    vr = np.repeat(v, 3, axis=1)
+    assert np.allclose(o, A.exact_attention(q, kr, vr, False), atol=1e-15)
+    e = A.sa3_emulated_attention(q, k, v, True, bc=16)
+    er = A.sa3_emulated_attention(q, kr, vr, True, bc=16)
+    assert np.array_equal(e, er)
+
+
+def test_quantised_pipeline_is_close_to_exact_on_iid_inputs():
+    # sanity: the full scheme on i.i.d. N(0,1) data tracks exact attention
+    rng = np.random.default_rng(0)
+    q = rng.standard_normal((1, 2, 256, 64)).astype(np.float32)
+    k = rng.standard_normal((1, 2, 256, 64)).astype(np.float32)
+    v = rng.standard_normal((1, 2, 256, 64)).astype(np.float32)
+    (qd, kd, vd), _ = A.dequantized_operands(q, k, v)
+    e = A.sa3_emulated_attention(qd, kd, vd, False)
+    x = A.exact_attention(q, k, v, False)
+    cos = A.cosine_per_head(e, x)
+    assert np.all(cos > 0.95)
