@@ -1,0 +1,347 @@
+"""Benchmark of the SageAttention3-style attention forward on GB300.
+
+One step = one pass of the whole hot path over one batch of the LLM-prefill
+workload (B=2, H=16, L=4096, d=128, non-causal; K carries a per-channel bias):
+  sa_quantize (smooth-K mean + NVFP4 quantisation of Q, K, V)
+  -> sa_attn_fwd NVFP4 (block-scaled FP4 tcgen05 MMAs, two-level P quantisation)
+  -> sa_attn_fwd BF16 (the exact path).
+`value` is the NVFP4 path's throughput, 4*B*H*L^2*d / (quantise + fused attention
+time), in TOPS, with inputs resident in HBM; the L2 is flushed (256 MB write)
+before every step.  `e2e` is the same metric through the public API with host
+buffers: pinned-host -> device copies of Q, K, V, the two calls, and the copy of
+O back, inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch with torch.distributed.run (one rank per GPU); every rank runs
+its own independent batch (weak scaling, no collective on the data path) and
+rank 0 prints the max-over-ranks time.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+WORKLOAD = "llm_prefill"
+METRIC = "attention fwd TOPS (4BHL^2d/time), NVFP4 and BF16 paths, 1 GB300; % of peak"
+NVFP4_OVER_BF16 = 6.0      # nominal dense FP4 : BF16 tensor ratio on GB300 (13.5 / 2.25 PFLOP/s)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sus=p.get("bf16_tflops_sustained"),
+                    src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu):
+        self.gpu = gpu
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.p:
+            self.p.terminate()
+            self.p.wait()
+
+    def summary(self):
+        self.f.seek(0)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            c = [x.strip() for x in line.split(",")]
+            if len(c) < 9:
+                continue
+            try:
+                sm.append(float(c[1]))
+                mx = float(c[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, c[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_sample(w, heads, nrows, seed=0):
+    """Times the oracle (NVFP4 quantiser + tile-by-tile SA3 emulation, as it
+    stands) on `heads` heads x `nrows` query rows of the workload; returns
+    (seconds, counted flops of the sampled rows, description)."""
+    import numpy as np
+    from oracle import attention as A
+    x = W.make_inputs(w)
+    rows = np.array(W.sample_rows(w["L"], nrows, seed=seed))
+    G = w["H"] // w["Hkv"]
+    t0 = time.perf_counter()
+    for h in range(heads):
+        q = x["q"][0:1, h:h + 1].float().numpy()
+        k = x["k"][0:1, h // G:h // G + 1].float().numpy()
+        v = x["v"][0:1, h // G:h // G + 1].float().numpy()
+        (qd, kd, vd), _ = A.dequantized_operands(q, k, v)
+        A.sa3_emulated_attention(qd, kd, vd, w["causal"], rows=rows)
+    dt = time.perf_counter() - t0
+    fl = 4.0 * heads * len(rows) * w["L"] * w["d"] / (2 if w["causal"] else 1)
+    desc = (f"{heads} head(s) x {len(rows)} query rows of {w['name']} (full-length keys): NumPy oracle "
+            "quantiser (K mean, Q/K/V NVFP4) + SA3 tile-by-tile emulation")
+    return dt, fl, desc
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = W.spec(args.workload)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        dt, fl, desc = cpu_oracle_sample(w, heads=1, nrows=64, seed=i)
+        if i >= args.warmup:
+            vals.append(fl / dt / 1e12)
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64/f32 (CPU oracle)", "data": "synthetic",
+            "config": {"workload": f"{w['name']}: B={w['B']} H={w['H']} Hkv={w['Hkv']} L={w['L']} d={w['d']} "
+                                   f"{'causal' if w['causal'] else 'non-causal'}", "sample": desc},
+            "cpu_baseline": {"value": v, "unit": "TOPS", "cores": host_cores(), "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import quantized_attention_x16_gb300 as sa
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = W.spec(args.workload, seed=W.spec(args.workload)["seed"] + 1000 * rank)   # independent batch per rank
+    B, H, Hkv, L, d = w["B"], w["H"], w["Hkv"], w["L"], w["d"]
+    x = W.make_inputs(w)
+    q, k, v = (x[n].to(dev) for n in "qkv")
+    fq = sa.FP4QKV(B, H, Hkv, L, d, device=dev)
+    o4 = torch.empty_like(q)
+    o16 = torch.empty_like(q)
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+    fl = W.flops(w)
+    causal = w["causal"]
+
+    def step(ev):
+        ev[0].record()
+        sa.sa_quantize(q, k, v, out=fq)
+        ev[1].record()
+        sa.sa_attn_fwd(fq, o=o4, causal=causal, mode="nvfp4")
+        ev[2].record()
+        sa.sa_attn_fwd(q, k, v, o=o16, causal=causal, mode="bf16")
+        ev[3].record()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+    torch.cuda.synchronize()
+    assert sa.sa_last_device_error() == sa.SA_OK
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local_rank) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            step(evs[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    launches = args.steps * (4 + 1 + 1)      # sa_quantize: 4 kernels; each attention call: 1
+    tq = [a[0].elapsed_time(a[1]) * 1e-3 for a in evs]
+    t4 = [a[1].elapsed_time(a[2]) * 1e-3 for a in evs]
+    t16 = [a[2].elapsed_time(a[3]) * 1e-3 for a in evs]
+    mean = lambda xs: sum(xs) / len(xs)   # noqa: E731
+    t_q, t_4, t_16 = mean(tq), mean(t4), mean(t16)
+    t_path = t_q + t_4
+    if world > 1:
+        tt = torch.tensor([t_path, t_q, t_4, t_16], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_path, t_q, t_4, t_16 = tt.tolist()
+    assert sa.sa_last_device_error() == sa.SA_OK
+
+    # ---- end to end through the public API with host buffers (same metric)
+    hq, hk, hv = (x[n].pin_memory() for n in "qkv")
+    ho = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size()
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        sa.sa_quantize(dq, dk, dv, out=fq)
+        sa.sa_attn_fwd(fq, o=o4, causal=causal, mode="nvfp4")
+        ho.copy_(o4, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    t_e2e = e0.elapsed_time(e1) * 1e-3 / args.steps
+    if world > 1:
+        tt = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = tt.item()
+
+    if rank != 0:
+        return
+    pk = peaks()
+    nvfp4_peak = pk["bf16"] * NVFP4_OVER_BF16
+    a4 = fl / t_4 / 1e12
+    a16 = fl / t_16 / 1e12
+    qbytes = quant_bytes(w)
+    clocks = clk.summary()
+    prof = load_profile_traffic()
+    cpu = None
+    if not args.skip_cpu_baseline:
+        cpu_dt, cpu_fl, cpu_desc = cpu_oracle_sample(w, heads=2, nrows=128)
+        cpu = {"value": cpu_fl / cpu_dt / 1e12, "unit": "TOPS", "cores": host_cores(), "kind": "oracle",
+               "sample": cpu_desc, "seconds": cpu_dt}
+    line = {
+        "metric": METRIC,
+        "value": world * fl / t_path / 1e12,
+        "unit": "TOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": (t_q + t_4 + t_16) * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "nvfp4 (e2m1 x e4m3-scaled, fp32 accumulate); bf16 path alongside",
+        "data": "synthetic (seeded torch.Generator, bf16)",
+        "config": {"workload": f"{w['name']}: B={B} H={H} Hkv={Hkv} L={L} d={d} "
+                               f"{'causal' if causal else 'non-causal'} ({w['kind']} inputs)",
+                   "B": B, "H": H, "Hkv": Hkv, "L": L, "d": d, "causal": causal,
+                   "l2": "flushed by a 256 MB write before every step",
+                   "value_def": "4*B*H*L^2*d / (sa_quantize + NVFP4 sa_attn_fwd) per GPU, summed over GPUs",
+                   "parallelism": f"independent batch per GPU ({world} GPU)"},
+        "paths": {
+            "nvfp4_attn_only_tops": a4,
+            "nvfp4_attn_us": t_4 * 1e6,
+            "quantize_us": t_q * 1e6,
+            "quantize_gbs": qbytes / t_q / 1e9,
+            "nvfp4_end_to_end_tops": fl / t_path / 1e12,
+            "bf16_tflops": a16,
+            "bf16_attn_us": t_16 * 1e6,
+            "bf16_frac_of_measured_peak": a16 / pk["bf16"],
+        },
+        "roofline": {"kernel": f"attn_nvfp4_kernel<{d}>", "bound": "tensor", "achieved": a4, "peak": nvfp4_peak,
+                     "unit": "TFLOP/s", "frac": a4 / nvfp4_peak,
+                     "traffic": prof.get("attn_nvfp4"),
+                     "peak_src": f"{pk['src']} bf16 burst {pk['bf16']} x nominal FP4:BF16 ratio {NVFP4_OVER_BF16}"},
+        "roofline_bf16": {"kernel": f"attn_bf16_kernel<{d}>", "bound": "tensor", "achieved": a16, "peak": pk["bf16"],
+                          "unit": "TFLOP/s", "frac": a16 / pk["bf16"], "traffic": prof.get("attn_bf16"),
+                          "peak_src": f"{pk['src']} bf16 burst"},
+        "roofline_quantize": {"kernel": "sa_quantize (4 kernels)", "bound": "hbm", "achieved": qbytes / t_q / 1e9,
+                              "peak": pk["hbm"], "unit": "GB/s", "frac": qbytes / t_q / 1e9 / pk["hbm"],
+                              "traffic": prof.get("quantize"), "algorithmic_bytes": qbytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * fl / t_e2e / 1e12, "unit": "TOPS", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def quant_bytes(w):
+    """Algorithmic HBM bytes of sa_quantize: read Q, K, V (bf16) + K again for the
+    mean, write codes (0.5 B/elem) and scales (1/16 B/elem), the mean and its partials."""
+    B, H, Hkv, L, d = w["B"], w["H"], w["Hkv"], w["L"], w["d"]
+    nq, nk = B * H * L * d, B * Hkv * L * d
+    reads = 2 * nq + 2 * nk * 2 + 2 * nk
+    writes = (nq + 2 * nk) * (0.5 + 1 / 16)
+    return reads + writes
+
+
+def load_profile_traffic():
+    """DRAM bytes per launch recorded from ncu captures (profiles/traffic.json), if present."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            return json.load(f)
+    except Exception:
+        return {}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(W.WORKLOADS),
+                    help="another workload (profiling and sweeps; the headline is llm_prefill)")
+    ap.add_argument("--skip-cpu-baseline", action="store_true",
+                    help="omit the oracle timing (profiling runs)")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

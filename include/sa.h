@@ -1,0 +1,164 @@
+/*
+ * sa.h -- C ABI of the GB300 (sm_103a) SageAttention3-style attention library.
+ *
+ * What it computes (source pages, by title and section):
+ *  - "FlashAttention kernels", sections 0-1: exact softmax attention computed
+ *    tile by tile with online softmax, never materialising the L x L scores.
+ *  - "GPU kernel porting with AI agents", section "Sage Attention 3": Q, K, V
+ *    in NVFP4 (e2m1 values, 1x16 groups, FP8 e4m3 scales); P quantised in two
+ *    levels (per-row rescale to [0, 448 x 6], then FP4 microscaling).
+ *  - "kernel overview", SageAttention technique chain: smooth-K (subtract the
+ *    per-channel mean of K over tokens before quantising K).
+ *  - "cuda kernel pretrain", section 3: GQA -- query head h uses KV head
+ *    h / (H / Hkv).
+ *
+ * Conventions for every entry point:
+ *  - Tensors are device pointers, row-major, BHLD: Q and O are [B, H, L, d],
+ *    K and V are [B, Hkv, L, d], all bfloat16.  The softmax scale is
+ *    1/sqrt(d); causal means key j is visible to query i iff j <= i.
+ *  - Ownership: the caller allocates and owns every buffer.  The library
+ *    allocates no device memory and keeps no state between calls other than
+ *    a device error word (see sa_last_device_error).
+ *  - Asynchrony: work is enqueued on `stream` (NULL = legacy default stream)
+ *    and the call returns before it finishes.
+ *  - Errors: arguments are validated before anything is enqueued; on any
+ *    argument error nothing is launched.  SA_ERR_INVALID_ARG: null or
+ *    misaligned pointer (all pointers must be 16-byte aligned), non-positive
+ *    size, H % Hkv != 0.  SA_ERR_UNSUPPORTED: d not in {64, 128} or L not a
+ *    multiple of 128.  SA_ERR_CUDA: a launch or driver call failed (the CUDA
+ *    error is not cleared).
+ *  - Inputs are assumed finite; NaN/Inf inputs give unspecified results.
+ */
+#ifndef SA_H_
+#define SA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* sa_stream_t;   /* same handle as cudaStream_t */
+
+typedef enum {
+  SA_OK = 0,
+  SA_ERR_INVALID_ARG = 1,
+  SA_ERR_UNSUPPORTED = 2,
+  SA_ERR_CUDA = 3,
+  SA_ERR_TIMEOUT = 4
+} sa_status;
+
+typedef enum { SA_MODE_BF16 = 0, SA_MODE_NVFP4 = 1 } sa_mode;
+
+/* Output-format flag OR-ed into the `mode` argument of sa_attn_fwd: with it,
+ * o is float32 [B, H, L, d] (the FP32 accumulator divided by the row sum,
+ * without the final bf16 rounding); without it o is bfloat16. */
+#define SA_OUT_FP32 16
+
+/*
+ * Quantised operands produced by sa_quantize (device pointers, caller-owned).
+ *
+ * Codes: two e2m1 nibbles per byte, element 2i in the low nibble.
+ *   q_codes [B, H, L, d/2]    Q, groups of 16 along d
+ *   k_codes [B, Hkv, L, d/2]  K' = K - mean_tokens(K), groups along d
+ *   v_codes [B, Hkv, d, L/2]  V transposed (channel rows), groups of 16
+ *                             consecutive tokens
+ * Scale factors (e4m3 bytes) in 512-byte blocks of 128 rows x 4 groups; the
+ * byte at m0*16 + j*4 + k of a block is the scale of row 32*j + m0, group k:
+ *   q_sf [B, H, L/128, d/64, 512]   rows = tokens, groups = d/16 along d
+ *   k_sf [B, Hkv, L/128, d/64, 512]
+ *   v_sf [B, Hkv, L/64, 512]        rows = channels (rows >= d are 0),
+ *                                   groups = 16-token groups of a 64-token chunk
+ * k_mean [B, Hkv, d] float32: the smooth-K mean, computed as the float32 sum
+ *   over 128-token chunks (token order inside a chunk, then chunk order)
+ *   divided by L.
+ * workspace: scratch for sa_quantize (float32 [B, Hkv, L/128, d] partial sums).
+ * This is the layout the tcgen05 block-scaled MMA consumes (scale blocks are
+ * copied to tensor memory unchanged).
+ */
+typedef struct {
+  void* q_codes;
+  void* q_sf;
+  void* k_codes;
+  void* k_sf;
+  void* v_codes;
+  void* v_sf;
+  float* k_mean;
+  void* workspace;
+} sa_fp4_qkv;
+
+/*
+ * Bytes of one device blob holding every sa_fp4_qkv buffer, each at a
+ * 256-byte aligned offset.  offsets_out (may be NULL) receives 8 offsets in
+ * struct order (q_codes, q_sf, k_codes, k_sf, v_codes, v_sf, k_mean,
+ * workspace).  Returns 0 for unsupported sizes.
+ */
+size_t sa_fp4_qkv_bytes(int B, int H, int Hkv, int L, int d, size_t offsets_out[8]);
+
+/* Fill `out` with pointers into `blob` (device memory of sa_fp4_qkv_bytes). */
+sa_status sa_fp4_qkv_from_blob(void* blob, int B, int H, int Hkv, int L, int d,
+                               sa_fp4_qkv* out);
+
+/*
+ * sa_quantize -- smooth-K mean, then NVFP4 quantisation of Q, K' and V
+ * ("Sage Attention 3" section of "GPU kernel porting with AI agents";
+ * smooth-K from "kernel overview").  For every 1x16 group x (float32):
+ *   s8 = e4m3_rne_satfinite(max|x| / 6)      (IEEE float32 division)
+ *   code_i = e2m1_rne_satfinite(x_i / decode(s8)); all codes +0 if s8 == 0
+ * with K' = float32(k) - k_mean[c].  Results are bit-exact functions of the
+ * inputs.  q, k, v: bf16 BHLD device tensors; out: buffers as documented
+ * above (all eight pointers required).  Enqueues 4 kernels on `stream`.
+ */
+sa_status sa_quantize(const void* q, const void* k, const void* v,
+                      int B, int H, int Hkv, int L, int d,
+                      const sa_fp4_qkv* out, sa_stream_t stream);
+
+/*
+ * sa_attn_fwd -- fused attention forward, O = softmax(Q K^T / sqrt(d)) V,
+ * tile by tile with online softmax ("FlashAttention kernels" sections 0-1).
+ *  mode SA_MODE_BF16:  q, k, v are bf16 BHLD device tensors; tcgen05 BF16
+ *    MMAs with FP32 accumulation; P rounded to bf16 for the P.V product.
+ *  mode SA_MODE_NVFP4: q points to a host `const sa_fp4_qkv*` produced by
+ *    sa_quantize for the same sizes; k and v must be NULL.  QK^T and P.V are
+ *    tcgen05 block-scaled FP4 MMAs (FP32 accumulation); P is quantised in
+ *    two levels in the kernel ("Sage Attention 3"): per row and 128-key
+ *    tile, P2 = p~ * 2688 / rowmax_tile(p~), then 1x16 e2m1 groups along the
+ *    keys with e4m3 scales; the tile's P.V is weighted by rowmax/2688.
+ *  o: bf16 [B, H, L, d] device output (float32 if mode has SA_OUT_FP32).
+ *  causal: 0 or 1 (top-left aligned).
+ *  Heads map as GQA: head h reads KV head h / (H / Hkv).
+ */
+sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o,
+                      int B, int H, int Hkv, int L, int d, int causal,
+                      int mode, sa_stream_t stream);
+
+/* Static string for a status code. */
+const char* sa_status_string(sa_status s);
+
+/*
+ * Reads and clears the device error word on the current device
+ * (synchronises the device).  Kernels bound every wait on a barrier; a wait
+ * that gives up records SA_ERR_TIMEOUT here and the kernel returns early, so
+ * its output is then invalid.  Returns SA_OK if no kernel recorded an error,
+ * SA_ERR_CUDA if the word could not be read.
+ */
+sa_status sa_last_device_error(void);
+
+/*
+ * Self-test of the bounded-wait path used by every kernel: launches one CTA
+ * that waits, with the given limit (nanoseconds, 1..10^10), on a
+ * shared-memory barrier that nothing completes.  The wait gives up, records
+ * SA_ERR_TIMEOUT in the device error word and the kernel returns normally,
+ * leaving the context usable.  Read the result with sa_last_device_error().
+ */
+sa_status sa_selftest_wait_timeout(uint64_t limit_ns, sa_stream_t stream);
+
+/* Library version string. */
+const char* sa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SA_H_ */

@@ -21,7 +21,7 @@ unquantised p~; the P.V products of a tile are multiplied by s1.
 
 import numpy as np
 
-from .quant import quantize_groups, dequantize_groups
+from .quant import quantize_groups, dequantize_groups, quantize_groups_spread
 
 LOG2E = 1.4426950408889634
 P_RANGE = 448.0 * 6.0          # the [0, 448 x 6] target range of the first level
@@ -64,7 +64,7 @@ def exact_attention(q, k, v, causal, scale=None, rows=None, block=1024):
 
 
 def sa3_tile_rows(qrows, kh, vh, row_idx, causal, bc=128, scale=None,
-                  quantize_p=True, debug=None):
+                  quantize_p=True, debug=None, tie_rel=0.0, return_bound=False):
     """SA3 emulation for a set of query rows of one head.
 
     qrows [n, d]: dequantised Q^ rows; kh [L, d]: dequantised smoothed K^';
@@ -82,7 +82,14 @@ def sa3_tile_rows(qrows, kh, vh, row_idx, causal, bc=128, scale=None,
       acc   = alpha*acc + s1 * (P^ V^_tile)
     and finally O = acc / l.  Rows with no visible key in a tile skip it.
     With quantize_p=False the second level is the identity (P^ = P2).
-    ``debug`` (a list) receives per-tile dicts for pins."""
+    ``debug`` (a list) receives per-tile dicts for pins.
+
+    return_bound=True also returns, per output element, a bound on how far O
+    can move when P2 is known only to a relative error ``tie_rel`` (any
+    implementation computes the exponentials and the scores with its own
+    rounding): every P quantisation decision within tie_rel of a rounding
+    boundary may go either way, and the bound adds |change of P^| * s1 * |V^|
+    over those decisions, carried through the same rescaling as acc."""
     qrows = np.asarray(qrows, np.float64)
     n, d = qrows.shape
     L = kh.shape[0]
@@ -93,6 +100,7 @@ def sa3_tile_rows(qrows, kh, vh, row_idx, causal, bc=128, scale=None,
     m = np.full(n, -np.inf)
     l = np.zeros(n)
     acc = np.zeros((n, d))
+    bnd = np.zeros((n, d))
     row_idx = np.asarray(row_idx)
     for j0 in range(0, L, bc):
         j1 = min(L, j0 + bc)
@@ -116,6 +124,9 @@ def sa3_tile_rows(qrows, kh, vh, row_idx, causal, bc=128, scale=None,
             p2p = np.concatenate([p2, np.zeros((n, padw), np.float32)], axis=1) if padw else p2
             codes, sc = quantize_groups(p2p)
             ph = dequantize_groups(codes, sc)[:, :width]
+            if return_bound:
+                _, spread = quantize_groups_spread(p2p, tie_rel)
+                bnd = alpha[:, None] * bnd + s1[:, None] * (spread[:, :width] @ np.abs(np.asarray(vh[j0:j1], np.float64)))
         else:
             ph = p2                              # identity second level, FP64
             sc = None
@@ -124,26 +135,35 @@ def sa3_tile_rows(qrows, kh, vh, row_idx, causal, bc=128, scale=None,
         m = m_new
         if debug is not None:
             debug.append(dict(j0=j0, m_t=m_t, s1=s1, p2=p2, scales=sc, phat=ph))
+    if return_bound:
+        return acc / l[:, None], bnd / l[:, None]
     return acc / l[:, None]
 
 
 def sa3_emulated_attention(qd, kd, vd, causal, bc=128, scale=None, rows=None,
-                           quantize_p=True):
+                           quantize_p=True, tie_rel=0.0, return_bound=False):
     """Tile-by-tile SA3 emulation over all heads.
 
     qd [B,H,L,d], kd [B,Hkv,L,d], vd [B,Hkv,L,d]: dequantised Q^, K^' (after
-    smooth-K) and V^ (token-major), float64.  Returns [B, H, len(rows), d]."""
+    smooth-K) and V^ (token-major), float64.  Returns [B, H, len(rows), d]
+    (and the decision-ambiguity bound of ``sa3_tile_rows`` if asked)."""
     qd = np.asarray(qd, np.float64)
     B, H, L, d = qd.shape
     Hkv = kd.shape[1]
     rows = np.arange(L) if rows is None else np.asarray(rows)
     out = np.empty((B, H, len(rows), d), np.float64)
+    bound = np.zeros_like(out)
     for b in range(B):
         for h in range(H):
             kh = _kv_head(h, H, Hkv)
-            out[b, h] = sa3_tile_rows(qd[b, h, rows], kd[b, kh], vd[b, kh], rows,
-                                      causal, bc=bc, scale=scale, quantize_p=quantize_p)
-    return out
+            r = sa3_tile_rows(qd[b, h, rows], kd[b, kh], vd[b, kh], rows, causal, bc=bc,
+                              scale=scale, quantize_p=quantize_p, tie_rel=tie_rel,
+                              return_bound=return_bound)
+            if return_bound:
+                out[b, h], bound[b, h] = r
+            else:
+                out[b, h] = r
+    return (out, bound) if return_bound else out
 
 
 def dequantized_operands(q, k, v):

@@ -20,7 +20,7 @@ Readings (the pages give no formulas):
 
 import numpy as np
 
-from .formats import e2m1_encode, e4m3_encode, e4m3_decode
+from .formats import E2M1_MAGNITUDES, e2m1_encode, e4m3_encode, e4m3_decode
 
 GROUP = 16
 KMEAN_CHUNK = 128
@@ -95,3 +95,47 @@ def quantize_v(v):
     scales [B,Hkv,d,L/16]."""
     vt = np.ascontiguousarray(np.swapaxes(np.asarray(v, np.float32), -1, -2))
     return quantize_groups(vt)
+
+
+#: e2m1 rounding boundaries (midpoints between neighbouring magnitudes) and
+#: the gap between the two neighbours
+E2M1_MIDPOINTS = ((E2M1_MAGNITUDES[1:] + E2M1_MAGNITUDES[:-1]) / 2,
+                  E2M1_MAGNITUDES[1:] - E2M1_MAGNITUDES[:-1])
+
+
+def quantize_groups_spread(x, rel):
+    """Decision ambiguity of ``quantize_groups`` under relative input error.
+
+    When the group inputs are only known to a relative error below ``rel``
+    (another implementation computes them with different rounding), a value
+    close to a rounding boundary may legitimately land on either side: a code
+    within rel of an e2m1 midpoint, or a scale whose argument max|x|/6 lies
+    within rel of an e4m3 midpoint.  Returns (deq, spread): the dequantised
+    groups of ``quantize_groups`` (float64, shape of x) and, per element, the
+    largest change of its dequantised value over every such alternative
+    decision (0 where the decision is unambiguous; rel = 0 gives all zeros)."""
+    x = np.asarray(x, dtype=np.float32)
+    n = x.shape[-1]
+    g = x.reshape(x.shape[:-1] + (n // GROUP, GROUP)).astype(np.float64)
+    codes, s8 = quantize_groups(x)
+    base = dequantize_groups(codes, s8).reshape(g.shape)
+    spread = np.zeros(g.shape)
+    if rel <= 0:
+        return base.reshape(x.shape), spread.reshape(x.shape)
+    amax = np.max(np.abs(g), axis=-1)
+    mids, gaps = E2M1_MIDPOINTS
+    for s8c in (e4m3_encode(amax / 6 * (1 - rel)), s8, e4m3_encode(amax / 6 * (1 + rel))):
+        sf = e4m3_decode(s8c)[..., None]
+        safe = np.where(sf > 0, sf, 1.0)
+        v = np.abs(g) / safe
+        alt = np.where(sf > 0, np.sign(g) * e2m1_decode_mag(v) * sf, 0.0)
+        near = np.abs(v[..., None] - mids) < rel * mids                   # [..., 16, 7]
+        tie = np.max(np.where(near, gaps, 0.0), axis=-1) * np.where(sf > 0, sf, 0.0)
+        spread = np.maximum(spread, np.abs(alt - base) + tie)
+    return base.reshape(x.shape), spread.reshape(x.shape)
+
+
+def e2m1_decode_mag(v):
+    """Magnitude of the e2m1 value nearest to v >= 0 (ties to even, saturating)."""
+    from .formats import e2m1_decode
+    return e2m1_decode(e2m1_encode(v) & 0x7)

@@ -1,0 +1,199 @@
+"""Python binding of libsa, the GB300 (sm_103a) SageAttention3-style attention library.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/sa.h``.  PyTorch provides
+device memory and streams.  Importing this package loads ``libsa.so`` from
+this directory and raises ``ImportError`` if it has not been built (build it
+with ``python -m quantized_attention_x16_gb300.build``); there is no CPU
+fallback.
+
+Names follow the C ABI:
+
+* ``sa_fp4_qkv_bytes`` / ``FP4QKV``   -- the caller-owned quantised-operand blob
+* ``sa_quantize(q, k, v, out=None)``  -- smooth-K + NVFP4 quantisation of Q, K, V
+* ``sa_attn_fwd(q, k, v, o=None, causal=False, mode="bf16"|"nvfp4")``
+* ``sa_last_device_error()``, ``sa_selftest_wait_timeout(ns)``, ``sa_version()``
+"""
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libsa.so")
+
+SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA, SA_ERR_TIMEOUT = range(5)
+SA_MODE_BF16, SA_MODE_NVFP4 = 0, 1
+SA_OUT_FP32 = 16
+
+#: every symbol include/sa.h declares
+EXPORTS = ("sa_fp4_qkv_bytes", "sa_fp4_qkv_from_blob", "sa_quantize", "sa_attn_fwd", "sa_status_string",
+           "sa_last_device_error", "sa_selftest_wait_timeout", "sa_version")
+
+
+class SaFp4Qkv(ctypes.Structure):
+    """Mirror of ``sa_fp4_qkv`` (eight device pointers)."""
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("q_codes", "q_sf", "k_codes", "k_sf", "v_codes", "v_sf", "k_mean", "workspace")]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run `python -m quantized_attention_x16_gb300.build` "
+                          "(the library has no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    i, sz, vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+    lib.sa_fp4_qkv_bytes.argtypes = [i, i, i, i, i, ctypes.POINTER(sz)]
+    lib.sa_fp4_qkv_bytes.restype = sz
+    lib.sa_fp4_qkv_from_blob.argtypes = [vp, i, i, i, i, i, ctypes.POINTER(SaFp4Qkv)]
+    lib.sa_fp4_qkv_from_blob.restype = i
+    lib.sa_quantize.argtypes = [vp, vp, vp, i, i, i, i, i, ctypes.POINTER(SaFp4Qkv), vp]
+    lib.sa_quantize.restype = i
+    lib.sa_attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
+    lib.sa_attn_fwd.restype = i
+    lib.sa_status_string.argtypes = [i]
+    lib.sa_status_string.restype = ctypes.c_char_p
+    lib.sa_last_device_error.argtypes = []
+    lib.sa_last_device_error.restype = i
+    lib.sa_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    lib.sa_selftest_wait_timeout.restype = i
+    lib.sa_version.argtypes = []
+    lib.sa_version.restype = ctypes.c_char_p
+    return lib
+
+
+lib = _load()
+
+
+class SaError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: {lib.sa_status_string(status).decode()} (status {status})")
+
+
+def _check(status, what):
+    if status != SA_OK:
+        raise SaError(status, what)
+
+
+def sa_version():
+    return lib.sa_version().decode()
+
+
+def sa_status_string(status):
+    return lib.sa_status_string(int(status)).decode()
+
+
+def sa_fp4_qkv_bytes(B, H, Hkv, L, d):
+    """(total bytes, [8 offsets]) of the quantised-operand blob."""
+    offs = (ctypes.c_size_t * 8)()
+    n = lib.sa_fp4_qkv_bytes(B, H, Hkv, L, d, offs)
+    return int(n), [int(o) for o in offs]
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _bf16_cuda(t, name):
+    import torch
+    if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 4):
+        raise ValueError(f"{name} must be a contiguous 4-D bfloat16 CUDA tensor (BHLD)")
+
+
+class FP4QKV:
+    """Caller-owned device blob holding the quantised Q, K', V (see sa.h)."""
+
+    def __init__(self, B, H, Hkv, L, d, device="cuda"):
+        import torch
+        self.dims = (B, H, Hkv, L, d)
+        n, self.offsets = sa_fp4_qkv_bytes(B, H, Hkv, L, d)
+        if n == 0:
+            raise SaError(SA_ERR_UNSUPPORTED, "sa_fp4_qkv_bytes")
+        self.blob = torch.empty(n, dtype=torch.uint8, device=device)
+        self.struct = SaFp4Qkv()
+        _check(lib.sa_fp4_qkv_from_blob(_ptr(self.blob), B, H, Hkv, L, d, ctypes.byref(self.struct)),
+               "sa_fp4_qkv_from_blob")
+
+    def views(self):
+        """Torch views of each region, shaped as documented in sa.h."""
+        import torch
+        B, H, Hkv, L, d = self.dims
+        shapes = [
+            ("q_codes", (B, H, L, d // 2), torch.uint8),
+            ("q_sf", (B, H, L // 128, d // 64, 512), torch.uint8),
+            ("k_codes", (B, Hkv, L, d // 2), torch.uint8),
+            ("k_sf", (B, Hkv, L // 128, d // 64, 512), torch.uint8),
+            ("v_codes", (B, Hkv, d, L // 2), torch.uint8),
+            ("v_sf", (B, Hkv, L // 64, 512), torch.uint8),
+            ("k_mean", (B, Hkv, d), torch.float32),
+        ]
+        out = {}
+        for (name, shape, dt), off in zip(shapes, self.offsets):
+            nbytes = 1
+            for s in shape:
+                nbytes *= s
+            nbytes *= 4 if dt == torch.float32 else 1
+            out[name] = self.blob[off:off + nbytes].view(dt).view(shape)
+        return out
+
+
+def sa_quantize(q, k, v, out=None, stream=None):
+    """Smooth-K + NVFP4 quantisation of bf16 BHLD tensors; returns an FP4QKV."""
+    _bf16_cuda(q, "q"), _bf16_cuda(k, "k"), _bf16_cuda(v, "v")
+    B, H, L, d = q.shape
+    Hkv = k.shape[1]
+    if out is None:
+        out = FP4QKV(B, H, Hkv, L, d, device=q.device)
+    _check(lib.sa_quantize(_ptr(q), _ptr(k), _ptr(v), B, H, Hkv, L, d, ctypes.byref(out.struct), _stream(stream)),
+           "sa_quantize")
+    return out
+
+
+def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=None, stream=None):
+    """Fused attention forward.  mode "bf16": q, k, v bf16 BHLD tensors.
+    mode "nvfp4": q is an FP4QKV from sa_quantize, k and v None.
+    out_dtype: torch.bfloat16 (default) or torch.float32 (SA_OUT_FP32).  Returns o."""
+    import torch
+    if mode == "bf16":
+        _bf16_cuda(q, "q"), _bf16_cuda(k, "k"), _bf16_cuda(v, "v")
+        B, H, L, d = q.shape
+        Hkv = k.shape[1]
+        args = (_ptr(q), _ptr(k), _ptr(v))
+        m = SA_MODE_BF16
+        dev = q.device
+    elif mode == "nvfp4":
+        if not isinstance(q, FP4QKV) or k is not None or v is not None:
+            raise ValueError("nvfp4 mode takes an FP4QKV as q and no k, v")
+        B, H, Hkv, L, d = q.dims
+        args = (ctypes.cast(ctypes.pointer(q.struct), ctypes.c_void_p), None, None)
+        m = SA_MODE_NVFP4
+        dev = q.blob.device
+    else:
+        raise ValueError(f"unknown mode {mode!r}")
+    if out_dtype is None:
+        out_dtype = o.dtype if o is not None else torch.bfloat16
+    if out_dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("out_dtype must be torch.bfloat16 or torch.float32")
+    if out_dtype == torch.float32:
+        m |= SA_OUT_FP32
+    if o is None:
+        o = torch.empty((B, H, L, d), dtype=out_dtype, device=dev)
+    if not (o.is_cuda and o.dtype == out_dtype and o.is_contiguous() and tuple(o.shape) == (B, H, L, d)):
+        raise ValueError("o must be a contiguous CUDA tensor of shape (B, H, L, d) and dtype out_dtype")
+    _check(lib.sa_attn_fwd(*args, _ptr(o), B, H, Hkv, L, d, int(bool(causal)), m, _stream(stream)),
+           "sa_attn_fwd")
+    return o
+
+
+def sa_last_device_error():
+    return int(lib.sa_last_device_error())
+
+
+def sa_selftest_wait_timeout(limit_ns, stream=None):
+    _check(lib.sa_selftest_wait_timeout(int(limit_ns), _stream(stream)), "sa_selftest_wait_timeout")

@@ -1,0 +1,385 @@
+// attn_bf16.cu -- exact BF16 fused attention forward on tcgen05 tensor cores.
+//
+// Data flow (page "FlashAttention kernels", sections 0-1): tile by tile with
+// online softmax; the L x L scores never leave the SM.  Work partitioning
+// (same page, FA2): one CTA per (batch, head, 256 query rows).  Hardware
+// mapping: TMA tile loads into 128B-swizzled SMEM, tcgen05 MMAs with FP32
+// accumulators in tensor memory, warp specialisation (load / MMA / softmax
+// roles) as in the Blackwell attention pipelines the page "kernel overview"
+// describes (AVO: MMA, softmax, correction and load warps).
+//
+// CTA layout (384 threads):
+//   warps 0-3  : softmax + correction + epilogue of query tile 0 (rows 0-127)
+//   warps 4-7  : the same for query tile 1 (rows 128-255)
+//   warp 8     : TMA producer (Q once, then K/V tiles into an NS-stage ring)
+//   warp 9     : MMA issuer (one thread)
+//   warps 10-11: idle
+// Tensor memory (512 columns): S (one 128-column region shared by the two
+// query tiles), O0, O1 (d columns each), P0, P1 (64 columns each, bf16
+// pairs).  S = Q K^T is read into registers, P = 2^(x - m) is written back as
+// bf16 into tensor memory and consumed by the P.V MMA as its A operand.
+// Online softmax keeps a stale maximum until the true one exceeds it by more
+// than 2^8 (exact in real arithmetic; the O rescale then runs rarely).
+
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "sm100.cuh"
+
+namespace sa {
+namespace {
+
+constexpr int BM = 128;         // query rows per tile
+constexpr int BN = 128;         // keys per KV tile
+constexpr int kThreads = 384;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+template <int D>
+struct CfgBF16 {
+  static constexpr int NS = (D == 64) ? 4 : 2;            // K/V ring depth
+  static constexpr int kHalfBytes = 128 * 64 * 2;         // one [128 x 64] bf16 box (16 KB)
+  static constexpr int kTileBytes = (D / 64) * kHalfBytes;
+  static constexpr int kOffQ = 0;                         // Q0, Q1
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + NS * kTileBytes;
+  static constexpr int kOffBar = kOffV + NS * kTileBytes;
+  static constexpr int kNumBars = 1 + 4 * NS + 8 + 1;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;   // + alignment slack
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColO0 = 128;
+  static constexpr uint32_t kColP0 = 128 + 2 * D;
+  static constexpr uint32_t kIdescS = idesc_bf16(BM, BN, 0, 0);
+  static constexpr uint32_t kIdescPV = idesc_bf16(BM, D, 0, 1);
+};
+
+struct BarsBF16 {
+  uint64_t* q_full;
+  uint64_t* k_full;
+  uint64_t* k_empty;
+  uint64_t* v_full;
+  uint64_t* v_empty;
+  uint64_t* s_full;   // [2]
+  uint64_t* s_free;   // [2]
+  uint64_t* p_full;   // [2]
+  uint64_t* o_done;   // [2]
+  uint64_t* drain;    // MMA clean-up on abort
+};
+
+template <int D, bool OUT32>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v, void* __restrict__ out_ptr, int H, int Hkv,
+                     int L, int causal, uint64_t wait_ns) {
+  using C = CfgBF16<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar_base = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  BarsBF16 bars;
+  bars.q_full = bar_base;
+  bars.k_full = bar_base + 1;
+  bars.k_empty = bars.k_full + C::NS;
+  bars.v_full = bars.k_empty + C::NS;
+  bars.v_empty = bars.v_full + C::NS;
+  bars.s_full = bars.v_empty + C::NS;
+  bars.s_free = bars.s_full + 2;
+  bars.p_full = bars.s_free + 2;
+  bars.o_done = bars.p_full + 2;
+  bars.drain = bars.o_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_base + C::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int nqt = L / BM;                                       // query tiles per head
+  const int nblk = (nqt + 1) / 2;
+  const int blk = causal ? (nblk - 1 - (int)blockIdx.x) : (int)blockIdx.x;   // longest first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int hk = h / (H / Hkv);
+  const int qt0 = 2 * blk;
+  const bool q1_valid = (qt0 + 1) < nqt;
+  int ntq[2];
+  ntq[0] = causal ? qt0 + 1 : L / BN;
+  ntq[1] = q1_valid ? (causal ? qt0 + 2 : L / BN) : 0;
+  const int nt = ntq[0] > ntq[1] ? ntq[0] : ntq[1];
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNumBars; ++i) mbar_init(bar_base + i, 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(bars.s_free + q, 128);
+      mbar_init(bars.p_full + q, 128);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  const long long q_row0 = ((long long)b * H + h) * L;      // first row of this head in Q/O
+  const long long kv_row0 = ((long long)b * Hkv + hk) * L;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_q);
+      tma_prefetch_desc(&tmap_k);
+      tma_prefetch_desc(&tmap_v);
+      const int nq = q1_valid ? 2 : 1;
+      mbar_arrive_expect_tx(bars.q_full, nq * C::kTileBytes);
+      for (int q = 0; q < nq; ++q)
+        for (int hh = 0; hh < D / 64; ++hh)
+          tma_load_2d(smem + C::kOffQ + q * C::kTileBytes + hh * C::kHalfBytes, &tmap_q, bars.q_full, hh * 64,
+                      (int)(q_row0 + (long long)(qt0 + q) * BM));
+      int issued = 0;
+      for (int j = 0; j < nt; ++j) {
+        const int s = j % C::NS;
+        const uint32_t par = ((j / C::NS) - 1) & 1;
+        const int y = (int)(kv_row0 + (long long)j * BN);
+        if (j >= C::NS && !mbar_wait(bars.k_empty + s, par, abort_flag, wait_ns)) break;
+        mbar_arrive_expect_tx(bars.k_full + s, C::kTileBytes);
+        for (int hh = 0; hh < D / 64; ++hh)
+          tma_load_2d(smem + C::kOffK + s * C::kTileBytes + hh * C::kHalfBytes, &tmap_k, bars.k_full + s, hh * 64,
+                      y);
+        if (j >= C::NS && !mbar_wait(bars.v_empty + s, par, abort_flag, wait_ns)) {
+          issued = 2 * j + 1;
+          break;
+        }
+        mbar_arrive_expect_tx(bars.v_full + s, C::kTileBytes);
+        for (int hh = 0; hh < D / 64; ++hh)
+          tma_load_2d(smem + C::kOffV + s * C::kTileBytes + hh * C::kHalfBytes, &tmap_v, bars.v_full + s, hh * 64,
+                      y);
+        issued = 2 * j + 2;
+      }
+      if (*abort_flag) {
+        // drain: wait (bounded) for every armed load so none lands after exit
+        mbar_wait_drain(bars.q_full, 0, wait_ns);
+        for (int u = (issued > 2 * C::NS ? issued - 2 * C::NS : 0); u < issued; ++u) {
+          const int j = u / 2, s = j % C::NS;
+          mbar_wait_drain((u % 2 == 0) ? bars.k_full + s : bars.v_full + s, (j / C::NS) & 1, wait_ns);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sQ = smem_u32(smem + C::kOffQ);
+      const uint32_t sK = smem_u32(smem + C::kOffK);
+      const uint32_t sV = smem_u32(smem + C::kOffV);
+      int last_q = -1, last_j = 0;
+      bool ok = mbar_wait(bars.q_full, 0, abort_flag, wait_ns);
+      auto issue_s = [&](int q, int j) -> bool {
+        if (last_q >= 0 && !mbar_wait(bars.s_free + last_q, last_j & 1, abort_flag, wait_ns)) return false;
+        tc_fence_after();
+        const int s = j % C::NS;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
+          const uint64_t a = sdesc(sQ + q * C::kTileBytes + off, 16, 1024, kSwizzle128B);
+          const uint64_t bd = sdesc(sK + s * C::kTileBytes + off, 16, 1024, kSwizzle128B);
+          mma_bf16_ss(tbase + C::kColS, a, bd, C::kIdescS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bars.s_full + q);
+        last_q = q;
+        last_j = j;
+        return true;
+      };
+      auto issue_pv = [&](int q, int j) -> bool {
+        if (!mbar_wait(bars.p_full + q, j & 1, abort_flag, wait_ns)) return false;
+        tc_fence_after();
+        const int s = j % C::NS;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t bd = sdesc(sV + s * C::kTileBytes + kk * 16 * 128, C::kHalfBytes, 1024, kSwizzle128B);
+          mma_bf16_ts(tbase + C::kColO0 + q * D, tbase + C::kColP0 + q * 64 + kk * 8, bd, C::kIdescPV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(bars.o_done + q);
+        return true;
+      };
+      if (ok) {
+        ok = mbar_wait(bars.k_full, 0, abort_flag, wait_ns);
+        tc_fence_after();
+        if (ok && ntq[0] > 0) ok = issue_s(0, 0);
+        if (ok && ntq[1] > 0) ok = issue_s(1, 0);
+        if (ok) tc_commit(bars.k_empty);
+      }
+      for (int j = 0; ok && j < nt; ++j) {
+        const int s = j % C::NS;
+        const int s1 = (j + 1) % C::NS;
+        if (j + 1 < nt) {
+          ok = mbar_wait(bars.k_full + s1, ((j + 1) / C::NS) & 1, abort_flag, wait_ns);
+          tc_fence_after();
+          if (ok && j + 1 < ntq[0]) ok = issue_s(0, j + 1);
+        }
+        if (ok) ok = mbar_wait(bars.v_full + s, (j / C::NS) & 1, abort_flag, wait_ns);
+        tc_fence_after();
+        if (ok && j < ntq[0]) ok = issue_pv(0, j);
+        if (ok && j + 1 < nt) {
+          if (j + 1 < ntq[1]) ok = issue_s(1, j + 1);
+          if (ok) tc_commit(bars.k_empty + s1);
+        }
+        if (ok && j < ntq[1]) ok = issue_pv(1, j);
+        if (ok) tc_commit(bars.v_empty + s);
+      }
+      if (!ok) {
+        // drain the tensor pipe before tensor memory is released
+        tc_commit(bars.drain);
+        mbar_wait_drain(bars.drain, 0, wait_ns);
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax
+    const int q = warp / 4;
+    const int r = (warp % 4) * 32 + lane;                      // row within the query tile
+    const uint32_t lane_addr = tbase + (((warp % 4) * 32) << 16);
+    const int qt = qt0 + q;
+    const float c = 1.4426950408889634f * rsqrtf((float)D);
+    float m_use = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntq[q]; ++j) {
+      if (!mbar_wait_warp(bars.s_full + q, j & 1, abort_flag, wait_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) tmem_ld32(lane_addr + C::kColS + 32 * i, sr[i]);
+      tmem_ld_wait(sr[0]);
+      tmem_launder(sr[1]);
+      tmem_launder(sr[2]);
+      tmem_launder(sr[3]);
+      tc_fence_before();
+      mbar_arrive(bars.s_free + q);
+      float sv[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
+      if (causal && j == qt) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i > r) sv[i] = -INFINITY;
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, sv[i]);
+      const float m_t = mx * c;
+      float alpha = 1.f;
+      bool resc = false;
+      if (m_t > m_use + kRescaleThreshold) {
+        alpha = ex2_approx(m_use - m_t);
+        m_use = m_t;
+        resc = (j > 0);
+      }
+      const float negm = -m_use;
+      float sum = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float p0 = ex2_approx(fmaf(sv[2 * i], c, negm));
+        const float p1 = ex2_approx(fmaf(sv[2 * i + 1], c, negm));
+        sum += p0 + p1;
+        pk[i] = pack_bf16x2(p0, p1);
+      }
+      l = l * alpha + sum;
+      if (j > 0) {
+        if (!mbar_wait_warp(bars.o_done + q, (j - 1) & 1, abort_flag, wait_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + C::kColO0 + q * D + 32 * cc, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(lane_addr + C::kColO0 + q * D + 32 * cc, o);
+        }
+      }
+      uint32_t p_lo[32], p_hi[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        p_lo[i] = pk[i];
+        p_hi[i] = pk[32 + i];
+      }
+      tmem_st32(lane_addr + C::kColP0 + q * 64, p_lo);
+      tmem_st32(lane_addr + C::kColP0 + q * 64 + 32, p_hi);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bars.p_full + q);
+    }
+    // ---- epilogue: O / l -> bf16
+    if (ok && ntq[q] > 0 && mbar_wait_warp(bars.o_done + q, (ntq[q] - 1) & 1, abort_flag, wait_ns)) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const long long obase = (q_row0 + (long long)qt * BM + r) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(lane_addr + C::kColO0 + q * D + 32 * cc, o);
+        tmem_ld_wait(o);
+        if constexpr (OUT32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_ptr) + obase + 32 * cc);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                 __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+        } else {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_ptr) + obase + 32 * cc);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D, bool OUT32>
+cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o, const Dims& dm,
+                     int causal, cudaStream_t s) {
+  using C = CfgBF16<D>;
+  static bool attr_done = false;   // the attribute is a property of the function, set once per process
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bf16_kernel<D, OUT32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int nqt = dm.L / BM;
+  dim3 grid((nqt + 1) / 2, dm.H, dm.B);
+  attn_bf16_kernel<D, OUT32><<<grid, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, o, dm.H, dm.Hkv, dm.L, causal,
+                                                                    kWaitLimitNs);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bf16(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o,
+                             const Dims& dm, int causal, bool out_f32, cudaStream_t s) {
+  if (dm.d == 64) return out_f32 ? launch_d<64, true>(tq, tk, tv, o, dm, causal, s)
+                                 : launch_d<64, false>(tq, tk, tv, o, dm, causal, s);
+  return out_f32 ? launch_d<128, true>(tq, tk, tv, o, dm, causal, s)
+                 : launch_d<128, false>(tq, tk, tv, o, dm, causal, s);
+}
+
+cudaError_t attn_bf16_read_error(int* out) { return read_and_clear_device_error(out); }
+
+}  // namespace sa

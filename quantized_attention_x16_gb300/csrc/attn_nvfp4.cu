@@ -1,0 +1,456 @@
+// attn_nvfp4.cu -- SageAttention3-style fused attention forward with NVFP4
+// operands on tcgen05 block-scaled tensor cores.
+//
+// Method (page "GPU kernel porting with AI agents", section "Sage Attention
+// 3"): Q, K' (smooth-K applied) and V are e2m1 in 1x16 groups with e4m3
+// scales (produced by sa_quantize); S = Q^ K^'^T is one block-scaled FP4 MMA
+// per 64 of d; P is quantised in two levels inside the kernel -- per row and
+// 128-key tile it is rescaled so that its maximum is 448 x 6 = 2688, then
+// microscaled to e2m1 in 1x16 groups along the keys with e4m3 scales -- and
+// O += P^ V^ is a second block-scaled FP4 MMA.  Online softmax tile by tile
+// (page "FlashAttention kernels", sections 0-1).
+//
+// Per row and tile j with tile maximum m_j (base-2 logits x = S*log2(e)/sqrt(d)):
+//   P2   = 2^(x - m_j) * 2688                 (first level; max exactly 2688)
+//   P^   = e2m1(P2 / s2) * s2, s2 = e4m3(max16(P2) / 6)   (second level)
+//   A_j  = A_{j-1} * 2^(m_{j-1} - m_j) + P^ V^      (tensor memory, FP32)
+//   lam_j = lam_{j-1} * 2^(m_{j-1} - m_j) + sum(P2)
+// and O = A / lam: the first-level factor s1 = 2^(m_j - m_run)/2688 and the
+// running-max factor cancel between A and lam, so the accumulator is kept in
+// units of the latest tile's maximum.  A tile whose maximum lies more than
+// 2^64 below the running maximum contributes below float32 resolution and is
+// skipped for that row (its P^ row is zero).
+//
+// CTA layout (384 threads): warps 0-3 / 4-7 own query tiles 0 / 1 (one thread
+// per row: softmax, P quantisation, O correction, epilogue); warp 8 issues TMA
+// and bulk copies; warp 9 issues MMAs and scale-factor copies; warps 10-11 idle.
+// Tensor memory: S (128 columns, shared by both query tiles), O0, O1 (d
+// columns each), then scale factors (4 columns per 64-deep K chunk, copied
+// from SMEM with tcgen05.cp, replicated to the four lane quarters).
+
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "sm100.cuh"
+
+namespace sa {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int kThreads = 384;
+constexpr float kLog2PRange = 11.392317422778761f;   // log2(448 * 6)
+constexpr float kSkipBelow = 64.0f;                   // log2 units
+
+template <int D>
+struct CfgF4 {
+  static constexpr int NS = 4;
+  static constexpr int kRowBytes = D / 2;                  // packed codes per Q/K row
+  static constexpr int kQBytes = BM * kRowBytes;           // one Q tile of codes
+  static constexpr int kQSfBytes = (D / 64) * 512;         // its scale blocks
+  static constexpr int kKBytes = BN * kRowBytes;
+  static constexpr int kKSfBytes = (D / 64) * 512;
+  static constexpr int kVBytes = D * (BN / 2);             // V^T tile: d rows x 64 bytes
+  static constexpr int kVSfBytes = 2 * 512;                // two 64-token chunks
+  static constexpr int kPBytes = BM * (BN / 2);            // P^ tile: 128 rows x 64 bytes
+  static constexpr int kPSfBytes = 2 * 512;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * kQBytes;
+  static constexpr int kOffV = kOffK + NS * kKBytes;
+  static constexpr int kOffP = kOffV + NS * kVBytes;
+  static constexpr int kOffQSf = kOffP + 2 * kPBytes;
+  static constexpr int kOffKSf = kOffQSf + 2 * kQSfBytes;
+  static constexpr int kOffVSf = kOffKSf + NS * kKSfBytes;
+  static constexpr int kOffPSf = kOffVSf + NS * kVSfBytes;
+  static constexpr int kOffBar = kOffPSf + 2 * kPSfBytes;
+  static constexpr int kNumBars = 1 + 4 * NS + 8 + 1;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+  // Q/K rows of 64 bytes use the 64B swizzle, rows of 32 bytes the 32B one.
+  static constexpr uint32_t kQKSwz = (D == 128) ? kSwizzle64B : kSwizzle32B;
+  static constexpr uint32_t kQKSbo = 8 * kRowBytes;
+  // tensor-memory columns
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColO0 = 128;
+  static constexpr uint32_t kColSf = 128 + 2 * D;
+  static constexpr uint32_t kColSfQ0 = kColSf + 0;
+  static constexpr uint32_t kColSfQ1 = kColSf + 8;
+  static constexpr uint32_t kColSfK = kColSf + 16;
+  static constexpr uint32_t kColSfV = kColSf + 24;
+  static constexpr uint32_t kColSfP0 = kColSf + 32;
+  static constexpr uint32_t kColSfP1 = kColSf + 40;
+  static constexpr uint32_t kIdescS = idesc_nvf4(BM, BN);
+  static constexpr uint32_t kIdescPV = idesc_nvf4(BM, D);
+  static_assert(kColSf + 48 <= 512, "tensor memory overflow");
+};
+
+struct BarsF4 {
+  uint64_t *q_full, *k_full, *k_empty, *v_full, *v_empty, *s_full, *s_free, *p_full, *o_done, *drain;
+};
+
+// Copies `nblk` consecutive 512-byte scale blocks from SMEM to tensor memory
+// columns [col, col + 4*nblk), replicated across the four lane quarters.
+__device__ __forceinline__ void copy_sf(uint32_t tcol, uint32_t saddr, int nblk) {
+  for (int i = 0; i < nblk; ++i) tmem_cp_32x128b_warpx4(tcol + 4 * i, sdesc(saddr + 512 * i, 0, 128, kSwizzleNone));
+}
+
+template <int D, bool OUT32>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v, const uint8_t* __restrict__ q_sf,
+                      const uint8_t* __restrict__ k_sf, const uint8_t* __restrict__ v_sf,
+                      void* __restrict__ out_ptr, int H, int Hkv, int L, int causal, uint64_t wait_ns) {
+  using C = CfgF4<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar_base = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  BarsF4 bars;
+  bars.q_full = bar_base;
+  bars.k_full = bar_base + 1;
+  bars.k_empty = bars.k_full + C::NS;
+  bars.v_full = bars.k_empty + C::NS;
+  bars.v_empty = bars.v_full + C::NS;
+  bars.s_full = bars.v_empty + C::NS;
+  bars.s_free = bars.s_full + 2;
+  bars.p_full = bars.s_free + 2;
+  bars.o_done = bars.p_full + 2;
+  bars.drain = bars.o_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_base + C::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int nqt = L / BM;
+  const int nblk = (nqt + 1) / 2;
+  const int blk = causal ? (nblk - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int hk = h / (H / Hkv);
+  const int qt0 = 2 * blk;
+  const bool q1_valid = (qt0 + 1) < nqt;
+  int ntq[2];
+  ntq[0] = causal ? qt0 + 1 : L / BN;
+  ntq[1] = q1_valid ? (causal ? qt0 + 2 : L / BN) : 0;
+  const int nt = ntq[0] > ntq[1] ? ntq[0] : ntq[1];
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNumBars; ++i) mbar_init(bar_base + i, 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(bars.s_free + q, 128);
+      mbar_init(bars.p_full + q, 128);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  const long long bhq = (long long)b * H + h;
+  const long long bhk = (long long)b * Hkv + hk;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_q);
+      tma_prefetch_desc(&tmap_k);
+      tma_prefetch_desc(&tmap_v);
+      const int nq = q1_valid ? 2 : 1;
+      mbar_arrive_expect_tx(bars.q_full, nq * (C::kQBytes + C::kQSfBytes));
+      for (int q = 0; q < nq; ++q) {
+        const int qt = qt0 + q;
+        tma_load_2d(smem + C::kOffQ + q * C::kQBytes, &tmap_q, bars.q_full, 0, (int)(bhq * L + (long long)qt * BM));
+        bulk_load(smem + C::kOffQSf + q * C::kQSfBytes, q_sf + (bhq * (L / 128) + qt) * C::kQSfBytes,
+                  C::kQSfBytes, bars.q_full);
+      }
+      int issued = 0;
+      for (int j = 0; j < nt; ++j) {
+        const int s = j % C::NS;
+        const uint32_t par = ((j / C::NS) - 1) & 1;
+        if (j >= C::NS && !mbar_wait(bars.k_empty + s, par, abort_flag, wait_ns)) break;
+        mbar_arrive_expect_tx(bars.k_full + s, C::kKBytes + C::kKSfBytes);
+        tma_load_2d(smem + C::kOffK + s * C::kKBytes, &tmap_k, bars.k_full + s, 0,
+                    (int)(bhk * L + (long long)j * BN));
+        bulk_load(smem + C::kOffKSf + s * C::kKSfBytes, k_sf + (bhk * (L / 128) + j) * C::kKSfBytes, C::kKSfBytes,
+                  bars.k_full + s);
+        if (j >= C::NS && !mbar_wait(bars.v_empty + s, par, abort_flag, wait_ns)) {
+          issued = 2 * j + 1;
+          break;
+        }
+        mbar_arrive_expect_tx(bars.v_full + s, C::kVBytes + C::kVSfBytes);
+        tma_load_2d(smem + C::kOffV + s * C::kVBytes, &tmap_v, bars.v_full + s, j * (BN / 2), (int)(bhk * D));
+        bulk_load(smem + C::kOffVSf + s * C::kVSfBytes, v_sf + (bhk * (L / 64) + 2 * j) * 512, C::kVSfBytes,
+                  bars.v_full + s);
+        issued = 2 * j + 2;
+      }
+      if (*abort_flag) {
+        mbar_wait_drain(bars.q_full, 0, wait_ns);
+        for (int u = (issued > 2 * C::NS ? issued - 2 * C::NS : 0); u < issued; ++u) {
+          const int j = u / 2, s = j % C::NS;
+          mbar_wait_drain((u % 2 == 0) ? bars.k_full + s : bars.v_full + s, (j / C::NS) & 1, wait_ns);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sQ = smem_u32(smem + C::kOffQ);
+      const uint32_t sK = smem_u32(smem + C::kOffK);
+      const uint32_t sV = smem_u32(smem + C::kOffV);
+      const uint32_t sP = smem_u32(smem + C::kOffP);
+      const uint32_t sQSf = smem_u32(smem + C::kOffQSf);
+      const uint32_t sKSf = smem_u32(smem + C::kOffKSf);
+      const uint32_t sVSf = smem_u32(smem + C::kOffVSf);
+      const uint32_t sPSf = smem_u32(smem + C::kOffPSf);
+      int last_q = -1, last_j = 0;
+      auto issue_s = [&](int q, int j) -> bool {
+        if (last_q >= 0 && !mbar_wait(bars.s_free + last_q, last_j & 1, abort_flag, wait_ns)) return false;
+        tc_fence_after();
+        const int s = j % C::NS;
+        const uint32_t sfq = tbase + (q ? C::kColSfQ1 : C::kColSfQ0);
+#pragma unroll
+        for (int kk = 0; kk < D / 64; ++kk) {
+          const uint64_t a = sdesc(sQ + q * C::kQBytes + kk * 32, 16, C::kQKSbo, C::kQKSwz);
+          const uint64_t bd = sdesc(sK + s * C::kKBytes + kk * 32, 16, C::kQKSbo, C::kQKSwz);
+          mma_nvf4(tbase + C::kColS, a, bd, C::kIdescS, sfq + 4 * kk, tbase + C::kColSfK + 4 * kk,
+                   kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bars.s_full + q);
+        last_q = q;
+        last_j = j;
+        return true;
+      };
+      auto issue_pv = [&](int q, int j) -> bool {
+        if (!mbar_wait(bars.p_full + q, j & 1, abort_flag, wait_ns)) return false;
+        tc_fence_after();
+        const int s = j % C::NS;
+        const uint32_t sfp = tbase + (q ? C::kColSfP1 : C::kColSfP0);
+        copy_sf(sfp, sPSf + q * C::kPSfBytes, 2);
+#pragma unroll
+        for (int kk = 0; kk < BN / 64; ++kk) {
+          const uint64_t a = sdesc(sP + q * C::kPBytes + kk * 32, 16, 512, kSwizzle64B);
+          const uint64_t bd = sdesc(sV + s * C::kVBytes + kk * 32, 16, 512, kSwizzle64B);
+          mma_nvf4(tbase + C::kColO0 + q * D, a, bd, C::kIdescPV, sfp + 4 * kk, tbase + C::kColSfV + 4 * kk,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(bars.o_done + q);
+        return true;
+      };
+      bool ok = mbar_wait(bars.q_full, 0, abort_flag, wait_ns);
+      if (ok) {
+        tc_fence_after();
+        copy_sf(tbase + C::kColSfQ0, sQSf, D / 64);
+        if (q1_valid) copy_sf(tbase + C::kColSfQ1, sQSf + C::kQSfBytes, D / 64);
+        ok = mbar_wait(bars.k_full, 0, abort_flag, wait_ns);
+      }
+      if (ok) {
+        tc_fence_after();
+        copy_sf(tbase + C::kColSfK, sKSf, D / 64);
+        if (ntq[0] > 0) ok = issue_s(0, 0);
+        if (ok && ntq[1] > 0) ok = issue_s(1, 0);
+        if (ok) tc_commit(bars.k_empty);
+      }
+      for (int j = 0; ok && j < nt; ++j) {
+        const int s = j % C::NS;
+        const int s1 = (j + 1) % C::NS;
+        if (j + 1 < nt) {
+          ok = mbar_wait(bars.k_full + s1, ((j + 1) / C::NS) & 1, abort_flag, wait_ns);
+          if (ok) {
+            tc_fence_after();
+            copy_sf(tbase + C::kColSfK, sKSf + s1 * C::kKSfBytes, D / 64);
+            if (j + 1 < ntq[0]) ok = issue_s(0, j + 1);
+          }
+        }
+        if (ok) ok = mbar_wait(bars.v_full + s, (j / C::NS) & 1, abort_flag, wait_ns);
+        if (ok) {
+          tc_fence_after();
+          copy_sf(tbase + C::kColSfV, sVSf + s * C::kVSfBytes, 2);
+          if (j < ntq[0]) ok = issue_pv(0, j);
+        }
+        if (ok && j + 1 < nt) {
+          if (j + 1 < ntq[1]) ok = issue_s(1, j + 1);
+          if (ok) tc_commit(bars.k_empty + s1);
+        }
+        if (ok && j < ntq[1]) ok = issue_pv(1, j);
+        if (ok) tc_commit(bars.v_empty + s);
+      }
+      if (!ok) {
+        tc_commit(bars.drain);
+        mbar_wait_drain(bars.drain, 0, wait_ns);
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax + P quantisation
+    const int q = warp / 4;
+    const int r = (warp % 4) * 32 + lane;
+    const uint32_t lane_addr = tbase + (((warp % 4) * 32) << 16);
+    const int qt = qt0 + q;
+    const float c = 1.4426950408889634f * rsqrtf((float)D);
+    uint8_t* prow = smem + C::kOffP + q * C::kPBytes + r * 64;
+    uint8_t* psf = smem + C::kOffPSf + q * C::kPSfBytes + (r % 32) * 16 + (r / 32) * 4;
+    float m_run = -INFINITY, m_ref = 0.f, lam = 0.f;
+    bool have_ref = false, ok = true;
+    for (int j = 0; j < ntq[q]; ++j) {
+      if (!mbar_wait_warp(bars.s_full + q, j & 1, abort_flag, wait_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) tmem_ld32(lane_addr + C::kColS + 32 * i, sr[i]);
+      tmem_ld_wait(sr[0]);
+      tmem_launder(sr[1]);
+      tmem_launder(sr[2]);
+      tmem_launder(sr[3]);
+      tc_fence_before();
+      mbar_arrive(bars.s_free + q);
+      float sv[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
+      if (causal && j == qt) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i > r) sv[i] = -INFINITY;
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, sv[i]);
+      const float m_t = mx * c;
+      const float m_new = fmaxf(m_run, m_t);
+      const bool live = (m_t > -INFINITY) && (m_t >= m_new - kSkipBelow);
+      m_run = m_new;
+      uint32_t codes[16];
+      uint32_t sfw[2] = {0u, 0u};
+      float corr = 1.f;
+      if (live) {
+        const float bias = kLog2PRange - m_t;
+        float rs = 0.f;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          sv[i] = ex2_approx(fmaf(sv[i], c, bias));
+          rs += sv[i];
+        }
+        corr = have_ref ? ex2_approx(m_ref - m_t) : 1.f;
+        lam = have_ref ? fmaf(lam, corr, rs) : rs;
+        m_ref = m_t;
+        have_ref = true;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          float amax = sv[16 * g];
+#pragma unroll
+          for (int i = 1; i < 16; ++i) amax = fmaxf(amax, sv[16 * g + i]);
+          const uint32_t s8 = cvt_e4m3x2(amax * (1.0f / 6.0f), 0.f) & 0xFFu;
+          const float sf = e4m3_to_f32(s8);
+          const float inv = s8 ? rcp_approx(sf) : 0.f;
+          const float* p = sv + 16 * g;
+          codes[2 * g] = cvt_e2m1x8(p[0] * inv, p[1] * inv, p[2] * inv, p[3] * inv, p[4] * inv, p[5] * inv,
+                                    p[6] * inv, p[7] * inv);
+          codes[2 * g + 1] = cvt_e2m1x8(p[8] * inv, p[9] * inv, p[10] * inv, p[11] * inv, p[12] * inv,
+                                        p[13] * inv, p[14] * inv, p[15] * inv);
+          sfw[g / 4] |= s8 << (8 * (g % 4));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) codes[i] = 0u;
+      }
+      if (j > 0) {
+        if (!mbar_wait_warp(bars.o_done + q, (j - 1) & 1, abort_flag, wait_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      // P^ row r: four 16-byte chunks, 64B-swizzled (chunk c at c ^ ((r >> 1) & 3))
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+        *reinterpret_cast<uint4*>(prow + ((ch ^ ((r >> 1) & 3)) * 16)) =
+            make_uint4(codes[4 * ch], codes[4 * ch + 1], codes[4 * ch + 2], codes[4 * ch + 3]);
+      *reinterpret_cast<uint32_t*>(psf) = sfw[0];
+      *reinterpret_cast<uint32_t*>(psf + 512) = sfw[1];
+      if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + C::kColO0 + q * D + 32 * cc, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+          tmem_st32(lane_addr + C::kColO0 + q * D + 32 * cc, o);
+        }
+        tmem_st_wait();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bars.p_full + q);
+    }
+    if (ok && ntq[q] > 0 && mbar_wait_warp(bars.o_done + q, (ntq[q] - 1) & 1, abort_flag, wait_ns)) {
+      tc_fence_after();
+      const float inv_l = 1.f / lam;
+      const long long obase = (bhq * L + (long long)qt * BM + r) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(lane_addr + C::kColO0 + q * D + 32 * cc, o);
+        tmem_ld_wait(o);
+        if constexpr (OUT32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_ptr) + obase + 32 * cc);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                 __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+        } else {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_ptr) + obase + 32 * cc);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D, bool OUT32>
+cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const sa_fp4_qkv& x,
+                     void* o, const Dims& dm, int causal, cudaStream_t s) {
+  using C = CfgF4<D>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(attn_nvfp4_kernel<D, OUT32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  dim3 grid((dm.L / BM + 1) / 2, dm.H, dm.B);
+  attn_nvfp4_kernel<D, OUT32><<<grid, kThreads, C::kSmemBytes, s>>>(
+      tq, tk, tv, static_cast<const uint8_t*>(x.q_sf), static_cast<const uint8_t*>(x.k_sf),
+      static_cast<const uint8_t*>(x.v_sf), o, dm.H, dm.Hkv, dm.L, causal, kWaitLimitNs);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_nvfp4(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const sa_fp4_qkv& qkv, void* o, const Dims& dm, int causal, bool out_f32,
+                              cudaStream_t s) {
+  if (dm.d == 64) return out_f32 ? launch_d<64, true>(tq, tk, tv, qkv, o, dm, causal, s)
+                                 : launch_d<64, false>(tq, tk, tv, qkv, o, dm, causal, s);
+  return out_f32 ? launch_d<128, true>(tq, tk, tv, qkv, o, dm, causal, s)
+                 : launch_d<128, false>(tq, tk, tv, qkv, o, dm, causal, s);
+}
+
+cudaError_t attn_nvfp4_read_error(int* out) { return read_and_clear_device_error(out); }
+
+}  // namespace sa

@@ -1,0 +1,35 @@
+// internal.h -- launchers shared between the translation units of libsa.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sa.h"
+
+namespace sa {
+
+struct Dims {
+  int B, H, Hkv, L, d;
+};
+
+// Barrier-wait limit used by the attention kernels (nanoseconds).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// quant.cu
+cudaError_t launch_quantize(const void* q, const void* k, const void* v, const Dims& dm, const sa_fp4_qkv& out,
+                            cudaStream_t s);
+
+// attn_bf16.cu
+cudaError_t launch_attn_bf16(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o,
+                             const Dims& dm, int causal, bool out_f32, cudaStream_t s);
+// attn_nvfp4.cu
+cudaError_t launch_attn_nvfp4(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const sa_fp4_qkv& qkv, void* o, const Dims& dm, int causal, bool out_f32,
+                              cudaStream_t s);
+
+// Per-unit readers of the device error word (each clears its word).
+cudaError_t attn_bf16_read_error(int* out);
+cudaError_t attn_nvfp4_read_error(int* out);
+
+}  // namespace sa

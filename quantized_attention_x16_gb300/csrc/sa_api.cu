@@ -1,0 +1,202 @@
+// sa_api.cu -- the C ABI declared in include/sa.h: argument validation, TMA
+// descriptor encoding, kernel launches on the caller's stream, status codes.
+// Nothing here allocates device memory.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "sm100.cuh"
+
+namespace sa {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D row-major tensor [outer][inner] of `elem` bytes per element.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+              uint32_t elem, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * elem};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+sa_status check_dims(int B, int H, int Hkv, int L, int d) {
+  if (B <= 0 || H <= 0 || Hkv <= 0 || L <= 0 || d <= 0) return SA_ERR_INVALID_ARG;
+  if (H % Hkv != 0) return SA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return SA_ERR_UNSUPPORTED;
+  if (L % 128 != 0) return SA_ERR_UNSUPPORTED;
+  // TMA coordinates are 32-bit: every row index of Q/K/V (and d * B * Hkv) must fit.
+  if ((long long)B * H * L >= (1ll << 31) || (long long)B * Hkv * d >= (1ll << 31)) return SA_ERR_UNSUPPORTED;
+  if (H > 65535 || B > 65535) return SA_ERR_UNSUPPORTED;
+  return SA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+void blob_sizes(int B, int H, int Hkv, int L, int d, size_t sz[8]) {
+  const size_t nq = (size_t)B * H * L, nk = (size_t)B * Hkv * L;
+  sz[0] = nq * (d / 2);                             // q_codes
+  sz[1] = (size_t)B * H * (L / 128) * (d / 64) * 512;   // q_sf
+  sz[2] = nk * (d / 2);                             // k_codes
+  sz[3] = (size_t)B * Hkv * (L / 128) * (d / 64) * 512;
+  sz[4] = nk * (d / 2);                             // v_codes (transposed)
+  sz[5] = (size_t)B * Hkv * (L / 64) * 512;         // v_sf
+  sz[6] = (size_t)B * Hkv * d * sizeof(float);      // k_mean
+  sz[7] = (size_t)B * Hkv * (L / 128) * d * sizeof(float);   // K-mean partial sums
+}
+
+__global__ void wait_selftest_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);   // expects one arrival that never comes
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, reinterpret_cast<volatile int*>(&abort_flag), limit_ns);
+  __syncthreads();
+}
+
+}  // namespace
+}  // namespace sa
+
+using namespace sa;
+
+extern "C" {
+
+const char* sa_version(void) { return "sa-gb300 0.1 (sm_103a)"; }
+
+const char* sa_status_string(sa_status s) {
+  switch (s) {
+    case SA_OK: return "ok";
+    case SA_ERR_INVALID_ARG: return "invalid argument";
+    case SA_ERR_UNSUPPORTED: return "unsupported size";
+    case SA_ERR_CUDA: return "CUDA error";
+    case SA_ERR_TIMEOUT: return "device barrier wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t sa_fp4_qkv_bytes(int B, int H, int Hkv, int L, int d, size_t offsets_out[8]) {
+  if (check_dims(B, H, Hkv, L, d) != SA_OK) return 0;
+  size_t sz[8];
+  blob_sizes(B, H, Hkv, L, d, sz);
+  size_t off = 0;
+  for (int i = 0; i < 8; ++i) {
+    if (offsets_out) offsets_out[i] = off;
+    off = align256(off + sz[i]);
+  }
+  return off;
+}
+
+sa_status sa_fp4_qkv_from_blob(void* blob, int B, int H, int Hkv, int L, int d, sa_fp4_qkv* out) {
+  if (!out || !blob || (reinterpret_cast<uintptr_t>(blob) & 255u)) return SA_ERR_INVALID_ARG;
+  size_t off[8];
+  if (sa_fp4_qkv_bytes(B, H, Hkv, L, d, off) == 0) return check_dims(B, H, Hkv, L, d);
+  uint8_t* p = static_cast<uint8_t*>(blob);
+  out->q_codes = p + off[0];
+  out->q_sf = p + off[1];
+  out->k_codes = p + off[2];
+  out->k_sf = p + off[3];
+  out->v_codes = p + off[4];
+  out->v_sf = p + off[5];
+  out->k_mean = reinterpret_cast<float*>(p + off[6]);
+  out->workspace = p + off[7];
+  return SA_OK;
+}
+
+static bool fp4_ptrs_ok(const sa_fp4_qkv* x) {
+  return x && aligned16(x->q_codes) && aligned16(x->q_sf) && aligned16(x->k_codes) && aligned16(x->k_sf) &&
+         aligned16(x->v_codes) && aligned16(x->v_sf) && aligned16(x->k_mean) && aligned16(x->workspace);
+}
+
+sa_status sa_quantize(const void* q, const void* k, const void* v, int B, int H, int Hkv, int L, int d,
+                      const sa_fp4_qkv* out, sa_stream_t stream) {
+  const sa_status st = check_dims(B, H, Hkv, L, d);
+  if (st != SA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !fp4_ptrs_ok(out)) return SA_ERR_INVALID_ARG;
+  const Dims dm{B, H, Hkv, L, d};
+  return launch_quantize(q, k, v, dm, *out, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SA_OK
+                                                                                                  : SA_ERR_CUDA;
+}
+
+sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int L, int d,
+                      int causal, int mode_flags, sa_stream_t stream) {
+  const sa_status st = check_dims(B, H, Hkv, L, d);
+  if (st != SA_OK) return st;
+  if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
+  if (mode_flags & ~(0xF | SA_OUT_FP32)) return SA_ERR_INVALID_ARG;
+  const int mode = mode_flags & 0xF;
+  const bool out_f32 = (mode_flags & SA_OUT_FP32) != 0;
+  if (!aligned16(o)) return SA_ERR_INVALID_ARG;
+  const Dims dm{B, H, Hkv, L, d};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  CUtensorMap tq, tk, tv;
+  if (mode == SA_MODE_BF16) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return SA_ERR_INVALID_ARG;
+    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!make_map(&tq, bf, q, d, (uint64_t)B * H * L, 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tk, bf, k, d, (uint64_t)B * Hkv * L, 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tv, bf, v, d, (uint64_t)B * Hkv * L, 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+      return SA_ERR_CUDA;
+    return launch_attn_bf16(tq, tk, tv, o, dm, causal, out_f32, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+  }
+  if (mode == SA_MODE_NVFP4) {
+    if (k != nullptr || v != nullptr || q == nullptr) return SA_ERR_INVALID_ARG;
+    const sa_fp4_qkv* x = static_cast<const sa_fp4_qkv*>(q);
+    if (!aligned16(x->q_codes) || !aligned16(x->q_sf) || !aligned16(x->k_codes) || !aligned16(x->k_sf) ||
+        !aligned16(x->v_codes) || !aligned16(x->v_sf))
+      return SA_ERR_INVALID_ARG;
+    const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const CUtensorMapSwizzle qk_swz = d == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    if (!make_map(&tq, u8, x->q_codes, d / 2, (uint64_t)B * H * L, 1, d / 2, 128, qk_swz) ||
+        !make_map(&tk, u8, x->k_codes, d / 2, (uint64_t)B * Hkv * L, 1, d / 2, 128, qk_swz) ||
+        !make_map(&tv, u8, x->v_codes, L / 2, (uint64_t)B * Hkv * d, 1, 64, d, CU_TENSOR_MAP_SWIZZLE_64B))
+      return SA_ERR_CUDA;
+    return launch_attn_nvfp4(tq, tk, tv, *x, o, dm, causal, out_f32, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+  }
+  return SA_ERR_INVALID_ARG;
+}
+
+sa_status sa_last_device_error(void) {
+  int e1 = 0, e2 = 0, e3 = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SA_ERR_CUDA;
+  if (attn_bf16_read_error(&e1) != cudaSuccess || attn_nvfp4_read_error(&e2) != cudaSuccess ||
+      read_and_clear_device_error(&e3) != cudaSuccess)
+    return SA_ERR_CUDA;
+  const int e = e1 ? e1 : (e2 ? e2 : e3);
+  return e ? static_cast<sa_status>(e) : SA_OK;
+}
+
+sa_status sa_selftest_wait_timeout(uint64_t limit_ns, sa_stream_t stream) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return SA_ERR_INVALID_ARG;
+  wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns);
+  return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+}  // extern "C"

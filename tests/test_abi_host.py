@@ -1,0 +1,103 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/sa.h declares, sizes the operand blob as documented,
+and rejects bad arguments before launching anything."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def sa():
+    lib_path = os.path.join(ROOT, "quantized_attention_x16_gb300", "libsa.so")
+    if not os.path.exists(lib_path):
+        # build.py imports nothing from the package, so load it by path
+        import importlib.util
+        spec = importlib.util.spec_from_file_location(
+            "qa_build", os.path.join(ROOT, "quantized_attention_x16_gb300", "build.py"))
+        mod = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(mod)
+        mod.build()
+    import quantized_attention_x16_gb300 as m
+    return m
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "sa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(sa):
+    declared = header_functions()
+    assert declared, "no declarations found"
+    assert sorted(sa.EXPORTS) == declared
+    lib = ctypes.CDLL(sa.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(sa):
+    assert "sm_103a" in sa.sa_version()
+    assert sa.sa_status_string(0) == "ok"
+    assert "timed out" in sa.sa_status_string(4)
+
+
+def test_blob_layout_sizes(sa):
+    B, H, Hkv, L, d = 2, 8, 4, 384, 128
+    n, off = sa.sa_fp4_qkv_bytes(B, H, Hkv, L, d)
+    sizes = [B * H * L * d // 2, B * H * (L // 128) * (d // 64) * 512, B * Hkv * L * d // 2,
+             B * Hkv * (L // 128) * (d // 64) * 512, B * Hkv * d * L // 2, B * Hkv * (L // 64) * 512,
+             B * Hkv * d * 4, B * Hkv * (L // 128) * d * 4]
+    for i in range(8):
+        assert off[i] % 256 == 0
+        nxt = off[i + 1] if i < 7 else n
+        assert nxt - off[i] >= sizes[i]
+        assert nxt - off[i] < sizes[i] + 256
+    assert sa.sa_fp4_qkv_bytes(1, 2, 2, 100, 64)[0] == 0          # L % 128 != 0
+    assert sa.sa_fp4_qkv_bytes(1, 2, 2, 128, 96)[0] == 0          # unsupported d
+
+
+def test_argument_errors_launch_nothing(sa):
+    lib = sa.lib
+    p = ctypes.c_void_p(1 << 20)          # aligned, never dereferenced
+    bad = ctypes.c_void_p(1 << 20 | 8)    # misaligned
+    z = ctypes.c_void_p(0)
+    # (q, k, v, o, B, H, Hkv, L, d, causal, mode)
+    cases = [
+        ((p, p, p, p, 1, 2, 2, 256, 96, 0, 0), sa.SA_ERR_UNSUPPORTED),
+        ((p, p, p, p, 1, 2, 2, 200, 64, 0, 0), sa.SA_ERR_UNSUPPORTED),
+        ((p, p, p, p, 1, 3, 2, 256, 64, 0, 0), sa.SA_ERR_INVALID_ARG),
+        ((p, p, p, p, 0, 2, 2, 256, 64, 0, 0), sa.SA_ERR_INVALID_ARG),
+        ((p, p, p, z, 1, 2, 2, 256, 64, 0, 0), sa.SA_ERR_INVALID_ARG),
+        ((p, bad, p, p, 1, 2, 2, 256, 64, 0, 0), sa.SA_ERR_INVALID_ARG),
+        ((p, p, p, p, 1, 2, 2, 256, 64, 2, 0), sa.SA_ERR_INVALID_ARG),
+        ((p, p, p, p, 1, 2, 2, 256, 64, 0, 7), sa.SA_ERR_INVALID_ARG),
+        ((z, z, z, p, 1, 2, 2, 256, 64, 0, 1), sa.SA_ERR_INVALID_ARG),      # nvfp4 needs the struct
+        ((p, p, z, p, 1, 2, 2, 256, 64, 0, 1), sa.SA_ERR_INVALID_ARG),      # nvfp4 with k given
+    ]
+    for args, want in cases:
+        assert lib.sa_attn_fwd(*args, None) == want, args
+    s = sa.SaFp4Qkv()
+    assert lib.sa_quantize(p, p, p, 1, 2, 2, 256, 64, ctypes.byref(s), None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_quantize(p, p, p, 1, 2, 2, 256, 80, ctypes.byref(s), None) == sa.SA_ERR_UNSUPPORTED
+    assert lib.sa_selftest_wait_timeout(0, None) == sa.SA_ERR_INVALID_ARG
+    blob = ctypes.c_void_p(1 << 20 | 128)    # not 256-aligned
+    assert lib.sa_fp4_qkv_from_blob(blob, 1, 2, 2, 256, 64, ctypes.byref(s)) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_fp4_qkv_from_blob(p, 1, 2, 2, 256, 64, ctypes.byref(s)) == sa.SA_OK
+    n, off = sa.sa_fp4_qkv_bytes(1, 2, 2, 256, 64)
+    assert s.q_codes == (1 << 20) + off[0] and s.workspace == (1 << 20) + off[7]
+
+
+def test_product_path_has_no_oracle_dependency():
+    pkg = os.path.join(ROOT, "quantized_attention_x16_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle", text, flags=re.M), f
+                assert "oracle/" not in text, f

@@ -1,0 +1,159 @@
+"""GPU parity of sa_attn_fwd against the oracle.
+
+NVFP4 path, against the tile-by-tile SA3 emulation (same Bc = 128, the
+oracle's own quantiser):
+  |O_gpu - O_emul| <= 2e-3 * max|O_emul| + B
+where B is the oracle's decision-ambiguity bound: a P quantisation decision
+whose input lies within TIE_REL (relative) of an e2m1/e4m3 rounding boundary
+may legitimately go either way, because the kernel forms P2 with float32
+scores from the tensor core and ex2.approx while the oracle uses FP64 (several
+results are correct there; B is the most any of them can move O).  TIE_REL =
+1e-4 covers the kernel's P2 error: float32 accumulation of the scores (<= 8
+rounded additions of terms whose magnitudes sum to at most a few hundred,
+times log2(e)/sqrt(d)), the fused multiply-add and bias rounding of the
+exponent (~2e-6 absolute) and ex2.approx (2 ulp), with margin.  This is
+checked on the FP32 output (SA_OUT_FP32); the bf16 output adds its own
+rounding, at most 2^-9 of each element.  The cosine against exact FP64
+attention is reported and must not fall below the emulation's own cosine by
+more than 2e-3 (the scheme, not the kernel, sets that cosine; on these
+synthetic inputs it is about 0.98, below the 0.995 target).
+BF16 path: mean per-head cosine >= 0.99999 against exact FP64 attention and
+max-abs <= 8e-3 * max|O| (bf16 rounding of P and of O, 2^-9 relative each).
+Small cases check every row; the full-size workloads check sampled rows of
+two heads in the launch configuration the bench times.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import attention as A
+
+pytestmark = pytest.mark.gpu
+
+NVFP4_TOL = 2e-3
+TIE_REL = 1e-4
+BF16_COS = 0.99999
+BF16_TOL = 8e-3
+
+
+@pytest.fixture(scope="module")
+def sa():
+    import quantized_attention_x16_gb300 as m
+    return m
+
+
+def run_gpu(sa, x, causal, mode, out_dtype=torch.bfloat16):
+    q, k, v = (x[n].cuda() for n in "qkv")
+    if mode == "bf16":
+        o = sa.sa_attn_fwd(q, k, v, causal=causal, mode="bf16", out_dtype=out_dtype)
+    else:
+        f = sa.sa_quantize(q, k, v)
+        o = sa.sa_attn_fwd(f, causal=causal, mode="nvfp4", out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert sa.sa_last_device_error() == 0
+    return o.float().cpu().numpy()
+
+
+def oracle_heads(x, causal, heads, rows, mode):
+    """Exact (and, for nvfp4, emulated) output of the given (b, h) pairs."""
+    B, H, L, d = x["q"].shape
+    G = H // x["k"].shape[1]
+    ex, em, bd = [], [], []
+    for (b, h) in heads:
+        q = x["q"][b:b + 1, h:h + 1].float().numpy()
+        k = x["k"][b:b + 1, h // G:h // G + 1].float().numpy()
+        v = x["v"][b:b + 1, h // G:h // G + 1].float().numpy()
+        ex.append(A.exact_attention(q, k, v, causal, rows=rows)[0, 0])
+        if mode == "nvfp4":
+            (qd, kd, vd), _ = A.dequantized_operands(q, k, v)
+            e, bound = A.sa3_emulated_attention(qd, kd, vd, causal, rows=rows, tie_rel=TIE_REL,
+                                                return_bound=True)
+            em.append(e[0, 0])
+            bd.append(bound[0, 0])
+    if mode == "nvfp4":
+        return np.stack(ex), np.stack(em), np.stack(bd)
+    return np.stack(ex), None, None
+
+
+def _cos(a, b):
+    return np.array([np.dot(g.ravel(), e.ravel()) / np.linalg.norm(g) / np.linalg.norm(e) for g, e in zip(a, b)])
+
+
+def check(o, x, causal, heads, rows, mode, o32=None):
+    got = np.stack([o[b, h][rows] for (b, h) in heads])
+    ex, em, bound = oracle_heads(x, causal, heads, rows, mode)
+    assert np.all(np.isfinite(got))
+    cos = _cos(got, ex)
+    if mode == "bf16":
+        err = np.abs(got - ex).max() / np.abs(ex).max()
+        print(f"bf16: cos {cos.mean():.7f} (min {cos.min():.7f}) max-abs/max {err:.2e}")
+        assert cos.mean() >= BF16_COS, cos
+        assert err <= BF16_TOL
+        return
+    M = np.abs(em).max()
+    cos_em = _cos(em, ex)
+    tol = NVFP4_TOL * M + bound
+    clean = bound.max(axis=-1) == 0
+    for name, g, extra in (("fp32-out", None if o32 is None else np.stack([o32[b, h][rows] for (b, h) in heads]), 0),
+                           ("bf16-out", got, 2.0 ** -9 * (np.abs(em) + tol))):
+        if g is None:
+            continue
+        err = np.abs(g - em)
+        worst = (err - tol - extra).max() / M
+        print(f"nvfp4 {name}: max|O-O_emul|/max {err.max() / M:.2e}; beyond bound {worst:.2e}; "
+              f"rows with ambiguous P decisions {np.mean(~clean):.3f}; max err on unambiguous rows "
+              f"{(err[clean].max() / M) if clean.any() else 0:.2e}; cos vs exact gpu {_cos(g, ex).mean():.5f} "
+              f"emulation {cos_em.mean():.5f}")
+        assert np.all(err <= tol + extra), worst
+        assert _cos(g, ex).mean() >= cos_em.mean() - 2e-3
+
+
+SMALL = [
+    dict(W.spec("tiny")),
+    dict(W.spec("tiny"), causal=True, seed=1),
+    dict(W.spec("llm_prefill"), B=1, H=2, Hkv=2, L=512, seed=11),
+    dict(W.spec("causal_gqa"), B=1, H=4, Hkv=2, L=384, seed=12),           # odd tile count, GQA, causal
+    dict(W.spec("dit_video"), B=2, H=2, Hkv=1, L=640, d=64, seed=13),      # MQA, d=64, 5 tiles
+    dict(W.spec("sweep_causal_d64_L1024"), H=2, Hkv=2, L=128, seed=14),     # a single tile
+]
+
+
+def _id(w):
+    return f"{w['name']}-B{w['B']}H{w['H']}K{w['Hkv']}L{w['L']}d{w['d']}{'c' if w['causal'] else ''}"
+
+
+@pytest.mark.parametrize("mode", ["bf16", "nvfp4"])
+@pytest.mark.parametrize("w", SMALL, ids=_id)
+def test_attention_small_all_rows(sa, w, mode):
+    x = W.make_inputs(w)
+    o = run_gpu(sa, x, w["causal"], mode)
+    o32 = run_gpu(sa, x, w["causal"], mode, torch.float32) if mode == "nvfp4" else None
+    heads = [(b, h) for b in range(w["B"]) for h in range(w["H"])]
+    check(o, x, w["causal"], heads, np.arange(w["L"]), mode, o32)
+
+
+FULL = ["llm_prefill", "causal_gqa", "dit_video", "sweep_causal_d64_L32768", "sweep_full_d128_L32768"]
+
+
+@pytest.mark.parametrize("mode", ["bf16", "nvfp4"])
+@pytest.mark.parametrize("name", FULL)
+def test_attention_full_size_sampled_rows(sa, name, mode):
+    w = W.spec(name)
+    x = W.make_inputs(w)
+    o = run_gpu(sa, x, w["causal"], mode)
+    o32 = run_gpu(sa, x, w["causal"], mode, torch.float32) if mode == "nvfp4" else None
+    rows = np.array(W.sample_rows(w["L"], 192, seed=w["seed"]))
+    heads = [(0, 0), (w["B"] - 1, w["H"] - 1)]
+    check(o, x, w["causal"], heads, rows, mode, o32)
+
+
+def test_wait_timeout_is_reported_and_context_survives(sa):
+    sa.sa_selftest_wait_timeout(2_000_000)      # 2 ms wait on a barrier nothing completes
+    assert sa.sa_last_device_error() == sa.SA_ERR_TIMEOUT
+    assert sa.sa_last_device_error() == sa.SA_OK      # read-and-clear
+    w = W.spec("tiny")
+    x = W.make_inputs(w)
+    o = run_gpu(sa, x, False, "bf16")             # the context still works
+    check(o, x, False, [(0, 0)], np.arange(64), "bf16")

@@ -225,3 +225,74 @@ def test_quantised_pipeline_is_close_to_exact_on_iid_inputs():
     x = A.exact_attention(q, k, v, False)
     cos = A.cosine_per_head(e, x)
     assert np.all(cos > 0.95)
+
+
+# ---------------------------------------------------------------- decision ambiguity bound
+
+def test_ambiguity_bound_zero_without_window():
+    rng = np.random.default_rng(40)
+    q, k, v = (rng.standard_normal((1, 1, 128, 32)) for _ in range(3))
+    o, b = A.sa3_emulated_attention(q, k, v, False, bc=64, return_bound=True, tie_rel=0.0)
+    assert np.all(b == 0)
+    assert np.array_equal(o, A.sa3_emulated_attention(q, k, v, False, bc=64))
+
+
+def test_ambiguity_bound_hand_worked_tie():
+    # golden "one_tile" case: P2/448 = 6 3 1.5 0.75 0.375 ...; only 0.75 sits on an
+    # e2m1 midpoint (gap 0.5), so the bound is 0.5*448/2688 * |V_3| / l0 = |V_3| / (12 l0)
+    d = 16
+    q = np.zeros((1, d)); q[0, 0] = 1.0
+    kk = np.zeros((16, d)); kk[:, 0] = -np.arange(16)
+    v = np.random.default_rng(3).standard_normal((16, d))
+    o, b = A.sa3_tile_rows(q, kk, v, np.array([15]), False, bc=16, scale=1.0 / A.LOG2E,
+                           tie_rel=1e-5, return_bound=True)
+    l0 = 2.0 - 2.0 ** -15
+    assert np.allclose(b[0], np.abs(v[3]) / (12 * l0), rtol=1e-12, atol=0)
+
+
+def _kernel_like(qd, kd, vd, bc, jitter, rng):
+    """An independent implementation of the scheme with float32 arithmetic in
+    the order a kernel takes it (float32 scores, P2 = 2^(x - m_t + log2 2688)
+    from a fused multiply-add, scale by a multiply with 1/6, codes by a
+    multiply with the reciprocal scale, accumulator in units of the latest tile
+    maximum) plus a relative jitter on P2."""
+    from oracle import formats
+    n, d = qd.shape
+    c = np.float32(A.LOG2E) * np.float32(1 / np.sqrt(np.float32(d)))
+    S = (qd @ kd.T).astype(np.float32)
+    m_ref = np.zeros(n, np.float32)
+    lam = np.zeros(n)
+    acc = np.zeros((n, d))
+    for j0 in range(0, kd.shape[0], bc):
+        s = S[:, j0:j0 + bc]
+        mt = (s.max(1) * c).astype(np.float32)
+        bias = (np.float32(np.log2(2688.0)) - mt).astype(np.float32)
+        x = (s.astype(np.float64) * c + bias[:, None]).astype(np.float32)
+        p2 = np.exp2(x.astype(np.float64)) * (1 + rng.uniform(-jitter, jitter, x.shape))
+        p2 = p2.astype(np.float32)
+        g = p2.reshape(n, -1, 16)
+        sf = formats.e4m3_decode(formats.e4m3_encode((g.max(-1) * np.float32(1 / 6)).astype(np.float32)))
+        inv = np.where(sf > 0, 1 / np.where(sf > 0, sf, 1), 0).astype(np.float32)
+        ph = (formats.e2m1_decode(formats.e2m1_encode((g * inv[..., None]).astype(np.float32))) * sf[..., None])
+        corr = np.exp2(m_ref.astype(np.float64) - mt) if j0 else np.ones(n)
+        lam = lam * corr + p2.astype(np.float64).sum(1)
+        acc = acc * corr[:, None] + ph.reshape(n, -1) @ vd[j0:j0 + bc]
+        m_ref = mt
+    return acc / lam[:, None]
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_ambiguity_bound_covers_a_perturbed_implementation(seed):
+    # the bound must contain every result an implementation with slightly
+    # different rounding (relative error << tie_rel on P2) can produce
+    rng = np.random.default_rng(seed)
+    L, d = 512, 64
+    q = rng.standard_normal((1, 1, L, d)).astype(np.float32)
+    k = (rng.standard_normal((1, 1, L, d)) * 1.5).astype(np.float32)
+    v = rng.standard_normal((1, 1, L, d)).astype(np.float32)
+    (qd, kd, vd), _ = A.dequantized_operands(q, k, v)
+    em, bound = A.sa3_emulated_attention(qd, kd, vd, False, tie_rel=2e-5, return_bound=True)
+    sim = _kernel_like(qd[0, 0], kd[0, 0], vd[0, 0], 128, 2e-6, rng)
+    err = np.abs(sim - em[0, 0])
+    M = np.abs(em).max()
+    assert np.all(err <= bound[0, 0] + 1e-5 * M)
