@@ -115,6 +115,39 @@ sa_status sa_quantize(const void* q, const void* k, const void* v,
                       const sa_fp4_qkv* out, sa_stream_t stream);
 
 /*
+ * sa_quantize_static_scratch -- sa_quantize for callers that cannot allocate
+ * device memory.  (The pages describe no such call; it is part of this
+ * library's interface only.)
+ *
+ * sa_quantize needs a scratch buffer for the K-mean partial sums, which the
+ * caller normally provides inside the sa_fp4_qkv blob.  Some callers have no
+ * way to obtain one: host code embedded in a runtime that plans all device
+ * memory ahead of time and forbids cudaMalloc once it is running, plugin or
+ * custom-operator interfaces that hand over only the input and output
+ * buffers, and code that must not risk the implicit device synchronisation an
+ * allocation can cause.  This entry point does the same work, bit for bit,
+ * with the partial sums kept in a fixed array compiled into the library
+ * (SA_STATIC_SCRATCH_FLOATS floats = 4 MiB, held by every GPU that loads the
+ * library until the process exits).  It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *  - Arguments as for sa_quantize; out->workspace is ignored and may be NULL.
+ *  - Sizes with B * Hkv * (L/128) * d > SA_STATIC_SCRATCH_FLOATS return
+ *    SA_ERR_UNSUPPORTED before anything is launched.
+ *  - The first call on each device, made with that device current, looks up
+ *    the array's device address (cudaGetSymbolAddress); make that first call
+ *    before any stream capture.
+ *  - Every call on a device uses the same array.  Each call writes every
+ *    partial sum it reads before reading it, so leftovers from an earlier
+ *    call never reach the outputs and nothing needs clearing; but calls whose
+ *    kernels overlap on the GPU (other streams, other host threads) race on
+ *    the array and must be serialised by the caller.
+ */
+#define SA_STATIC_SCRATCH_FLOATS 1048576
+sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v,
+                                     int B, int H, int Hkv, int L, int d,
+                                     const sa_fp4_qkv* out, sa_stream_t stream);
+
+/*
  * sa_attn_fwd -- fused attention forward, O = softmax(Q K^T / sqrt(d)) V,
  * tile by tile with online softmax ("FlashAttention kernels" sections 0-1).
  *  mode SA_MODE_BF16:  q, k, v are bf16 BHLD device tensors; tcgen05 BF16

@@ -4,13 +4,14 @@ Argument marshalling only: every step of the computation runs in the CUDA
 kernels behind the C ABI declared in ``include/sa.h``.  PyTorch provides
 device memory and streams.  Importing this package loads ``libsa.so`` from
 this directory and raises ``ImportError`` if it has not been built (build it
-with ``python -m quantized_attention_x16_gb300.build``); there is no CPU
+with ``python quantized_attention_x16_gb300/build.py``); there is no CPU
 fallback.
 
 Names follow the C ABI:
 
 * ``sa_fp4_qkv_bytes`` / ``FP4QKV``   -- the caller-owned quantised-operand blob
 * ``sa_quantize(q, k, v, out=None)``  -- smooth-K + NVFP4 quantisation of Q, K, V
+* ``sa_quantize_static_scratch(...)`` -- the same without caller-provided scratch
 * ``sa_attn_fwd(q, k, v, o=None, causal=False, mode="bf16"|"nvfp4")``
 * ``sa_last_device_error()``, ``sa_selftest_wait_timeout(ns)``, ``sa_version()``
 """
@@ -26,8 +27,9 @@ SA_MODE_BF16, SA_MODE_NVFP4 = 0, 1
 SA_OUT_FP32 = 16
 
 #: every symbol include/sa.h declares
-EXPORTS = ("sa_fp4_qkv_bytes", "sa_fp4_qkv_from_blob", "sa_quantize", "sa_attn_fwd", "sa_status_string",
-           "sa_last_device_error", "sa_selftest_wait_timeout", "sa_version")
+EXPORTS = ("sa_fp4_qkv_bytes", "sa_fp4_qkv_from_blob", "sa_quantize", "sa_quantize_static_scratch", "sa_attn_fwd",
+           "sa_status_string", "sa_last_device_error", "sa_selftest_wait_timeout", "sa_version")
+SA_STATIC_SCRATCH_FLOATS = 1 << 20
 
 
 class SaFp4Qkv(ctypes.Structure):
@@ -38,7 +40,7 @@ class SaFp4Qkv(ctypes.Structure):
 
 def _load():
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"{LIB_PATH} is not built; run `python -m quantized_attention_x16_gb300.build` "
+        raise ImportError(f"{LIB_PATH} is not built; run `python quantized_attention_x16_gb300/build.py` "
                           "(the library has no CPU fallback)")
     lib = ctypes.CDLL(LIB_PATH)
     i, sz, vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
@@ -48,6 +50,8 @@ def _load():
     lib.sa_fp4_qkv_from_blob.restype = i
     lib.sa_quantize.argtypes = [vp, vp, vp, i, i, i, i, i, ctypes.POINTER(SaFp4Qkv), vp]
     lib.sa_quantize.restype = i
+    lib.sa_quantize_static_scratch.argtypes = [vp, vp, vp, i, i, i, i, i, ctypes.POINTER(SaFp4Qkv), vp]
+    lib.sa_quantize_static_scratch.restype = i
     lib.sa_attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.sa_attn_fwd.restype = i
     lib.sa_status_string.argtypes = [i]
@@ -152,6 +156,20 @@ def sa_quantize(q, k, v, out=None, stream=None):
         out = FP4QKV(B, H, Hkv, L, d, device=q.device)
     _check(lib.sa_quantize(_ptr(q), _ptr(k), _ptr(v), B, H, Hkv, L, d, ctypes.byref(out.struct), _stream(stream)),
            "sa_quantize")
+    return out
+
+
+def sa_quantize_static_scratch(q, k, v, out=None, stream=None):
+    """sa_quantize without caller-provided scratch (see sa.h): the K-mean partial
+    sums live in the library's fixed per-device array.  Returns an FP4QKV."""
+    _bf16_cuda(q, "q"), _bf16_cuda(k, "k"), _bf16_cuda(v, "v")
+    B, H, L, d = q.shape
+    Hkv = k.shape[1]
+    if out is None:
+        out = FP4QKV(B, H, Hkv, L, d, device=q.device)
+    _check(lib.sa_quantize_static_scratch(_ptr(q), _ptr(k), _ptr(v), B, H, Hkv, L, d, ctypes.byref(out.struct),
+                                          _stream(stream)),
+           "sa_quantize_static_scratch")
     return out
 
 

@@ -2,7 +2,8 @@
 
 Each CUDA translation unit is compiled in parallel, then linked into one
 shared object next to this file.  Used by ``__graft_entry__.build()`` and
-runnable as ``python -m quantized_attention_x16_gb300.build``.
+runnable as ``python quantized_attention_x16_gb300/build.py``; it imports
+nothing from the package (importing the package needs the built library).
 """
 
 import os

@@ -13,6 +13,8 @@
 
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "sm100.cuh"
 
@@ -174,6 +176,68 @@ cudaError_t launch_quantize(const void* q, const void* k, const void* v, const D
   const int nbh = dm.B * dm.Hkv;
   const int cpb = 128 / (dm.d / 8);
   float* part = static_cast<float*>(out.workspace);
+  kmean_partial_kernel<<<dim3((nchunk + cpb - 1) / cpb, nbh), 128, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(k), part, dm.L, dm.d, nchunk);
+  kmean_final_kernel<<<(nbh * dm.d + 127) / 128, 128, 0, s>>>(part, out.k_mean, nbh, nchunk, dm.d, dm.L);
+  const long long nq = (long long)dm.B * dm.H * dm.L * (dm.d / 64);
+  const long long nk = (long long)nbh * dm.L * (dm.d / 64);
+  const long long blocks = (nq + nk + 255) / 256;
+  quant_qk_kernel<<<(unsigned)(blocks < 65535 * 16 ? blocks : 65535 * 16), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), out.k_mean,
+      static_cast<uint8_t*>(out.q_codes), static_cast<uint8_t*>(out.q_sf), static_cast<uint8_t*>(out.k_codes),
+      static_cast<uint8_t*>(out.k_sf), dm.L, dm.d, nq, nk);
+  quant_v_kernel<<<dim3(dm.L / 64, nbh), dm.d, 0, s>>>(static_cast<const __nv_bfloat16*>(v),
+                                                       static_cast<uint8_t*>(out.v_codes),
+                                                       static_cast<uint8_t*>(out.v_sf), dm.L, dm.d);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant (sa_quantize_static_scratch).  The K-mean partial
+// sums go to a fixed array compiled into this library instead of the
+// caller's workspace.  Each device that loads the library holds the array
+// (kStaticScratchFloats floats, 4 MiB) until the process exits.  Its device
+// address is looked up once per device, on the first call made with that
+// device current; host code never passes the array's own name to a kernel.
+namespace {
+
+static __device__ __align__(256) float g_quant_scratch[kStaticScratchFloats];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+float* g_scratch_addr[kMaxDevices] = {};
+
+cudaError_t static_scratch_address(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_quant_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = static_cast<float*>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_static_scratch(const void* q, const void* k, const void* v, const Dims& dm,
+                                           const sa_fp4_qkv& out, cudaStream_t s) {
+  const size_t need = (size_t)dm.B * dm.Hkv * (dm.L / kMeanChunk) * dm.d;
+  if (need > kStaticScratchFloats) return cudaErrorInvalidValue;
+  float* part = nullptr;
+  cudaError_t e = static_scratch_address(&part);
+  if (e != cudaSuccess) return e;
+  // Every partial sum read below is written first by kmean_partial_kernel in
+  // the same call, so earlier contents of the array never reach the outputs
+  // and nothing needs clearing.
+  const int nchunk = dm.L / kMeanChunk;
+  const int nbh = dm.B * dm.Hkv;
+  const int cpb = 128 / (dm.d / 8);
   kmean_partial_kernel<<<dim3((nchunk + cpb - 1) / cpb, nbh), 128, 0, s>>>(
       static_cast<const __nv_bfloat16*>(k), part, dm.L, dm.d, nchunk);
   kmean_final_kernel<<<(nbh * dm.d + 127) / 128, 128, 0, s>>>(part, out.k_mean, nbh, nchunk, dm.d, dm.L);

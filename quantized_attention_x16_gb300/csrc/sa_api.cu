@@ -145,6 +145,21 @@ sa_status sa_quantize(const void* q, const void* k, const void* v, int B, int H,
                                                                                                   : SA_ERR_CUDA;
 }
 
+sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v, int B, int H, int Hkv, int L,
+                                     int d, const sa_fp4_qkv* out, sa_stream_t stream) {
+  const sa_status st = check_dims(B, H, Hkv, L, d);
+  if (st != SA_OK) return st;
+  if ((size_t)B * Hkv * (L / 128) * d > (size_t)SA_STATIC_SCRATCH_FLOATS) return SA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !out || !aligned16(out->q_codes) ||
+      !aligned16(out->q_sf) || !aligned16(out->k_codes) || !aligned16(out->k_sf) || !aligned16(out->v_codes) ||
+      !aligned16(out->v_sf) || !aligned16(out->k_mean))
+    return SA_ERR_INVALID_ARG;
+  const Dims dm{B, H, Hkv, L, d};
+  return launch_quantize_static_scratch(q, k, v, dm, *out, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SA_OK
+             : SA_ERR_CUDA;
+}
+
 sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int L, int d,
                       int causal, int mode_flags, sa_stream_t stream) {
   const sa_status st = check_dims(B, H, Hkv, L, d);
