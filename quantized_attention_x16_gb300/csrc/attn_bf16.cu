@@ -8,12 +8,14 @@
 // roles) as in the Blackwell attention pipelines the page "kernel overview"
 // describes (AVO: MMA, softmax, correction and load warps).
 //
-// CTA layout (384 threads):
-//   warps 0-3  : softmax + correction + epilogue of query tile 0 (rows 0-127)
-//   warps 4-7  : the same for query tile 1 (rows 128-255)
-//   warp 8     : TMA producer (Q once, then K/V tiles into an NS-stage ring)
-//   warp 9     : MMA issuer (one thread)
-//   warps 10-11: idle
+// CTA layout (640 threads):
+//   warps 0-15 : softmax + correction + epilogue; warp w serves query tile
+//                w/8, key half (w/4)%2 (64 of the 128 score columns) and rows
+//                32*(w%4)..+31 -- two threads per row exchange half-row maxima
+//                through SMEM and each handles its half of P and of O
+//   warp 16    : TMA producer (Q once, then K/V tiles into an NS-stage ring)
+//   warp 17    : MMA issuer (one thread)
+//   warps 18-19: idle
 // Tensor memory (512 columns): S (one 128-column region shared by the two
 // query tiles), O0, O1 (d columns each), P0, P1 (64 columns each, bf16
 // pairs).  S = Q K^T is read into registers, P = 2^(x - m) is written back as
@@ -31,7 +33,11 @@ namespace {
 
 constexpr int BM = 128;         // query rows per tile
 constexpr int BN = 128;         // keys per KV tile
-constexpr int kThreads = 384;
+constexpr int kThreads = 640;
+constexpr int kSoftmaxRegs = 104;   // 16 softmax warps
+constexpr int kOtherRegs = 64;      // producer / MMA warpgroup
+constexpr int kLaunchRegs = 96;     // 65536 / 640 rounded down to a multiple of 8
+static_assert(16 * 32 * kSoftmaxRegs + 4 * 32 * kOtherRegs <= kThreads * kLaunchRegs, "register split");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 template <int D>
@@ -42,7 +48,8 @@ struct CfgBF16 {
   static constexpr int kOffQ = 0;                         // Q0, Q1
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + NS * kTileBytes;
-  static constexpr int kOffBar = kOffV + NS * kTileBytes;
+  static constexpr int kOffX = kOffV + NS * kTileBytes;     // [2 slots][2 q][2 halves][128 rows] float
+  static constexpr int kOffBar = kOffX + 2 * 2 * 2 * 128 * 4;
   static constexpr int kNumBars = 1 + 4 * NS + 8 + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;   // + alignment slack
   static constexpr uint32_t kColS = 0;
@@ -104,13 +111,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i) mbar_init(bar_base + i, 1);
     for (int q = 0; q < 2; ++q) {
-      mbar_init(bars.s_free + q, 128);
-      mbar_init(bars.p_full + q, 128);
+      mbar_init(bars.s_free + q, 256);
+      mbar_init(bars.p_full + q, 256);
     }
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 8) {
+  if (warp == 16) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -122,7 +129,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long q_row0 = ((long long)b * H + h) * L;      // first row of this head in Q/O
   const long long kv_row0 = ((long long)b * Hkv + hk) * L;
 
-  if (warp == 8) {
+  if (warp >= 16) {
+    // Register split: the launch gives every thread kLaunchRegs; this
+    // warpgroup (producer, MMA issuer, two idle warps) keeps kOtherRegs and the
+    // four softmax warpgroups take kSoftmaxRegs (sum checked above).
+    reg_dealloc<kOtherRegs>();
+    if (warp == 16) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmap_q);
@@ -163,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == 17) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t sQ = smem_u32(smem + C::kOffQ);
@@ -231,99 +243,116 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(bars.drain, 0, wait_ns);
       }
     }
-  } else if (warp < 8) {
+    }
+  } else {
+    reg_alloc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax
-    const int q = warp / 4;
+    const int q = warp / 8;                                    // query tile
+    const int hf = (warp / 4) & 1;                             // key half: columns 64*hf .. +63
     const int r = (warp % 4) * 32 + lane;                      // row within the query tile
     const uint32_t lane_addr = tbase + (((warp % 4) * 32) << 16);
     const int qt = qt0 + q;
+    const int bar_id = 1 + q * 4 + (warp % 4);                 // the two warps sharing these rows
     const float c = 1.4426950408889634f * rsqrtf((float)D);
+    float* xch = reinterpret_cast<float*>(smem + C::kOffX);    // [slot][q][half][row]
+    const uint32_t ocol = C::kColO0 + q * D + hf * (D / 2);    // this thread's half of O
     float m_use = -INFINITY, l = 0.f;
     bool ok = true;
+    // Both warps of a row pair execute every named barrier the same number of
+    // times (once per tile, once at the end), also after a bounded wait gave up.
     for (int j = 0; j < ntq[q]; ++j) {
-      if (!mbar_wait_warp(bars.s_full + q, j & 1, abort_flag, wait_ns)) {
-        ok = false;
-        break;
+      if (ok) ok = mbar_wait_warp(bars.s_full + q, j & 1, abort_flag, wait_ns);
+      uint32_t sr[2][32];
+      if (ok) {
+        tc_fence_after();
+        tmem_ld32(lane_addr + C::kColS + 64 * hf, sr[0]);
+        tmem_ld32(lane_addr + C::kColS + 64 * hf + 32, sr[1]);
+        tmem_ld_wait(sr[0]);
+        tmem_launder(sr[1]);
+        tc_fence_before();
+        mbar_arrive(bars.s_free + q);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) sr[i / 32][i % 32] = 0u;
       }
-      tc_fence_after();
-      uint32_t sr[4][32];
+      float sv[64];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) tmem_ld32(lane_addr + C::kColS + 32 * i, sr[i]);
-      tmem_ld_wait(sr[0]);
-      tmem_launder(sr[1]);
-      tmem_launder(sr[2]);
-      tmem_launder(sr[3]);
-      tc_fence_before();
-      mbar_arrive(bars.s_free + q);
-      float sv[128];
-#pragma unroll
-      for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
+      for (int i = 0; i < 64; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
       if (causal && j == qt) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i > r) sv[i] = -INFINITY;
+        for (int i = 0; i < 64; ++i)
+          if (64 * hf + i > r) sv[i] = -INFINITY;
       }
-      float mx = sv[0];
-#pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, sv[i]);
+      float* slot = xch + (j & 1) * 512 + q * 256;
+      slot[hf * 128 + r] = max3(max3(max16(sv), max16(sv + 16), max16(sv + 32)), max16(sv + 48), -INFINITY);
+      named_barrier_sync(bar_id, 64);
+      const float mx = fmaxf(slot[r], slot[128 + r]);
+      if (!ok) continue;
       const float m_t = mx * c;
       float alpha = 1.f;
       bool resc = false;
-      if (m_t > m_use + kRescaleThreshold) {
+      if (m_t > m_use + kRescaleThreshold) {      // both halves decide alike (shared m_t)
         alpha = ex2_approx(m_use - m_t);
         m_use = m_t;
         resc = (j > 0);
       }
       const float negm = -m_use;
-      float sum = 0.f;
-      uint32_t pk[64];
+      float sp[8];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float p0 = ex2_approx(fmaf(sv[2 * i], c, negm));
-        const float p1 = ex2_approx(fmaf(sv[2 * i + 1], c, negm));
-        sum += p0 + p1;
-        pk[i] = pack_bf16x2(p0, p1);
-      }
-      l = l * alpha + sum;
-      if (j > 0) {
-        if (!mbar_wait_warp(bars.o_done + q, (j - 1) & 1, abort_flag, wait_ns)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
-      if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(lane_addr + C::kColO0 + q * D + 32 * cc, o);
-          tmem_ld_wait(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(lane_addr + C::kColO0 + q * D + 32 * cc, o);
-        }
-      }
-      uint32_t p_lo[32], p_hi[32];
+      for (int i = 0; i < 8; ++i) sp[i] = 0.f;
+      uint32_t pk[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        p_lo[i] = pk[i];
-        p_hi[i] = pk[32 + i];
+        float p0, p1;
+        fma2(p0, p1, sv[2 * i], sv[2 * i + 1], c, c, negm, negm);
+        p0 = ex2_approx(p0);
+        p1 = ex2_approx(p1);
+        const int a = i % 4;
+        add2(sp[2 * a], sp[2 * a + 1], sp[2 * a], sp[2 * a + 1], p0, p1);
+        pk[i] = pack_bf16x2(p0, p1);
       }
-      tmem_st32(lane_addr + C::kColP0 + q * 64, p_lo);
-      tmem_st32(lane_addr + C::kColP0 + q * 64 + 32, p_hi);
+      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+      l = l * alpha + sum;                                     // this half's share of the row sum
+      if (j > 0) {
+        ok = mbar_wait_warp(bars.o_done + q, (j - 1) & 1, abort_flag, wait_ns);
+        if (!ok) continue;
+        tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, resc)) {     // rare: one 32-column chunk at a time
+#pragma unroll 1
+        for (int cc = 0; cc < D / 64; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + ocol + 32 * cc, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float a = __uint_as_float(o[i]), b = __uint_as_float(o[i + 1]);
+            mul2(a, b, a, b, alpha, alpha);
+            o[i] = __float_as_uint(a);
+            o[i + 1] = __float_as_uint(b);
+          }
+          tmem_st32(lane_addr + ocol + 32 * cc, o);
+        }
+      }
+      tmem_st32(lane_addr + C::kColP0 + q * 64 + 32 * hf, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bars.p_full + q);
     }
-    // ---- epilogue: O / l -> bf16
-    if (ok && ntq[q] > 0 && mbar_wait_warp(bars.o_done + q, (ntq[q] - 1) & 1, abort_flag, wait_ns)) {
+    // ---- epilogue: combine the halves' row sums, then O / l for this half
+    const bool ok_all = __all_sync(0xffffffffu, ok);
+    float* slot = xch + (ntq[q] & 1) * 512 + q * 256;
+    slot[hf * 128 + r] = l;
+    named_barrier_sync(bar_id, 64);
+    const float l_row = slot[r] + slot[128 + r];
+    if (ok_all && ntq[q] > 0 && mbar_wait_warp(bars.o_done + q, (ntq[q] - 1) & 1, abort_flag, wait_ns)) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
-      const long long obase = (q_row0 + (long long)qt * BM + r) * D;
+      const float inv_l = 1.f / l_row;
+      const long long obase = (q_row0 + (long long)qt * BM + r) * D + hf * (D / 2);
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t o[32];
-        tmem_ld32(lane_addr + C::kColO0 + q * D + 32 * cc, o);
+        tmem_ld32(lane_addr + ocol + 32 * cc, o);
         tmem_ld_wait(o);
         if constexpr (OUT32) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_ptr) + obase + 32 * cc);
@@ -346,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 16) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
@@ -358,8 +387,14 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   using C = CfgBF16<D>;
   static bool attr_done = false;   // the attribute is a property of the function, set once per process
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bf16_kernel<D, OUT32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+    // The warpgroup register split assumes kLaunchRegs registers per thread at
+    // launch; with fewer, a setmaxnreg increase could never be satisfied.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_bf16_kernel<D, OUT32>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(attn_bf16_kernel<D, OUT32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }

@@ -21,9 +21,13 @@
 // 2^64 below the running maximum contributes below float32 resolution and is
 // skipped for that row (its P^ row is zero).
 //
-// CTA layout (384 threads): warps 0-3 / 4-7 own query tiles 0 / 1 (one thread
-// per row: softmax, P quantisation, O correction, epilogue); warp 8 issues TMA
-// and bulk copies; warp 9 issues MMAs and scale-factor copies; warps 10-11 idle.
+// CTA layout (640 threads): warps 0-15 are softmax warps -- warp w serves query
+// tile w/8, key half (w/4)%2 (64 of the 128 columns of a score tile) and rows
+// 32*(w%4)..+31, so every row is shared by two threads (one per key half) that
+// exchange their half-row maxima through SMEM; each thread quantises its half
+// of P, corrects its half of O and writes its half of the output.  Warp 16
+// issues TMA and bulk copies, warp 17 issues MMAs and scale-factor copies,
+// warps 18-19 idle.
 // Tensor memory: S (128 columns, shared by both query tiles), O0, O1 (d
 // columns each), then scale factors (4 columns per 64-deep K chunk, copied
 // from SMEM with tcgen05.cp, replicated to the four lane quarters).
@@ -38,7 +42,11 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int kThreads = 384;
+constexpr int kThreads = 640;
+constexpr int kSoftmaxRegs = 104;   // 16 softmax warps
+constexpr int kOtherRegs = 64;      // producer / MMA warpgroup
+constexpr int kLaunchRegs = 96;     // 65536 / 640 rounded down to a multiple of 8
+static_assert(16 * 32 * kSoftmaxRegs + 4 * 32 * kOtherRegs <= kThreads * kLaunchRegs, "register split");
 constexpr float kLog2PRange = 11.392317422778761f;   // log2(448 * 6)
 constexpr float kSkipBelow = 64.0f;                   // log2 units
 
@@ -62,7 +70,8 @@ struct CfgF4 {
   static constexpr int kOffKSf = kOffQSf + 2 * kQSfBytes;
   static constexpr int kOffVSf = kOffKSf + NS * kKSfBytes;
   static constexpr int kOffPSf = kOffVSf + NS * kVSfBytes;
-  static constexpr int kOffBar = kOffPSf + 2 * kPSfBytes;
+  static constexpr int kOffX = kOffPSf + 2 * kPSfBytes;     // [2 slots][2 q][2 halves][128 rows] float
+  static constexpr int kOffBar = kOffX + 2 * 2 * 2 * 128 * 4;
   static constexpr int kNumBars = 1 + 4 * NS + 8 + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   // Q/K rows of 64 bytes use the 64B swizzle, rows of 32 bytes the 32B one.
@@ -133,13 +142,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i) mbar_init(bar_base + i, 1);
     for (int q = 0; q < 2; ++q) {
-      mbar_init(bars.s_free + q, 128);
-      mbar_init(bars.p_full + q, 128);
+      mbar_init(bars.s_free + q, 256);
+      mbar_init(bars.p_full + q, 256);
     }
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 8) {
+  if (warp == 16) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -151,7 +160,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long bhq = (long long)b * H + h;
   const long long bhk = (long long)b * Hkv + hk;
 
-  if (warp == 8) {
+  if (warp >= 16) {
+    // Register split: the launch gives every thread kLaunchRegs; this
+    // warpgroup (producer, MMA issuer, two idle warps) keeps kOtherRegs and the
+    // four softmax warpgroups take kSoftmaxRegs (sum checked above).
+    reg_dealloc<kOtherRegs>();
+    if (warp == 16) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmap_q);
@@ -193,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == 17) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t sQ = smem_u32(smem + C::kOffQ);
@@ -281,104 +295,141 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(bars.drain, 0, wait_ns);
       }
     }
-  } else if (warp < 8) {
+    }
+  } else {
+    reg_alloc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax + P quantisation
-    const int q = warp / 4;
-    const int r = (warp % 4) * 32 + lane;
+    const int q = warp / 8;                                   // query tile
+    const int hf = (warp / 4) & 1;                            // key half: columns 64*hf .. +63
+    const int r = (warp % 4) * 32 + lane;                     // row within the query tile
     const uint32_t lane_addr = tbase + (((warp % 4) * 32) << 16);
     const int qt = qt0 + q;
+    const int bar_id = 1 + q * 4 + (warp % 4);                // the two warps sharing these rows
     const float c = 1.4426950408889634f * rsqrtf((float)D);
+    float* xch = reinterpret_cast<float*>(smem + C::kOffX);   // [slot][q][half][row]
     uint8_t* prow = smem + C::kOffP + q * C::kPBytes + r * 64;
-    uint8_t* psf = smem + C::kOffPSf + q * C::kPSfBytes + (r % 32) * 16 + (r / 32) * 4;
+    uint8_t* psf = smem + C::kOffPSf + q * C::kPSfBytes + hf * 512 + (r % 32) * 16 + (r / 32) * 4;
+    const uint32_t ocol = C::kColO0 + q * D + hf * (D / 2);   // this thread's half of O
     float m_run = -INFINITY, m_ref = 0.f, lam = 0.f;
     bool have_ref = false, ok = true;
+    // Both warps of a row pair execute every named barrier below the same
+    // number of times (once per tile, once at the end), also when a bounded
+    // wait gave up: a warp that gave up keeps iterating, skipping the work.
     for (int j = 0; j < ntq[q]; ++j) {
-      if (!mbar_wait_warp(bars.s_full + q, j & 1, abort_flag, wait_ns)) {
-        ok = false;
-        break;
+      if (ok) ok = mbar_wait_warp(bars.s_full + q, j & 1, abort_flag, wait_ns);
+      uint32_t sr[2][32];
+      if (ok) {
+        tc_fence_after();
+        tmem_ld32(lane_addr + C::kColS + 64 * hf, sr[0]);
+        tmem_ld32(lane_addr + C::kColS + 64 * hf + 32, sr[1]);
+        tmem_ld_wait(sr[0]);
+        tmem_launder(sr[1]);
+        tc_fence_before();
+        mbar_arrive(bars.s_free + q);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) sr[i / 32][i % 32] = 0u;
       }
-      tc_fence_after();
-      uint32_t sr[4][32];
+      float sv[64];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) tmem_ld32(lane_addr + C::kColS + 32 * i, sr[i]);
-      tmem_ld_wait(sr[0]);
-      tmem_launder(sr[1]);
-      tmem_launder(sr[2]);
-      tmem_launder(sr[3]);
-      tc_fence_before();
-      mbar_arrive(bars.s_free + q);
-      float sv[128];
-#pragma unroll
-      for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
+      for (int i = 0; i < 64; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
       if (causal && j == qt) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i > r) sv[i] = -INFINITY;
+        for (int i = 0; i < 64; ++i)
+          if (64 * hf + i > r) sv[i] = -INFINITY;
       }
-      float mx = sv[0];
+      // Group maxima of the raw scores; the row maximum follows from them (and
+      // the partner's half), and since x -> 2^(x*c + b) is increasing, each
+      // group's P2 maximum is the exponential of its score maximum.
+      float gm[4];
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, sv[i]);
+      for (int g = 0; g < 4; ++g) gm[g] = max16(sv + 16 * g);
+      float* slot = xch + (j & 1) * 512 + q * 256;
+      slot[hf * 128 + r] = fmaxf(fmaxf(gm[0], gm[1]), fmaxf(gm[2], gm[3]));
+      named_barrier_sync(bar_id, 64);
+      const float mx = fmaxf(slot[r], slot[128 + r]);
+      if (!ok) continue;
       const float m_t = mx * c;
       const float m_new = fmaxf(m_run, m_t);
       const bool live = (m_t > -INFINITY) && (m_t >= m_new - kSkipBelow);
       m_run = m_new;
-      uint32_t codes[16];
-      uint32_t sfw[2] = {0u, 0u};
+      uint32_t codes[8];
+      uint32_t sfw = 0u;
       float corr = 1.f;
       if (live) {
         const float bias = kLog2PRange - m_t;
-        float rs = 0.f;
+        float rsp[8];   // independent partial sums keep the add chain short
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          sv[i] = ex2_approx(fmaf(sv[i], c, bias));
-          rs += sv[i];
+        for (int i = 0; i < 8; ++i) rsp[i] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          fma2(sv[i], sv[i + 1], sv[i], sv[i + 1], c, c, bias, bias);
+          sv[i] = ex2_approx(sv[i]);
+          sv[i + 1] = ex2_approx(sv[i + 1]);
+          const int a = (i / 2) % 4;
+          add2(rsp[2 * a], rsp[2 * a + 1], rsp[2 * a], rsp[2 * a + 1], sv[i], sv[i + 1]);
         }
+        const float rs = ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
         corr = have_ref ? ex2_approx(m_ref - m_t) : 1.f;
-        lam = have_ref ? fmaf(lam, corr, rs) : rs;
+        lam = have_ref ? fmaf(lam, corr, rs) : rs;    // this half's share of the row sum
         m_ref = m_t;
         have_ref = true;
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          float amax = sv[16 * g];
+        for (int g = 0; g < 4; g += 2) {
+          const float a0 = ex2_approx(fmaf(gm[g], c, bias)), a1 = ex2_approx(fmaf(gm[g + 1], c, bias));
+          float sc0, sc1;
+          mul2(sc0, sc1, a0, a1, 1.0f / 6.0f, 1.0f / 6.0f);
+          const uint32_t s16 = cvt_e4m3x2(sc0, sc1);
+          const uint32_t s80 = s16 & 0xFFu, s81 = s16 >> 8;
+          const float inv0 = s80 ? rcp_approx(e4m3_to_f32(s80)) : 0.f;
+          const float inv1 = s81 ? rcp_approx(e4m3_to_f32(s81)) : 0.f;
+          float* p = sv + 16 * g;
 #pragma unroll
-          for (int i = 1; i < 16; ++i) amax = fmaxf(amax, sv[16 * g + i]);
-          const uint32_t s8 = cvt_e4m3x2(amax * (1.0f / 6.0f), 0.f) & 0xFFu;
-          const float sf = e4m3_to_f32(s8);
-          const float inv = s8 ? rcp_approx(sf) : 0.f;
-          const float* p = sv + 16 * g;
-          codes[2 * g] = cvt_e2m1x8(p[0] * inv, p[1] * inv, p[2] * inv, p[3] * inv, p[4] * inv, p[5] * inv,
-                                    p[6] * inv, p[7] * inv);
-          codes[2 * g + 1] = cvt_e2m1x8(p[8] * inv, p[9] * inv, p[10] * inv, p[11] * inv, p[12] * inv,
-                                        p[13] * inv, p[14] * inv, p[15] * inv);
-          sfw[g / 4] |= s8 << (8 * (g % 4));
+          for (int i = 0; i < 16; i += 2) mul2(p[i], p[i + 1], p[i], p[i + 1], inv0, inv0);
+#pragma unroll
+          for (int i = 16; i < 32; i += 2) mul2(p[i], p[i + 1], p[i], p[i + 1], inv1, inv1);
+          codes[2 * g] = cvt_e2m1x8(p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7]);
+          codes[2 * g + 1] = cvt_e2m1x8(p[8], p[9], p[10], p[11], p[12], p[13], p[14], p[15]);
+          codes[2 * g + 2] = cvt_e2m1x8(p[16], p[17], p[18], p[19], p[20], p[21], p[22], p[23]);
+          codes[2 * g + 3] = cvt_e2m1x8(p[24], p[25], p[26], p[27], p[28], p[29], p[30], p[31]);
+          sfw |= s16 << (8 * g);
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) codes[i] = 0u;
+        for (int i = 0; i < 8; ++i) codes[i] = 0u;
       }
       if (j > 0) {
-        if (!mbar_wait_warp(bars.o_done + q, (j - 1) & 1, abort_flag, wait_ns)) {
-          ok = false;
-          break;
-        }
+        ok = mbar_wait_warp(bars.o_done + q, (j - 1) & 1, abort_flag, wait_ns);
+        if (!ok) continue;
         tc_fence_after();
       }
-      // P^ row r: four 16-byte chunks, 64B-swizzled (chunk c at c ^ ((r >> 1) & 3))
+      // this half of P^ row r: 16-byte chunks 2*hf and 2*hf+1 of the 64-byte
+      // row, 64B-swizzled (chunk c is stored at c ^ ((r >> 1) & 3))
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
+      for (int k = 0; k < 2; ++k) {
+        const int ch = 2 * hf + k;
         *reinterpret_cast<uint4*>(prow + ((ch ^ ((r >> 1) & 3)) * 16)) =
-            make_uint4(codes[4 * ch], codes[4 * ch + 1], codes[4 * ch + 2], codes[4 * ch + 3]);
-      *reinterpret_cast<uint32_t*>(psf) = sfw[0];
-      *reinterpret_cast<uint32_t*>(psf + 512) = sfw[1];
+            make_uint4(codes[4 * k], codes[4 * k + 1], codes[4 * k + 2], codes[4 * k + 3]);
+      }
+      *reinterpret_cast<uint32_t*>(psf) = sfw;
       if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(lane_addr + C::kColO0 + q * D + 32 * cc, o);
-          tmem_ld_wait(o);
+        // this half of the O row: loaded before one wait, scaled, stored back
+        uint32_t o[D / 64][32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
-          tmem_st32(lane_addr + C::kColO0 + q * D + 32 * cc, o);
+        for (int cc = 0; cc < D / 64; ++cc) tmem_ld32(lane_addr + ocol + 32 * cc, o[cc]);
+        tmem_ld_wait(o[0]);
+#pragma unroll
+        for (int cc = 1; cc < D / 64; ++cc) tmem_launder(o[cc]);
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float a = __uint_as_float(o[cc][i]), b = __uint_as_float(o[cc][i + 1]);
+            mul2(a, b, a, b, corr, corr);
+            o[cc][i] = __float_as_uint(a);
+            o[cc][i + 1] = __float_as_uint(b);
+          }
+          tmem_st32(lane_addr + ocol + 32 * cc, o[cc]);
         }
         tmem_st_wait();
       }
@@ -386,14 +437,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bars.p_full + q);
     }
-    if (ok && ntq[q] > 0 && mbar_wait_warp(bars.o_done + q, (ntq[q] - 1) & 1, abort_flag, wait_ns)) {
+    // the two halves' row sums are in the same units (both follow the shared
+    // tile maxima); combine them, then write this half of the output row
+    const bool ok_all = __all_sync(0xffffffffu, ok);
+    float* slot = xch + (ntq[q] & 1) * 512 + q * 256;
+    slot[hf * 128 + r] = lam;
+    named_barrier_sync(bar_id, 64);
+    const float lam_row = slot[r] + slot[128 + r];
+    if (ok_all && ntq[q] > 0 && mbar_wait_warp(bars.o_done + q, (ntq[q] - 1) & 1, abort_flag, wait_ns)) {
       tc_fence_after();
-      const float inv_l = 1.f / lam;
-      const long long obase = (bhq * L + (long long)qt * BM + r) * D;
+      const float inv_l = 1.f / lam_row;
+      const long long obase = (bhq * L + (long long)qt * BM + r) * D + hf * (D / 2);
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t o[32];
-        tmem_ld32(lane_addr + C::kColO0 + q * D + 32 * cc, o);
+        tmem_ld32(lane_addr + ocol + 32 * cc, o);
         tmem_ld_wait(o);
         if constexpr (OUT32) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_ptr) + obase + 32 * cc);
@@ -416,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 16) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
@@ -428,8 +486,14 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   using C = CfgF4<D>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(attn_nvfp4_kernel<D, OUT32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+    // The warpgroup register split assumes kLaunchRegs registers per thread at
+    // launch; with fewer, a setmaxnreg increase could never be satisfied.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_nvfp4_kernel<D, OUT32>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(attn_nvfp4_kernel<D, OUT32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
