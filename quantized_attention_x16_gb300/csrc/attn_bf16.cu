@@ -8,14 +8,14 @@
 // roles) as in the Blackwell attention pipelines the page "kernel overview"
 // describes (AVO: MMA, softmax, correction and load warps).
 //
-// CTA layout (640 threads):
-//   warps 0-15 : softmax + correction + epilogue; warp w serves query tile
-//                w/8, key half (w/4)%2 (64 of the 128 score columns) and rows
-//                32*(w%4)..+31 -- two threads per row exchange half-row maxima
-//                through SMEM and each handles its half of P and of O
-//   warp 16    : TMA producer (Q once, then K/V tiles into an NS-stage ring)
-//   warp 17    : MMA issuer (one thread)
-//   warps 18-19: idle
+// CTA layout (384 threads):
+//   warps 0-3  : softmax + correction + epilogue of query tile 0 (one thread
+//                per row)
+//   warps 4-7  : the same for query tile 1
+//   warp 8     : TMA producer (Q once, then K/V tiles into an NS-stage ring)
+//   warp 9     : MMA issuer (one thread; descriptors built once, a use adds
+//                its byte offset to the start-address field)
+//   warps 10-11: idle
 // Tensor memory (512 columns): S (one 128-column region shared by the two
 // query tiles), O0, O1 (d columns each), P0, P1 (64 columns each, bf16
 // pairs).  S = Q K^T is read into registers, P = 2^(x - m) is written back as
@@ -33,11 +33,11 @@ namespace {
 
 constexpr int BM = 128;         // query rows per tile
 constexpr int BN = 128;         // keys per KV tile
-constexpr int kThreads = 640;
-constexpr int kSoftmaxRegs = 104;   // 16 softmax warps
+constexpr int kThreads = 384;
+constexpr int kSoftmaxRegs = 216;   // 8 softmax warps
 constexpr int kOtherRegs = 64;      // producer / MMA warpgroup
-constexpr int kLaunchRegs = 96;     // 65536 / 640 rounded down to a multiple of 8
-static_assert(16 * 32 * kSoftmaxRegs + 4 * 32 * kOtherRegs <= kThreads * kLaunchRegs, "register split");
+constexpr int kLaunchRegs = 168;    // 65536 / 384 rounded down to a multiple of 8
+static_assert(8 * 32 * kSoftmaxRegs + 4 * 32 * kOtherRegs <= kThreads * kLaunchRegs, "register split");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 template <int D>
@@ -48,8 +48,7 @@ struct CfgBF16 {
   static constexpr int kOffQ = 0;                         // Q0, Q1
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + NS * kTileBytes;
-  static constexpr int kOffX = kOffV + NS * kTileBytes;     // [2 slots][2 q][2 halves][128 rows] float
-  static constexpr int kOffBar = kOffX + 2 * 2 * 2 * 128 * 4;
+  static constexpr int kOffBar = kOffV + NS * kTileBytes;
   static constexpr int kNumBars = 1 + 4 * NS + 8 + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;   // + alignment slack
   static constexpr uint32_t kColS = 0;
@@ -71,6 +70,10 @@ struct BarsBF16 {
   uint64_t* o_done;   // [2]
   uint64_t* drain;    // MMA clean-up on abort
 };
+
+// A shared-memory descriptor displaced by `bytes` (16-byte units land in the
+// 14-bit start-address field; addresses stay below 256 KB, so no carry).
+__device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
 
 template <int D, bool OUT32>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -111,13 +114,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i) mbar_init(bar_base + i, 1);
     for (int q = 0; q < 2; ++q) {
-      mbar_init(bars.s_free + q, 256);
-      mbar_init(bars.p_full + q, 256);
+      mbar_init(bars.s_free + q, 128);
+      mbar_init(bars.p_full + q, 128);
     }
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 16) {
+  if (warp == 8) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -129,12 +132,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long q_row0 = ((long long)b * H + h) * L;      // first row of this head in Q/O
   const long long kv_row0 = ((long long)b * Hkv + hk) * L;
 
-  if (warp >= 16) {
+  if (warp >= 8) {
     // Register split: the launch gives every thread kLaunchRegs; this
     // warpgroup (producer, MMA issuer, two idle warps) keeps kOtherRegs and the
-    // four softmax warpgroups take kSoftmaxRegs (sum checked above).
+    // two softmax warpgroups take kSoftmaxRegs (sum checked above).
     reg_dealloc<kOtherRegs>();
-    if (warp == 16) {
+    if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmap_q);
@@ -175,24 +178,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 17) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t sQ = smem_u32(smem + C::kOffQ);
-      const uint32_t sK = smem_u32(smem + C::kOffK);
-      const uint32_t sV = smem_u32(smem + C::kOffV);
+      const uint64_t dQ = sdesc(smem_u32(smem + C::kOffQ), 16, 1024, kSwizzle128B);
+      const uint64_t dK = sdesc(smem_u32(smem + C::kOffK), 16, 1024, kSwizzle128B);
+      const uint64_t dV = sdesc(smem_u32(smem + C::kOffV), C::kHalfBytes, 1024, kSwizzle128B);
+      const uint32_t tS = tbase + C::kColS;
       int last_q = -1, last_j = 0;
       bool ok = mbar_wait(bars.q_full, 0, abort_flag, wait_ns);
       auto issue_s = [&](int q, int j) -> bool {
         if (last_q >= 0 && !mbar_wait(bars.s_free + last_q, last_j & 1, abort_flag, wait_ns)) return false;
         tc_fence_after();
-        const int s = j % C::NS;
+        const uint32_t s = j % C::NS;
+        const uint64_t a0 = dadd(dQ, q * C::kTileBytes), b0 = dadd(dK, s * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
-          const uint64_t a = sdesc(sQ + q * C::kTileBytes + off, 16, 1024, kSwizzle128B);
-          const uint64_t bd = sdesc(sK + s * C::kTileBytes + off, 16, 1024, kSwizzle128B);
-          mma_bf16_ss(tbase + C::kColS, a, bd, C::kIdescS, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tS, dadd(a0, off), dadd(b0, off), C::kIdescS, kk > 0 ? 1u : 0u);
         }
         tc_commit(bars.s_full + q);
         last_q = q;
@@ -202,13 +205,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int q, int j) -> bool {
         if (!mbar_wait(bars.p_full + q, j & 1, abort_flag, wait_ns)) return false;
         tc_fence_after();
-        const int s = j % C::NS;
+        const uint32_t s = j % C::NS;
+        const uint64_t b0 = dadd(dV, s * C::kTileBytes);
+        const uint32_t tO = tbase + C::kColO0 + q * D, tP = tbase + C::kColP0 + q * 64;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd = sdesc(sV + s * C::kTileBytes + kk * 16 * 128, C::kHalfBytes, 1024, kSwizzle128B);
-          mma_bf16_ts(tbase + C::kColO0 + q * D, tbase + C::kColP0 + q * 64 + kk * 8, bd, C::kIdescPV,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_bf16_ts(tO, tP + kk * 8, dadd(b0, kk * 16 * 128), C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(bars.o_done + q);
         return true;
       };
@@ -247,51 +249,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     reg_alloc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax
-    const int q = warp / 8;                                    // query tile
-    const int hf = (warp / 4) & 1;                             // key half: columns 64*hf .. +63
+    const int q = warp / 4;
     const int r = (warp % 4) * 32 + lane;                      // row within the query tile
     const uint32_t lane_addr = tbase + (((warp % 4) * 32) << 16);
     const int qt = qt0 + q;
-    const int bar_id = 1 + q * 4 + (warp % 4);                 // the two warps sharing these rows
     const float c = 1.4426950408889634f * rsqrtf((float)D);
-    float* xch = reinterpret_cast<float*>(smem + C::kOffX);    // [slot][q][half][row]
-    const uint32_t ocol = C::kColO0 + q * D + hf * (D / 2);    // this thread's half of O
+    const uint32_t ocol = C::kColO0 + q * D;
     float m_use = -INFINITY, l = 0.f;
     bool ok = true;
-    // Both warps of a row pair execute every named barrier the same number of
-    // times (once per tile, once at the end), also after a bounded wait gave up.
     for (int j = 0; j < ntq[q]; ++j) {
-      if (ok) ok = mbar_wait_warp(bars.s_full + q, j & 1, abort_flag, wait_ns);
-      uint32_t sr[2][32];
-      if (ok) {
-        tc_fence_after();
-        tmem_ld32(lane_addr + C::kColS + 64 * hf, sr[0]);
-        tmem_ld32(lane_addr + C::kColS + 64 * hf + 32, sr[1]);
-        tmem_ld_wait(sr[0]);
-        tmem_launder(sr[1]);
-        tc_fence_before();
-        mbar_arrive(bars.s_free + q);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) sr[i / 32][i % 32] = 0u;
+      if (!mbar_wait_warp(bars.s_full + q, j & 1, abort_flag, wait_ns)) {
+        ok = false;
+        break;
       }
-      float sv[64];
+      tc_fence_after();
+      uint32_t sr[4][32];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
+      for (int i = 0; i < 4; ++i) tmem_ld32(lane_addr + C::kColS + 32 * i, sr[i]);
+      tmem_ld_wait(sr[0]);
+      tmem_launder(sr[1]);
+      tmem_launder(sr[2]);
+      tmem_launder(sr[3]);
+      tc_fence_before();
+      mbar_arrive(bars.s_free + q);
+      float sv[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
       if (causal && j == qt) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (64 * hf + i > r) sv[i] = -INFINITY;
+        for (int i = 0; i < 128; ++i)
+          if (i > r) sv[i] = -INFINITY;
       }
-      float* slot = xch + (j & 1) * 512 + q * 256;
-      slot[hf * 128 + r] = max3(max3(max16(sv), max16(sv + 16), max16(sv + 32)), max16(sv + 48), -INFINITY);
-      named_barrier_sync(bar_id, 64);
-      const float mx = fmaxf(slot[r], slot[128 + r]);
-      if (!ok) continue;
+      float gm[8];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) gm[g] = max16(sv + 16 * g);
+      const float mx = max3(max3(gm[0], gm[1], gm[2]), max3(gm[3], gm[4], gm[5]), fmaxf(gm[6], gm[7]));
       const float m_t = mx * c;
       float alpha = 1.f;
       bool resc = false;
-      if (m_t > m_use + kRescaleThreshold) {      // both halves decide alike (shared m_t)
+      if (m_t > m_use + kRescaleThreshold) {
         alpha = ex2_approx(m_use - m_t);
         m_use = m_t;
         resc = (j > 0);
@@ -300,9 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sp[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) sp[i] = 0.f;
-      uint32_t pk[32];
+      uint32_t pk[64];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 64; ++i) {
         float p0, p1;
         fma2(p0, p1, sv[2 * i], sv[2 * i + 1], c, c, negm, negm);
         p0 = ex2_approx(p0);
@@ -312,45 +308,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk[i] = pack_bf16x2(p0, p1);
       }
       const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-      l = l * alpha + sum;                                     // this half's share of the row sum
+      l = l * alpha + sum;
       if (j > 0) {
-        ok = mbar_wait_warp(bars.o_done + q, (j - 1) & 1, abort_flag, wait_ns);
-        if (!ok) continue;
+        if (!mbar_wait_warp(bars.o_done + q, (j - 1) & 1, abort_flag, wait_ns)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
       }
       if (__any_sync(0xffffffffu, resc)) {     // rare: one 32-column chunk at a time
 #pragma unroll 1
-        for (int cc = 0; cc < D / 64; ++cc) {
+        for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
           tmem_ld32(lane_addr + ocol + 32 * cc, o);
           tmem_ld_wait(o);
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            float a = __uint_as_float(o[i]), b = __uint_as_float(o[i + 1]);
-            mul2(a, b, a, b, alpha, alpha);
+            float a = __uint_as_float(o[i]), bb = __uint_as_float(o[i + 1]);
+            mul2(a, bb, a, bb, alpha, alpha);
             o[i] = __float_as_uint(a);
-            o[i + 1] = __float_as_uint(b);
+            o[i + 1] = __float_as_uint(bb);
           }
           tmem_st32(lane_addr + ocol + 32 * cc, o);
         }
       }
-      tmem_st32(lane_addr + C::kColP0 + q * 64 + 32 * hf, pk);
+      uint32_t p_lo[32], p_hi[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        p_lo[i] = pk[i];
+        p_hi[i] = pk[32 + i];
+      }
+      tmem_st32(lane_addr + C::kColP0 + q * 64, p_lo);
+      tmem_st32(lane_addr + C::kColP0 + q * 64 + 32, p_hi);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bars.p_full + q);
     }
-    // ---- epilogue: combine the halves' row sums, then O / l for this half
-    const bool ok_all = __all_sync(0xffffffffu, ok);
-    float* slot = xch + (ntq[q] & 1) * 512 + q * 256;
-    slot[hf * 128 + r] = l;
-    named_barrier_sync(bar_id, 64);
-    const float l_row = slot[r] + slot[128 + r];
-    if (ok_all && ntq[q] > 0 && mbar_wait_warp(bars.o_done + q, (ntq[q] - 1) & 1, abort_flag, wait_ns)) {
+    // ---- epilogue: O / l
+    if (ok && ntq[q] > 0 && mbar_wait_warp(bars.o_done + q, (ntq[q] - 1) & 1, abort_flag, wait_ns)) {
       tc_fence_after();
-      const float inv_l = 1.f / l_row;
-      const long long obase = (q_row0 + (long long)qt * BM + r) * D + hf * (D / 2);
+      const float inv_l = 1.f / l;
+      const long long obase = (q_row0 + (long long)qt * BM + r) * D;
 #pragma unroll 1
-      for (int cc = 0; cc < D / 64; ++cc) {
+      for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         tmem_ld32(lane_addr + ocol + 32 * cc, o);
         tmem_ld_wait(o);
@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 16) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }

@@ -21,16 +21,17 @@
 // 2^64 below the running maximum contributes below float32 resolution and is
 // skipped for that row (its P^ row is zero).
 //
-// CTA layout (640 threads): warps 0-15 are softmax warps -- warp w serves query
-// tile w/8, key half (w/4)%2 (64 of the 128 columns of a score tile) and rows
-// 32*(w%4)..+31, so every row is shared by two threads (one per key half) that
-// exchange their half-row maxima through SMEM; each thread quantises its half
-// of P, corrects its half of O and writes its half of the output.  Warp 16
-// issues TMA and bulk copies, warp 17 issues MMAs and scale-factor copies,
-// warps 18-19 idle.
-// Tensor memory: S (128 columns, shared by both query tiles), O0, O1 (d
-// columns each), then scale factors (4 columns per 64-deep K chunk, copied
-// from SMEM with tcgen05.cp, replicated to the four lane quarters).
+// Arithmetic per element: the group maximum of P2 is 2^(max16(x) - m_j) * 2688
+// (2^x is increasing), and the division by the group scale is folded into
+// the exponent, P2 / s2 = 2^(x*c + b - log2 s2); so one FMA and one exp2 give
+// the value to encode, and sum(P2) = sum over groups of s2 * sum(P2/s2).
+//
+// CTA layout (384 threads): warps 0-3 / 4-7 own query tiles 0 / 1 (one thread
+// per row: softmax, P quantisation, O correction, epilogue); warp 8 issues TMA
+// and bulk copies; warp 9 issues MMAs and scale-factor copies;
+// warps 10-11 idle.  Tensor memory: S (128 columns, shared by both query
+// tiles), O0, O1 (d columns each), then scale factors (4 columns per 64-deep K
+// chunk, copied from SMEM with tcgen05.cp, replicated to the four lane quarters).
 
 #include <cuda_bf16.h>
 
@@ -42,11 +43,11 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int kThreads = 640;
-constexpr int kSoftmaxRegs = 104;   // 16 softmax warps
-constexpr int kOtherRegs = 64;      // producer / MMA warpgroup
-constexpr int kLaunchRegs = 96;     // 65536 / 640 rounded down to a multiple of 8
-static_assert(16 * 32 * kSoftmaxRegs + 4 * 32 * kOtherRegs <= kThreads * kLaunchRegs, "register split");
+constexpr int kThreads = 384;
+constexpr int kSoftmaxRegs = 200;   // 8 softmax warps
+constexpr int kOtherRegs = 96;      // producer / MMA warpgroup
+constexpr int kLaunchRegs = 168;    // 65536 / 384 rounded down to a multiple of 8
+static_assert(8 * 32 * kSoftmaxRegs + 4 * 32 * kOtherRegs <= kThreads * kLaunchRegs, "register split");
 constexpr float kLog2PRange = 11.392317422778761f;   // log2(448 * 6)
 constexpr float kSkipBelow = 64.0f;                   // log2 units
 
@@ -70,8 +71,7 @@ struct CfgF4 {
   static constexpr int kOffKSf = kOffQSf + 2 * kQSfBytes;
   static constexpr int kOffVSf = kOffKSf + NS * kKSfBytes;
   static constexpr int kOffPSf = kOffVSf + NS * kVSfBytes;
-  static constexpr int kOffX = kOffPSf + 2 * kPSfBytes;     // [2 slots][2 q][2 halves][128 rows] float
-  static constexpr int kOffBar = kOffX + 2 * 2 * 2 * 128 * 4;
+  static constexpr int kOffBar = kOffPSf + 2 * kPSfBytes;
   static constexpr int kNumBars = 1 + 4 * NS + 8 + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   // Q/K rows of 64 bytes use the 64B swizzle, rows of 32 bytes the 32B one.
@@ -81,25 +81,39 @@ struct CfgF4 {
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColO0 = 128;
   static constexpr uint32_t kColSf = 128 + 2 * D;
+  // K and V scale columns are double-buffered by tile parity: a tcgen05.cp
+  // is not ordered after earlier MMAs that read the columns it overwrites, so
+  // tile j+1's scales must not land where tile j's MMAs may still be reading.
   static constexpr uint32_t kColSfQ0 = kColSf + 0;
   static constexpr uint32_t kColSfQ1 = kColSf + 8;
-  static constexpr uint32_t kColSfK = kColSf + 16;
-  static constexpr uint32_t kColSfV = kColSf + 24;
-  static constexpr uint32_t kColSfP0 = kColSf + 32;
-  static constexpr uint32_t kColSfP1 = kColSf + 40;
+  static constexpr uint32_t kColSfK = kColSf + 16;     // + 8 * (j & 1)
+  static constexpr uint32_t kColSfV = kColSf + 32;     // + 8 * (j & 1)
+  static constexpr uint32_t kColSfP0 = kColSf + 48;
+  static constexpr uint32_t kColSfP1 = kColSf + 56;
   static constexpr uint32_t kIdescS = idesc_nvf4(BM, BN);
   static constexpr uint32_t kIdescPV = idesc_nvf4(BM, D);
-  static_assert(kColSf + 48 <= 512, "tensor memory overflow");
+  static_assert(kColSf + 64 <= 512, "tensor memory overflow");
 };
 
 struct BarsF4 {
   uint64_t *q_full, *k_full, *k_empty, *v_full, *v_empty, *s_full, *s_free, *p_full, *o_done, *drain;
 };
 
-// Copies `nblk` consecutive 512-byte scale blocks from SMEM to tensor memory
-// columns [col, col + 4*nblk), replicated across the four lane quarters.
+// Descriptors are built at each use from a 32-bit shared address.  (Kernels
+// that kept precomputed 64-bit descriptors in registers and offset them were
+// observed to feed the first MMA of a CTA an all-zero A descriptor -- it read
+// the reserved head of the shared window -- while building them in place, as
+// here, gave exact results; the cause was not visible from the source.)
+__device__ __forceinline__ uint64_t desc_qk(uint32_t saddr, uint32_t sbo, uint32_t swz) {
+  return sdesc(saddr, 16, sbo, swz);
+}
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) { return sdesc(saddr, 0, 128, kSwizzleNone); }
+
+// Copies `nblk` consecutive 512-byte scale blocks at shared address `saddr` to
+// tensor memory columns [col, col + 4*nblk), replicated across the four lane
+// quarters.
 __device__ __forceinline__ void copy_sf(uint32_t tcol, uint32_t saddr, int nblk) {
-  for (int i = 0; i < nblk; ++i) tmem_cp_32x128b_warpx4(tcol + 4 * i, sdesc(saddr + 512 * i, 0, 128, kSwizzleNone));
+  for (int i = 0; i < nblk; ++i) tmem_cp_32x128b_warpx4(tcol + 4 * i, desc_sf(saddr + 512 * i));
 }
 
 template <int D, bool OUT32>
@@ -142,13 +156,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i) mbar_init(bar_base + i, 1);
     for (int q = 0; q < 2; ++q) {
-      mbar_init(bars.s_free + q, 256);
-      mbar_init(bars.p_full + q, 256);
+      mbar_init(bars.s_free + q, 128);
+      mbar_init(bars.p_full + q, 128);
     }
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 16) {
+  if (warp == 8) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -160,14 +174,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long bhq = (long long)b * H + h;
   const long long bhk = (long long)b * Hkv + hk;
 
-  if (warp >= 16) {
+  if (warp >= 8) {
     // Register split: the launch gives every thread kLaunchRegs; this
     // warpgroup (producer, MMA issuer, two idle warps) keeps kOtherRegs and the
-    // four softmax warpgroups take kSoftmaxRegs (sum checked above).
+    // two softmax warpgroups take kSoftmaxRegs (sum checked above).
     reg_dealloc<kOtherRegs>();
-    if (warp == 16) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (warp == 8 && lane == 0) {
+      // ---------------------------------------------------------- producer
       tma_prefetch_desc(&tmap_q);
       tma_prefetch_desc(&tmap_k);
       tma_prefetch_desc(&tmap_v);
@@ -206,31 +219,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_drain((u % 2 == 0) ? bars.k_full + s : bars.v_full + s, (j / C::NS) & 1, wait_ns);
         }
       }
-    }
-  } else if (warp == 17) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t sQ = smem_u32(smem + C::kOffQ);
-      const uint32_t sK = smem_u32(smem + C::kOffK);
-      const uint32_t sV = smem_u32(smem + C::kOffV);
-      const uint32_t sP = smem_u32(smem + C::kOffP);
-      const uint32_t sQSf = smem_u32(smem + C::kOffQSf);
-      const uint32_t sKSf = smem_u32(smem + C::kOffKSf);
-      const uint32_t sVSf = smem_u32(smem + C::kOffVSf);
-      const uint32_t sPSf = smem_u32(smem + C::kOffPSf);
+    } else if (warp == 9 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      const uint32_t sb = smem_u32(smem);
+      const uint32_t tS = tbase + C::kColS;
       int last_q = -1, last_j = 0;
       auto issue_s = [&](int q, int j) -> bool {
         if (last_q >= 0 && !mbar_wait(bars.s_free + last_q, last_j & 1, abort_flag, wait_ns)) return false;
         tc_fence_after();
-        const int s = j % C::NS;
+        const uint32_t s = j % C::NS;
         const uint32_t sfq = tbase + (q ? C::kColSfQ1 : C::kColSfQ0);
+        const uint32_t sfk = tbase + C::kColSfK + 8 * (j & 1);
 #pragma unroll
-        for (int kk = 0; kk < D / 64; ++kk) {
-          const uint64_t a = sdesc(sQ + q * C::kQBytes + kk * 32, 16, C::kQKSbo, C::kQKSwz);
-          const uint64_t bd = sdesc(sK + s * C::kKBytes + kk * 32, 16, C::kQKSbo, C::kQKSwz);
-          mma_nvf4(tbase + C::kColS, a, bd, C::kIdescS, sfq + 4 * kk, tbase + C::kColSfK + 4 * kk,
-                   kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < D / 64; ++kk)
+          mma_nvf4(tS, desc_qk(sb + C::kOffQ + q * C::kQBytes + kk * 32, C::kQKSbo, C::kQKSwz),
+                   desc_qk(sb + C::kOffK + s * C::kKBytes + kk * 32, C::kQKSbo, C::kQKSwz), C::kIdescS, sfq + 4 * kk,
+                   sfk + 4 * kk, kk > 0 ? 1u : 0u);
         tc_commit(bars.s_full + q);
         last_q = q;
         last_j = j;
@@ -239,29 +243,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int q, int j) -> bool {
         if (!mbar_wait(bars.p_full + q, j & 1, abort_flag, wait_ns)) return false;
         tc_fence_after();
-        const int s = j % C::NS;
+        const uint32_t s = j % C::NS;
         const uint32_t sfp = tbase + (q ? C::kColSfP1 : C::kColSfP0);
-        copy_sf(sfp, sPSf + q * C::kPSfBytes, 2);
+        copy_sf(sfp, sb + C::kOffPSf + q * C::kPSfBytes, 2);
+        const uint32_t tO = tbase + C::kColO0 + q * D;
+        const uint32_t sfv = tbase + C::kColSfV + 8 * (j & 1);
 #pragma unroll
-        for (int kk = 0; kk < BN / 64; ++kk) {
-          const uint64_t a = sdesc(sP + q * C::kPBytes + kk * 32, 16, 512, kSwizzle64B);
-          const uint64_t bd = sdesc(sV + s * C::kVBytes + kk * 32, 16, 512, kSwizzle64B);
-          mma_nvf4(tbase + C::kColO0 + q * D, a, bd, C::kIdescPV, sfp + 4 * kk, tbase + C::kColSfV + 4 * kk,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BN / 64; ++kk)
+          mma_nvf4(tO, desc_qk(sb + C::kOffP + q * C::kPBytes + kk * 32, 512, kSwizzle64B),
+                   desc_qk(sb + C::kOffV + s * C::kVBytes + kk * 32, 512, kSwizzle64B), C::kIdescPV, sfp + 4 * kk,
+                   sfv + 4 * kk, (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(bars.o_done + q);
         return true;
       };
       bool ok = mbar_wait(bars.q_full, 0, abort_flag, wait_ns);
       if (ok) {
         tc_fence_after();
-        copy_sf(tbase + C::kColSfQ0, sQSf, D / 64);
-        if (q1_valid) copy_sf(tbase + C::kColSfQ1, sQSf + C::kQSfBytes, D / 64);
+        copy_sf(tbase + C::kColSfQ0, sb + C::kOffQSf, D / 64);
+        if (q1_valid) copy_sf(tbase + C::kColSfQ1, sb + C::kOffQSf + C::kQSfBytes, D / 64);
         ok = mbar_wait(bars.k_full, 0, abort_flag, wait_ns);
       }
       if (ok) {
         tc_fence_after();
-        copy_sf(tbase + C::kColSfK, sKSf, D / 64);
+        copy_sf(tbase + C::kColSfK, sb + C::kOffKSf, D / 64);             // tile 0: parity 0
         if (ntq[0] > 0) ok = issue_s(0, 0);
         if (ok && ntq[1] > 0) ok = issue_s(1, 0);
         if (ok) tc_commit(bars.k_empty);
@@ -273,14 +277,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(bars.k_full + s1, ((j + 1) / C::NS) & 1, abort_flag, wait_ns);
           if (ok) {
             tc_fence_after();
-            copy_sf(tbase + C::kColSfK, sKSf + s1 * C::kKSfBytes, D / 64);
+            copy_sf(tbase + C::kColSfK + 8 * ((j + 1) & 1), sb + C::kOffKSf + s1 * C::kKSfBytes, D / 64);
             if (j + 1 < ntq[0]) ok = issue_s(0, j + 1);
           }
         }
         if (ok) ok = mbar_wait(bars.v_full + s, (j / C::NS) & 1, abort_flag, wait_ns);
         if (ok) {
           tc_fence_after();
-          copy_sf(tbase + C::kColSfV, sVSf + s * C::kVSfBytes, 2);
+          copy_sf(tbase + C::kColSfV + 8 * (j & 1), sb + C::kOffVSf + s * C::kVSfBytes, 2);
           if (j < ntq[0]) ok = issue_pv(0, j);
         }
         if (ok && j + 1 < nt) {
@@ -295,139 +299,133 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(bars.drain, 0, wait_ns);
       }
     }
-    }
   } else {
     reg_alloc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax + P quantisation
-    const int q = warp / 8;                                   // query tile
-    const int hf = (warp / 4) & 1;                            // key half: columns 64*hf .. +63
-    const int r = (warp % 4) * 32 + lane;                     // row within the query tile
+    const int q = warp / 4;
+    const int r = (warp % 4) * 32 + lane;
     const uint32_t lane_addr = tbase + (((warp % 4) * 32) << 16);
     const int qt = qt0 + q;
-    const int bar_id = 1 + q * 4 + (warp % 4);                // the two warps sharing these rows
     const float c = 1.4426950408889634f * rsqrtf((float)D);
-    float* xch = reinterpret_cast<float*>(smem + C::kOffX);   // [slot][q][half][row]
     uint8_t* prow = smem + C::kOffP + q * C::kPBytes + r * 64;
-    uint8_t* psf = smem + C::kOffPSf + q * C::kPSfBytes + hf * 512 + (r % 32) * 16 + (r / 32) * 4;
-    const uint32_t ocol = C::kColO0 + q * D + hf * (D / 2);   // this thread's half of O
+    uint8_t* psf = smem + C::kOffPSf + q * C::kPSfBytes + (r % 32) * 16 + (r / 32) * 4;
+    const uint32_t ocol = C::kColO0 + q * D;
     float m_run = -INFINITY, m_ref = 0.f, lam = 0.f;
     bool have_ref = false, ok = true;
-    // Both warps of a row pair execute every named barrier below the same
-    // number of times (once per tile, once at the end), also when a bounded
-    // wait gave up: a warp that gave up keeps iterating, skipping the work.
     for (int j = 0; j < ntq[q]; ++j) {
-      if (ok) ok = mbar_wait_warp(bars.s_full + q, j & 1, abort_flag, wait_ns);
-      uint32_t sr[2][32];
-      if (ok) {
-        tc_fence_after();
-        tmem_ld32(lane_addr + C::kColS + 64 * hf, sr[0]);
-        tmem_ld32(lane_addr + C::kColS + 64 * hf + 32, sr[1]);
-        tmem_ld_wait(sr[0]);
-        tmem_launder(sr[1]);
-        tc_fence_before();
-        mbar_arrive(bars.s_free + q);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) sr[i / 32][i % 32] = 0u;
+      if (!mbar_wait_warp(bars.s_full + q, j & 1, abort_flag, wait_ns)) {
+        ok = false;
+        break;
       }
-      float sv[64];
+      tc_fence_after();
+      uint32_t sr[4][32];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
+      for (int i = 0; i < 4; ++i) tmem_ld32(lane_addr + C::kColS + 32 * i, sr[i]);
+      tmem_ld_wait(sr[0]);
+      tmem_launder(sr[1]);
+      tmem_launder(sr[2]);
+      tmem_launder(sr[3]);
+      tc_fence_before();
+      mbar_arrive(bars.s_free + q);
+      float sv[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
       if (causal && j == qt) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (64 * hf + i > r) sv[i] = -INFINITY;
+        for (int i = 0; i < 128; ++i)
+          if (i > r) sv[i] = -INFINITY;
       }
-      // Group maxima of the raw scores; the row maximum follows from them (and
-      // the partner's half), and since x -> 2^(x*c + b) is increasing, each
-      // group's P2 maximum is the exponential of its score maximum.
-      float gm[4];
+      float gm[8];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) gm[g] = max16(sv + 16 * g);
-      float* slot = xch + (j & 1) * 512 + q * 256;
-      slot[hf * 128 + r] = fmaxf(fmaxf(gm[0], gm[1]), fmaxf(gm[2], gm[3]));
-      named_barrier_sync(bar_id, 64);
-      const float mx = fmaxf(slot[r], slot[128 + r]);
-      if (!ok) continue;
+      for (int g = 0; g < 8; ++g) gm[g] = max16(sv + 16 * g);
+      const float mx = max3(max3(gm[0], gm[1], gm[2]), max3(gm[3], gm[4], gm[5]), fmaxf(gm[6], gm[7]));
       const float m_t = mx * c;
       const float m_new = fmaxf(m_run, m_t);
       const bool live = (m_t > -INFINITY) && (m_t >= m_new - kSkipBelow);
       m_run = m_new;
-      uint32_t codes[8];
-      uint32_t sfw = 0u;
+      uint32_t codes[16];
+      uint32_t sfw[2] = {0u, 0u};
       float corr = 1.f;
       if (live) {
         const float bias = kLog2PRange - m_t;
-        float rsp[8];   // independent partial sums keep the add chain short
+        float rs = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) rsp[i] = 0.f;
-#pragma unroll
-        for (int i = 0; i < 64; i += 2) {
-          fma2(sv[i], sv[i + 1], sv[i], sv[i + 1], c, c, bias, bias);
-          sv[i] = ex2_approx(sv[i]);
-          sv[i + 1] = ex2_approx(sv[i + 1]);
-          const int a = (i / 2) % 4;
-          add2(rsp[2 * a], rsp[2 * a + 1], rsp[2 * a], rsp[2 * a + 1], sv[i], sv[i + 1]);
-        }
-        const float rs = ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
-        corr = have_ref ? ex2_approx(m_ref - m_t) : 1.f;
-        lam = have_ref ? fmaf(lam, corr, rs) : rs;    // this half's share of the row sum
-        m_ref = m_t;
-        have_ref = true;
-#pragma unroll
-        for (int g = 0; g < 4; g += 2) {
-          const float a0 = ex2_approx(fmaf(gm[g], c, bias)), a1 = ex2_approx(fmaf(gm[g + 1], c, bias));
+        for (int g = 0; g < 8; g += 2) {
+          // group scales from the group maxima of P2 = 2^(x*c + bias)
+          float a0, a1;
+          fma2(a0, a1, gm[g], gm[g + 1], c, c, bias, bias);
+          a0 = ex2_approx(a0);
+          a1 = ex2_approx(a1);
           float sc0, sc1;
           mul2(sc0, sc1, a0, a1, 1.0f / 6.0f, 1.0f / 6.0f);
           const uint32_t s16 = cvt_e4m3x2(sc0, sc1);
           const uint32_t s80 = s16 & 0xFFu, s81 = s16 >> 8;
-          const float inv0 = s80 ? rcp_approx(e4m3_to_f32(s80)) : 0.f;
-          const float inv1 = s81 ? rcp_approx(e4m3_to_f32(s81)) : 0.f;
+          // exponent offsets: P2 / s2 = 2^(x*c + bias - log2 s2); a zero scale
+          // (the whole group underflows) encodes zeros and sums P2 itself
+          const float f0 = s80 ? e4m3_to_f32(s80) : 1.f, f1 = s81 ? e4m3_to_f32(s81) : 1.f;
+          const float b0 = bias - lg2_approx(f0), b1 = bias - lg2_approx(f1);
           float* p = sv + 16 * g;
+          float u[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int i = 0; i < 16; i += 2) mul2(p[i], p[i + 1], p[i], p[i + 1], inv0, inv0);
+          for (int i = 0; i < 16; i += 2) {
+            fma2(p[i], p[i + 1], p[i], p[i + 1], c, c, b0, b0);
+            p[i] = ex2_approx(p[i]);
+            p[i + 1] = ex2_approx(p[i + 1]);
+            add2(u[0], u[1], u[0], u[1], p[i], p[i + 1]);
+          }
 #pragma unroll
-          for (int i = 16; i < 32; i += 2) mul2(p[i], p[i + 1], p[i], p[i + 1], inv1, inv1);
-          codes[2 * g] = cvt_e2m1x8(p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7]);
-          codes[2 * g + 1] = cvt_e2m1x8(p[8], p[9], p[10], p[11], p[12], p[13], p[14], p[15]);
-          codes[2 * g + 2] = cvt_e2m1x8(p[16], p[17], p[18], p[19], p[20], p[21], p[22], p[23]);
-          codes[2 * g + 3] = cvt_e2m1x8(p[24], p[25], p[26], p[27], p[28], p[29], p[30], p[31]);
-          sfw |= s16 << (8 * g);
+          for (int i = 16; i < 32; i += 2) {
+            fma2(p[i], p[i + 1], p[i], p[i + 1], c, c, b1, b1);
+            p[i] = ex2_approx(p[i]);
+            p[i + 1] = ex2_approx(p[i + 1]);
+            add2(u[2], u[3], u[2], u[3], p[i], p[i + 1]);
+          }
+          rs = fmaf(u[0] + u[1], f0, rs);
+          rs = fmaf(u[2] + u[3], f1, rs);
+          codes[2 * g] = s80 ? cvt_e2m1x8(p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7]) : 0u;
+          codes[2 * g + 1] = s80 ? cvt_e2m1x8(p[8], p[9], p[10], p[11], p[12], p[13], p[14], p[15]) : 0u;
+          codes[2 * g + 2] = s81 ? cvt_e2m1x8(p[16], p[17], p[18], p[19], p[20], p[21], p[22], p[23]) : 0u;
+          codes[2 * g + 3] = s81 ? cvt_e2m1x8(p[24], p[25], p[26], p[27], p[28], p[29], p[30], p[31]) : 0u;
+          sfw[g / 4] |= s16 << (8 * (g % 4));
         }
+        corr = have_ref ? ex2_approx(m_ref - m_t) : 1.f;
+        lam = have_ref ? fmaf(lam, corr, rs) : rs;
+        m_ref = m_t;
+        have_ref = true;
       } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) codes[i] = 0u;
+        for (int i = 0; i < 16; ++i) codes[i] = 0u;
       }
       if (j > 0) {
-        ok = mbar_wait_warp(bars.o_done + q, (j - 1) & 1, abort_flag, wait_ns);
-        if (!ok) continue;
+        if (!mbar_wait_warp(bars.o_done + q, (j - 1) & 1, abort_flag, wait_ns)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
       }
-      // this half of P^ row r: 16-byte chunks 2*hf and 2*hf+1 of the 64-byte
-      // row, 64B-swizzled (chunk c is stored at c ^ ((r >> 1) & 3))
+      // P^ row r: four 16-byte chunks, 64B-swizzled (chunk c at c ^ ((r >> 1) & 3))
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int ch = 2 * hf + k;
+      for (int ch = 0; ch < 4; ++ch)
         *reinterpret_cast<uint4*>(prow + ((ch ^ ((r >> 1) & 3)) * 16)) =
-            make_uint4(codes[4 * k], codes[4 * k + 1], codes[4 * k + 2], codes[4 * k + 3]);
-      }
-      *reinterpret_cast<uint32_t*>(psf) = sfw;
+            make_uint4(codes[4 * ch], codes[4 * ch + 1], codes[4 * ch + 2], codes[4 * ch + 3]);
+      *reinterpret_cast<uint32_t*>(psf) = sfw[0];
+      *reinterpret_cast<uint32_t*>(psf + 512) = sfw[1];
       if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-        // this half of the O row: loaded before one wait, scaled, stored back
-        uint32_t o[D / 64][32];
+        // the O row: all chunks loaded before one wait, scaled, stored back
+        uint32_t o[D / 32][32];
 #pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) tmem_ld32(lane_addr + ocol + 32 * cc, o[cc]);
+        for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(lane_addr + ocol + 32 * cc, o[cc]);
         tmem_ld_wait(o[0]);
 #pragma unroll
-        for (int cc = 1; cc < D / 64; ++cc) tmem_launder(o[cc]);
+        for (int cc = 1; cc < D / 32; ++cc) tmem_launder(o[cc]);
 #pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) {
+        for (int cc = 0; cc < D / 32; ++cc) {
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            float a = __uint_as_float(o[cc][i]), b = __uint_as_float(o[cc][i + 1]);
-            mul2(a, b, a, b, corr, corr);
+            float a = __uint_as_float(o[cc][i]), bb = __uint_as_float(o[cc][i + 1]);
+            mul2(a, bb, a, bb, corr, corr);
             o[cc][i] = __float_as_uint(a);
-            o[cc][i + 1] = __float_as_uint(b);
+            o[cc][i + 1] = __float_as_uint(bb);
           }
           tmem_st32(lane_addr + ocol + 32 * cc, o[cc]);
         }
@@ -437,19 +435,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bars.p_full + q);
     }
-    // the two halves' row sums are in the same units (both follow the shared
-    // tile maxima); combine them, then write this half of the output row
-    const bool ok_all = __all_sync(0xffffffffu, ok);
-    float* slot = xch + (ntq[q] & 1) * 512 + q * 256;
-    slot[hf * 128 + r] = lam;
-    named_barrier_sync(bar_id, 64);
-    const float lam_row = slot[r] + slot[128 + r];
-    if (ok_all && ntq[q] > 0 && mbar_wait_warp(bars.o_done + q, (ntq[q] - 1) & 1, abort_flag, wait_ns)) {
+    if (ok && ntq[q] > 0 && mbar_wait_warp(bars.o_done + q, (ntq[q] - 1) & 1, abort_flag, wait_ns)) {
       tc_fence_after();
-      const float inv_l = 1.f / lam_row;
-      const long long obase = (bhq * L + (long long)qt * BM + r) * D + hf * (D / 2);
+      const float inv_l = 1.f / lam;
+      const long long obase = (bhq * L + (long long)qt * BM + r) * D;
 #pragma unroll 1
-      for (int cc = 0; cc < D / 64; ++cc) {
+      for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         tmem_ld32(lane_addr + ocol + 32 * cc, o);
         tmem_ld_wait(o);
@@ -474,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 16) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
