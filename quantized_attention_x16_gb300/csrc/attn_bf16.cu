@@ -34,8 +34,9 @@ namespace {
 constexpr int BM = 128;         // query rows per tile
 constexpr int BN = 128;         // keys per KV tile
 constexpr int kThreads = 384;
+constexpr uint32_t kProducerSleepNs = 256;   // poll interval of the TMA producer's waits
 constexpr int kSoftmaxRegs = 216;   // 8 softmax warps
-constexpr int kOtherRegs = 64;      // producer / MMA warpgroup
+constexpr int kOtherRegs = 72;      // producer / MMA warpgroup
 constexpr int kLaunchRegs = 168;    // 65536 / 384 rounded down to a multiple of 8
 static_assert(8 * 32 * kSoftmaxRegs + 4 * 32 * kOtherRegs <= kThreads * kLaunchRegs, "register split");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -137,36 +138,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warpgroup (producer, MMA issuer, two idle warps) keeps kOtherRegs and the
     // two softmax warpgroups take kSoftmaxRegs (sum checked above).
     reg_dealloc<kOtherRegs>();
+    // The producer and MMA warps run their loops with all 32 lanes (waits are
+    // warp-wide, addresses and descriptors warp-uniform); one elected lane
+    // issues each TMA copy, tcgen05 instruction and commit.
     if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmap_q);
-      tma_prefetch_desc(&tmap_k);
-      tma_prefetch_desc(&tmap_v);
+      // ---------------------------------------------------------- producer
+      const bool leader = elect_one();
       const int nq = q1_valid ? 2 : 1;
-      mbar_arrive_expect_tx(bars.q_full, nq * C::kTileBytes);
-      for (int q = 0; q < nq; ++q)
-        for (int hh = 0; hh < D / 64; ++hh)
-          tma_load_2d(smem + C::kOffQ + q * C::kTileBytes + hh * C::kHalfBytes, &tmap_q, bars.q_full, hh * 64,
-                      (int)(q_row0 + (long long)(qt0 + q) * BM));
+      if (leader) {
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_v);
+        mbar_arrive_expect_tx(bars.q_full, nq * C::kTileBytes);
+        for (int q = 0; q < nq; ++q)
+          for (int hh = 0; hh < D / 64; ++hh)
+            tma_load_2d(smem + C::kOffQ + q * C::kTileBytes + hh * C::kHalfBytes, &tmap_q, bars.q_full, hh * 64,
+                        (int)(q_row0 + (long long)(qt0 + q) * BM));
+      }
       int issued = 0;
       for (int j = 0; j < nt; ++j) {
         const int s = j % C::NS;
         const uint32_t par = ((j / C::NS) - 1) & 1;
         const int y = (int)(kv_row0 + (long long)j * BN);
-        if (j >= C::NS && !mbar_wait(bars.k_empty + s, par, abort_flag, wait_ns)) break;
-        mbar_arrive_expect_tx(bars.k_full + s, C::kTileBytes);
-        for (int hh = 0; hh < D / 64; ++hh)
-          tma_load_2d(smem + C::kOffK + s * C::kTileBytes + hh * C::kHalfBytes, &tmap_k, bars.k_full + s, hh * 64,
-                      y);
-        if (j >= C::NS && !mbar_wait(bars.v_empty + s, par, abort_flag, wait_ns)) {
+        if (j >= C::NS && !mbar_wait_backoff_warp(bars.k_empty + s, par, abort_flag, wait_ns, kProducerSleepNs)) break;
+        if (leader) {
+          mbar_arrive_expect_tx(bars.k_full + s, C::kTileBytes);
+          for (int hh = 0; hh < D / 64; ++hh)
+            tma_load_2d(smem + C::kOffK + s * C::kTileBytes + hh * C::kHalfBytes, &tmap_k, bars.k_full + s,
+                        hh * 64, y);
+        }
+        if (j >= C::NS && !mbar_wait_backoff_warp(bars.v_empty + s, par, abort_flag, wait_ns, kProducerSleepNs)) {
           issued = 2 * j + 1;
           break;
         }
-        mbar_arrive_expect_tx(bars.v_full + s, C::kTileBytes);
-        for (int hh = 0; hh < D / 64; ++hh)
-          tma_load_2d(smem + C::kOffV + s * C::kTileBytes + hh * C::kHalfBytes, &tmap_v, bars.v_full + s, hh * 64,
-                      y);
+        if (leader) {
+          mbar_arrive_expect_tx(bars.v_full + s, C::kTileBytes);
+          for (int hh = 0; hh < D / 64; ++hh)
+            tma_load_2d(smem + C::kOffV + s * C::kTileBytes + hh * C::kHalfBytes, &tmap_v, bars.v_full + s,
+                        hh * 64, y);
+        }
         issued = 2 * j + 2;
       }
       if (*abort_flag) {
@@ -177,74 +187,82 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_drain((u % 2 == 0) ? bars.k_full + s : bars.v_full + s, (j / C::NS) & 1, wait_ns);
         }
       }
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 9) {
+      // ---------------------------------------------------------- MMA issuer
+      const bool leader = elect_one();
       const uint64_t dQ = sdesc(smem_u32(smem + C::kOffQ), 16, 1024, kSwizzle128B);
       const uint64_t dK = sdesc(smem_u32(smem + C::kOffK), 16, 1024, kSwizzle128B);
       const uint64_t dV = sdesc(smem_u32(smem + C::kOffV), C::kHalfBytes, 1024, kSwizzle128B);
       const uint32_t tS = tbase + C::kColS;
       int last_q = -1, last_j = 0;
-      bool ok = mbar_wait(bars.q_full, 0, abort_flag, wait_ns);
+      bool ok = mbar_wait_warp(bars.q_full, 0, abort_flag, wait_ns);
       auto issue_s = [&](int q, int j) -> bool {
-        if (last_q >= 0 && !mbar_wait(bars.s_free + last_q, last_j & 1, abort_flag, wait_ns)) return false;
+        if (last_q >= 0 && !mbar_wait_warp(bars.s_free + last_q, last_j & 1, abort_flag, wait_ns)) return false;
         tc_fence_after();
         const uint32_t s = j % C::NS;
         const uint64_t a0 = dadd(dQ, q * C::kTileBytes), b0 = dadd(dK, s * C::kTileBytes);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
-          mma_bf16_ss(tS, dadd(a0, off), dadd(b0, off), C::kIdescS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
+            mma_bf16_ss(tS, dadd(a0, off), dadd(b0, off), C::kIdescS, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bars.s_full + q);
         }
-        tc_commit(bars.s_full + q);
+        __syncwarp();
         last_q = q;
         last_j = j;
         return true;
       };
       auto issue_pv = [&](int q, int j) -> bool {
-        if (!mbar_wait(bars.p_full + q, j & 1, abort_flag, wait_ns)) return false;
+        if (!mbar_wait_warp(bars.p_full + q, j & 1, abort_flag, wait_ns)) return false;
         tc_fence_after();
         const uint32_t s = j % C::NS;
         const uint64_t b0 = dadd(dV, s * C::kTileBytes);
         const uint32_t tO = tbase + C::kColO0 + q * D, tP = tbase + C::kColP0 + q * 64;
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ts(tO, tP + kk * 8, dadd(b0, kk * 16 * 128), C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bars.o_done + q);
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_bf16_ts(tO, tP + kk * 8, dadd(b0, kk * 16 * 128), C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(bars.o_done + q);
+        }
+        __syncwarp();
         return true;
       };
       if (ok) {
-        ok = mbar_wait(bars.k_full, 0, abort_flag, wait_ns);
+        ok = mbar_wait_warp(bars.k_full, 0, abort_flag, wait_ns);
         tc_fence_after();
         if (ok && ntq[0] > 0) ok = issue_s(0, 0);
         if (ok && ntq[1] > 0) ok = issue_s(1, 0);
-        if (ok) tc_commit(bars.k_empty);
+        if (ok && leader) tc_commit(bars.k_empty);
+        __syncwarp();
       }
       for (int j = 0; ok && j < nt; ++j) {
         const int s = j % C::NS;
         const int s1 = (j + 1) % C::NS;
         if (j + 1 < nt) {
-          ok = mbar_wait(bars.k_full + s1, ((j + 1) / C::NS) & 1, abort_flag, wait_ns);
+          ok = mbar_wait_warp(bars.k_full + s1, ((j + 1) / C::NS) & 1, abort_flag, wait_ns);
           tc_fence_after();
           if (ok && j + 1 < ntq[0]) ok = issue_s(0, j + 1);
         }
-        if (ok) ok = mbar_wait(bars.v_full + s, (j / C::NS) & 1, abort_flag, wait_ns);
+        if (ok) ok = mbar_wait_warp(bars.v_full + s, (j / C::NS) & 1, abort_flag, wait_ns);
         tc_fence_after();
         if (ok && j < ntq[0]) ok = issue_pv(0, j);
         if (ok && j + 1 < nt) {
           if (j + 1 < ntq[1]) ok = issue_s(1, j + 1);
-          if (ok) tc_commit(bars.k_empty + s1);
+          if (ok && leader) tc_commit(bars.k_empty + s1);
+          __syncwarp();
         }
         if (ok && j < ntq[1]) ok = issue_pv(1, j);
-        if (ok) tc_commit(bars.v_empty + s);
+        if (ok && leader) tc_commit(bars.v_empty + s);
+        __syncwarp();
       }
       if (!ok) {
         // drain the tensor pipe before tensor memory is released
-        tc_commit(bars.drain);
+        if (leader) tc_commit(bars.drain);
+        __syncwarp();
         mbar_wait_drain(bars.drain, 0, wait_ns);
       }
-    }
     }
   } else {
     reg_alloc<kSoftmaxRegs>();

@@ -28,7 +28,8 @@
 //
 // CTA layout (384 threads): warps 0-3 / 4-7 own query tiles 0 / 1 (one thread
 // per row: softmax, P quantisation, O correction, epilogue); warp 8 issues TMA
-// and bulk copies; warp 9 issues MMAs and scale-factor copies;
+// and bulk copies; warp 9 issues MMAs and scale-factor copies (both warps run
+// their loops with all lanes and issue from one elected lane);
 // warps 10-11 idle.  Tensor memory: S (128 columns, shared by both query
 // tiles), O0, O1 (d columns each), then scale factors (4 columns per 64-deep K
 // chunk, copied from SMEM with tcgen05.cp, replicated to the four lane quarters).
@@ -44,6 +45,7 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int kThreads = 384;
+constexpr uint32_t kProducerSleepNs = 256;   // poll interval of the TMA producer's waits
 constexpr int kSoftmaxRegs = 200;   // 8 softmax warps
 constexpr int kOtherRegs = 96;      // producer / MMA warpgroup
 constexpr int kLaunchRegs = 168;    // 65536 / 384 rounded down to a multiple of 8
@@ -179,123 +181,154 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warpgroup (producer, MMA issuer, two idle warps) keeps kOtherRegs and the
     // two softmax warpgroups take kSoftmaxRegs (sum checked above).
     reg_dealloc<kOtherRegs>();
-    if (warp == 8 && lane == 0) {
+    // The producer and MMA warps run their loops with all 32 lanes (waits are
+    // warp-wide, addresses and descriptors warp-uniform); one elected lane
+    // issues each TMA copy, tcgen05 instruction and commit.
+    if (warp == 8) {
       // ---------------------------------------------------------- producer
-      tma_prefetch_desc(&tmap_q);
-      tma_prefetch_desc(&tmap_k);
-      tma_prefetch_desc(&tmap_v);
+      const bool leader = elect_one();
       const int nq = q1_valid ? 2 : 1;
-      mbar_arrive_expect_tx(bars.q_full, nq * (C::kQBytes + C::kQSfBytes));
-      for (int q = 0; q < nq; ++q) {
-        const int qt = qt0 + q;
-        tma_load_2d(smem + C::kOffQ + q * C::kQBytes, &tmap_q, bars.q_full, 0, (int)(bhq * L + (long long)qt * BM));
-        bulk_load(smem + C::kOffQSf + q * C::kQSfBytes, q_sf + (bhq * (L / 128) + qt) * C::kQSfBytes,
-                  C::kQSfBytes, bars.q_full);
+      if (leader) {
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_v);
+        mbar_arrive_expect_tx(bars.q_full, nq * (C::kQBytes + C::kQSfBytes));
+        for (int q = 0; q < nq; ++q) {
+          const int qt = qt0 + q;
+          tma_load_2d(smem + C::kOffQ + q * C::kQBytes, &tmap_q, bars.q_full, 0,
+                      (int)(bhq * L + (long long)qt * BM));
+          bulk_load(smem + C::kOffQSf + q * C::kQSfBytes, q_sf + (bhq * (L / 128) + qt) * C::kQSfBytes,
+                    C::kQSfBytes, bars.q_full);
+        }
       }
       int issued = 0;
       for (int j = 0; j < nt; ++j) {
         const int s = j % C::NS;
         const uint32_t par = ((j / C::NS) - 1) & 1;
-        if (j >= C::NS && !mbar_wait(bars.k_empty + s, par, abort_flag, wait_ns)) break;
-        mbar_arrive_expect_tx(bars.k_full + s, C::kKBytes + C::kKSfBytes);
-        tma_load_2d(smem + C::kOffK + s * C::kKBytes, &tmap_k, bars.k_full + s, 0,
-                    (int)(bhk * L + (long long)j * BN));
-        bulk_load(smem + C::kOffKSf + s * C::kKSfBytes, k_sf + (bhk * (L / 128) + j) * C::kKSfBytes, C::kKSfBytes,
-                  bars.k_full + s);
-        if (j >= C::NS && !mbar_wait(bars.v_empty + s, par, abort_flag, wait_ns)) {
+        if (j >= C::NS && !mbar_wait_backoff_warp(bars.k_empty + s, par, abort_flag, wait_ns, kProducerSleepNs)) break;
+        if (leader) {
+          mbar_arrive_expect_tx(bars.k_full + s, C::kKBytes + C::kKSfBytes);
+          tma_load_2d(smem + C::kOffK + s * C::kKBytes, &tmap_k, bars.k_full + s, 0,
+                      (int)(bhk * L + (long long)j * BN));
+          bulk_load(smem + C::kOffKSf + s * C::kKSfBytes, k_sf + (bhk * (L / 128) + j) * C::kKSfBytes,
+                    C::kKSfBytes, bars.k_full + s);
+        }
+        if (j >= C::NS && !mbar_wait_backoff_warp(bars.v_empty + s, par, abort_flag, wait_ns, kProducerSleepNs)) {
           issued = 2 * j + 1;
           break;
         }
-        mbar_arrive_expect_tx(bars.v_full + s, C::kVBytes + C::kVSfBytes);
-        tma_load_2d(smem + C::kOffV + s * C::kVBytes, &tmap_v, bars.v_full + s, j * (BN / 2), (int)(bhk * D));
-        bulk_load(smem + C::kOffVSf + s * C::kVSfBytes, v_sf + (bhk * (L / 64) + 2 * j) * 512, C::kVSfBytes,
-                  bars.v_full + s);
+        if (leader) {
+          mbar_arrive_expect_tx(bars.v_full + s, C::kVBytes + C::kVSfBytes);
+          tma_load_2d(smem + C::kOffV + s * C::kVBytes, &tmap_v, bars.v_full + s, j * (BN / 2), (int)(bhk * D));
+          bulk_load(smem + C::kOffVSf + s * C::kVSfBytes, v_sf + (bhk * (L / 64) + 2 * j) * 512, C::kVSfBytes,
+                    bars.v_full + s);
+        }
         issued = 2 * j + 2;
       }
       if (*abort_flag) {
+        // let every copy already issued land before the CTA (and its shared
+        // memory) goes away
         mbar_wait_drain(bars.q_full, 0, wait_ns);
         for (int u = (issued > 2 * C::NS ? issued - 2 * C::NS : 0); u < issued; ++u) {
           const int j = u / 2, s = j % C::NS;
           mbar_wait_drain((u % 2 == 0) ? bars.k_full + s : bars.v_full + s, (j / C::NS) & 1, wait_ns);
         }
       }
-    } else if (warp == 9 && lane == 0) {
+    } else if (warp == 9) {
       // ---------------------------------------------------------- MMA issuer
+      const bool leader = elect_one();
       const uint32_t sb = smem_u32(smem);
       const uint32_t tS = tbase + C::kColS;
       int last_q = -1, last_j = 0;
       auto issue_s = [&](int q, int j) -> bool {
-        if (last_q >= 0 && !mbar_wait(bars.s_free + last_q, last_j & 1, abort_flag, wait_ns)) return false;
+        if (last_q >= 0 && !mbar_wait_warp(bars.s_free + last_q, last_j & 1, abort_flag, wait_ns)) return false;
         tc_fence_after();
         const uint32_t s = j % C::NS;
         const uint32_t sfq = tbase + (q ? C::kColSfQ1 : C::kColSfQ0);
         const uint32_t sfk = tbase + C::kColSfK + 8 * (j & 1);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 64; ++kk)
-          mma_nvf4(tS, desc_qk(sb + C::kOffQ + q * C::kQBytes + kk * 32, C::kQKSbo, C::kQKSwz),
-                   desc_qk(sb + C::kOffK + s * C::kKBytes + kk * 32, C::kQKSbo, C::kQKSwz), C::kIdescS, sfq + 4 * kk,
-                   sfk + 4 * kk, kk > 0 ? 1u : 0u);
-        tc_commit(bars.s_full + q);
+          for (int kk = 0; kk < D / 64; ++kk)
+            mma_nvf4(tS, desc_qk(sb + C::kOffQ + q * C::kQBytes + kk * 32, C::kQKSbo, C::kQKSwz),
+                     desc_qk(sb + C::kOffK + s * C::kKBytes + kk * 32, C::kQKSbo, C::kQKSwz), C::kIdescS,
+                     sfq + 4 * kk, sfk + 4 * kk, kk > 0 ? 1u : 0u);
+          tc_commit(bars.s_full + q);
+        }
+        __syncwarp();
         last_q = q;
         last_j = j;
         return true;
       };
       auto issue_pv = [&](int q, int j) -> bool {
-        if (!mbar_wait(bars.p_full + q, j & 1, abort_flag, wait_ns)) return false;
+        if (!mbar_wait_warp(bars.p_full + q, j & 1, abort_flag, wait_ns)) return false;
         tc_fence_after();
         const uint32_t s = j % C::NS;
         const uint32_t sfp = tbase + (q ? C::kColSfP1 : C::kColSfP0);
-        copy_sf(sfp, sb + C::kOffPSf + q * C::kPSfBytes, 2);
         const uint32_t tO = tbase + C::kColO0 + q * D;
         const uint32_t sfv = tbase + C::kColSfV + 8 * (j & 1);
+        if (leader) {
+          copy_sf(sfp, sb + C::kOffPSf + q * C::kPSfBytes, 2);
 #pragma unroll
-        for (int kk = 0; kk < BN / 64; ++kk)
-          mma_nvf4(tO, desc_qk(sb + C::kOffP + q * C::kPBytes + kk * 32, 512, kSwizzle64B),
-                   desc_qk(sb + C::kOffV + s * C::kVBytes + kk * 32, 512, kSwizzle64B), C::kIdescPV, sfp + 4 * kk,
-                   sfv + 4 * kk, (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bars.o_done + q);
+          for (int kk = 0; kk < BN / 64; ++kk)
+            mma_nvf4(tO, desc_qk(sb + C::kOffP + q * C::kPBytes + kk * 32, 512, kSwizzle64B),
+                     desc_qk(sb + C::kOffV + s * C::kVBytes + kk * 32, 512, kSwizzle64B), C::kIdescPV, sfp + 4 * kk,
+                     sfv + 4 * kk, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(bars.o_done + q);
+        }
+        __syncwarp();
         return true;
       };
-      bool ok = mbar_wait(bars.q_full, 0, abort_flag, wait_ns);
+      bool ok = mbar_wait_warp(bars.q_full, 0, abort_flag, wait_ns);
       if (ok) {
         tc_fence_after();
-        copy_sf(tbase + C::kColSfQ0, sb + C::kOffQSf, D / 64);
-        if (q1_valid) copy_sf(tbase + C::kColSfQ1, sb + C::kOffQSf + C::kQSfBytes, D / 64);
-        ok = mbar_wait(bars.k_full, 0, abort_flag, wait_ns);
+        if (leader) {
+          copy_sf(tbase + C::kColSfQ0, sb + C::kOffQSf, D / 64);
+          if (q1_valid) copy_sf(tbase + C::kColSfQ1, sb + C::kOffQSf + C::kQSfBytes, D / 64);
+        }
+        __syncwarp();
+        ok = mbar_wait_warp(bars.k_full, 0, abort_flag, wait_ns);
       }
       if (ok) {
         tc_fence_after();
-        copy_sf(tbase + C::kColSfK, sb + C::kOffKSf, D / 64);             // tile 0: parity 0
+        if (leader) copy_sf(tbase + C::kColSfK, sb + C::kOffKSf, D / 64);      // tile 0: parity 0
+        __syncwarp();
         if (ntq[0] > 0) ok = issue_s(0, 0);
         if (ok && ntq[1] > 0) ok = issue_s(1, 0);
-        if (ok) tc_commit(bars.k_empty);
+        if (ok && leader) tc_commit(bars.k_empty);
+        __syncwarp();
       }
       for (int j = 0; ok && j < nt; ++j) {
         const int s = j % C::NS;
         const int s1 = (j + 1) % C::NS;
         if (j + 1 < nt) {
-          ok = mbar_wait(bars.k_full + s1, ((j + 1) / C::NS) & 1, abort_flag, wait_ns);
+          ok = mbar_wait_warp(bars.k_full + s1, ((j + 1) / C::NS) & 1, abort_flag, wait_ns);
           if (ok) {
             tc_fence_after();
-            copy_sf(tbase + C::kColSfK + 8 * ((j + 1) & 1), sb + C::kOffKSf + s1 * C::kKSfBytes, D / 64);
+            if (leader)
+              copy_sf(tbase + C::kColSfK + 8 * ((j + 1) & 1), sb + C::kOffKSf + s1 * C::kKSfBytes, D / 64);
+            __syncwarp();
             if (j + 1 < ntq[0]) ok = issue_s(0, j + 1);
           }
         }
-        if (ok) ok = mbar_wait(bars.v_full + s, (j / C::NS) & 1, abort_flag, wait_ns);
+        if (ok) ok = mbar_wait_warp(bars.v_full + s, (j / C::NS) & 1, abort_flag, wait_ns);
         if (ok) {
           tc_fence_after();
-          copy_sf(tbase + C::kColSfV + 8 * (j & 1), sb + C::kOffVSf + s * C::kVSfBytes, 2);
+          if (leader) copy_sf(tbase + C::kColSfV + 8 * (j & 1), sb + C::kOffVSf + s * C::kVSfBytes, 2);
+          __syncwarp();
           if (j < ntq[0]) ok = issue_pv(0, j);
         }
         if (ok && j + 1 < nt) {
           if (j + 1 < ntq[1]) ok = issue_s(1, j + 1);
-          if (ok) tc_commit(bars.k_empty + s1);
+          if (ok && leader) tc_commit(bars.k_empty + s1);
+          __syncwarp();
         }
         if (ok && j < ntq[1]) ok = issue_pv(1, j);
-        if (ok) tc_commit(bars.v_empty + s);
+        if (ok && leader) tc_commit(bars.v_empty + s);
+        __syncwarp();
       }
       if (!ok) {
-        tc_commit(bars.drain);
+        if (leader) tc_commit(bars.drain);
+        __syncwarp();
         mbar_wait_drain(bars.drain, 0, wait_ns);
       }
     }
@@ -345,63 +378,82 @@ __global__ void __launch_bounds__(kThreads, 1)
       m_run = m_new;
       uint32_t codes[16];
       uint32_t sfw[2] = {0u, 0u};
-      float corr = 1.f;
-      if (live) {
-        const float bias = kLog2PRange - m_t;
-        float rs = 0.f;
-#pragma unroll
-        for (int g = 0; g < 8; g += 2) {
-          // group scales from the group maxima of P2 = 2^(x*c + bias)
-          float a0, a1;
-          fma2(a0, a1, gm[g], gm[g + 1], c, c, bias, bias);
-          a0 = ex2_approx(a0);
-          a1 = ex2_approx(a1);
-          float sc0, sc1;
-          mul2(sc0, sc1, a0, a1, 1.0f / 6.0f, 1.0f / 6.0f);
-          const uint32_t s16 = cvt_e4m3x2(sc0, sc1);
-          const uint32_t s80 = s16 & 0xFFu, s81 = s16 >> 8;
-          // exponent offsets: P2 / s2 = 2^(x*c + bias - log2 s2); a zero scale
-          // (the whole group underflows) encodes zeros and sums P2 itself
-          const float f0 = s80 ? e4m3_to_f32(s80) : 1.f, f1 = s81 ? e4m3_to_f32(s81) : 1.f;
-          const float b0 = bias - lg2_approx(f0), b1 = bias - lg2_approx(f1);
-          float* p = sv + 16 * g;
-          float u[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int i = 0; i < 16; i += 2) {
-            fma2(p[i], p[i + 1], p[i], p[i + 1], c, c, b0, b0);
-            p[i] = ex2_approx(p[i]);
-            p[i + 1] = ex2_approx(p[i + 1]);
-            add2(u[0], u[1], u[0], u[1], p[i], p[i + 1]);
-          }
-#pragma unroll
-          for (int i = 16; i < 32; i += 2) {
-            fma2(p[i], p[i + 1], p[i], p[i + 1], c, c, b1, b1);
-            p[i] = ex2_approx(p[i]);
-            p[i + 1] = ex2_approx(p[i + 1]);
-            add2(u[2], u[3], u[2], u[3], p[i], p[i + 1]);
-          }
-          rs = fmaf(u[0] + u[1], f0, rs);
-          rs = fmaf(u[2] + u[3], f1, rs);
-          codes[2 * g] = s80 ? cvt_e2m1x8(p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7]) : 0u;
-          codes[2 * g + 1] = s80 ? cvt_e2m1x8(p[8], p[9], p[10], p[11], p[12], p[13], p[14], p[15]) : 0u;
-          codes[2 * g + 2] = s81 ? cvt_e2m1x8(p[16], p[17], p[18], p[19], p[20], p[21], p[22], p[23]) : 0u;
-          codes[2 * g + 3] = s81 ? cvt_e2m1x8(p[24], p[25], p[26], p[27], p[28], p[29], p[30], p[31]) : 0u;
-          sfw[g / 4] |= s16 << (8 * (g % 4));
-        }
-        corr = have_ref ? ex2_approx(m_ref - m_t) : 1.f;
-        lam = have_ref ? fmaf(lam, corr, rs) : rs;
-        m_ref = m_t;
-        have_ref = true;
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) codes[i] = 0u;
-      }
+      const float corr = (live && have_ref) ? ex2_approx(m_ref - m_t) : 1.f;
+      // O is rescaled to the new tile maximum in 16-column chunks interleaved
+      // with the P work below (its loads overlap the arithmetic); warp-uniform
+      const bool do_corr = j > 0 && __any_sync(0xffffffffu, corr != 1.f);
       if (j > 0) {
+        // P^ and O of this query tile are free once P.V of the last tile is done
         if (!mbar_wait_warp(bars.o_done + q, (j - 1) & 1, abort_flag, wait_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
+      }
+      {
+        // Warp-uniform: a row that skips this tile gets bias = -inf, so its
+        // P2, codes, scales and sum are all zero (the O chunks below use
+        // warp-collective tensor-memory instructions).
+        const float bias = live ? kLog2PRange - m_t : -INFINITY;
+        // group scales s2 = e4m3(max16(P2) / 6) from the group maxima of
+        // P2 = 2^(x*c + bias), and the exponent offsets b_g = bias - log2 s2 so
+        // that P2 / s2 = 2^(x*c + b_g).  A zero scale (the group underflows:
+        // every P2 < 6 * 2^-10) keeps b_g = bias; its values are then below
+        // 0.25 and encode as code 0, and its sum is P2's own.
+        float bg[8], fg[8];
+        uint32_t s16[4];
+#pragma unroll
+        for (int g = 0; g < 8; g += 2) {
+          float a0, a1;
+          fma2(a0, a1, gm[g], gm[g + 1], c, c, bias, bias);
+          a0 = ex2_approx(a0);
+          a1 = ex2_approx(a1);
+          mul2(a0, a1, a0, a1, 1.0f / 6.0f, 1.0f / 6.0f);
+          s16[g / 2] = cvt_e4m3x2(a0, a1);
+          e4m3x2_to_f32(s16[g / 2], fg[g], fg[g + 1]);
+        }
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          fg[g] = fg[g] == 0.f ? 1.f : fg[g];
+          bg[g] = bias - lg2_approx(fg[g]);
+        }
+        sfw[0] = s16[0] | (s16[1] << 16);
+        sfw[1] = s16[2] | (s16[3] << 16);
+        float rs = 0.f;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          uint32_t o[16];
+          const bool chunk = do_corr && g < D / 16;
+          if (chunk) tmem_ld16(lane_addr + ocol + 16 * g, o);
+          float u[2] = {0.f, 0.f};
+          float* p = sv + 16 * g;
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            fma2(p[i], p[i + 1], p[i], p[i + 1], c, c, bg[g], bg[g]);
+            p[i] = ex2_approx(p[i]);
+            p[i + 1] = ex2_approx(p[i + 1]);
+            add2(u[0], u[1], u[0], u[1], p[i], p[i + 1]);
+          }
+          rs = fmaf(u[0] + u[1], fg[g], rs);
+          codes[2 * g] = cvt_e2m1x8(p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7]);
+          codes[2 * g + 1] = cvt_e2m1x8(p[8], p[9], p[10], p[11], p[12], p[13], p[14], p[15]);
+          if (chunk) {
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+              float x0 = __uint_as_float(o[i]), x1 = __uint_as_float(o[i + 1]);
+              mul2(x0, x1, x0, x1, corr, corr);
+              o[i] = __float_as_uint(x0);
+              o[i + 1] = __float_as_uint(x1);
+            }
+            tmem_st16(lane_addr + ocol + 16 * g, o);
+          }
+        }
+        if (live) {
+          lam = have_ref ? fmaf(lam, corr, rs) : rs;
+          m_ref = m_t;
+          have_ref = true;
+        }
       }
       // P^ row r: four 16-byte chunks, 64B-swizzled (chunk c at c ^ ((r >> 1) & 3))
 #pragma unroll
@@ -410,27 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             make_uint4(codes[4 * ch], codes[4 * ch + 1], codes[4 * ch + 2], codes[4 * ch + 3]);
       *reinterpret_cast<uint32_t*>(psf) = sfw[0];
       *reinterpret_cast<uint32_t*>(psf + 512) = sfw[1];
-      if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-        // the O row: all chunks loaded before one wait, scaled, stored back
-        uint32_t o[D / 32][32];
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(lane_addr + ocol + 32 * cc, o[cc]);
-        tmem_ld_wait(o[0]);
-#pragma unroll
-        for (int cc = 1; cc < D / 32; ++cc) tmem_launder(o[cc]);
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float a = __uint_as_float(o[cc][i]), bb = __uint_as_float(o[cc][i + 1]);
-            mul2(a, bb, a, bb, corr, corr);
-            o[cc][i] = __float_as_uint(a);
-            o[cc][i + 1] = __float_as_uint(bb);
-          }
-          tmem_st32(lane_addr + ocol + 32 * cc, o[cc]);
-        }
-        tmem_st_wait();
-      }
+      if (do_corr) tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bars.p_full + q);

@@ -80,6 +80,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Bounded wait for latency-tolerant waiters (the TMA producer, which runs
+// several stages ahead): sleeps `sleep_ns` between polls so that the waiting
+// warp leaves its scheduler's issue slots to the compute warps sharing it.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  uint64_t limit_ns, uint32_t sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      if (atomicExch((int*)abort, 1) == 0) atomicCAS(&g_device_error, 0, 4);
+      return false;
+    }
+  }
+}
+
 // Bounded wait used on clean-up paths: ignores the abort flag, records nothing.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
@@ -93,6 +111,21 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
                                                uint64_t limit_ns) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, limit_ns));
+}
+
+// Elects one lane of the (converged) warp: true in exactly one lane.  The
+// issuing warps run their loops with all 32 lanes, so the addresses and
+// descriptors feeding an instruction issued by the elected lane are
+// warp-uniform values.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
+  return p != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_backoff_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                       uint64_t limit_ns, uint32_t sleep_ns) {
+  return __all_sync(0xffffffffu, mbar_wait_backoff(bar, parity, abort, limit_ns, sleep_ns));
 }
 
 __device__ __forceinline__ void fence_barrier_init() {
@@ -256,6 +289,26 @@ __device__ __forceinline__ void tmem_launder(uint32_t (&r)[32]) {
   asm volatile("" : SA_M8(r, 0), SA_M8(r, 8), SA_M8(r, 16), SA_M8(r, 24));
 }
 
+// 16-column variants (lane i: columns [c, c + 16) of TMEM lane base + i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : SA_R8(r, 0), SA_R8(r, 8)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  asm volatile("" : SA_M8(r, 0), SA_M8(r, 8));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      SA_W8(r, 0), SA_W8(r, 8)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -295,6 +348,15 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
   // normal: (8 + m) * 2^(e - 10); subnormal: m * 2^-9
   const float mag = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : static_cast<float>(m) * 0.001953125f;
   return (b & 0x80u) ? -mag : mag;
+}
+
+// Two e4m3 codes (low byte -> lo) to float, exactly (every e4m3 value is an
+// f16 value).
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t codes16, float& lo, float& hi) {
+  asm("{\n\t.reg .b32 h;\n\t.reg .b16 a, l, u;\n\tcvt.u16.u32 a, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h, a;\n\tmov.b32 {l, u}, h;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, u;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(codes16));
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
