@@ -193,7 +193,7 @@ def run_ours(args, rank, world, local_rank):
         wall = time.perf_counter() - t0
     if world > 1:
         dist.barrier()
-    launches = args.steps * (3 + 1 + 1)      # sa_quantize: 3 kernels; each attention call: 1
+    launches = args.steps * (2 + 1 + 1)      # sa_quantize: 2 kernels; each attention call: 1
     tq = [a[0].elapsed_time(a[1]) * 1e-3 for a in evs]
     t4 = [a[1].elapsed_time(a[2]) * 1e-3 for a in evs]
     t16 = [a[2].elapsed_time(a[3]) * 1e-3 for a in evs]
@@ -286,10 +286,10 @@ def run_ours(args, rank, world, local_rank):
         "roofline_bf16": {"kernel": f"attn_bf16_kernel<{d}>", "bound": "tensor", "achieved": a16, "peak": pk["bf16"],
                           "unit": "TFLOP/s", "frac": a16 / pk["bf16"], "traffic": prof.get("attn_bf16"),
                           "peak_src": f"{pk['src']} bf16 burst"},
-        "roofline_quantize": {"kernel": "sa_quantize (3 kernels)", "bound": "hbm", "achieved": qbytes / t_q / 1e9,
+        "roofline_quantize": {"kernel": "sa_quantize (2 kernels)", "bound": "hbm", "achieved": qbytes / t_q / 1e9,
                               "peak": pk["hbm"], "unit": "GB/s", "frac": qbytes / t_q / 1e9 / pk["hbm"],
                               "traffic": None, "algorithmic_bytes": qbytes,
-                              "traffic_quant_kernel_only": prof.get("quant_kernel")},
+                              "traffic_kernels": {k: prof.get(k) for k in ("quant_qv_kernel", "quant_k_kernel")}},
         "cpu_baseline": cpu,
         "e2e": {"value": world * fl / t_e2e / 1e12, "unit": "TOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},

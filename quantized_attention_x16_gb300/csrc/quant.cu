@@ -34,60 +34,75 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
 }
 
 // Quantises one 1x16 group: returns the e4m3 scale byte, writes 2 words of codes.
+//
+// Both divisions are done as correctly rounded quotients without a divide
+// instruction (Markstein's correction step: with y = RN(1/b), q0 = RN(x*y)
+// and the exact remainder r = x - q0*b from one FMA, RN(q0 + r*y) = RN(x/b)).
+// This was checked exhaustively over all 2^23 significands against each
+// divisor significand 9/8 .. 15/8, which covers b = 6 (= 12/8 * 4) and every
+// e4m3 scale; exponents only shift the result.
+//  * scale: s = RN(max|x| / 6) with y = RN(1/6);
+//  * codes: the quotient is formed for the divisor -s, i.e. qn = RN(x / -s) =
+//    -RN(x / s) (rounding is symmetric), and the code sign bits are flipped
+//    afterwards (e2m1 is sign-magnitude).  This keeps the sign of a zero
+//    input: x = -0.0 gives qn = +0 and code 0x8, x = +0.0 gives code 0x0.
 __device__ __forceinline__ uint32_t quant_group16(const float* x, uint32_t* codes) {
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  const float s = __fdiv_rn(amax, 6.0f);
+  const float y6 = __uint_as_float(0x3E2AAAABu);        // RN(1/6)
+  const float q6 = amax * y6;
+  const float s = fmaf(fmaf(-q6, 6.0f, amax), y6, q6);
   const uint32_t s8 = cvt_e4m3x2(s, 0.f) & 0xFFu;
   if (s8 == 0u) {
     codes[0] = 0u;
     codes[1] = 0u;
     return 0u;
   }
-  const float sf = e4m3_to_f32(s8);
-  // x / sf, correctly rounded, without a per-element division: with
-  // y = RN(1/sf), q0 = RN(x*y) and the exact remainder r = x - q0*sf (one
-  // FMA), q = RN(q0 + r*y) equals RN(x/sf) for every float32 x and every e4m3
-  // scale (Markstein's correction step; checked exhaustively over all 2^23
-  // significands against each of the eight e4m3 significands -- a scale's
-  // exponent only shifts the result; zero inputs are handled by the sign copy).
-  const float y = __frcp_rn(sf);
+  float sf, unused;
+  e4m3x2_to_f32(s8, sf, unused);
+  const float ny = -__frcp_rn(sf);                      // RN(1 / -sf)
   float q[16];
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
-    float q0a, q0b, ra, rb;
-    mul2(q0a, q0b, x[i], x[i + 1], y, y);
-    fma2(ra, rb, -q0a, -q0b, sf, sf, x[i], x[i + 1]);
-    fma2(q[i], q[i + 1], ra, rb, y, y, q0a, q0b);
-    // the quotient carries the sign of x; the correction step would turn an
-    // input of exactly -0.0 into +0 (+0 + -0 = +0), which would lose code 0x8
-    q[i] = copysignf(q[i], x[i]);
-    q[i + 1] = copysignf(q[i + 1], x[i + 1]);
+    float n0, n1, t0, t1;
+    mul2(n0, n1, x[i], x[i + 1], ny, ny);               // q0' = RN(x * y')
+    fma2(t0, t1, n0, n1, sf, sf, x[i], x[i + 1]);       // r' = x - q0' * (-sf), exact
+    fma2(q[i], q[i + 1], t0, t1, ny, ny, n0, n1);       // RN(q0' + r' * y')
   }
-  codes[0] = cvt_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
-  codes[1] = cvt_e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]);
+  codes[0] = cvt_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]) ^ 0x88888888u;
+  codes[1] = cvt_e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]) ^ 0x88888888u;
   return s8;
 }
 
 // ---------------------------------------------------------------------------
-// Three launches, 256 threads per CTA:
-//   1. kpart_kernel : smooth-K partial sums, one thread per channel pair of one
-//                     128-token chunk, summed token by token (the documented
-//                     order); reads K once.
-//   2. kfinal_kernel: mean[c] = (partials summed in chunk order) / L.
-//   3. quant_kernel : three kinds of CTA --
-//        K CTAs first (K was just read by launch 1 and is still in L2):
-//                one thread per 1x16 group of K - mean along d;
-//        Q CTAs: one thread per 1x16 group along d (coalesced 32-byte reads,
-//                8-byte code writes; the four scales of a 64-element chunk
-//                are gathered with shuffles into one 32-bit store in the MMA
-//                scale layout);
-//        V CTAs: two 64-token chunks of one (b, kv head) staged in SMEM, one
-//                thread per (chunk, channel) quantising four 16-token groups.
+// Two launches, 256 threads per CTA.
+//   1. quant_vk_kernel -- two kinds of CTA:
+//        V CTAs:     one thread per (channel pair, 64-token chunk): 64 4-byte
+//                    loads (each warp load is one 128-byte row segment), four
+//                    16-token groups per channel, codes stored transposed;
+//        Kpart CTAs: smooth-K partial sums, one thread per channel pair of one
+//                    128-token chunk, summed token by token from 0 (the
+//                    documented order).  They run last, so K is still in L2
+//                    for launch 2.
+//   2. quant_kq_kernel -- two kinds of CTA:
+//        K CTAs:     one per (b, kv head, 512-token block).  The head's
+//                    partial sums are staged in shared memory (coalesced, all
+//                    loads in flight) and summed in chunk order, then / L: the
+//                    same float operations in the same order in every CTA, so
+//                    mu is bit-exact and identical everywhere; the head's first
+//                    CTA also writes mu.  K - mu is then quantised quad by
+//                    quad, reading K from L2.
+//        Q CTAs:     each thread quantises kQuadsPerThread "quads" (64
+//                    consecutive channels of one row = four 1x16 groups = one
+//                    32-bit word of scale bytes), the next quad's eight
+//                    16-byte loads in flight while the current one is
+//                    computed.  Q streams from HBM while the K CTAs wait on L2.
 
 constexpr int kThreadsQ = 256;
-constexpr int kVChunks = 2;                             // 64-token chunks per V CTA (L % 128 == 0)
+constexpr int kQuadsPerThread = 4;                      // Q quads per thread
+constexpr int kKTokens = 512;                           // tokens per K CTA
+constexpr int kMeanSlice = 32;                          // 128-token chunks staged per pass
 
 struct QuantArgs {
   const __nv_bfloat16* q;
@@ -97,98 +112,110 @@ struct QuantArgs {
   float* part;      // [B*Hkv][L/128][D]
   float* kmean;     // [B*Hkv][D]
   int L, nbh_q, nbh_kv;
-  long long nq_groups, nk_groups;
-  int nblk_k, nblk_q, nblk_v;
+  long long nq_quads;
+  int nblk_q, nblk_v, nblk_kpart, nblk_k_per_head, nblk_k;
 };
 
-// Writes the group's codes and gathers the four scale bytes of its 64-element
-// chunk (four consecutive lanes) into one word in the MMA scale layout.
-template <int D>
-__device__ __forceinline__ void store_row_group(uint8_t* codes_base, uint8_t* sf_base, long long row, int gi,
-                                                int L, uint32_t s8, const uint32_t* codes, bool valid) {
-  uint32_t w = valid ? (s8 << (8 * (gi & 3))) : 0u;
-  w |= __shfl_xor_sync(0xffffffffu, w, 1);
-  w |= __shfl_xor_sync(0xffffffffu, w, 2);
-  if (!valid) return;
-  *reinterpret_cast<uint2*>(codes_base + row * (D / 2) + gi * 8) = make_uint2(codes[0], codes[1]);
-  if ((gi & 3) == 0) {
-    const long long bh = row / L;
-    const int t = (int)(row % L), rb = t / 128, r = t % 128;
-    const long long blk = (bh * (L / 128) + rb) * (D / 64) + gi / 4;
-    *reinterpret_cast<uint32_t*>(sf_base + blk * 512 + (r % 32) * 16 + (r / 32) * 4) = w;
-  }
+// Loads the 64 bf16 values of one quad (eight 16-byte loads, all in flight).
+__device__ __forceinline__ void load_quad(const __nv_bfloat16* src, uint4 (&w)[8]) {
+  const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = __ldg(p + i);
 }
 
-// One group of Q (mean == nullptr) or of K - mean along d.
+// Quantises one quad (minus the 64 means at `mean`, when given) and stores its
+// 32 bytes of codes and its scale word.  `row` is the global row (b*H + h)*L + t,
+// `quad` the 64-channel block within the row.
 template <int D>
-__device__ __forceinline__ void quant_rows_cta(const __nv_bfloat16* src_base, const float* mean, uint8_t* codes_base,
-                                               uint8_t* sf_base, long long ngroups, int L, int blk) {
-  const long long g = (long long)blk * kThreadsQ + threadIdx.x;
-  const bool valid = g < ngroups;
-  const long long row = valid ? g / (D / 16) : 0;
-  const int gi = (int)(g % (D / 16));
-  uint32_t codes[2] = {0u, 0u};
-  uint32_t s8 = 0;
-  if (valid) {
-    float x[16];
-    const uint4* src = reinterpret_cast<const uint4*>(src_base + row * D + gi * 16);
-    bf16x8_to_f32(__ldg(src), x);
-    bf16x8_to_f32(__ldg(src + 1), x + 8);
-    if (mean != nullptr) {
-      const float4* m4 = reinterpret_cast<const float4*>(mean + (row / L) * D + gi * 16);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 m = __ldg(m4 + i);
-        x[4 * i + 0] = __fsub_rn(x[4 * i + 0], m.x);
-        x[4 * i + 1] = __fsub_rn(x[4 * i + 1], m.y);
-        x[4 * i + 2] = __fsub_rn(x[4 * i + 2], m.z);
-        x[4 * i + 3] = __fsub_rn(x[4 * i + 3], m.w);
-      }
-    }
-    s8 = quant_group16(x, codes);
-  }
-  store_row_group<D>(codes_base, sf_base, row, gi, L, s8, codes, valid);
-}
-
-template <int D>
-__device__ __forceinline__ void quant_v_cta(const QuantArgs& a, int blk, __nv_bfloat16* tile) {
-  constexpr int kChunks = kVChunks;
-  const int cpb = a.L / 64;                             // chunks per head (even)
-  const int first = blk * kChunks;                      // global chunk index
-  const int bh = first / cpb, tc0 = first % cpb;
-  const __nv_bfloat16* src = a.v + ((size_t)bh * a.L + (size_t)tc0 * 64) * D;
-  constexpr int kVec = kChunks * 64 * D / 8;
-#pragma unroll
-  for (int i = threadIdx.x; i < kVec; i += kThreadsQ)
-    reinterpret_cast<uint4*>(tile)[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
-  __syncthreads();
-  if (threadIdx.x >= kChunks * D) return;               // d = 64: half the CTA only loads
-  const int ch = threadIdx.x / D, c = threadIdx.x % D;
-  const int tc = tc0 + ch;
+__device__ __forceinline__ void quant_quad(const uint4 (&w)[8], const float* mean, uint8_t* codes_base,
+                                           uint8_t* sf_base, long long row, int quad, int L) {
   uint32_t codes[8];
   uint32_t sfw = 0;
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     float x[16];
+    bf16x8_to_f32(w[2 * g], x);
+    bf16x8_to_f32(w[2 * g + 1], x + 8);
+    if (mean != nullptr) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = __bfloat162float(tile[(ch * 64 + 16 * g + i) * D + c]);
+      for (int i = 0; i < 16; ++i) x[i] = __fsub_rn(x[i], mean[16 * g + i]);
+    }
     sfw |= quant_group16(x, codes + 2 * g) << (8 * g);
   }
-  uint8_t* cdst = a.vc + ((size_t)bh * D + c) * (a.L / 2) + (size_t)tc * 32;
-  reinterpret_cast<uint4*>(cdst)[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-  reinterpret_cast<uint4*>(cdst)[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+  uint4* cdst = reinterpret_cast<uint4*>(codes_base + row * (D / 2) + quad * 32);
+  cdst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+  cdst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+  const long long bh = row / L;
+  const int t = (int)(row % L), rb = t / 128, r = t % 128;
+  const long long blk = (bh * (L / 128) + rb) * (D / 64) + quad;
+  *reinterpret_cast<uint32_t*>(sf_base + blk * 512 + (r % 32) * 16 + (r / 32) * 4) = sfw;
+}
+
+template <int D>
+__device__ __forceinline__ void quant_q_cta(const QuantArgs& a, int blk) {
+  // quads blk*256*kQuadsPerThread + i*256 + tid, i = 0 .. kQuadsPerThread-1
+  long long gq = (long long)blk * kThreadsQ * kQuadsPerThread + threadIdx.x;
+  uint4 w[8];
+  if (gq < a.nq_quads) load_quad(a.q + (gq / (D / 64)) * D + (gq % (D / 64)) * 64, w);
+#pragma unroll 1
+  for (int i = 0; i < kQuadsPerThread && gq < a.nq_quads; ++i, gq += kThreadsQ) {
+    const long long row = gq / (D / 64);
+    const int quad = (int)(gq % (D / 64));
+    uint4 cur[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) cur[k] = w[k];
+    const long long nx = gq + kThreadsQ;
+    if (i + 1 < kQuadsPerThread && nx < a.nq_quads) load_quad(a.q + (nx / (D / 64)) * D + (nx % (D / 64)) * 64, w);
+    quant_quad<D>(cur, nullptr, a.qc, a.qsf, row, quad, a.L);
+  }
+}
+
+// One thread per (channel pair, 64-token chunk).  Items are ordered channel
+// pair fastest, so a warp covers 64 consecutive channels of one chunk and each
+// of its 64 loads reads one 128-byte segment of a V row.
+template <int D>
+__device__ __forceinline__ void quant_v_cta(const QuantArgs& a, int blk) {
+  constexpr int kPairs = D / 2;
+  const long long item = (long long)blk * kThreadsQ + threadIdx.x;
+  const int cpb = a.L / 64;                             // chunks per head
+  if (item >= (long long)a.nbh_kv * cpb * kPairs) return;
+  const int c = 2 * (int)(item % kPairs);
+  const long long chunk = item / kPairs;                // over B*Hkv*cpb
+  const long long bh = chunk / cpb;
+  const int tc = (int)(chunk % cpb);
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(a.v + ((size_t)bh * a.L + (size_t)tc * 64) * D + c);
+  uint32_t w[64];
+#pragma unroll
+  for (int t = 0; t < 64; ++t) w[t] = __ldg(src + (size_t)t * (D / 2));
   uint8_t* sblk = a.vsf + ((size_t)bh * cpb + tc) * 512;
-  *reinterpret_cast<uint32_t*>(sblk + (c % 32) * 16 + (c / 32) * 4) = sfw;
-  if (D == 64) *reinterpret_cast<uint32_t*>(sblk + (c % 32) * 16 + (c / 32 + 2) * 4) = 0u;   // padding rows
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {                         // channel c + h
+    uint32_t codes[8];
+    uint32_t sfw = 0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      float x[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        x[i] = __uint_as_float(h ? (w[16 * g + i] & 0xFFFF0000u) : (w[16 * g + i] << 16));
+      sfw |= quant_group16(x, codes + 2 * g) << (8 * g);
+    }
+    const int ch = c + h;
+    uint8_t* cdst = a.vc + ((size_t)bh * D + ch) * (a.L / 2) + (size_t)tc * 32;
+    reinterpret_cast<uint4*>(cdst)[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+    reinterpret_cast<uint4*>(cdst)[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+    *reinterpret_cast<uint32_t*>(sblk + (ch % 32) * 16 + (ch / 32) * 4) = sfw;
+    if (D == 64) *reinterpret_cast<uint32_t*>(sblk + (ch % 32) * 16 + (ch / 32 + 2) * 4) = 0u;   // padding rows
+  }
 }
 
 // part[bh][chunk][c] = sum over the chunk's 128 tokens, token by token from 0.
 template <int D>
-__global__ void __launch_bounds__(kThreadsQ) kpart_kernel(const QuantArgs a) {
+__device__ __forceinline__ void kpart_cta(const QuantArgs& a, int blk) {
   constexpr int kPairs = D / 2;
   constexpr int kChunksPerCta = kThreadsQ / kPairs;
   const int nchunk = a.L / kMeanChunk;
-  const int gchunk = blockIdx.x * kChunksPerCta + threadIdx.x / kPairs;     // over B*Hkv*nchunk
+  const int gchunk = blk * kChunksPerCta + threadIdx.x / kPairs;     // over B*Hkv*nchunk
   if (gchunk >= a.nbh_kv * nchunk) return;
   const int bh = gchunk / nchunk, chunk = gchunk % nchunk;
   const int c = 2 * (threadIdx.x % kPairs);
@@ -209,38 +236,75 @@ __global__ void __launch_bounds__(kThreadsQ) kpart_kernel(const QuantArgs a) {
   *reinterpret_cast<float2*>(a.part + ((size_t)bh * nchunk + chunk) * D + c) = make_float2(acc0, acc1);
 }
 
-// mean[bh][c] = (partials summed in chunk order) / L; one thread per (bh, c).
 template <int D>
-__global__ void __launch_bounds__(kThreadsQ) kfinal_kernel(const QuantArgs a) {
-  const int i = blockIdx.x * kThreadsQ + threadIdx.x;
-  if (i >= a.nbh_kv * D) return;
-  const int bh = i / D, c = i % D;
+__global__ void __launch_bounds__(kThreadsQ) quant_vk_kernel(const QuantArgs a) {
+  const int blk = blockIdx.x;
+  if (blk < a.nblk_v)
+    quant_v_cta<D>(a, blk);
+  else
+    kpart_cta<D>(a, blk - a.nblk_v);
+}
+
+// mean[c] = (partials summed in chunk order) / L for one (b, kv head), into
+// shared memory; written to k_mean as well when `publish`.
+template <int D>
+__device__ __forceinline__ void head_mean(const QuantArgs& a, int bh, float* mean, float* stage, bool publish) {
   const int nchunk = a.L / kMeanChunk;
-  const float* p = a.part + (size_t)bh * nchunk * D + c;
+  const float* part = a.part + (size_t)bh * nchunk * D;
   float tot = 0.f;
-#pragma unroll 1
-  for (int c0 = 0; c0 < nchunk; c0 += 8) {
-    float v[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = (c0 + j < nchunk) ? p[(size_t)(c0 + j) * D] : 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (c0 + j < nchunk) tot = __fadd_rn(tot, v[j]);
+  for (int c0 = 0; c0 < nchunk; c0 += kMeanSlice) {
+    const int nc = min(kMeanSlice, nchunk - c0);
+    __syncthreads();                                    // previous slice consumed
+    for (int i = threadIdx.x; i < nc * D; i += kThreadsQ) stage[i] = __ldcg(part + (size_t)c0 * D + i);
+    __syncthreads();
+    if (threadIdx.x < D)
+      for (int j = 0; j < nc; ++j) tot = __fadd_rn(tot, stage[j * D + threadIdx.x]);
   }
-  a.kmean[i] = __fdiv_rn(tot, (float)a.L);
+  if (threadIdx.x < D) {
+    const float mu = __fdiv_rn(tot, (float)a.L);
+    mean[threadIdx.x] = mu;
+    if (publish) a.kmean[(size_t)bh * D + threadIdx.x] = mu;
+  }
+  __syncthreads();
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreadsQ) quant_kernel(const QuantArgs a) {
-  __shared__ __align__(16) __nv_bfloat16 tile[kVChunks * 64 * D];
-  const int blk = blockIdx.x;
-  if (blk < a.nblk_k) {
-    quant_rows_cta<D>(a.k, a.kmean, a.kc, a.ksf, a.nk_groups, a.L, blk);
-  } else if (blk < a.nblk_k + a.nblk_q) {
-    quant_rows_cta<D>(a.q, nullptr, a.qc, a.qsf, a.nq_groups, a.L, blk - a.nblk_k);
-  } else {
-    quant_v_cta<D>(a, blk - a.nblk_k - a.nblk_q, tile);
+__device__ __forceinline__ void quant_k_cta(const QuantArgs& a, int blk, float* mean, float* stage) {
+  constexpr int kQuadsPerRow = D / 64;
+  const int bh = blk / a.nblk_k_per_head;
+  const int t0 = (blk % a.nblk_k_per_head) * kKTokens;
+  const int nquads = min(kKTokens, a.L - t0) * kQuadsPerRow;
+  const __nv_bfloat16* kbase = a.k + ((size_t)bh * a.L + t0) * D;
+  // the first quad's loads are in flight while the mean is formed
+  int qi = threadIdx.x;
+  uint4 w[8];
+  if (qi < nquads) load_quad(kbase + (size_t)(qi / kQuadsPerRow) * D + (qi % kQuadsPerRow) * 64, w);
+  head_mean<D>(a, bh, mean, stage, t0 == 0);
+  for (; qi < nquads; qi += kThreadsQ) {
+    const int quad = qi % kQuadsPerRow;
+    const long long row = (long long)bh * a.L + t0 + qi / kQuadsPerRow;
+    uint4 cur[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) cur[k] = w[k];
+    const int nx = qi + kThreadsQ;
+    if (nx < nquads) load_quad(kbase + (size_t)(nx / kQuadsPerRow) * D + (nx % kQuadsPerRow) * 64, w);
+    quant_quad<D>(cur, mean + quad * 64, a.kc, a.ksf, row, quad, a.L);
   }
+}
+
+// K and Q CTAs are interleaved in proportion (K block i sits near position
+// i * total / nK), so the L2-bound K work and the HBM-bound Q stream run side
+// by side from the start.
+template <int D>
+__global__ void __launch_bounds__(kThreadsQ) quant_kq_kernel(const QuantArgs a) {
+  __shared__ __align__(16) float mean[D];
+  __shared__ __align__(16) float stage[kMeanSlice * D];
+  const long long blk = blockIdx.x, total = (long long)a.nblk_k + a.nblk_q;
+  const long long k_before = blk * a.nblk_k / total, k_through = (blk + 1) * a.nblk_k / total;
+  if (k_through > k_before)
+    quant_k_cta<D>(a, (int)k_before, mean, stage);
+  else
+    quant_q_cta<D>(a, (int)(blk - k_before));
 }
 
 template <int D>
@@ -261,16 +325,16 @@ cudaError_t launch_quantize_impl(const void* q, const void* k, const void* v, co
   a.L = dm.L;
   a.nbh_q = dm.B * dm.H;
   a.nbh_kv = dm.B * dm.Hkv;
-  a.nq_groups = (long long)a.nbh_q * dm.L * (D / 16);
-  a.nk_groups = (long long)a.nbh_kv * dm.L * (D / 16);
-  a.nblk_q = (int)((a.nq_groups + kThreadsQ - 1) / kThreadsQ);
-  a.nblk_k = (int)((a.nk_groups + kThreadsQ - 1) / kThreadsQ);
-  a.nblk_v = a.nbh_kv * (dm.L / 64) / kVChunks;
+  a.nq_quads = (long long)a.nbh_q * dm.L * (D / 64);
+  a.nblk_q = (int)((a.nq_quads + kThreadsQ * kQuadsPerThread - 1) / (kThreadsQ * kQuadsPerThread));
+  a.nblk_v = (int)(((long long)a.nbh_kv * (dm.L / 64) * (D / 2) + kThreadsQ - 1) / kThreadsQ);
   const int kchunks = a.nbh_kv * (dm.L / kMeanChunk);
   const int kcpb = kThreadsQ / (D / 2);
-  kpart_kernel<D><<<(kchunks + kcpb - 1) / kcpb, kThreadsQ, 0, s>>>(a);
-  kfinal_kernel<D><<<(a.nbh_kv * D + kThreadsQ - 1) / kThreadsQ, kThreadsQ, 0, s>>>(a);
-  quant_kernel<D><<<a.nblk_k + a.nblk_q + a.nblk_v, kThreadsQ, 0, s>>>(a);
+  a.nblk_kpart = (kchunks + kcpb - 1) / kcpb;
+  a.nblk_k_per_head = (dm.L + kKTokens - 1) / kKTokens;
+  a.nblk_k = a.nbh_kv * a.nblk_k_per_head;
+  quant_vk_kernel<D><<<a.nblk_v + a.nblk_kpart, kThreadsQ, 0, s>>>(a);
+  quant_kq_kernel<D><<<a.nblk_k + a.nblk_q, kThreadsQ, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -323,9 +387,9 @@ cudaError_t launch_quantize_static_scratch(const void* q, const void* k, const v
   float* part = nullptr;
   cudaError_t e = static_scratch_address(&part);
   if (e != cudaSuccess) return e;
-  // Every partial sum read is written first by the same call (the K CTAs of
-  // the first launch), so earlier contents of the array never reach the
-  // outputs and nothing needs clearing.
+  // Every partial sum read is written first by the same call (the partial-sum
+  // CTAs of its first launch), so earlier contents of the array never reach
+  // the outputs and nothing needs clearing.
   return dm.d == 64 ? launch_quantize_impl<64>(q, k, v, dm, out, part, s)
                     : launch_quantize_impl<128>(q, k, v, dm, out, part, s);
 }
