@@ -151,6 +151,7 @@ def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
     import quantized_attention_x16_gb300 as sa
+    from quantized_attention_x16_gb300 import shard
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -200,10 +201,8 @@ def run_ours(args, rank, world, local_rank):
     mean = lambda xs: sum(xs) / len(xs)   # noqa: E731
     t_q, t_4, t_16 = mean(tq), mean(t4), mean(t16)
     t_path = t_q + t_4
-    if world > 1:
-        tt = torch.tensor([t_path, t_q, t_4, t_16], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_path, t_q, t_4, t_16 = tt.tolist()
+    # the slowest rank sets each time (no-ops at N = 1)
+    t_path, t_q, t_4, t_16 = (shard.max_over_ranks(t, device=dev) for t in (t_path, t_q, t_4, t_16))
     assert sa.sa_last_device_error() == sa.SA_OK
 
     # ---- end to end through the public API with host buffers (same metric)
@@ -230,11 +229,7 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
     e1.record()
     torch.cuda.synchronize()
-    t_e2e = e0.elapsed_time(e1) * 1e-3 / args.steps
-    if world > 1:
-        tt = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = tt.item()
+    t_e2e = shard.max_over_ranks(e0.elapsed_time(e1) * 1e-3 / args.steps, device=dev)
 
     if rank != 0:
         return
