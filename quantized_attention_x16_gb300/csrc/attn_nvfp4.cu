@@ -38,6 +38,7 @@
 
 #include "internal.h"
 #include "sm100.cuh"
+#include "work.cuh"
 
 namespace sa {
 namespace {
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const uint8_t* __restrict__ q_sf,
                       const uint8_t* __restrict__ k_sf, const uint8_t* __restrict__ v_sf,
-                      void* __restrict__ out_ptr, int H, int Hkv, int L, int causal, uint64_t wait_ns) {
+                      void* __restrict__ out_ptr, int H, int Hkv, int L, int causal, const AttnWork work, uint64_t wait_ns) {
   using C = CfgF4<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -143,13 +144,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int nqt = L / BM;
-  const int nblk = (nqt + 1) / 2;
-  const int blk = causal ? (nblk - 1 - (int)blockIdx.x) : (int)blockIdx.x;
-  const int h = blockIdx.y, b = blockIdx.z;
+  int bh, qt0, nqu;
+  attn_unit(work, (int)blockIdx.x, bh, qt0, nqu);                  // this CTA's query tiles
+  const int h = bh % H, b = bh / H;
   const int hk = h / (H / Hkv);
-  const int qt0 = 2 * blk;
-  const bool q1_valid = (qt0 + 1) < nqt;
+  const bool q1_valid = nqu == 2;
   int ntq[2];
   ntq[0] = causal ? qt0 + 1 : L / BN;
   ntq[1] = q1_valid ? (causal ? qt0 + 2 : L / BN) : 0;
@@ -520,10 +519,11 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  dim3 grid((dm.L / BM + 1) / 2, dm.H, dm.B);
-  attn_nvfp4_kernel<D, OUT32><<<grid, kThreads, C::kSmemBytes, s>>>(
+  int ctas = 0;
+  const AttnWork work = make_attn_work(dm.B, dm.H, dm.L, causal, device_sm_count(), &ctas);
+  attn_nvfp4_kernel<D, OUT32><<<ctas, kThreads, C::kSmemBytes, s>>>(
       tq, tk, tv, static_cast<const uint8_t*>(x.q_sf), static_cast<const uint8_t*>(x.k_sf),
-      static_cast<const uint8_t*>(x.v_sf), o, dm.H, dm.Hkv, dm.L, causal, kWaitLimitNs);
+      static_cast<const uint8_t*>(x.v_sf), o, dm.H, dm.Hkv, dm.L, causal, work, kWaitLimitNs);
   return cudaGetLastError();
 }
 

@@ -13,6 +13,18 @@ struct Dims {
   int B, H, Hkv, L, d;
 };
 
+// Number of SMs of the current device (cached per device; 0 if unknown).
+inline int device_sm_count() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
 // Barrier-wait limit used by the attention kernels (nanoseconds).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
