@@ -13,9 +13,11 @@
 //                per row)
 //   warps 4-7  : the same for query tile 1
 //   warp 8     : TMA producer (Q once, then K/V tiles into an NS-stage ring)
-//   warp 9     : MMA issuer (one thread; descriptors built once, a use adds
-//                its byte offset to the start-address field)
-//   warps 10-11: idle
+//   warp 9     : S MMA issuer, warp 10: P.V MMA issuer (each runs its loop
+//                with all lanes and issues from one elected lane; operand
+//                descriptors are built once, a use adds its byte offset to
+//                the start-address field)
+//   warp 11    : idle
 // Tensor memory (512 columns): S (one 128-column region shared by the two
 // query tiles), O0, O1 (d columns each), P0, P1 (64 columns each, bf16
 // pairs).  S = Q K^T is read into registers, P = 2^(x - m) is written back as
@@ -36,8 +38,8 @@ constexpr int BM = 128;         // query rows per tile
 constexpr int BN = 128;         // keys per KV tile
 constexpr int kThreads = 384;
 constexpr uint32_t kProducerSleepNs = 256;   // poll interval of the TMA producer's waits
-constexpr int kSoftmaxRegs = 216;   // 8 softmax warps
-constexpr int kOtherRegs = 72;      // producer / MMA warpgroup
+constexpr int kSoftmaxRegs = 200;   // 8 softmax warps
+constexpr int kOtherRegs = 104;      // producer / MMA warpgroup
 constexpr int kLaunchRegs = 168;    // 65536 / 384 rounded down to a multiple of 8
 static_assert(8 * 32 * kSoftmaxRegs + 4 * 32 * kOtherRegs <= kThreads * kLaunchRegs, "register split");
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -51,7 +53,7 @@ struct CfgBF16 {
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + NS * kTileBytes;
   static constexpr int kOffBar = kOffV + NS * kTileBytes;
-  static constexpr int kNumBars = 1 + 4 * NS + 8 + 1;
+  static constexpr int kNumBars = 1 + 4 * NS + 8 + 2;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;   // + alignment slack
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColO0 = 128;
@@ -187,73 +189,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else if (warp == 9) {
-      // ---------------------------------------------------------- MMA issuer
+      // ---------------------------------------------------------- S issuer
+      // S0(0), S1(0), S0(1), S1(1), ... into the one S region; each waits
+      // until the softmax warps have read the previous S.
       const bool leader = elect_one();
       const uint64_t dQ = sdesc(smem_u32(smem + C::kOffQ), 16, 1024, kSwizzle128B);
       const uint64_t dK = sdesc(smem_u32(smem + C::kOffK), 16, 1024, kSwizzle128B);
-      const uint64_t dV = sdesc(smem_u32(smem + C::kOffV), C::kHalfBytes, 1024, kSwizzle128B);
       const uint32_t tS = tbase + C::kColS;
       int last_q = -1, last_j = 0;
       bool ok = mbar_wait_warp(bars.q_full, 0, abort_flag, wait_ns);
-      auto issue_s = [&](int q, int j) -> bool {
-        if (last_q >= 0 && !mbar_wait_warp(bars.s_free + last_q, last_j & 1, abort_flag, wait_ns)) return false;
-        tc_fence_after();
-        const uint32_t s = j % C::NS;
-        const uint64_t a0 = dadd(dQ, q * C::kTileBytes), b0 = dadd(dK, s * C::kTileBytes);
-        if (leader) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
-            mma_bf16_ss(tS, dadd(a0, off), dadd(b0, off), C::kIdescS, kk > 0 ? 1u : 0u);
-          }
-          tc_commit(bars.s_full + q);
-        }
-        __syncwarp();
-        last_q = q;
-        last_j = j;
-        return true;
-      };
-      auto issue_pv = [&](int q, int j) -> bool {
-        if (!mbar_wait_warp(bars.p_full + q, j & 1, abort_flag, wait_ns)) return false;
-        tc_fence_after();
-        const uint32_t s = j % C::NS;
-        const uint64_t b0 = dadd(dV, s * C::kTileBytes);
-        const uint32_t tO = tbase + C::kColO0 + q * D, tP = tbase + C::kColP0 + q * 64;
-        if (leader) {
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_bf16_ts(tO, tP + kk * 8, dadd(b0, kk * 16 * 128), C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(bars.o_done + q);
-        }
-        __syncwarp();
-        return true;
-      };
-      if (ok) {
-        ok = mbar_wait_warp(bars.k_full, 0, abort_flag, wait_ns);
-        tc_fence_after();
-        if (ok && ntq[0] > 0) ok = issue_s(0, 0);
-        if (ok && ntq[1] > 0) ok = issue_s(1, 0);
-        if (ok && leader) tc_commit(bars.k_empty);
-        __syncwarp();
-      }
       for (int j = 0; ok && j < nt; ++j) {
         const int s = j % C::NS;
-        const int s1 = (j + 1) % C::NS;
-        if (j + 1 < nt) {
-          ok = mbar_wait_warp(bars.k_full + s1, ((j + 1) / C::NS) & 1, abort_flag, wait_ns);
+        ok = mbar_wait_warp(bars.k_full + s, (j / C::NS) & 1, abort_flag, wait_ns);
+        if (!ok) break;
+        for (int q = 0; ok && q < 2; ++q) {
+          if (j >= ntq[q]) continue;
+          if (last_q >= 0) ok = mbar_wait_warp(bars.s_free + last_q, last_j & 1, abort_flag, wait_ns);
+          if (!ok) break;
           tc_fence_after();
-          if (ok && j + 1 < ntq[0]) ok = issue_s(0, j + 1);
-        }
-        if (ok) ok = mbar_wait_warp(bars.v_full + s, (j / C::NS) & 1, abort_flag, wait_ns);
-        tc_fence_after();
-        if (ok && j < ntq[0]) ok = issue_pv(0, j);
-        if (ok && j + 1 < nt) {
-          if (j + 1 < ntq[1]) ok = issue_s(1, j + 1);
-          if (ok && leader) tc_commit(bars.k_empty + s1);
+          const uint64_t a0 = dadd(dQ, q * C::kTileBytes), b0 = dadd(dK, s * C::kTileBytes);
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
+              mma_bf16_ss(tS, dadd(a0, off), dadd(b0, off), C::kIdescS, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(bars.s_full + q);
+          }
           __syncwarp();
+          last_q = q;
+          last_j = j;
         }
-        if (ok && j < ntq[1]) ok = issue_pv(1, j);
-        if (ok && leader) tc_commit(bars.v_empty + s);
+        if (ok && leader) tc_commit(bars.k_empty + s);      // K slot free once these S MMAs are done
         __syncwarp();
       }
       if (!ok) {
@@ -261,6 +228,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) tc_commit(bars.drain);
         __syncwarp();
         mbar_wait_drain(bars.drain, 0, wait_ns);
+      }
+    } else if (warp == 10) {
+      // ---------------------------------------------------------- P.V issuer
+      // P0.V(j), P1.V(j), ... each once its softmax warps have stored P.
+      const bool leader = elect_one();
+      const uint64_t dV = sdesc(smem_u32(smem + C::kOffV), C::kHalfBytes, 1024, kSwizzle128B);
+      bool ok = true;
+      for (int j = 0; ok && j < nt; ++j) {
+        const int s = j % C::NS;
+        ok = mbar_wait_warp(bars.v_full + s, (j / C::NS) & 1, abort_flag, wait_ns);
+        if (!ok) break;
+        for (int q = 0; ok && q < 2; ++q) {
+          if (j >= ntq[q]) continue;
+          ok = mbar_wait_warp(bars.p_full + q, j & 1, abort_flag, wait_ns);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t b0 = dadd(dV, s * C::kTileBytes);
+          const uint32_t tO = tbase + C::kColO0 + q * D, tP = tbase + C::kColP0 + q * 64;
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_bf16_ts(tO, tP + kk * 8, dadd(b0, kk * 16 * 128), C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(bars.o_done + q);
+          }
+          __syncwarp();
+        }
+        if (ok && leader) tc_commit(bars.v_empty + s);      // V slot free once these P.V MMAs are done
+        __syncwarp();
+      }
+      if (!ok) {
+        if (leader) tc_commit(bars.drain + 1);
+        __syncwarp();
+        mbar_wait_drain(bars.drain + 1, 0, wait_ns);
       }
     }
   } else {

@@ -28,9 +28,9 @@
 //
 // CTA layout (384 threads): warps 0-3 / 4-7 own query tiles 0 / 1 (one thread
 // per row: softmax, P quantisation, O correction, epilogue); warp 8 issues TMA
-// and bulk copies; warp 9 issues MMAs and scale-factor copies (both warps run
-// their loops with all lanes and issue from one elected lane);
-// warps 10-11 idle.  Tensor memory: S (128 columns, shared by both query
+// and bulk copies; warp 9 issues the S MMAs and warp 10 the P.V MMAs, each
+// with the scale-factor copies they need (the three warps run their loops with
+// all lanes and issue from one elected lane); warp 11 idles.  Tensor memory: S (128 columns, shared by both query
 // tiles), O0, O1 (d columns each), then scale factors (4 columns per 64-deep K
 // chunk, copied from SMEM with tcgen05.cp, replicated to the four lane quarters).
 
@@ -75,7 +75,7 @@ struct CfgF4 {
   static constexpr int kOffVSf = kOffKSf + NS * kKSfBytes;
   static constexpr int kOffPSf = kOffVSf + NS * kVSfBytes;
   static constexpr int kOffBar = kOffPSf + 2 * kPSfBytes;
-  static constexpr int kNumBars = 1 + 4 * NS + 8 + 1;
+  static constexpr int kNumBars = 1 + 4 * NS + 8 + 2;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   // Q/K rows of 64 bytes use the 64B swizzle, rows of 32 bytes the 32B one.
   static constexpr uint32_t kQKSwz = (D == 128) ? kSwizzle64B : kSwizzle32B;
@@ -234,49 +234,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else if (warp == 9) {
-      // ---------------------------------------------------------- MMA issuer
+      // ---------------------------------------------------------- S issuer
+      // S0(0), S1(0), S0(1), S1(1), ... into the one S region; each waits
+      // until the softmax warps have read the previous S.  A tile's K scales
+      // go to the buffer of its parity; the buffer was last read by the S
+      // MMAs of tile j-2, complete once the S before S(j-1) has been read.
       const bool leader = elect_one();
       const uint32_t sb = smem_u32(smem);
       const uint32_t tS = tbase + C::kColS;
       int last_q = -1, last_j = 0;
-      auto issue_s = [&](int q, int j) -> bool {
-        if (last_q >= 0 && !mbar_wait_warp(bars.s_free + last_q, last_j & 1, abort_flag, wait_ns)) return false;
-        tc_fence_after();
-        const uint32_t s = j % C::NS;
-        const uint32_t sfq = tbase + (q ? C::kColSfQ1 : C::kColSfQ0);
-        const uint32_t sfk = tbase + C::kColSfK + 8 * (j & 1);
-        if (leader) {
-#pragma unroll
-          for (int kk = 0; kk < D / 64; ++kk)
-            mma_nvf4(tS, desc_qk(sb + C::kOffQ + q * C::kQBytes + kk * 32, C::kQKSbo, C::kQKSwz),
-                     desc_qk(sb + C::kOffK + s * C::kKBytes + kk * 32, C::kQKSbo, C::kQKSwz), C::kIdescS,
-                     sfq + 4 * kk, sfk + 4 * kk, kk > 0 ? 1u : 0u);
-          tc_commit(bars.s_full + q);
-        }
-        __syncwarp();
-        last_q = q;
-        last_j = j;
-        return true;
-      };
-      auto issue_pv = [&](int q, int j) -> bool {
-        if (!mbar_wait_warp(bars.p_full + q, j & 1, abort_flag, wait_ns)) return false;
-        tc_fence_after();
-        const uint32_t s = j % C::NS;
-        const uint32_t sfp = tbase + (q ? C::kColSfP1 : C::kColSfP0);
-        const uint32_t tO = tbase + C::kColO0 + q * D;
-        const uint32_t sfv = tbase + C::kColSfV + 8 * (j & 1);
-        if (leader) {
-          copy_sf(sfp, sb + C::kOffPSf + q * C::kPSfBytes, 2);
-#pragma unroll
-          for (int kk = 0; kk < BN / 64; ++kk)
-            mma_nvf4(tO, desc_qk(sb + C::kOffP + q * C::kPBytes + kk * 32, 512, kSwizzle64B),
-                     desc_qk(sb + C::kOffV + s * C::kVBytes + kk * 32, 512, kSwizzle64B), C::kIdescPV, sfp + 4 * kk,
-                     sfv + 4 * kk, (j > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(bars.o_done + q);
-        }
-        __syncwarp();
-        return true;
-      };
       bool ok = mbar_wait_warp(bars.q_full, 0, abort_flag, wait_ns);
       if (ok) {
         tc_fence_after();
@@ -285,50 +251,83 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (q1_valid) copy_sf(tbase + C::kColSfQ1, sb + C::kOffQSf + C::kQSfBytes, D / 64);
         }
         __syncwarp();
-        ok = mbar_wait_warp(bars.k_full, 0, abort_flag, wait_ns);
-      }
-      if (ok) {
-        tc_fence_after();
-        if (leader) copy_sf(tbase + C::kColSfK, sb + C::kOffKSf, D / 64);      // tile 0: parity 0
-        __syncwarp();
-        if (ntq[0] > 0) ok = issue_s(0, 0);
-        if (ok && ntq[1] > 0) ok = issue_s(1, 0);
-        if (ok && leader) tc_commit(bars.k_empty);
-        __syncwarp();
       }
       for (int j = 0; ok && j < nt; ++j) {
         const int s = j % C::NS;
-        const int s1 = (j + 1) % C::NS;
-        if (j + 1 < nt) {
-          ok = mbar_wait_warp(bars.k_full + s1, ((j + 1) / C::NS) & 1, abort_flag, wait_ns);
-          if (ok) {
-            tc_fence_after();
-            if (leader)
-              copy_sf(tbase + C::kColSfK + 8 * ((j + 1) & 1), sb + C::kOffKSf + s1 * C::kKSfBytes, D / 64);
-            __syncwarp();
-            if (j + 1 < ntq[0]) ok = issue_s(0, j + 1);
-          }
-        }
-        if (ok) ok = mbar_wait_warp(bars.v_full + s, (j / C::NS) & 1, abort_flag, wait_ns);
-        if (ok) {
+        ok = mbar_wait_warp(bars.k_full + s, (j / C::NS) & 1, abort_flag, wait_ns);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sfk = tbase + C::kColSfK + 8 * (j & 1);
+        if (leader) copy_sf(sfk, sb + C::kOffKSf + s * C::kKSfBytes, D / 64);
+        __syncwarp();
+        for (int q = 0; ok && q < 2; ++q) {
+          if (j >= ntq[q]) continue;
+          if (last_q >= 0) ok = mbar_wait_warp(bars.s_free + last_q, last_j & 1, abort_flag, wait_ns);
+          if (!ok) break;
           tc_fence_after();
-          if (leader) copy_sf(tbase + C::kColSfV + 8 * (j & 1), sb + C::kOffVSf + s * C::kVSfBytes, 2);
+          const uint32_t sfq = tbase + (q ? C::kColSfQ1 : C::kColSfQ0);
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < D / 64; ++kk)
+              mma_nvf4(tS, desc_qk(sb + C::kOffQ + q * C::kQBytes + kk * 32, C::kQKSbo, C::kQKSwz),
+                       desc_qk(sb + C::kOffK + s * C::kKBytes + kk * 32, C::kQKSbo, C::kQKSwz), C::kIdescS,
+                       sfq + 4 * kk, sfk + 4 * kk, kk > 0 ? 1u : 0u);
+            tc_commit(bars.s_full + q);
+          }
           __syncwarp();
-          if (j < ntq[0]) ok = issue_pv(0, j);
+          last_q = q;
+          last_j = j;
         }
-        if (ok && j + 1 < nt) {
-          if (j + 1 < ntq[1]) ok = issue_s(1, j + 1);
-          if (ok && leader) tc_commit(bars.k_empty + s1);
-          __syncwarp();
-        }
-        if (ok && j < ntq[1]) ok = issue_pv(1, j);
-        if (ok && leader) tc_commit(bars.v_empty + s);
+        if (ok && leader) tc_commit(bars.k_empty + s);      // K slot free once these S MMAs are done
         __syncwarp();
       }
       if (!ok) {
         if (leader) tc_commit(bars.drain);
         __syncwarp();
         mbar_wait_drain(bars.drain, 0, wait_ns);
+      }
+    } else if (warp == 10) {
+      // ---------------------------------------------------------- P.V issuer
+      // P0.V(j), P1.V(j), ... each once its softmax warps have written P^.
+      // V scales of tile j go to the buffer of its parity, last read by the
+      // P.V MMAs of tile j-2, which the softmax warps have seen complete
+      // before releasing P^(j-1).
+      const bool leader = elect_one();
+      const uint32_t sb = smem_u32(smem);
+      bool ok = true;
+      for (int j = 0; ok && j < nt; ++j) {
+        const int s = j % C::NS;
+        ok = mbar_wait_warp(bars.v_full + s, (j / C::NS) & 1, abort_flag, wait_ns);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sfv = tbase + C::kColSfV + 8 * (j & 1);
+        if (leader) copy_sf(sfv, sb + C::kOffVSf + s * C::kVSfBytes, 2);
+        __syncwarp();
+        for (int q = 0; ok && q < 2; ++q) {
+          if (j >= ntq[q]) continue;
+          ok = mbar_wait_warp(bars.p_full + q, j & 1, abort_flag, wait_ns);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sfp = tbase + (q ? C::kColSfP1 : C::kColSfP0);
+          const uint32_t tO = tbase + C::kColO0 + q * D;
+          if (leader) {
+            copy_sf(sfp, sb + C::kOffPSf + q * C::kPSfBytes, 2);
+#pragma unroll
+            for (int kk = 0; kk < BN / 64; ++kk)
+              mma_nvf4(tO, desc_qk(sb + C::kOffP + q * C::kPBytes + kk * 32, 512, kSwizzle64B),
+                       desc_qk(sb + C::kOffV + s * C::kVBytes + kk * 32, 512, kSwizzle64B), C::kIdescPV,
+                       sfp + 4 * kk, sfv + 4 * kk, (j > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(bars.o_done + q);
+          }
+          __syncwarp();
+        }
+        if (ok && leader) tc_commit(bars.v_empty + s);      // V slot free once these P.V MMAs are done
+        __syncwarp();
+      }
+      if (!ok) {
+        if (leader) tc_commit(bars.drain + 1);
+        __syncwarp();
+        mbar_wait_drain(bars.drain + 1, 0, wait_ns);
       }
     }
   } else {
