@@ -78,8 +78,8 @@ __device__ __forceinline__ uint32_t quant_group16(const float* x, uint32_t* code
 // ---------------------------------------------------------------------------
 // Two launches, 256 threads per CTA.
 //   1. quant_vk_kernel -- two kinds of CTA:
-//        V CTAs:     one thread per (channel pair, 64-token chunk): 64 4-byte
-//                    loads (each warp load is one 128-byte row segment), four
+//        V CTAs:     one thread per (channel pair, 32 tokens): 32 4-byte loads
+//                    (each warp load is one 128-byte row segment), two
 //                    16-token groups per channel, codes stored transposed;
 //        Kpart CTAs: smooth-K partial sums, one thread per channel pair of one
 //                    128-token chunk, summed token by token from 0 (the
@@ -100,7 +100,7 @@ __device__ __forceinline__ uint32_t quant_group16(const float* x, uint32_t* code
 //                    computed.  Q streams from HBM while the K CTAs wait on L2.
 
 constexpr int kThreadsQ = 256;
-constexpr int kQuadsPerThread = 4;                      // Q quads per thread
+constexpr int kQuadsPerThread = 1;                      // Q quads per thread
 constexpr int kKTokens = 512;                           // tokens per K CTA
 constexpr int kMeanSlice = 32;                          // 128-token chunks staged per pass
 
@@ -170,30 +170,31 @@ __device__ __forceinline__ void quant_q_cta(const QuantArgs& a, int blk) {
   }
 }
 
-// One thread per (channel pair, 64-token chunk).  Items are ordered channel
-// pair fastest, so a warp covers 64 consecutive channels of one chunk and each
-// of its 64 loads reads one 128-byte segment of a V row.
+// One thread per (channel pair, 32 tokens = two 16-token groups).  Items are
+// ordered channel pair fastest, so a warp covers 64 consecutive channels of
+// the same 32 tokens and each of its 32 loads reads one 128-byte segment of a
+// V row.  A channel's two scale bytes are one half of its 64-token scale word.
 template <int D>
 __device__ __forceinline__ void quant_v_cta(const QuantArgs& a, int blk) {
   constexpr int kPairs = D / 2;
   const long long item = (long long)blk * kThreadsQ + threadIdx.x;
-  const int cpb = a.L / 64;                             // chunks per head
-  if (item >= (long long)a.nbh_kv * cpb * kPairs) return;
+  const int npb = a.L / 32;                             // 32-token pieces per head
+  if (item >= (long long)a.nbh_kv * npb * kPairs) return;
   const int c = 2 * (int)(item % kPairs);
-  const long long chunk = item / kPairs;                // over B*Hkv*cpb
-  const long long bh = chunk / cpb;
-  const int tc = (int)(chunk % cpb);
-  const uint32_t* src = reinterpret_cast<const uint32_t*>(a.v + ((size_t)bh * a.L + (size_t)tc * 64) * D + c);
-  uint32_t w[64];
+  const long long piece = item / kPairs;                // over B*Hkv*npb
+  const long long bh = piece / npb;
+  const int tp = (int)(piece % npb);
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(a.v + ((size_t)bh * a.L + (size_t)tp * 32) * D + c);
+  uint32_t w[32];
 #pragma unroll
-  for (int t = 0; t < 64; ++t) w[t] = __ldg(src + (size_t)t * (D / 2));
-  uint8_t* sblk = a.vsf + ((size_t)bh * cpb + tc) * 512;
+  for (int t = 0; t < 32; ++t) w[t] = __ldg(src + (size_t)t * (D / 2));
+  uint8_t* sblk = a.vsf + ((size_t)bh * (a.L / 64) + tp / 2) * 512 + (tp % 2) * 2;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {                         // channel c + h
-    uint32_t codes[8];
+    uint32_t codes[4];
     uint32_t sfw = 0;
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < 2; ++g) {
       float x[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i)
@@ -201,11 +202,10 @@ __device__ __forceinline__ void quant_v_cta(const QuantArgs& a, int blk) {
       sfw |= quant_group16(x, codes + 2 * g) << (8 * g);
     }
     const int ch = c + h;
-    uint8_t* cdst = a.vc + ((size_t)bh * D + ch) * (a.L / 2) + (size_t)tc * 32;
-    reinterpret_cast<uint4*>(cdst)[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-    reinterpret_cast<uint4*>(cdst)[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-    *reinterpret_cast<uint32_t*>(sblk + (ch % 32) * 16 + (ch / 32) * 4) = sfw;
-    if (D == 64) *reinterpret_cast<uint32_t*>(sblk + (ch % 32) * 16 + (ch / 32 + 2) * 4) = 0u;   // padding rows
+    *reinterpret_cast<uint4*>(a.vc + ((size_t)bh * D + ch) * (a.L / 2) + (size_t)tp * 16) =
+        make_uint4(codes[0], codes[1], codes[2], codes[3]);
+    *reinterpret_cast<uint16_t*>(sblk + (ch % 32) * 16 + (ch / 32) * 4) = (uint16_t)sfw;
+    if (D == 64) *reinterpret_cast<uint16_t*>(sblk + (ch % 32) * 16 + (ch / 32 + 2) * 4) = 0;   // padding rows
   }
 }
 
@@ -237,12 +237,14 @@ __device__ __forceinline__ void kpart_cta(const QuantArgs& a, int blk) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreadsQ) quant_vk_kernel(const QuantArgs a) {
+__global__ void __launch_bounds__(kThreadsQ, 3) quant_vk_kernel(const QuantArgs a) {
   const int blk = blockIdx.x;
-  if (blk < a.nblk_v)
-    quant_v_cta<D>(a, blk);
+  if (blk < a.nblk_q)
+    quant_q_cta<D>(a, blk);
+  else if (blk < a.nblk_q + a.nblk_v)
+    quant_v_cta<D>(a, blk - a.nblk_q);
   else
-    kpart_cta<D>(a, blk - a.nblk_v);
+    kpart_cta<D>(a, blk - a.nblk_q - a.nblk_v);
 }
 
 // mean[c] = (partials summed in chunk order) / L for one (b, kv head), into
@@ -255,7 +257,16 @@ __device__ __forceinline__ void head_mean(const QuantArgs& a, int bh, float* mea
   for (int c0 = 0; c0 < nchunk; c0 += kMeanSlice) {
     const int nc = min(kMeanSlice, nchunk - c0);
     __syncthreads();                                    // previous slice consumed
-    for (int i = threadIdx.x; i < nc * D; i += kThreadsQ) stage[i] = __ldcg(part + (size_t)c0 * D + i);
+    // all of this thread's loads are issued before the first store
+    constexpr int kPer = kMeanSlice * D / kThreadsQ;
+    float v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = threadIdx.x + k * kThreadsQ;
+      v[k] = i < nc * D ? __ldcg(part + (size_t)c0 * D + i) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) stage[threadIdx.x + k * kThreadsQ] = v[k];
     __syncthreads();
     if (threadIdx.x < D)
       for (int j = 0; j < nc; ++j) tot = __fadd_rn(tot, stage[j * D + threadIdx.x]);
@@ -292,19 +303,11 @@ __device__ __forceinline__ void quant_k_cta(const QuantArgs& a, int blk, float* 
   }
 }
 
-// K and Q CTAs are interleaved in proportion (K block i sits near position
-// i * total / nK), so the L2-bound K work and the HBM-bound Q stream run side
-// by side from the start.
 template <int D>
 __global__ void __launch_bounds__(kThreadsQ) quant_kq_kernel(const QuantArgs a) {
   __shared__ __align__(16) float mean[D];
   __shared__ __align__(16) float stage[kMeanSlice * D];
-  const long long blk = blockIdx.x, total = (long long)a.nblk_k + a.nblk_q;
-  const long long k_before = blk * a.nblk_k / total, k_through = (blk + 1) * a.nblk_k / total;
-  if (k_through > k_before)
-    quant_k_cta<D>(a, (int)k_before, mean, stage);
-  else
-    quant_q_cta<D>(a, (int)(blk - k_before));
+  quant_k_cta<D>(a, (int)blockIdx.x, mean, stage);
 }
 
 template <int D>
@@ -327,14 +330,14 @@ cudaError_t launch_quantize_impl(const void* q, const void* k, const void* v, co
   a.nbh_kv = dm.B * dm.Hkv;
   a.nq_quads = (long long)a.nbh_q * dm.L * (D / 64);
   a.nblk_q = (int)((a.nq_quads + kThreadsQ * kQuadsPerThread - 1) / (kThreadsQ * kQuadsPerThread));
-  a.nblk_v = (int)(((long long)a.nbh_kv * (dm.L / 64) * (D / 2) + kThreadsQ - 1) / kThreadsQ);
+  a.nblk_v = (int)(((long long)a.nbh_kv * (dm.L / 32) * (D / 2) + kThreadsQ - 1) / kThreadsQ);
   const int kchunks = a.nbh_kv * (dm.L / kMeanChunk);
   const int kcpb = kThreadsQ / (D / 2);
   a.nblk_kpart = (kchunks + kcpb - 1) / kcpb;
   a.nblk_k_per_head = (dm.L + kKTokens - 1) / kKTokens;
   a.nblk_k = a.nbh_kv * a.nblk_k_per_head;
-  quant_vk_kernel<D><<<a.nblk_v + a.nblk_kpart, kThreadsQ, 0, s>>>(a);
-  quant_kq_kernel<D><<<a.nblk_k + a.nblk_q, kThreadsQ, 0, s>>>(a);
+  quant_vk_kernel<D><<<a.nblk_q + a.nblk_v + a.nblk_kpart, kThreadsQ, 0, s>>>(a);
+  quant_kq_kernel<D><<<a.nblk_k, kThreadsQ, 0, s>>>(a);
   return cudaGetLastError();
 }
 
