@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = fmaxf(m_run, m_t);
       const bool live = (m_t > -INFINITY) && (m_t >= m_new - kSkipBelow);
       m_run = m_new;
-      uint32_t codes[16];
+      uint32_t codes[4];
       uint32_t sfw[2] = {0u, 0u};
       const float corr = (live && have_ref) ? ex2_approx(m_ref - m_t) : 1.f;
       // O is rescaled to the new tile maximum in 16-column chunks interleaved
@@ -433,8 +433,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             add2(u[0], u[1], u[0], u[1], p[i], p[i + 1]);
           }
           rs = fmaf(u[0] + u[1], fg[g], rs);
-          codes[2 * g] = cvt_e2m1x8(p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7]);
-          codes[2 * g + 1] = cvt_e2m1x8(p[8], p[9], p[10], p[11], p[12], p[13], p[14], p[15]);
+          codes[2 * (g & 1)] = cvt_e2m1x8(p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7]);
+          codes[2 * (g & 1) + 1] = cvt_e2m1x8(p[8], p[9], p[10], p[11], p[12], p[13], p[14], p[15]);
+          if (g & 1) {
+            // P^ row r, 16-byte chunk g/2 (two groups), 64B-swizzled: chunk c at
+            // c ^ ((r >> 1) & 3); stored as soon as it is encoded
+            const int ch = g >> 1;
+            *reinterpret_cast<uint4*>(prow + ((ch ^ ((r >> 1) & 3)) * 16)) =
+                make_uint4(codes[0], codes[1], codes[2], codes[3]);
+          }
           if (chunk) {
             tmem_ld_wait(o);
 #pragma unroll
@@ -453,11 +460,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           have_ref = true;
         }
       }
-      // P^ row r: four 16-byte chunks, 64B-swizzled (chunk c at c ^ ((r >> 1) & 3))
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
-        *reinterpret_cast<uint4*>(prow + ((ch ^ ((r >> 1) & 3)) * 16)) =
-            make_uint4(codes[4 * ch], codes[4 * ch + 1], codes[4 * ch + 2], codes[4 * ch + 3]);
       *reinterpret_cast<uint32_t*>(psf) = sfw[0];
       *reinterpret_cast<uint32_t*>(psf + 512) = sfw[1];
       if (do_corr) tmem_st_wait();
