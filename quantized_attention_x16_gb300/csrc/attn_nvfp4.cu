@@ -70,11 +70,11 @@ struct CfgF4 {
   static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffV = kOffK + NS * kKBytes;
   static constexpr int kOffP = kOffV + NS * kVBytes;
-  static constexpr int kOffQSf = kOffP + 2 * kPBytes;
+  static constexpr int kOffQSf = kOffP + 4 * kPBytes;      // P^ double-buffered per query tile
   static constexpr int kOffKSf = kOffQSf + 2 * kQSfBytes;
   static constexpr int kOffVSf = kOffKSf + NS * kKSfBytes;
   static constexpr int kOffPSf = kOffVSf + NS * kVSfBytes;
-  static constexpr int kOffBar = kOffPSf + 2 * kPSfBytes;
+  static constexpr int kOffBar = kOffPSf + 4 * kPSfBytes;
   static constexpr int kNumBars = 1 + 4 * NS + 8 + 2;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   // Q/K rows of 64 bytes use the 64B swizzle, rows of 32 bytes the 32B one.
@@ -311,10 +311,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sfp = tbase + (q ? C::kColSfP1 : C::kColSfP0);
           const uint32_t tO = tbase + C::kColO0 + q * D;
           if (leader) {
-            copy_sf(sfp, sb + C::kOffPSf + q * C::kPSfBytes, 2);
+            const int pb = 2 * q + (j & 1);                  // P^ buffer of this tile
+            copy_sf(sfp, sb + C::kOffPSf + pb * C::kPSfBytes, 2);
 #pragma unroll
             for (int kk = 0; kk < BN / 64; ++kk)
-              mma_nvf4(tO, desc_qk(sb + C::kOffP + q * C::kPBytes + kk * 32, 512, kSwizzle64B),
+              mma_nvf4(tO, desc_qk(sb + C::kOffP + pb * C::kPBytes + kk * 32, 512, kSwizzle64B),
                        desc_qk(sb + C::kOffV + s * C::kVBytes + kk * 32, 512, kSwizzle64B), C::kIdescPV,
                        sfp + 4 * kk, sfv + 4 * kk, (j > 0 || kk > 0) ? 1u : 0u);
             tc_commit(bars.o_done + q);
@@ -338,8 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = tbase + (((warp % 4) * 32) << 16);
     const int qt = qt0 + q;
     const float c = 1.4426950408889634f * rsqrtf((float)D);
-    uint8_t* prow = smem + C::kOffP + q * C::kPBytes + r * 64;
-    uint8_t* psf = smem + C::kOffPSf + q * C::kPSfBytes + (r % 32) * 16 + (r / 32) * 4;
+    uint8_t* prow0 = smem + C::kOffP + 2 * q * C::kPBytes + r * 64;
+    uint8_t* psf0 = smem + C::kOffPSf + 2 * q * C::kPSfBytes + (r % 32) * 16 + (r / 32) * 4;
     const uint32_t ocol = C::kColO0 + q * D;
     float m_run = -INFINITY, m_ref = 0.f, lam = 0.f;
     bool have_ref = false, ok = true;
@@ -377,17 +378,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t codes[4];
       uint32_t sfw[2] = {0u, 0u};
       const float corr = (live && have_ref) ? ex2_approx(m_ref - m_t) : 1.f;
-      // O is rescaled to the new tile maximum in 16-column chunks interleaved
-      // with the P work below (its loads overlap the arithmetic); warp-uniform
+      // whether O must be rescaled to the new tile maximum (warp-uniform)
       const bool do_corr = j > 0 && __any_sync(0xffffffffu, corr != 1.f);
-      if (j > 0) {
-        // P^ and O of this query tile are free once P.V of the last tile is done
-        if (!mbar_wait_warp(bars.o_done + q, (j - 1) & 1, abort_flag, wait_ns)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
+      // P^ of tile j goes to buffer j & 1, last read by P.V of tile j-2, whose
+      // completion this thread waited for in tile j-1
+      uint8_t* prow = prow0 + (j & 1) * C::kPBytes;
+      uint8_t* psf = psf0 + (j & 1) * C::kPSfBytes;
       {
         // Warp-uniform: a row that skips this tile gets bias = -inf, so its
         // P2, codes, scales and sum are all zero (the O chunks below use
@@ -420,9 +416,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         float rs = 0.f;
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-          uint32_t o[16];
-          const bool chunk = do_corr && g < D / 16;
-          if (chunk) tmem_ld16(lane_addr + ocol + 16 * g, o);
           float u[2] = {0.f, 0.f};
           float* p = sv + 16 * g;
 #pragma unroll
@@ -442,17 +435,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(prow + ((ch ^ ((r >> 1) & 3)) * 16)) =
                 make_uint4(codes[0], codes[1], codes[2], codes[3]);
           }
-          if (chunk) {
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-              float x0 = __uint_as_float(o[i]), x1 = __uint_as_float(o[i + 1]);
-              mul2(x0, x1, x0, x1, corr, corr);
-              o[i] = __float_as_uint(x0);
-              o[i + 1] = __float_as_uint(x1);
-            }
-            tmem_st16(lane_addr + ocol + 16 * g, o);
-          }
         }
         if (live) {
           lam = have_ref ? fmaf(lam, corr, rs) : rs;
@@ -462,7 +444,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       *reinterpret_cast<uint32_t*>(psf) = sfw[0];
       *reinterpret_cast<uint32_t*>(psf + 512) = sfw[1];
-      if (do_corr) tmem_st_wait();
+      if (j > 0) {
+        // O may be rescaled once P.V of the last tile is done (long since, as
+        // a rule: the P work of this tile ran in between)
+        if (!mbar_wait_warp(bars.o_done + q, (j - 1) & 1, abort_flag, wait_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      if (do_corr) {
+        // the O row to the new tile maximum: all chunks loaded before one
+        // wait (the score registers are free again), scaled, stored back
+        uint32_t o[D / 32][32];
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(lane_addr + ocol + 32 * cc, o[cc]);
+        tmem_ld_wait(o[0]);
+#pragma unroll
+        for (int cc = 1; cc < D / 32; ++cc) tmem_launder(o[cc]);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float x0 = __uint_as_float(o[cc][i]), x1 = __uint_as_float(o[cc][i + 1]);
+            mul2(x0, x1, x0, x1, corr, corr);
+            o[cc][i] = __float_as_uint(x0);
+            o[cc][i + 1] = __float_as_uint(x1);
+          }
+          tmem_st32(lane_addr + ocol + 32 * cc, o[cc]);
+        }
+        tmem_st_wait();
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bars.p_full + q);
