@@ -29,12 +29,14 @@ inline int device_sm_count() {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // quant.cu
+// tq / tk: bf16 Q and K as [rows][d], boxes of 64 channels x 128 rows, 128B swizzle.
 cudaError_t launch_quantize(const void* q, const void* k, const void* v, const Dims& dm, const sa_fp4_qkv& out,
-                            cudaStream_t s);
+                            const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t s);
 // Same kernels, K-mean partial sums in the library's fixed per-device array.
 constexpr size_t kStaticScratchFloats = SA_STATIC_SCRATCH_FLOATS;
 cudaError_t launch_quantize_static_scratch(const void* q, const void* k, const void* v, const Dims& dm,
-                                           const sa_fp4_qkv& out, cudaStream_t s);
+                                           const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk,
+                                           cudaStream_t s);
 
 // attn_bf16.cu
 cudaError_t launch_attn_bf16(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o,

@@ -77,51 +77,53 @@ __device__ __forceinline__ uint32_t quant_group16(const float* x, uint32_t* code
 
 // ---------------------------------------------------------------------------
 // Two launches, 256 threads per CTA.
-//   1. quant_vk_kernel -- two kinds of CTA:
-//        V CTAs:     one thread per (channel pair, 32 tokens): 32 4-byte loads
-//                    (each warp load is one 128-byte row segment), two
-//                    16-token groups per channel, codes stored transposed;
-//        Kpart CTAs: smooth-K partial sums, one thread per channel pair of one
-//                    128-token chunk, summed token by token from 0 (the
-//                    documented order).  They run last, so K is still in L2
-//                    for launch 2.
-//   2. quant_kq_kernel -- two kinds of CTA:
-//        K CTAs:     one per (b, kv head, 512-token block).  The head's
-//                    partial sums are staged in shared memory (coalesced, all
-//                    loads in flight) and summed in chunk order, then / L: the
-//                    same float operations in the same order in every CTA, so
-//                    mu is bit-exact and identical everywhere; the head's first
-//                    CTA also writes mu.  K - mu is then quantised quad by
-//                    quad, reading K from L2.
-//        Q CTAs:     each thread quantises kQuadsPerThread "quads" (64
-//                    consecutive channels of one row = four 1x16 groups = one
-//                    32-bit word of scale bytes), the next quad's eight
-//                    16-byte loads in flight while the current one is
-//                    computed.  Q streams from HBM while the K CTAs wait on L2.
+//   1. quant_v_mean_kernel -- clusters of kMeanCluster CTAs, of two kinds
+//        spread evenly over the grid (the latency-bound mean clusters run
+//        beside the bandwidth-bound V CTAs):
+//        mean clusters: one per (b, kv head).  CTA r sums its share of the
+//                    head's 128-token chunks, one thread per channel pair and
+//                    chunk, token by token from 0 (the documented order), into
+//                    the scratch buffer.  After a cluster barrier
+//                    (release/acquire at cluster scope) CTA 0 adds the chunk
+//                    sums in chunk order and divides by L (bit-exact mu), and
+//                    writes mu;
+//        V clusters: eight independent CTAs, one thread per channel pair and
+//                    32 tokens: 32 4-byte loads (each warp load is one 128-byte
+//                    row segment), two 16-token groups per channel, codes
+//                    stored transposed.
+//   2. quant_qk_kernel -- persistent CTAs over tiles of 256 "quads" (a quad =
+//        64 consecutive channels of one row = four 1x16 groups = one 32-bit
+//        word of scale bytes): K tiles first (launch 1 has just read K, so it
+//        comes from L2), then Q tiles.  Tiles arrive by TMA in 128B-swizzled
+//        shared memory (128-row boxes of 64 channels) through a two-stage
+//        ring; each thread reads its quad with conflict-free 16-byte loads,
+//        subtracts mu for K (64 means through L1), and stores 32 bytes of
+//        codes and the scale word in the MMA scale layout.
 
 constexpr int kThreadsQ = 256;
-constexpr int kQuadsPerThread = 1;                      // Q quads per thread
-constexpr int kKTokens = 512;                           // tokens per K CTA
-constexpr int kMeanSlice = 32;                          // 128-token chunks staged per pass
+constexpr int kMeanCluster = 8;                          // CTAs per head in the mean clusters
+
+template <int D>
+struct TileQK {
+  static constexpr int kRows = kThreadsQ / (D / 64);     // rows per tile: 128 (d = 128), 256 (d = 64)
+  static constexpr int kBoxes = 2;                       // 128-row x 64-channel boxes per tile
+  static constexpr int kBoxBytes = 128 * 64 * 2;
+  static constexpr int kSmemBytes = kBoxes * kBoxBytes;
+};
 
 struct QuantArgs {
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
   uint8_t *qc, *qsf, *kc, *ksf, *vc, *vsf;
-  float* part;      // [B*Hkv][L/128][D]
+  float* part;      // scratch: chunk sums [B*Hkv][L/128][D]
   float* kmean;     // [B*Hkv][D]
-  int L, nbh_q, nbh_kv;
-  long long nq_quads;
-  int nblk_q, nblk_v, nblk_kpart, nblk_k_per_head, nblk_k;
+  int L, nbh_q, nbh_kv, chunks_per_cta;
+  long long q_rows, k_rows;
+  int ntile_q, ntile_k, nblk_v;
+  int nclu_mean, nclu_v;            // launch 1: mean clusters, V clusters
+  uint64_t wait_ns;
 };
-
-// Loads the 64 bf16 values of one quad (eight 16-byte loads, all in flight).
-__device__ __forceinline__ void load_quad(const __nv_bfloat16* src, uint4 (&w)[8]) {
-  const uint4* p = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) w[i] = __ldg(p + i);
-}
 
 // Quantises one quad (minus the 64 means at `mean`, when given) and stores its
 // 32 bytes of codes and its scale word.  `row` is the global row (b*H + h)*L + t,
@@ -137,8 +139,15 @@ __device__ __forceinline__ void quant_quad(const uint4 (&w)[8], const float* mea
     bf16x8_to_f32(w[2 * g], x);
     bf16x8_to_f32(w[2 * g + 1], x + 8);
     if (mean != nullptr) {
+      const float4* m4 = reinterpret_cast<const float4*>(mean + 16 * g);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = __fsub_rn(x[i], mean[16 * g + i]);
+      for (int i = 0; i < 4; ++i) {
+        const float4 m = __ldg(m4 + i);
+        x[4 * i + 0] = __fsub_rn(x[4 * i + 0], m.x);
+        x[4 * i + 1] = __fsub_rn(x[4 * i + 1], m.y);
+        x[4 * i + 2] = __fsub_rn(x[4 * i + 2], m.z);
+        x[4 * i + 3] = __fsub_rn(x[4 * i + 3], m.w);
+      }
     }
     sfw |= quant_group16(x, codes + 2 * g) << (8 * g);
   }
@@ -151,23 +160,46 @@ __device__ __forceinline__ void quant_quad(const uint4 (&w)[8], const float* mea
   *reinterpret_cast<uint32_t*>(sf_base + blk * 512 + (r % 32) * 16 + (r / 32) * 4) = sfw;
 }
 
+// Issues the TMA copies of Q/K tile `tile` (tiles [0, ntile_k) are K, then Q)
+// into `dst`: rows [t*kRows, ...) of the row-major [rows][D] tensor, boxes of
+// 64 channels x 128 rows (d = 128: the two channel halves; d = 64: two row
+// blocks).
 template <int D>
-__device__ __forceinline__ void quant_q_cta(const QuantArgs& a, int blk) {
-  // quads blk*256*kQuadsPerThread + i*256 + tid, i = 0 .. kQuadsPerThread-1
-  long long gq = (long long)blk * kThreadsQ * kQuadsPerThread + threadIdx.x;
-  uint4 w[8];
-  if (gq < a.nq_quads) load_quad(a.q + (gq / (D / 64)) * D + (gq % (D / 64)) * 64, w);
-#pragma unroll 1
-  for (int i = 0; i < kQuadsPerThread && gq < a.nq_quads; ++i, gq += kThreadsQ) {
-    const long long row = gq / (D / 64);
-    const int quad = (int)(gq % (D / 64));
-    uint4 cur[8];
+__device__ __forceinline__ void issue_tile_qk(const QuantArgs& a, const CUtensorMap* tq, const CUtensorMap* tk,
+                                              int tile, uint8_t* dst, uint64_t* bar) {
+  using T = TileQK<D>;
+  const bool is_k = tile < a.ntile_k;
+  const CUtensorMap* map = is_k ? tk : tq;
+  const long long row0 = (long long)(is_k ? tile : tile - a.ntile_k) * T::kRows;
+  mbar_arrive_expect_tx(bar, T::kBoxes * T::kBoxBytes);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) cur[k] = w[k];
-    const long long nx = gq + kThreadsQ;
-    if (i + 1 < kQuadsPerThread && nx < a.nq_quads) load_quad(a.q + (nx / (D / 64)) * D + (nx % (D / 64)) * 64, w);
-    quant_quad<D>(cur, nullptr, a.qc, a.qsf, row, quad, a.L);
+  for (int b = 0; b < T::kBoxes; ++b) {
+    const int x = D == 128 ? 64 * b : 0;
+    const long long y = D == 128 ? row0 : row0 + 128 * b;
+    tma_load_2d(dst + b * T::kBoxBytes, map, bar, x, (int)y);
   }
+}
+
+// Quantises the tile in `src` (128B swizzle: 16-byte chunk i of box row rr
+// sits at chunk i ^ (rr & 7)); one quad per thread.
+template <int D>
+__device__ __forceinline__ void quant_tile_smem(const QuantArgs& a, int tile, const uint8_t* src) {
+  using T = TileQK<D>;
+  const bool is_k = tile < a.ntile_k;
+  const long long row0 = (long long)(is_k ? tile : tile - a.ntile_k) * T::kRows;
+  const long long nrows = is_k ? a.k_rows : a.q_rows;
+  const int r = threadIdx.x / (D / 64), quad = threadIdx.x % (D / 64);
+  const long long row = row0 + r;
+  if (row >= nrows) return;
+  const int box = D == 128 ? quad : r / 128, rr = D == 128 ? r : r % 128;
+  const uint8_t* base = src + box * T::kBoxBytes + rr * 128;
+  uint4 w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = *reinterpret_cast<const uint4*>(base + ((i ^ (rr & 7)) * 16));
+  if (is_k)
+    quant_quad<D>(w, a.kmean + (row / a.L) * D + quad * 64, a.kc, a.ksf, row, quad, a.L);
+  else
+    quant_quad<D>(w, nullptr, a.qc, a.qsf, row, quad, a.L);
 }
 
 // One thread per (channel pair, 32 tokens = two 16-token groups).  Items are
@@ -209,110 +241,131 @@ __device__ __forceinline__ void quant_v_cta(const QuantArgs& a, int blk) {
   }
 }
 
-// part[bh][chunk][c] = sum over the chunk's 128 tokens, token by token from 0.
+// mu[bh][c] = (chunk sums in chunk order) / L, chunk sum = the chunk's 128
+// tokens added token by token from 0.  Called by all CTAs of one cluster.
 template <int D>
-__device__ __forceinline__ void kpart_cta(const QuantArgs& a, int blk) {
+__device__ __forceinline__ void mean_cluster(const QuantArgs& a, int bh) {
   constexpr int kPairs = D / 2;
-  constexpr int kChunksPerCta = kThreadsQ / kPairs;
-  const int nchunk = a.L / kMeanChunk;
-  const int gchunk = blk * kChunksPerCta + threadIdx.x / kPairs;     // over B*Hkv*nchunk
-  if (gchunk >= a.nbh_kv * nchunk) return;
-  const int bh = gchunk / nchunk, chunk = gchunk % nchunk;
+  constexpr int kChunksAtOnce = kThreadsQ / kPairs;
+  const uint32_t rank = cluster_ctarank();
+  const int nchunk = a.L / kMeanChunk, cpc = a.chunks_per_cta;
+  const int first = (int)rank * cpc, last = min(nchunk, first + cpc);
   const int c = 2 * (threadIdx.x % kPairs);
-  const uint32_t* src =
-      reinterpret_cast<const uint32_t*>(a.k + ((size_t)bh * a.L + (size_t)chunk * kMeanChunk) * D + c);
-  float acc0 = 0.f, acc1 = 0.f;
+  for (int ch = first + (int)threadIdx.x / kPairs; ch < last; ch += kChunksAtOnce) {
+    const uint32_t* src =
+        reinterpret_cast<const uint32_t*>(a.k + ((size_t)bh * a.L + (size_t)ch * kMeanChunk) * D + c);
+    float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll 1
-  for (int t0 = 0; t0 < kMeanChunk; t0 += 32) {
-    uint32_t w[32];
+    for (int t0 = 0; t0 < kMeanChunk; t0 += 32) {
+      uint32_t w[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = __ldg(src + (size_t)(t0 + i) * (D / 2));
+      for (int i = 0; i < 32; ++i) w[i] = __ldg(src + (size_t)(t0 + i) * (D / 2));
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      acc0 = __fadd_rn(acc0, __uint_as_float(w[i] << 16));
-      acc1 = __fadd_rn(acc1, __uint_as_float(w[i] & 0xFFFF0000u));
+      for (int i = 0; i < 32; ++i) {
+        acc0 = __fadd_rn(acc0, __uint_as_float(w[i] << 16));
+        acc1 = __fadd_rn(acc1, __uint_as_float(w[i] & 0xFFFF0000u));
+      }
     }
+    *reinterpret_cast<float2*>(a.part + ((size_t)bh * nchunk + ch) * D + c) = make_float2(acc0, acc1);
   }
-  *reinterpret_cast<float2*>(a.part + ((size_t)bh * nchunk + chunk) * D + c) = make_float2(acc0, acc1);
+  cluster_sync();                                       // every chunk sum of the head is written
+  if (rank == 0 && threadIdx.x < D) {
+    const int col = threadIdx.x;
+    float tot = 0.f;
+#pragma unroll 1
+    for (int c0 = 0; c0 < nchunk; c0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int ch = c0 + j;
+        v[j] = ch < nchunk ? __ldcg(a.part + ((size_t)bh * nchunk + ch) * D + col) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (c0 + j < nchunk) tot = __fadd_rn(tot, v[j]);
+    }
+    a.kmean[(size_t)bh * D + col] = __fdiv_rn(tot, (float)a.L);
+  }
 }
 
+// Mean clusters sit near positions i * total / nclu_mean, so they run beside
+// the V clusters throughout the launch.
 template <int D>
-__global__ void __launch_bounds__(kThreadsQ, 3) quant_vk_kernel(const QuantArgs a) {
-  const int blk = blockIdx.x;
-  if (blk < a.nblk_q)
-    quant_q_cta<D>(a, blk);
-  else if (blk < a.nblk_q + a.nblk_v)
-    quant_v_cta<D>(a, blk - a.nblk_q);
-  else
-    kpart_cta<D>(a, blk - a.nblk_q - a.nblk_v);
+__global__ void __cluster_dims__(kMeanCluster, 1, 1) __launch_bounds__(kThreadsQ)
+    quant_v_mean_kernel(const QuantArgs a) {
+  const long long clu = blockIdx.x / kMeanCluster, total = (long long)a.nclu_mean + a.nclu_v;
+  const long long m_before = clu * a.nclu_mean / total, m_through = (clu + 1) * a.nclu_mean / total;
+  if (m_through > m_before) {
+    mean_cluster<D>(a, (int)m_before);
+    return;
+  }
+  const int blk = (int)(clu - m_before) * kMeanCluster + (int)(blockIdx.x % kMeanCluster);
+  if (blk < a.nblk_v) quant_v_cta<D>(a, blk);
 }
 
-// mean[c] = (partials summed in chunk order) / L for one (b, kv head), into
-// shared memory; written to k_mean as well when `publish`.
+// Persistent: CTA c takes tiles c, c + G, c + 2G, ... (G = grid size) through
+// a two-stage TMA ring, the next tile's copy in flight while the current one
+// is quantised.
 template <int D>
-__device__ __forceinline__ void head_mean(const QuantArgs& a, int bh, float* mean, float* stage, bool publish) {
-  const int nchunk = a.L / kMeanChunk;
-  const float* part = a.part + (size_t)bh * nchunk * D;
-  float tot = 0.f;
-  for (int c0 = 0; c0 < nchunk; c0 += kMeanSlice) {
-    const int nc = min(kMeanSlice, nchunk - c0);
-    __syncthreads();                                    // previous slice consumed
-    // all of this thread's loads are issued before the first store
-    constexpr int kPer = kMeanSlice * D / kThreadsQ;
-    float v[kPer];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int i = threadIdx.x + k * kThreadsQ;
-      v[k] = i < nc * D ? __ldcg(part + (size_t)c0 * D + i) : 0.f;
-    }
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) stage[threadIdx.x + k * kThreadsQ] = v[k];
-    __syncthreads();
-    if (threadIdx.x < D)
-      for (int j = 0; j < nc; ++j) tot = __fadd_rn(tot, stage[j * D + threadIdx.x]);
-  }
-  if (threadIdx.x < D) {
-    const float mu = __fdiv_rn(tot, (float)a.L);
-    mean[threadIdx.x] = mu;
-    if (publish) a.kmean[(size_t)bh * D + threadIdx.x] = mu;
+__global__ void __launch_bounds__(kThreadsQ) quant_qk_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                                                             const __grid_constant__ CUtensorMap tmap_k,
+                                                             const QuantArgs a) {
+  using T = TileQK<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t full[2];
+  __shared__ int abort_flag;
+  const int ntiles = a.ntile_k + a.ntile_q, G = gridDim.x;
+  if (threadIdx.x == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    abort_flag = 0;
+    fence_barrier_init();
   }
   __syncthreads();
-}
-
-template <int D>
-__device__ __forceinline__ void quant_k_cta(const QuantArgs& a, int blk, float* mean, float* stage) {
-  constexpr int kQuadsPerRow = D / 64;
-  const int bh = blk / a.nblk_k_per_head;
-  const int t0 = (blk % a.nblk_k_per_head) * kKTokens;
-  const int nquads = min(kKTokens, a.L - t0) * kQuadsPerRow;
-  const __nv_bfloat16* kbase = a.k + ((size_t)bh * a.L + t0) * D;
-  // the first quad's loads are in flight while the mean is formed
-  int qi = threadIdx.x;
-  uint4 w[8];
-  if (qi < nquads) load_quad(kbase + (size_t)(qi / kQuadsPerRow) * D + (qi % kQuadsPerRow) * 64, w);
-  head_mean<D>(a, bh, mean, stage, t0 == 0);
-  for (; qi < nquads; qi += kThreadsQ) {
-    const int quad = qi % kQuadsPerRow;
-    const long long row = (long long)bh * a.L + t0 + qi / kQuadsPerRow;
-    uint4 cur[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) cur[k] = w[k];
-    const int nx = qi + kThreadsQ;
-    if (nx < nquads) load_quad(kbase + (size_t)(nx / kQuadsPerRow) * D + (nx % kQuadsPerRow) * 64, w);
-    quant_quad<D>(cur, mean + quad * 64, a.kc, a.ksf, row, quad, a.L);
+  const bool leader = threadIdx.x == 0;
+  int tile = blockIdx.x;
+  int issued[2] = {0, 0};                               // loads issued per stage (leader's count)
+  if (leader) {
+    if (tile < ntiles) {
+      issue_tile_qk<D>(a, &tmap_q, &tmap_k, tile, smem, &full[0]);
+      issued[0] = 1;
+    }
+    if (tile + G < ntiles) {
+      issue_tile_qk<D>(a, &tmap_q, &tmap_k, tile + G, smem + T::kSmemBytes, &full[1]);
+      issued[1] = 1;
+    }
   }
-}
-
-template <int D>
-__global__ void __launch_bounds__(kThreadsQ) quant_kq_kernel(const QuantArgs a) {
-  __shared__ __align__(16) float mean[D];
-  __shared__ __align__(16) float stage[kMeanSlice * D];
-  quant_k_cta<D>(a, (int)blockIdx.x, mean, stage);
+  bool ok = true;
+  int i = 0;
+  for (; tile < ntiles; ++i, tile += G) {
+    const int st = i & 1;
+    if (!mbar_wait(&full[st], (i >> 1) & 1, &abort_flag, a.wait_ns)) {
+      ok = false;
+      break;
+    }
+    quant_tile_smem<D>(a, tile, smem + st * T::kSmemBytes);
+    __syncthreads();                                    // stage st has been read by every thread
+    if (leader && tile + 2 * G < ntiles) {
+      issue_tile_qk<D>(a, &tmap_q, &tmap_k, tile + 2 * G, smem + st * T::kSmemBytes, &full[st]);
+      ++issued[st];
+    }
+  }
+  if (!ok && leader) {
+    // never leave with a copy in flight: wait (bounded) for each stage's last
+    // issued load, the use-th load of a stage completing phase use - 1
+    for (int st = 0; st < 2; ++st) {
+      const int consumed = (i + 1 - st) / 2;            // loads of stage st waited for so far
+      if (issued[st] > consumed) mbar_wait_drain(&full[st], (issued[st] - 1) & 1, a.wait_ns);
+    }
+  }
 }
 
 template <int D>
 cudaError_t launch_quantize_impl(const void* q, const void* k, const void* v, const Dims& dm,
-                                 const sa_fp4_qkv& out, float* partials, cudaStream_t s) {
+                                 const sa_fp4_qkv& out, float* partials, const CUtensorMap& tq,
+                                 const CUtensorMap& tk, cudaStream_t s) {
+  using T = TileQK<D>;
   QuantArgs a;
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.k = static_cast<const __nv_bfloat16*>(k);
@@ -328,26 +381,38 @@ cudaError_t launch_quantize_impl(const void* q, const void* k, const void* v, co
   a.L = dm.L;
   a.nbh_q = dm.B * dm.H;
   a.nbh_kv = dm.B * dm.Hkv;
-  a.nq_quads = (long long)a.nbh_q * dm.L * (D / 64);
-  a.nblk_q = (int)((a.nq_quads + kThreadsQ * kQuadsPerThread - 1) / (kThreadsQ * kQuadsPerThread));
+  const int nchunk = dm.L / kMeanChunk;
+  a.chunks_per_cta = (nchunk + kMeanCluster - 1) / kMeanCluster;
+  a.q_rows = (long long)a.nbh_q * dm.L;
+  a.k_rows = (long long)a.nbh_kv * dm.L;
+  a.ntile_q = (int)((a.q_rows + T::kRows - 1) / T::kRows);
+  a.ntile_k = (int)((a.k_rows + T::kRows - 1) / T::kRows);
   a.nblk_v = (int)(((long long)a.nbh_kv * (dm.L / 32) * (D / 2) + kThreadsQ - 1) / kThreadsQ);
-  const int kchunks = a.nbh_kv * (dm.L / kMeanChunk);
-  const int kcpb = kThreadsQ / (D / 2);
-  a.nblk_kpart = (kchunks + kcpb - 1) / kcpb;
-  a.nblk_k_per_head = (dm.L + kKTokens - 1) / kKTokens;
-  a.nblk_k = a.nbh_kv * a.nblk_k_per_head;
-  quant_vk_kernel<D><<<a.nblk_q + a.nblk_v + a.nblk_kpart, kThreadsQ, 0, s>>>(a);
-  quant_kq_kernel<D><<<a.nblk_k, kThreadsQ, 0, s>>>(a);
+  a.nclu_mean = a.nbh_kv;
+  a.nclu_v = (a.nblk_v + kMeanCluster - 1) / kMeanCluster;
+  a.wait_ns = kWaitLimitNs;
+  constexpr int kSmem = 2 * T::kSmemBytes + 1024;        // two stages + alignment slack
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(quant_qk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int ntiles = a.ntile_k + a.ntile_q;
+  const int sms = device_sm_count() > 0 ? device_sm_count() : 148;
+  const int grid = ntiles < 3 * sms ? ntiles : 3 * sms;    // three resident CTAs per SM
+  quant_v_mean_kernel<D><<<(a.nclu_mean + a.nclu_v) * kMeanCluster, kThreadsQ, 0, s>>>(a);
+  quant_qk_kernel<D><<<grid, kThreadsQ, kSmem, s>>>(tq, tk, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_quantize(const void* q, const void* k, const void* v, const Dims& dm, const sa_fp4_qkv& out,
-                            cudaStream_t s) {
+                            const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t s) {
   float* part = static_cast<float*>(out.workspace);
-  return dm.d == 64 ? launch_quantize_impl<64>(q, k, v, dm, out, part, s)
-                    : launch_quantize_impl<128>(q, k, v, dm, out, part, s);
+  return dm.d == 64 ? launch_quantize_impl<64>(q, k, v, dm, out, part, tq, tk, s)
+                    : launch_quantize_impl<128>(q, k, v, dm, out, part, tq, tk, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -384,17 +449,18 @@ cudaError_t static_scratch_address(float** out) {
 }  // namespace
 
 cudaError_t launch_quantize_static_scratch(const void* q, const void* k, const void* v, const Dims& dm,
-                                           const sa_fp4_qkv& out, cudaStream_t s) {
+                                           const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk,
+                                           cudaStream_t s) {
   const size_t need = (size_t)dm.B * dm.Hkv * (dm.L / kMeanChunk) * dm.d;
   if (need > kStaticScratchFloats) return cudaErrorInvalidValue;
   float* part = nullptr;
   cudaError_t e = static_scratch_address(&part);
   if (e != cudaSuccess) return e;
-  // Every partial sum read is written first by the same call (the partial-sum
-  // CTAs of its first launch), so earlier contents of the array never reach
-  // the outputs and nothing needs clearing.
-  return dm.d == 64 ? launch_quantize_impl<64>(q, k, v, dm, out, part, s)
-                    : launch_quantize_impl<128>(q, k, v, dm, out, part, s);
+  // Every chunk sum read is written first by the same call (its first
+  // launch), so earlier contents of the array never reach the outputs and
+  // nothing needs clearing.
+  return dm.d == 64 ? launch_quantize_impl<64>(q, k, v, dm, out, part, tq, tk, s)
+                    : launch_quantize_impl<128>(q, k, v, dm, out, part, tq, tk, s);
 }
 
 }  // namespace sa

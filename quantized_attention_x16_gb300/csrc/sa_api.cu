@@ -44,6 +44,14 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// bf16 Q and K as [rows][d] with boxes of 64 channels x 128 rows, 128B swizzle
+// (the tiles of both the BF16 attention kernel and the quantiser).
+bool make_bf16_row_maps(const void* q, const void* k, const Dims& dm, CUtensorMap* tq, CUtensorMap* tk) {
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return make_map(tq, bf, q, dm.d, (uint64_t)dm.B * dm.H * dm.L, 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(tk, bf, k, dm.d, (uint64_t)dm.B * dm.Hkv * dm.L, 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 sa_status check_dims(int B, int H, int Hkv, int L, int d) {
   if (B <= 0 || H <= 0 || Hkv <= 0 || L <= 0 || d <= 0) return SA_ERR_INVALID_ARG;
   if (H % Hkv != 0) return SA_ERR_INVALID_ARG;
@@ -141,8 +149,11 @@ sa_status sa_quantize(const void* q, const void* k, const void* v, int B, int H,
   if (st != SA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !fp4_ptrs_ok(out)) return SA_ERR_INVALID_ARG;
   const Dims dm{B, H, Hkv, L, d};
-  return launch_quantize(q, k, v, dm, *out, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SA_OK
-                                                                                                  : SA_ERR_CUDA;
+  CUtensorMap tq, tk;
+  if (!make_bf16_row_maps(q, k, dm, &tq, &tk)) return SA_ERR_CUDA;
+  return launch_quantize(q, k, v, dm, *out, tq, tk, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SA_OK
+             : SA_ERR_CUDA;
 }
 
 sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v, int B, int H, int Hkv, int L,
@@ -155,7 +166,10 @@ sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v
       !aligned16(out->v_sf) || !aligned16(out->k_mean))
     return SA_ERR_INVALID_ARG;
   const Dims dm{B, H, Hkv, L, d};
-  return launch_quantize_static_scratch(q, k, v, dm, *out, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+  CUtensorMap tq, tk;
+  if (!make_bf16_row_maps(q, k, dm, &tq, &tk)) return SA_ERR_CUDA;
+  return launch_quantize_static_scratch(q, k, v, dm, *out, tq, tk, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
              ? SA_OK
              : SA_ERR_CUDA;
 }

@@ -128,6 +128,17 @@ __device__ __forceinline__ bool mbar_wait_backoff_warp(uint64_t* bar, uint32_t p
   return __all_sync(0xffffffffu, mbar_wait_backoff(bar, parity, abort, limit_ns, sleep_ns));
 }
 
+// ------------------------------------------------------------ clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// All threads of all CTAs of the cluster: release this CTA's shared-memory
+// writes, acquire the others'.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
