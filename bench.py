@@ -284,7 +284,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline_quantize": {"kernel": "sa_quantize (2 kernels)", "bound": "hbm", "achieved": qbytes / t_q / 1e9,
                               "peak": pk["hbm"], "unit": "GB/s", "frac": qbytes / t_q / 1e9 / pk["hbm"],
                               "traffic": None, "algorithmic_bytes": qbytes,
-                              "traffic_kernels": {k: prof.get(k) for k in ("quant_qv_kernel", "quant_k_kernel")}},
+                              "traffic_kernels": {k: prof.get(k) for k in ("quant_v_mean_kernel", "quant_qk_kernel")}},
         "cpu_baseline": cpu,
         "e2e": {"value": world * fl / t_e2e / 1e12, "unit": "TOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
