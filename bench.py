@@ -45,9 +45,9 @@ def peaks():
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
         return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sus=p.get("bf16_tflops_sustained"),
-                    src="measured")
+                    sm_max_mhz=p.get("sm_max_mhz", 2070.0), src="measured")
     except Exception:
-        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, sm_max_mhz=2070.0, src="fallback")
 
 
 class Clocks:
@@ -278,6 +278,7 @@ def run_ours(args, rank, world, local_rank):
                      "unit": "TFLOP/s", "frac": a4 / nvfp4_peak,
                      "traffic": prof.get("attn_nvfp4"),
                      "peak_src": f"{pk['src']} bf16 burst {pk['bf16']} x nominal FP4:BF16 ratio {NVFP4_OVER_BF16}"},
+        "roofline_secondary": mufu_roofline(a4, d, pk),
         "roofline_bf16": {"kernel": f"attn_bf16_kernel<{d}>", "bound": "tensor", "achieved": a16, "peak": pk["bf16"],
                           "unit": "TFLOP/s", "frac": a16 / pk["bf16"], "traffic": prof.get("attn_bf16"),
                           "peak_src": f"{pk['src']} bf16 burst"},
@@ -293,6 +294,25 @@ def run_ours(args, rank, world, local_rank):
         "wall_s_timed_region": wall,
     }
     print(json.dumps(line), flush=True)
+
+
+# Exponentials per SM per clock on this GPU (ex2.approx: measured with a
+# throughput probe of independent chains over the whole device).
+MUFU_EX2_PER_SM_CLK = 32
+
+
+def mufu_roofline(achieved_tops, d, pk):
+    """Secondary bound of the fused attention: one ex2 per score element on the
+    MUFU, 4*d flops per element, at the maximum SM clock."""
+    try:
+        import torch
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    except Exception:
+        sms = 152
+    peak = MUFU_EX2_PER_SM_CLK * 4 * d * sms * pk["sm_max_mhz"] * 1e6 / 1e12
+    return {"kernel": f"attn_nvfp4_kernel<{d}>", "bound": "alu (MUFU ex2, one per score)", "achieved": achieved_tops,
+            "peak": peak, "unit": "TOPS", "frac": achieved_tops / peak,
+            "peak_src": f"{MUFU_EX2_PER_SM_CLK} ex2/clk/SM (measured) x 4d flops x {sms} SMs x {pk['sm_max_mhz']} MHz"}
 
 
 def quant_bytes(w):
