@@ -18,7 +18,8 @@
  *    1/sqrt(d); causal means key j is visible to query i iff j <= i.
  *  - Ownership: the caller allocates and owns every buffer.  The library
  *    allocates no device memory and keeps no state between calls other than
- *    a device error word (see sa_last_device_error).
+ *    a device error word (see sa_last_device_error) and, once
+ *    sa_attn_fwd_host has been called, its copy streams and events.
  *  - Asynchrony: work is enqueued on `stream` (NULL = legacy default stream)
  *    and the call returns before it finishes.
  *  - Errors: arguments are validated before anything is enqueued; on any
@@ -165,6 +166,42 @@ sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v
 sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o,
                       int B, int H, int Hkv, int L, int d, int causal,
                       int mode, sa_stream_t stream);
+
+/*
+ * sa_attn_fwd_host -- the path of sa_attn_fwd (mode SA_MODE_NVFP4:
+ * sa_quantize then the FP4 attention; SA_MODE_BF16: the BF16 attention) on
+ * bf16 BHLD Q, K, V in pinned HOST memory, writing O to pinned host memory.
+ * (A library entry point for callers whose tensors live on the host; the
+ * pages describe the computation only.)
+ *  q, k, v, o: host pointers inside page-locked allocations (cudaHostAlloc or
+ *    cudaHostRegister; anything else is SA_ERR_INVALID_ARG), laid out as for
+ *    sa_attn_fwd; o is bf16, or float32 with SA_OUT_FP32 in `mode`.
+ *  workspace: device buffer of at least
+ *    sa_attn_fwd_host_workspace_bytes(B, H, Hkv, L, d, mode, chunk_pairs)
+ *    bytes, 256-byte aligned; must not be used by anything else until the
+ *    call's work on `stream` has completed.
+ *  chunk_pairs: (batch, kv head) pairs per chunk; 0 = the library's choice
+ *    (the most pairs whose attention CTAs fit in one wave on the SMs, and at
+ *    least two chunks).
+ * The problem is cut into chunks of consecutive (batch, kv head) pairs with
+ * all their query heads.  Each chunk's inputs are copied host -> device on a
+ * copy stream, computed on `stream` (the same kernels as the device-buffer
+ * calls, so results are bit-identical to them), and its O copied back on a
+ * second copy stream; two workspace slots alternate between chunks, so the
+ * copies of one chunk overlap the compute of its neighbours.  The copies
+ * start after the work already enqueued on `stream`, and `stream` reaches
+ * the end of the call's work only after O is in host memory (synchronise on
+ * `stream` before reading o).  The two copy streams and seven events are
+ * created on the first call on each device and kept until the process
+ * exits; calls on one device must not be made concurrently from several host
+ * threads.  Errors as for sa_attn_fwd; a failure after the first copy was
+ * enqueued leaves o partly written.
+ */
+size_t sa_attn_fwd_host_workspace_bytes(int B, int H, int Hkv, int L, int d, int mode, int chunk_pairs);
+sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,
+                           int B, int H, int Hkv, int L, int d, int causal, int mode,
+                           void* workspace, size_t workspace_bytes, int chunk_pairs,
+                           sa_stream_t stream);
 
 /* Static string for a status code. */
 const char* sa_status_string(sa_status s);

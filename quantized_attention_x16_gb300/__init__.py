@@ -13,6 +13,8 @@ Names follow the C ABI:
 * ``sa_quantize(q, k, v, out=None)``  -- smooth-K + NVFP4 quantisation of Q, K, V
 * ``sa_quantize_static_scratch(...)`` -- the same without caller-provided scratch
 * ``sa_attn_fwd(q, k, v, o=None, causal=False, mode="bf16"|"nvfp4")``
+* ``sa_attn_fwd_host(q, k, v, o=None, causal=False, mode=...)`` -- the same on
+  pinned host tensors, copies overlapped with compute inside the library
 * ``sa_last_device_error()``, ``sa_selftest_wait_timeout(ns)``, ``sa_version()``
 """
 
@@ -28,6 +30,7 @@ SA_OUT_FP32 = 16
 
 #: every symbol include/sa.h declares
 EXPORTS = ("sa_fp4_qkv_bytes", "sa_fp4_qkv_from_blob", "sa_quantize", "sa_quantize_static_scratch", "sa_attn_fwd",
+           "sa_attn_fwd_host_workspace_bytes", "sa_attn_fwd_host",
            "sa_status_string", "sa_last_device_error", "sa_selftest_wait_timeout", "sa_version")
 SA_STATIC_SCRATCH_FLOATS = 1 << 20
 
@@ -54,6 +57,10 @@ def _load():
     lib.sa_quantize_static_scratch.restype = i
     lib.sa_attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.sa_attn_fwd.restype = i
+    lib.sa_attn_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+    lib.sa_attn_fwd_host_workspace_bytes.restype = sz
+    lib.sa_attn_fwd_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, sz, i, vp]
+    lib.sa_attn_fwd_host.restype = i
     lib.sa_status_string.argtypes = [i]
     lib.sa_status_string.restype = ctypes.c_char_p
     lib.sa_last_device_error.argtypes = []
@@ -206,6 +213,53 @@ def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=
         raise ValueError("o must be a contiguous CUDA tensor of shape (B, H, L, d) and dtype out_dtype")
     _check(lib.sa_attn_fwd(*args, _ptr(o), B, H, Hkv, L, d, int(bool(causal)), m, _stream(stream)),
            "sa_attn_fwd")
+    return o
+
+
+def _bf16_pinned(t, name):
+    import torch
+    if not (t.device.type == "cpu" and t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 4
+            and t.is_pinned()):
+        raise ValueError(f"{name} must be a contiguous 4-D bfloat16 pinned host tensor (BHLD)")
+
+
+def sa_attn_fwd_host_workspace_bytes(B, H, Hkv, L, d, mode="nvfp4", out_dtype=None, chunk_pairs=0):
+    import torch
+    m = {"bf16": SA_MODE_BF16, "nvfp4": SA_MODE_NVFP4}[mode] | (SA_OUT_FP32 if out_dtype == torch.float32 else 0)
+    return int(lib.sa_attn_fwd_host_workspace_bytes(B, H, Hkv, L, d, m, int(chunk_pairs)))
+
+
+def sa_attn_fwd_host(q, k, v, o=None, causal=False, mode="nvfp4", out_dtype=None, workspace=None, chunk_pairs=0,
+                     stream=None):
+    """The path of sa_attn_fwd on pinned host tensors (see sa.h): q, k, v bf16
+    BHLD pinned CPU tensors; o (allocated pinned if None) receives the output
+    once ``stream`` has finished.  workspace: a uint8 CUDA tensor of at least
+    sa_attn_fwd_host_workspace_bytes(...) bytes (allocated on the current
+    device if None).  Returns o."""
+    import torch
+    _bf16_pinned(q, "q"), _bf16_pinned(k, "k"), _bf16_pinned(v, "v")
+    B, H, L, d = q.shape
+    Hkv = k.shape[1]
+    if out_dtype is None:
+        out_dtype = o.dtype if o is not None else torch.bfloat16
+    if out_dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("out_dtype must be torch.bfloat16 or torch.float32")
+    m = {"bf16": SA_MODE_BF16, "nvfp4": SA_MODE_NVFP4}[mode] | (SA_OUT_FP32 if out_dtype == torch.float32 else 0)
+    if o is None:
+        o = torch.empty((B, H, L, d), dtype=out_dtype).pin_memory()
+    if not (o.device.type == "cpu" and o.dtype == out_dtype and o.is_contiguous() and o.is_pinned()
+            and tuple(o.shape) == (B, H, L, d)):
+        raise ValueError("o must be a contiguous pinned host tensor of shape (B, H, L, d) and dtype out_dtype")
+    need = int(lib.sa_attn_fwd_host_workspace_bytes(B, H, Hkv, L, d, m, int(chunk_pairs)))
+    if need == 0:
+        raise SaError(SA_ERR_UNSUPPORTED, "sa_attn_fwd_host_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+    if not (workspace.is_cuda and workspace.dtype == torch.uint8 and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous uint8 CUDA tensor")
+    _check(lib.sa_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Hkv, L, d, int(bool(causal)), m,
+                                _ptr(workspace), workspace.numel(), int(chunk_pairs), _stream(stream)),
+           "sa_attn_fwd_host")
     return o
 
 

@@ -1,0 +1,200 @@
+// host_pipe.cu -- sa_attn_fwd_host: the whole attention path on tensors in
+// pinned host memory, with the host<->device copies overlapped with compute.
+//
+// Every (batch, kv head) pair is an independent problem: its G = H / Hkv query
+// heads read only that kv head's K and V, the smooth-K mean is per pair, and
+// the quantiser and attention kernels work per head.  The problem is cut into
+// chunks of consecutive pairs (all G query heads of each); in BHLD layout a
+// chunk's Q, K, V and O are contiguous ranges, so a chunk is itself a problem
+// with B = 1, H = n * G, Hkv = n.  Chunk c uses device slot c & 1 of the
+// caller's workspace:
+//   copy-in stream : Q, K, V of chunk c  host -> slot        (after chunk c-2's compute)
+//   caller's stream: sa_quantize + sa_attn_fwd on the slot    (after its copy-in and
+//                                                              chunk c-2's copy-out)
+//   copy-out stream: O of chunk c  slot -> host              (after its compute)
+// so the copies of one chunk run beside the compute of its neighbours.  The
+// kernels compute every head exactly as on the whole problem, so the results
+// are bit-identical to sa_quantize + sa_attn_fwd on device buffers.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace sa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Two copy streams and the events that order the slots, per device; created
+// on first use and kept for the life of the process.
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t cin = nullptr, cout = nullptr;
+  cudaEvent_t start = nullptr, in[2] = {}, comp[2] = {}, out[2] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mu;
+
+HostPipe* pipe_for_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  HostPipe& p = g_pipe[dev];
+  if (!p.ready) {
+    const unsigned ef = cudaEventDisableTiming;
+    if (cudaStreamCreateWithFlags(&p.cin, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p.cout, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.start, ef) != cudaSuccess)
+      return nullptr;
+    for (int i = 0; i < 2; ++i)
+      if (cudaEventCreateWithFlags(&p.in[i], ef) != cudaSuccess ||
+          cudaEventCreateWithFlags(&p.comp[i], ef) != cudaSuccess ||
+          cudaEventCreateWithFlags(&p.out[i], ef) != cudaSuccess)
+        return nullptr;
+    p.ready = true;
+  }
+  return &p;
+}
+
+size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Pairs per chunk: the most whose attention CTAs fit in one wave on the SMs
+// (a chunk's kernels then take about one CTA lifetime), and at least two
+// chunks when there are two pairs or more.
+int default_chunk_pairs(int B, int H, int Hkv, int L) {
+  const int G = H / Hkv, pairs = B * Hkv;
+  const int units = G * ((L / 128 + 1) / 2);   // attention CTAs of one pair
+  int n = device_sm_count() / (units > 0 ? units : 1);
+  if (n < 1) n = 1;
+  if (pairs >= 2 && n > (pairs + 1) / 2) n = (pairs + 1) / 2;
+  return n;
+}
+
+// Byte layout of one slot for chunks of up to n pairs.
+struct SlotLayout {
+  size_t q, k, v, o, blob, bytes;
+};
+SlotLayout slot_layout(int n, int G, int L, int d, bool fp4, size_t osz) {
+  SlotLayout s;
+  const size_t rows_q = (size_t)n * G * L, rows_k = (size_t)n * L;
+  size_t off = 0;
+  s.q = off, off = al256(off + rows_q * d * 2);
+  s.k = off, off = al256(off + rows_k * d * 2);
+  s.v = off, off = al256(off + rows_k * d * 2);
+  s.o = off, off = al256(off + rows_q * d * osz);
+  s.blob = off;
+  if (fp4) off = al256(off + sa_fp4_qkv_bytes(1, n * G, n, L, d, nullptr));
+  s.bytes = off;
+  return s;
+}
+
+bool pinned_host(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
+sa_status check_host_args(int B, int H, int Hkv, int L, int d, int causal, int mode_flags, int chunk_pairs) {
+  if (B <= 0 || H <= 0 || Hkv <= 0 || L <= 0 || d <= 0 || H % Hkv != 0) return SA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
+  if (mode_flags & ~(0xF | SA_OUT_FP32)) return SA_ERR_INVALID_ARG;
+  const int mode = mode_flags & 0xF;
+  if (mode != SA_MODE_BF16 && mode != SA_MODE_NVFP4) return SA_ERR_INVALID_ARG;
+  if (chunk_pairs < 0) return SA_ERR_INVALID_ARG;
+  // the whole problem must be one the device calls accept
+  if (sa_fp4_qkv_bytes(B, H, Hkv, L, d, nullptr) == 0) return SA_ERR_UNSUPPORTED;
+  return SA_OK;
+}
+
+}  // namespace
+}  // namespace sa
+
+using namespace sa;
+
+extern "C" {
+
+size_t sa_attn_fwd_host_workspace_bytes(int B, int H, int Hkv, int L, int d, int mode_flags, int chunk_pairs) {
+  if (check_host_args(B, H, Hkv, L, d, 0, mode_flags, chunk_pairs) != SA_OK) return 0;
+  const int n = chunk_pairs > 0 ? (chunk_pairs < B * Hkv ? chunk_pairs : B * Hkv)
+                                : default_chunk_pairs(B, H, Hkv, L);
+  const bool fp4 = (mode_flags & 0xF) == SA_MODE_NVFP4;
+  const size_t osz = (mode_flags & SA_OUT_FP32) ? 4 : 2;
+  return 2 * slot_layout(n, H / Hkv, L, d, fp4, osz).bytes;
+}
+
+sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int L, int d,
+                           int causal, int mode_flags, void* workspace, size_t workspace_bytes, int chunk_pairs,
+                           sa_stream_t stream) {
+  sa_status st = check_host_args(B, H, Hkv, L, d, causal, mode_flags, chunk_pairs);
+  if (st != SA_OK) return st;
+  if (!q || !k || !v || !o || !workspace) return SA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SA_ERR_INVALID_ARG;
+  if (!pinned_host(q) || !pinned_host(k) || !pinned_host(v) || !pinned_host(o)) return SA_ERR_INVALID_ARG;
+  const int pairs = B * Hkv, G = H / Hkv;
+  const int n = chunk_pairs > 0 ? (chunk_pairs < pairs ? chunk_pairs : pairs) : default_chunk_pairs(B, H, Hkv, L);
+  const bool fp4 = (mode_flags & 0xF) == SA_MODE_NVFP4;
+  const size_t osz = (mode_flags & SA_OUT_FP32) ? 4 : 2;
+  const SlotLayout lay = slot_layout(n, G, L, d, fp4, osz);
+  if (workspace_bytes < 2 * lay.bytes) return SA_ERR_INVALID_ARG;
+  HostPipe* p = pipe_for_current_device();
+  if (!p) return SA_ERR_CUDA;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t q_pair = (size_t)G * L * d * 2, kv_pair = (size_t)L * d * 2, o_pair = (size_t)G * L * d * osz;
+  const uint8_t* hq = static_cast<const uint8_t*>(q);
+  const uint8_t* hk = static_cast<const uint8_t*>(k);
+  const uint8_t* hv = static_cast<const uint8_t*>(v);
+  uint8_t* ho = static_cast<uint8_t*>(o);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  bool ok = true;
+  auto cu = [&ok](cudaError_t e) { ok = ok && e == cudaSuccess; };
+
+  // both copy streams start after the work already on the caller's stream
+  // (an earlier call on the same workspace, for one)
+  cu(cudaEventRecord(p->start, s));
+  cu(cudaStreamWaitEvent(p->cin, p->start, 0));
+  cu(cudaStreamWaitEvent(p->cout, p->start, 0));
+  const int nchunks = (pairs + n - 1) / n;
+  for (int c = 0; ok && c < nchunks; ++c) {
+    const int slot = c & 1, p0 = c * n, nc = (pairs - p0) < n ? (pairs - p0) : n;
+    uint8_t* base = ws + slot * lay.bytes;
+    uint8_t *dq = base + lay.q, *dk = base + lay.k, *dv = base + lay.v, *dout = base + lay.o;
+    // copy in, once chunk c-2 is done reading this slot
+    if (c >= 2) cu(cudaStreamWaitEvent(p->cin, p->comp[slot], 0));
+    cu(cudaMemcpyAsync(dq, hq + p0 * q_pair, nc * q_pair, cudaMemcpyHostToDevice, p->cin));
+    cu(cudaMemcpyAsync(dk, hk + p0 * kv_pair, nc * kv_pair, cudaMemcpyHostToDevice, p->cin));
+    cu(cudaMemcpyAsync(dv, hv + p0 * kv_pair, nc * kv_pair, cudaMemcpyHostToDevice, p->cin));
+    cu(cudaEventRecord(p->in[slot], p->cin));
+    // compute, once the inputs are in and chunk c-2's O has left the slot
+    cu(cudaStreamWaitEvent(s, p->in[slot], 0));
+    if (c >= 2) cu(cudaStreamWaitEvent(s, p->out[slot], 0));
+    if (!ok) break;
+    if (fp4) {
+      sa_fp4_qkv x;
+      st = sa_fp4_qkv_from_blob(base + lay.blob, 1, nc * G, nc, L, d, &x);
+      if (st == SA_OK) st = sa_quantize(dq, dk, dv, 1, nc * G, nc, L, d, &x, stream);
+      if (st == SA_OK) st = sa_attn_fwd(&x, nullptr, nullptr, dout, 1, nc * G, nc, L, d, causal, mode_flags, stream);
+    } else {
+      st = sa_attn_fwd(dq, dk, dv, dout, 1, nc * G, nc, L, d, causal, mode_flags, stream);
+    }
+    if (st != SA_OK) return st;
+    cu(cudaEventRecord(p->comp[slot], s));
+    // copy out
+    cu(cudaStreamWaitEvent(p->cout, p->comp[slot], 0));
+    cu(cudaMemcpyAsync(ho + p0 * o_pair, dout, nc * o_pair, cudaMemcpyDeviceToHost, p->cout));
+    cu(cudaEventRecord(p->out[slot], p->cout));
+  }
+  // the caller's stream completes after the last copy out (the copy-out
+  // stream is in order, so its last event covers every chunk)
+  const int last = (nchunks - 1) & 1;
+  cu(cudaStreamWaitEvent(s, p->out[last], 0));
+  return ok ? SA_OK : SA_ERR_CUDA;
+}
+
+}  // extern "C"
