@@ -22,12 +22,16 @@
  *    sa_attn_fwd_host has been called, its copy streams and events.
  *  - Asynchrony: work is enqueued on `stream` (NULL = legacy default stream)
  *    and the call returns before it finishes.
+ *  - Sizes: any L >= 1 (a ragged last 128-token tile is masked: keys past L
+ *    get no weight, rows past L are not written); d in {64, 128}; H a
+ *    multiple of Hkv.  An empty problem (B == 0 or L == 0) is valid: the call
+ *    returns SA_OK without enqueueing anything or reading any pointer.
  *  - Errors: arguments are validated before anything is enqueued; on any
  *    argument error nothing is launched.  SA_ERR_INVALID_ARG: null or
- *    misaligned pointer (all pointers must be 16-byte aligned), non-positive
- *    size, H % Hkv != 0.  SA_ERR_UNSUPPORTED: d not in {64, 128} or L not a
- *    multiple of 128.  SA_ERR_CUDA: a launch or driver call failed (the CUDA
- *    error is not cleared).
+ *    misaligned pointer (all pointers must be 16-byte aligned), negative B or
+ *    L, H or Hkv < 1, H % Hkv != 0.  SA_ERR_UNSUPPORTED: d not in {64, 128},
+ *    or B * H * Lp >= 2^31 (Lp = L rounded up to 128).  SA_ERR_CUDA: a launch
+ *    or driver call failed (the CUDA error is not cleared).
  *  - Inputs are assumed finite; NaN/Inf inputs give unspecified results.
  */
 #ifndef SA_H_
@@ -59,22 +63,25 @@ typedef enum { SA_MODE_BF16 = 0, SA_MODE_NVFP4 = 1 } sa_mode;
 
 /*
  * Quantised operands produced by sa_quantize (device pointers, caller-owned).
+ * Every layout holds Lp = L rounded up to a multiple of 128 tokens per head;
+ * tokens past L have zero codes and zero scales, and a V group that straddles
+ * L is quantised with zeros for its missing tokens.
  *
  * Codes: two e2m1 nibbles per byte, element 2i in the low nibble.
- *   q_codes [B, H, L, d/2]    Q, groups of 16 along d
- *   k_codes [B, Hkv, L, d/2]  K' = K - mean_tokens(K), groups along d
- *   v_codes [B, Hkv, d, L/2]  V transposed (channel rows), groups of 16
- *                             consecutive tokens
+ *   q_codes [B, H, Lp, d/2]    Q, groups of 16 along d
+ *   k_codes [B, Hkv, Lp, d/2]  K' = K - mean_tokens(K), groups along d
+ *   v_codes [B, Hkv, d, Lp/2]  V transposed (channel rows), groups of 16
+ *                              consecutive tokens
  * Scale factors (e4m3 bytes) in 512-byte blocks of 128 rows x 4 groups; the
  * byte at m0*16 + j*4 + k of a block is the scale of row 32*j + m0, group k:
- *   q_sf [B, H, L/128, d/64, 512]   rows = tokens, groups = d/16 along d
- *   k_sf [B, Hkv, L/128, d/64, 512]
- *   v_sf [B, Hkv, L/64, 512]        rows = channels (rows >= d are 0),
- *                                   groups = 16-token groups of a 64-token chunk
+ *   q_sf [B, H, Lp/128, d/64, 512]   rows = tokens, groups = d/16 along d
+ *   k_sf [B, Hkv, Lp/128, d/64, 512]
+ *   v_sf [B, Hkv, Lp/64, 512]        rows = channels (rows >= d are 0),
+ *                                    groups = 16-token groups of a 64-token chunk
  * k_mean [B, Hkv, d] float32: the smooth-K mean, computed as the float32 sum
- *   over 128-token chunks (token order inside a chunk, then chunk order)
- *   divided by L.
- * workspace: scratch for sa_quantize (float32 [B, Hkv, L/128, d] partial sums).
+ *   over 128-token chunks (token order inside a chunk, then chunk order; the
+ *   last chunk holds the L % 128 remaining tokens) divided by L.
+ * workspace: scratch for sa_quantize (float32 [B, Hkv, Lp/128, d] partial sums).
  * This is the layout the tcgen05 block-scaled MMA consumes (scale blocks are
  * copied to tensor memory unchanged).
  */
@@ -93,7 +100,8 @@ typedef struct {
  * Bytes of one device blob holding every sa_fp4_qkv buffer, each at a
  * 256-byte aligned offset.  offsets_out (may be NULL) receives 8 offsets in
  * struct order (q_codes, q_sf, k_codes, k_sf, v_codes, v_sf, k_mean,
- * workspace).  Returns 0 for unsupported sizes.
+ * workspace).  Returns 0 for unsupported sizes and for an empty problem
+ * (which needs no blob).
  */
 size_t sa_fp4_qkv_bytes(int B, int H, int Hkv, int L, int d, size_t offsets_out[8]);
 
@@ -132,7 +140,7 @@ sa_status sa_quantize(const void* q, const void* k, const void* v,
  * library until the process exits).  It calls no cudaMalloc, cudaFree or
  * other allocating routine.
  *  - Arguments as for sa_quantize; out->workspace is ignored and may be NULL.
- *  - Sizes with B * Hkv * (L/128) * d > SA_STATIC_SCRATCH_FLOATS return
+ *  - Sizes with B * Hkv * (Lp/128) * d > SA_STATIC_SCRATCH_FLOATS return
  *    SA_ERR_UNSUPPORTED before anything is launched.
  *  - The first call on each device, made with that device current, looks up
  *    the array's device address (cudaGetSymbolAddress); make that first call

@@ -176,7 +176,8 @@ def dequantized_operands(q, k, v):
     vc, vs = quant.quantize_v(v)
     qd = dequantize_groups(qc, qs)
     kd = dequantize_groups(kc, ks)
-    vd = np.swapaxes(dequantize_groups(vc, vs), -1, -2)
+    L = np.asarray(v).shape[-2]
+    vd = np.swapaxes(dequantize_groups(vc, vs), -1, -2)[..., :L, :]     # drop V's zero completion
     return (qd, kd, vd), dict(mu=mu, qc=qc, qs=qs, kc=kc, ks=ks, vc=vc, vs=vs)
 
 

@@ -91,9 +91,15 @@ def quantize_k(k, mu):
 def quantize_v(v):
     """V [B,Hkv,L,d] -> groups of 16 consecutive tokens per channel.
 
-    Returns codes [B,Hkv,d,L] (channel-major, i.e. V transposed) and
-    scales [B,Hkv,d,L/16]."""
+    Returns codes [B,Hkv,d,L16] (channel-major, i.e. V transposed) and
+    scales [B,Hkv,d,L16/16], L16 = L rounded up to a multiple of 16.  When L
+    is not a multiple of 16 the last group of each channel is completed with
+    zero tokens (reading: the missing tokens of a group that straddles the end
+    of the sequence quantise as zeros; they meet only zero weights in P.V)."""
     vt = np.ascontiguousarray(np.swapaxes(np.asarray(v, np.float32), -1, -2))
+    pad = (-vt.shape[-1]) % GROUP
+    if pad:
+        vt = np.concatenate([vt, np.zeros(vt.shape[:-1] + (pad,), np.float32)], axis=-1)
     return quantize_groups(vt)
 
 

@@ -135,13 +135,14 @@ class FP4QKV:
         """Torch views of each region, shaped as documented in sa.h."""
         import torch
         B, H, Hkv, L, d = self.dims
+        Lp = -(-L // 128) * 128           # the layouts hold whole 128-token tiles
         shapes = [
-            ("q_codes", (B, H, L, d // 2), torch.uint8),
-            ("q_sf", (B, H, L // 128, d // 64, 512), torch.uint8),
-            ("k_codes", (B, Hkv, L, d // 2), torch.uint8),
-            ("k_sf", (B, Hkv, L // 128, d // 64, 512), torch.uint8),
-            ("v_codes", (B, Hkv, d, L // 2), torch.uint8),
-            ("v_sf", (B, Hkv, L // 64, 512), torch.uint8),
+            ("q_codes", (B, H, Lp, d // 2), torch.uint8),
+            ("q_sf", (B, H, Lp // 128, d // 64, 512), torch.uint8),
+            ("k_codes", (B, Hkv, Lp, d // 2), torch.uint8),
+            ("k_sf", (B, Hkv, Lp // 128, d // 64, 512), torch.uint8),
+            ("v_codes", (B, Hkv, d, Lp // 2), torch.uint8),
+            ("v_sf", (B, Hkv, Lp // 64, 512), torch.uint8),
             ("k_mean", (B, Hkv, d), torch.float32),
         ]
         out = {}

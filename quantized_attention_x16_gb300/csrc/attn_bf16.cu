@@ -109,8 +109,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hk = h / (H / Hkv);
   const bool q1_valid = nqu == 2;
   int ntq[2];
-  ntq[0] = causal ? qt0 + 1 : L / BN;
-  ntq[1] = q1_valid ? (causal ? qt0 + 2 : L / BN) : 0;
+  const int nkt = (L + BN - 1) / BN;                // key tiles; a ragged last one is zero-filled past L
+  ntq[0] = causal ? qt0 + 1 : nkt;
+  ntq[1] = q1_valid ? (causal ? qt0 + 2 : nkt) : 0;
   const int nt = ntq[0] > ntq[1] ? ntq[0] : ntq[1];
 
   if (threadIdx.x == 0) {
@@ -131,8 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  const long long q_row0 = ((long long)b * H + h) * L;      // first row of this head in Q/O
-  const long long kv_row0 = ((long long)b * Hkv + hk) * L;
+  const int bhq = b * H + h, bhk = b * Hkv + hk;            // head index of the 3-D Q/O and K/V maps
+  const long long q_row0 = (long long)bhq * L;             // first row of this head in O
 
   if (warp >= 8) {
     // Register split: the launch gives every thread kLaunchRegs; this
@@ -153,20 +154,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(bars.q_full, nq * C::kTileBytes);
         for (int q = 0; q < nq; ++q)
           for (int hh = 0; hh < D / 64; ++hh)
-            tma_load_2d(smem + C::kOffQ + q * C::kTileBytes + hh * C::kHalfBytes, &tmap_q, bars.q_full, hh * 64,
-                        (int)(q_row0 + (long long)(qt0 + q) * BM));
+            tma_load_3d(smem + C::kOffQ + q * C::kTileBytes + hh * C::kHalfBytes, &tmap_q, bars.q_full, hh * 64,
+                        (qt0 + q) * BM, bhq);
       }
       int issued = 0;
       for (int j = 0; j < nt; ++j) {
         const int s = j % C::NS;
         const uint32_t par = ((j / C::NS) - 1) & 1;
-        const int y = (int)(kv_row0 + (long long)j * BN);
+        const int y = j * BN;
         if (j >= C::NS && !mbar_wait_backoff_warp(bars.k_empty + s, par, abort_flag, wait_ns, kProducerSleepNs)) break;
         if (leader) {
           mbar_arrive_expect_tx(bars.k_full + s, C::kTileBytes);
           for (int hh = 0; hh < D / 64; ++hh)
-            tma_load_2d(smem + C::kOffK + s * C::kTileBytes + hh * C::kHalfBytes, &tmap_k, bars.k_full + s,
-                        hh * 64, y);
+            tma_load_3d(smem + C::kOffK + s * C::kTileBytes + hh * C::kHalfBytes, &tmap_k, bars.k_full + s,
+                        hh * 64, y, bhk);
         }
         if (j >= C::NS && !mbar_wait_backoff_warp(bars.v_empty + s, par, abort_flag, wait_ns, kProducerSleepNs)) {
           issued = 2 * j + 1;
@@ -175,8 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) {
           mbar_arrive_expect_tx(bars.v_full + s, C::kTileBytes);
           for (int hh = 0; hh < D / 64; ++hh)
-            tma_load_2d(smem + C::kOffV + s * C::kTileBytes + hh * C::kHalfBytes, &tmap_v, bars.v_full + s,
-                        hh * 64, y);
+            tma_load_3d(smem + C::kOffV + s * C::kTileBytes + hh * C::kHalfBytes, &tmap_v, bars.v_full + s,
+                        hh * 64, y, bhk);
         }
         issued = 2 * j + 2;
       }
@@ -292,10 +293,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sv[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
-      if (causal && j == qt) {
+      // keys this row may not see: past the diagonal (causal) and past L (the
+      // zero fill of a ragged last tile)
+      const int lim = min(causal && j == qt ? r + 1 : BN, L - j * BN);
+      if (lim < BN) {
 #pragma unroll
         for (int i = 0; i < 128; ++i)
-          if (i > r) sv[i] = -INFINITY;
+          if (i >= lim) sv[i] = -INFINITY;
       }
       float gm[8];
 #pragma unroll
@@ -366,11 +370,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = 1.f / l;
       const long long obase = (q_row0 + (long long)qt * BM + r) * D;
+      const bool row_in = qt * BM + r < L;              // rows past L (a ragged last tile) are not stored
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         tmem_ld32(lane_addr + ocol + 32 * cc, o);
         tmem_ld_wait(o);
+        if (!row_in) continue;
         if constexpr (OUT32) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_ptr) + obase + 32 * cc);
 #pragma unroll

@@ -150,8 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hk = h / (H / Hkv);
   const bool q1_valid = nqu == 2;
   int ntq[2];
-  ntq[0] = causal ? qt0 + 1 : L / BN;
-  ntq[1] = q1_valid ? (causal ? qt0 + 2 : L / BN) : 0;
+  // the quantised operands hold Lp = L rounded up to whole tiles per head
+  const int Lp = (L + 127) & ~127;
+  ntq[0] = causal ? qt0 + 1 : Lp / BN;
+  ntq[1] = q1_valid ? (causal ? qt0 + 2 : Lp / BN) : 0;
   const int nt = ntq[0] > ntq[1] ? ntq[0] : ntq[1];
 
   if (threadIdx.x == 0) {
@@ -195,8 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < nq; ++q) {
           const int qt = qt0 + q;
           tma_load_2d(smem + C::kOffQ + q * C::kQBytes, &tmap_q, bars.q_full, 0,
-                      (int)(bhq * L + (long long)qt * BM));
-          bulk_load(smem + C::kOffQSf + q * C::kQSfBytes, q_sf + (bhq * (L / 128) + qt) * C::kQSfBytes,
+                      (int)(bhq * Lp + (long long)qt * BM));
+          bulk_load(smem + C::kOffQSf + q * C::kQSfBytes, q_sf + (bhq * (Lp / 128) + qt) * C::kQSfBytes,
                     C::kQSfBytes, bars.q_full);
         }
       }
@@ -208,8 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) {
           mbar_arrive_expect_tx(bars.k_full + s, C::kKBytes + C::kKSfBytes);
           tma_load_2d(smem + C::kOffK + s * C::kKBytes, &tmap_k, bars.k_full + s, 0,
-                      (int)(bhk * L + (long long)j * BN));
-          bulk_load(smem + C::kOffKSf + s * C::kKSfBytes, k_sf + (bhk * (L / 128) + j) * C::kKSfBytes,
+                      (int)(bhk * Lp + (long long)j * BN));
+          bulk_load(smem + C::kOffKSf + s * C::kKSfBytes, k_sf + (bhk * (Lp / 128) + j) * C::kKSfBytes,
                     C::kKSfBytes, bars.k_full + s);
         }
         if (j >= C::NS && !mbar_wait_backoff_warp(bars.v_empty + s, par, abort_flag, wait_ns, kProducerSleepNs)) {
@@ -219,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) {
           mbar_arrive_expect_tx(bars.v_full + s, C::kVBytes + C::kVSfBytes);
           tma_load_2d(smem + C::kOffV + s * C::kVBytes, &tmap_v, bars.v_full + s, j * (BN / 2), (int)(bhk * D));
-          bulk_load(smem + C::kOffVSf + s * C::kVSfBytes, v_sf + (bhk * (L / 64) + 2 * j) * 512, C::kVSfBytes,
+          bulk_load(smem + C::kOffVSf + s * C::kVSfBytes, v_sf + (bhk * (Lp / 64) + 2 * j) * 512, C::kVSfBytes,
                     bars.v_full + s);
         }
         issued = 2 * j + 2;
@@ -362,10 +364,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sv[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
-      if (causal && j == qt) {
+      // keys this row may not see: past the diagonal (causal) and past L (the
+      // zero padding of a ragged last tile)
+      const int lim = min(causal && j == qt ? r + 1 : BN, L - j * BN);
+      if (lim < BN) {
 #pragma unroll
         for (int i = 0; i < 128; ++i)
-          if (i > r) sv[i] = -INFINITY;
+          if (i >= lim) sv[i] = -INFINITY;
       }
       float gm[8];
 #pragma unroll
@@ -483,11 +488,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = 1.f / lam;
       const long long obase = (bhq * L + (long long)qt * BM + r) * D;
+      const bool row_in = qt * BM + r < L;              // rows of the padding are not stored
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         tmem_ld32(lane_addr + ocol + 32 * cc, o);
         tmem_ld_wait(o);
+        if (!row_in) continue;
         if constexpr (OUT32) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_ptr) + obase + 32 * cc);
 #pragma unroll

@@ -100,15 +100,18 @@ bool pinned_host(const void* p) {
   return a.type == cudaMemoryTypeHost;
 }
 
+// SA_OK for a problem the pipeline takes (empty ones included: B == 0 or
+// L == 0), or the error to return.
 sa_status check_host_args(int B, int H, int Hkv, int L, int d, int causal, int mode_flags, int chunk_pairs) {
-  if (B <= 0 || H <= 0 || Hkv <= 0 || L <= 0 || d <= 0 || H % Hkv != 0) return SA_ERR_INVALID_ARG;
+  if (B < 0 || H <= 0 || Hkv <= 0 || L < 0 || d <= 0 || H % Hkv != 0) return SA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
   if (mode_flags & ~(0xF | SA_OUT_FP32)) return SA_ERR_INVALID_ARG;
   const int mode = mode_flags & 0xF;
   if (mode != SA_MODE_BF16 && mode != SA_MODE_NVFP4) return SA_ERR_INVALID_ARG;
   if (chunk_pairs < 0) return SA_ERR_INVALID_ARG;
-  // the whole problem must be one the device calls accept
-  if (sa_fp4_qkv_bytes(B, H, Hkv, L, d, nullptr) == 0) return SA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return SA_ERR_UNSUPPORTED;
+  // a non-empty problem must be one the device calls accept
+  if (B > 0 && L > 0 && sa_fp4_qkv_bytes(B, H, Hkv, L, d, nullptr) == 0) return SA_ERR_UNSUPPORTED;
   return SA_OK;
 }
 
@@ -120,7 +123,7 @@ using namespace sa;
 extern "C" {
 
 size_t sa_attn_fwd_host_workspace_bytes(int B, int H, int Hkv, int L, int d, int mode_flags, int chunk_pairs) {
-  if (check_host_args(B, H, Hkv, L, d, 0, mode_flags, chunk_pairs) != SA_OK) return 0;
+  if (check_host_args(B, H, Hkv, L, d, 0, mode_flags, chunk_pairs) != SA_OK || B == 0 || L == 0) return 0;
   const int n = chunk_pairs > 0 ? (chunk_pairs < B * Hkv ? chunk_pairs : B * Hkv)
                                 : default_chunk_pairs(B, H, Hkv, L);
   const bool fp4 = (mode_flags & 0xF) == SA_MODE_NVFP4;
@@ -133,6 +136,7 @@ sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,
                            sa_stream_t stream) {
   sa_status st = check_host_args(B, H, Hkv, L, d, causal, mode_flags, chunk_pairs);
   if (st != SA_OK) return st;
+  if (B == 0 || L == 0) return SA_OK;                  // nothing to compute or copy
   if (!q || !k || !v || !o || !workspace) return SA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SA_ERR_INVALID_ARG;
   if (!pinned_host(q) || !pinned_host(k) || !pinned_host(v) || !pinned_host(o)) return SA_ERR_INVALID_ARG;

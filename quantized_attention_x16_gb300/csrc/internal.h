@@ -13,6 +13,10 @@ struct Dims {
   int B, H, Hkv, L, d;
 };
 
+// The sequence length padded to whole 128-token tiles: the row count of every
+// quantised layout (rows past L hold zero codes and zero scales).
+inline int padded_len(int L) { return (L + 127) & ~127; }
+
 // Number of SMs of the current device (cached per device; 0 if unknown).
 inline int device_sm_count() {
   static int cache[64] = {};

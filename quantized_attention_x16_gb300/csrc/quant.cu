@@ -93,12 +93,17 @@ __device__ __forceinline__ uint32_t quant_group16(const float* x, uint32_t* code
 //                    stored transposed.
 //   2. quant_qk_kernel -- persistent CTAs over tiles of 256 "quads" (a quad =
 //        64 consecutive channels of one row = four 1x16 groups = one 32-bit
-//        word of scale bytes): K tiles first (launch 1 has just read K, so it
-//        comes from L2), then Q tiles.  Tiles arrive by TMA in 128B-swizzled
-//        shared memory (128-row boxes of 64 channels) through a two-stage
-//        ring; each thread reads its quad with conflict-free 16-byte loads,
-//        subtracts mu for K (64 means through L1), and stores 32 bytes of
-//        codes and the scale word in the MMA scale layout.
+//        word of scale bytes) of one head: K tiles first (launch 1 has just
+//        read K, so it comes from L2), then Q tiles.  Tiles arrive by TMA in
+//        128B-swizzled shared memory (boxes of 64 channels x 128 tokens of one
+//        head; tokens past L arrive as zeros) through a two-stage ring; each
+//        thread reads its quad with conflict-free 16-byte loads, subtracts mu
+//        for K (64 means through L1), and stores 32 bytes of codes and the
+//        scale word in the MMA scale layout.
+// Every layout holds Lp = L rounded up to 128 tokens per head; the tokens
+// past L are written as zero codes with zero scales (Q and K rows, V token
+// groups), and a V group that straddles L is quantised with zeros for its
+// missing tokens.
 
 constexpr int kThreadsQ = 256;
 constexpr int kMeanCluster = 8;                          // CTAs per head in the mean clusters
@@ -116,21 +121,21 @@ struct QuantArgs {
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
   uint8_t *qc, *qsf, *kc, *ksf, *vc, *vsf;
-  float* part;      // scratch: chunk sums [B*Hkv][L/128][D]
+  float* part;      // scratch: chunk sums [B*Hkv][Lp/128][D]
   float* kmean;     // [B*Hkv][D]
-  int L, nbh_q, nbh_kv, chunks_per_cta;
-  long long q_rows, k_rows;
+  int L, Lp, nbh_q, nbh_kv, chunks_per_cta;
+  int tiles_per_head;               // Q/K tiles of kRows tokens per head
   int ntile_q, ntile_k, nblk_v;
   int nclu_mean, nclu_v;            // launch 1: mean clusters, V clusters
   uint64_t wait_ns;
 };
 
 // Quantises one quad (minus the 64 means at `mean`, when given) and stores its
-// 32 bytes of codes and its scale word.  `row` is the global row (b*H + h)*L + t,
-// `quad` the 64-channel block within the row.
+// 32 bytes of codes and its scale word: token t of head bh (rows of Lp tokens
+// per head), `quad` the 64-channel block within the row.
 template <int D>
 __device__ __forceinline__ void quant_quad(const uint4 (&w)[8], const float* mean, uint8_t* codes_base,
-                                           uint8_t* sf_base, long long row, int quad, int L) {
+                                           uint8_t* sf_base, long long bh, int t, int quad, int Lp) {
   uint32_t codes[8];
   uint32_t sfw = 0;
 #pragma unroll
@@ -151,32 +156,40 @@ __device__ __forceinline__ void quant_quad(const uint4 (&w)[8], const float* mea
     }
     sfw |= quant_group16(x, codes + 2 * g) << (8 * g);
   }
-  uint4* cdst = reinterpret_cast<uint4*>(codes_base + row * (D / 2) + quad * 32);
+  uint4* cdst = reinterpret_cast<uint4*>(codes_base + (bh * Lp + t) * (D / 2) + quad * 32);
   cdst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
   cdst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-  const long long bh = row / L;
-  const int t = (int)(row % L), rb = t / 128, r = t % 128;
-  const long long blk = (bh * (L / 128) + rb) * (D / 64) + quad;
+  const int rb = t / 128, r = t % 128;
+  const long long blk = (bh * (Lp / 128) + rb) * (D / 64) + quad;
   *reinterpret_cast<uint32_t*>(sf_base + blk * 512 + (r % 32) * 16 + (r / 32) * 4) = sfw;
 }
 
-// Issues the TMA copies of Q/K tile `tile` (tiles [0, ntile_k) are K, then Q)
-// into `dst`: rows [t*kRows, ...) of the row-major [rows][D] tensor, boxes of
-// 64 channels x 128 rows (d = 128: the two channel halves; d = 64: two row
-// blocks).
+// Head and first token of Q/K tile `tile` (tiles [0, ntile_k) are K, then Q).
+__device__ __forceinline__ void tile_head(const QuantArgs& a, int tile, int rows, bool& is_k, int& bh, int& t0) {
+  is_k = tile < a.ntile_k;
+  const int u = is_k ? tile : tile - a.ntile_k;
+  bh = u / a.tiles_per_head;
+  t0 = (u % a.tiles_per_head) * rows;
+}
+
+// Issues the TMA copies of Q/K tile `tile` into `dst`: tokens [t0, t0 + kRows)
+// of one head, boxes of 64 channels x 128 tokens (d = 128: the two channel
+// halves; d = 64: two token blocks).  Tokens past L (and a second box wholly
+// past Lp) arrive as zeros.
 template <int D>
 __device__ __forceinline__ void issue_tile_qk(const QuantArgs& a, const CUtensorMap* tq, const CUtensorMap* tk,
                                               int tile, uint8_t* dst, uint64_t* bar) {
   using T = TileQK<D>;
-  const bool is_k = tile < a.ntile_k;
+  bool is_k;
+  int bh, t0;
+  tile_head(a, tile, T::kRows, is_k, bh, t0);
   const CUtensorMap* map = is_k ? tk : tq;
-  const long long row0 = (long long)(is_k ? tile : tile - a.ntile_k) * T::kRows;
   mbar_arrive_expect_tx(bar, T::kBoxes * T::kBoxBytes);
 #pragma unroll
   for (int b = 0; b < T::kBoxes; ++b) {
     const int x = D == 128 ? 64 * b : 0;
-    const long long y = D == 128 ? row0 : row0 + 128 * b;
-    tma_load_2d(dst + b * T::kBoxBytes, map, bar, x, (int)y);
+    const int y = D == 128 ? t0 : t0 + 128 * b;
+    tma_load_3d(dst + b * T::kBoxBytes, map, bar, x, y, bh);
   }
 }
 
@@ -185,21 +198,22 @@ __device__ __forceinline__ void issue_tile_qk(const QuantArgs& a, const CUtensor
 template <int D>
 __device__ __forceinline__ void quant_tile_smem(const QuantArgs& a, int tile, const uint8_t* src) {
   using T = TileQK<D>;
-  const bool is_k = tile < a.ntile_k;
-  const long long row0 = (long long)(is_k ? tile : tile - a.ntile_k) * T::kRows;
-  const long long nrows = is_k ? a.k_rows : a.q_rows;
+  bool is_k;
+  int bh, t0;
+  tile_head(a, tile, T::kRows, is_k, bh, t0);
   const int r = threadIdx.x / (D / 64), quad = threadIdx.x % (D / 64);
-  const long long row = row0 + r;
-  if (row >= nrows) return;
+  const int t = t0 + r;
+  if (t >= a.Lp) return;
   const int box = D == 128 ? quad : r / 128, rr = D == 128 ? r : r % 128;
   const uint8_t* base = src + box * T::kBoxBytes + rr * 128;
   uint4 w[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) w[i] = *reinterpret_cast<const uint4*>(base + ((i ^ (rr & 7)) * 16));
+  // a token past L arrived as zeros; K' there is kept zero (no mean subtracted)
   if (is_k)
-    quant_quad<D>(w, a.kmean + (row / a.L) * D + quad * 64, a.kc, a.ksf, row, quad, a.L);
+    quant_quad<D>(w, t < a.L ? a.kmean + (size_t)bh * D + quad * 64 : nullptr, a.kc, a.ksf, bh, t, quad, a.Lp);
   else
-    quant_quad<D>(w, nullptr, a.qc, a.qsf, row, quad, a.L);
+    quant_quad<D>(w, nullptr, a.qc, a.qsf, bh, t, quad, a.Lp);
 }
 
 // One thread per (channel pair, 32 tokens = two 16-token groups).  Items are
@@ -210,17 +224,24 @@ template <int D>
 __device__ __forceinline__ void quant_v_cta(const QuantArgs& a, int blk) {
   constexpr int kPairs = D / 2;
   const long long item = (long long)blk * kThreadsQ + threadIdx.x;
-  const int npb = a.L / 32;                             // 32-token pieces per head
+  const int npb = a.Lp / 32;                            // 32-token pieces per head (padded length)
   if (item >= (long long)a.nbh_kv * npb * kPairs) return;
   const int c = 2 * (int)(item % kPairs);
   const long long piece = item / kPairs;                // over B*Hkv*npb
   const long long bh = piece / npb;
   const int tp = (int)(piece % npb);
+  const int nvalid = a.L - tp * 32;                     // tokens of this piece below L (may be <= 0)
   const uint32_t* src = reinterpret_cast<const uint32_t*>(a.v + ((size_t)bh * a.L + (size_t)tp * 32) * D + c);
   uint32_t w[32];
+  if (nvalid >= 32) {
 #pragma unroll
-  for (int t = 0; t < 32; ++t) w[t] = __ldg(src + (size_t)t * (D / 2));
-  uint8_t* sblk = a.vsf + ((size_t)bh * (a.L / 64) + tp / 2) * 512 + (tp % 2) * 2;
+    for (int t = 0; t < 32; ++t) w[t] = __ldg(src + (size_t)t * (D / 2));
+  } else {
+    // the ragged end of the head: tokens past L count as zeros
+#pragma unroll
+    for (int t = 0; t < 32; ++t) w[t] = t < nvalid ? __ldg(src + (size_t)t * (D / 2)) : 0u;
+  }
+  uint8_t* sblk = a.vsf + ((size_t)bh * (a.Lp / 64) + tp / 2) * 512 + (tp % 2) * 2;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {                         // channel c + h
     uint32_t codes[4];
@@ -234,32 +255,36 @@ __device__ __forceinline__ void quant_v_cta(const QuantArgs& a, int blk) {
       sfw |= quant_group16(x, codes + 2 * g) << (8 * g);
     }
     const int ch = c + h;
-    *reinterpret_cast<uint4*>(a.vc + ((size_t)bh * D + ch) * (a.L / 2) + (size_t)tp * 16) =
+    *reinterpret_cast<uint4*>(a.vc + ((size_t)bh * D + ch) * (a.Lp / 2) + (size_t)tp * 16) =
         make_uint4(codes[0], codes[1], codes[2], codes[3]);
     *reinterpret_cast<uint16_t*>(sblk + (ch % 32) * 16 + (ch / 32) * 4) = (uint16_t)sfw;
     if (D == 64) *reinterpret_cast<uint16_t*>(sblk + (ch % 32) * 16 + (ch / 32 + 2) * 4) = 0;   // padding rows
   }
 }
 
-// mu[bh][c] = (chunk sums in chunk order) / L, chunk sum = the chunk's 128
-// tokens added token by token from 0.  Called by all CTAs of one cluster.
+// mu[bh][c] = (chunk sums in chunk order) / L, chunk sum = the chunk's tokens
+// (128, fewer in a ragged last chunk) added token by token from 0.  Called by
+// all CTAs of one cluster.
 template <int D>
 __device__ __forceinline__ void mean_cluster(const QuantArgs& a, int bh) {
   constexpr int kPairs = D / 2;
   constexpr int kChunksAtOnce = kThreadsQ / kPairs;
   const uint32_t rank = cluster_ctarank();
-  const int nchunk = a.L / kMeanChunk, cpc = a.chunks_per_cta;
+  const int nchunk = a.Lp / kMeanChunk, cpc = a.chunks_per_cta;
   const int first = (int)rank * cpc, last = min(nchunk, first + cpc);
   const int c = 2 * (threadIdx.x % kPairs);
   for (int ch = first + (int)threadIdx.x / kPairs; ch < last; ch += kChunksAtOnce) {
     const uint32_t* src =
         reinterpret_cast<const uint32_t*>(a.k + ((size_t)bh * a.L + (size_t)ch * kMeanChunk) * D + c);
     float acc0 = 0.f, acc1 = 0.f;
+    const int nvalid = a.L - ch * kMeanChunk;           // tokens of this chunk below L
 #pragma unroll 1
     for (int t0 = 0; t0 < kMeanChunk; t0 += 32) {
+      // a token past L adds +0, which leaves a float32 sum unchanged (the
+      // sum starts at +0 and never becomes -0)
       uint32_t w[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) w[i] = __ldg(src + (size_t)(t0 + i) * (D / 2));
+      for (int i = 0; i < 32; ++i) w[i] = t0 + i < nvalid ? __ldg(src + (size_t)(t0 + i) * (D / 2)) : 0u;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         acc0 = __fadd_rn(acc0, __uint_as_float(w[i] << 16));
@@ -379,15 +404,15 @@ cudaError_t launch_quantize_impl(const void* q, const void* k, const void* v, co
   a.part = partials;
   a.kmean = out.k_mean;
   a.L = dm.L;
+  a.Lp = padded_len(dm.L);
   a.nbh_q = dm.B * dm.H;
   a.nbh_kv = dm.B * dm.Hkv;
-  const int nchunk = dm.L / kMeanChunk;
+  const int nchunk = a.Lp / kMeanChunk;
   a.chunks_per_cta = (nchunk + kMeanCluster - 1) / kMeanCluster;
-  a.q_rows = (long long)a.nbh_q * dm.L;
-  a.k_rows = (long long)a.nbh_kv * dm.L;
-  a.ntile_q = (int)((a.q_rows + T::kRows - 1) / T::kRows);
-  a.ntile_k = (int)((a.k_rows + T::kRows - 1) / T::kRows);
-  a.nblk_v = (int)(((long long)a.nbh_kv * (dm.L / 32) * (D / 2) + kThreadsQ - 1) / kThreadsQ);
+  a.tiles_per_head = (a.Lp + T::kRows - 1) / T::kRows;
+  a.ntile_q = a.nbh_q * a.tiles_per_head;
+  a.ntile_k = a.nbh_kv * a.tiles_per_head;
+  a.nblk_v = (int)(((long long)a.nbh_kv * (a.Lp / 32) * (D / 2) + kThreadsQ - 1) / kThreadsQ);
   a.nclu_mean = a.nbh_kv;
   a.nclu_v = (a.nblk_v + kMeanCluster - 1) / kMeanCluster;
   a.wait_ns = kWaitLimitNs;
@@ -451,7 +476,7 @@ cudaError_t static_scratch_address(float** out) {
 cudaError_t launch_quantize_static_scratch(const void* q, const void* k, const void* v, const Dims& dm,
                                            const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk,
                                            cudaStream_t s) {
-  const size_t need = (size_t)dm.B * dm.Hkv * (dm.L / kMeanChunk) * dm.d;
+  const size_t need = (size_t)dm.B * dm.Hkv * (padded_len(dm.L) / kMeanChunk) * dm.d;
   if (need > kStaticScratchFloats) return cudaErrorInvalidValue;
   float* part = nullptr;
   cudaError_t e = static_scratch_address(&part);

@@ -44,37 +44,57 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// bf16 Q and K as [rows][d] with boxes of 64 channels x 128 rows, 128B swizzle
-// (the tiles of both the BF16 attention kernel and the quantiser).
-bool make_bf16_row_maps(const void* q, const void* k, const Dims& dm, CUtensorMap* tq, CUtensorMap* tk) {
-  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  return make_map(tq, bf, q, dm.d, (uint64_t)dm.B * dm.H * dm.L, 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         make_map(tk, bf, k, dm.d, (uint64_t)dm.B * dm.Hkv * dm.L, 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+// bf16 [B*heads][L][d] as a 3-D map (channel, token, head) with boxes of 64
+// channels x 128 tokens x 1 head, 128B swizzle (the tiles of the BF16 attention
+// kernel and the quantiser): a tile that runs past the head's last token reads
+// zeros there instead of the next head's rows.
+bool make_bf16_head_map(CUtensorMap* m, const void* base, int heads, const Dims& dm) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)dm.d, (cuuint64_t)dm.L, (cuuint64_t)heads};
+  const cuuint64_t strides[2] = {(cuuint64_t)dm.d * 2, (cuuint64_t)dm.L * dm.d * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_bf16_row_maps(const void* q, const void* k, const Dims& dm, CUtensorMap* tq, CUtensorMap* tk) {
+  return make_bf16_head_map(tq, q, dm.B * dm.H, dm) && make_bf16_head_map(tk, k, dm.B * dm.Hkv, dm);
+}
+
+// SA_OK for a problem the kernels take, or the error to return.  Empty
+// problems (B == 0 or L == 0) pass here; the entry points return before
+// touching any pointer for them.
 sa_status check_dims(int B, int H, int Hkv, int L, int d) {
-  if (B <= 0 || H <= 0 || Hkv <= 0 || L <= 0 || d <= 0) return SA_ERR_INVALID_ARG;
+  if (B < 0 || H <= 0 || Hkv <= 0 || L < 0 || d <= 0) return SA_ERR_INVALID_ARG;
   if (H % Hkv != 0) return SA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return SA_ERR_UNSUPPORTED;
-  if (L % 128 != 0) return SA_ERR_UNSUPPORTED;
-  // TMA coordinates are 32-bit: every row index of Q/K/V (and d * B * Hkv) must fit.
-  if ((long long)B * H * L >= (1ll << 31) || (long long)B * Hkv * d >= (1ll << 31)) return SA_ERR_UNSUPPORTED;
+  // TMA coordinates are 32-bit: every row index of the padded layouts (and
+  // d * B * Hkv) must fit.
+  const long long Lp = ((long long)L + 127) / 128 * 128;
+  if ((long long)B * H * Lp >= (1ll << 31) || (long long)B * Hkv * d >= (1ll << 31)) return SA_ERR_UNSUPPORTED;
   if (H > 65535 || B > 65535) return SA_ERR_UNSUPPORTED;
   return SA_OK;
 }
 
+bool empty_problem(int B, int L) { return B == 0 || L == 0; }
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Every quantised layout has Lp = L rounded up to 128 token rows.
 void blob_sizes(int B, int H, int Hkv, int L, int d, size_t sz[8]) {
-  const size_t nq = (size_t)B * H * L, nk = (size_t)B * Hkv * L;
+  const int Lp = padded_len(L);
+  const size_t nq = (size_t)B * H * Lp, nk = (size_t)B * Hkv * Lp;
   sz[0] = nq * (d / 2);                             // q_codes
-  sz[1] = (size_t)B * H * (L / 128) * (d / 64) * 512;   // q_sf
+  sz[1] = (size_t)B * H * (Lp / 128) * (d / 64) * 512;   // q_sf
   sz[2] = nk * (d / 2);                             // k_codes
-  sz[3] = (size_t)B * Hkv * (L / 128) * (d / 64) * 512;
+  sz[3] = (size_t)B * Hkv * (Lp / 128) * (d / 64) * 512;
   sz[4] = nk * (d / 2);                             // v_codes (transposed)
-  sz[5] = (size_t)B * Hkv * (L / 64) * 512;         // v_sf
+  sz[5] = (size_t)B * Hkv * (Lp / 64) * 512;        // v_sf
   sz[6] = (size_t)B * Hkv * d * sizeof(float);      // k_mean
-  sz[7] = (size_t)B * Hkv * (L / 128) * d * sizeof(float);   // K-mean partial sums
+  sz[7] = (size_t)B * Hkv * (Lp / 128) * d * sizeof(float);   // K-mean partial sums
 }
 
 __global__ void wait_selftest_kernel(uint64_t limit_ns) {
@@ -111,7 +131,7 @@ const char* sa_status_string(sa_status s) {
 }
 
 size_t sa_fp4_qkv_bytes(int B, int H, int Hkv, int L, int d, size_t offsets_out[8]) {
-  if (check_dims(B, H, Hkv, L, d) != SA_OK) return 0;
+  if (check_dims(B, H, Hkv, L, d) != SA_OK || empty_problem(B, L)) return 0;
   size_t sz[8];
   blob_sizes(B, H, Hkv, L, d, sz);
   size_t off = 0;
@@ -125,7 +145,10 @@ size_t sa_fp4_qkv_bytes(int B, int H, int Hkv, int L, int d, size_t offsets_out[
 sa_status sa_fp4_qkv_from_blob(void* blob, int B, int H, int Hkv, int L, int d, sa_fp4_qkv* out) {
   if (!out || !blob || (reinterpret_cast<uintptr_t>(blob) & 255u)) return SA_ERR_INVALID_ARG;
   size_t off[8];
-  if (sa_fp4_qkv_bytes(B, H, Hkv, L, d, off) == 0) return check_dims(B, H, Hkv, L, d);
+  if (sa_fp4_qkv_bytes(B, H, Hkv, L, d, off) == 0) {
+    const sa_status st = check_dims(B, H, Hkv, L, d);
+    return st != SA_OK ? st : SA_ERR_INVALID_ARG;     // an empty problem has no blob
+  }
   uint8_t* p = static_cast<uint8_t*>(blob);
   out->q_codes = p + off[0];
   out->q_sf = p + off[1];
@@ -147,6 +170,7 @@ sa_status sa_quantize(const void* q, const void* k, const void* v, int B, int H,
                       const sa_fp4_qkv* out, sa_stream_t stream) {
   const sa_status st = check_dims(B, H, Hkv, L, d);
   if (st != SA_OK) return st;
+  if (empty_problem(B, L)) return SA_OK;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !fp4_ptrs_ok(out)) return SA_ERR_INVALID_ARG;
   const Dims dm{B, H, Hkv, L, d};
   CUtensorMap tq, tk;
@@ -160,7 +184,8 @@ sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v
                                      int d, const sa_fp4_qkv* out, sa_stream_t stream) {
   const sa_status st = check_dims(B, H, Hkv, L, d);
   if (st != SA_OK) return st;
-  if ((size_t)B * Hkv * (L / 128) * d > (size_t)SA_STATIC_SCRATCH_FLOATS) return SA_ERR_UNSUPPORTED;
+  if (empty_problem(B, L)) return SA_OK;
+  if ((size_t)B * Hkv * (padded_len(L) / 128) * d > (size_t)SA_STATIC_SCRATCH_FLOATS) return SA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !out || !aligned16(out->q_codes) ||
       !aligned16(out->q_sf) || !aligned16(out->k_codes) || !aligned16(out->k_sf) || !aligned16(out->v_codes) ||
       !aligned16(out->v_sf) || !aligned16(out->k_mean))
@@ -181,6 +206,8 @@ sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o, int 
   if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
   if (mode_flags & ~(0xF | SA_OUT_FP32)) return SA_ERR_INVALID_ARG;
   const int mode = mode_flags & 0xF;
+  if (mode != SA_MODE_BF16 && mode != SA_MODE_NVFP4) return SA_ERR_INVALID_ARG;
+  if (empty_problem(B, L)) return SA_OK;
   const bool out_f32 = (mode_flags & SA_OUT_FP32) != 0;
   if (!aligned16(o)) return SA_ERR_INVALID_ARG;
   const Dims dm{B, H, Hkv, L, d};
@@ -188,10 +215,8 @@ sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o, int 
   CUtensorMap tq, tk, tv;
   if (mode == SA_MODE_BF16) {
     if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return SA_ERR_INVALID_ARG;
-    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    if (!make_map(&tq, bf, q, d, (uint64_t)B * H * L, 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tk, bf, k, d, (uint64_t)B * Hkv * L, 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tv, bf, v, d, (uint64_t)B * Hkv * L, 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!make_bf16_head_map(&tq, q, B * H, dm) || !make_bf16_head_map(&tk, k, B * Hkv, dm) ||
+        !make_bf16_head_map(&tv, v, B * Hkv, dm))
       return SA_ERR_CUDA;
     return launch_attn_bf16(tq, tk, tv, o, dm, causal, out_f32, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
   }
@@ -203,9 +228,10 @@ sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o, int 
       return SA_ERR_INVALID_ARG;
     const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
     const CUtensorMapSwizzle qk_swz = d == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
-    if (!make_map(&tq, u8, x->q_codes, d / 2, (uint64_t)B * H * L, 1, d / 2, 128, qk_swz) ||
-        !make_map(&tk, u8, x->k_codes, d / 2, (uint64_t)B * Hkv * L, 1, d / 2, 128, qk_swz) ||
-        !make_map(&tv, u8, x->v_codes, L / 2, (uint64_t)B * Hkv * d, 1, 64, d, CU_TENSOR_MAP_SWIZZLE_64B))
+    const int Lp = padded_len(L);      // the quantised layouts hold whole 128-token tiles
+    if (!make_map(&tq, u8, x->q_codes, d / 2, (uint64_t)B * H * Lp, 1, d / 2, 128, qk_swz) ||
+        !make_map(&tk, u8, x->k_codes, d / 2, (uint64_t)B * Hkv * Lp, 1, d / 2, 128, qk_swz) ||
+        !make_map(&tv, u8, x->v_codes, Lp / 2, (uint64_t)B * Hkv * d, 1, 64, d, CU_TENSOR_MAP_SWIZZLE_64B))
       return SA_ERR_CUDA;
     return launch_attn_nvfp4(tq, tk, tv, *x, o, dm, causal, out_f32, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
   }

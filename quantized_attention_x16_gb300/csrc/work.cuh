@@ -27,7 +27,7 @@ struct AttnWork {
 // Host: the work list for a problem and the number of CTAs to launch.
 inline AttnWork make_attn_work(int B, int H, int L, int causal, int num_sms, int* ctas) {
   AttnWork w;
-  w.nqt = L / 128;
+  w.nqt = (L + 127) / 128;   // a ragged last tile counts as a tile
   w.ppr = (w.nqt + 1) / 2;
   w.nbh = B * H;
   w.causal = causal;

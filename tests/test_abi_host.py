@@ -58,8 +58,17 @@ def test_blob_layout_sizes(sa):
         nxt = off[i + 1] if i < 7 else n
         assert nxt - off[i] >= sizes[i]
         assert nxt - off[i] < sizes[i] + 256
-    assert sa.sa_fp4_qkv_bytes(1, 2, 2, 100, 64)[0] == 0          # L % 128 != 0
     assert sa.sa_fp4_qkv_bytes(1, 2, 2, 128, 96)[0] == 0          # unsupported d
+    assert sa.sa_fp4_qkv_bytes(0, 2, 2, 128, 64)[0] == 0          # empty problems have no blob
+    assert sa.sa_fp4_qkv_bytes(1, 2, 2, 0, 64)[0] == 0
+
+
+@pytest.mark.parametrize("L", [1, 100, 129, 200, 255])
+def test_blob_layout_pads_ragged_lengths_to_whole_tiles(sa, L):
+    # every quantised layout holds Lp = L rounded up to 128 tokens per head
+    B, H, Hkv, d = 1, 4, 2, 64
+    Lp = -(-L // 128) * 128
+    assert sa.sa_fp4_qkv_bytes(B, H, Hkv, L, d) == sa.sa_fp4_qkv_bytes(B, H, Hkv, Lp, d)
 
 
 def test_argument_errors_launch_nothing(sa):
@@ -70,9 +79,10 @@ def test_argument_errors_launch_nothing(sa):
     # (q, k, v, o, B, H, Hkv, L, d, causal, mode)
     cases = [
         ((p, p, p, p, 1, 2, 2, 256, 96, 0, 0), sa.SA_ERR_UNSUPPORTED),
-        ((p, p, p, p, 1, 2, 2, 200, 64, 0, 0), sa.SA_ERR_UNSUPPORTED),
         ((p, p, p, p, 1, 3, 2, 256, 64, 0, 0), sa.SA_ERR_INVALID_ARG),
-        ((p, p, p, p, 0, 2, 2, 256, 64, 0, 0), sa.SA_ERR_INVALID_ARG),
+        ((p, p, p, p, -1, 2, 2, 256, 64, 0, 0), sa.SA_ERR_INVALID_ARG),
+        ((p, p, p, p, 1, 2, 2, -5, 64, 0, 0), sa.SA_ERR_INVALID_ARG),
+        ((p, p, p, p, 1, 0, 2, 256, 64, 0, 0), sa.SA_ERR_INVALID_ARG),
         ((p, p, p, z, 1, 2, 2, 256, 64, 0, 0), sa.SA_ERR_INVALID_ARG),
         ((p, bad, p, p, 1, 2, 2, 256, 64, 0, 0), sa.SA_ERR_INVALID_ARG),
         ((p, p, p, p, 1, 2, 2, 256, 64, 2, 0), sa.SA_ERR_INVALID_ARG),
@@ -82,6 +92,15 @@ def test_argument_errors_launch_nothing(sa):
     ]
     for args, want in cases:
         assert lib.sa_attn_fwd(*args, None) == want, args
+    # empty problems (B == 0 or L == 0) succeed without touching any pointer
+    for B, L in [(0, 256), (2, 0)]:
+        for mode in (0, 1):
+            assert lib.sa_attn_fwd(z, z, z, z, B, 2, 2, L, 64, 0, mode, None) == sa.SA_OK
+        assert lib.sa_quantize(z, z, z, B, 2, 2, L, 64, None, None) == sa.SA_OK
+        assert lib.sa_quantize_static_scratch(z, z, z, B, 2, 2, L, 64, None, None) == sa.SA_OK
+        assert lib.sa_attn_fwd_host(z, z, z, z, B, 2, 2, L, 64, 0, 1, z, 0, 0, None) == sa.SA_OK
+        assert lib.sa_attn_fwd_host_workspace_bytes(B, 2, 2, L, 64, 1, 0) == 0
+    assert lib.sa_attn_fwd(z, z, z, z, 0, 2, 2, 256, 96, 0, 0, None) == sa.SA_ERR_UNSUPPORTED   # d still checked
     s = sa.SaFp4Qkv()
     assert lib.sa_quantize(p, p, p, 1, 2, 2, 256, 64, ctypes.byref(s), None) == sa.SA_ERR_INVALID_ARG
     assert lib.sa_quantize(p, p, p, 1, 2, 2, 256, 80, ctypes.byref(s), None) == sa.SA_ERR_UNSUPPORTED

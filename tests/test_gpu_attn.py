@@ -117,6 +117,12 @@ SMALL = [
     dict(W.spec("causal_gqa"), B=1, H=4, Hkv=2, L=384, seed=12),           # odd tile count, GQA, causal
     dict(W.spec("dit_video"), B=2, H=2, Hkv=1, L=640, d=64, seed=13),      # MQA, d=64, 5 tiles
     dict(W.spec("sweep_causal_d64_L1024"), H=2, Hkv=2, L=128, seed=14),     # a single tile
+    # ragged tails: the last tile is partial (keys past L masked, rows past L not stored)
+    dict(W.spec("llm_prefill"), B=1, H=2, Hkv=1, L=200, seed=15),           # 2 tiles, 72 in the last
+    dict(W.spec("causal_gqa"), B=1, H=4, Hkv=2, L=333, seed=16),            # causal, 3 tiles, 77 in the last
+    dict(W.spec("dit_video"), B=1, H=2, Hkv=2, L=77, d=64, seed=17),        # one partial tile, odd L
+    dict(W.spec("tiny"), B=1, H=2, Hkv=2, L=1, seed=18),                    # a single token: O = V
+    dict(W.spec("tiny"), B=2, H=2, Hkv=1, L=129, d=128, causal=True, seed=19),   # one key in the last tile
 ]
 
 

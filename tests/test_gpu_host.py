@@ -45,6 +45,7 @@ CASES = [
     dict(W.spec("causal_gqa"), B=2, H=6, Hkv=3, L=384, seed=21),          # 6 pairs, G = 2, causal
     dict(W.spec("llm_prefill"), B=3, H=1, Hkv=1, L=512, seed=22),         # 3 pairs: ragged last chunk
     dict(W.spec("dit_video"), B=1, H=4, Hkv=2, L=256, d=64, seed=23),     # d = 64
+    dict(W.spec("llm_prefill"), B=2, H=2, Hkv=2, L=300, seed=24),         # ragged L
 ]
 
 
@@ -95,8 +96,10 @@ def test_host_path_rejects_bad_arguments(sa):
         sa.SA_ERR_INVALID_ARG
     assert lib.sa_attn_fwd_host(p(hq), p(hk), p(hv), p(o), B, H, 1, L, d, 0, 1, p(ws), need - 256, 0, s) == \
         sa.SA_ERR_INVALID_ARG
+    assert lib.sa_attn_fwd_host(p(hq), p(hk), p(hv), p(o), B, H, 1, L, 96, 0, 1, p(ws), need, 0, s) == \
+        sa.SA_ERR_UNSUPPORTED                          # head dimension 96
     assert lib.sa_attn_fwd_host(p(hq), p(hk), p(hv), p(o), B, H, 1, L + 64, d, 0, 1, p(ws), need, 0, s) == \
-        sa.SA_ERR_UNSUPPORTED
+        sa.SA_ERR_INVALID_ARG                          # a longer (ragged) problem needs a larger workspace
     assert lib.sa_attn_fwd_host(p(hq), p(hk), p(hv), p(o), B, H, 1, L, d, 0, 7, p(ws), need, 0, s) == \
         sa.SA_ERR_INVALID_ARG
     torch.cuda.synchronize()

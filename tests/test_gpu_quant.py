@@ -32,9 +32,9 @@ def oracle_quant(x):
     qc, qs = quant.quantize_q(q)
     kc, ks = quant.quantize_k(k, mu)
     vc, vs = quant.quantize_v(v)
-    return dict(k_mean=mu, q_codes=layout.pack_nibbles(qc), q_sf=layout.pack_qk_scales(qs),
-                k_codes=layout.pack_nibbles(kc), k_sf=layout.pack_qk_scales(ks),
-                v_codes=layout.pack_nibbles(vc), v_sf=layout.pack_v_scales(vs))
+    return dict(k_mean=mu, q_codes=layout.pack_qk_codes(qc), q_sf=layout.pack_qk_scales(qs),
+                k_codes=layout.pack_qk_codes(kc), k_sf=layout.pack_qk_scales(ks),
+                v_codes=layout.pack_v_codes(vc), v_sf=layout.pack_v_scales(vs))
 
 
 def assert_same(g, o, names=None):
@@ -53,6 +53,12 @@ SMALL = [
     dict(W.spec("llm_prefill"), B=1, H=4, Hkv=2, L=512, seed=7),
     dict(W.spec("causal_gqa"), B=2, H=8, Hkv=2, L=384, d=64, seed=8),
     dict(W.spec("dit_video"), B=1, H=3, Hkv=3, L=256, seed=9),
+    # ragged lengths: partial last tile, partial last V group, a single token
+    dict(W.spec("llm_prefill"), B=2, H=4, Hkv=2, L=200, seed=40),
+    dict(W.spec("causal_gqa"), B=1, H=4, Hkv=1, L=333, d=64, seed=41),
+    dict(W.spec("dit_video"), B=1, H=2, Hkv=2, L=77, seed=42),
+    dict(W.spec("tiny"), B=1, H=1, Hkv=1, L=1, seed=43),
+    dict(W.spec("tiny"), B=1, H=2, Hkv=2, L=129, d=64, seed=44),
 ]
 
 

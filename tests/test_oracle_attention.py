@@ -105,11 +105,13 @@ def test_smooth_k_shift_invariance(causal):
     assert np.allclose(a, b, atol=1e-12)
 
 
+@pytest.mark.parametrize("L", [96, 100, 1])
 @pytest.mark.parametrize("bc", [16, 32, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_emulation_without_quantisers_is_exact(bc, causal):
+def test_emulation_without_quantisers_is_exact(bc, causal, L):
+    # ragged lengths included: a last tile narrower than bc (and than 16)
     rng = np.random.default_rng(8)
-    B, H, Hkv, L, d = 1, 4, 2, 96, 16
+    B, H, Hkv, d = 1, 4, 2, 16
     q = rng.standard_normal((B, H, L, d)) * 2
     k = rng.standard_normal((B, Hkv, L, d)) * 2
     v = rng.standard_normal((B, Hkv, L, d))

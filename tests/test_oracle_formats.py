@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import attention as A
 from oracle import formats, quant, layout
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
@@ -164,6 +165,53 @@ def test_v_groups_run_along_tokens():
     assert np.all(codes[0, 0, 3, :16] == 7) and scales[0, 0, 3, 0] == 0x38
     assert np.all(codes[0, 0, 3, 16:] == 0) and scales[0, 0, 3, 1] == 0
     assert np.all(scales[0, 0, :3] == 0)
+
+
+def test_v_groups_straddling_the_end_are_completed_with_zeros():
+    # L = 20: channel 5 holds 1..20 at tokens 0..19; group 1 = tokens 16..19
+    # and 12 missing tokens, which quantise as zeros
+    v = np.zeros((1, 1, 20, 16), np.float32)
+    v[0, 0, :, 5] = np.arange(1, 21, dtype=np.float32)
+    codes, scales = quant.quantize_v(v)
+    assert codes.shape == (1, 1, 16, 32) and scales.shape == (1, 1, 16, 2)
+    full = np.zeros((1, 1, 32, 16), np.float32)
+    full[0, 0, :20] = v[0, 0]
+    c2, s2 = quant.quantize_v(full)                     # the same values, explicitly padded
+    assert np.array_equal(codes, c2) and np.array_equal(scales, s2)
+    # group 1 of channel 5: max 20 -> s = 20/6 = 3.33 -> e4m3 3.25 (0x45); 17/3.25 = 5.23 -> 6 (code 0x7)
+    assert scales[0, 0, 5, 1] == 0x45 and codes[0, 0, 5, 16] == 0x7 and np.all(codes[0, 0, 5, 20:] == 0)
+    assert codes[0, 0, 5, 19] == 0x7 and codes[0, 0, 5, 18] == 0x7   # 20/3.25 = 6.15 (saturates), 19/3.25 = 5.85
+    # the dequantised operands drop the completion again
+    (qd, kd, vd), _ = A.dequantized_operands(np.zeros((1, 1, 20, 16), np.float32), v, v)
+    assert vd.shape == (1, 1, 20, 16)
+
+
+def test_ragged_k_mean_counts_only_real_tokens():
+    rng = np.random.default_rng(15)
+    k = rng.integers(-8, 8, (1, 2, 200, 16)).astype(np.float32)   # chunks of 128 and 72 tokens
+    mu = quant.k_mean(k)
+    assert np.array_equal(mu, (k.astype(np.float64).sum(2) / 200).astype(np.float32))
+
+
+@pytest.mark.parametrize("L", [1, 77, 128, 200])
+def test_padded_layout_of_ragged_lengths(L):
+    rng = np.random.default_rng(L)
+    Lp = layout.padded_len(L)
+    assert Lp % 128 == 0 and Lp - 128 < L <= Lp
+    codes = rng.integers(0, 16, (1, 2, L, 64)).astype(np.uint8)
+    packed = layout.pack_qk_codes(codes)
+    assert packed.shape == (1, 2, Lp, 32)
+    assert np.array_equal(layout.unpack_nibbles(packed)[:, :, :L], codes) and not packed[:, :, L:].any()
+    sc = rng.integers(1, 255, (1, 2, L, 4)).astype(np.uint8)
+    blk = layout.pack_qk_scales(sc)
+    assert blk.shape == (1, 2, Lp // 128, 1, 512) and np.count_nonzero(blk) == np.count_nonzero(sc)
+    L16 = -(-L // 16) * 16
+    vc = rng.integers(0, 16, (1, 1, 64, L16)).astype(np.uint8)
+    vp = layout.pack_v_codes(vc)
+    assert vp.shape == (1, 1, 64, Lp // 2) and not vp[..., L16 // 2:].any()
+    vs = rng.integers(1, 255, (1, 1, 64, L16 // 16)).astype(np.uint8)
+    vb = layout.pack_v_scales(vs)
+    assert vb.shape == (1, 1, Lp // 64, 512) and np.count_nonzero(vb) == vs.size
 
 
 def test_layout_nibbles_and_scale_blocks():
