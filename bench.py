@@ -167,13 +167,18 @@ def run_ours(args, rank, world, local_rank):
     fl = W.flops(w)
     causal = w["causal"]
 
+    # split-KV when the library chooses it (problems too small to fill the
+    # SMs); the workspace is allocated once, outside the timed region
+    nsplit_ws = sa.sa_attn_fwd_workspace_bytes(B, H, Hkv, L, d, causal, "nvfp4", 0)
+    ws = torch.empty(max(nsplit_ws, 16), dtype=torch.uint8, device=dev)
+
     def step(ev):
         ev[0].record()
         sa.sa_quantize(q, k, v, out=fq)
         ev[1].record()
-        sa.sa_attn_fwd(fq, o=o4, causal=causal, mode="nvfp4")
+        sa.sa_attn_fwd(fq, o=o4, causal=causal, mode="nvfp4", nsplit=0, workspace=ws)
         ev[2].record()
-        sa.sa_attn_fwd(q, k, v, o=o16, causal=causal, mode="bf16")
+        sa.sa_attn_fwd(q, k, v, o=o16, causal=causal, mode="bf16", nsplit=0, workspace=ws)
         ev[3].record()
 
     for _ in range(args.warmup):
@@ -195,7 +200,8 @@ def run_ours(args, rank, world, local_rank):
         wall = time.perf_counter() - t0
     if world > 1:
         dist.barrier()
-    launches = args.steps * (2 + 1 + 1)      # sa_quantize: 2 kernels; each attention call: 1
+    # sa_quantize: 2 kernels; each attention call: 1, plus the combine kernel when split
+    launches = args.steps * (2 + 2 * (2 if nsplit_ws > 0 else 1))
     tq = [a[0].elapsed_time(a[1]) * 1e-3 for a in evs]
     t4 = [a[1].elapsed_time(a[2]) * 1e-3 for a in evs]
     t16 = [a[2].elapsed_time(a[3]) * 1e-3 for a in evs]
@@ -263,7 +269,9 @@ def run_ours(args, rank, world, local_rank):
                    "B": B, "H": H, "Hkv": Hkv, "L": L, "d": d, "causal": causal,
                    "l2": "flushed by a 256 MB write before every step",
                    "value_def": "4*B*H*L^2*d / (sa_quantize + NVFP4 sa_attn_fwd) per GPU, summed over GPUs",
-                   "parallelism": f"independent batch per GPU ({world} GPU)"},
+                   "parallelism": f"independent batch per GPU ({world} GPU)",
+                   "split_kv": "library choice (sa_attn_fwd_ws, nsplit=0): "
+                               + ("split" if nsplit_ws > 0 else "no split for this size")},
         "paths": {
             "nvfp4_attn_only_tops": a4,
             "nvfp4_attn_us": t_4 * 1e6,

@@ -176,6 +176,33 @@ sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o,
                       int mode, sa_stream_t stream);
 
 /*
+ * Split-KV ("FlashAttention kernels": the online-softmax rescaling that merges
+ * tiles also merges independent shares of the key range).  When the (batch,
+ * head, pair of query tiles) units alone cannot fill the GPU, each unit's key
+ * tiles are cut into nsplit contiguous shares computed by separate CTAs, and
+ * a combine kernel merges the shares' partial results (unnormalised O, row
+ * maximum, row sum) into O.  Shares are whole 128-key tiles, so the P
+ * quantisation is unchanged and only the float32 summation order differs
+ * from the unsplit call.
+ *
+ * sa_attn_fwd_workspace_bytes: device workspace bytes sa_attn_fwd_ws needs
+ *   for the given sizes and `nsplit` (0 = the library's choice: split only
+ *   while the units leave at least half of the SMs idle and every share keeps
+ *   16 key tiles or more, at most 16 shares; 1 = no split; n > 1 = n shares,
+ *   at most one per key tile).  0 when no split would be used, or for invalid or
+ *   empty sizes.  causal and mode do not change the size.
+ * sa_attn_fwd_ws: sa_attn_fwd with split-KV.  Arguments as sa_attn_fwd, plus
+ *   nsplit as above and a caller-owned, 16-byte aligned device workspace of
+ *   workspace_bytes.  With nsplit 0 a missing or short workspace means no
+ *   split; with nsplit > 1 it is SA_ERR_INVALID_ARG.  Enqueues the attention
+ *   kernel and, when split, the combine kernel, on `stream`.
+ */
+size_t sa_attn_fwd_workspace_bytes(int B, int H, int Hkv, int L, int d, int causal, int mode, int nsplit);
+sa_status sa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o,
+                         int B, int H, int Hkv, int L, int d, int causal, int mode, int nsplit,
+                         void* workspace, size_t workspace_bytes, sa_stream_t stream);
+
+/*
  * sa_attn_fwd_host -- the path of sa_attn_fwd (mode SA_MODE_NVFP4:
  * sa_quantize then the FP4 attention; SA_MODE_BF16: the BF16 attention) on
  * bf16 BHLD Q, K, V in pinned HOST memory, writing O to pinned host memory.

@@ -30,6 +30,7 @@ SA_OUT_FP32 = 16
 
 #: every symbol include/sa.h declares
 EXPORTS = ("sa_fp4_qkv_bytes", "sa_fp4_qkv_from_blob", "sa_quantize", "sa_quantize_static_scratch", "sa_attn_fwd",
+           "sa_attn_fwd_workspace_bytes", "sa_attn_fwd_ws",
            "sa_attn_fwd_host_workspace_bytes", "sa_attn_fwd_host",
            "sa_status_string", "sa_last_device_error", "sa_selftest_wait_timeout", "sa_version")
 SA_STATIC_SCRATCH_FLOATS = 1 << 20
@@ -57,6 +58,10 @@ def _load():
     lib.sa_quantize_static_scratch.restype = i
     lib.sa_attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.sa_attn_fwd.restype = i
+    lib.sa_attn_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+    lib.sa_attn_fwd_workspace_bytes.restype = sz
+    lib.sa_attn_fwd_ws.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp, sz, vp]
+    lib.sa_attn_fwd_ws.restype = i
     lib.sa_attn_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
     lib.sa_attn_fwd_host_workspace_bytes.restype = sz
     lib.sa_attn_fwd_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, sz, i, vp]
@@ -181,10 +186,19 @@ def sa_quantize_static_scratch(q, k, v, out=None, stream=None):
     return out
 
 
-def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=None, stream=None):
+def sa_attn_fwd_workspace_bytes(B, H, Hkv, L, d, causal=False, mode="bf16", nsplit=0):
+    m = {"bf16": SA_MODE_BF16, "nvfp4": SA_MODE_NVFP4}[mode]
+    return int(lib.sa_attn_fwd_workspace_bytes(B, H, Hkv, L, d, int(bool(causal)), m, int(nsplit)))
+
+
+def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=None, stream=None,
+                nsplit=None, workspace=None):
     """Fused attention forward.  mode "bf16": q, k, v bf16 BHLD tensors.
     mode "nvfp4": q is an FP4QKV from sa_quantize, k and v None.
-    out_dtype: torch.bfloat16 (default) or torch.float32 (SA_OUT_FP32).  Returns o."""
+    out_dtype: torch.bfloat16 (default) or torch.float32 (SA_OUT_FP32).
+    nsplit None: sa_attn_fwd (no split-KV); otherwise sa_attn_fwd_ws with that
+    nsplit (0 = the library's choice) and `workspace` (a uint8 CUDA tensor,
+    allocated here when None).  Returns o."""
     import torch
     if mode == "bf16":
         _bf16_cuda(q, "q"), _bf16_cuda(k, "k"), _bf16_cuda(v, "v")
@@ -212,8 +226,16 @@ def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=
         o = torch.empty((B, H, L, d), dtype=out_dtype, device=dev)
     if not (o.is_cuda and o.dtype == out_dtype and o.is_contiguous() and tuple(o.shape) == (B, H, L, d)):
         raise ValueError("o must be a contiguous CUDA tensor of shape (B, H, L, d) and dtype out_dtype")
-    _check(lib.sa_attn_fwd(*args, _ptr(o), B, H, Hkv, L, d, int(bool(causal)), m, _stream(stream)),
-           "sa_attn_fwd")
+    if nsplit is None:
+        _check(lib.sa_attn_fwd(*args, _ptr(o), B, H, Hkv, L, d, int(bool(causal)), m, _stream(stream)),
+               "sa_attn_fwd")
+        return o
+    need = int(lib.sa_attn_fwd_workspace_bytes(B, H, Hkv, L, d, int(bool(causal)), m & 0xF, int(nsplit)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws, nbytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel())
+    _check(lib.sa_attn_fwd_ws(*args, _ptr(o), B, H, Hkv, L, d, int(bool(causal)), m, int(nsplit), ws, nbytes,
+                              _stream(stream)), "sa_attn_fwd_ws")
     return o
 
 

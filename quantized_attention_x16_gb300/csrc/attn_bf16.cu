@@ -83,7 +83,7 @@ template <int D, bool OUT32>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, void* __restrict__ out_ptr, int H, int Hkv,
-                     int L, int causal, const AttnWork work, uint64_t wait_ns) {
+                     int L, int causal, const AttnWork work, const SplitOut part, uint64_t wait_ns) {
   using C = CfgBF16<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -103,8 +103,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  int bh, qt0, nqu;
-  attn_unit(work, (int)blockIdx.x, bh, qt0, nqu);                  // this CTA's query tiles
+  int bh, qt0, nqu, sp;
+  attn_unit(work, (int)blockIdx.x, bh, qt0, nqu, sp);              // this CTA's query tiles and split
   const int h = bh % H, b = bh / H;
   const int hk = h / (H / Hkv);
   const bool q1_valid = nqu == 2;
@@ -112,6 +112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkt = (L + BN - 1) / BN;                // key tiles; a ragged last one is zero-filled past L
   ntq[0] = causal ? qt0 + 1 : nkt;
   ntq[1] = q1_valid ? (causal ? qt0 + 2 : nkt) : 0;
+  // key tiles [jb, jb + ntq[q]) of this CTA; loop indices below count from jb
+  const int jb = work.nsplit > 1 ? split_range(sp, work.nsplit, ntq) : 0;
   const int nt = ntq[0] > ntq[1] ? ntq[0] : ntq[1];
 
   if (threadIdx.x == 0) {
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nt; ++j) {
         const int s = j % C::NS;
         const uint32_t par = ((j / C::NS) - 1) & 1;
-        const int y = j * BN;
+        const int y = (jb + j) * BN;
         if (j >= C::NS && !mbar_wait_backoff_warp(bars.k_empty + s, par, abort_flag, wait_ns, kProducerSleepNs)) break;
         if (leader) {
           mbar_arrive_expect_tx(bars.k_full + s, C::kTileBytes);
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
       // keys this row may not see: past the diagonal (causal) and past L (the
       // zero fill of a ragged last tile)
-      const int lim = min(causal && j == qt ? r + 1 : BN, L - j * BN);
+      const int lim = min(causal && jb + j == qt ? r + 1 : BN, L - (jb + j) * BN);
       if (lim < BN) {
 #pragma unroll
         for (int i = 0; i < 128; ++i)
@@ -366,17 +368,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bars.p_full + q);
     }
     // ---- epilogue: O / l
+    const bool row_in = qt * BM + r < L;                // rows past L (a ragged last tile) are not stored
+    // split-KV: this CTA's partial result of the row -- O unnormalised (in
+    // units of 2^m_use, as is l), m_use (-inf if no key was visible) and l --
+    // goes to split sp's slot; a combine pass forms O
+    const bool split = work.nsplit > 1;
+    const long long prow = ((long long)sp * work.nbh + bhq) * padded_len_dev(L) + (long long)qt * BM + r;
+    if (split && ok && ntq[q] == 0 && (q == 0 || q1_valid) && row_in)
+      *reinterpret_cast<float2*>(part.ml + 2 * prow) = make_float2(-INFINITY, 0.f);
     if (ok && ntq[q] > 0 && mbar_wait_warp(bars.o_done + q, (ntq[q] - 1) & 1, abort_flag, wait_ns)) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       const long long obase = (q_row0 + (long long)qt * BM + r) * D;
-      const bool row_in = qt * BM + r < L;              // rows past L (a ragged last tile) are not stored
+      if (split && row_in) *reinterpret_cast<float2*>(part.ml + 2 * prow) = make_float2(m_use, l);
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         tmem_ld32(lane_addr + ocol + 32 * cc, o);
         tmem_ld_wait(o);
         if (!row_in) continue;
+        if (split) {
+          float4* dst = reinterpret_cast<float4*>(part.o + prow * D + 32 * cc);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                 __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+          continue;
+        }
         if constexpr (OUT32) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_ptr) + obase + 32 * cc);
 #pragma unroll
@@ -406,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool OUT32>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o, const Dims& dm,
-                     int causal, cudaStream_t s) {
+                     int causal, int nsplit, const SplitOut& part, cudaStream_t s) {
   using C = CfgBF16<D>;
   static bool attr_done = false;   // the attribute is a property of the function, set once per process
   if (!attr_done) {
@@ -422,20 +440,23 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     attr_done = true;
   }
   int ctas = 0;
-  const AttnWork work = make_attn_work(dm.B, dm.H, dm.L, causal, device_sm_count(), &ctas);
+  const AttnWork work = make_attn_work(dm.B, dm.H, dm.L, causal, device_sm_count(), &ctas, nsplit);
   attn_bf16_kernel<D, OUT32><<<ctas, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, o, dm.H, dm.Hkv, dm.L, causal,
-                                                                    work, kWaitLimitNs);
-  return cudaGetLastError();
+                                                                    work, part, kWaitLimitNs);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess && work.nsplit > 1) e = launch_splitkv_combine(part, work.nsplit, dm, o, OUT32, s);
+  return e;
 }
 
 }  // namespace
 
 cudaError_t launch_attn_bf16(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o,
-                             const Dims& dm, int causal, bool out_f32, cudaStream_t s) {
-  if (dm.d == 64) return out_f32 ? launch_d<64, true>(tq, tk, tv, o, dm, causal, s)
-                                 : launch_d<64, false>(tq, tk, tv, o, dm, causal, s);
-  return out_f32 ? launch_d<128, true>(tq, tk, tv, o, dm, causal, s)
-                 : launch_d<128, false>(tq, tk, tv, o, dm, causal, s);
+                             const Dims& dm, int causal, bool out_f32, int nsplit, const SplitOut& part,
+                             cudaStream_t s) {
+  if (dm.d == 64) return out_f32 ? launch_d<64, true>(tq, tk, tv, o, dm, causal, nsplit, part, s)
+                                 : launch_d<64, false>(tq, tk, tv, o, dm, causal, nsplit, part, s);
+  return out_f32 ? launch_d<128, true>(tq, tk, tv, o, dm, causal, nsplit, part, s)
+                 : launch_d<128, false>(tq, tk, tv, o, dm, causal, nsplit, part, s);
 }
 
 cudaError_t attn_bf16_read_error(int* out) { return read_and_clear_device_error(out); }

@@ -124,7 +124,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const uint8_t* __restrict__ q_sf,
                       const uint8_t* __restrict__ k_sf, const uint8_t* __restrict__ v_sf,
-                      void* __restrict__ out_ptr, int H, int Hkv, int L, int causal, const AttnWork work, uint64_t wait_ns) {
+                      void* __restrict__ out_ptr, int H, int Hkv, int L, int causal, const AttnWork work,
+                      const SplitOut part, uint64_t wait_ns) {
   using C = CfgF4<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -144,8 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  int bh, qt0, nqu;
-  attn_unit(work, (int)blockIdx.x, bh, qt0, nqu);                  // this CTA's query tiles
+  int bh, qt0, nqu, sp;
+  attn_unit(work, (int)blockIdx.x, bh, qt0, nqu, sp);              // this CTA's query tiles and split
   const int h = bh % H, b = bh / H;
   const int hk = h / (H / Hkv);
   const bool q1_valid = nqu == 2;
@@ -154,6 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Lp = (L + 127) & ~127;
   ntq[0] = causal ? qt0 + 1 : Lp / BN;
   ntq[1] = q1_valid ? (causal ? qt0 + 2 : Lp / BN) : 0;
+  // key tiles [jb, jb + ntq[q]) of this CTA; loop indices below count from jb
+  const int jb = work.nsplit > 1 ? split_range(sp, work.nsplit, ntq) : 0;
   const int nt = ntq[0] > ntq[1] ? ntq[0] : ntq[1];
 
   if (threadIdx.x == 0) {
@@ -210,8 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) {
           mbar_arrive_expect_tx(bars.k_full + s, C::kKBytes + C::kKSfBytes);
           tma_load_2d(smem + C::kOffK + s * C::kKBytes, &tmap_k, bars.k_full + s, 0,
-                      (int)(bhk * Lp + (long long)j * BN));
-          bulk_load(smem + C::kOffKSf + s * C::kKSfBytes, k_sf + (bhk * (Lp / 128) + j) * C::kKSfBytes,
+                      (int)(bhk * Lp + (long long)(jb + j) * BN));
+          bulk_load(smem + C::kOffKSf + s * C::kKSfBytes, k_sf + (bhk * (Lp / 128) + jb + j) * C::kKSfBytes,
                     C::kKSfBytes, bars.k_full + s);
         }
         if (j >= C::NS && !mbar_wait_backoff_warp(bars.v_empty + s, par, abort_flag, wait_ns, kProducerSleepNs)) {
@@ -220,8 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (leader) {
           mbar_arrive_expect_tx(bars.v_full + s, C::kVBytes + C::kVSfBytes);
-          tma_load_2d(smem + C::kOffV + s * C::kVBytes, &tmap_v, bars.v_full + s, j * (BN / 2), (int)(bhk * D));
-          bulk_load(smem + C::kOffVSf + s * C::kVSfBytes, v_sf + (bhk * (Lp / 64) + 2 * j) * 512, C::kVSfBytes,
+          tma_load_2d(smem + C::kOffV + s * C::kVBytes, &tmap_v, bars.v_full + s, (jb + j) * (BN / 2),
+                      (int)(bhk * D));
+          bulk_load(smem + C::kOffVSf + s * C::kVSfBytes, v_sf + (bhk * (Lp / 64) + 2 * (jb + j)) * 512, C::kVSfBytes,
                     bars.v_full + s);
         }
         issued = 2 * j + 2;
@@ -246,7 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tS = tbase + C::kColS;
       int last_q = -1, last_j = 0;
       bool ok = mbar_wait_warp(bars.q_full, 0, abort_flag, wait_ns);
-      if (ok) {
+      // (an empty split issues no MMA, and so no copy whose completion a
+      // commit would have to cover)
+      if (ok && nt > 0) {
         tc_fence_after();
         if (leader) {
           copy_sf(tbase + C::kColSfQ0, sb + C::kOffQSf, D / 64);
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
       // keys this row may not see: past the diagonal (causal) and past L (the
       // zero padding of a ragged last tile)
-      const int lim = min(causal && j == qt ? r + 1 : BN, L - j * BN);
+      const int lim = min(causal && jb + j == qt ? r + 1 : BN, L - (jb + j) * BN);
       if (lim < BN) {
 #pragma unroll
         for (int i = 0; i < 128; ++i)
@@ -484,17 +490,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bars.p_full + q);
     }
+    const bool row_in = qt * BM + r < L;                // rows of the padding are not stored
+    // split-KV: this CTA's partial result of the row -- O unnormalised (in
+    // units of 2^m_ref / 2688, as is lam), m_ref (-inf if no key tile was
+    // live) and lam -- goes to split sp's slot; a combine pass forms O
+    const bool split = work.nsplit > 1;
+    const long long prow = ((long long)sp * work.nbh + bhq) * Lp + (long long)qt * BM + r;
+    if (split && ok && ntq[q] == 0 && (q == 0 || q1_valid) && row_in)
+      *reinterpret_cast<float2*>(part.ml + 2 * prow) = make_float2(-INFINITY, 0.f);
     if (ok && ntq[q] > 0 && mbar_wait_warp(bars.o_done + q, (ntq[q] - 1) & 1, abort_flag, wait_ns)) {
       tc_fence_after();
       const float inv_l = 1.f / lam;
       const long long obase = (bhq * L + (long long)qt * BM + r) * D;
-      const bool row_in = qt * BM + r < L;              // rows of the padding are not stored
+      if (split && row_in)
+        *reinterpret_cast<float2*>(part.ml + 2 * prow) = make_float2(have_ref ? m_ref : -INFINITY, lam);
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         tmem_ld32(lane_addr + ocol + 32 * cc, o);
         tmem_ld_wait(o);
         if (!row_in) continue;
+        if (split) {
+          float4* dst = reinterpret_cast<float4*>(part.o + prow * D + 32 * cc);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                 __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+          continue;
+        }
         if constexpr (OUT32) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_ptr) + obase + 32 * cc);
 #pragma unroll
@@ -524,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool OUT32>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const sa_fp4_qkv& x,
-                     void* o, const Dims& dm, int causal, cudaStream_t s) {
+                     void* o, const Dims& dm, int causal, int nsplit, const SplitOut& part, cudaStream_t s) {
   using C = CfgF4<D>;
   static bool attr_done = false;
   if (!attr_done) {
@@ -540,22 +563,24 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     attr_done = true;
   }
   int ctas = 0;
-  const AttnWork work = make_attn_work(dm.B, dm.H, dm.L, causal, device_sm_count(), &ctas);
+  const AttnWork work = make_attn_work(dm.B, dm.H, dm.L, causal, device_sm_count(), &ctas, nsplit);
   attn_nvfp4_kernel<D, OUT32><<<ctas, kThreads, C::kSmemBytes, s>>>(
       tq, tk, tv, static_cast<const uint8_t*>(x.q_sf), static_cast<const uint8_t*>(x.k_sf),
-      static_cast<const uint8_t*>(x.v_sf), o, dm.H, dm.Hkv, dm.L, causal, work, kWaitLimitNs);
-  return cudaGetLastError();
+      static_cast<const uint8_t*>(x.v_sf), o, dm.H, dm.Hkv, dm.L, causal, work, part, kWaitLimitNs);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess && work.nsplit > 1) e = launch_splitkv_combine(part, work.nsplit, dm, o, OUT32, s);
+  return e;
 }
 
 }  // namespace
 
 cudaError_t launch_attn_nvfp4(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const sa_fp4_qkv& qkv, void* o, const Dims& dm, int causal, bool out_f32,
-                              cudaStream_t s) {
-  if (dm.d == 64) return out_f32 ? launch_d<64, true>(tq, tk, tv, qkv, o, dm, causal, s)
-                                 : launch_d<64, false>(tq, tk, tv, qkv, o, dm, causal, s);
-  return out_f32 ? launch_d<128, true>(tq, tk, tv, qkv, o, dm, causal, s)
-                 : launch_d<128, false>(tq, tk, tv, qkv, o, dm, causal, s);
+                              const sa_fp4_qkv& qkv, void* o, const Dims& dm, int causal, bool out_f32, int nsplit,
+                              const SplitOut& part, cudaStream_t s) {
+  if (dm.d == 64) return out_f32 ? launch_d<64, true>(tq, tk, tv, qkv, o, dm, causal, nsplit, part, s)
+                                 : launch_d<64, false>(tq, tk, tv, qkv, o, dm, causal, nsplit, part, s);
+  return out_f32 ? launch_d<128, true>(tq, tk, tv, qkv, o, dm, causal, nsplit, part, s)
+                 : launch_d<128, false>(tq, tk, tv, qkv, o, dm, causal, nsplit, part, s);
 }
 
 cudaError_t attn_nvfp4_read_error(int* out) { return read_and_clear_device_error(out); }

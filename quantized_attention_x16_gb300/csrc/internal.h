@@ -42,13 +42,34 @@ cudaError_t launch_quantize_static_scratch(const void* q, const void* k, const v
                                            const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk,
                                            cudaStream_t s);
 
+// Split-KV partial results (device, caller's workspace): for split s and
+// padded row R = (b*H + h)*Lp + t, the unnormalised O row at o + (s*rows + R)*d
+// and (m, l) at ml + 2*(s*rows + R), rows = B*H*Lp.  Unused with nsplit 1.
+struct SplitOut {
+  float* o;
+  float* ml;
+};
+inline size_t splitkv_workspace_bytes(const Dims& dm, int nsplit) {
+  const size_t rows = (size_t)dm.B * dm.H * padded_len(dm.L);
+  return nsplit > 1 ? (size_t)nsplit * rows * ((size_t)dm.d + 2) * sizeof(float) : 0;
+}
+inline SplitOut splitkv_layout(void* ws, const Dims& dm, int nsplit) {
+  const size_t rows = (size_t)dm.B * dm.H * padded_len(dm.L);
+  float* f = static_cast<float*>(ws);
+  return SplitOut{f, f + (size_t)nsplit * rows * dm.d};
+}
+
 // attn_bf16.cu
 cudaError_t launch_attn_bf16(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o,
-                             const Dims& dm, int causal, bool out_f32, cudaStream_t s);
+                             const Dims& dm, int causal, bool out_f32, int nsplit, const SplitOut& part,
+                             cudaStream_t s);
 // attn_nvfp4.cu
 cudaError_t launch_attn_nvfp4(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const sa_fp4_qkv& qkv, void* o, const Dims& dm, int causal, bool out_f32,
-                              cudaStream_t s);
+                              int nsplit, const SplitOut& part, cudaStream_t s);
+// splitkv.cu: O from the nsplit partial results of every row t < L.
+cudaError_t launch_splitkv_combine(const SplitOut& part, int nsplit, const Dims& dm, void* o, bool out_f32,
+                                   cudaStream_t s);
 
 // Per-unit readers of the device error word (each clears its word).
 cudaError_t attn_bf16_read_error(int* out);

@@ -8,6 +8,7 @@
 
 #include "internal.h"
 #include "sm100.cuh"
+#include "work.cuh"
 
 namespace sa {
 namespace {
@@ -199,18 +200,36 @@ sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v
              : SA_ERR_CUDA;
 }
 
-sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int L, int d,
-                      int causal, int mode_flags, sa_stream_t stream) {
+// Splits for split-KV: `requested` 0 = the library's choice, 1 = none, n > 1 =
+// n (at most one per key tile of the longest query tile's range).
+static int resolve_nsplit(int B, int H, int L, int requested) {
+  if (requested == 1) return 1;
+  if (requested == 0) return choose_nsplit(B, H, L, device_sm_count());
+  const int nkt = (L + 127) / 128;
+  return requested < nkt ? requested : nkt;
+}
+
+static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int L,
+                               int d, int causal, int mode_flags, int nsplit_req, void* workspace,
+                               size_t workspace_bytes, sa_stream_t stream) {
   const sa_status st = check_dims(B, H, Hkv, L, d);
   if (st != SA_OK) return st;
   if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
   if (mode_flags & ~(0xF | SA_OUT_FP32)) return SA_ERR_INVALID_ARG;
   const int mode = mode_flags & 0xF;
   if (mode != SA_MODE_BF16 && mode != SA_MODE_NVFP4) return SA_ERR_INVALID_ARG;
+  if (nsplit_req < 0) return SA_ERR_INVALID_ARG;
   if (empty_problem(B, L)) return SA_OK;
   const bool out_f32 = (mode_flags & SA_OUT_FP32) != 0;
   if (!aligned16(o)) return SA_ERR_INVALID_ARG;
   const Dims dm{B, H, Hkv, L, d};
+  // split-KV only with a workspace large enough for the partial results
+  int nsplit = resolve_nsplit(B, H, L, nsplit_req);
+  if (nsplit > 1 && nsplit_req > 1 && (workspace == nullptr || workspace_bytes < splitkv_workspace_bytes(dm, nsplit)))
+    return SA_ERR_INVALID_ARG;
+  if (nsplit > 1 && (workspace == nullptr || workspace_bytes < splitkv_workspace_bytes(dm, nsplit))) nsplit = 1;
+  if (nsplit > 1 && !aligned16(workspace)) return SA_ERR_INVALID_ARG;
+  const SplitOut part = nsplit > 1 ? splitkv_layout(workspace, dm, nsplit) : SplitOut{nullptr, nullptr};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   CUtensorMap tq, tk, tv;
   if (mode == SA_MODE_BF16) {
@@ -218,24 +237,42 @@ sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o, int 
     if (!make_bf16_head_map(&tq, q, B * H, dm) || !make_bf16_head_map(&tk, k, B * Hkv, dm) ||
         !make_bf16_head_map(&tv, v, B * Hkv, dm))
       return SA_ERR_CUDA;
-    return launch_attn_bf16(tq, tk, tv, o, dm, causal, out_f32, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+    return launch_attn_bf16(tq, tk, tv, o, dm, causal, out_f32, nsplit, part, s) == cudaSuccess ? SA_OK
+                                                                                                : SA_ERR_CUDA;
   }
-  if (mode == SA_MODE_NVFP4) {
-    if (k != nullptr || v != nullptr || q == nullptr) return SA_ERR_INVALID_ARG;
-    const sa_fp4_qkv* x = static_cast<const sa_fp4_qkv*>(q);
-    if (!aligned16(x->q_codes) || !aligned16(x->q_sf) || !aligned16(x->k_codes) || !aligned16(x->k_sf) ||
-        !aligned16(x->v_codes) || !aligned16(x->v_sf))
-      return SA_ERR_INVALID_ARG;
-    const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    const CUtensorMapSwizzle qk_swz = d == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
-    const int Lp = padded_len(L);      // the quantised layouts hold whole 128-token tiles
-    if (!make_map(&tq, u8, x->q_codes, d / 2, (uint64_t)B * H * Lp, 1, d / 2, 128, qk_swz) ||
-        !make_map(&tk, u8, x->k_codes, d / 2, (uint64_t)B * Hkv * Lp, 1, d / 2, 128, qk_swz) ||
-        !make_map(&tv, u8, x->v_codes, Lp / 2, (uint64_t)B * Hkv * d, 1, 64, d, CU_TENSOR_MAP_SWIZZLE_64B))
-      return SA_ERR_CUDA;
-    return launch_attn_nvfp4(tq, tk, tv, *x, o, dm, causal, out_f32, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
-  }
-  return SA_ERR_INVALID_ARG;
+  if (k != nullptr || v != nullptr || q == nullptr) return SA_ERR_INVALID_ARG;
+  const sa_fp4_qkv* x = static_cast<const sa_fp4_qkv*>(q);
+  if (!aligned16(x->q_codes) || !aligned16(x->q_sf) || !aligned16(x->k_codes) || !aligned16(x->k_sf) ||
+      !aligned16(x->v_codes) || !aligned16(x->v_sf))
+    return SA_ERR_INVALID_ARG;
+  const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUtensorMapSwizzle qk_swz = d == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  const int Lp = padded_len(L);      // the quantised layouts hold whole 128-token tiles
+  if (!make_map(&tq, u8, x->q_codes, d / 2, (uint64_t)B * H * Lp, 1, d / 2, 128, qk_swz) ||
+      !make_map(&tk, u8, x->k_codes, d / 2, (uint64_t)B * Hkv * Lp, 1, d / 2, 128, qk_swz) ||
+      !make_map(&tv, u8, x->v_codes, Lp / 2, (uint64_t)B * Hkv * d, 1, 64, d, CU_TENSOR_MAP_SWIZZLE_64B))
+    return SA_ERR_CUDA;
+  return launch_attn_nvfp4(tq, tk, tv, *x, o, dm, causal, out_f32, nsplit, part, s) == cudaSuccess ? SA_OK
+                                                                                                  : SA_ERR_CUDA;
+}
+
+sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int L, int d,
+                      int causal, int mode_flags, sa_stream_t stream) {
+  return attn_fwd_impl(q, k, v, o, B, H, Hkv, L, d, causal, mode_flags, 1, nullptr, 0, stream);
+}
+
+size_t sa_attn_fwd_workspace_bytes(int B, int H, int Hkv, int L, int d, int causal, int mode, int nsplit) {
+  (void)causal;
+  (void)mode;
+  if (check_dims(B, H, Hkv, L, d) != SA_OK || empty_problem(B, L) || nsplit < 0) return 0;
+  const Dims dm{B, H, Hkv, L, d};
+  return splitkv_workspace_bytes(dm, resolve_nsplit(B, H, L, nsplit));
+}
+
+sa_status sa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int L, int d,
+                         int causal, int mode, int nsplit, void* workspace, size_t workspace_bytes,
+                         sa_stream_t stream) {
+  return attn_fwd_impl(q, k, v, o, B, H, Hkv, L, d, causal, mode, nsplit, workspace, workspace_bytes, stream);
 }
 
 sa_status sa_last_device_error(void) {

@@ -1,0 +1,84 @@
+// splitkv.cu -- the combine pass of split-KV attention.
+//
+// With split-KV each CTA of an attention kernel covers a contiguous share of
+// a query tile's key tiles (online softmax, "FlashAttention kernels",
+// sections 0-1) and leaves, per row, its unnormalised accumulator a_s, its row
+// sum l_s -- both in units of 2^m_s for the split's own reference maximum m_s
+// (log2 units; -inf when no key of the share was visible) -- instead of O.
+// Merging the shares is the online-softmax rescaling step applied once more:
+//   M = max_s m_s,  O = sum_s 2^(m_s - M) a_s / sum_s 2^(m_s - M) l_s.
+// In the NVFP4 path every share has the same extra factor 1/2688 in both a_s
+// and l_s (the first P level), so it cancels here as it does in O = A / lam.
+// The P quantisation is per key tile, and shares are whole key tiles, so the
+// split changes only the float32 summation order.
+//
+// One warp per row; lane i holds columns i, i + 32, ... (coalesced 128-byte
+// rows).  Memory-bound and small: it reads nsplit * d + 2 floats per row.
+
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace sa {
+namespace {
+
+constexpr int kRowsPerCta = 8;
+
+template <int D, bool OUT32>
+__global__ void __launch_bounds__(32 * kRowsPerCta) splitkv_combine_kernel(const SplitOut part, int nsplit,
+                                                                         long long nrows, int L, int Lp,
+                                                                         long long split_rows, void* out) {
+  const long long row = (long long)blockIdx.x * kRowsPerCta + threadIdx.x / 32;
+  if (row >= nrows) return;
+  const int lane = threadIdx.x % 32;
+  const long long bh = row / L;
+  const long long prow = bh * Lp + row % L;          // row in the padded partial layout
+  float mmax = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) {
+    const float2 ml = *reinterpret_cast<const float2*>(part.ml + 2 * (s * split_rows + prow));
+    if (ml.y > 0.f) mmax = fmaxf(mmax, ml.x);
+  }
+  float acc[D / 32];
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
+  float lsum = 0.f;
+  for (int s = 0; s < nsplit; ++s) {
+    const float2 ml = *reinterpret_cast<const float2*>(part.ml + 2 * (s * split_rows + prow));
+    if (!(ml.y > 0.f)) continue;                     // an empty share (its a_s is never read)
+    const float w = exp2f(ml.x - mmax);
+    lsum = fmaf(w, ml.y, lsum);
+    const float* a = part.o + (s * split_rows + prow) * D;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) acc[i] = fmaf(w, a[lane + 32 * i], acc[i]);
+  }
+  const float inv = 1.f / lsum;
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) {
+    const long long idx = row * D + lane + 32 * i;
+    if constexpr (OUT32)
+      static_cast<float*>(out)[idx] = acc[i] * inv;
+    else
+      static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(acc[i] * inv);
+  }
+}
+
+template <int D, bool OUT32>
+cudaError_t launch(const SplitOut& part, int nsplit, const Dims& dm, void* o, cudaStream_t s) {
+  const long long nrows = (long long)dm.B * dm.H * dm.L;
+  const int Lp = padded_len(dm.L);
+  const long long split_rows = (long long)dm.B * dm.H * Lp;
+  const long long ctas = (nrows + kRowsPerCta - 1) / kRowsPerCta;
+  splitkv_combine_kernel<D, OUT32><<<(unsigned)ctas, 32 * kRowsPerCta, 0, s>>>(part, nsplit, nrows, dm.L, Lp,
+                                                                              split_rows, o);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_splitkv_combine(const SplitOut& part, int nsplit, const Dims& dm, void* o, bool out_f32,
+                                   cudaStream_t s) {
+  if (dm.d == 64) return out_f32 ? launch<64, true>(part, nsplit, dm, o, s) : launch<64, false>(part, nsplit, dm, o, s);
+  return out_f32 ? launch<128, true>(part, nsplit, dm, o, s) : launch<128, false>(part, nsplit, dm, o, s);
+}
+
+}  // namespace sa

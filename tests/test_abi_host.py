@@ -101,6 +101,13 @@ def test_argument_errors_launch_nothing(sa):
         assert lib.sa_attn_fwd_host(z, z, z, z, B, 2, 2, L, 64, 0, 1, z, 0, 0, None) == sa.SA_OK
         assert lib.sa_attn_fwd_host_workspace_bytes(B, 2, 2, L, 64, 1, 0) == 0
     assert lib.sa_attn_fwd(z, z, z, z, 0, 2, 2, 256, 96, 0, 0, None) == sa.SA_ERR_UNSUPPORTED   # d still checked
+    # split-KV: a forced split needs a workspace; a negative split count is invalid
+    assert lib.sa_attn_fwd_ws(p, p, p, p, 1, 2, 2, 1024, 64, 0, 0, 4, z, 0, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_attn_fwd_ws(p, p, p, p, 1, 2, 2, 1024, 64, 0, 0, -1, p, 1 << 30, None) == sa.SA_ERR_INVALID_ARG
+    need = lib.sa_attn_fwd_workspace_bytes(1, 2, 2, 1024, 64, 0, 0, 4)
+    assert need == 4 * (1 * 2 * 1024) * (64 + 2) * 4                       # partial O rows plus (m, l)
+    assert lib.sa_attn_fwd_ws(p, p, p, p, 1, 2, 2, 1024, 64, 0, 0, 4, p, need - 16, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_attn_fwd_workspace_bytes(1, 2, 2, 1024, 64, 0, 0, 1) == 0
     s = sa.SaFp4Qkv()
     assert lib.sa_quantize(p, p, p, 1, 2, 2, 256, 64, ctypes.byref(s), None) == sa.SA_ERR_INVALID_ARG
     assert lib.sa_quantize(p, p, p, 1, 2, 2, 256, 80, ctypes.byref(s), None) == sa.SA_ERR_UNSUPPORTED

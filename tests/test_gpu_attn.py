@@ -163,3 +163,62 @@ def test_wait_timeout_is_reported_and_context_survives(sa):
     x = W.make_inputs(w)
     o = run_gpu(sa, x, False, "bf16")             # the context still works
     check(o, x, False, [(0, 0)], np.arange(64), "bf16")
+
+
+# Split-KV: the key tiles of every query-tile pair are cut into shares computed
+# by separate CTAs and merged by a combine kernel.  Shares are whole key
+# tiles, so the P quantisation decisions are the unsplit ones and the result
+# must meet the same bar against the oracle (and stay within float32
+# summation-order differences of the unsplit call).
+SPLIT = [
+    (dict(W.spec("sweep_full_d128_L1024"), H=2, Hkv=2, seed=50), 4),
+    (dict(W.spec("causal_gqa"), B=1, H=4, Hkv=2, L=640, seed=51), 3),      # causal: early pairs get empty shares
+    (dict(W.spec("dit_video"), B=1, H=2, Hkv=1, L=333, d=64, seed=52), 2),  # ragged L, MQA
+    (dict(W.spec("tiny"), B=1, H=2, Hkv=2, L=512, causal=True, seed=53), 4),
+    (dict(W.spec("llm_prefill"), B=1, H=2, Hkv=2, L=384, seed=54), 3),      # one key tile per share
+]
+
+
+def run_split(sa, x, causal, mode, nsplit, out_dtype=torch.bfloat16):
+    q, k, v = (x[n].cuda() for n in "qkv")
+    args = (q, k, v) if mode == "bf16" else (sa.sa_quantize(q, k, v),)
+    o = sa.sa_attn_fwd(*args, causal=causal, mode=mode, out_dtype=out_dtype, nsplit=nsplit)
+    torch.cuda.synchronize()
+    assert sa.sa_last_device_error() == 0
+    return o.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("mode", ["bf16", "nvfp4"])
+@pytest.mark.parametrize("case", SPLIT, ids=lambda c: _id(c[0]) + f"-s{c[1]}")
+def test_split_kv_small_all_rows(sa, case, mode):
+    w, nsplit = case
+    x = W.make_inputs(w)
+    o = run_split(sa, x, w["causal"], mode, nsplit)
+    o32 = run_split(sa, x, w["causal"], mode, nsplit, torch.float32) if mode == "nvfp4" else None
+    heads = [(b, h) for b in range(w["B"]) for h in range(w["H"])]
+    check(o, x, w["causal"], heads, np.arange(w["L"]), mode, o32)
+    # against the unsplit call.  NVFP4: P2 and its quantisation depend on the
+    # tile alone, so the decisions are the unsplit ones and only the float32
+    # summation order differs.  BF16: P is rounded to bf16 relative to each
+    # share's own running maximum, so the two calls round P at different
+    # scales (2^-9 relative per element, up to ~2^-8 of O), inside the bar.
+    ref = run_gpu(sa, x, w["causal"], mode, torch.float32)
+    got = run_split(sa, x, w["causal"], mode, nsplit, torch.float32)
+    bound = 1e-5 if mode == "nvfp4" else BF16_TOL
+    assert np.abs(got - ref).max() <= bound * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("mode", ["bf16", "nvfp4"])
+@pytest.mark.parametrize("case", [(dict(W.spec("sweep_full_d128_L4096"), H=1, Hkv=1), True),   # 16 pairs, 32 key tiles
+                                  (dict(W.spec("sweep_full_d128_L1024")), False)],        # shares would be short
+                         ids=["H1-L4096-split", "H8-L1024-nosplit"])
+def test_split_kv_library_choice(sa, case, mode):
+    # the library splits a problem that leaves most SMs idle only when every
+    # share keeps 16 key tiles or more; its choice stays on the parity bar
+    w, splits = case
+    assert (sa.sa_attn_fwd_workspace_bytes(w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["causal"], mode) > 0) == splits
+    x = W.make_inputs(w)
+    o = run_split(sa, x, w["causal"], mode, 0)
+    o32 = run_split(sa, x, w["causal"], mode, 0, torch.float32) if mode == "nvfp4" else None
+    rows = np.array(W.sample_rows(w["L"], 192, seed=w["seed"]))
+    check(o, x, w["causal"], [(0, 0), (w["B"] - 1, w["H"] - 1)], rows, mode, o32)
