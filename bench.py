@@ -167,9 +167,12 @@ def run_ours(args, rank, world, local_rank):
     fl = W.flops(w)
     causal = w["causal"]
 
-    # split-KV when the library chooses it (problems too small to fill the
-    # SMs); the workspace is allocated once, outside the timed region
-    nsplit_ws = sa.sa_attn_fwd_workspace_bytes(B, H, Hkv, L, d, causal, "nvfp4", 0)
+    # the library's work split (stream-K for the NVFP4 path once the pairs
+    # fill the SMs, split-KV for problems too small to); the workspace is
+    # allocated once, outside the timed region
+    ws4 = sa.sa_attn_fwd_workspace_bytes(B, H, Hkv, L, d, causal, "nvfp4", 0)
+    ws16 = sa.sa_attn_fwd_workspace_bytes(B, H, Hkv, L, d, causal, "bf16", 0)
+    nsplit_ws = max(ws4, ws16)
     ws = torch.empty(max(nsplit_ws, 16), dtype=torch.uint8, device=dev)
 
     def step(ev):
@@ -200,8 +203,9 @@ def run_ours(args, rank, world, local_rank):
         wall = time.perf_counter() - t0
     if world > 1:
         dist.barrier()
-    # sa_quantize: 2 kernels; each attention call: 1, plus the combine kernel when split
-    launches = args.steps * (2 + 2 * (2 if nsplit_ws > 0 else 1))
+    # sa_quantize: 2 kernels; each attention call: 1, plus a combine kernel
+    # when its work is split
+    launches = args.steps * (2 + (2 if ws4 > 0 else 1) + (2 if ws16 > 0 else 1))
     tq = [a[0].elapsed_time(a[1]) * 1e-3 for a in evs]
     t4 = [a[1].elapsed_time(a[2]) * 1e-3 for a in evs]
     t16 = [a[2].elapsed_time(a[3]) * 1e-3 for a in evs]
@@ -270,8 +274,9 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "flushed by a 256 MB write before every step",
                    "value_def": "4*B*H*L^2*d / (sa_quantize + NVFP4 sa_attn_fwd) per GPU, summed over GPUs",
                    "parallelism": f"independent batch per GPU ({world} GPU)",
-                   "split_kv": "library choice (sa_attn_fwd_ws, nsplit=0): "
-                               + ("split" if nsplit_ws > 0 else "no split for this size")},
+                   "work_split": "library choice (sa_attn_fwd_ws, nsplit=0): nvfp4 "
+                                 + ("stream-K/split" if ws4 > 0 else "one unit per CTA") + ", bf16 "
+                                 + ("split-KV" if ws16 > 0 else "one unit per CTA")},
         "paths": {
             "nvfp4_attn_only_tops": a4,
             "nvfp4_attn_us": t_4 * 1e6,

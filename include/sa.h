@@ -185,17 +185,24 @@ sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o,
  * quantisation is unchanged and only the float32 summation order differs
  * from the unsplit call.
  *
+ * Stream-K (NVFP4 path): persistent CTAs, one per SM, each over an equal
+ * range of (query-tile pair, key tile) items; a pair cut by a range
+ * boundary is computed in segments and merged the same way.
+ *
  * sa_attn_fwd_workspace_bytes: device workspace bytes sa_attn_fwd_ws needs
- *   for the given sizes and `nsplit` (0 = the library's choice: split only
- *   while the units leave at least half of the SMs idle and every share keeps
- *   16 key tiles or more, at most 16 shares; 1 = no split; n > 1 = n shares,
- *   at most one per key tile).  0 when no split would be used, or for invalid or
- *   empty sizes.  causal and mode do not change the size.
- * sa_attn_fwd_ws: sa_attn_fwd with split-KV.  Arguments as sa_attn_fwd, plus
- *   nsplit as above and a caller-owned, 16-byte aligned device workspace of
- *   workspace_bytes.  With nsplit 0 a missing or short workspace means no
- *   split; with nsplit > 1 it is SA_ERR_INVALID_ARG.  Enqueues the attention
- *   kernel and, when split, the combine kernel, on `stream`.
+ *   for the given sizes and `nsplit`: 0 = the library's choice (NVFP4:
+ *   stream-K once the pairs fill the SMs; split-KV while the units leave at
+ *   least half of the SMs idle and every share keeps 16 key tiles or more, at
+ *   most 16 shares; else neither); 1 = one unit per CTA; n > 1 = n shares, at
+ *   most one per key tile; -1 = stream-K (NVFP4 only).  0 when neither would
+ *   be used, or for invalid or empty sizes.
+ * sa_attn_fwd_ws: sa_attn_fwd with split-KV or stream-K.  Arguments as
+ *   sa_attn_fwd, plus nsplit as above and a caller-owned, 16-byte aligned
+ *   device workspace of workspace_bytes.  With nsplit 0 a missing or short
+ *   workspace means one unit per CTA; with nsplit > 1 or -1 it is
+ *   SA_ERR_INVALID_ARG; -1 with the BF16 path is SA_ERR_UNSUPPORTED.
+ *   Enqueues the attention kernel and, when work is split, the combine
+ *   kernel, on `stream`.
  */
 size_t sa_attn_fwd_workspace_bytes(int B, int H, int Hkv, int L, int d, int causal, int mode, int nsplit);
 sa_status sa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o,

@@ -30,9 +30,18 @@
 // per row: softmax, P quantisation, O correction, epilogue); warp 8 issues TMA
 // and bulk copies; warp 9 issues the S MMAs and warp 10 the P.V MMAs, each
 // with the scale-factor copies they need (the three warps run their loops with
-// all lanes and issue from one elected lane); warp 11 idles.  Tensor memory: S (128 columns, shared by both query
-// tiles), O0, O1 (d columns each), then scale factors (4 columns per 64-deep K
-// chunk, copied from SMEM with tcgen05.cp, replicated to the four lane quarters).
+// all lanes and issue from one elected lane); warp 11 idles.  Tensor memory: S
+// (128 columns, shared by both query tiles), O0, O1 (d columns each), then
+// scale factors (4 columns per 64-deep K chunk, copied from SMEM with
+// tcgen05.cp, replicated to the four lane quarters).
+//
+// A CTA works through a list of units (work.cuh): one entry of the work list,
+// or, persistent under stream-K, a range of (pair, key tile) items that spans
+// several pairs.  Every role walks the same list and counts its barrier
+// phases, stages and buffers over the whole list, so the next unit's Q and
+// first K/V tiles load, and its first S is computed, while the softmax warps
+// finish the current one.  Q and its scales are double-buffered by unit
+// parity.
 
 #include <cuda_bf16.h>
 
@@ -66,16 +75,16 @@ struct CfgF4 {
   static constexpr int kVSfBytes = 2 * 512;                // two 64-token chunks
   static constexpr int kPBytes = BM * (BN / 2);            // P^ tile: 128 rows x 64 bytes
   static constexpr int kPSfBytes = 2 * 512;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + 2 * kQBytes;
+  static constexpr int kOffQ = 0;                          // [unit parity][query tile]
+  static constexpr int kOffK = kOffQ + 4 * kQBytes;
   static constexpr int kOffV = kOffK + NS * kKBytes;
   static constexpr int kOffP = kOffV + NS * kVBytes;
   static constexpr int kOffQSf = kOffP + 4 * kPBytes;      // P^ double-buffered per query tile
-  static constexpr int kOffKSf = kOffQSf + 2 * kQSfBytes;
+  static constexpr int kOffKSf = kOffQSf + 4 * kQSfBytes;
   static constexpr int kOffVSf = kOffKSf + NS * kKSfBytes;
   static constexpr int kOffPSf = kOffVSf + NS * kVSfBytes;
   static constexpr int kOffBar = kOffPSf + 4 * kPSfBytes;
-  static constexpr int kNumBars = 1 + 4 * NS + 8 + 2;
+  static constexpr int kNumBars = 4 + 4 * NS + 8 + 2;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   // Q/K rows of 64 bytes use the 64B swizzle, rows of 32 bytes the 32B one.
   static constexpr uint32_t kQKSwz = (D == 128) ? kSwizzle64B : kSwizzle32B;
@@ -87,19 +96,19 @@ struct CfgF4 {
   // K and V scale columns are double-buffered by tile parity: a tcgen05.cp
   // is not ordered after earlier MMAs that read the columns it overwrites, so
   // tile j+1's scales must not land where tile j's MMAs may still be reading.
-  static constexpr uint32_t kColSfQ0 = kColSf + 0;
-  static constexpr uint32_t kColSfQ1 = kColSf + 8;
-  static constexpr uint32_t kColSfK = kColSf + 16;     // + 8 * (j & 1)
-  static constexpr uint32_t kColSfV = kColSf + 32;     // + 8 * (j & 1)
-  static constexpr uint32_t kColSfP0 = kColSf + 48;
-  static constexpr uint32_t kColSfP1 = kColSf + 56;
+  // Q scales likewise by unit parity: [unit parity][query tile] x 8 columns.
+  static constexpr uint32_t kColSfQ = kColSf + 0;      // + 16 * (unit & 1) + 8 * q
+  static constexpr uint32_t kColSfK = kColSf + 32;     // + 8 * (j & 1)
+  static constexpr uint32_t kColSfV = kColSf + 48;     // + 8 * (j & 1)
+  static constexpr uint32_t kColSfP0 = kColSf + 64;
+  static constexpr uint32_t kColSfP1 = kColSf + 72;
   static constexpr uint32_t kIdescS = idesc_nvf4(BM, BN);
   static constexpr uint32_t kIdescPV = idesc_nvf4(BM, D);
-  static_assert(kColSf + 64 <= 512, "tensor memory overflow");
+  static_assert(kColSf + 80 <= 512, "tensor memory overflow");
 };
 
 struct BarsF4 {
-  uint64_t *q_full, *k_full, *k_empty, *v_full, *v_empty, *s_full, *s_free, *p_full, *o_done, *drain;
+  uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *s_free, *p_full, *o_done, *drain;
 };
 
 // Descriptors are built at each use from a 32-bit shared address.  (Kernels
@@ -131,8 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar_base = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   BarsF4 bars;
-  bars.q_full = bar_base;
-  bars.k_full = bar_base + 1;
+  bars.q_full = bar_base;                 // [unit parity]
+  bars.q_empty = bar_base + 2;            // [unit parity]: that unit's S MMAs are complete
+  bars.k_full = bar_base + 4;
   bars.k_empty = bars.k_full + C::NS;
   bars.v_full = bars.k_empty + C::NS;
   bars.v_empty = bars.v_full + C::NS;
@@ -145,19 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  int bh, qt0, nqu, sp;
-  attn_unit(work, (int)blockIdx.x, bh, qt0, nqu, sp);              // this CTA's query tiles and split
-  const int h = bh % H, b = bh / H;
-  const int hk = h / (H / Hkv);
-  const bool q1_valid = nqu == 2;
-  int ntq[2];
   // the quantised operands hold Lp = L rounded up to whole tiles per head
   const int Lp = (L + 127) & ~127;
-  ntq[0] = causal ? qt0 + 1 : Lp / BN;
-  ntq[1] = q1_valid ? (causal ? qt0 + 2 : Lp / BN) : 0;
-  // key tiles [jb, jb + ntq[q]) of this CTA; loop indices below count from jb
-  const int jb = work.nsplit > 1 ? split_range(sp, work.nsplit, ntq) : 0;
-  const int nt = ntq[0] > ntq[1] ? ntq[0] : ntq[1];
+  const int G = H / Hkv;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i) mbar_init(bar_base + i, 1);
@@ -177,9 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  const long long bhq = (long long)b * H + h;
-  const long long bhk = (long long)b * Hkv + hk;
-
+  // (each role below walks the CTA's unit list with its own iterator)
   if (warp >= 8) {
     // Register split: the launch gives every thread kLaunchRegs; this
     // warpgroup (producer, MMA issuer, two idle warps) keeps kOtherRegs and the
@@ -191,103 +189,150 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 8) {
       // ---------------------------------------------------------- producer
       const bool leader = elect_one();
-      const int nq = q1_valid ? 2 : 1;
+      UnitIter it;
+      unit_iter_init(work, it);
+      AttnUnitRef u;
       if (leader) {
         tma_prefetch_desc(&tmap_q);
         tma_prefetch_desc(&tmap_k);
         tma_prefetch_desc(&tmap_v);
-        mbar_arrive_expect_tx(bars.q_full, nq * (C::kQBytes + C::kQSfBytes));
-        for (int q = 0; q < nq; ++q) {
-          const int qt = qt0 + q;
-          tma_load_2d(smem + C::kOffQ + q * C::kQBytes, &tmap_q, bars.q_full, 0,
-                      (int)(bhq * Lp + (long long)qt * BM));
-          bulk_load(smem + C::kOffQSf + q * C::kQSfBytes, q_sf + (bhq * (Lp / 128) + qt) * C::kQSfBytes,
-                    C::kQSfBytes, bars.q_full);
-        }
       }
-      int issued = 0;
-      for (int j = 0; j < nt; ++j) {
-        const int s = j % C::NS;
-        const uint32_t par = ((j / C::NS) - 1) & 1;
-        if (j >= C::NS && !mbar_wait_backoff_warp(bars.k_empty + s, par, abort_flag, wait_ns, kProducerSleepNs)) break;
-        if (leader) {
-          mbar_arrive_expect_tx(bars.k_full + s, C::kKBytes + C::kKSfBytes);
-          tma_load_2d(smem + C::kOffK + s * C::kKBytes, &tmap_k, bars.k_full + s, 0,
-                      (int)(bhk * Lp + (long long)(jb + j) * BN));
-          bulk_load(smem + C::kOffKSf + s * C::kKSfBytes, k_sf + (bhk * (Lp / 128) + jb + j) * C::kKSfBytes,
-                    C::kKSfBytes, bars.k_full + s);
-        }
-        if (j >= C::NS && !mbar_wait_backoff_warp(bars.v_empty + s, par, abort_flag, wait_ns, kProducerSleepNs)) {
-          issued = 2 * j + 1;
+      // K and V tiles and Q units issued so far (over the whole list); the
+      // counts also tell the abort path which copies may still be in flight
+      int nk = 0, nv = 0, ug = 0;
+      bool ok = true;
+      while (ok && unit_next(work, it, u)) {
+        const int qb = ug & 1;
+        // Q of this unit into buffer qb, once the S MMAs of unit ug-2 (the
+        // last to read that buffer) are complete
+        if (ug >= 2 && !mbar_wait_backoff_warp(bars.q_empty + qb, ((ug >> 1) - 1) & 1, abort_flag, wait_ns,
+                                               kProducerSleepNs)) {
+          ok = false;
           break;
         }
+        const long long bhq = u.bh;
+        const long long bhk = (long long)(u.bh / H) * Hkv + (u.bh % H) / G;
         if (leader) {
-          mbar_arrive_expect_tx(bars.v_full + s, C::kVBytes + C::kVSfBytes);
-          tma_load_2d(smem + C::kOffV + s * C::kVBytes, &tmap_v, bars.v_full + s, (jb + j) * (BN / 2),
-                      (int)(bhk * D));
-          bulk_load(smem + C::kOffVSf + s * C::kVSfBytes, v_sf + (bhk * (Lp / 64) + 2 * (jb + j)) * 512, C::kVSfBytes,
-                    bars.v_full + s);
+          mbar_arrive_expect_tx(bars.q_full + qb, u.nq * (C::kQBytes + C::kQSfBytes));
+          for (int q = 0; q < u.nq; ++q) {
+            const int qt = u.qt0 + q;
+            tma_load_2d(smem + C::kOffQ + (2 * qb + q) * C::kQBytes, &tmap_q, bars.q_full + qb, 0,
+                        (int)(bhq * Lp + (long long)qt * BM));
+            bulk_load(smem + C::kOffQSf + (2 * qb + q) * C::kQSfBytes,
+                      q_sf + (bhq * (Lp / 128) + qt) * C::kQSfBytes, C::kQSfBytes, bars.q_full + qb);
+          }
         }
-        issued = 2 * j + 2;
+        ++ug;
+        const int nt = u.n[0] > u.n[1] ? u.n[0] : u.n[1];
+        for (int j = 0; j < nt; ++j) {
+          const int s = nk % C::NS;
+          const uint32_t par = ((nk / C::NS) - 1) & 1;
+          const int ja = u.jb + j;                      // the key tile
+          if (nk >= C::NS &&
+              !mbar_wait_backoff_warp(bars.k_empty + s, par, abort_flag, wait_ns, kProducerSleepNs)) {
+            ok = false;
+            break;
+          }
+          if (leader) {
+            mbar_arrive_expect_tx(bars.k_full + s, C::kKBytes + C::kKSfBytes);
+            tma_load_2d(smem + C::kOffK + s * C::kKBytes, &tmap_k, bars.k_full + s, 0,
+                        (int)(bhk * Lp + (long long)ja * BN));
+            bulk_load(smem + C::kOffKSf + s * C::kKSfBytes, k_sf + (bhk * (Lp / 128) + ja) * C::kKSfBytes,
+                      C::kKSfBytes, bars.k_full + s);
+          }
+          ++nk;
+          if (nv >= C::NS &&
+              !mbar_wait_backoff_warp(bars.v_empty + s, par, abort_flag, wait_ns, kProducerSleepNs)) {
+            ok = false;
+            break;
+          }
+          if (leader) {
+            mbar_arrive_expect_tx(bars.v_full + s, C::kVBytes + C::kVSfBytes);
+            tma_load_2d(smem + C::kOffV + s * C::kVBytes, &tmap_v, bars.v_full + s, ja * (BN / 2),
+                        (int)(bhk * D));
+            bulk_load(smem + C::kOffVSf + s * C::kVSfBytes, v_sf + (bhk * (Lp / 64) + 2 * ja) * 512,
+                      C::kVSfBytes, bars.v_full + s);
+          }
+          ++nv;
+        }
       }
       if (*abort_flag) {
         // let every copy already issued land before the CTA (and its shared
-        // memory) goes away
-        mbar_wait_drain(bars.q_full, 0, wait_ns);
-        for (int u = (issued > 2 * C::NS ? issued - 2 * C::NS : 0); u < issued; ++u) {
-          const int j = u / 2, s = j % C::NS;
-          mbar_wait_drain((u % 2 == 0) ? bars.k_full + s : bars.v_full + s, (j / C::NS) & 1, wait_ns);
-        }
+        // memory) goes away: the last issue into each Q buffer and each stage
+        for (int g = (ug > 2 ? ug - 2 : 0); g < ug; ++g) mbar_wait_drain(bars.q_full + (g & 1), (g >> 1) & 1, wait_ns);
+        for (int g = (nk > C::NS ? nk - C::NS : 0); g < nk; ++g)
+          mbar_wait_drain(bars.k_full + g % C::NS, (g / C::NS) & 1, wait_ns);
+        for (int g = (nv > C::NS ? nv - C::NS : 0); g < nv; ++g)
+          mbar_wait_drain(bars.v_full + g % C::NS, (g / C::NS) & 1, wait_ns);
       }
     } else if (warp == 9) {
       // ---------------------------------------------------------- S issuer
       // S0(0), S1(0), S0(1), S1(1), ... into the one S region; each waits
-      // until the softmax warps have read the previous S.  A tile's K scales
-      // go to the buffer of its parity; the buffer was last read by the S
-      // MMAs of tile j-2, complete once the S before S(j-1) has been read.
+      // until the softmax warps have read the previous S (over the whole
+      // list).  A tile's K scales go to the buffer of its parity; the buffer
+      // was last read by the S MMAs two tiles earlier, complete once the S
+      // before the previous tile's has been read.
       const bool leader = elect_one();
       const uint32_t sb = smem_u32(smem);
       const uint32_t tS = tbase + C::kColS;
-      int last_q = -1, last_j = 0;
-      bool ok = mbar_wait_warp(bars.q_full, 0, abort_flag, wait_ns);
-      // (an empty split issues no MMA, and so no copy whose completion a
-      // commit would have to cover)
-      if (ok && nt > 0) {
-        tc_fence_after();
-        if (leader) {
-          copy_sf(tbase + C::kColSfQ0, sb + C::kOffQSf, D / 64);
-          if (q1_valid) copy_sf(tbase + C::kColSfQ1, sb + C::kOffQSf + C::kQSfBytes, D / 64);
-        }
-        __syncwarp();
-      }
-      for (int j = 0; ok && j < nt; ++j) {
-        const int s = j % C::NS;
-        ok = mbar_wait_warp(bars.k_full + s, (j / C::NS) & 1, abort_flag, wait_ns);
+      UnitIter it;
+      unit_iter_init(work, it);
+      AttnUnitRef u;
+      int last_q = -1;
+      uint32_t last_par = 0;
+      int cs[2] = {0, 0};       // S MMAs issued per query tile
+      int gk = 0, ug = 0;
+      bool ok = true;
+      while (ok && unit_next(work, it, u)) {
+        const int qb = ug & 1;
+        const int nt = u.n[0] > u.n[1] ? u.n[0] : u.n[1];
+        ok = mbar_wait_warp(bars.q_full + qb, (ug >> 1) & 1, abort_flag, wait_ns);
         if (!ok) break;
-        tc_fence_after();
-        const uint32_t sfk = tbase + C::kColSfK + 8 * (j & 1);
-        if (leader) copy_sf(sfk, sb + C::kOffKSf + s * C::kKSfBytes, D / 64);
-        __syncwarp();
-        for (int q = 0; ok && q < 2; ++q) {
-          if (j >= ntq[q]) continue;
-          if (last_q >= 0) ok = mbar_wait_warp(bars.s_free + last_q, last_j & 1, abort_flag, wait_ns);
+        // Q scales of this unit to the columns of its parity, last read by
+        // the S MMAs of unit ug-2, complete before S of unit ug-1 was issued.
+        // (A unit without key tiles issues no MMA, and so no copy whose
+        // completion a commit would have to cover.)
+        if (nt > 0) {
+          tc_fence_after();
+          if (leader)
+            for (int q = 0; q < u.nq; ++q)
+              copy_sf(tbase + C::kColSfQ + 16 * qb + 8 * q, sb + C::kOffQSf + (2 * qb + q) * C::kQSfBytes, D / 64);
+          __syncwarp();
+        }
+        for (int j = 0; ok && j < nt; ++j, ++gk) {
+          const int s = gk % C::NS;
+          ok = mbar_wait_warp(bars.k_full + s, (gk / C::NS) & 1, abort_flag, wait_ns);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t sfq = tbase + (q ? C::kColSfQ1 : C::kColSfQ0);
-          if (leader) {
-#pragma unroll
-            for (int kk = 0; kk < D / 64; ++kk)
-              mma_nvf4(tS, desc_qk(sb + C::kOffQ + q * C::kQBytes + kk * 32, C::kQKSbo, C::kQKSwz),
-                       desc_qk(sb + C::kOffK + s * C::kKBytes + kk * 32, C::kQKSbo, C::kQKSwz), C::kIdescS,
-                       sfq + 4 * kk, sfk + 4 * kk, kk > 0 ? 1u : 0u);
-            tc_commit(bars.s_full + q);
-          }
+          const uint32_t sfk = tbase + C::kColSfK + 8 * (gk & 1);
+          if (leader) copy_sf(sfk, sb + C::kOffKSf + s * C::kKSfBytes, D / 64);
           __syncwarp();
-          last_q = q;
-          last_j = j;
+          for (int q = 0; ok && q < 2; ++q) {
+            if (j >= (q ? u.n[1] : u.n[0])) continue;
+            if (last_q >= 0) ok = mbar_wait_warp(bars.s_free + last_q, last_par, abort_flag, wait_ns);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t sfq = tbase + C::kColSfQ + 16 * qb + 8 * q;
+            if (leader) {
+#pragma unroll
+              for (int kk = 0; kk < D / 64; ++kk)
+                mma_nvf4(tS, desc_qk(sb + C::kOffQ + (2 * qb + q) * C::kQBytes + kk * 32, C::kQKSbo, C::kQKSwz),
+                         desc_qk(sb + C::kOffK + s * C::kKBytes + kk * 32, C::kQKSbo, C::kQKSwz), C::kIdescS,
+                         sfq + 4 * kk, sfk + 4 * kk, kk > 0 ? 1u : 0u);
+              tc_commit(bars.s_full + q);
+            }
+            __syncwarp();
+            last_q = q;
+            last_par = cs[q] & 1;
+            ++cs[q];
+          }
+          if (ok && leader) tc_commit(bars.k_empty + s);      // K slot free once these S MMAs are done
+          __syncwarp();
         }
-        if (ok && leader) tc_commit(bars.k_empty + s);      // K slot free once these S MMAs are done
+        if (!ok) break;
+        if (leader) tc_commit(bars.q_empty + qb);            // Q buffer free once this unit's S MMAs are done
         __syncwarp();
+        ++ug;
       }
       if (!ok) {
         if (leader) tc_commit(bars.drain);
@@ -297,41 +342,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 10) {
       // ---------------------------------------------------------- P.V issuer
       // P0.V(j), P1.V(j), ... each once its softmax warps have written P^.
-      // V scales of tile j go to the buffer of its parity, last read by the
-      // P.V MMAs of tile j-2, which the softmax warps have seen complete
-      // before releasing P^(j-1).
+      // V scales of a tile go to the buffer of its parity, last read by the
+      // P.V MMAs two tiles earlier, which the softmax warps have seen complete
+      // before releasing the previous P^.  The first P.V of a unit starts the
+      // accumulator afresh: the softmax warps read the previous unit's O
+      // before they release that P^.
       const bool leader = elect_one();
       const uint32_t sb = smem_u32(smem);
+      UnitIter it;
+      unit_iter_init(work, it);
+      AttnUnitRef u;
+      int cp[2] = {0, 0};       // P.V MMAs issued per query tile
+      int gk = 0;
       bool ok = true;
-      for (int j = 0; ok && j < nt; ++j) {
-        const int s = j % C::NS;
-        ok = mbar_wait_warp(bars.v_full + s, (j / C::NS) & 1, abort_flag, wait_ns);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t sfv = tbase + C::kColSfV + 8 * (j & 1);
-        if (leader) copy_sf(sfv, sb + C::kOffVSf + s * C::kVSfBytes, 2);
-        __syncwarp();
-        for (int q = 0; ok && q < 2; ++q) {
-          if (j >= ntq[q]) continue;
-          ok = mbar_wait_warp(bars.p_full + q, j & 1, abort_flag, wait_ns);
+      while (ok && unit_next(work, it, u)) {
+        const int nt = u.n[0] > u.n[1] ? u.n[0] : u.n[1];
+        for (int j = 0; ok && j < nt; ++j, ++gk) {
+          const int s = gk % C::NS;
+          ok = mbar_wait_warp(bars.v_full + s, (gk / C::NS) & 1, abort_flag, wait_ns);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t sfp = tbase + (q ? C::kColSfP1 : C::kColSfP0);
-          const uint32_t tO = tbase + C::kColO0 + q * D;
-          if (leader) {
-            const int pb = 2 * q + (j & 1);                  // P^ buffer of this tile
-            copy_sf(sfp, sb + C::kOffPSf + pb * C::kPSfBytes, 2);
+          const uint32_t sfv = tbase + C::kColSfV + 8 * (gk & 1);
+          if (leader) copy_sf(sfv, sb + C::kOffVSf + s * C::kVSfBytes, 2);
+          __syncwarp();
+          for (int q = 0; ok && q < 2; ++q) {
+            if (j >= (q ? u.n[1] : u.n[0])) continue;
+            ok = mbar_wait_warp(bars.p_full + q, cp[q] & 1, abort_flag, wait_ns);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t sfp = tbase + (q ? C::kColSfP1 : C::kColSfP0);
+            const uint32_t tO = tbase + C::kColO0 + q * D;
+            if (leader) {
+              const int pb = 2 * q + (cp[q] & 1);            // P^ buffer of this tile
+              copy_sf(sfp, sb + C::kOffPSf + pb * C::kPSfBytes, 2);
 #pragma unroll
-            for (int kk = 0; kk < BN / 64; ++kk)
-              mma_nvf4(tO, desc_qk(sb + C::kOffP + pb * C::kPBytes + kk * 32, 512, kSwizzle64B),
-                       desc_qk(sb + C::kOffV + s * C::kVBytes + kk * 32, 512, kSwizzle64B), C::kIdescPV,
-                       sfp + 4 * kk, sfv + 4 * kk, (j > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(bars.o_done + q);
+              for (int kk = 0; kk < BN / 64; ++kk)
+                mma_nvf4(tO, desc_qk(sb + C::kOffP + pb * C::kPBytes + kk * 32, 512, kSwizzle64B),
+                         desc_qk(sb + C::kOffV + s * C::kVBytes + kk * 32, 512, kSwizzle64B), C::kIdescPV,
+                         sfp + 4 * kk, sfv + 4 * kk, (j > 0 || kk > 0) ? 1u : 0u);
+              tc_commit(bars.o_done + q);
+            }
+            __syncwarp();
+            ++cp[q];
           }
+          if (ok && leader) tc_commit(bars.v_empty + s);      // V slot free once these P.V MMAs are done
           __syncwarp();
         }
-        if (ok && leader) tc_commit(bars.v_empty + s);      // V slot free once these P.V MMAs are done
-        __syncwarp();
       }
       if (!ok) {
         if (leader) tc_commit(bars.drain + 1);
@@ -345,194 +401,218 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp / 4;
     const int r = (warp % 4) * 32 + lane;
     const uint32_t lane_addr = tbase + (((warp % 4) * 32) << 16);
-    const int qt = qt0 + q;
     const float c = 1.4426950408889634f * rsqrtf((float)D);
     uint8_t* prow0 = smem + C::kOffP + 2 * q * C::kPBytes + r * 64;
     uint8_t* psf0 = smem + C::kOffPSf + 2 * q * C::kPSfBytes + (r % 32) * 16 + (r / 32) * 4;
     const uint32_t ocol = C::kColO0 + q * D;
-    float m_run = -INFINITY, m_ref = 0.f, lam = 0.f;
-    bool have_ref = false, ok = true;
-    for (int j = 0; j < ntq[q]; ++j) {
-      if (!mbar_wait_warp(bars.s_full + q, j & 1, abort_flag, wait_ns)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) tmem_ld32(lane_addr + C::kColS + 32 * i, sr[i]);
-      tmem_ld_wait(sr[0]);
-      tmem_launder(sr[1]);
-      tmem_launder(sr[2]);
-      tmem_launder(sr[3]);
-      tc_fence_before();
-      mbar_arrive(bars.s_free + q);
-      float sv[128];
-#pragma unroll
-      for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
-      // keys this row may not see: past the diagonal (causal) and past L (the
-      // zero padding of a ragged last tile)
-      const int lim = min(causal && jb + j == qt ? r + 1 : BN, L - (jb + j) * BN);
-      if (lim < BN) {
-#pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i >= lim) sv[i] = -INFINITY;
-      }
-      float gm[8];
-#pragma unroll
-      for (int g = 0; g < 8; ++g) gm[g] = max16(sv + 16 * g);
-      const float mx = max3(max3(gm[0], gm[1], gm[2]), max3(gm[3], gm[4], gm[5]), fmaxf(gm[6], gm[7]));
-      const float m_t = mx * c;
-      const float m_new = fmaxf(m_run, m_t);
-      const bool live = (m_t > -INFINITY) && (m_t >= m_new - kSkipBelow);
-      m_run = m_new;
-      uint32_t codes[4];
-      uint32_t sfw[2] = {0u, 0u};
-      const float corr = (live && have_ref) ? ex2_approx(m_ref - m_t) : 1.f;
-      // whether O must be rescaled to the new tile maximum (warp-uniform)
-      const bool do_corr = j > 0 && __any_sync(0xffffffffu, corr != 1.f);
-      // P^ of tile j goes to buffer j & 1, last read by P.V of tile j-2, whose
-      // completion this thread waited for in tile j-1
-      uint8_t* prow = prow0 + (j & 1) * C::kPBytes;
-      uint8_t* psf = psf0 + (j & 1) * C::kPSfBytes;
-      {
-        // Warp-uniform: a row that skips this tile gets bias = -inf, so its
-        // P2, codes, scales and sum are all zero (the O chunks below use
-        // warp-collective tensor-memory instructions).
-        const float bias = live ? kLog2PRange - m_t : -INFINITY;
-        // group scales s2 = e4m3(max16(P2) / 6) from the group maxima of
-        // P2 = 2^(x*c + bias), and the exponent offsets b_g = bias - log2 s2 so
-        // that P2 / s2 = 2^(x*c + b_g).  A zero scale (the group underflows:
-        // every P2 < 6 * 2^-10) keeps b_g = bias; its values are then below
-        // 0.25 and encode as code 0, and its sum is P2's own.
-        float bg[8], fg[8];
-        uint32_t s16[4];
-#pragma unroll
-        for (int g = 0; g < 8; g += 2) {
-          float a0, a1;
-          fma2(a0, a1, gm[g], gm[g + 1], c, c, bias, bias);
-          a0 = ex2_approx(a0);
-          a1 = ex2_approx(a1);
-          mul2(a0, a1, a0, a1, 1.0f / 6.0f, 1.0f / 6.0f);
-          s16[g / 2] = cvt_e4m3x2(a0, a1);
-          e4m3x2_to_f32(s16[g / 2], fg[g], fg[g + 1]);
-        }
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          fg[g] = fg[g] == 0.f ? 1.f : fg[g];
-          bg[g] = bias - lg2_approx(fg[g]);
-        }
-        sfw[0] = s16[0] | (s16[1] << 16);
-        sfw[1] = s16[2] | (s16[3] << 16);
-        float rs = 0.f;
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          float u[2] = {0.f, 0.f};
-          float* p = sv + 16 * g;
-#pragma unroll
-          for (int i = 0; i < 16; i += 2) {
-            fma2(p[i], p[i + 1], p[i], p[i + 1], c, c, bg[g], bg[g]);
-            p[i] = ex2_approx(p[i]);
-            p[i + 1] = ex2_approx(p[i + 1]);
-            add2(u[0], u[1], u[0], u[1], p[i], p[i + 1]);
-          }
-          rs = fmaf(u[0] + u[1], fg[g], rs);
-          codes[2 * (g & 1)] = cvt_e2m1x8(p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7]);
-          codes[2 * (g & 1) + 1] = cvt_e2m1x8(p[8], p[9], p[10], p[11], p[12], p[13], p[14], p[15]);
-          if (g & 1) {
-            // P^ row r, 16-byte chunk g/2 (two groups), 64B-swizzled: chunk c at
-            // c ^ ((r >> 1) & 3); stored as soon as it is encoded
-            const int ch = g >> 1;
-            *reinterpret_cast<uint4*>(prow + ((ch ^ ((r >> 1) & 3)) * 16)) =
-                make_uint4(codes[0], codes[1], codes[2], codes[3]);
-          }
-        }
-        if (live) {
-          lam = have_ref ? fmaf(lam, corr, rs) : rs;
-          m_ref = m_t;
-          have_ref = true;
-        }
-      }
-      *reinterpret_cast<uint32_t*>(psf) = sfw[0];
-      *reinterpret_cast<uint32_t*>(psf + 512) = sfw[1];
-      if (j > 0) {
-        // O may be rescaled once P.V of the last tile is done (long since, as
-        // a rule: the P work of this tile ran in between)
-        if (!mbar_wait_warp(bars.o_done + q, (j - 1) & 1, abort_flag, wait_ns)) {
+    UnitIter it;
+    unit_iter_init(work, it);
+    AttnUnitRef u;
+    int cq = 0;               // tiles of this query-tile slot so far (over the whole list)
+    bool ok = true;
+    while (ok && unit_next(work, it, u)) {
+      const int nq = q ? u.n[1] : u.n[0];
+      if (q >= u.nq) continue;                         // the unit has no second query tile
+      const int qt = u.qt0 + q;
+      float m_run = -INFINITY, m_ref = 0.f, lam = 0.f;
+      bool have_ref = false;
+      for (int j = 0; j < nq; ++j, ++cq) {
+        if (!mbar_wait_warp(bars.s_full + q, cq & 1, abort_flag, wait_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
-      }
-      if (do_corr) {
-        // the O row to the new tile maximum: all chunks loaded before one
-        // wait (the score registers are free again), scaled, stored back
-        uint32_t o[D / 32][32];
+        uint32_t sr[4][32];
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(lane_addr + ocol + 32 * cc, o[cc]);
-        tmem_ld_wait(o[0]);
+        for (int i = 0; i < 4; ++i) tmem_ld32(lane_addr + C::kColS + 32 * i, sr[i]);
+        tmem_ld_wait(sr[0]);
+        tmem_launder(sr[1]);
+        tmem_launder(sr[2]);
+        tmem_launder(sr[3]);
+        tc_fence_before();
+        mbar_arrive(bars.s_free + q);
+        float sv[128];
 #pragma unroll
-        for (int cc = 1; cc < D / 32; ++cc) tmem_launder(o[cc]);
+        for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
+        // keys this row may not see: past the diagonal (causal) and past L (the
+        // zero padding of a ragged last tile)
+        const int ja = u.jb + j;
+        const int lim = min(causal && ja == qt ? r + 1 : BN, L - ja * BN);
+        if (lim < BN) {
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+          for (int i = 0; i < 128; ++i)
+            if (i >= lim) sv[i] = -INFINITY;
+        }
+        float gm[8];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float x0 = __uint_as_float(o[cc][i]), x1 = __uint_as_float(o[cc][i + 1]);
-            mul2(x0, x1, x0, x1, corr, corr);
-            o[cc][i] = __float_as_uint(x0);
-            o[cc][i + 1] = __float_as_uint(x1);
+        for (int g = 0; g < 8; ++g) gm[g] = max16(sv + 16 * g);
+        const float mx = max3(max3(gm[0], gm[1], gm[2]), max3(gm[3], gm[4], gm[5]), fmaxf(gm[6], gm[7]));
+        const float m_t = mx * c;
+        const float m_new = fmaxf(m_run, m_t);
+        const bool live = (m_t > -INFINITY) && (m_t >= m_new - kSkipBelow);
+        m_run = m_new;
+        uint32_t codes[4];
+        uint32_t sfw[2] = {0u, 0u};
+        const float corr = (live && have_ref) ? ex2_approx(m_ref - m_t) : 1.f;
+        // whether O must be rescaled to the new tile maximum (warp-uniform)
+        const bool do_corr = j > 0 && __any_sync(0xffffffffu, corr != 1.f);
+        // P^ of this tile goes to buffer cq & 1, last read by the P.V two
+        // tiles back, whose completion this thread waited for at the
+        // previous tile (or in the previous unit's epilogue)
+        uint8_t* prow = prow0 + (cq & 1) * C::kPBytes;
+        uint8_t* psf = psf0 + (cq & 1) * C::kPSfBytes;
+        {
+          // Warp-uniform: a row that skips this tile gets bias = -inf, so its
+          // P2, codes, scales and sum are all zero (the O chunks below use
+          // warp-collective tensor-memory instructions).
+          const float bias = live ? kLog2PRange - m_t : -INFINITY;
+          // group scales s2 = e4m3(max16(P2) / 6) from the group maxima of
+          // P2 = 2^(x*c + bias), and the exponent offsets b_g = bias - log2 s2 so
+          // that P2 / s2 = 2^(x*c + b_g).  A zero scale (the group underflows:
+          // every P2 < 6 * 2^-10) keeps b_g = bias; its values are then below
+          // 0.25 and encode as code 0, and its sum is P2's own.
+          float bg[8], fg[8];
+          uint32_t s16[4];
+#pragma unroll
+          for (int g = 0; g < 8; g += 2) {
+            float a0, a1;
+            fma2(a0, a1, gm[g], gm[g + 1], c, c, bias, bias);
+            a0 = ex2_approx(a0);
+            a1 = ex2_approx(a1);
+            mul2(a0, a1, a0, a1, 1.0f / 6.0f, 1.0f / 6.0f);
+            s16[g / 2] = cvt_e4m3x2(a0, a1);
+            e4m3x2_to_f32(s16[g / 2], fg[g], fg[g + 1]);
           }
-          tmem_st32(lane_addr + ocol + 32 * cc, o[cc]);
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            fg[g] = fg[g] == 0.f ? 1.f : fg[g];
+            bg[g] = bias - lg2_approx(fg[g]);
+          }
+          sfw[0] = s16[0] | (s16[1] << 16);
+          sfw[1] = s16[2] | (s16[3] << 16);
+          float rs = 0.f;
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            float uu[2] = {0.f, 0.f};
+            float* pp = sv + 16 * g;
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+              fma2(pp[i], pp[i + 1], pp[i], pp[i + 1], c, c, bg[g], bg[g]);
+              pp[i] = ex2_approx(pp[i]);
+              pp[i + 1] = ex2_approx(pp[i + 1]);
+              add2(uu[0], uu[1], uu[0], uu[1], pp[i], pp[i + 1]);
+            }
+            rs = fmaf(uu[0] + uu[1], fg[g], rs);
+            codes[2 * (g & 1)] = cvt_e2m1x8(pp[0], pp[1], pp[2], pp[3], pp[4], pp[5], pp[6], pp[7]);
+            codes[2 * (g & 1) + 1] = cvt_e2m1x8(pp[8], pp[9], pp[10], pp[11], pp[12], pp[13], pp[14], pp[15]);
+            if (g & 1) {
+              // P^ row r, 16-byte chunk g/2 (two groups), 64B-swizzled: chunk c at
+              // c ^ ((r >> 1) & 3); stored as soon as it is encoded
+              const int ch = g >> 1;
+              *reinterpret_cast<uint4*>(prow + ((ch ^ ((r >> 1) & 3)) * 16)) =
+                  make_uint4(codes[0], codes[1], codes[2], codes[3]);
+            }
+          }
+          if (live) {
+            lam = have_ref ? fmaf(lam, corr, rs) : rs;
+            m_ref = m_t;
+            have_ref = true;
+          }
         }
-        tmem_st_wait();
+        *reinterpret_cast<uint32_t*>(psf) = sfw[0];
+        *reinterpret_cast<uint32_t*>(psf + 512) = sfw[1];
+        if (j > 0) {
+          // O may be rescaled once P.V of the last tile is done (long since, as
+          // a rule: the P work of this tile ran in between)
+          if (!mbar_wait_warp(bars.o_done + q, (cq - 1) & 1, abort_flag, wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        if (do_corr) {
+          // the O row to the new tile maximum: all chunks loaded before one
+          // wait (the score registers are free again), scaled, stored back
+          uint32_t o[D / 32][32];
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(lane_addr + ocol + 32 * cc, o[cc]);
+          tmem_ld_wait(o[0]);
+#pragma unroll
+          for (int cc = 1; cc < D / 32; ++cc) tmem_launder(o[cc]);
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float x0 = __uint_as_float(o[cc][i]), x1 = __uint_as_float(o[cc][i + 1]);
+              mul2(x0, x1, x0, x1, corr, corr);
+              o[cc][i] = __float_as_uint(x0);
+              o[cc][i + 1] = __float_as_uint(x1);
+            }
+            tmem_st32(lane_addr + ocol + 32 * cc, o[cc]);
+          }
+          tmem_st_wait();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bars.p_full + q);
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bars.p_full + q);
-    }
-    const bool row_in = qt * BM + r < L;                // rows of the padding are not stored
-    // split-KV: this CTA's partial result of the row -- O unnormalised (in
-    // units of 2^m_ref / 2688, as is lam), m_ref (-inf if no key tile was
-    // live) and lam -- goes to split sp's slot; a combine pass forms O
-    const bool split = work.nsplit > 1;
-    const long long prow = ((long long)sp * work.nbh + bhq) * Lp + (long long)qt * BM + r;
-    if (split && ok && ntq[q] == 0 && (q == 0 || q1_valid) && row_in)
-      *reinterpret_cast<float2*>(part.ml + 2 * prow) = make_float2(-INFINITY, 0.f);
-    if (ok && ntq[q] > 0 && mbar_wait_warp(bars.o_done + q, (ntq[q] - 1) & 1, abort_flag, wait_ns)) {
-      tc_fence_after();
-      const float inv_l = 1.f / lam;
-      const long long obase = (bhq * L + (long long)qt * BM + r) * D;
-      if (split && row_in)
-        *reinterpret_cast<float2*>(part.ml + 2 * prow) = make_float2(have_ref ? m_ref : -INFINITY, lam);
+      if (!ok) break;
+      // ---- the unit's result for this row: O, or a partial for the combine
+      // pass (O unnormalised in units of 2^m_ref / 2688 as is lam, m_ref
+      // (-inf if no key tile was live) and lam)
+      const bool row_in = qt * BM + r < L;              // rows of the padding are not stored
+      const bool partial = u.slot >= 0;
+      const long long bhq = u.bh;
+      long long prow;
+      if (work.streamk)
+        prow = (long long)u.slot * (2 * BM) + q * BM + r;
+      else
+        prow = ((long long)u.slot * work.nbh + bhq) * Lp + (long long)qt * BM + r;
+      if (partial && nq == 0 && row_in)
+        *reinterpret_cast<float2*>(part.ml + 2 * prow) = make_float2(-INFINITY, 0.f);
+      if (nq > 0) {
+        if (!mbar_wait_warp(bars.o_done + q, (cq - 1) & 1, abort_flag, wait_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float inv_l = 1.f / lam;
+        const long long obase = (bhq * L + (long long)qt * BM + r) * D;
+        if (partial && row_in)
+          *reinterpret_cast<float2*>(part.ml + 2 * prow) = make_float2(have_ref ? m_ref : -INFINITY, lam);
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(lane_addr + ocol + 32 * cc, o);
-        tmem_ld_wait(o);
-        if (!row_in) continue;
-        if (split) {
-          float4* dst = reinterpret_cast<float4*>(part.o + prow * D + 32 * cc);
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + ocol + 32 * cc, o);
+          tmem_ld_wait(o);
+          if (!row_in) continue;
+          if (partial) {
+            float4* dst = reinterpret_cast<float4*>(part.o + prow * D + 32 * cc);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
-                                 __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
-          continue;
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                   __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+            continue;
+          }
+          if constexpr (OUT32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_ptr) + obase + 32 * cc);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                   __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+          } else {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_ptr) + obase + 32 * cc);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
         }
-        if constexpr (OUT32) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_ptr) + obase + 32 * cc);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
-                                 __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
-        } else {
-          uint32_t w[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_ptr) + obase + 32 * cc);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-        }
+        // (the tensor-memory loads above are complete: the next unit's first
+        // P.V, which overwrites O, is issued only after this thread's next
+        // p_full arrival)
       }
     }
   }
@@ -563,12 +643,15 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     attr_done = true;
   }
   int ctas = 0;
-  const AttnWork work = make_attn_work(dm.B, dm.H, dm.L, causal, device_sm_count(), &ctas, nsplit);
+  const AttnWork work = nsplit == kStreamK
+                            ? make_streamk_work(dm.B, dm.H, dm.L, causal, device_sm_count(), &ctas)
+                            : make_attn_work(dm.B, dm.H, dm.L, causal, device_sm_count(), &ctas, nsplit);
   attn_nvfp4_kernel<D, OUT32><<<ctas, kThreads, C::kSmemBytes, s>>>(
       tq, tk, tv, static_cast<const uint8_t*>(x.q_sf), static_cast<const uint8_t*>(x.k_sf),
       static_cast<const uint8_t*>(x.v_sf), o, dm.H, dm.Hkv, dm.L, causal, work, part, kWaitLimitNs);
   cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess && work.nsplit > 1) e = launch_splitkv_combine(part, work.nsplit, dm, o, OUT32, s);
+  if (e == cudaSuccess && work.streamk) e = launch_streamk_combine(work, ctas, part, dm, o, OUT32, s);
+  else if (e == cudaSuccess && work.nsplit > 1) e = launch_splitkv_combine(part, work.nsplit, dm, o, OUT32, s);
   return e;
 }
 

@@ -71,6 +71,22 @@ cudaError_t launch_attn_nvfp4(const CUtensorMap& tq, const CUtensorMap& tk, cons
 cudaError_t launch_splitkv_combine(const SplitOut& part, int nsplit, const Dims& dm, void* o, bool out_f32,
                                    cudaStream_t s);
 
+// Stream-K (nsplit == kStreamK): persistent CTAs, one per SM, over equal
+// ranges of (pair, key tile) items.  A pair cut by a range boundary leaves
+// partial results in two slots per CTA (slot 2c: the CTA's first unit, 2c + 1:
+// its last), 2 * BM rows of d + 2 floats each.
+constexpr int kStreamK = -1;
+inline size_t streamk_workspace_bytes(const Dims& dm, int ctas) {
+  return (size_t)2 * ctas * 256 * ((size_t)dm.d + 2) * sizeof(float);
+}
+struct AttnWork;
+cudaError_t launch_streamk_combine(const AttnWork& w, int ctas, const SplitOut& part, const Dims& dm, void* o,
+                                   bool out_f32, cudaStream_t s);
+inline SplitOut streamk_layout(void* ws, const Dims& dm, int ctas) {
+  float* f = static_cast<float*>(ws);
+  return SplitOut{f, f + (size_t)2 * ctas * 256 * dm.d};
+}
+
 // Per-unit readers of the device error word (each clears its word).
 cudaError_t attn_bf16_read_error(int* out);
 cudaError_t attn_nvfp4_read_error(int* out);

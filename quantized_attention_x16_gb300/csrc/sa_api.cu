@@ -200,13 +200,36 @@ sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v
              : SA_ERR_CUDA;
 }
 
-// Splits for split-KV: `requested` 0 = the library's choice, 1 = none, n > 1 =
-// n (at most one per key tile of the longest query tile's range).
-static int resolve_nsplit(int B, int H, int L, int requested) {
+// The work split: `requested` 0 = the library's choice, 1 = one unit per CTA,
+// n > 1 = split-KV with n shares (at most one per key tile), -1 = stream-K.
+// The library chooses stream-K for the NVFP4 path when the pairs alone can
+// fill every SM (measured on one GB300 in one process, llm_prefill NVFP4
+// attention: 198.7 us for one pair per CTA before the persistent form, 196.6
+// us one pair per CTA now, 194.5 us stream-K, operands L2-resident after the
+// quantiser; 201.4 / 197.3 / 195.2 us after an L2 flush), split-KV when the
+// pairs leave half of the SMs idle and the shares stay long, else one unit
+// per CTA.
+static int resolve_nsplit(int B, int H, int L, int causal, int mode, int requested) {
+  (void)causal;
   if (requested == 1) return 1;
-  if (requested == 0) return choose_nsplit(B, H, L, device_sm_count());
+  if (requested == kStreamK) return kStreamK;
+  const int sms = device_sm_count();
+  if (requested == 0) {
+    const long long pairs = (long long)(((L + 127) / 128 + 1) / 2) * B * H;
+    if (mode == SA_MODE_NVFP4 && sms > 0 && pairs >= sms && streamk_fits(B, H, L)) return kStreamK;
+    return choose_nsplit(B, H, L, sms);
+  }
   const int nkt = (L + 127) / 128;
   return requested < nkt ? requested : nkt;
+}
+
+static size_t work_split_bytes(const Dims& dm, int causal, int nsplit) {
+  if (nsplit == kStreamK) {
+    int ctas = 0;
+    make_streamk_work(dm.B, dm.H, dm.L, causal, device_sm_count() > 0 ? device_sm_count() : 1, &ctas);
+    return streamk_workspace_bytes(dm, ctas);
+  }
+  return splitkv_workspace_bytes(dm, nsplit);
 }
 
 static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int L,
@@ -218,18 +241,28 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
   if (mode_flags & ~(0xF | SA_OUT_FP32)) return SA_ERR_INVALID_ARG;
   const int mode = mode_flags & 0xF;
   if (mode != SA_MODE_BF16 && mode != SA_MODE_NVFP4) return SA_ERR_INVALID_ARG;
-  if (nsplit_req < 0) return SA_ERR_INVALID_ARG;
+  if (nsplit_req < kStreamK) return SA_ERR_INVALID_ARG;
+  if (nsplit_req == kStreamK && (mode != SA_MODE_NVFP4 || !streamk_fits(B, H, L))) return SA_ERR_UNSUPPORTED;
   if (empty_problem(B, L)) return SA_OK;
   const bool out_f32 = (mode_flags & SA_OUT_FP32) != 0;
   if (!aligned16(o)) return SA_ERR_INVALID_ARG;
   const Dims dm{B, H, Hkv, L, d};
-  // split-KV only with a workspace large enough for the partial results
-  int nsplit = resolve_nsplit(B, H, L, nsplit_req);
-  if (nsplit > 1 && nsplit_req > 1 && (workspace == nullptr || workspace_bytes < splitkv_workspace_bytes(dm, nsplit)))
-    return SA_ERR_INVALID_ARG;
-  if (nsplit > 1 && (workspace == nullptr || workspace_bytes < splitkv_workspace_bytes(dm, nsplit))) nsplit = 1;
-  if (nsplit > 1 && !aligned16(workspace)) return SA_ERR_INVALID_ARG;
-  const SplitOut part = nsplit > 1 ? splitkv_layout(workspace, dm, nsplit) : SplitOut{nullptr, nullptr};
+  // split-KV and stream-K only with a workspace large enough for the partial
+  // results (a forced choice without one is an argument error; the library's
+  // own choice then falls back to one unit per CTA)
+  int nsplit = resolve_nsplit(B, H, L, causal, mode, nsplit_req);
+  const bool needs_ws = nsplit > 1 || nsplit == kStreamK;
+  const bool ws_ok = workspace != nullptr && workspace_bytes >= work_split_bytes(dm, causal, nsplit);
+  if (needs_ws && !ws_ok && nsplit_req != 0) return SA_ERR_INVALID_ARG;
+  if (needs_ws && !ws_ok) nsplit = 1;
+  if (nsplit != 1 && !aligned16(workspace)) return SA_ERR_INVALID_ARG;
+  SplitOut part{nullptr, nullptr};
+  if (nsplit > 1) part = splitkv_layout(workspace, dm, nsplit);
+  if (nsplit == kStreamK) {
+    int ctas = 0;
+    make_streamk_work(B, H, L, causal, device_sm_count() > 0 ? device_sm_count() : 1, &ctas);
+    part = streamk_layout(workspace, dm, ctas);
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   CUtensorMap tq, tk, tv;
   if (mode == SA_MODE_BF16) {
@@ -262,11 +295,12 @@ sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o, int 
 }
 
 size_t sa_attn_fwd_workspace_bytes(int B, int H, int Hkv, int L, int d, int causal, int mode, int nsplit) {
-  (void)causal;
-  (void)mode;
-  if (check_dims(B, H, Hkv, L, d) != SA_OK || empty_problem(B, L) || nsplit < 0) return 0;
+  const int m = mode & 0xF;
+  if (check_dims(B, H, Hkv, L, d) != SA_OK || empty_problem(B, L) || nsplit < kStreamK) return 0;
+  if (causal != 0 && causal != 1) return 0;
+  if (nsplit == kStreamK && m != SA_MODE_NVFP4) return 0;
   const Dims dm{B, H, Hkv, L, d};
-  return splitkv_workspace_bytes(dm, resolve_nsplit(B, H, L, nsplit));
+  return work_split_bytes(dm, causal, resolve_nsplit(B, H, L, causal, m, nsplit));
 }
 
 sa_status sa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int L, int d,

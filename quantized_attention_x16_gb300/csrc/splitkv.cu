@@ -18,6 +18,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "work.cuh"
 
 namespace sa {
 namespace {
@@ -73,7 +74,66 @@ cudaError_t launch(const SplitOut& part, int nsplit, const Dims& dm, void* o, cu
   return cudaGetLastError();
 }
 
+// Stream-K: CTAs (k, y) for cut pair k and y in 0..31, eight rows each (one
+// per warp), so the latency-bound row merges run spread over the GPU.  A cut
+// pair's segments -- one per CTA whose range meets it -- are merged into O;
+// pairs no boundary cuts were written whole by the attention kernel.
+template <int D, bool OUT32>
+__global__ void __launch_bounds__(32 * kRowsPerCta) streamk_combine_kernel(const __grid_constant__ StreamKCuts cuts,
+                                                                         const SplitOut part, int L, void* out) {
+  const int* e = cuts.e[blockIdx.x];
+  const int bh = e[0], qt0 = e[1], nq = e[2], cta0 = e[3], nseg = e[4] - e[3] + 1, first_last = e[5];
+  const int rr = blockIdx.y * kRowsPerCta + threadIdx.x / 32;   // row of the pair (query tile rr / 128)
+  const int t = qt0 * 128 + rr;                                  // its token
+  if (rr >= nq * 128 || t >= L) return;
+  const int lane = threadIdx.x % 32;
+  float mmax = -INFINITY;
+  for (int k = 0; k < nseg; ++k) {
+    const long long prow = (long long)(2 * (cta0 + k) + (k == 0 ? first_last : 0)) * 256 + rr;
+    const float2 ml = *reinterpret_cast<const float2*>(part.ml + 2 * prow);
+    if (ml.y > 0.f) mmax = fmaxf(mmax, ml.x);
+  }
+  float acc[D / 32];
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
+  float lsum = 0.f;
+  for (int k = 0; k < nseg; ++k) {
+    const long long prow = (long long)(2 * (cta0 + k) + (k == 0 ? first_last : 0)) * 256 + rr;
+    const float2 ml = *reinterpret_cast<const float2*>(part.ml + 2 * prow);
+    if (!(ml.y > 0.f)) continue;                     // a segment without keys for this row
+    const float wgt = exp2f(ml.x - mmax);
+    lsum = fmaf(wgt, ml.y, lsum);
+    const float* a = part.o + prow * D;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) acc[i] = fmaf(wgt, a[lane + 32 * i], acc[i]);
+  }
+  const float inv = 1.f / lsum;
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) {
+    const long long idx = ((long long)bh * L + t) * D + lane + 32 * i;
+    if constexpr (OUT32)
+      static_cast<float*>(out)[idx] = acc[i] * inv;
+    else
+      static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(acc[i] * inv);
+  }
+}
+
+template <int D, bool OUT32>
+cudaError_t launch_sk(const AttnWork& w, int ctas, const SplitOut& part, const Dims& dm, void* o, cudaStream_t s) {
+  StreamKCuts cuts;
+  make_streamk_cuts(w, ctas, &cuts);
+  if (cuts.n == 0) return cudaSuccess;               // no pair was cut
+  streamk_combine_kernel<D, OUT32><<<dim3(cuts.n, 256 / kRowsPerCta), 32 * kRowsPerCta, 0, s>>>(cuts, part, dm.L, o);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_streamk_combine(const AttnWork& w, int ctas, const SplitOut& part, const Dims& dm, void* o,
+                                   bool out_f32, cudaStream_t s) {
+  if (dm.d == 64) return out_f32 ? launch_sk<64, true>(w, ctas, part, dm, o, s) : launch_sk<64, false>(w, ctas, part, dm, o, s);
+  return out_f32 ? launch_sk<128, true>(w, ctas, part, dm, o, s) : launch_sk<128, false>(w, ctas, part, dm, o, s);
+}
 
 cudaError_t launch_splitkv_combine(const SplitOut& part, int nsplit, const Dims& dm, void* o, bool out_f32,
                                    cudaStream_t s) {

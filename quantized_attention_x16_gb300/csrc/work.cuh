@@ -20,6 +20,8 @@
 
 namespace sa {
 
+constexpr int kMaxStreamKCtas = 160;   // persistent grid cap (one CTA per SM)
+
 struct AttnWork {
   int nqt;     // 128-row query tiles per head
   int ppr;     // pair slots per head, ceil(nqt / 2)
@@ -27,6 +29,9 @@ struct AttnWork {
   int npair;   // units [0, npair) are pairs; then 2 * (ppr * nbh - npair) singles
   int causal;
   int nsplit;  // key-range splits per pair (1: none)
+  int streamk; // 1: persistent CTAs over equal ranges of (pair, key tile) items
+  long long items;   // stream-K: total items (key tiles over all pairs)
+  int sk_x0[kMaxStreamKCtas + 1];   // stream-K: first item of CTA c's range (c = 0..C)
 };
 
 // Host: the work list for a problem and the number of CTAs to launch.
@@ -37,6 +42,8 @@ inline AttnWork make_attn_work(int B, int H, int L, int causal, int num_sms, int
   w.nbh = B * H;
   w.causal = causal;
   w.nsplit = nsplit > 1 ? nsplit : 1;
+  w.streamk = 0;
+  w.items = 0;
   const long long pairs = (long long)w.ppr * w.nbh;
   if (w.nsplit > 1) {
     w.npair = (int)pairs;
@@ -51,6 +58,140 @@ inline AttnWork make_attn_work(int B, int H, int L, int causal, int num_sms, int
   w.npair = (int)(pairs - split);
   *ctas = (int)(pairs + split);
   return w;
+}
+
+// ---------------------------------------------------------------- stream-K
+// Persistent scheduling: the pairs (in dispatch order, no singles) are laid
+// end to end as "items", one per key tile of the pair's union key range, and
+// CTA c of C takes items [c*T/C, (c+1)*T/C).  Every SM then gets the same
+// number of key-tile steps; a pair cut by a range boundary is computed in
+// segments whose partial results a combine pass merges.
+
+// Key tiles of pair slot p (dispatch order): the union of its query tiles'
+// ranges (causal: up to the diagonal of its second query tile).
+__host__ __device__ inline int sk_pair_tiles(const AttnWork& w, long long p) {
+  const int nkt = w.nqt;
+  if (!w.causal) return nkt;
+  const int pi = w.ppr - 1 - (int)(p / w.nbh);
+  const int qt0 = 2 * pi;
+  return qt0 + 1 < w.nqt ? qt0 + 2 : qt0 + 1;
+}
+
+// Items before pair slot p.
+__host__ __device__ inline long long sk_prefix(const AttnWork& w, long long p) {
+  if (!w.causal) return p * w.nqt;
+  const long long g = p / w.nbh;                  // whole groups of nbh pairs before p
+  // group g' holds pairs of index pi = ppr-1-g' with 2*(ppr-g') tiles, one
+  // fewer for g' = 0 when the head has an odd number of query tiles
+  long long t = (long long)w.nbh * (2 * g * w.ppr - g * (g - 1));
+  if ((w.nqt & 1) && g > 0) t -= w.nbh;
+  return t + (p - g * w.nbh) * sk_pair_tiles(w, p);
+}
+
+// The pair holding item x (0 <= x < items).
+__host__ __device__ inline long long sk_pair_of(const AttnWork& w, long long x) {
+  long long lo = 0, hi = (long long)w.ppr * w.nbh - 1;
+  while (lo < hi) {                               // last p with prefix(p) <= x
+    const long long mid = (lo + hi + 1) / 2;
+    if (sk_prefix(w, mid) <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// First item of CTA c's range, and the CTA whose range holds item x.
+__host__ __device__ inline long long sk_start(const AttnWork& w, long long c, long long C) {
+  return c * w.items / C;
+}
+__host__ __device__ inline long long sk_cta_of(const AttnWork& w, long long x, long long C) {
+  return ((x + 1) * C - 1) / w.items;
+}
+
+// One unit of a CTA's work: query tiles qt0 (and qt0 + 1 if nq == 2) of head
+// bh, key tiles [jb, jb + n[q]) for query tile q, and where its result goes:
+// slot -1 = O itself; split-KV = share index; stream-K = partial slot
+// 2c (the CTA's first unit) or 2c + 1 (its last).
+struct AttnUnitRef {
+  int bh, qt0, nq, jb, n[2], slot;
+};
+
+__host__ __device__ inline void pair_head(const AttnWork& w, long long p, int& bh, int& qt0, int& nq) {
+  int pi;
+  if (w.causal) {
+    pi = w.ppr - 1 - (int)(p / w.nbh);
+    bh = (int)(p % w.nbh);
+  } else {
+    pi = (int)(p % w.ppr);
+    bh = (int)(p / w.ppr);
+  }
+  qt0 = 2 * pi;
+  nq = (qt0 + 1 < w.nqt) ? 2 : 1;
+}
+
+// Walks the units of one CTA; every warp role of the CTA walks the same list.
+struct UnitIter {
+  int x, xe, p;     // stream-K: next item, end of range, its pair
+  int x0;           // stream-K: first item of the range
+  int done;
+};
+
+// Host: the stream-K work list (pairs only) and its grid, one CTA per SM (or
+// per item when there are fewer items).
+// The ranges are fixed on the host (first items in sk_x0, 32-bit: stream-K
+// is used only while the item count fits).
+inline AttnWork make_streamk_work(int B, int H, int L, int causal, int num_sms, int* ctas) {
+  AttnWork w = make_attn_work(B, H, L, causal, num_sms, ctas, 2);   // pairs only
+  w.nsplit = 1;
+  w.streamk = 1;
+  w.items = sk_prefix(w, (long long)w.ppr * w.nbh);
+  long long c = w.items < num_sms ? w.items : num_sms;
+  if (c > kMaxStreamKCtas) c = kMaxStreamKCtas;
+  if (c < 1) c = 1;
+  for (long long i = 0; i <= c; ++i) w.sk_x0[i] = (int)sk_start(w, i, c);
+  *ctas = (int)c;
+  return w;
+}
+inline bool streamk_fits(int B, int H, int L) {
+  const long long nqt = (L + 127) / 128;
+  return (nqt + 1) / 2 * (long long)B * H * nqt < (1ll << 31);
+}
+
+// The pairs that range boundaries cut, for the combine pass: per cut pair its
+// head, first query tile and query-tile count, the first and last CTA whose
+// range meets it (cta0, cta1), and whether it is cta0's last unit (cta0_last;
+// otherwise it begins cta0's range).  Segment k of the pair sits in slot
+// 2 (cta0 + k) + (k == 0 && cta0_last).
+struct StreamKCuts {
+  int n;
+  int e[kMaxStreamKCtas][6];   // bh, qt0, nq, cta0, cta1, cta0_last
+};
+inline void make_streamk_cuts(const AttnWork& w, int C, StreamKCuts* cuts) {
+  cuts->n = 0;
+  auto cta_of = [&](long long x) {             // last CTA whose range starts at or before x
+    int c = 0;
+    while (c + 1 < C && w.sk_x0[c + 1] <= x) ++c;
+    return c;
+  };
+  for (int c = 1; c < C; ++c) {
+    const long long x = w.sk_x0[c];
+    if (x >= w.items) break;
+    const long long p = sk_pair_of(w, x), P = sk_prefix(w, p);
+    if (x == P || w.sk_x0[c - 1] > P) continue;   // no cut, or an earlier boundary cut this pair
+    int* e = cuts->e[cuts->n++];
+    const int nt = sk_pair_tiles(w, p);
+    int pi;
+    if (w.causal) {
+      pi = w.ppr - 1 - (int)(p / w.nbh);
+      e[0] = (int)(p % w.nbh);
+    } else {
+      pi = (int)(p % w.ppr);
+      e[0] = (int)(p / w.ppr);
+    }
+    e[1] = 2 * pi;
+    e[2] = 2 * pi + 1 < w.nqt ? 2 : 1;
+    e[3] = cta_of(P);
+    e[4] = cta_of(P + nt - 1);
+    e[5] = w.sk_x0[e[3]] < P ? 1 : 0;
+  }
 }
 
 // Splits of the key range for split-KV, chosen only while the pairs alone
@@ -77,7 +218,7 @@ __device__ __forceinline__ int padded_len_dev(int L) { return (L + 127) & ~127; 
 // each query tile q, given each query tile's full count n[q] (query tile 1
 // never has fewer than query tile 0): the union of the pair's key tiles is
 // cut into nsplit near-equal contiguous pieces.
-__device__ __forceinline__ int split_range(int sp, int nsplit, int (&n)[2]) {
+__host__ __device__ inline int split_range(int sp, int nsplit, int (&n)[2]) {
   const int nun = n[1] > n[0] ? n[1] : n[0];
   const int jb = sp * nun / nsplit, je = (sp + 1) * nun / nsplit;
 #pragma unroll
@@ -86,6 +227,37 @@ __device__ __forceinline__ int split_range(int sp, int nsplit, int (&n)[2]) {
     n[q] = e > jb ? e - jb : 0;
   }
   return jb;
+}
+
+// Stream-K range walk of CTA `cta` (host-callable, for tests of the schedule).
+__host__ __device__ inline void sk_iter_init(const AttnWork& w, int cta, UnitIter& it) {
+  it.done = 0;
+  it.x0 = w.sk_x0[cta];
+  it.x = it.x0;
+  it.xe = w.sk_x0[cta + 1];
+  it.p = it.x < it.xe ? (int)sk_pair_of(w, it.x) : 0;
+}
+__host__ __device__ inline bool sk_next(const AttnWork& w, int cta, UnitIter& it, AttnUnitRef& u) {
+  if (it.x >= it.xe) return false;
+  const int P = (int)sk_prefix(w, it.p);
+  const int nt = sk_pair_tiles(w, it.p);
+  const int a = it.x - P;
+  const int b = it.xe - P < nt ? it.xe - P : nt;
+  pair_head(w, it.p, u.bh, u.qt0, u.nq);
+  u.jb = a;
+  const int n0 = w.causal ? u.qt0 + 1 : w.nqt;
+  const int n1 = u.nq == 2 ? (w.causal ? u.qt0 + 2 : w.nqt) : 0;
+  u.n[0] = (n0 < b ? n0 : b) > a ? (n0 < b ? n0 : b) - a : 0;
+  u.n[1] = (n1 < b ? n1 : b) > a ? (n1 < b ? n1 : b) - a : 0;
+  u.slot = (a == 0 && b == nt) ? -1 : 2 * cta + (it.x == it.x0 ? 0 : 1);
+  it.x = P + b;
+  ++it.p;
+  return true;
+}
+
+__device__ __forceinline__ void unit_iter_init(const AttnWork& w, UnitIter& it) {
+  it.done = 0;
+  if (w.streamk) sk_iter_init(w, blockIdx.x, it);
 }
 
 // Device: (b*H + h, first query tile, number of query tiles, split) of unit u.
@@ -108,6 +280,27 @@ __device__ __forceinline__ void attn_unit(const AttnWork& w, int u, int& bh, int
     qt0 += (u - w.npair) & 1;
     nq = 1;
   }
+}
+
+}  // namespace sa
+
+namespace sa {
+
+// Next unit of this CTA (false when none is left).
+__device__ __forceinline__ bool unit_next(const AttnWork& w, UnitIter& it, AttnUnitRef& u) {
+  if (it.done) return false;
+  if (!w.streamk) {
+    // one unit: this CTA's entry of the work list (a share of it under split-KV)
+    int sp;
+    attn_unit(w, (int)blockIdx.x, u.bh, u.qt0, u.nq, sp);
+    u.n[0] = w.causal ? u.qt0 + 1 : w.nqt;
+    u.n[1] = u.nq == 2 ? (w.causal ? u.qt0 + 2 : w.nqt) : 0;
+    u.jb = w.nsplit > 1 ? split_range(sp, w.nsplit, u.n) : 0;
+    u.slot = w.nsplit > 1 ? sp : -1;
+    it.done = 1;
+    return true;
+  }
+  return sk_next(w, (int)blockIdx.x, it, u);
 }
 
 }  // namespace sa

@@ -102,8 +102,13 @@ def test_argument_errors_launch_nothing(sa):
         assert lib.sa_attn_fwd_host_workspace_bytes(B, 2, 2, L, 64, 1, 0) == 0
     assert lib.sa_attn_fwd(z, z, z, z, 0, 2, 2, 256, 96, 0, 0, None) == sa.SA_ERR_UNSUPPORTED   # d still checked
     # split-KV: a forced split needs a workspace; a negative split count is invalid
+    s_ptr = ctypes.cast(ctypes.pointer(sa.SaFp4Qkv(*([1 << 20] * 8))), ctypes.c_void_p)
     assert lib.sa_attn_fwd_ws(p, p, p, p, 1, 2, 2, 1024, 64, 0, 0, 4, z, 0, None) == sa.SA_ERR_INVALID_ARG
-    assert lib.sa_attn_fwd_ws(p, p, p, p, 1, 2, 2, 1024, 64, 0, 0, -1, p, 1 << 30, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_attn_fwd_ws(p, p, p, p, 1, 2, 2, 1024, 64, 0, 0, -2, p, 1 << 30, None) == sa.SA_ERR_INVALID_ARG
+    # nsplit -1 (stream-K) is an NVFP4-path schedule; it also needs a workspace
+    assert lib.sa_attn_fwd_ws(p, p, p, p, 1, 2, 2, 1024, 64, 0, 0, -1, p, 1 << 30, None) == sa.SA_ERR_UNSUPPORTED
+    assert lib.sa_attn_fwd_workspace_bytes(1, 2, 2, 1024, 64, 0, 0, -1) == 0
+    assert lib.sa_attn_fwd_ws(s_ptr, z, z, p, 1, 2, 2, 1024, 64, 0, 1, -1, z, 0, None) == sa.SA_ERR_INVALID_ARG
     need = lib.sa_attn_fwd_workspace_bytes(1, 2, 2, 1024, 64, 0, 0, 4)
     assert need == 4 * (1 * 2 * 1024) * (64 + 2) * 4                       # partial O rows plus (m, l)
     assert lib.sa_attn_fwd_ws(p, p, p, p, 1, 2, 2, 1024, 64, 0, 0, 4, p, need - 16, None) == sa.SA_ERR_INVALID_ARG

@@ -222,3 +222,40 @@ def test_split_kv_library_choice(sa, case, mode):
     o32 = run_split(sa, x, w["causal"], mode, 0, torch.float32) if mode == "nvfp4" else None
     rows = np.array(W.sample_rows(w["L"], 192, seed=w["seed"]))
     check(o, x, w["causal"], [(0, 0), (w["B"] - 1, w["H"] - 1)], rows, mode, o32)
+
+
+# Stream-K (NVFP4 path): persistent CTAs over equal ranges of (pair, key tile)
+# items.  Forced on small problems every CTA holds a few items, so pairs are
+# cut into many segments and the combine pass merges them all; at full size
+# it is the library's own choice once the pairs fill the SMs.
+STREAMK = [
+    dict(W.spec("tiny")),                                                   # 2 tiles of work per head
+    dict(W.spec("causal_gqa"), B=1, H=4, Hkv=2, L=640, seed=61),            # causal, GQA, odd pairs
+    dict(W.spec("dit_video"), B=2, H=2, Hkv=1, L=333, d=64, seed=62),       # ragged L, MQA, d = 64
+    dict(W.spec("llm_prefill"), B=1, H=2, Hkv=2, L=1024, seed=63),
+    dict(W.spec("tiny"), B=1, H=1, Hkv=1, L=77, seed=64),                   # a single partial tile
+]
+
+
+@pytest.mark.parametrize("w", STREAMK, ids=_id)
+def test_streamk_small_all_rows(sa, w):
+    x = W.make_inputs(w)
+    o = run_split(sa, x, w["causal"], "nvfp4", -1)
+    o32 = run_split(sa, x, w["causal"], "nvfp4", -1, torch.float32)
+    heads = [(b, h) for b in range(w["B"]) for h in range(w["H"])]
+    check(o, x, w["causal"], heads, np.arange(w["L"]), "nvfp4", o32)
+    ref = run_gpu(sa, x, w["causal"], "nvfp4", torch.float32)          # one unit per CTA
+    assert np.abs(o32 - ref).max() <= 1e-5 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("name", ["llm_prefill", "causal_gqa"])
+def test_streamk_full_size(sa, name):
+    w = W.spec(name)
+    assert sa.sa_attn_fwd_workspace_bytes(w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["causal"], "nvfp4", -1) > 0
+    x = W.make_inputs(w)
+    o = run_split(sa, x, w["causal"], "nvfp4", -1)
+    o32 = run_split(sa, x, w["causal"], "nvfp4", -1, torch.float32)
+    rows = np.array(W.sample_rows(w["L"], 192, seed=w["seed"]))
+    check(o, x, w["causal"], [(0, 0), (w["B"] - 1, w["H"] - 1)], rows, "nvfp4", o32)
+    ref = run_gpu(sa, x, w["causal"], "nvfp4", torch.float32)
+    assert np.abs(o32 - ref).max() <= 1e-5 * np.abs(ref).max()
