@@ -14,7 +14,8 @@
  *
  * Conventions for every entry point:
  *  - Tensors are device pointers, row-major, BHLD: Q and O are [B, H, L, d],
- *    K and V are [B, Hkv, L, d], all bfloat16.  The softmax scale is
+ *    K and V are [B, Hkv, L, d], all bfloat16 (or BLHD, [B, L, heads, d],
+ *    with the SA_LAYOUT_BLHD flag where an entry point takes it).  The softmax scale is
  *    1/sqrt(d); causal means key j is visible to query i iff j <= i.
  *  - Ownership: the caller allocates and owns every buffer.  The library
  *    allocates no device memory and keeps no state between calls other than
@@ -60,6 +61,15 @@ typedef enum { SA_MODE_BF16 = 0, SA_MODE_NVFP4 = 1 } sa_mode;
  * o is float32 [B, H, L, d] (the FP32 accumulator divided by the row sum,
  * without the final bf16 rounding); without it o is bfloat16. */
 #define SA_OUT_FP32 16
+
+/* Layout flag, OR-ed into `mode` (sa_attn_fwd, sa_attn_fwd_ws) or `flags`
+ * (sa_quantize_ex): the bf16 tensors q, k, v (and o, bf16 or float32) are
+ * [B, L, heads, d] ("BLHD", d contiguous) instead of [B, heads, L, d].  The
+ * quantised operands keep the one layout documented below whatever the
+ * inputs' layout, and the results are bit-identical to the BHLD calls on the
+ * same values.  Not accepted by sa_attn_fwd_host and
+ * sa_quantize_static_scratch. */
+#define SA_LAYOUT_BLHD 32
 
 /*
  * Quantised operands produced by sa_quantize (device pointers, caller-owned).
@@ -122,6 +132,13 @@ sa_status sa_fp4_qkv_from_blob(void* blob, int B, int H, int Hkv, int L, int d,
 sa_status sa_quantize(const void* q, const void* k, const void* v,
                       int B, int H, int Hkv, int L, int d,
                       const sa_fp4_qkv* out, sa_stream_t stream);
+
+/* sa_quantize_ex -- sa_quantize with `flags`: 0 or SA_LAYOUT_BLHD (q, k, v
+ * given as [B, L, heads, d]); the outputs are the same bytes as sa_quantize
+ * on the BHLD tensors with the same values. */
+sa_status sa_quantize_ex(const void* q, const void* k, const void* v,
+                         int B, int H, int Hkv, int L, int d, int flags,
+                         const sa_fp4_qkv* out, sa_stream_t stream);
 
 /*
  * sa_quantize_static_scratch -- sa_quantize for callers that cannot allocate

@@ -27,9 +27,11 @@ LIB_PATH = os.path.join(HERE, "libsa.so")
 SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA, SA_ERR_TIMEOUT = range(5)
 SA_MODE_BF16, SA_MODE_NVFP4 = 0, 1
 SA_OUT_FP32 = 16
+SA_LAYOUT_BLHD = 32
 
 #: every symbol include/sa.h declares
-EXPORTS = ("sa_fp4_qkv_bytes", "sa_fp4_qkv_from_blob", "sa_quantize", "sa_quantize_static_scratch", "sa_attn_fwd",
+EXPORTS = ("sa_fp4_qkv_bytes", "sa_fp4_qkv_from_blob", "sa_quantize", "sa_quantize_ex", "sa_quantize_static_scratch",
+           "sa_attn_fwd",
            "sa_attn_fwd_workspace_bytes", "sa_attn_fwd_ws",
            "sa_attn_fwd_host_workspace_bytes", "sa_attn_fwd_host",
            "sa_status_string", "sa_last_device_error", "sa_selftest_wait_timeout", "sa_version")
@@ -54,6 +56,8 @@ def _load():
     lib.sa_fp4_qkv_from_blob.restype = i
     lib.sa_quantize.argtypes = [vp, vp, vp, i, i, i, i, i, ctypes.POINTER(SaFp4Qkv), vp]
     lib.sa_quantize.restype = i
+    lib.sa_quantize_ex.argtypes = [vp, vp, vp, i, i, i, i, i, i, ctypes.POINTER(SaFp4Qkv), vp]
+    lib.sa_quantize_ex.restype = i
     lib.sa_quantize_static_scratch.argtypes = [vp, vp, vp, i, i, i, i, i, ctypes.POINTER(SaFp4Qkv), vp]
     lib.sa_quantize_static_scratch.restype = i
     lib.sa_attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
@@ -160,15 +164,27 @@ class FP4QKV:
         return out
 
 
-def sa_quantize(q, k, v, out=None, stream=None):
-    """Smooth-K + NVFP4 quantisation of bf16 BHLD tensors; returns an FP4QKV."""
+def _dims(q, k, layout):
+    """(B, H, Hkv, L, d) of q [B, H, L, d] / k [B, Hkv, L, d] (layout "bhld") or
+    q [B, L, H, d] / k [B, L, Hkv, d] ("blhd"), and the layout flag."""
+    if layout == "bhld":
+        B, H, L, d = q.shape
+        return (B, H, k.shape[1], L, d), 0
+    if layout == "blhd":
+        B, L, H, d = q.shape
+        return (B, H, k.shape[2], L, d), SA_LAYOUT_BLHD
+    raise ValueError(f"unknown layout {layout!r}")
+
+
+def sa_quantize(q, k, v, out=None, stream=None, layout="bhld"):
+    """Smooth-K + NVFP4 quantisation of bf16 tensors (layout "bhld" or
+    "blhd"); returns an FP4QKV (the quantised layout is the same either way)."""
     _bf16_cuda(q, "q"), _bf16_cuda(k, "k"), _bf16_cuda(v, "v")
-    B, H, L, d = q.shape
-    Hkv = k.shape[1]
+    (B, H, Hkv, L, d), flag = _dims(q, k, layout)
     if out is None:
         out = FP4QKV(B, H, Hkv, L, d, device=q.device)
-    _check(lib.sa_quantize(_ptr(q), _ptr(k), _ptr(v), B, H, Hkv, L, d, ctypes.byref(out.struct), _stream(stream)),
-           "sa_quantize")
+    _check(lib.sa_quantize_ex(_ptr(q), _ptr(k), _ptr(v), B, H, Hkv, L, d, flag, ctypes.byref(out.struct),
+                              _stream(stream)), "sa_quantize_ex")
     return out
 
 
@@ -192,18 +208,21 @@ def sa_attn_fwd_workspace_bytes(B, H, Hkv, L, d, causal=False, mode="bf16", nspl
 
 
 def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=None, stream=None,
-                nsplit=None, workspace=None):
+                nsplit=None, workspace=None, layout="bhld"):
     """Fused attention forward.  mode "bf16": q, k, v bf16 BHLD tensors.
     mode "nvfp4": q is an FP4QKV from sa_quantize, k and v None.
     out_dtype: torch.bfloat16 (default) or torch.float32 (SA_OUT_FP32).
     nsplit None: sa_attn_fwd (no split-KV); otherwise sa_attn_fwd_ws with that
     nsplit (0 = the library's choice) and `workspace` (a uint8 CUDA tensor,
-    allocated here when None).  Returns o."""
+    allocated here when None).  layout "bhld" or "blhd" (q, k, v and o as
+    [B, L, heads, d]; with nvfp4 it applies to o).  Returns o."""
     import torch
+    if layout not in ("bhld", "blhd"):
+        raise ValueError(f"unknown layout {layout!r}")
+    lflag = SA_LAYOUT_BLHD if layout == "blhd" else 0
     if mode == "bf16":
         _bf16_cuda(q, "q"), _bf16_cuda(k, "k"), _bf16_cuda(v, "v")
-        B, H, L, d = q.shape
-        Hkv = k.shape[1]
+        (B, H, Hkv, L, d), _ = _dims(q, k, layout)
         args = (_ptr(q), _ptr(k), _ptr(v))
         m = SA_MODE_BF16
         dev = q.device
@@ -222,10 +241,12 @@ def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=
         raise ValueError("out_dtype must be torch.bfloat16 or torch.float32")
     if out_dtype == torch.float32:
         m |= SA_OUT_FP32
+    m |= lflag
+    oshape = (B, L, H, d) if lflag else (B, H, L, d)
     if o is None:
-        o = torch.empty((B, H, L, d), dtype=out_dtype, device=dev)
-    if not (o.is_cuda and o.dtype == out_dtype and o.is_contiguous() and tuple(o.shape) == (B, H, L, d)):
-        raise ValueError("o must be a contiguous CUDA tensor of shape (B, H, L, d) and dtype out_dtype")
+        o = torch.empty(oshape, dtype=out_dtype, device=dev)
+    if not (o.is_cuda and o.dtype == out_dtype and o.is_contiguous() and tuple(o.shape) == oshape):
+        raise ValueError(f"o must be a contiguous CUDA tensor of shape {oshape} and dtype out_dtype")
     if nsplit is None:
         _check(lib.sa_attn_fwd(*args, _ptr(o), B, H, Hkv, L, d, int(bool(causal)), m, _stream(stream)),
                "sa_attn_fwd")

@@ -83,7 +83,8 @@ template <int D, bool OUT32>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, void* __restrict__ out_ptr, int H, int Hkv,
-                     int L, int causal, const AttnWork work, const SplitOut part, uint64_t wait_ns) {
+                     int L, int causal, const AttnWork work, const SplitOut part, const Strides so,
+                     uint64_t wait_ns) {
   using C = CfgBF16<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -134,8 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  const int bhq = b * H + h, bhk = b * Hkv + hk;            // head index of the 3-D Q/O and K/V maps
-  const long long q_row0 = (long long)bhq * L;             // first row of this head in O
+  const int bhq = b * H + h;                                // head index of the partial results
+  const long long obase0 = (long long)b * so.b + (long long)h * so.h;   // this head in O
 
   if (warp >= 8) {
     // Register split: the launch gives every thread kLaunchRegs; this
@@ -156,8 +157,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(bars.q_full, nq * C::kTileBytes);
         for (int q = 0; q < nq; ++q)
           for (int hh = 0; hh < D / 64; ++hh)
-            tma_load_3d(smem + C::kOffQ + q * C::kTileBytes + hh * C::kHalfBytes, &tmap_q, bars.q_full, hh * 64,
-                        (qt0 + q) * BM, bhq);
+            tma_load_4d(smem + C::kOffQ + q * C::kTileBytes + hh * C::kHalfBytes, &tmap_q, bars.q_full, hh * 64,
+                        (qt0 + q) * BM, h, b);
       }
       int issued = 0;
       for (int j = 0; j < nt; ++j) {
@@ -168,8 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) {
           mbar_arrive_expect_tx(bars.k_full + s, C::kTileBytes);
           for (int hh = 0; hh < D / 64; ++hh)
-            tma_load_3d(smem + C::kOffK + s * C::kTileBytes + hh * C::kHalfBytes, &tmap_k, bars.k_full + s,
-                        hh * 64, y, bhk);
+            tma_load_4d(smem + C::kOffK + s * C::kTileBytes + hh * C::kHalfBytes, &tmap_k, bars.k_full + s,
+                        hh * 64, y, hk, b);
         }
         if (j >= C::NS && !mbar_wait_backoff_warp(bars.v_empty + s, par, abort_flag, wait_ns, kProducerSleepNs)) {
           issued = 2 * j + 1;
@@ -178,8 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) {
           mbar_arrive_expect_tx(bars.v_full + s, C::kTileBytes);
           for (int hh = 0; hh < D / 64; ++hh)
-            tma_load_3d(smem + C::kOffV + s * C::kTileBytes + hh * C::kHalfBytes, &tmap_v, bars.v_full + s,
-                        hh * 64, y, bhk);
+            tma_load_4d(smem + C::kOffV + s * C::kTileBytes + hh * C::kHalfBytes, &tmap_v, bars.v_full + s,
+                        hh * 64, y, hk, b);
         }
         issued = 2 * j + 2;
       }
@@ -379,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && ntq[q] > 0 && mbar_wait_warp(bars.o_done + q, (ntq[q] - 1) & 1, abort_flag, wait_ns)) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      const long long obase = (q_row0 + (long long)qt * BM + r) * D;
+      const long long obase = obase0 + ((long long)qt * BM + r) * so.t;
       if (split && row_in) *reinterpret_cast<float2*>(part.ml + 2 * prow) = make_float2(m_use, l);
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
@@ -423,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D, bool OUT32>
-cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o, const Dims& dm,
-                     int causal, int nsplit, const SplitOut& part, cudaStream_t s) {
+cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o, const Strides& so,
+                     const Dims& dm, int causal, int nsplit, const SplitOut& part, cudaStream_t s) {
   using C = CfgBF16<D>;
   static bool attr_done = false;   // the attribute is a property of the function, set once per process
   if (!attr_done) {
@@ -442,21 +443,21 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   int ctas = 0;
   const AttnWork work = make_attn_work(dm.B, dm.H, dm.L, causal, device_sm_count(), &ctas, nsplit);
   attn_bf16_kernel<D, OUT32><<<ctas, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, o, dm.H, dm.Hkv, dm.L, causal,
-                                                                    work, part, kWaitLimitNs);
+                                                                    work, part, so, kWaitLimitNs);
   cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess && work.nsplit > 1) e = launch_splitkv_combine(part, work.nsplit, dm, o, OUT32, s);
+  if (e == cudaSuccess && work.nsplit > 1) e = launch_splitkv_combine(part, work.nsplit, dm, o, so, OUT32, s);
   return e;
 }
 
 }  // namespace
 
 cudaError_t launch_attn_bf16(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o,
-                             const Dims& dm, int causal, bool out_f32, int nsplit, const SplitOut& part,
-                             cudaStream_t s) {
-  if (dm.d == 64) return out_f32 ? launch_d<64, true>(tq, tk, tv, o, dm, causal, nsplit, part, s)
-                                 : launch_d<64, false>(tq, tk, tv, o, dm, causal, nsplit, part, s);
-  return out_f32 ? launch_d<128, true>(tq, tk, tv, o, dm, causal, nsplit, part, s)
-                 : launch_d<128, false>(tq, tk, tv, o, dm, causal, nsplit, part, s);
+                             const Strides& so, const Dims& dm, int causal, bool out_f32, int nsplit,
+                             const SplitOut& part, cudaStream_t s) {
+  if (dm.d == 64) return out_f32 ? launch_d<64, true>(tq, tk, tv, o, so, dm, causal, nsplit, part, s)
+                                 : launch_d<64, false>(tq, tk, tv, o, so, dm, causal, nsplit, part, s);
+  return out_f32 ? launch_d<128, true>(tq, tk, tv, o, so, dm, causal, nsplit, part, s)
+                 : launch_d<128, false>(tq, tk, tv, o, so, dm, causal, nsplit, part, s);
 }
 
 cudaError_t attn_bf16_read_error(int* out) { return read_and_clear_device_error(out); }

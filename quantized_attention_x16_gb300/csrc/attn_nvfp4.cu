@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmap_v, const uint8_t* __restrict__ q_sf,
                       const uint8_t* __restrict__ k_sf, const uint8_t* __restrict__ v_sf,
                       void* __restrict__ out_ptr, int H, int Hkv, int L, int causal, const AttnWork work,
-                      const SplitOut part, uint64_t wait_ns) {
+                      const SplitOut part, const Strides so, uint64_t wait_ns) {
   using C = CfgF4<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const float inv_l = 1.f / lam;
-        const long long obase = (bhq * L + (long long)qt * BM + r) * D;
+        const long long obase = (bhq / H) * so.b + (bhq % H) * so.h + ((long long)qt * BM + r) * so.t;
         if (partial && row_in)
           *reinterpret_cast<float2*>(part.ml + 2 * prow) = make_float2(have_ref ? m_ref : -INFINITY, lam);
 #pragma unroll 1
@@ -627,7 +627,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool OUT32>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const sa_fp4_qkv& x,
-                     void* o, const Dims& dm, int causal, int nsplit, const SplitOut& part, cudaStream_t s) {
+                     void* o, const Strides& so, const Dims& dm, int causal, int nsplit, const SplitOut& part,
+                     cudaStream_t s) {
   using C = CfgF4<D>;
   static bool attr_done = false;
   if (!attr_done) {
@@ -648,22 +649,22 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
                             : make_attn_work(dm.B, dm.H, dm.L, causal, device_sm_count(), &ctas, nsplit);
   attn_nvfp4_kernel<D, OUT32><<<ctas, kThreads, C::kSmemBytes, s>>>(
       tq, tk, tv, static_cast<const uint8_t*>(x.q_sf), static_cast<const uint8_t*>(x.k_sf),
-      static_cast<const uint8_t*>(x.v_sf), o, dm.H, dm.Hkv, dm.L, causal, work, part, kWaitLimitNs);
+      static_cast<const uint8_t*>(x.v_sf), o, dm.H, dm.Hkv, dm.L, causal, work, part, so, kWaitLimitNs);
   cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess && work.streamk) e = launch_streamk_combine(work, ctas, part, dm, o, OUT32, s);
-  else if (e == cudaSuccess && work.nsplit > 1) e = launch_splitkv_combine(part, work.nsplit, dm, o, OUT32, s);
+  if (e == cudaSuccess && work.streamk) e = launch_streamk_combine(work, ctas, part, dm, o, so, OUT32, s);
+  else if (e == cudaSuccess && work.nsplit > 1) e = launch_splitkv_combine(part, work.nsplit, dm, o, so, OUT32, s);
   return e;
 }
 
 }  // namespace
 
 cudaError_t launch_attn_nvfp4(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const sa_fp4_qkv& qkv, void* o, const Dims& dm, int causal, bool out_f32, int nsplit,
-                              const SplitOut& part, cudaStream_t s) {
-  if (dm.d == 64) return out_f32 ? launch_d<64, true>(tq, tk, tv, qkv, o, dm, causal, nsplit, part, s)
-                                 : launch_d<64, false>(tq, tk, tv, qkv, o, dm, causal, nsplit, part, s);
-  return out_f32 ? launch_d<128, true>(tq, tk, tv, qkv, o, dm, causal, nsplit, part, s)
-                 : launch_d<128, false>(tq, tk, tv, qkv, o, dm, causal, nsplit, part, s);
+                              const sa_fp4_qkv& qkv, void* o, const Strides& so, const Dims& dm, int causal,
+                              bool out_f32, int nsplit, const SplitOut& part, cudaStream_t s) {
+  if (dm.d == 64) return out_f32 ? launch_d<64, true>(tq, tk, tv, qkv, o, so, dm, causal, nsplit, part, s)
+                                 : launch_d<64, false>(tq, tk, tv, qkv, o, so, dm, causal, nsplit, part, s);
+  return out_f32 ? launch_d<128, true>(tq, tk, tv, qkv, o, so, dm, causal, nsplit, part, s)
+                 : launch_d<128, false>(tq, tk, tv, qkv, o, so, dm, causal, nsplit, part, s);
 }
 
 cudaError_t attn_nvfp4_read_error(int* out) { return read_and_clear_device_error(out); }

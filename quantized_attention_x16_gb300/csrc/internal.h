@@ -17,6 +17,17 @@ struct Dims {
 // quantised layout (rows past L hold zero codes and zero scales).
 inline int padded_len(int L) { return (L + 127) & ~127; }
 
+// Element strides of a bf16 (or float32 output) tensor of `heads` heads with d
+// contiguous: element (b, h, t, c) sits at b*b_ + h*h_ + t*t_ + c.  BHLD
+// ([B, heads, L, d]) and BLHD ([B, L, heads, d], flag SA_LAYOUT_BLHD).
+struct Strides {
+  long long b, h, t;
+};
+inline Strides layout_strides(bool blhd, int heads, int L, int d) {
+  return blhd ? Strides{(long long)L * heads * d, d, (long long)heads * d}
+              : Strides{(long long)heads * L * d, (long long)L * d, d};
+}
+
 // Number of SMs of the current device (cached per device; 0 if unknown).
 inline int device_sm_count() {
   static int cache[64] = {};
@@ -34,8 +45,8 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // quant.cu
 // tq / tk: bf16 Q and K as [rows][d], boxes of 64 channels x 128 rows, 128B swizzle.
-cudaError_t launch_quantize(const void* q, const void* k, const void* v, const Dims& dm, const sa_fp4_qkv& out,
-                            const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t s);
+cudaError_t launch_quantize(const void* q, const void* k, const void* v, const Dims& dm, bool blhd,
+                            const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t s);
 // Same kernels, K-mean partial sums in the library's fixed per-device array.
 constexpr size_t kStaticScratchFloats = SA_STATIC_SCRATCH_FLOATS;
 cudaError_t launch_quantize_static_scratch(const void* q, const void* k, const void* v, const Dims& dm,
@@ -61,15 +72,15 @@ inline SplitOut splitkv_layout(void* ws, const Dims& dm, int nsplit) {
 
 // attn_bf16.cu
 cudaError_t launch_attn_bf16(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o,
-                             const Dims& dm, int causal, bool out_f32, int nsplit, const SplitOut& part,
-                             cudaStream_t s);
+                             const Strides& so, const Dims& dm, int causal, bool out_f32, int nsplit,
+                             const SplitOut& part, cudaStream_t s);
 // attn_nvfp4.cu
 cudaError_t launch_attn_nvfp4(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const sa_fp4_qkv& qkv, void* o, const Dims& dm, int causal, bool out_f32,
-                              int nsplit, const SplitOut& part, cudaStream_t s);
+                              const sa_fp4_qkv& qkv, void* o, const Strides& so, const Dims& dm, int causal,
+                              bool out_f32, int nsplit, const SplitOut& part, cudaStream_t s);
 // splitkv.cu: O from the nsplit partial results of every row t < L.
-cudaError_t launch_splitkv_combine(const SplitOut& part, int nsplit, const Dims& dm, void* o, bool out_f32,
-                                   cudaStream_t s);
+cudaError_t launch_splitkv_combine(const SplitOut& part, int nsplit, const Dims& dm, void* o, const Strides& so,
+                                   bool out_f32, cudaStream_t s);
 
 // Stream-K (nsplit == kStreamK): persistent CTAs, one per SM, over equal
 // ranges of (pair, key tile) items.  A pair cut by a range boundary leaves
@@ -81,7 +92,7 @@ inline size_t streamk_workspace_bytes(const Dims& dm, int ctas) {
 }
 struct AttnWork;
 cudaError_t launch_streamk_combine(const AttnWork& w, int ctas, const SplitOut& part, const Dims& dm, void* o,
-                                   bool out_f32, cudaStream_t s);
+                                   const Strides& so, bool out_f32, cudaStream_t s);
 inline SplitOut streamk_layout(void* ws, const Dims& dm, int ctas) {
   float* f = static_cast<float*>(ws);
   return SplitOut{f, f + (size_t)2 * ctas * 256 * dm.d};

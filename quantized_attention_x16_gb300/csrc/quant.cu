@@ -124,6 +124,8 @@ struct QuantArgs {
   float* part;      // scratch: chunk sums [B*Hkv][Lp/128][D]
   float* kmean;     // [B*Hkv][D]
   int L, Lp, nbh_q, nbh_kv, chunks_per_cta;
+  int H, Hkv;                       // heads of Q and of K / V (bh = b * heads + h)
+  Strides sq, skv;                  // element strides of the bf16 Q and K / V (BHLD or BLHD)
   int tiles_per_head;               // Q/K tiles of kRows tokens per head
   int ntile_q, ntile_k, nblk_v;
   int nclu_mean, nclu_v;            // launch 1: mean clusters, V clusters
@@ -184,12 +186,13 @@ __device__ __forceinline__ void issue_tile_qk(const QuantArgs& a, const CUtensor
   int bh, t0;
   tile_head(a, tile, T::kRows, is_k, bh, t0);
   const CUtensorMap* map = is_k ? tk : tq;
+  const int heads = is_k ? a.Hkv : a.H;
   mbar_arrive_expect_tx(bar, T::kBoxes * T::kBoxBytes);
 #pragma unroll
   for (int b = 0; b < T::kBoxes; ++b) {
     const int x = D == 128 ? 64 * b : 0;
     const int y = D == 128 ? t0 : t0 + 128 * b;
-    tma_load_3d(dst + b * T::kBoxBytes, map, bar, x, y, bh);
+    tma_load_4d(dst + b * T::kBoxBytes, map, bar, x, y, bh % heads, bh / heads);
   }
 }
 
@@ -231,15 +234,18 @@ __device__ __forceinline__ void quant_v_cta(const QuantArgs& a, int blk) {
   const long long bh = piece / npb;
   const int tp = (int)(piece % npb);
   const int nvalid = a.L - tp * 32;                     // tokens of this piece below L (may be <= 0)
-  const uint32_t* src = reinterpret_cast<const uint32_t*>(a.v + ((size_t)bh * a.L + (size_t)tp * 32) * D + c);
+  const long long vb = bh / a.Hkv, vh = bh % a.Hkv;
+  const uint32_t* src =
+      reinterpret_cast<const uint32_t*>(a.v + vb * a.skv.b + vh * a.skv.h + (long long)tp * 32 * a.skv.t + c);
+  const size_t tstep = (size_t)(a.skv.t / 2);           // token stride in bf16 pairs
   uint32_t w[32];
   if (nvalid >= 32) {
 #pragma unroll
-    for (int t = 0; t < 32; ++t) w[t] = __ldg(src + (size_t)t * (D / 2));
+    for (int t = 0; t < 32; ++t) w[t] = __ldg(src + t * tstep);
   } else {
     // the ragged end of the head: tokens past L count as zeros
 #pragma unroll
-    for (int t = 0; t < 32; ++t) w[t] = t < nvalid ? __ldg(src + (size_t)t * (D / 2)) : 0u;
+    for (int t = 0; t < 32; ++t) w[t] = t < nvalid ? __ldg(src + t * tstep) : 0u;
   }
   uint8_t* sblk = a.vsf + ((size_t)bh * (a.Lp / 64) + tp / 2) * 512 + (tp % 2) * 2;
 #pragma unroll
@@ -274,8 +280,10 @@ __device__ __forceinline__ void mean_cluster(const QuantArgs& a, int bh) {
   const int first = (int)rank * cpc, last = min(nchunk, first + cpc);
   const int c = 2 * (threadIdx.x % kPairs);
   for (int ch = first + (int)threadIdx.x / kPairs; ch < last; ch += kChunksAtOnce) {
-    const uint32_t* src =
-        reinterpret_cast<const uint32_t*>(a.k + ((size_t)bh * a.L + (size_t)ch * kMeanChunk) * D + c);
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(a.k + (long long)(bh / a.Hkv) * a.skv.b +
+                                                            (long long)(bh % a.Hkv) * a.skv.h +
+                                                            (long long)ch * kMeanChunk * a.skv.t + c);
+    const size_t tstep = (size_t)(a.skv.t / 2);         // token stride in bf16 pairs
     float acc0 = 0.f, acc1 = 0.f;
     const int nvalid = a.L - ch * kMeanChunk;           // tokens of this chunk below L
 #pragma unroll 1
@@ -284,7 +292,7 @@ __device__ __forceinline__ void mean_cluster(const QuantArgs& a, int bh) {
       // sum starts at +0 and never becomes -0)
       uint32_t w[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) w[i] = t0 + i < nvalid ? __ldg(src + (size_t)(t0 + i) * (D / 2)) : 0u;
+      for (int i = 0; i < 32; ++i) w[i] = t0 + i < nvalid ? __ldg(src + (t0 + i) * tstep) : 0u;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         acc0 = __fadd_rn(acc0, __uint_as_float(w[i] << 16));
@@ -387,7 +395,7 @@ __global__ void __launch_bounds__(kThreadsQ) quant_qk_kernel(const __grid_consta
 }
 
 template <int D>
-cudaError_t launch_quantize_impl(const void* q, const void* k, const void* v, const Dims& dm,
+cudaError_t launch_quantize_impl(const void* q, const void* k, const void* v, const Dims& dm, bool blhd,
                                  const sa_fp4_qkv& out, float* partials, const CUtensorMap& tq,
                                  const CUtensorMap& tk, cudaStream_t s) {
   using T = TileQK<D>;
@@ -405,6 +413,10 @@ cudaError_t launch_quantize_impl(const void* q, const void* k, const void* v, co
   a.kmean = out.k_mean;
   a.L = dm.L;
   a.Lp = padded_len(dm.L);
+  a.H = dm.H;
+  a.Hkv = dm.Hkv;
+  a.sq = layout_strides(blhd, dm.H, dm.L, dm.d);
+  a.skv = layout_strides(blhd, dm.Hkv, dm.L, dm.d);
   a.nbh_q = dm.B * dm.H;
   a.nbh_kv = dm.B * dm.Hkv;
   const int nchunk = a.Lp / kMeanChunk;
@@ -433,11 +445,11 @@ cudaError_t launch_quantize_impl(const void* q, const void* k, const void* v, co
 
 }  // namespace
 
-cudaError_t launch_quantize(const void* q, const void* k, const void* v, const Dims& dm, const sa_fp4_qkv& out,
-                            const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t s) {
+cudaError_t launch_quantize(const void* q, const void* k, const void* v, const Dims& dm, bool blhd,
+                            const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t s) {
   float* part = static_cast<float*>(out.workspace);
-  return dm.d == 64 ? launch_quantize_impl<64>(q, k, v, dm, out, part, tq, tk, s)
-                    : launch_quantize_impl<128>(q, k, v, dm, out, part, tq, tk, s);
+  return dm.d == 64 ? launch_quantize_impl<64>(q, k, v, dm, blhd, out, part, tq, tk, s)
+                    : launch_quantize_impl<128>(q, k, v, dm, blhd, out, part, tq, tk, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -484,8 +496,8 @@ cudaError_t launch_quantize_static_scratch(const void* q, const void* k, const v
   // Every chunk sum read is written first by the same call (its first
   // launch), so earlier contents of the array never reach the outputs and
   // nothing needs clearing.
-  return dm.d == 64 ? launch_quantize_impl<64>(q, k, v, dm, out, part, tq, tk, s)
-                    : launch_quantize_impl<128>(q, k, v, dm, out, part, tq, tk, s);
+  return dm.d == 64 ? launch_quantize_impl<64>(q, k, v, dm, false, out, part, tq, tk, s)
+                    : launch_quantize_impl<128>(q, k, v, dm, false, out, part, tq, tk, s);
 }
 
 }  // namespace sa

@@ -45,24 +45,26 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// bf16 [B*heads][L][d] as a 3-D map (channel, token, head) with boxes of 64
-// channels x 128 tokens x 1 head, 128B swizzle (the tiles of the BF16 attention
-// kernel and the quantiser): a tile that runs past the head's last token reads
-// zeros there instead of the next head's rows.
-bool make_bf16_head_map(CUtensorMap* m, const void* base, int heads, const Dims& dm) {
+// bf16 [B][heads][L][d] (or BLHD) as a 4-D map (channel, token, head, batch)
+// with boxes of 64 channels x 128 tokens x 1 x 1, 128B swizzle (the tiles of
+// the BF16 attention kernel and the quantiser): a tile that runs past the
+// head's last token reads zeros there instead of another head's rows.
+bool make_bf16_head_map(CUtensorMap* m, const void* base, int heads, const Dims& dm, bool blhd) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)dm.d, (cuuint64_t)dm.L, (cuuint64_t)heads};
-  const cuuint64_t strides[2] = {(cuuint64_t)dm.d * 2, (cuuint64_t)dm.L * dm.d * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  const Strides st = layout_strides(blhd, heads, dm.L, dm.d);
+  const cuuint64_t dims[4] = {(cuuint64_t)dm.d, (cuuint64_t)dm.L, (cuuint64_t)heads, (cuuint64_t)dm.B};
+  const cuuint64_t strides[3] = {(cuuint64_t)st.t * 2, (cuuint64_t)st.h * 2, (cuuint64_t)st.b * 2};
+  const cuuint32_t box[4] = {64, 128, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_bf16_row_maps(const void* q, const void* k, const Dims& dm, CUtensorMap* tq, CUtensorMap* tk) {
-  return make_bf16_head_map(tq, q, dm.B * dm.H, dm) && make_bf16_head_map(tk, k, dm.B * dm.Hkv, dm);
+bool make_bf16_row_maps(const void* q, const void* k, const Dims& dm, bool blhd, CUtensorMap* tq,
+                        CUtensorMap* tk) {
+  return make_bf16_head_map(tq, q, dm.H, dm, blhd) && make_bf16_head_map(tk, k, dm.Hkv, dm, blhd);
 }
 
 // SA_OK for a problem the kernels take, or the error to return.  Empty
@@ -167,18 +169,25 @@ static bool fp4_ptrs_ok(const sa_fp4_qkv* x) {
          aligned16(x->v_codes) && aligned16(x->v_sf) && aligned16(x->k_mean) && aligned16(x->workspace);
 }
 
-sa_status sa_quantize(const void* q, const void* k, const void* v, int B, int H, int Hkv, int L, int d,
-                      const sa_fp4_qkv* out, sa_stream_t stream) {
+sa_status sa_quantize_ex(const void* q, const void* k, const void* v, int B, int H, int Hkv, int L, int d, int flags,
+                         const sa_fp4_qkv* out, sa_stream_t stream) {
   const sa_status st = check_dims(B, H, Hkv, L, d);
   if (st != SA_OK) return st;
+  if (flags & ~SA_LAYOUT_BLHD) return SA_ERR_INVALID_ARG;
   if (empty_problem(B, L)) return SA_OK;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !fp4_ptrs_ok(out)) return SA_ERR_INVALID_ARG;
   const Dims dm{B, H, Hkv, L, d};
+  const bool blhd = (flags & SA_LAYOUT_BLHD) != 0;
   CUtensorMap tq, tk;
-  if (!make_bf16_row_maps(q, k, dm, &tq, &tk)) return SA_ERR_CUDA;
-  return launch_quantize(q, k, v, dm, *out, tq, tk, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+  if (!make_bf16_row_maps(q, k, dm, blhd, &tq, &tk)) return SA_ERR_CUDA;
+  return launch_quantize(q, k, v, dm, blhd, *out, tq, tk, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? SA_OK
              : SA_ERR_CUDA;
+}
+
+sa_status sa_quantize(const void* q, const void* k, const void* v, int B, int H, int Hkv, int L, int d,
+                      const sa_fp4_qkv* out, sa_stream_t stream) {
+  return sa_quantize_ex(q, k, v, B, H, Hkv, L, d, 0, out, stream);
 }
 
 sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v, int B, int H, int Hkv, int L,
@@ -193,7 +202,7 @@ sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v
     return SA_ERR_INVALID_ARG;
   const Dims dm{B, H, Hkv, L, d};
   CUtensorMap tq, tk;
-  if (!make_bf16_row_maps(q, k, dm, &tq, &tk)) return SA_ERR_CUDA;
+  if (!make_bf16_row_maps(q, k, dm, false, &tq, &tk)) return SA_ERR_CUDA;
   return launch_quantize_static_scratch(q, k, v, dm, *out, tq, tk, reinterpret_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? SA_OK
@@ -238,15 +247,17 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
   const sa_status st = check_dims(B, H, Hkv, L, d);
   if (st != SA_OK) return st;
   if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
-  if (mode_flags & ~(0xF | SA_OUT_FP32)) return SA_ERR_INVALID_ARG;
+  if (mode_flags & ~(0xF | SA_OUT_FP32 | SA_LAYOUT_BLHD)) return SA_ERR_INVALID_ARG;
   const int mode = mode_flags & 0xF;
   if (mode != SA_MODE_BF16 && mode != SA_MODE_NVFP4) return SA_ERR_INVALID_ARG;
   if (nsplit_req < kStreamK) return SA_ERR_INVALID_ARG;
   if (nsplit_req == kStreamK && (mode != SA_MODE_NVFP4 || !streamk_fits(B, H, L))) return SA_ERR_UNSUPPORTED;
   if (empty_problem(B, L)) return SA_OK;
   const bool out_f32 = (mode_flags & SA_OUT_FP32) != 0;
+  const bool blhd = (mode_flags & SA_LAYOUT_BLHD) != 0;
   if (!aligned16(o)) return SA_ERR_INVALID_ARG;
   const Dims dm{B, H, Hkv, L, d};
+  const Strides so = layout_strides(blhd, H, L, d);            // O (and Q) strides
   // split-KV and stream-K only with a workspace large enough for the partial
   // results (a forced choice without one is an argument error; the library's
   // own choice then falls back to one unit per CTA)
@@ -267,11 +278,11 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
   CUtensorMap tq, tk, tv;
   if (mode == SA_MODE_BF16) {
     if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return SA_ERR_INVALID_ARG;
-    if (!make_bf16_head_map(&tq, q, B * H, dm) || !make_bf16_head_map(&tk, k, B * Hkv, dm) ||
-        !make_bf16_head_map(&tv, v, B * Hkv, dm))
+    if (!make_bf16_head_map(&tq, q, H, dm, blhd) || !make_bf16_head_map(&tk, k, Hkv, dm, blhd) ||
+        !make_bf16_head_map(&tv, v, Hkv, dm, blhd))
       return SA_ERR_CUDA;
-    return launch_attn_bf16(tq, tk, tv, o, dm, causal, out_f32, nsplit, part, s) == cudaSuccess ? SA_OK
-                                                                                                : SA_ERR_CUDA;
+    return launch_attn_bf16(tq, tk, tv, o, so, dm, causal, out_f32, nsplit, part, s) == cudaSuccess ? SA_OK
+                                                                                                    : SA_ERR_CUDA;
   }
   if (k != nullptr || v != nullptr || q == nullptr) return SA_ERR_INVALID_ARG;
   const sa_fp4_qkv* x = static_cast<const sa_fp4_qkv*>(q);
@@ -285,8 +296,9 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
       !make_map(&tk, u8, x->k_codes, d / 2, (uint64_t)B * Hkv * Lp, 1, d / 2, 128, qk_swz) ||
       !make_map(&tv, u8, x->v_codes, Lp / 2, (uint64_t)B * Hkv * d, 1, 64, d, CU_TENSOR_MAP_SWIZZLE_64B))
     return SA_ERR_CUDA;
-  return launch_attn_nvfp4(tq, tk, tv, *x, o, dm, causal, out_f32, nsplit, part, s) == cudaSuccess ? SA_OK
-                                                                                                  : SA_ERR_CUDA;
+  return launch_attn_nvfp4(tq, tk, tv, *x, o, so, dm, causal, out_f32, nsplit, part, s) == cudaSuccess
+             ? SA_OK
+             : SA_ERR_CUDA;
 }
 
 sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int L, int d,

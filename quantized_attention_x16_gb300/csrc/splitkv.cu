@@ -28,7 +28,8 @@ constexpr int kRowsPerCta = 8;
 template <int D, bool OUT32>
 __global__ void __launch_bounds__(32 * kRowsPerCta) splitkv_combine_kernel(const SplitOut part, int nsplit,
                                                                          long long nrows, int L, int Lp,
-                                                                         long long split_rows, void* out) {
+                                                                         long long split_rows, int H,
+                                                                         const Strides so, void* out) {
   const long long row = (long long)blockIdx.x * kRowsPerCta + threadIdx.x / 32;
   if (row >= nrows) return;
   const int lane = threadIdx.x % 32;
@@ -55,7 +56,7 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) splitkv_combine_kernel(const
   const float inv = 1.f / lsum;
 #pragma unroll
   for (int i = 0; i < D / 32; ++i) {
-    const long long idx = row * D + lane + 32 * i;
+    const long long idx = (bh / H) * so.b + (bh % H) * so.h + (row % L) * so.t + lane + 32 * i;
     if constexpr (OUT32)
       static_cast<float*>(out)[idx] = acc[i] * inv;
     else
@@ -64,13 +65,13 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) splitkv_combine_kernel(const
 }
 
 template <int D, bool OUT32>
-cudaError_t launch(const SplitOut& part, int nsplit, const Dims& dm, void* o, cudaStream_t s) {
+cudaError_t launch(const SplitOut& part, int nsplit, const Dims& dm, void* o, const Strides& so, cudaStream_t s) {
   const long long nrows = (long long)dm.B * dm.H * dm.L;
   const int Lp = padded_len(dm.L);
   const long long split_rows = (long long)dm.B * dm.H * Lp;
   const long long ctas = (nrows + kRowsPerCta - 1) / kRowsPerCta;
   splitkv_combine_kernel<D, OUT32><<<(unsigned)ctas, 32 * kRowsPerCta, 0, s>>>(part, nsplit, nrows, dm.L, Lp,
-                                                                              split_rows, o);
+                                                                              split_rows, dm.H, so, o);
   return cudaGetLastError();
 }
 
@@ -80,7 +81,8 @@ cudaError_t launch(const SplitOut& part, int nsplit, const Dims& dm, void* o, cu
 // pairs no boundary cuts were written whole by the attention kernel.
 template <int D, bool OUT32>
 __global__ void __launch_bounds__(32 * kRowsPerCta) streamk_combine_kernel(const __grid_constant__ StreamKCuts cuts,
-                                                                         const SplitOut part, int L, void* out) {
+                                                                         const SplitOut part, int L, int H,
+                                                                         const Strides so, void* out) {
   const int* e = cuts.e[blockIdx.x];
   const int bh = e[0], qt0 = e[1], nq = e[2], cta0 = e[3], nseg = e[4] - e[3] + 1, first_last = e[5];
   const int rr = blockIdx.y * kRowsPerCta + threadIdx.x / 32;   // row of the pair (query tile rr / 128)
@@ -110,7 +112,7 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) streamk_combine_kernel(const
   const float inv = 1.f / lsum;
 #pragma unroll
   for (int i = 0; i < D / 32; ++i) {
-    const long long idx = ((long long)bh * L + t) * D + lane + 32 * i;
+    const long long idx = (long long)(bh / H) * so.b + (long long)(bh % H) * so.h + (long long)t * so.t + lane + 32 * i;
     if constexpr (OUT32)
       static_cast<float*>(out)[idx] = acc[i] * inv;
     else
@@ -119,26 +121,30 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) streamk_combine_kernel(const
 }
 
 template <int D, bool OUT32>
-cudaError_t launch_sk(const AttnWork& w, int ctas, const SplitOut& part, const Dims& dm, void* o, cudaStream_t s) {
+cudaError_t launch_sk(const AttnWork& w, int ctas, const SplitOut& part, const Dims& dm, void* o, const Strides& so,
+                      cudaStream_t s) {
   StreamKCuts cuts;
   make_streamk_cuts(w, ctas, &cuts);
   if (cuts.n == 0) return cudaSuccess;               // no pair was cut
-  streamk_combine_kernel<D, OUT32><<<dim3(cuts.n, 256 / kRowsPerCta), 32 * kRowsPerCta, 0, s>>>(cuts, part, dm.L, o);
+  streamk_combine_kernel<D, OUT32><<<dim3(cuts.n, 256 / kRowsPerCta), 32 * kRowsPerCta, 0, s>>>(cuts, part, dm.L,
+                                                                                                dm.H, so, o);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_streamk_combine(const AttnWork& w, int ctas, const SplitOut& part, const Dims& dm, void* o,
-                                   bool out_f32, cudaStream_t s) {
-  if (dm.d == 64) return out_f32 ? launch_sk<64, true>(w, ctas, part, dm, o, s) : launch_sk<64, false>(w, ctas, part, dm, o, s);
-  return out_f32 ? launch_sk<128, true>(w, ctas, part, dm, o, s) : launch_sk<128, false>(w, ctas, part, dm, o, s);
+                                   const Strides& so, bool out_f32, cudaStream_t s) {
+  if (dm.d == 64)
+    return out_f32 ? launch_sk<64, true>(w, ctas, part, dm, o, so, s) : launch_sk<64, false>(w, ctas, part, dm, o, so, s);
+  return out_f32 ? launch_sk<128, true>(w, ctas, part, dm, o, so, s) : launch_sk<128, false>(w, ctas, part, dm, o, so, s);
 }
 
-cudaError_t launch_splitkv_combine(const SplitOut& part, int nsplit, const Dims& dm, void* o, bool out_f32,
-                                   cudaStream_t s) {
-  if (dm.d == 64) return out_f32 ? launch<64, true>(part, nsplit, dm, o, s) : launch<64, false>(part, nsplit, dm, o, s);
-  return out_f32 ? launch<128, true>(part, nsplit, dm, o, s) : launch<128, false>(part, nsplit, dm, o, s);
+cudaError_t launch_splitkv_combine(const SplitOut& part, int nsplit, const Dims& dm, void* o, const Strides& so,
+                                   bool out_f32, cudaStream_t s) {
+  if (dm.d == 64)
+    return out_f32 ? launch<64, true>(part, nsplit, dm, o, so, s) : launch<64, false>(part, nsplit, dm, o, so, s);
+  return out_f32 ? launch<128, true>(part, nsplit, dm, o, so, s) : launch<128, false>(part, nsplit, dm, o, so, s);
 }
 
 }  // namespace sa
