@@ -32,10 +32,18 @@ def _kv_head(h, H, Hkv):
     return h // (H // Hkv)
 
 
+def causal_offset(Lq, Lkv):
+    """Key positions visible to query i under the causal mask: j <= i + off,
+    off = Lkv - Lq (the queries are the last Lq positions of the key
+    sequence; off = 0 for self-attention, Lq = Lkv)."""
+    return Lkv - Lq
+
+
 def exact_attention(q, k, v, causal, scale=None, rows=None, block=1024):
     """O = softmax(Q K^T * scale + mask) V in FP64, per (b, h).
 
-    q [B,H,L,d]; k, v [B,Hkv,L,d] (any float arrays; promoted to float64).
+    q [B,H,Lq,d]; k, v [B,Hkv,Lkv,d] (any float arrays; promoted to float64).
+    Causal: key j visible to query i iff j <= i + Lkv - Lq.
     rows: optional 1-D array of query indices to evaluate (default all).
     Returns float64 [B, H, len(rows), d]."""
     q = np.asarray(q, np.float64)
@@ -43,6 +51,7 @@ def exact_attention(q, k, v, causal, scale=None, rows=None, block=1024):
     v = np.asarray(v, np.float64)
     B, H, L, d = q.shape
     Hkv = k.shape[1]
+    off = causal_offset(L, k.shape[2])
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     rows = np.arange(L) if rows is None else np.asarray(rows)
@@ -55,7 +64,7 @@ def exact_attention(q, k, v, causal, scale=None, rows=None, block=1024):
                 r = rows[s0:s0 + block]
                 s = (q[b, h, r] @ k[b, kh].T) * scale
                 if causal:
-                    s = np.where(cols[None, :] <= r[:, None], s, -np.inf)
+                    s = np.where(cols[None, :] <= r[:, None] + off, s, -np.inf)
                 s = s - np.max(s, axis=1, keepdims=True)
                 p = np.exp(s)
                 p = p / np.sum(p, axis=1, keepdims=True)
@@ -64,12 +73,13 @@ def exact_attention(q, k, v, causal, scale=None, rows=None, block=1024):
 
 
 def sa3_tile_rows(qrows, kh, vh, row_idx, causal, bc=128, scale=None,
-                  quantize_p=True, debug=None, tie_rel=0.0, return_bound=False):
+                  quantize_p=True, debug=None, tie_rel=0.0, return_bound=False, off=0):
     """SA3 emulation for a set of query rows of one head.
 
     qrows [n, d]: dequantised Q^ rows; kh [L, d]: dequantised smoothed K^';
     vh [L, d]: dequantised V^ (all float64, exact grid values).
-    row_idx [n]: the query positions (for the causal mask).
+    row_idx [n]: the query positions (for the causal mask: key j visible iff
+    j <= row + off, off = Lkv - Lq).
 
     Per KV tile j of ``bc`` keys, in the order of online softmax:
       x     = (Q^ K^'^T) * scale * log2(e)                  (base-2 logits)
@@ -106,7 +116,7 @@ def sa3_tile_rows(qrows, kh, vh, row_idx, causal, bc=128, scale=None,
         j1 = min(L, j0 + bc)
         x = x_all[:, j0:j1]
         cols = np.arange(j0, j1)
-        vis = (cols[None, :] <= row_idx[:, None]) if causal else np.ones(x.shape, bool)
+        vis = (cols[None, :] <= row_idx[:, None] + off) if causal else np.ones(x.shape, bool)
         x = np.where(vis, x, -np.inf)
         m_t = np.max(x, axis=1)
         live = np.isfinite(m_t)
@@ -144,12 +154,13 @@ def sa3_emulated_attention(qd, kd, vd, causal, bc=128, scale=None, rows=None,
                            quantize_p=True, tie_rel=0.0, return_bound=False):
     """Tile-by-tile SA3 emulation over all heads.
 
-    qd [B,H,L,d], kd [B,Hkv,L,d], vd [B,Hkv,L,d]: dequantised Q^, K^' (after
-    smooth-K) and V^ (token-major), float64.  Returns [B, H, len(rows), d]
+    qd [B,H,Lq,d], kd [B,Hkv,Lkv,d], vd [B,Hkv,Lkv,d]: dequantised Q^, K^'
+    (after smooth-K) and V^ (token-major), float64.  Returns [B, H, len(rows), d]
     (and the decision-ambiguity bound of ``sa3_tile_rows`` if asked)."""
     qd = np.asarray(qd, np.float64)
     B, H, L, d = qd.shape
     Hkv = kd.shape[1]
+    off = causal_offset(L, kd.shape[2])
     rows = np.arange(L) if rows is None else np.asarray(rows)
     out = np.empty((B, H, len(rows), d), np.float64)
     bound = np.zeros_like(out)
@@ -158,7 +169,7 @@ def sa3_emulated_attention(qd, kd, vd, causal, bc=128, scale=None, rows=None,
             kh = _kv_head(h, H, Hkv)
             r = sa3_tile_rows(qd[b, h, rows], kd[b, kh], vd[b, kh], rows, causal, bc=bc,
                               scale=scale, quantize_p=quantize_p, tie_rel=tie_rel,
-                              return_bound=return_bound)
+                              return_bound=return_bound, off=off)
             if return_bound:
                 out[b, h], bound[b, h] = r
             else:

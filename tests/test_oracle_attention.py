@@ -298,3 +298,54 @@ def test_ambiguity_bound_covers_a_perturbed_implementation(seed):
     err = np.abs(sim - em[0, 0])
     M = np.abs(em).max()
     assert np.all(err <= bound[0, 0] + 1e-5 * M)
+
+
+# ---- query length different from key length (decode, chunked prefill) ----
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Lq,Lkv", [(1, 37), (5, 40), (40, 40), (17, 96)])
+def test_exact_lq_lkv_matches_brute_force(Lq, Lkv, causal):
+    rng = np.random.default_rng(Lq * 100 + Lkv)
+    d = 8
+    q = rng.standard_normal((1, 2, Lq, d))
+    k = rng.standard_normal((1, 1, Lkv, d))
+    v = rng.standard_normal((1, 1, Lkv, d))
+    got = A.exact_attention(q, k, v, causal)
+    for h in range(2):
+        for i in range(Lq):
+            w = []
+            for j in range(Lkv):
+                if causal and j > i + (Lkv - Lq):       # bottom-right aligned
+                    w.append(0.0)
+                else:
+                    w.append(np.exp(float(q[0, h, i] @ k[0, 0, j]) / np.sqrt(d)))
+            w = np.array(w) / sum(w)
+            assert np.allclose(got[0, h, i], w @ v[0, 0], atol=1e-12)
+
+
+@pytest.mark.parametrize("Lq", [1, 7, 64])
+def test_causal_suffix_queries_equal_the_full_problem_rows(Lq):
+    # the queries of a chunk are the last Lq positions: their outputs are the
+    # last Lq rows of causal self-attention over all Lkv positions
+    rng = np.random.default_rng(3 + Lq)
+    Lkv, d = 96, 16
+    qf = rng.standard_normal((1, 2, Lkv, d))
+    k = rng.standard_normal((1, 2, Lkv, d))
+    v = rng.standard_normal((1, 2, Lkv, d))
+    full = A.exact_attention(qf, k, v, True)
+    part = A.exact_attention(qf[:, :, -Lq:], k, v, True)
+    assert np.allclose(part, full[:, :, -Lq:], atol=1e-13)
+    # and a single causal query sees every key: the non-causal result
+    if Lq == 1:
+        assert np.allclose(part, A.exact_attention(qf[:, :, -1:], k, v, False), atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_emulation_without_quantisers_is_exact_lq_lkv(causal):
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((1, 2, 50, 16)) * 2
+    k = rng.standard_normal((1, 1, 300, 16)) * 2
+    v = rng.standard_normal((1, 1, 300, 16))
+    for bc in (32, 128):
+        e = A.sa3_emulated_attention(q, k, v, causal, bc=bc, quantize_p=False)
+        assert np.allclose(e, A.exact_attention(q, k, v, causal), atol=1e-12)
