@@ -107,6 +107,22 @@ typedef struct {
 } sa_fp4_qkv;
 
 /*
+ * Sizes of a problem whose query length differs from its key length: Q (and
+ * O) [B, H, Lq, d], K and V [B, Hkv, Lkv, d] -- a chunk of queries against a
+ * longer key/value sequence (chunked prefill, decode).  Under the causal mask
+ * the queries are the last Lq positions of the sequence: key j is visible to
+ * query i iff j <= i + Lkv - Lq (causal calls need Lkv >= Lq).  The `_s`
+ * entry points take this struct; the others are the special case Lq = Lkv =
+ * L.  With Lq != Lkv the quantised layouts below have Lq rows for Q and Lkv
+ * rows (or token columns) for K and V, each rounded up to 128.
+ */
+typedef struct {
+  int B, H, Hkv;   /* batch, query heads, key/value heads (H % Hkv == 0) */
+  int Lq, Lkv;     /* query tokens, key/value tokens */
+  int d;           /* head dimension, 64 or 128 */
+} sa_shape;
+
+/*
  * Bytes of one device blob holding every sa_fp4_qkv buffer, each at a
  * 256-byte aligned offset.  offsets_out (may be NULL) receives 8 offsets in
  * struct order (q_codes, q_sf, k_codes, k_sf, v_codes, v_sf, k_mean,
@@ -118,6 +134,9 @@ size_t sa_fp4_qkv_bytes(int B, int H, int Hkv, int L, int d, size_t offsets_out[
 /* Fill `out` with pointers into `blob` (device memory of sa_fp4_qkv_bytes). */
 sa_status sa_fp4_qkv_from_blob(void* blob, int B, int H, int Hkv, int L, int d,
                                sa_fp4_qkv* out);
+/* The same two for an sa_shape (0 / an error for empty or invalid sizes). */
+size_t sa_fp4_qkv_bytes_s(const sa_shape* shape, size_t offsets_out[8]);
+sa_status sa_fp4_qkv_from_blob_s(void* blob, const sa_shape* shape, sa_fp4_qkv* out);
 
 /*
  * sa_quantize -- smooth-K mean, then NVFP4 quantisation of Q, K' and V
@@ -139,6 +158,11 @@ sa_status sa_quantize(const void* q, const void* k, const void* v,
 sa_status sa_quantize_ex(const void* q, const void* k, const void* v,
                          int B, int H, int Hkv, int L, int d, int flags,
                          const sa_fp4_qkv* out, sa_stream_t stream);
+/* sa_quantize_ex for an sa_shape: Q with Lq tokens, K and V with Lkv (the
+ * smooth-K mean runs over the Lkv key tokens).  Lq == 0 with Lkv > 0 is
+ * SA_ERR_INVALID_ARG. */
+sa_status sa_quantize_s(const void* q, const void* k, const void* v, const sa_shape* shape,
+                        int flags, const sa_fp4_qkv* out, sa_stream_t stream);
 
 /*
  * sa_quantize_static_scratch -- sa_quantize for callers that cannot allocate
@@ -225,6 +249,13 @@ size_t sa_attn_fwd_workspace_bytes(int B, int H, int Hkv, int L, int d, int caus
 sa_status sa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o,
                          int B, int H, int Hkv, int L, int d, int causal, int mode, int nsplit,
                          void* workspace, size_t workspace_bytes, sa_stream_t stream);
+/* The same two for an sa_shape (o is [B, H, Lq, d]; split shares and stream-K
+ * items run over the Lkv key tiles; a causal call with Lkv < Lq is
+ * SA_ERR_INVALID_ARG, and so is Lkv == 0 with Lq > 0). */
+size_t sa_attn_fwd_workspace_bytes_s(const sa_shape* shape, int causal, int mode, int nsplit);
+sa_status sa_attn_fwd_s(const void* q, const void* k, const void* v, void* o, const sa_shape* shape,
+                        int causal, int mode, int nsplit, void* workspace, size_t workspace_bytes,
+                        sa_stream_t stream);
 
 /*
  * sa_attn_fwd_host -- the path of sa_attn_fwd (mode SA_MODE_NVFP4:

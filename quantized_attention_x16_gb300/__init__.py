@@ -33,6 +33,8 @@ SA_LAYOUT_BLHD = 32
 EXPORTS = ("sa_fp4_qkv_bytes", "sa_fp4_qkv_from_blob", "sa_quantize", "sa_quantize_ex", "sa_quantize_static_scratch",
            "sa_attn_fwd",
            "sa_attn_fwd_workspace_bytes", "sa_attn_fwd_ws",
+           "sa_fp4_qkv_bytes_s", "sa_fp4_qkv_from_blob_s", "sa_quantize_s", "sa_attn_fwd_workspace_bytes_s",
+           "sa_attn_fwd_s",
            "sa_attn_fwd_host_workspace_bytes", "sa_attn_fwd_host",
            "sa_status_string", "sa_last_device_error", "sa_selftest_wait_timeout", "sa_version")
 SA_STATIC_SCRATCH_FLOATS = 1 << 20
@@ -42,6 +44,11 @@ class SaFp4Qkv(ctypes.Structure):
     """Mirror of ``sa_fp4_qkv`` (eight device pointers)."""
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("q_codes", "q_sf", "k_codes", "k_sf", "v_codes", "v_sf", "k_mean", "workspace")]
+
+
+class SaShape(ctypes.Structure):
+    """Mirror of ``sa_shape``: Q [B, H, Lq, d], K and V [B, Hkv, Lkv, d]."""
+    _fields_ = [(n, ctypes.c_int) for n in ("B", "H", "Hkv", "Lq", "Lkv", "d")]
 
 
 def _load():
@@ -58,6 +65,17 @@ def _load():
     lib.sa_quantize.restype = i
     lib.sa_quantize_ex.argtypes = [vp, vp, vp, i, i, i, i, i, i, ctypes.POINTER(SaFp4Qkv), vp]
     lib.sa_quantize_ex.restype = i
+    shp = ctypes.POINTER(SaShape)
+    lib.sa_fp4_qkv_bytes_s.argtypes = [shp, ctypes.POINTER(sz)]
+    lib.sa_fp4_qkv_bytes_s.restype = sz
+    lib.sa_fp4_qkv_from_blob_s.argtypes = [vp, shp, ctypes.POINTER(SaFp4Qkv)]
+    lib.sa_fp4_qkv_from_blob_s.restype = i
+    lib.sa_quantize_s.argtypes = [vp, vp, vp, shp, i, ctypes.POINTER(SaFp4Qkv), vp]
+    lib.sa_quantize_s.restype = i
+    lib.sa_attn_fwd_workspace_bytes_s.argtypes = [shp, i, i, i]
+    lib.sa_attn_fwd_workspace_bytes_s.restype = sz
+    lib.sa_attn_fwd_s.argtypes = [vp, vp, vp, vp, shp, i, i, i, vp, sz, vp]
+    lib.sa_attn_fwd_s.restype = i
     lib.sa_quantize_static_scratch.argtypes = [vp, vp, vp, i, i, i, i, i, ctypes.POINTER(SaFp4Qkv), vp]
     lib.sa_quantize_static_scratch.restype = i
     lib.sa_attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
@@ -127,31 +145,38 @@ def _bf16_cuda(t, name):
 
 
 class FP4QKV:
-    """Caller-owned device blob holding the quantised Q, K', V (see sa.h)."""
+    """Caller-owned device blob holding the quantised Q, K', V (see sa.h).
+    L is the query length; Lkv the key/value length (default L)."""
 
-    def __init__(self, B, H, Hkv, L, d, device="cuda"):
+    def __init__(self, B, H, Hkv, L, d, device="cuda", Lkv=None):
         import torch
+        Lkv = L if Lkv is None else Lkv
         self.dims = (B, H, Hkv, L, d)
-        n, self.offsets = sa_fp4_qkv_bytes(B, H, Hkv, L, d)
+        self.Lkv = Lkv
+        self.shape = SaShape(B, H, Hkv, L, Lkv, d)
+        offs = (ctypes.c_size_t * 8)()
+        n = int(lib.sa_fp4_qkv_bytes_s(ctypes.byref(self.shape), offs))
         if n == 0:
-            raise SaError(SA_ERR_UNSUPPORTED, "sa_fp4_qkv_bytes")
+            raise SaError(SA_ERR_UNSUPPORTED, "sa_fp4_qkv_bytes_s")
+        self.offsets = [int(o) for o in offs]
         self.blob = torch.empty(n, dtype=torch.uint8, device=device)
         self.struct = SaFp4Qkv()
-        _check(lib.sa_fp4_qkv_from_blob(_ptr(self.blob), B, H, Hkv, L, d, ctypes.byref(self.struct)),
-               "sa_fp4_qkv_from_blob")
+        _check(lib.sa_fp4_qkv_from_blob_s(_ptr(self.blob), ctypes.byref(self.shape), ctypes.byref(self.struct)),
+               "sa_fp4_qkv_from_blob_s")
 
     def views(self):
         """Torch views of each region, shaped as documented in sa.h."""
         import torch
         B, H, Hkv, L, d = self.dims
         Lp = -(-L // 128) * 128           # the layouts hold whole 128-token tiles
+        Lkp = -(-self.Lkv // 128) * 128
         shapes = [
             ("q_codes", (B, H, Lp, d // 2), torch.uint8),
             ("q_sf", (B, H, Lp // 128, d // 64, 512), torch.uint8),
-            ("k_codes", (B, Hkv, Lp, d // 2), torch.uint8),
-            ("k_sf", (B, Hkv, Lp // 128, d // 64, 512), torch.uint8),
-            ("v_codes", (B, Hkv, d, Lp // 2), torch.uint8),
-            ("v_sf", (B, Hkv, Lp // 64, 512), torch.uint8),
+            ("k_codes", (B, Hkv, Lkp, d // 2), torch.uint8),
+            ("k_sf", (B, Hkv, Lkp // 128, d // 64, 512), torch.uint8),
+            ("v_codes", (B, Hkv, d, Lkp // 2), torch.uint8),
+            ("v_sf", (B, Hkv, Lkp // 64, 512), torch.uint8),
             ("k_mean", (B, Hkv, d), torch.float32),
         ]
         out = {}
@@ -165,14 +190,14 @@ class FP4QKV:
 
 
 def _dims(q, k, layout):
-    """(B, H, Hkv, L, d) of q [B, H, L, d] / k [B, Hkv, L, d] (layout "bhld") or
-    q [B, L, H, d] / k [B, L, Hkv, d] ("blhd"), and the layout flag."""
+    """(B, H, Hkv, Lq, Lkv, d) of q [B, H, Lq, d] / k [B, Hkv, Lkv, d] (layout
+    "bhld") or q [B, Lq, H, d] / k [B, Lkv, Hkv, d] ("blhd"), and the layout flag."""
     if layout == "bhld":
         B, H, L, d = q.shape
-        return (B, H, k.shape[1], L, d), 0
+        return (B, H, k.shape[1], L, k.shape[2], d), 0
     if layout == "blhd":
         B, L, H, d = q.shape
-        return (B, H, k.shape[2], L, d), SA_LAYOUT_BLHD
+        return (B, H, k.shape[2], L, k.shape[1], d), SA_LAYOUT_BLHD
     raise ValueError(f"unknown layout {layout!r}")
 
 
@@ -180,11 +205,12 @@ def sa_quantize(q, k, v, out=None, stream=None, layout="bhld"):
     """Smooth-K + NVFP4 quantisation of bf16 tensors (layout "bhld" or
     "blhd"); returns an FP4QKV (the quantised layout is the same either way)."""
     _bf16_cuda(q, "q"), _bf16_cuda(k, "k"), _bf16_cuda(v, "v")
-    (B, H, Hkv, L, d), flag = _dims(q, k, layout)
+    (B, H, Hkv, L, Lkv, d), flag = _dims(q, k, layout)
     if out is None:
-        out = FP4QKV(B, H, Hkv, L, d, device=q.device)
-    _check(lib.sa_quantize_ex(_ptr(q), _ptr(k), _ptr(v), B, H, Hkv, L, d, flag, ctypes.byref(out.struct),
-                              _stream(stream)), "sa_quantize_ex")
+        out = FP4QKV(B, H, Hkv, L, d, device=q.device, Lkv=Lkv)
+    shape = SaShape(B, H, Hkv, L, Lkv, d)
+    _check(lib.sa_quantize_s(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shape), flag, ctypes.byref(out.struct),
+                             _stream(stream)), "sa_quantize_s")
     return out
 
 
@@ -202,9 +228,10 @@ def sa_quantize_static_scratch(q, k, v, out=None, stream=None):
     return out
 
 
-def sa_attn_fwd_workspace_bytes(B, H, Hkv, L, d, causal=False, mode="bf16", nsplit=0):
+def sa_attn_fwd_workspace_bytes(B, H, Hkv, L, d, causal=False, mode="bf16", nsplit=0, Lkv=None):
     m = {"bf16": SA_MODE_BF16, "nvfp4": SA_MODE_NVFP4}[mode]
-    return int(lib.sa_attn_fwd_workspace_bytes(B, H, Hkv, L, d, int(bool(causal)), m, int(nsplit)))
+    shape = SaShape(B, H, Hkv, L, L if Lkv is None else Lkv, d)
+    return int(lib.sa_attn_fwd_workspace_bytes_s(ctypes.byref(shape), int(bool(causal)), m, int(nsplit)))
 
 
 def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=None, stream=None,
@@ -222,7 +249,7 @@ def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=
     lflag = SA_LAYOUT_BLHD if layout == "blhd" else 0
     if mode == "bf16":
         _bf16_cuda(q, "q"), _bf16_cuda(k, "k"), _bf16_cuda(v, "v")
-        (B, H, Hkv, L, d), _ = _dims(q, k, layout)
+        (B, H, Hkv, L, Lkv, d), _ = _dims(q, k, layout)
         args = (_ptr(q), _ptr(k), _ptr(v))
         m = SA_MODE_BF16
         dev = q.device
@@ -230,6 +257,7 @@ def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=
         if not isinstance(q, FP4QKV) or k is not None or v is not None:
             raise ValueError("nvfp4 mode takes an FP4QKV as q and no k, v")
         B, H, Hkv, L, d = q.dims
+        Lkv = q.Lkv
         args = (ctypes.cast(ctypes.pointer(q.struct), ctypes.c_void_p), None, None)
         m = SA_MODE_NVFP4
         dev = q.blob.device
@@ -247,16 +275,18 @@ def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=
         o = torch.empty(oshape, dtype=out_dtype, device=dev)
     if not (o.is_cuda and o.dtype == out_dtype and o.is_contiguous() and tuple(o.shape) == oshape):
         raise ValueError(f"o must be a contiguous CUDA tensor of shape {oshape} and dtype out_dtype")
-    if nsplit is None:
+    if nsplit is None and Lkv == L:
         _check(lib.sa_attn_fwd(*args, _ptr(o), B, H, Hkv, L, d, int(bool(causal)), m, _stream(stream)),
                "sa_attn_fwd")
         return o
-    need = int(lib.sa_attn_fwd_workspace_bytes(B, H, Hkv, L, d, int(bool(causal)), m & 0xF, int(nsplit)))
+    shape = SaShape(B, H, Hkv, L, Lkv, d)
+    ns = 1 if nsplit is None else int(nsplit)
+    need = int(lib.sa_attn_fwd_workspace_bytes_s(ctypes.byref(shape), int(bool(causal)), m & 0xF, ns))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws, nbytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel())
-    _check(lib.sa_attn_fwd_ws(*args, _ptr(o), B, H, Hkv, L, d, int(bool(causal)), m, int(nsplit), ws, nbytes,
-                              _stream(stream)), "sa_attn_fwd_ws")
+    _check(lib.sa_attn_fwd_s(*args, _ptr(o), ctypes.byref(shape), int(bool(causal)), m, ns, ws, nbytes,
+                             _stream(stream)), "sa_attn_fwd_s")
     return o
 
 

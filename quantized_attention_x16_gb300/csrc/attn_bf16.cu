@@ -1,7 +1,7 @@
 // attn_bf16.cu -- exact BF16 fused attention forward on tcgen05 tensor cores.
 //
 // Data flow (page "FlashAttention kernels", sections 0-1): tile by tile with
-// online softmax; the L x L scores never leave the SM.  Work partitioning
+// online softmax; the Lq x Lkv scores never leave the SM.  Work partitioning
 // (same page, FA2): one CTA per (batch, head, 256 query rows).  Hardware
 // mapping: TMA tile loads into 128B-swizzled SMEM, tcgen05 MMAs with FP32
 // accumulators in tensor memory, warp specialisation (load / MMA / softmax
@@ -83,7 +83,7 @@ template <int D, bool OUT32>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, void* __restrict__ out_ptr, int H, int Hkv,
-                     int L, int causal, const AttnWork work, const SplitOut part, const Strides so,
+                     int Lq, int Lkv, int causal, const AttnWork work, const SplitOut part, const Strides so,
                      uint64_t wait_ns) {
   using C = CfgBF16<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -110,9 +110,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hk = h / (H / Hkv);
   const bool q1_valid = nqu == 2;
   int ntq[2];
-  const int nkt = (L + BN - 1) / BN;                // key tiles; a ragged last one is zero-filled past L
-  ntq[0] = causal ? qt0 + 1 : nkt;
-  ntq[1] = q1_valid ? (causal ? qt0 + 2 : nkt) : 0;
+  // key tiles (a ragged last one is zero-filled past Lkv), up to the causal
+  // limit of each query tile
+  ntq[0] = q_tile_keys(work, qt0);
+  ntq[1] = q1_valid ? q_tile_keys(work, qt0 + 1) : 0;
   // key tiles [jb, jb + ntq[q]) of this CTA; loop indices below count from jb
   const int jb = work.nsplit > 1 ? split_range(sp, work.nsplit, ntq) : 0;
   const int nt = ntq[0] > ntq[1] ? ntq[0] : ntq[1];
@@ -296,9 +297,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sv[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
-      // keys this row may not see: past the diagonal (causal) and past L (the
-      // zero fill of a ragged last tile)
-      const int lim = min(causal && jb + j == qt ? r + 1 : BN, L - (jb + j) * BN);
+      // keys this row may not see: past Lkv (the zero fill of a ragged last
+      // tile) and, causal, past its position qt*128 + r + Lkv - Lq
+      int lim = Lkv - (jb + j) * BN;
+      if (causal) lim = min(lim, qt * BM + r + work.coff - (jb + j) * BN + 1);
+      lim = min(lim, BN);
       if (lim < BN) {
 #pragma unroll
         for (int i = 0; i < 128; ++i)
@@ -369,12 +372,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bars.p_full + q);
     }
     // ---- epilogue: O / l
-    const bool row_in = qt * BM + r < L;                // rows past L (a ragged last tile) are not stored
+    const bool row_in = qt * BM + r < Lq;               // rows past Lq (a ragged last tile) are not stored
     // split-KV: this CTA's partial result of the row -- O unnormalised (in
     // units of 2^m_use, as is l), m_use (-inf if no key was visible) and l --
     // goes to split sp's slot; a combine pass forms O
     const bool split = work.nsplit > 1;
-    const long long prow = ((long long)sp * work.nbh + bhq) * padded_len_dev(L) + (long long)qt * BM + r;
+    const long long prow = ((long long)sp * work.nbh + bhq) * padded_len_dev(Lq) + (long long)qt * BM + r;
     if (split && ok && ntq[q] == 0 && (q == 0 || q1_valid) && row_in)
       *reinterpret_cast<float2*>(part.ml + 2 * prow) = make_float2(-INFINITY, 0.f);
     if (ok && ntq[q] > 0 && mbar_wait_warp(bars.o_done + q, (ntq[q] - 1) & 1, abort_flag, wait_ns)) {
@@ -441,8 +444,8 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     attr_done = true;
   }
   int ctas = 0;
-  const AttnWork work = make_attn_work(dm.B, dm.H, dm.L, causal, device_sm_count(), &ctas, nsplit);
-  attn_bf16_kernel<D, OUT32><<<ctas, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, o, dm.H, dm.Hkv, dm.L, causal,
+  const AttnWork work = make_attn_work(dm.B, dm.H, dm.Lq, dm.Lkv, causal, device_sm_count(), &ctas, nsplit);
+  attn_bf16_kernel<D, OUT32><<<ctas, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, o, dm.H, dm.Hkv, dm.Lq, dm.Lkv, causal,
                                                                     work, part, so, kWaitLimitNs);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess && work.nsplit > 1) e = launch_splitkv_combine(part, work.nsplit, dm, o, so, OUT32, s);

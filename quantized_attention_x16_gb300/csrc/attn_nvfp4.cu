@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const uint8_t* __restrict__ q_sf,
                       const uint8_t* __restrict__ k_sf, const uint8_t* __restrict__ v_sf,
-                      void* __restrict__ out_ptr, int H, int Hkv, int L, int causal, const AttnWork work,
+                      void* __restrict__ out_ptr, int H, int Hkv, int Lq, int Lkv, int causal, const AttnWork work,
                       const SplitOut part, const Strides so, uint64_t wait_ns) {
   using C = CfgF4<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -155,8 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // the quantised operands hold Lp = L rounded up to whole tiles per head
-  const int Lp = (L + 127) & ~127;
+  // the quantised operands hold Lq and Lkv rounded up to whole tiles per head
+  const int Lqp = (Lq + 127) & ~127, Lkvp = (Lkv + 127) & ~127;
   const int G = H / Hkv;
 
   if (threadIdx.x == 0) {
@@ -217,9 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < u.nq; ++q) {
             const int qt = u.qt0 + q;
             tma_load_2d(smem + C::kOffQ + (2 * qb + q) * C::kQBytes, &tmap_q, bars.q_full + qb, 0,
-                        (int)(bhq * Lp + (long long)qt * BM));
+                        (int)(bhq * Lqp + (long long)qt * BM));
             bulk_load(smem + C::kOffQSf + (2 * qb + q) * C::kQSfBytes,
-                      q_sf + (bhq * (Lp / 128) + qt) * C::kQSfBytes, C::kQSfBytes, bars.q_full + qb);
+                      q_sf + (bhq * (Lqp / 128) + qt) * C::kQSfBytes, C::kQSfBytes, bars.q_full + qb);
           }
         }
         ++ug;
@@ -236,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (leader) {
             mbar_arrive_expect_tx(bars.k_full + s, C::kKBytes + C::kKSfBytes);
             tma_load_2d(smem + C::kOffK + s * C::kKBytes, &tmap_k, bars.k_full + s, 0,
-                        (int)(bhk * Lp + (long long)ja * BN));
-            bulk_load(smem + C::kOffKSf + s * C::kKSfBytes, k_sf + (bhk * (Lp / 128) + ja) * C::kKSfBytes,
+                        (int)(bhk * Lkvp + (long long)ja * BN));
+            bulk_load(smem + C::kOffKSf + s * C::kKSfBytes, k_sf + (bhk * (Lkvp / 128) + ja) * C::kKSfBytes,
                       C::kKSfBytes, bars.k_full + s);
           }
           ++nk;
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(bars.v_full + s, C::kVBytes + C::kVSfBytes);
             tma_load_2d(smem + C::kOffV + s * C::kVBytes, &tmap_v, bars.v_full + s, ja * (BN / 2),
                         (int)(bhk * D));
-            bulk_load(smem + C::kOffVSf + s * C::kVSfBytes, v_sf + (bhk * (Lp / 64) + 2 * ja) * 512,
+            bulk_load(smem + C::kOffVSf + s * C::kVSfBytes, v_sf + (bhk * (Lkvp / 64) + 2 * ja) * 512,
                       C::kVSfBytes, bars.v_full + s);
           }
           ++nv;
@@ -434,10 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         float sv[128];
 #pragma unroll
         for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
-        // keys this row may not see: past the diagonal (causal) and past L (the
-        // zero padding of a ragged last tile)
+        // keys this row may not see: past Lkv (the zero padding of a ragged
+        // last tile) and, causal, past its position qt*128 + r + Lkv - Lq
         const int ja = u.jb + j;
-        const int lim = min(causal && ja == qt ? r + 1 : BN, L - ja * BN);
+        int lim = Lkv - ja * BN;
+        if (causal) lim = min(lim, qt * BM + r + work.coff - ja * BN + 1);
+        lim = min(lim, BN);
         if (lim < BN) {
 #pragma unroll
           for (int i = 0; i < 128; ++i)
@@ -560,14 +562,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- the unit's result for this row: O, or a partial for the combine
       // pass (O unnormalised in units of 2^m_ref / 2688 as is lam, m_ref
       // (-inf if no key tile was live) and lam)
-      const bool row_in = qt * BM + r < L;              // rows of the padding are not stored
+      const bool row_in = qt * BM + r < Lq;             // rows of the padding are not stored
       const bool partial = u.slot >= 0;
       const long long bhq = u.bh;
       long long prow;
       if (work.streamk)
         prow = (long long)u.slot * (2 * BM) + q * BM + r;
       else
-        prow = ((long long)u.slot * work.nbh + bhq) * Lp + (long long)qt * BM + r;
+        prow = ((long long)u.slot * work.nbh + bhq) * Lqp + (long long)qt * BM + r;
       if (partial && nq == 0 && row_in)
         *reinterpret_cast<float2*>(part.ml + 2 * prow) = make_float2(-INFINITY, 0.f);
       if (nq > 0) {
@@ -645,11 +647,11 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   }
   int ctas = 0;
   const AttnWork work = nsplit == kStreamK
-                            ? make_streamk_work(dm.B, dm.H, dm.L, causal, device_sm_count(), &ctas)
-                            : make_attn_work(dm.B, dm.H, dm.L, causal, device_sm_count(), &ctas, nsplit);
+                            ? make_streamk_work(dm.B, dm.H, dm.Lq, dm.Lkv, causal, device_sm_count(), &ctas)
+                            : make_attn_work(dm.B, dm.H, dm.Lq, dm.Lkv, causal, device_sm_count(), &ctas, nsplit);
   attn_nvfp4_kernel<D, OUT32><<<ctas, kThreads, C::kSmemBytes, s>>>(
       tq, tk, tv, static_cast<const uint8_t*>(x.q_sf), static_cast<const uint8_t*>(x.k_sf),
-      static_cast<const uint8_t*>(x.v_sf), o, dm.H, dm.Hkv, dm.L, causal, work, part, so, kWaitLimitNs);
+      static_cast<const uint8_t*>(x.v_sf), o, dm.H, dm.Hkv, dm.Lq, dm.Lkv, causal, work, part, so, kWaitLimitNs);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess && work.streamk) e = launch_streamk_combine(work, ctas, part, dm, o, so, OUT32, s);
   else if (e == cudaSuccess && work.nsplit > 1) e = launch_splitkv_combine(part, work.nsplit, dm, o, so, OUT32, s);

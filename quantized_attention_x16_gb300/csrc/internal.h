@@ -9,8 +9,9 @@
 
 namespace sa {
 
+// Sizes of one problem: Q [B, H, Lq, d], K and V [B, Hkv, Lkv, d].
 struct Dims {
-  int B, H, Hkv, L, d;
+  int B, H, Hkv, Lq, Lkv, d;
 };
 
 // The sequence length padded to whole 128-token tiles: the row count of every
@@ -61,11 +62,11 @@ struct SplitOut {
   float* ml;
 };
 inline size_t splitkv_workspace_bytes(const Dims& dm, int nsplit) {
-  const size_t rows = (size_t)dm.B * dm.H * padded_len(dm.L);
+  const size_t rows = (size_t)dm.B * dm.H * padded_len(dm.Lq);
   return nsplit > 1 ? (size_t)nsplit * rows * ((size_t)dm.d + 2) * sizeof(float) : 0;
 }
 inline SplitOut splitkv_layout(void* ws, const Dims& dm, int nsplit) {
-  const size_t rows = (size_t)dm.B * dm.H * padded_len(dm.L);
+  const size_t rows = (size_t)dm.B * dm.H * padded_len(dm.Lq);
   float* f = static_cast<float*>(ws);
   return SplitOut{f, f + (size_t)nsplit * rows * dm.d};
 }

@@ -123,10 +123,10 @@ struct QuantArgs {
   uint8_t *qc, *qsf, *kc, *ksf, *vc, *vsf;
   float* part;      // scratch: chunk sums [B*Hkv][Lp/128][D]
   float* kmean;     // [B*Hkv][D]
-  int L, Lp, nbh_q, nbh_kv, chunks_per_cta;
+  int Lq, Lqp, Lkv, Lkvp, nbh_q, nbh_kv, chunks_per_cta;   // Q and K/V tokens (and padded to 128)
   int H, Hkv;                       // heads of Q and of K / V (bh = b * heads + h)
   Strides sq, skv;                  // element strides of the bf16 Q and K / V (BHLD or BLHD)
-  int tiles_per_head;               // Q/K tiles of kRows tokens per head
+  int tph_q, tph_k;                 // Q / K tiles of kRows tokens per head
   int ntile_q, ntile_k, nblk_v;
   int nclu_mean, nclu_v;            // launch 1: mean clusters, V clusters
   uint64_t wait_ns;
@@ -170,8 +170,9 @@ __device__ __forceinline__ void quant_quad(const uint4 (&w)[8], const float* mea
 __device__ __forceinline__ void tile_head(const QuantArgs& a, int tile, int rows, bool& is_k, int& bh, int& t0) {
   is_k = tile < a.ntile_k;
   const int u = is_k ? tile : tile - a.ntile_k;
-  bh = u / a.tiles_per_head;
-  t0 = (u % a.tiles_per_head) * rows;
+  const int tph = is_k ? a.tph_k : a.tph_q;
+  bh = u / tph;
+  t0 = (u % tph) * rows;
 }
 
 // Issues the TMA copies of Q/K tile `tile` into `dst`: tokens [t0, t0 + kRows)
@@ -206,7 +207,7 @@ __device__ __forceinline__ void quant_tile_smem(const QuantArgs& a, int tile, co
   tile_head(a, tile, T::kRows, is_k, bh, t0);
   const int r = threadIdx.x / (D / 64), quad = threadIdx.x % (D / 64);
   const int t = t0 + r;
-  if (t >= a.Lp) return;
+  if (t >= (is_k ? a.Lkvp : a.Lqp)) return;
   const int box = D == 128 ? quad : r / 128, rr = D == 128 ? r : r % 128;
   const uint8_t* base = src + box * T::kBoxBytes + rr * 128;
   uint4 w[8];
@@ -214,9 +215,9 @@ __device__ __forceinline__ void quant_tile_smem(const QuantArgs& a, int tile, co
   for (int i = 0; i < 8; ++i) w[i] = *reinterpret_cast<const uint4*>(base + ((i ^ (rr & 7)) * 16));
   // a token past L arrived as zeros; K' there is kept zero (no mean subtracted)
   if (is_k)
-    quant_quad<D>(w, t < a.L ? a.kmean + (size_t)bh * D + quad * 64 : nullptr, a.kc, a.ksf, bh, t, quad, a.Lp);
+    quant_quad<D>(w, t < a.Lkv ? a.kmean + (size_t)bh * D + quad * 64 : nullptr, a.kc, a.ksf, bh, t, quad, a.Lkvp);
   else
-    quant_quad<D>(w, nullptr, a.qc, a.qsf, bh, t, quad, a.Lp);
+    quant_quad<D>(w, nullptr, a.qc, a.qsf, bh, t, quad, a.Lqp);
 }
 
 // One thread per (channel pair, 32 tokens = two 16-token groups).  Items are
@@ -227,13 +228,13 @@ template <int D>
 __device__ __forceinline__ void quant_v_cta(const QuantArgs& a, int blk) {
   constexpr int kPairs = D / 2;
   const long long item = (long long)blk * kThreadsQ + threadIdx.x;
-  const int npb = a.Lp / 32;                            // 32-token pieces per head (padded length)
+  const int npb = a.Lkvp / 32;                          // 32-token pieces per head (padded length)
   if (item >= (long long)a.nbh_kv * npb * kPairs) return;
   const int c = 2 * (int)(item % kPairs);
   const long long piece = item / kPairs;                // over B*Hkv*npb
   const long long bh = piece / npb;
   const int tp = (int)(piece % npb);
-  const int nvalid = a.L - tp * 32;                     // tokens of this piece below L (may be <= 0)
+  const int nvalid = a.Lkv - tp * 32;                   // tokens of this piece below Lkv (may be <= 0)
   const long long vb = bh / a.Hkv, vh = bh % a.Hkv;
   const uint32_t* src =
       reinterpret_cast<const uint32_t*>(a.v + vb * a.skv.b + vh * a.skv.h + (long long)tp * 32 * a.skv.t + c);
@@ -247,7 +248,7 @@ __device__ __forceinline__ void quant_v_cta(const QuantArgs& a, int blk) {
 #pragma unroll
     for (int t = 0; t < 32; ++t) w[t] = t < nvalid ? __ldg(src + t * tstep) : 0u;
   }
-  uint8_t* sblk = a.vsf + ((size_t)bh * (a.Lp / 64) + tp / 2) * 512 + (tp % 2) * 2;
+  uint8_t* sblk = a.vsf + ((size_t)bh * (a.Lkvp / 64) + tp / 2) * 512 + (tp % 2) * 2;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {                         // channel c + h
     uint32_t codes[4];
@@ -261,7 +262,7 @@ __device__ __forceinline__ void quant_v_cta(const QuantArgs& a, int blk) {
       sfw |= quant_group16(x, codes + 2 * g) << (8 * g);
     }
     const int ch = c + h;
-    *reinterpret_cast<uint4*>(a.vc + ((size_t)bh * D + ch) * (a.Lp / 2) + (size_t)tp * 16) =
+    *reinterpret_cast<uint4*>(a.vc + ((size_t)bh * D + ch) * (a.Lkvp / 2) + (size_t)tp * 16) =
         make_uint4(codes[0], codes[1], codes[2], codes[3]);
     *reinterpret_cast<uint16_t*>(sblk + (ch % 32) * 16 + (ch / 32) * 4) = (uint16_t)sfw;
     if (D == 64) *reinterpret_cast<uint16_t*>(sblk + (ch % 32) * 16 + (ch / 32 + 2) * 4) = 0;   // padding rows
@@ -276,7 +277,7 @@ __device__ __forceinline__ void mean_cluster(const QuantArgs& a, int bh) {
   constexpr int kPairs = D / 2;
   constexpr int kChunksAtOnce = kThreadsQ / kPairs;
   const uint32_t rank = cluster_ctarank();
-  const int nchunk = a.Lp / kMeanChunk, cpc = a.chunks_per_cta;
+  const int nchunk = a.Lkvp / kMeanChunk, cpc = a.chunks_per_cta;
   const int first = (int)rank * cpc, last = min(nchunk, first + cpc);
   const int c = 2 * (threadIdx.x % kPairs);
   for (int ch = first + (int)threadIdx.x / kPairs; ch < last; ch += kChunksAtOnce) {
@@ -285,7 +286,7 @@ __device__ __forceinline__ void mean_cluster(const QuantArgs& a, int bh) {
                                                             (long long)ch * kMeanChunk * a.skv.t + c);
     const size_t tstep = (size_t)(a.skv.t / 2);         // token stride in bf16 pairs
     float acc0 = 0.f, acc1 = 0.f;
-    const int nvalid = a.L - ch * kMeanChunk;           // tokens of this chunk below L
+    const int nvalid = a.Lkv - ch * kMeanChunk;         // tokens of this chunk below Lkv
 #pragma unroll 1
     for (int t0 = 0; t0 < kMeanChunk; t0 += 32) {
       // a token past L adds +0, which leaves a float32 sum unchanged (the
@@ -317,7 +318,7 @@ __device__ __forceinline__ void mean_cluster(const QuantArgs& a, int bh) {
       for (int j = 0; j < 8; ++j)
         if (c0 + j < nchunk) tot = __fadd_rn(tot, v[j]);
     }
-    a.kmean[(size_t)bh * D + col] = __fdiv_rn(tot, (float)a.L);
+    a.kmean[(size_t)bh * D + col] = __fdiv_rn(tot, (float)a.Lkv);
   }
 }
 
@@ -411,20 +412,23 @@ cudaError_t launch_quantize_impl(const void* q, const void* k, const void* v, co
   a.vsf = static_cast<uint8_t*>(out.v_sf);
   a.part = partials;
   a.kmean = out.k_mean;
-  a.L = dm.L;
-  a.Lp = padded_len(dm.L);
+  a.Lq = dm.Lq;
+  a.Lqp = padded_len(dm.Lq);
+  a.Lkv = dm.Lkv;
+  a.Lkvp = padded_len(dm.Lkv);
   a.H = dm.H;
   a.Hkv = dm.Hkv;
-  a.sq = layout_strides(blhd, dm.H, dm.L, dm.d);
-  a.skv = layout_strides(blhd, dm.Hkv, dm.L, dm.d);
+  a.sq = layout_strides(blhd, dm.H, dm.Lq, dm.d);
+  a.skv = layout_strides(blhd, dm.Hkv, dm.Lkv, dm.d);
   a.nbh_q = dm.B * dm.H;
   a.nbh_kv = dm.B * dm.Hkv;
-  const int nchunk = a.Lp / kMeanChunk;
+  const int nchunk = a.Lkvp / kMeanChunk;
   a.chunks_per_cta = (nchunk + kMeanCluster - 1) / kMeanCluster;
-  a.tiles_per_head = (a.Lp + T::kRows - 1) / T::kRows;
-  a.ntile_q = a.nbh_q * a.tiles_per_head;
-  a.ntile_k = a.nbh_kv * a.tiles_per_head;
-  a.nblk_v = (int)(((long long)a.nbh_kv * (a.Lp / 32) * (D / 2) + kThreadsQ - 1) / kThreadsQ);
+  a.tph_q = (a.Lqp + T::kRows - 1) / T::kRows;
+  a.tph_k = (a.Lkvp + T::kRows - 1) / T::kRows;
+  a.ntile_q = a.nbh_q * a.tph_q;
+  a.ntile_k = a.nbh_kv * a.tph_k;
+  a.nblk_v = (int)(((long long)a.nbh_kv * (a.Lkvp / 32) * (D / 2) + kThreadsQ - 1) / kThreadsQ);
   a.nclu_mean = a.nbh_kv;
   a.nclu_v = (a.nblk_v + kMeanCluster - 1) / kMeanCluster;
   a.wait_ns = kWaitLimitNs;
@@ -488,7 +492,7 @@ cudaError_t static_scratch_address(float** out) {
 cudaError_t launch_quantize_static_scratch(const void* q, const void* k, const void* v, const Dims& dm,
                                            const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk,
                                            cudaStream_t s) {
-  const size_t need = (size_t)dm.B * dm.Hkv * (padded_len(dm.L) / kMeanChunk) * dm.d;
+  const size_t need = (size_t)dm.B * dm.Hkv * (padded_len(dm.Lkv) / kMeanChunk) * dm.d;
   if (need > kStaticScratchFloats) return cudaErrorInvalidValue;
   float* part = nullptr;
   cudaError_t e = static_scratch_address(&part);

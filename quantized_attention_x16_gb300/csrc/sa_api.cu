@@ -49,11 +49,11 @@ bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 // with boxes of 64 channels x 128 tokens x 1 x 1, 128B swizzle (the tiles of
 // the BF16 attention kernel and the quantiser): a tile that runs past the
 // head's last token reads zeros there instead of another head's rows.
-bool make_bf16_head_map(CUtensorMap* m, const void* base, int heads, const Dims& dm, bool blhd) {
+bool make_bf16_head_map(CUtensorMap* m, const void* base, int heads, int L, const Dims& dm, bool blhd) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const Strides st = layout_strides(blhd, heads, dm.L, dm.d);
-  const cuuint64_t dims[4] = {(cuuint64_t)dm.d, (cuuint64_t)dm.L, (cuuint64_t)heads, (cuuint64_t)dm.B};
+  const Strides st = layout_strides(blhd, heads, L, dm.d);
+  const cuuint64_t dims[4] = {(cuuint64_t)dm.d, (cuuint64_t)L, (cuuint64_t)heads, (cuuint64_t)dm.B};
   const cuuint64_t strides[3] = {(cuuint64_t)st.t * 2, (cuuint64_t)st.h * 2, (cuuint64_t)st.b * 2};
   const cuuint32_t box[4] = {64, 128, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
@@ -64,40 +64,46 @@ bool make_bf16_head_map(CUtensorMap* m, const void* base, int heads, const Dims&
 
 bool make_bf16_row_maps(const void* q, const void* k, const Dims& dm, bool blhd, CUtensorMap* tq,
                         CUtensorMap* tk) {
-  return make_bf16_head_map(tq, q, dm.H, dm, blhd) && make_bf16_head_map(tk, k, dm.Hkv, dm, blhd);
+  return make_bf16_head_map(tq, q, dm.H, dm.Lq, dm, blhd) && make_bf16_head_map(tk, k, dm.Hkv, dm.Lkv, dm, blhd);
 }
 
-// SA_OK for a problem the kernels take, or the error to return.  Empty
-// problems (B == 0 or L == 0) pass here; the entry points return before
-// touching any pointer for them.
-sa_status check_dims(int B, int H, int Hkv, int L, int d) {
-  if (B < 0 || H <= 0 || Hkv <= 0 || L < 0 || d <= 0) return SA_ERR_INVALID_ARG;
-  if (H % Hkv != 0) return SA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return SA_ERR_UNSUPPORTED;
+// SA_OK for sizes the kernels take, or the error to return.  B == 0 or Lq ==
+// 0 passes (an empty problem: the entry points return before touching any
+// pointer); otherwise Lkv must be positive.
+sa_status check_dims(const Dims& dm) {
+  if (dm.B < 0 || dm.H <= 0 || dm.Hkv <= 0 || dm.Lq < 0 || dm.Lkv < 0 || dm.d <= 0) return SA_ERR_INVALID_ARG;
+  if (dm.H % dm.Hkv != 0) return SA_ERR_INVALID_ARG;
+  if (dm.d != 64 && dm.d != 128) return SA_ERR_UNSUPPORTED;
+  if (dm.B > 0 && dm.Lq > 0 && dm.Lkv == 0) return SA_ERR_INVALID_ARG;   // queries without keys
   // TMA coordinates are 32-bit: every row index of the padded layouts (and
   // d * B * Hkv) must fit.
-  const long long Lp = ((long long)L + 127) / 128 * 128;
-  if ((long long)B * H * Lp >= (1ll << 31) || (long long)B * Hkv * d >= (1ll << 31)) return SA_ERR_UNSUPPORTED;
-  if (H > 65535 || B > 65535) return SA_ERR_UNSUPPORTED;
+  const long long Lqp = ((long long)dm.Lq + 127) / 128 * 128, Lkvp = ((long long)dm.Lkv + 127) / 128 * 128;
+  if ((long long)dm.B * dm.H * Lqp >= (1ll << 31) || (long long)dm.B * dm.Hkv * Lkvp >= (1ll << 31) ||
+      (long long)dm.B * dm.Hkv * dm.d >= (1ll << 31))
+    return SA_ERR_UNSUPPORTED;
+  if (dm.H > 65535 || dm.B > 65535) return SA_ERR_UNSUPPORTED;
   return SA_OK;
 }
 
-bool empty_problem(int B, int L) { return B == 0 || L == 0; }
+bool empty_problem(const Dims& dm) { return dm.B == 0 || dm.Lq == 0; }
+
+Dims dims_of(const sa_shape* s) { return Dims{s->B, s->H, s->Hkv, s->Lq, s->Lkv, s->d}; }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Every quantised layout has Lp = L rounded up to 128 token rows.
-void blob_sizes(int B, int H, int Hkv, int L, int d, size_t sz[8]) {
-  const int Lp = padded_len(L);
-  const size_t nq = (size_t)B * H * Lp, nk = (size_t)B * Hkv * Lp;
-  sz[0] = nq * (d / 2);                             // q_codes
-  sz[1] = (size_t)B * H * (Lp / 128) * (d / 64) * 512;   // q_sf
-  sz[2] = nk * (d / 2);                             // k_codes
-  sz[3] = (size_t)B * Hkv * (Lp / 128) * (d / 64) * 512;
-  sz[4] = nk * (d / 2);                             // v_codes (transposed)
-  sz[5] = (size_t)B * Hkv * (Lp / 64) * 512;        // v_sf
-  sz[6] = (size_t)B * Hkv * d * sizeof(float);      // k_mean
-  sz[7] = (size_t)B * Hkv * (Lp / 128) * d * sizeof(float);   // K-mean partial sums
+// Every quantised layout has its length rounded up to 128 token rows.
+void blob_sizes(const Dims& dm, size_t sz[8]) {
+  const int Lqp = padded_len(dm.Lq), Lkvp = padded_len(dm.Lkv);
+  const size_t nq = (size_t)dm.B * dm.H * Lqp, nk = (size_t)dm.B * dm.Hkv * Lkvp;
+  const int d = dm.d;
+  sz[0] = nq * (d / 2);                                        // q_codes
+  sz[1] = (size_t)dm.B * dm.H * (Lqp / 128) * (d / 64) * 512;  // q_sf
+  sz[2] = nk * (d / 2);                                        // k_codes
+  sz[3] = (size_t)dm.B * dm.Hkv * (Lkvp / 128) * (d / 64) * 512;
+  sz[4] = nk * (d / 2);                                        // v_codes (transposed)
+  sz[5] = (size_t)dm.B * dm.Hkv * (Lkvp / 64) * 512;           // v_sf
+  sz[6] = (size_t)dm.B * dm.Hkv * d * sizeof(float);           // k_mean
+  sz[7] = (size_t)dm.B * dm.Hkv * (Lkvp / 128) * d * sizeof(float);   // K-mean partial sums
 }
 
 __global__ void wait_selftest_kernel(uint64_t limit_ns) {
@@ -133,10 +139,12 @@ const char* sa_status_string(sa_status s) {
   return "unknown status";
 }
 
-size_t sa_fp4_qkv_bytes(int B, int H, int Hkv, int L, int d, size_t offsets_out[8]) {
-  if (check_dims(B, H, Hkv, L, d) != SA_OK || empty_problem(B, L)) return 0;
+size_t sa_fp4_qkv_bytes_s(const sa_shape* shape, size_t offsets_out[8]) {
+  if (!shape) return 0;
+  const Dims dm = dims_of(shape);
+  if (check_dims(dm) != SA_OK || dm.B == 0 || dm.Lq == 0 || dm.Lkv == 0) return 0;
   size_t sz[8];
-  blob_sizes(B, H, Hkv, L, d, sz);
+  blob_sizes(dm, sz);
   size_t off = 0;
   for (int i = 0; i < 8; ++i) {
     if (offsets_out) offsets_out[i] = off;
@@ -145,11 +153,16 @@ size_t sa_fp4_qkv_bytes(int B, int H, int Hkv, int L, int d, size_t offsets_out[
   return off;
 }
 
-sa_status sa_fp4_qkv_from_blob(void* blob, int B, int H, int Hkv, int L, int d, sa_fp4_qkv* out) {
-  if (!out || !blob || (reinterpret_cast<uintptr_t>(blob) & 255u)) return SA_ERR_INVALID_ARG;
+size_t sa_fp4_qkv_bytes(int B, int H, int Hkv, int L, int d, size_t offsets_out[8]) {
+  const sa_shape s{B, H, Hkv, L, L, d};
+  return sa_fp4_qkv_bytes_s(&s, offsets_out);
+}
+
+sa_status sa_fp4_qkv_from_blob_s(void* blob, const sa_shape* shape, sa_fp4_qkv* out) {
+  if (!out || !blob || !shape || (reinterpret_cast<uintptr_t>(blob) & 255u)) return SA_ERR_INVALID_ARG;
   size_t off[8];
-  if (sa_fp4_qkv_bytes(B, H, Hkv, L, d, off) == 0) {
-    const sa_status st = check_dims(B, H, Hkv, L, d);
+  if (sa_fp4_qkv_bytes_s(shape, off) == 0) {
+    const sa_status st = check_dims(dims_of(shape));
     return st != SA_OK ? st : SA_ERR_INVALID_ARG;     // an empty problem has no blob
   }
   uint8_t* p = static_cast<uint8_t*>(blob);
@@ -164,19 +177,26 @@ sa_status sa_fp4_qkv_from_blob(void* blob, int B, int H, int Hkv, int L, int d, 
   return SA_OK;
 }
 
+sa_status sa_fp4_qkv_from_blob(void* blob, int B, int H, int Hkv, int L, int d, sa_fp4_qkv* out) {
+  const sa_shape s{B, H, Hkv, L, L, d};
+  return sa_fp4_qkv_from_blob_s(blob, &s, out);
+}
+
 static bool fp4_ptrs_ok(const sa_fp4_qkv* x) {
   return x && aligned16(x->q_codes) && aligned16(x->q_sf) && aligned16(x->k_codes) && aligned16(x->k_sf) &&
          aligned16(x->v_codes) && aligned16(x->v_sf) && aligned16(x->k_mean) && aligned16(x->workspace);
 }
 
-sa_status sa_quantize_ex(const void* q, const void* k, const void* v, int B, int H, int Hkv, int L, int d, int flags,
-                         const sa_fp4_qkv* out, sa_stream_t stream) {
-  const sa_status st = check_dims(B, H, Hkv, L, d);
+sa_status sa_quantize_s(const void* q, const void* k, const void* v, const sa_shape* shape, int flags,
+                        const sa_fp4_qkv* out, sa_stream_t stream) {
+  if (!shape) return SA_ERR_INVALID_ARG;
+  const Dims dm = dims_of(shape);
+  const sa_status st = check_dims(dm);
   if (st != SA_OK) return st;
   if (flags & ~SA_LAYOUT_BLHD) return SA_ERR_INVALID_ARG;
-  if (empty_problem(B, L)) return SA_OK;
+  if (dm.B == 0 || (dm.Lq == 0 && dm.Lkv == 0)) return SA_OK;
+  if (dm.Lq == 0) return SA_ERR_INVALID_ARG;            // keys without queries: nothing to quantise them for
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !fp4_ptrs_ok(out)) return SA_ERR_INVALID_ARG;
-  const Dims dm{B, H, Hkv, L, d};
   const bool blhd = (flags & SA_LAYOUT_BLHD) != 0;
   CUtensorMap tq, tk;
   if (!make_bf16_row_maps(q, k, dm, blhd, &tq, &tk)) return SA_ERR_CUDA;
@@ -185,22 +205,29 @@ sa_status sa_quantize_ex(const void* q, const void* k, const void* v, int B, int
              : SA_ERR_CUDA;
 }
 
+sa_status sa_quantize_ex(const void* q, const void* k, const void* v, int B, int H, int Hkv, int L, int d, int flags,
+                         const sa_fp4_qkv* out, sa_stream_t stream) {
+  const sa_shape s{B, H, Hkv, L, L, d};
+  return sa_quantize_s(q, k, v, &s, flags, out, stream);
+}
+
 sa_status sa_quantize(const void* q, const void* k, const void* v, int B, int H, int Hkv, int L, int d,
                       const sa_fp4_qkv* out, sa_stream_t stream) {
-  return sa_quantize_ex(q, k, v, B, H, Hkv, L, d, 0, out, stream);
+  const sa_shape s{B, H, Hkv, L, L, d};
+  return sa_quantize_s(q, k, v, &s, 0, out, stream);
 }
 
 sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v, int B, int H, int Hkv, int L,
                                      int d, const sa_fp4_qkv* out, sa_stream_t stream) {
-  const sa_status st = check_dims(B, H, Hkv, L, d);
+  const Dims dm{B, H, Hkv, L, L, d};
+  const sa_status st = check_dims(dm);
   if (st != SA_OK) return st;
-  if (empty_problem(B, L)) return SA_OK;
+  if (empty_problem(dm)) return SA_OK;
   if ((size_t)B * Hkv * (padded_len(L) / 128) * d > (size_t)SA_STATIC_SCRATCH_FLOATS) return SA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !out || !aligned16(out->q_codes) ||
       !aligned16(out->q_sf) || !aligned16(out->k_codes) || !aligned16(out->k_sf) || !aligned16(out->v_codes) ||
       !aligned16(out->v_sf) || !aligned16(out->k_mean))
     return SA_ERR_INVALID_ARG;
-  const Dims dm{B, H, Hkv, L, d};
   CUtensorMap tq, tk;
   if (!make_bf16_row_maps(q, k, dm, false, &tq, &tk)) return SA_ERR_CUDA;
   return launch_quantize_static_scratch(q, k, v, dm, *out, tq, tk, reinterpret_cast<cudaStream_t>(stream)) ==
@@ -218,50 +245,51 @@ sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v
 // quantiser; 201.4 / 197.3 / 195.2 us after an L2 flush), split-KV when the
 // pairs leave half of the SMs idle and the shares stay long, else one unit
 // per CTA.
-static int resolve_nsplit(int B, int H, int L, int causal, int mode, int requested) {
-  (void)causal;
+static int resolve_nsplit(const Dims& dm, int causal, int mode, int requested) {
   if (requested == 1) return 1;
   if (requested == kStreamK) return kStreamK;
   const int sms = device_sm_count();
   if (requested == 0) {
-    const long long pairs = (long long)(((L + 127) / 128 + 1) / 2) * B * H;
-    if (mode == SA_MODE_NVFP4 && sms > 0 && pairs >= sms && streamk_fits(B, H, L)) return kStreamK;
-    return choose_nsplit(B, H, L, sms);
+    const long long pairs = (long long)(((dm.Lq + 127) / 128 + 1) / 2) * dm.B * dm.H;
+    if (mode == SA_MODE_NVFP4 && sms > 0 && pairs >= sms && streamk_fits(dm.B, dm.H, dm.Lq, dm.Lkv, causal))
+      return kStreamK;
+    return choose_nsplit(dm.B, dm.H, dm.Lq, dm.Lkv, sms);
   }
-  const int nkt = (L + 127) / 128;
+  const int nkt = (dm.Lkv + 127) / 128;
   return requested < nkt ? requested : nkt;
 }
 
 static size_t work_split_bytes(const Dims& dm, int causal, int nsplit) {
   if (nsplit == kStreamK) {
     int ctas = 0;
-    make_streamk_work(dm.B, dm.H, dm.L, causal, device_sm_count() > 0 ? device_sm_count() : 1, &ctas);
+    make_streamk_work(dm.B, dm.H, dm.Lq, dm.Lkv, causal, device_sm_count() > 0 ? device_sm_count() : 1, &ctas);
     return streamk_workspace_bytes(dm, ctas);
   }
   return splitkv_workspace_bytes(dm, nsplit);
 }
 
-static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int L,
-                               int d, int causal, int mode_flags, int nsplit_req, void* workspace,
-                               size_t workspace_bytes, sa_stream_t stream) {
-  const sa_status st = check_dims(B, H, Hkv, L, d);
+static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, const Dims& dm, int causal,
+                               int mode_flags, int nsplit_req, void* workspace, size_t workspace_bytes,
+                               sa_stream_t stream) {
+  const sa_status st = check_dims(dm);
   if (st != SA_OK) return st;
   if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
+  if (causal && dm.Lkv < dm.Lq) return SA_ERR_INVALID_ARG;   // the first queries would see no key
   if (mode_flags & ~(0xF | SA_OUT_FP32 | SA_LAYOUT_BLHD)) return SA_ERR_INVALID_ARG;
   const int mode = mode_flags & 0xF;
   if (mode != SA_MODE_BF16 && mode != SA_MODE_NVFP4) return SA_ERR_INVALID_ARG;
   if (nsplit_req < kStreamK) return SA_ERR_INVALID_ARG;
-  if (nsplit_req == kStreamK && (mode != SA_MODE_NVFP4 || !streamk_fits(B, H, L))) return SA_ERR_UNSUPPORTED;
-  if (empty_problem(B, L)) return SA_OK;
+  if (nsplit_req == kStreamK && (mode != SA_MODE_NVFP4 || !streamk_fits(dm.B, dm.H, dm.Lq, dm.Lkv, causal)))
+    return SA_ERR_UNSUPPORTED;
+  if (empty_problem(dm)) return SA_OK;
   const bool out_f32 = (mode_flags & SA_OUT_FP32) != 0;
   const bool blhd = (mode_flags & SA_LAYOUT_BLHD) != 0;
   if (!aligned16(o)) return SA_ERR_INVALID_ARG;
-  const Dims dm{B, H, Hkv, L, d};
-  const Strides so = layout_strides(blhd, H, L, d);            // O (and Q) strides
+  const Strides so = layout_strides(blhd, dm.H, dm.Lq, dm.d);            // O strides
   // split-KV and stream-K only with a workspace large enough for the partial
   // results (a forced choice without one is an argument error; the library's
   // own choice then falls back to one unit per CTA)
-  int nsplit = resolve_nsplit(B, H, L, causal, mode, nsplit_req);
+  int nsplit = resolve_nsplit(dm, causal, mode, nsplit_req);
   const bool needs_ws = nsplit > 1 || nsplit == kStreamK;
   const bool ws_ok = workspace != nullptr && workspace_bytes >= work_split_bytes(dm, causal, nsplit);
   if (needs_ws && !ws_ok && nsplit_req != 0) return SA_ERR_INVALID_ARG;
@@ -271,15 +299,15 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
   if (nsplit > 1) part = splitkv_layout(workspace, dm, nsplit);
   if (nsplit == kStreamK) {
     int ctas = 0;
-    make_streamk_work(B, H, L, causal, device_sm_count() > 0 ? device_sm_count() : 1, &ctas);
+    make_streamk_work(dm.B, dm.H, dm.Lq, dm.Lkv, causal, device_sm_count() > 0 ? device_sm_count() : 1, &ctas);
     part = streamk_layout(workspace, dm, ctas);
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   CUtensorMap tq, tk, tv;
   if (mode == SA_MODE_BF16) {
     if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return SA_ERR_INVALID_ARG;
-    if (!make_bf16_head_map(&tq, q, H, dm, blhd) || !make_bf16_head_map(&tk, k, Hkv, dm, blhd) ||
-        !make_bf16_head_map(&tv, v, Hkv, dm, blhd))
+    if (!make_bf16_head_map(&tq, q, dm.H, dm.Lq, dm, blhd) || !make_bf16_head_map(&tk, k, dm.Hkv, dm.Lkv, dm, blhd) ||
+        !make_bf16_head_map(&tv, v, dm.Hkv, dm.Lkv, dm, blhd))
       return SA_ERR_CUDA;
     return launch_attn_bf16(tq, tk, tv, o, so, dm, causal, out_f32, nsplit, part, s) == cudaSuccess ? SA_OK
                                                                                                     : SA_ERR_CUDA;
@@ -290,11 +318,13 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
       !aligned16(x->v_codes) || !aligned16(x->v_sf))
     return SA_ERR_INVALID_ARG;
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const int d = dm.d;
   const CUtensorMapSwizzle qk_swz = d == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
-  const int Lp = padded_len(L);      // the quantised layouts hold whole 128-token tiles
-  if (!make_map(&tq, u8, x->q_codes, d / 2, (uint64_t)B * H * Lp, 1, d / 2, 128, qk_swz) ||
-      !make_map(&tk, u8, x->k_codes, d / 2, (uint64_t)B * Hkv * Lp, 1, d / 2, 128, qk_swz) ||
-      !make_map(&tv, u8, x->v_codes, Lp / 2, (uint64_t)B * Hkv * d, 1, 64, d, CU_TENSOR_MAP_SWIZZLE_64B))
+  // the quantised layouts hold whole 128-token tiles
+  const int Lqp = padded_len(dm.Lq), Lkvp = padded_len(dm.Lkv);
+  if (!make_map(&tq, u8, x->q_codes, d / 2, (uint64_t)dm.B * dm.H * Lqp, 1, d / 2, 128, qk_swz) ||
+      !make_map(&tk, u8, x->k_codes, d / 2, (uint64_t)dm.B * dm.Hkv * Lkvp, 1, d / 2, 128, qk_swz) ||
+      !make_map(&tv, u8, x->v_codes, Lkvp / 2, (uint64_t)dm.B * dm.Hkv * d, 1, 64, d, CU_TENSOR_MAP_SWIZZLE_64B))
     return SA_ERR_CUDA;
   return launch_attn_nvfp4(tq, tk, tv, *x, o, so, dm, causal, out_f32, nsplit, part, s) == cudaSuccess
              ? SA_OK
@@ -303,22 +333,35 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
 
 sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int L, int d,
                       int causal, int mode_flags, sa_stream_t stream) {
-  return attn_fwd_impl(q, k, v, o, B, H, Hkv, L, d, causal, mode_flags, 1, nullptr, 0, stream);
+  return attn_fwd_impl(q, k, v, o, Dims{B, H, Hkv, L, L, d}, causal, mode_flags, 1, nullptr, 0, stream);
+}
+
+size_t sa_attn_fwd_workspace_bytes_s(const sa_shape* shape, int causal, int mode, int nsplit) {
+  if (!shape) return 0;
+  const Dims dm = dims_of(shape);
+  const int m = mode & 0xF;
+  if (check_dims(dm) != SA_OK || empty_problem(dm) || nsplit < kStreamK) return 0;
+  if (causal != 0 && causal != 1) return 0;
+  if (nsplit == kStreamK && m != SA_MODE_NVFP4) return 0;
+  return work_split_bytes(dm, causal, resolve_nsplit(dm, causal, m, nsplit));
 }
 
 size_t sa_attn_fwd_workspace_bytes(int B, int H, int Hkv, int L, int d, int causal, int mode, int nsplit) {
-  const int m = mode & 0xF;
-  if (check_dims(B, H, Hkv, L, d) != SA_OK || empty_problem(B, L) || nsplit < kStreamK) return 0;
-  if (causal != 0 && causal != 1) return 0;
-  if (nsplit == kStreamK && m != SA_MODE_NVFP4) return 0;
-  const Dims dm{B, H, Hkv, L, d};
-  return work_split_bytes(dm, causal, resolve_nsplit(B, H, L, causal, m, nsplit));
+  const sa_shape s{B, H, Hkv, L, L, d};
+  return sa_attn_fwd_workspace_bytes_s(&s, causal, mode, nsplit);
+}
+
+sa_status sa_attn_fwd_s(const void* q, const void* k, const void* v, void* o, const sa_shape* shape, int causal,
+                        int mode, int nsplit, void* workspace, size_t workspace_bytes, sa_stream_t stream) {
+  if (!shape) return SA_ERR_INVALID_ARG;
+  return attn_fwd_impl(q, k, v, o, dims_of(shape), causal, mode, nsplit, workspace, workspace_bytes, stream);
 }
 
 sa_status sa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int L, int d,
                          int causal, int mode, int nsplit, void* workspace, size_t workspace_bytes,
                          sa_stream_t stream) {
-  return attn_fwd_impl(q, k, v, o, B, H, Hkv, L, d, causal, mode, nsplit, workspace, workspace_bytes, stream);
+  return attn_fwd_impl(q, k, v, o, Dims{B, H, Hkv, L, L, d}, causal, mode, nsplit, workspace, workspace_bytes,
+                       stream);
 }
 
 sa_status sa_last_device_error(void) {

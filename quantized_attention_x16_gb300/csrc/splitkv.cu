@@ -66,11 +66,11 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) splitkv_combine_kernel(const
 
 template <int D, bool OUT32>
 cudaError_t launch(const SplitOut& part, int nsplit, const Dims& dm, void* o, const Strides& so, cudaStream_t s) {
-  const long long nrows = (long long)dm.B * dm.H * dm.L;
-  const int Lp = padded_len(dm.L);
+  const long long nrows = (long long)dm.B * dm.H * dm.Lq;
+  const int Lp = padded_len(dm.Lq);
   const long long split_rows = (long long)dm.B * dm.H * Lp;
   const long long ctas = (nrows + kRowsPerCta - 1) / kRowsPerCta;
-  splitkv_combine_kernel<D, OUT32><<<(unsigned)ctas, 32 * kRowsPerCta, 0, s>>>(part, nsplit, nrows, dm.L, Lp,
+  splitkv_combine_kernel<D, OUT32><<<(unsigned)ctas, 32 * kRowsPerCta, 0, s>>>(part, nsplit, nrows, dm.Lq, Lp,
                                                                               split_rows, dm.H, so, o);
   return cudaGetLastError();
 }
@@ -126,7 +126,7 @@ cudaError_t launch_sk(const AttnWork& w, int ctas, const SplitOut& part, const D
   StreamKCuts cuts;
   make_streamk_cuts(w, ctas, &cuts);
   if (cuts.n == 0) return cudaSuccess;               // no pair was cut
-  streamk_combine_kernel<D, OUT32><<<dim3(cuts.n, 256 / kRowsPerCta), 32 * kRowsPerCta, 0, s>>>(cuts, part, dm.L,
+  streamk_combine_kernel<D, OUT32><<<dim3(cuts.n, 256 / kRowsPerCta), 32 * kRowsPerCta, 0, s>>>(cuts, part, dm.Lq,
                                                                                                 dm.H, so, o);
   return cudaGetLastError();
 }

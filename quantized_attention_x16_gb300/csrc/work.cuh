@@ -21,9 +21,12 @@
 namespace sa {
 
 constexpr int kMaxStreamKCtas = 160;   // persistent grid cap (one CTA per SM)
+constexpr int kMaxStreamKGroups = 512;  // causal stream-K: query-tile pairs per head (Lq <= 128k)
 
 struct AttnWork {
-  int nqt;     // 128-row query tiles per head
+  int nqt;     // 128-row query tiles per head (from Lq)
+  int nkt;     // 128-key tiles per head (from Lkv)
+  int coff;    // causal: key j is visible to query i iff j <= i + coff (coff = Lkv - Lq)
   int ppr;     // pair slots per head, ceil(nqt / 2)
   int nbh;     // B * H
   int npair;   // units [0, npair) are pairs; then 2 * (ppr * nbh - npair) singles
@@ -32,12 +35,23 @@ struct AttnWork {
   int streamk; // 1: persistent CTAs over equal ranges of (pair, key tile) items
   long long items;   // stream-K: total items (key tiles over all pairs)
   int sk_x0[kMaxStreamKCtas + 1];   // stream-K: first item of CTA c's range (c = 0..C)
+  long long sk_grp[kMaxStreamKGroups + 1];   // causal stream-K: items before pair group g
 };
 
+// Key tiles query tile qt needs: all of them, or under the causal mask up to
+// the tile holding the last key its last row may see.
+__host__ __device__ inline int q_tile_keys(const AttnWork& w, int qt) {
+  if (!w.causal) return w.nkt;
+  const long long n = ((long long)qt * 128 + 127 + w.coff) / 128 + 1;
+  return (int)(n < w.nkt ? n : w.nkt);
+}
+
 // Host: the work list for a problem and the number of CTAs to launch.
-inline AttnWork make_attn_work(int B, int H, int L, int causal, int num_sms, int* ctas, int nsplit = 1) {
+inline AttnWork make_attn_work(int B, int H, int Lq, int Lkv, int causal, int num_sms, int* ctas, int nsplit = 1) {
   AttnWork w;
-  w.nqt = (L + 127) / 128;   // a ragged last tile counts as a tile
+  w.nqt = (Lq + 127) / 128;   // a ragged last tile counts as a tile
+  w.nkt = (Lkv + 127) / 128;
+  w.coff = Lkv - Lq;
   w.ppr = (w.nqt + 1) / 2;
   w.nbh = B * H;
   w.causal = causal;
@@ -70,22 +84,19 @@ inline AttnWork make_attn_work(int B, int H, int L, int causal, int num_sms, int
 // Key tiles of pair slot p (dispatch order): the union of its query tiles'
 // ranges (causal: up to the diagonal of its second query tile).
 __host__ __device__ inline int sk_pair_tiles(const AttnWork& w, long long p) {
-  const int nkt = w.nqt;
-  if (!w.causal) return nkt;
+  if (!w.causal) return w.nkt;
   const int pi = w.ppr - 1 - (int)(p / w.nbh);
   const int qt0 = 2 * pi;
-  return qt0 + 1 < w.nqt ? qt0 + 2 : qt0 + 1;
+  return q_tile_keys(w, qt0 + 1 < w.nqt ? qt0 + 1 : qt0);
 }
 
-// Items before pair slot p.
+// Items before pair slot p.  Causal: the pairs of group g (index pi =
+// ppr-1-g in every head) all have the same tile count; sk_grp[g] holds the
+// items of the groups before g (filled on the host).
 __host__ __device__ inline long long sk_prefix(const AttnWork& w, long long p) {
-  if (!w.causal) return p * w.nqt;
-  const long long g = p / w.nbh;                  // whole groups of nbh pairs before p
-  // group g' holds pairs of index pi = ppr-1-g' with 2*(ppr-g') tiles, one
-  // fewer for g' = 0 when the head has an odd number of query tiles
-  long long t = (long long)w.nbh * (2 * g * w.ppr - g * (g - 1));
-  if ((w.nqt & 1) && g > 0) t -= w.nbh;
-  return t + (p - g * w.nbh) * sk_pair_tiles(w, p);
+  if (!w.causal) return p * w.nkt;
+  const long long g = p / w.nbh;
+  return w.sk_grp[g] + (p - g * w.nbh) * sk_pair_tiles(w, p);
 }
 
 // The pair holding item x (0 <= x < items).
@@ -138,11 +149,16 @@ struct UnitIter {
 // per item when there are fewer items).
 // The ranges are fixed on the host (first items in sk_x0, 32-bit: stream-K
 // is used only while the item count fits).
-inline AttnWork make_streamk_work(int B, int H, int L, int causal, int num_sms, int* ctas) {
-  AttnWork w = make_attn_work(B, H, L, causal, num_sms, ctas, 2);   // pairs only
+inline AttnWork make_streamk_work(int B, int H, int Lq, int Lkv, int causal, int num_sms, int* ctas) {
+  AttnWork w = make_attn_work(B, H, Lq, Lkv, causal, num_sms, ctas, 2);   // pairs only
   w.nsplit = 1;
   w.streamk = 1;
-  w.items = sk_prefix(w, (long long)w.ppr * w.nbh);
+  if (causal) {
+    w.sk_grp[0] = 0;
+    for (int g = 0; g < w.ppr && g < kMaxStreamKGroups; ++g)
+      w.sk_grp[g + 1] = w.sk_grp[g] + (long long)w.nbh * sk_pair_tiles(w, (long long)g * w.nbh);
+  }
+  w.items = causal ? w.sk_grp[w.ppr] : sk_prefix(w, (long long)w.ppr * w.nbh);
   long long c = w.items < num_sms ? w.items : num_sms;
   if (c > kMaxStreamKCtas) c = kMaxStreamKCtas;
   if (c < 1) c = 1;
@@ -150,9 +166,10 @@ inline AttnWork make_streamk_work(int B, int H, int L, int causal, int num_sms, 
   *ctas = (int)c;
   return w;
 }
-inline bool streamk_fits(int B, int H, int L) {
-  const long long nqt = (L + 127) / 128;
-  return (nqt + 1) / 2 * (long long)B * H * nqt < (1ll << 31);
+inline bool streamk_fits(int B, int H, int Lq, int Lkv, int causal) {
+  const long long nqt = (Lq + 127) / 128, nkt = (Lkv + 127) / 128;
+  if (causal && (nqt + 1) / 2 > kMaxStreamKGroups) return false;
+  return (nqt + 1) / 2 * (long long)B * H * nkt < (1ll << 31);
 }
 
 // The pairs that range boundaries cut, for the combine pass: per cut pair its
@@ -202,9 +219,9 @@ inline void make_streamk_cuts(const AttnWork& w, int C, StreamKCuts* cuts) {
 // B1 H8 L1024, eight key tiles per query tile, takes 19 us unsplit and 24-25
 // us in two or four shares).  Returns 1 (no split) otherwise.
 constexpr int kMinShareTiles = 16;
-inline int choose_nsplit(int B, int H, int L, int num_sms) {
-  const int nkt = (L + 127) / 128;
-  const long long pairs = (long long)((nkt + 1) / 2) * B * H;
+inline int choose_nsplit(int B, int H, int Lq, int Lkv, int num_sms) {
+  const int nqt = (Lq + 127) / 128, nkt = (Lkv + 127) / 128;
+  const long long pairs = (long long)((nqt + 1) / 2) * B * H;
   if (num_sms <= 0 || pairs <= 0 || 2 * pairs > num_sms) return 1;
   int s = (int)(num_sms / pairs);
   if (s > nkt / kMinShareTiles) s = nkt / kMinShareTiles;
@@ -245,8 +262,8 @@ __host__ __device__ inline bool sk_next(const AttnWork& w, int cta, UnitIter& it
   const int b = it.xe - P < nt ? it.xe - P : nt;
   pair_head(w, it.p, u.bh, u.qt0, u.nq);
   u.jb = a;
-  const int n0 = w.causal ? u.qt0 + 1 : w.nqt;
-  const int n1 = u.nq == 2 ? (w.causal ? u.qt0 + 2 : w.nqt) : 0;
+  const int n0 = q_tile_keys(w, u.qt0);
+  const int n1 = u.nq == 2 ? q_tile_keys(w, u.qt0 + 1) : 0;
   u.n[0] = (n0 < b ? n0 : b) > a ? (n0 < b ? n0 : b) - a : 0;
   u.n[1] = (n1 < b ? n1 : b) > a ? (n1 < b ? n1 : b) - a : 0;
   u.slot = (a == 0 && b == nt) ? -1 : 2 * cta + (it.x == it.x0 ? 0 : 1);
@@ -293,8 +310,8 @@ __device__ __forceinline__ bool unit_next(const AttnWork& w, UnitIter& it, AttnU
     // one unit: this CTA's entry of the work list (a share of it under split-KV)
     int sp;
     attn_unit(w, (int)blockIdx.x, u.bh, u.qt0, u.nq, sp);
-    u.n[0] = w.causal ? u.qt0 + 1 : w.nqt;
-    u.n[1] = u.nq == 2 ? (w.causal ? u.qt0 + 2 : w.nqt) : 0;
+    u.n[0] = q_tile_keys(w, u.qt0);
+    u.n[1] = u.nq == 2 ? q_tile_keys(w, u.qt0 + 1) : 0;
     u.jb = w.nsplit > 1 ? split_range(sp, w.nsplit, u.n) : 0;
     u.slot = w.nsplit > 1 ? sp : -1;
     it.done = 1;

@@ -7,7 +7,10 @@
 //    is 2c (it begins CTA c's range) or 2c + 1 (it ends it); the cut table
 //    lists every cut pair once, and its segments are exactly the partial
 //    units of that pair, in CTA order;
-//  * split-KV: the shares of each pair tile its key range.
+//  * split-KV: the shares of each pair tile its key range;
+//  * with a query length different from the key length, each query tile's
+//    key-tile count is the number of key tiles holding a key its rows may see
+//    (brute force over rows and keys under the bottom-right causal mask).
 // Prints "OK" and returns 0, or prints the first failure and returns 1.
 #include <cstdio>
 #include <vector>
@@ -21,9 +24,24 @@ static int fail(const char* what, int B, int H, int L, int causal, int C) {
   return 1;
 }
 
-static int check_streamk(int B, int H, int L, int causal, int sms) {
+static int check_key_counts(int Lq, int Lkv, int causal) {
+  int ctas = 0;
+  const AttnWork w = make_attn_work(1, 1, Lq, Lkv, causal, 152, &ctas);
+  for (int qt = 0; qt < w.nqt; ++qt) {
+    int need = 0;                                 // key tiles holding a key some valid row may see
+    for (int r = qt * 128; r < qt * 128 + 128 && r < Lq; ++r) {
+      const int last = causal ? r + (Lkv - Lq) : Lkv - 1;
+      const int tiles = last / 128 + 1;
+      if (tiles > need) need = tiles;
+    }
+    if (q_tile_keys(w, qt) != need) return fail("key tiles of a query tile", Lq, Lkv, qt, causal, 0);
+  }
+  return 0;
+}
+
+static int check_streamk(int B, int H, int L, int Lkv, int causal, int sms) {
   int C = 0;
-  AttnWork w = make_streamk_work(B, H, L, causal, sms, &C);
+  AttnWork w = make_streamk_work(B, H, L, Lkv, causal, sms, &C);
   const long long npairs = (long long)w.ppr * w.nbh;
   long long acc = 0;
   for (long long p = 0; p < npairs; ++p) {
@@ -65,8 +83,9 @@ static int check_streamk(int B, int H, int L, int causal, int sms) {
         if (u.slot != want) return fail("slot", B, H, L, causal, C);
         parts[p].push_back({c, u.slot});
       }
-      // per query tile counts: query tile 0 never exceeds the causal diagonal
-      if (causal && u.jb + u.n[0] > u.qt0 + 1) return fail("causal range", B, H, L, causal, C);
+      // per query tile counts: never past the tiles the query tile may see
+      if (u.jb + u.n[0] > q_tile_keys(w, u.qt0)) return fail("causal range", B, H, L, causal, C);
+      if (u.nq == 2 && u.jb + u.n[1] > q_tile_keys(w, u.qt0 + 1)) return fail("causal range 1", B, H, L, causal, C);
       ++k;
     }
     if (prev_end != w.sk_x0[c + 1]) return fail("range end", B, H, L, causal, C);
@@ -95,14 +114,14 @@ static int check_streamk(int B, int H, int L, int causal, int sms) {
   return 0;
 }
 
-static int check_split(int B, int H, int L, int causal, int nsplit) {
+static int check_split(int B, int H, int L, int Lkv, int causal, int nsplit) {
   AttnWork w;
   int ctas = 0;
-  w = make_attn_work(B, H, L, causal, 152, &ctas, nsplit);
+  w = make_attn_work(B, H, L, Lkv, causal, 152, &ctas, nsplit);
   for (int p = 0; p < w.ppr * w.nbh; ++p) {
     const int pi = causal ? w.ppr - 1 - p / w.nbh : p % w.ppr;
     const int qt0 = 2 * pi;
-    int full[2] = {causal ? qt0 + 1 : w.nqt, qt0 + 1 < w.nqt ? (causal ? qt0 + 2 : w.nqt) : 0};
+    int full[2] = {q_tile_keys(w, qt0), qt0 + 1 < w.nqt ? q_tile_keys(w, qt0 + 1) : 0};
     int next[2] = {0, 0};
     for (int s = 0; s < w.nsplit; ++s) {
       int n[2] = {full[0], full[1]};
@@ -118,15 +137,19 @@ static int check_split(int B, int H, int L, int causal, int nsplit) {
 }
 
 int main() {
-  const int shapes[][3] = {{1, 1, 128}, {1, 1, 200}, {1, 2, 640}, {2, 16, 4096}, {1, 32, 8192}, {1, 3, 1000},
-                           {3, 5, 1536}, {1, 8, 16384}, {1, 24, 16384}, {2, 1, 384}};
+  // B, H, Lq, Lkv (Lkv >= Lq: the causal mask needs it)
+  const int shapes[][4] = {{1, 1, 128, 128}, {1, 1, 200, 200}, {1, 2, 640, 640}, {2, 16, 4096, 4096},
+                           {1, 32, 8192, 8192}, {1, 3, 1000, 1000}, {3, 5, 1536, 1536}, {1, 8, 16384, 16384},
+                           {1, 24, 16384, 16384}, {2, 1, 384, 384}, {4, 8, 1, 4096}, {2, 3, 16, 1000},
+                           {1, 2, 200, 8192}, {3, 4, 300, 333}, {1, 1, 128, 32768}, {8, 4, 129, 2048}};
   const int grids[] = {1, 2, 7, 64, 148, 152, 160};
   for (auto& sh : shapes)
     for (int causal = 0; causal < 2; ++causal) {
+      if (check_key_counts(sh[2], sh[3], causal)) return 1;
       for (int g : grids)
-        if (check_streamk(sh[0], sh[1], sh[2], causal, g)) return 1;
+        if (check_streamk(sh[0], sh[1], sh[2], sh[3], causal, g)) return 1;
       for (int ns : {2, 3, 4, 7, 16})
-        if (check_split(sh[0], sh[1], sh[2], causal, ns)) return 1;
+        if (check_split(sh[0], sh[1], sh[2], sh[3], causal, ns)) return 1;
     }
   std::printf("OK\n");
   return 0;

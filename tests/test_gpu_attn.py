@@ -259,3 +259,45 @@ def test_streamk_full_size(sa, name):
     check(o, x, w["causal"], [(0, 0), (w["B"] - 1, w["H"] - 1)], rows, "nvfp4", o32)
     ref = run_gpu(sa, x, w["causal"], "nvfp4", torch.float32)
     assert np.abs(o32 - ref).max() <= 1e-5 * np.abs(ref).max()
+
+
+# Query length different from key length (decode, a chunk against a longer
+# key/value sequence): the causal mask is bottom-right aligned (key j visible
+# to query i iff j <= i + Lkv - Lq), as in the oracle.
+QK = [
+    (dict(W.spec("causal_gqa"), B=2, H=4, Hkv=2, seed=81), 1, 1000),        # decode: one query token
+    (dict(W.spec("dit_video"), B=1, H=4, Hkv=1, d=64, seed=82), 16, 700),
+    (dict(W.spec("llm_prefill"), B=1, H=2, Hkv=2, seed=83), 200, 1500),     # a chunk, ragged both ends
+    (dict(W.spec("causal_gqa"), B=1, H=4, Hkv=2, seed=84), 129, 384),
+    (dict(W.spec("llm_prefill"), B=1, H=2, Hkv=1, seed=85), 128, 4096),
+]
+
+
+def qk_inputs(w, Lq, Lkv):
+    kv = W.make_inputs(dict(w, L=Lkv))
+    q = W.make_inputs(dict(w, L=Lq, seed=w["seed"] + 1))["q"]
+    return dict(q=q, k=kv["k"], v=kv["v"])
+
+
+def run_qk(sa, x, causal, mode, nsplit, out_dtype=torch.bfloat16):
+    q, k, v = (x[n].cuda() for n in "qkv")
+    args = (q, k, v) if mode == "bf16" else (sa.sa_quantize(q, k, v),)
+    o = sa.sa_attn_fwd(*args, causal=causal, mode=mode, out_dtype=out_dtype, nsplit=nsplit)
+    torch.cuda.synchronize()
+    assert sa.sa_last_device_error() == 0
+    return o.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("nsplit", [None, 3, -1])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("mode", ["bf16", "nvfp4"])
+@pytest.mark.parametrize("case", QK, ids=lambda c: f"B{c[0]['B']}H{c[0]['H']}K{c[0]['Hkv']}d{c[0]['d']}-Lq{c[1]}-Lkv{c[2]}")
+def test_query_length_differs_from_key_length(sa, case, mode, causal, nsplit):
+    if nsplit == -1 and mode == "bf16":
+        pytest.skip("stream-K is a schedule of the NVFP4 path")
+    w, Lq, Lkv = case
+    x = qk_inputs(w, Lq, Lkv)
+    o = run_qk(sa, x, causal, mode, nsplit)
+    o32 = run_qk(sa, x, causal, mode, nsplit, torch.float32) if mode == "nvfp4" else None
+    heads = [(b, h) for b in range(w["B"]) for h in range(w["H"])]
+    check(o, x, causal, heads, np.arange(Lq), mode, o32)

@@ -68,6 +68,14 @@ def test_quantize_small_bit_exact(sa, w):
     assert_same(gpu_quant(sa, x), oracle_quant(x))
 
 
+@pytest.mark.parametrize("Lq,Lkv", [(1, 1000), (16, 700), (200, 129)])
+def test_quantize_query_and_key_lengths_differ(sa, Lq, Lkv):
+    w = dict(W.spec("causal_gqa"), B=2, H=4, Hkv=2, seed=90 + Lq)
+    kv = W.make_inputs(dict(w, L=Lkv))
+    x = dict(q=W.make_inputs(dict(w, L=Lq, seed=w["seed"] + 1))["q"], k=kv["k"], v=kv["v"])
+    assert_same(gpu_quant(sa, x), oracle_quant(x))
+
+
 def crafted_inputs(d=128, L=256):
     """Groups that hit every rounding corner: e2m1 midpoints, e4m3 scale ties,
     saturation, zero / tiny / subnormal-scale groups, signed zeros."""
