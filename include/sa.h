@@ -270,22 +270,28 @@ sa_status sa_attn_fwd_s(const void* q, const void* k, const void* v, void* o, co
  *    sa_attn_fwd_host_workspace_bytes(B, H, Hkv, L, d, mode, chunk_pairs)
  *    bytes, 256-byte aligned; must not be used by anything else until the
  *    call's work on `stream` has completed.
- *  chunk_pairs: (batch, kv head) pairs per chunk; 0 = the library's choice
- *    (the most pairs whose attention CTAs fit in one wave on the SMs, and at
- *    least two chunks).
+ *  chunk_pairs: (batch, kv head) pairs per chunk, the last chunk ragged;
+ *    0 = the library's chunking: chunks of n pairs (the most whose attention
+ *    CTAs fit in one wave on the SMs, and at least two chunks); for
+ *    SA_MODE_NVFP4 the last ones shrink by halves (..., n, 8, 4, 2 pairs)
+ *    and a chunk whose CTAs would leave half of the SMs idle runs with
+ *    split-KV (shares of 8 key tiles or more).
  * The problem is cut into chunks of consecutive (batch, kv head) pairs with
  * all their query heads.  Each chunk's inputs are copied host -> device on a
  * copy stream, computed on `stream` (the same kernels as the device-buffer
- * calls, so results are bit-identical to them), and its O copied back on a
- * second copy stream; two workspace slots alternate between chunks, so the
- * copies of one chunk overlap the compute of its neighbours.  The copies
- * start after the work already enqueued on `stream`, and `stream` reaches
- * the end of the call's work only after O is in host memory (synchronise on
- * `stream` before reading o).  The two copy streams and seven events are
- * created on the first call on each device and kept until the process
- * exits; calls on one device must not be made concurrently from several host
- * threads.  Errors as for sa_attn_fwd; a failure after the first copy was
- * enqueued leaves o partly written.
+ * calls) and its O copied back on a second copy stream; three workspace
+ * slots rotate between chunks, so the copies of one chunk overlap the compute
+ * of its neighbours, and the shrinking last chunks shorten the part of the
+ * call that no copy-in overlaps.  The results are bit-identical to
+ * sa_quantize + sa_attn_fwd on device buffers, except that a split NVFP4
+ * chunk (chunk_pairs 0) differs from them in float32 summation order (its P
+ * is quantised per key tile, so split-KV changes nothing else).  The copies start after the work already enqueued on
+ * `stream`, and `stream` reaches the end of the call's work only after O is
+ * in host memory (synchronise on `stream` before reading o).  The two copy
+ * streams and ten events are created on the first call on each device and
+ * kept until the process exits; calls on one device must not be made
+ * concurrently from several host threads.  Errors as for sa_attn_fwd; a
+ * failure after the first copy was enqueued leaves o partly written.
  */
 size_t sa_attn_fwd_host_workspace_bytes(int B, int H, int Hkv, int L, int d, int mode, int chunk_pairs);
 sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,

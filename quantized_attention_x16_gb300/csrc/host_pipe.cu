@@ -6,20 +6,31 @@
 // the quantiser and attention kernels work per head.  The problem is cut into
 // chunks of consecutive pairs (all G query heads of each); in BHLD layout a
 // chunk's Q, K, V and O are contiguous ranges, so a chunk is itself a problem
-// with B = 1, H = n * G, Hkv = n.  Chunk c uses device slot c & 1 of the
+// with B = 1, H = n * G, Hkv = n.  Chunk c uses device slot c % 3 of the
 // caller's workspace:
-//   copy-in stream : Q, K, V of chunk c  host -> slot        (after chunk c-2's compute)
-//   caller's stream: sa_quantize + sa_attn_fwd on the slot    (after its copy-in and
-//                                                              chunk c-2's copy-out)
+//   copy-in stream : Q, K, V of chunk c  host -> slot        (after chunk c-3's compute)
+//   caller's stream: sa_quantize + attention on the slot      (after its copy-in and
+//                                                              chunk c-3's copy-out)
 //   copy-out stream: O of chunk c  slot -> host              (after its compute)
 // so the copies of one chunk run beside the compute of its neighbours.  The
-// kernels compute every head exactly as on the whole problem, so the results
-// are bit-identical to sa_quantize + sa_attn_fwd on device buffers.
+// host link is the bound (the copies of the whole problem take longer than
+// its compute); what no copy-in overlaps is the compute and copy-out of the
+// last chunk.  So with the library's chunking of the NVFP4 path the last
+// chunks shrink (..., n, n/2, n/4, ...) and a chunk whose attention CTAs
+// would leave at least half of the SMs idle runs with split-KV (shares of 8
+// key tiles or more, one workspace region that the chunks take in turn on the
+// caller's stream).  The kernels compute every head as on the whole problem:
+// without split-KV the results are bit-identical to sa_quantize +
+// sa_attn_fwd on device buffers; a split NVFP4 chunk differs from them only
+// in float32 summation order, as its P is quantised per key tile whatever the
+// running maximum.  (The BF16 path rounds P relative to the running maximum,
+// which split-KV changes, so its chunks are never split.)
 
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 
@@ -27,13 +38,15 @@ namespace sa {
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kSlots = 3;
+constexpr int kTailMinShareTiles = 8;   // split-KV shares of the shrinking last chunks
 
 // Two copy streams and the events that order the slots, per device; created
 // on first use and kept for the life of the process.
 struct HostPipe {
   bool ready = false;
   cudaStream_t cin = nullptr, cout = nullptr;
-  cudaEvent_t start = nullptr, in[2] = {}, comp[2] = {}, out[2] = {};
+  cudaEvent_t start = nullptr, in[kSlots] = {}, comp[kSlots] = {}, out[kSlots] = {};
 };
 HostPipe g_pipe[kMaxDevices];
 std::mutex g_pipe_mu;
@@ -49,7 +62,7 @@ HostPipe* pipe_for_current_device() {
         cudaStreamCreateWithFlags(&p.cout, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&p.start, ef) != cudaSuccess)
       return nullptr;
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < kSlots; ++i)
       if (cudaEventCreateWithFlags(&p.in[i], ef) != cudaSuccess ||
           cudaEventCreateWithFlags(&p.comp[i], ef) != cudaSuccess ||
           cudaEventCreateWithFlags(&p.out[i], ef) != cudaSuccess)
@@ -61,21 +74,77 @@ HostPipe* pipe_for_current_device() {
 
 size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Attention CTAs of one (batch, kv head) pair: its G heads' query-tile pairs.
+long long units_per_pair(int G, int L) { return (long long)G * (((L + 127) / 128 + 1) / 2); }
+
 // Pairs per chunk: the most whose attention CTAs fit in one wave on the SMs
 // (a chunk's kernels then take about one CTA lifetime), and at least two
 // chunks when there are two pairs or more.
 int default_chunk_pairs(int B, int H, int Hkv, int L) {
   const int G = H / Hkv, pairs = B * Hkv;
-  const int units = G * ((L / 128 + 1) / 2);   // attention CTAs of one pair
-  int n = device_sm_count() / (units > 0 ? units : 1);
+  const long long units = units_per_pair(G, L);
+  long long n = device_sm_count() / (units > 0 ? units : 1);
   if (n < 1) n = 1;
   if (pairs >= 2 && n > (pairs + 1) / 2) n = (pairs + 1) / 2;
-  return n;
+  return (int)n;
+}
+
+// Split-KV shares for a chunk of n pairs in the library's chunking: enough to
+// fill the SMs when its CTAs would leave half of them idle, each share keeping
+// kTailMinShareTiles key tiles, at most 16.
+int chunk_nsplit(int n, int G, int L) {
+  const int sms = device_sm_count(), nkt = (L + 127) / 128;
+  const long long units = (long long)n * units_per_pair(G, L);
+  if (sms <= 0 || units <= 0 || 2 * units > sms) return 1;
+  long long sp = sms / units;
+  if (sp > nkt / kTailMinShareTiles) sp = nkt / kTailMinShareTiles;
+  if (sp > 16) sp = 16;
+  return sp > 1 ? (int)sp : 1;
+}
+
+struct Chunk {
+  int n, nsplit;
+};
+
+// The chunks in order.  A caller's chunk size, or the BF16 path: chunks of
+// chunk_pairs (default n; the last one ragged), no split-KV.  The library's
+// chunking of the NVFP4 path: chunks of n pairs, the last ones shrinking by
+// halves down to min(2, n) pairs (built from the end: 2, 4, 8, ... capped at
+// n), split-KV where chunk_nsplit says so.
+std::vector<Chunk> chunk_plan(int B, int H, int Hkv, int L, int chunk_pairs, bool fp4) {
+  const int pairs = B * Hkv, G = H / Hkv;
+  const int n = default_chunk_pairs(B, H, Hkv, L);
+  std::vector<Chunk> plan;
+  if (chunk_pairs > 0 || !fp4) {
+    const int m = chunk_pairs > 0 ? chunk_pairs : n;
+    for (int p0 = 0; p0 < pairs; p0 += m) plan.push_back(Chunk{pairs - p0 < m ? pairs - p0 : m, 1});
+    return plan;
+  }
+  int rem = pairs, size = n < 2 ? n : 2;
+  while (rem > 0) {
+    const int t = size < rem ? size : rem;
+    plan.push_back(Chunk{t, chunk_nsplit(t, G, L)});
+    rem -= t;
+    size = 2 * size < n ? 2 * size : n;
+  }
+  for (size_t i = 0, j = plan.size() - 1; i < j; ++i, --j) {
+    const Chunk c = plan[i];
+    plan[i] = plan[j];
+    plan[j] = c;
+  }
+  return plan;
 }
 
 // Byte layout of one slot for chunks of up to n pairs.
 struct SlotLayout {
   size_t q, k, v, o, blob, bytes;
+};
+
+// The workspace: kSlots slots for the largest chunk, then the split-KV region
+// (the largest any chunk needs).
+struct PipeLayout {
+  SlotLayout slot;
+  size_t split, split_bytes, bytes;
 };
 SlotLayout slot_layout(int n, int G, int L, int d, bool fp4, size_t osz) {
   SlotLayout s;
@@ -89,6 +158,24 @@ SlotLayout slot_layout(int n, int G, int L, int d, bool fp4, size_t osz) {
   if (fp4) off = al256(off + sa_fp4_qkv_bytes(1, n * G, n, L, d, nullptr));
   s.bytes = off;
   return s;
+}
+
+PipeLayout pipe_layout(const std::vector<Chunk>& plan, int G, int L, int d, bool fp4, size_t osz) {
+  int nmax = 0;
+  size_t split = 0;
+  for (const Chunk& c : plan) {
+    nmax = c.n > nmax ? c.n : nmax;
+    if (c.nsplit > 1) {
+      const size_t b = splitkv_workspace_bytes(Dims{1, c.n * G, c.n, L, L, d}, c.nsplit);
+      split = b > split ? b : split;
+    }
+  }
+  PipeLayout p;
+  p.slot = slot_layout(nmax, G, L, d, fp4, osz);
+  p.split = kSlots * p.slot.bytes;
+  p.split_bytes = split;
+  p.bytes = p.split + al256(split);
+  return p;
 }
 
 bool pinned_host(const void* p) {
@@ -124,11 +211,9 @@ extern "C" {
 
 size_t sa_attn_fwd_host_workspace_bytes(int B, int H, int Hkv, int L, int d, int mode_flags, int chunk_pairs) {
   if (check_host_args(B, H, Hkv, L, d, 0, mode_flags, chunk_pairs) != SA_OK || B == 0 || L == 0) return 0;
-  const int n = chunk_pairs > 0 ? (chunk_pairs < B * Hkv ? chunk_pairs : B * Hkv)
-                                : default_chunk_pairs(B, H, Hkv, L);
   const bool fp4 = (mode_flags & 0xF) == SA_MODE_NVFP4;
   const size_t osz = (mode_flags & SA_OUT_FP32) ? 4 : 2;
-  return 2 * slot_layout(n, H / Hkv, L, d, fp4, osz).bytes;
+  return pipe_layout(chunk_plan(B, H, Hkv, L, chunk_pairs, fp4), H / Hkv, L, d, fp4, osz).bytes;
 }
 
 sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int L, int d,
@@ -140,12 +225,12 @@ sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,
   if (!q || !k || !v || !o || !workspace) return SA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SA_ERR_INVALID_ARG;
   if (!pinned_host(q) || !pinned_host(k) || !pinned_host(v) || !pinned_host(o)) return SA_ERR_INVALID_ARG;
-  const int pairs = B * Hkv, G = H / Hkv;
-  const int n = chunk_pairs > 0 ? (chunk_pairs < pairs ? chunk_pairs : pairs) : default_chunk_pairs(B, H, Hkv, L);
+  const int G = H / Hkv;
   const bool fp4 = (mode_flags & 0xF) == SA_MODE_NVFP4;
+  const std::vector<Chunk> plan = chunk_plan(B, H, Hkv, L, chunk_pairs, fp4);
   const size_t osz = (mode_flags & SA_OUT_FP32) ? 4 : 2;
-  const SlotLayout lay = slot_layout(n, G, L, d, fp4, osz);
-  if (workspace_bytes < 2 * lay.bytes) return SA_ERR_INVALID_ARG;
+  const PipeLayout lay = pipe_layout(plan, G, L, d, fp4, osz);
+  if (workspace_bytes < lay.bytes) return SA_ERR_INVALID_ARG;
   HostPipe* p = pipe_for_current_device();
   if (!p) return SA_ERR_CUDA;
 
@@ -156,6 +241,7 @@ sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,
   const uint8_t* hv = static_cast<const uint8_t*>(v);
   uint8_t* ho = static_cast<uint8_t*>(o);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* split_ws = ws + lay.split;
   bool ok = true;
   auto cu = [&ok](cudaError_t e) { ok = ok && e == cudaSuccess; };
 
@@ -164,39 +250,47 @@ sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,
   cu(cudaEventRecord(p->start, s));
   cu(cudaStreamWaitEvent(p->cin, p->start, 0));
   cu(cudaStreamWaitEvent(p->cout, p->start, 0));
-  const int nchunks = (pairs + n - 1) / n;
+  const int nchunks = (int)plan.size();
+  size_t p0 = 0;
   for (int c = 0; ok && c < nchunks; ++c) {
-    const int slot = c & 1, p0 = c * n, nc = (pairs - p0) < n ? (pairs - p0) : n;
-    uint8_t* base = ws + slot * lay.bytes;
-    uint8_t *dq = base + lay.q, *dk = base + lay.k, *dv = base + lay.v, *dout = base + lay.o;
-    // copy in, once chunk c-2 is done reading this slot
-    if (c >= 2) cu(cudaStreamWaitEvent(p->cin, p->comp[slot], 0));
+    const int slot = c % kSlots, nc = plan[c].n, nsplit = plan[c].nsplit;
+    uint8_t* base = ws + slot * lay.slot.bytes;
+    uint8_t *dq = base + lay.slot.q, *dk = base + lay.slot.k, *dv = base + lay.slot.v, *dout = base + lay.slot.o;
+    // copy in, once chunk c-3 is done reading this slot
+    if (c >= kSlots) cu(cudaStreamWaitEvent(p->cin, p->comp[slot], 0));
     cu(cudaMemcpyAsync(dq, hq + p0 * q_pair, nc * q_pair, cudaMemcpyHostToDevice, p->cin));
     cu(cudaMemcpyAsync(dk, hk + p0 * kv_pair, nc * kv_pair, cudaMemcpyHostToDevice, p->cin));
     cu(cudaMemcpyAsync(dv, hv + p0 * kv_pair, nc * kv_pair, cudaMemcpyHostToDevice, p->cin));
     cu(cudaEventRecord(p->in[slot], p->cin));
-    // compute, once the inputs are in and chunk c-2's O has left the slot
+    // compute, once the inputs are in and chunk c-3's O has left the slot
     cu(cudaStreamWaitEvent(s, p->in[slot], 0));
-    if (c >= 2) cu(cudaStreamWaitEvent(s, p->out[slot], 0));
+    if (c >= kSlots) cu(cudaStreamWaitEvent(s, p->out[slot], 0));
     if (!ok) break;
+    const void* aq = dq;
+    const void* ak = dk;
+    const void* av = dv;
+    sa_fp4_qkv x;
     if (fp4) {
-      sa_fp4_qkv x;
-      st = sa_fp4_qkv_from_blob(base + lay.blob, 1, nc * G, nc, L, d, &x);
+      st = sa_fp4_qkv_from_blob(base + lay.slot.blob, 1, nc * G, nc, L, d, &x);
       if (st == SA_OK) st = sa_quantize(dq, dk, dv, 1, nc * G, nc, L, d, &x, stream);
-      if (st == SA_OK) st = sa_attn_fwd(&x, nullptr, nullptr, dout, 1, nc * G, nc, L, d, causal, mode_flags, stream);
-    } else {
-      st = sa_attn_fwd(dq, dk, dv, dout, 1, nc * G, nc, L, d, causal, mode_flags, stream);
+      aq = &x;
+      ak = av = nullptr;
     }
+    if (st == SA_OK)
+      st = nsplit > 1 ? sa_attn_fwd_ws(aq, ak, av, dout, 1, nc * G, nc, L, d, causal, mode_flags, nsplit, split_ws,
+                                       lay.split_bytes, stream)
+                      : sa_attn_fwd(aq, ak, av, dout, 1, nc * G, nc, L, d, causal, mode_flags, stream);
     if (st != SA_OK) return st;
     cu(cudaEventRecord(p->comp[slot], s));
     // copy out
     cu(cudaStreamWaitEvent(p->cout, p->comp[slot], 0));
     cu(cudaMemcpyAsync(ho + p0 * o_pair, dout, nc * o_pair, cudaMemcpyDeviceToHost, p->cout));
     cu(cudaEventRecord(p->out[slot], p->cout));
+    p0 += nc;
   }
   // the caller's stream completes after the last copy out (the copy-out
   // stream is in order, so its last event covers every chunk)
-  const int last = (nchunks - 1) & 1;
+  const int last = (nchunks - 1) % kSlots;
   cu(cudaStreamWaitEvent(s, p->out[last], 0));
   return ok ? SA_OK : SA_ERR_CUDA;
 }

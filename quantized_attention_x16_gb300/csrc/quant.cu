@@ -77,10 +77,10 @@ __device__ __forceinline__ uint32_t quant_group16(const float* x, uint32_t* code
 
 // ---------------------------------------------------------------------------
 // Two launches, 256 threads per CTA.
-//   1. quant_v_mean_kernel -- clusters of kMeanCluster CTAs, of two kinds
-//        spread evenly over the grid (the latency-bound mean clusters run
-//        beside the bandwidth-bound V CTAs):
-//        mean clusters: one per (b, kv head).  CTA r sums its share of the
+//   1. quant_v_mean_kernel -- clusters of kMeanCluster CTAs, of two kinds:
+//        mean clusters (first in the grid, so that the latency-bound sums
+//                    start at once and run beside the bandwidth-bound V CTAs):
+//                    one per (b, kv head).  CTA r sums its share of the
 //                    head's 128-token chunks, one thread per channel pair and
 //                    chunk, token by token from 0 (the documented order), into
 //                    the scratch buffer.  After a cluster barrier
@@ -93,8 +93,11 @@ __device__ __forceinline__ uint32_t quant_group16(const float* x, uint32_t* code
 //                    stored transposed.
 //   2. quant_qk_kernel -- persistent CTAs over tiles of 256 "quads" (a quad =
 //        64 consecutive channels of one row = four 1x16 groups = one 32-bit
-//        word of scale bytes) of one head: K tiles first (launch 1 has just
-//        read K, so it comes from L2), then Q tiles.  Tiles arrive by TMA in
+//        word of scale bytes) of one head: Q tiles first, then K tiles.  It is
+//        a programmatic dependent launch: its CTAs start while launch 1 drains
+//        and quantise Q, which launch 1 does not touch; before its first K
+//        tile each CTA waits for launch 1 to complete (mu), and K comes from
+//        L2, where launch 1 has just read it.  Tiles arrive by TMA in
 //        128B-swizzled shared memory (boxes of 64 channels x 128 tokens of one
 //        head; tokens past L arrive as zeros) through a two-stage ring; each
 //        thread reads its quad with conflict-free 16-byte loads, subtracts mu
@@ -166,10 +169,10 @@ __device__ __forceinline__ void quant_quad(const uint4 (&w)[8], const float* mea
   *reinterpret_cast<uint32_t*>(sf_base + blk * 512 + (r % 32) * 16 + (r / 32) * 4) = sfw;
 }
 
-// Head and first token of Q/K tile `tile` (tiles [0, ntile_k) are K, then Q).
+// Head and first token of Q/K tile `tile` (tiles [0, ntile_q) are Q, then K).
 __device__ __forceinline__ void tile_head(const QuantArgs& a, int tile, int rows, bool& is_k, int& bh, int& t0) {
-  is_k = tile < a.ntile_k;
-  const int u = is_k ? tile : tile - a.ntile_k;
+  is_k = tile >= a.ntile_q;
+  const int u = is_k ? tile - a.ntile_q : tile;
   const int tph = is_k ? a.tph_k : a.tph_q;
   bh = u / tph;
   t0 = (u % tph) * rows;
@@ -322,18 +325,19 @@ __device__ __forceinline__ void mean_cluster(const QuantArgs& a, int bh) {
   }
 }
 
-// Mean clusters sit near positions i * total / nclu_mean, so they run beside
-// the V clusters throughout the launch.
+// Clusters [0, nclu_mean) compute the means, the rest quantise V.  Every CTA
+// lets the dependent quant_qk_kernel launch at once (it waits for this
+// launch's completion before it reads mu).
 template <int D>
 __global__ void __cluster_dims__(kMeanCluster, 1, 1) __launch_bounds__(kThreadsQ)
     quant_v_mean_kernel(const QuantArgs a) {
-  const long long clu = blockIdx.x / kMeanCluster, total = (long long)a.nclu_mean + a.nclu_v;
-  const long long m_before = clu * a.nclu_mean / total, m_through = (clu + 1) * a.nclu_mean / total;
-  if (m_through > m_before) {
-    mean_cluster<D>(a, (int)m_before);
+  pdl_launch_dependents();
+  const int clu = blockIdx.x / kMeanCluster;
+  if (clu < a.nclu_mean) {
+    mean_cluster<D>(a, clu);
     return;
   }
-  const int blk = (int)(clu - m_before) * kMeanCluster + (int)(blockIdx.x % kMeanCluster);
+  const int blk = (clu - a.nclu_mean) * kMeanCluster + (int)(blockIdx.x % kMeanCluster);
   if (blk < a.nblk_v) quant_v_cta<D>(a, blk);
 }
 
@@ -341,7 +345,7 @@ __global__ void __cluster_dims__(kMeanCluster, 1, 1) __launch_bounds__(kThreadsQ
 // a two-stage TMA ring, the next tile's copy in flight while the current one
 // is quantised.
 template <int D>
-__global__ void __launch_bounds__(kThreadsQ) quant_qk_kernel(const __grid_constant__ CUtensorMap tmap_q,
+__global__ void __launch_bounds__(kThreadsQ, 3) quant_qk_kernel(const __grid_constant__ CUtensorMap tmap_q,
                                                              const __grid_constant__ CUtensorMap tmap_k,
                                                              const QuantArgs a) {
   using T = TileQK<D>;
@@ -370,13 +374,17 @@ __global__ void __launch_bounds__(kThreadsQ) quant_qk_kernel(const __grid_consta
       issued[1] = 1;
     }
   }
-  bool ok = true;
+  bool ok = true, waited = false;
   int i = 0;
   for (; tile < ntiles; ++i, tile += G) {
     const int st = i & 1;
     if (!mbar_wait(&full[st], (i >> 1) & 1, &abort_flag, a.wait_ns)) {
       ok = false;
       break;
+    }
+    if (!waited && tile >= a.ntile_q) {
+      pdl_wait();                                       // mu is written by launch 1
+      waited = true;
     }
     quant_tile_smem<D>(a, tile, smem + st * T::kSmemBytes);
     __syncthreads();                                    // stage st has been read by every thread
@@ -393,6 +401,9 @@ __global__ void __launch_bounds__(kThreadsQ) quant_qk_kernel(const __grid_consta
       if (issued[st] > consumed) mbar_wait_drain(&full[st], (issued[st] - 1) & 1, a.wait_ns);
     }
   }
+  // this launch completes only after launch 1 has: what follows in the stream
+  // may then read every output of sa_quantize
+  if (!waited) pdl_wait();
 }
 
 template <int D>
@@ -443,8 +454,20 @@ cudaError_t launch_quantize_impl(const void* q, const void* k, const void* v, co
   const int sms = device_sm_count() > 0 ? device_sm_count() : 148;
   const int grid = ntiles < 3 * sms ? ntiles : 3 * sms;    // three resident CTAs per SM
   quant_v_mean_kernel<D><<<(a.nclu_mean + a.nclu_v) * kMeanCluster, kThreadsQ, 0, s>>>(a);
-  quant_qk_kernel<D><<<grid, kThreadsQ, kSmem, s>>>(tq, tk, a);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // launch 2 may start while launch 1 drains (programmatic dependent launch)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreadsQ);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, quant_qk_kernel<D>, tq, tk, a);
 }
 
 }  // namespace

@@ -143,6 +143,16 @@ __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start once every CTA of the kernel before it in the
+// stream has called pdl_launch_dependents (or exited); it must call pdl_wait
+// before it reads anything that kernel writes (the wait returns when that
+// kernel has completed and its memory operations are visible).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Makes this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA, tensor core) before a synchronising arrive.
 __device__ __forceinline__ void fence_proxy_async_smem() {

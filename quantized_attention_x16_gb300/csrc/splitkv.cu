@@ -12,10 +12,15 @@
 // The P quantisation is per key tile, and shares are whole key tiles, so the
 // split changes only the float32 summation order.
 //
-// One warp per row; lane i holds columns i, i + 32, ... (coalesced 128-byte
-// rows).  Memory-bound and small: it reads nsplit * d + 2 floats per row.
+// Eight lanes per row, four rows per warp; lane i of a row holds d/8
+// consecutive columns.  Small: it reads nsplit * d + 2 floats per row, from
+// L2 as a rule, so its cost is load latency and the per-row scalar work (the
+// weights 2^(m_s - M) and 1 / l); the loads of two partial rows are issued
+// together and the scalar work is shared by eight lanes instead of 32.
 
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "internal.h"
 #include "work.cuh"
@@ -23,45 +28,128 @@
 namespace sa {
 namespace {
 
-constexpr int kRowsPerCta = 8;
+constexpr int kLanesPerRow = 8;                       // lanes sharing one output row
+constexpr int kRowsPerCta = 256 / kLanesPerRow;          // 256 threads, 32 rows
+constexpr int kSegBatch = 2;                             // partial rows whose loads are issued together
 
-template <int D, bool OUT32>
-__global__ void __launch_bounds__(32 * kRowsPerCta) splitkv_combine_kernel(const SplitOut part, int nsplit,
-                                                                         long long nrows, int L, int Lp,
-                                                                         long long split_rows, int H,
-                                                                         const Strides so, void* out) {
-  const long long row = (long long)blockIdx.x * kRowsPerCta + threadIdx.x / 32;
-  if (row >= nrows) return;
-  const int lane = threadIdx.x % 32;
-  const long long bh = row / L;
-  const long long prow = bh * Lp + row % L;          // row in the padded partial layout
-  float mmax = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) {
-    const float2 ml = *reinterpret_cast<const float2*>(part.ml + 2 * (s * split_rows + prow));
-    if (ml.y > 0.f) mmax = fmaxf(mmax, ml.x);
-  }
-  float acc[D / 32];
+// Merges the nseg partial rows seg(0), seg(1), ... of one output row; called
+// by the kLanesPerRow lanes of the row, lane i of them holding columns
+// [i*V, i*V + V), V = D / kLanesPerRow.  The loads of kSegBatch segments
+// (their (m, l) and their O rows) are issued before any is used, so a row
+// costs one memory round trip in the usual case of two segments; the
+// arithmetic is the same in every case: M first, then the weighted sums in
+// segment order.
+template <int D, typename SegRow>
+__device__ __forceinline__ void merge_partials(const SplitOut& part, int nseg, SegRow seg,
+                                               float (&out)[D / kLanesPerRow]) {
+  constexpr int V = D / kLanesPerRow, V4 = V / 4;
+  const int sub = threadIdx.x % kLanesPerRow;
+  float mmax = -INFINITY, lsum = 0.f;
+  float acc[V];
 #pragma unroll
-  for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
-  float lsum = 0.f;
-  for (int s = 0; s < nsplit; ++s) {
-    const float2 ml = *reinterpret_cast<const float2*>(part.ml + 2 * (s * split_rows + prow));
-    if (!(ml.y > 0.f)) continue;                     // an empty share (its a_s is never read)
+  for (int c = 0; c < V; ++c) acc[c] = 0.f;
+  auto load = [&](int k, float2& ml, float4 (&a)[V4]) {
+    const long long r = seg(k);
+    ml = *reinterpret_cast<const float2*>(part.ml + 2 * r);
+    const float4* src = reinterpret_cast<const float4*>(part.o + r * D + sub * V);
+#pragma unroll
+    for (int j = 0; j < V4; ++j) a[j] = src[j];
+  };
+  auto accumulate = [&](const float2& ml, const float4 (&a)[V4]) {
+    if (!(ml.y > 0.f)) return;                          // an empty segment (its O row is not read)
     const float w = exp2f(ml.x - mmax);
     lsum = fmaf(w, ml.y, lsum);
-    const float* a = part.o + (s * split_rows + prow) * D;
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) acc[i] = fmaf(w, a[lane + 32 * i], acc[i]);
+    for (int j = 0; j < V4; ++j) {
+      acc[4 * j + 0] = fmaf(w, a[j].x, acc[4 * j + 0]);
+      acc[4 * j + 1] = fmaf(w, a[j].y, acc[4 * j + 1]);
+      acc[4 * j + 2] = fmaf(w, a[j].z, acc[4 * j + 2]);
+      acc[4 * j + 3] = fmaf(w, a[j].w, acc[4 * j + 3]);
+    }
+  };
+  if (nseg <= kSegBatch) {
+    float2 ml[kSegBatch];
+    float4 a[kSegBatch][V4];
+#pragma unroll
+    for (int i = 0; i < kSegBatch; ++i) {
+      if (i < nseg)
+        load(i, ml[i], a[i]);
+      else
+        ml[i] = make_float2(-INFINITY, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < kSegBatch; ++i)
+      if (ml[i].y > 0.f) mmax = fmaxf(mmax, ml[i].x);
+#pragma unroll
+    for (int i = 0; i < kSegBatch; ++i) accumulate(ml[i], a[i]);
+  } else {
+    for (int k0 = 0; k0 < nseg; k0 += kSegBatch) {
+      float2 ml[kSegBatch];
+#pragma unroll
+      for (int i = 0; i < kSegBatch; ++i)
+        ml[i] = k0 + i < nseg ? *reinterpret_cast<const float2*>(part.ml + 2 * seg(k0 + i))
+                              : make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int i = 0; i < kSegBatch; ++i)
+        if (ml[i].y > 0.f) mmax = fmaxf(mmax, ml[i].x);
+    }
+    for (int k0 = 0; k0 < nseg; k0 += kSegBatch) {
+      float2 ml[kSegBatch];
+      float4 a[kSegBatch][V4];
+#pragma unroll
+      for (int i = 0; i < kSegBatch; ++i) {
+        if (k0 + i < nseg)
+          load(k0 + i, ml[i], a[i]);
+        else
+          ml[i] = make_float2(-INFINITY, 0.f);
+      }
+#pragma unroll
+      for (int i = 0; i < kSegBatch; ++i) accumulate(ml[i], a[i]);
+    }
   }
   const float inv = 1.f / lsum;
 #pragma unroll
-  for (int i = 0; i < D / 32; ++i) {
-    const long long idx = (bh / H) * so.b + (bh % H) * so.h + (row % L) * so.t + lane + 32 * i;
-    if constexpr (OUT32)
-      static_cast<float*>(out)[idx] = acc[i] * inv;
-    else
-      static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(acc[i] * inv);
+  for (int c = 0; c < V; ++c) out[c] = acc[c] * inv;
+}
+
+// Stores a lane's V = D / kLanesPerRow consecutive output columns (rows are
+// 16-byte aligned).
+template <int D, bool OUT32>
+__device__ __forceinline__ void store_row_part(void* out, long long idx, const float (&v)[D / kLanesPerRow]) {
+  constexpr int V = D / kLanesPerRow;
+  if constexpr (OUT32) {
+    float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + idx);
+#pragma unroll
+    for (int j = 0; j < V / 4; ++j) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  } else {
+    uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + idx);
+#pragma unroll
+    for (int j = 0; j < V / 8; ++j) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      o[j] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
   }
+}
+
+template <int D, bool OUT32>
+__global__ void __launch_bounds__(kRowsPerCta * kLanesPerRow) splitkv_combine_kernel(const SplitOut part, int nsplit,
+                                                                         long long nrows, int L, int Lp,
+                                                                         long long split_rows, int H,
+                                                                         const Strides so, void* out) {
+  const long long row = (long long)blockIdx.x * kRowsPerCta + threadIdx.x / kLanesPerRow;
+  if (row >= nrows) return;
+  const int sub = threadIdx.x % kLanesPerRow;
+  const long long bh = row / L;
+  const long long prow = bh * Lp + row % L;          // row in the padded partial layout
+  float v[D / kLanesPerRow];
+  merge_partials<D>(part, nsplit, [&](int s) { return s * split_rows + prow; }, v);
+  store_row_part<D, OUT32>(out, (bh / H) * so.b + (bh % H) * so.h + (row % L) * so.t + sub * (D / kLanesPerRow),
+                           v);
 }
 
 template <int D, bool OUT32>
@@ -70,54 +158,32 @@ cudaError_t launch(const SplitOut& part, int nsplit, const Dims& dm, void* o, co
   const int Lp = padded_len(dm.Lq);
   const long long split_rows = (long long)dm.B * dm.H * Lp;
   const long long ctas = (nrows + kRowsPerCta - 1) / kRowsPerCta;
-  splitkv_combine_kernel<D, OUT32><<<(unsigned)ctas, 32 * kRowsPerCta, 0, s>>>(part, nsplit, nrows, dm.Lq, Lp,
+  splitkv_combine_kernel<D, OUT32><<<(unsigned)ctas, kRowsPerCta * kLanesPerRow, 0, s>>>(part, nsplit, nrows, dm.Lq, Lp,
                                                                               split_rows, dm.H, so, o);
   return cudaGetLastError();
 }
 
-// Stream-K: CTAs (k, y) for cut pair k and y in 0..31, eight rows each (one
-// per warp), so the latency-bound row merges run spread over the GPU.  A cut
+// Stream-K: CTAs (k, y) for cut pair k and y in 0..7, 32 rows each, so the
+// latency-bound row merges run spread over the GPU.  A cut
 // pair's segments -- one per CTA whose range meets it -- are merged into O;
 // pairs no boundary cuts were written whole by the attention kernel.
 template <int D, bool OUT32>
-__global__ void __launch_bounds__(32 * kRowsPerCta) streamk_combine_kernel(const __grid_constant__ StreamKCuts cuts,
+__global__ void __launch_bounds__(kRowsPerCta * kLanesPerRow) streamk_combine_kernel(const __grid_constant__ StreamKCuts cuts,
                                                                          const SplitOut part, int L, int H,
                                                                          const Strides so, void* out) {
   const int* e = cuts.e[blockIdx.x];
   const int bh = e[0], qt0 = e[1], nq = e[2], cta0 = e[3], nseg = e[4] - e[3] + 1, first_last = e[5];
-  const int rr = blockIdx.y * kRowsPerCta + threadIdx.x / 32;   // row of the pair (query tile rr / 128)
+  const int rr = blockIdx.y * kRowsPerCta + threadIdx.x / kLanesPerRow;   // row of the pair (query tile rr / 128)
   const int t = qt0 * 128 + rr;                                  // its token
   if (rr >= nq * 128 || t >= L) return;
-  const int lane = threadIdx.x % 32;
-  float mmax = -INFINITY;
-  for (int k = 0; k < nseg; ++k) {
-    const long long prow = (long long)(2 * (cta0 + k) + (k == 0 ? first_last : 0)) * 256 + rr;
-    const float2 ml = *reinterpret_cast<const float2*>(part.ml + 2 * prow);
-    if (ml.y > 0.f) mmax = fmaxf(mmax, ml.x);
-  }
-  float acc[D / 32];
-#pragma unroll
-  for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
-  float lsum = 0.f;
-  for (int k = 0; k < nseg; ++k) {
-    const long long prow = (long long)(2 * (cta0 + k) + (k == 0 ? first_last : 0)) * 256 + rr;
-    const float2 ml = *reinterpret_cast<const float2*>(part.ml + 2 * prow);
-    if (!(ml.y > 0.f)) continue;                     // a segment without keys for this row
-    const float wgt = exp2f(ml.x - mmax);
-    lsum = fmaf(wgt, ml.y, lsum);
-    const float* a = part.o + prow * D;
-#pragma unroll
-    for (int i = 0; i < D / 32; ++i) acc[i] = fmaf(wgt, a[lane + 32 * i], acc[i]);
-  }
-  const float inv = 1.f / lsum;
-#pragma unroll
-  for (int i = 0; i < D / 32; ++i) {
-    const long long idx = (long long)(bh / H) * so.b + (long long)(bh % H) * so.h + (long long)t * so.t + lane + 32 * i;
-    if constexpr (OUT32)
-      static_cast<float*>(out)[idx] = acc[i] * inv;
-    else
-      static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(acc[i] * inv);
-  }
+  const int sub = threadIdx.x % kLanesPerRow;
+  float v[D / kLanesPerRow];
+  merge_partials<D>(
+      part, nseg, [&](int k) { return (long long)(2 * (cta0 + k) + (k == 0 ? first_last : 0)) * 256 + rr; }, v);
+  store_row_part<D, OUT32>(out,
+                           (long long)(bh / H) * so.b + (long long)(bh % H) * so.h + (long long)t * so.t +
+                               sub * (D / kLanesPerRow),
+                           v);
 }
 
 template <int D, bool OUT32>
@@ -126,7 +192,7 @@ cudaError_t launch_sk(const AttnWork& w, int ctas, const SplitOut& part, const D
   StreamKCuts cuts;
   make_streamk_cuts(w, ctas, &cuts);
   if (cuts.n == 0) return cudaSuccess;               // no pair was cut
-  streamk_combine_kernel<D, OUT32><<<dim3(cuts.n, 256 / kRowsPerCta), 32 * kRowsPerCta, 0, s>>>(cuts, part, dm.Lq,
+  streamk_combine_kernel<D, OUT32><<<dim3(cuts.n, 256 / kRowsPerCta), kRowsPerCta * kLanesPerRow, 0, s>>>(cuts, part, dm.Lq,
                                                                                                 dm.H, so, o);
   return cudaGetLastError();
 }
