@@ -102,5 +102,6 @@ inline SplitOut streamk_layout(void* ws, const Dims& dm, int ctas) {
 // Per-unit readers of the device error word (each clears its word).
 cudaError_t attn_bf16_read_error(int* out);
 cudaError_t attn_nvfp4_read_error(int* out);
+cudaError_t quant_read_error(int* out);
 
 }  // namespace sa

@@ -472,6 +472,8 @@ cudaError_t launch_quantize_impl(const void* q, const void* k, const void* v, co
 
 }  // namespace
 
+cudaError_t quant_read_error(int* out) { return read_and_clear_device_error(out); }
+
 cudaError_t launch_quantize(const void* q, const void* k, const void* v, const Dims& dm, bool blhd,
                             const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t s) {
   float* part = static_cast<float*>(out.workspace);

@@ -365,12 +365,12 @@ sa_status sa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, i
 }
 
 sa_status sa_last_device_error(void) {
-  int e1 = 0, e2 = 0, e3 = 0;
+  int e1 = 0, e2 = 0, e3 = 0, e4 = 0;
   if (cudaDeviceSynchronize() != cudaSuccess) return SA_ERR_CUDA;
   if (attn_bf16_read_error(&e1) != cudaSuccess || attn_nvfp4_read_error(&e2) != cudaSuccess ||
-      read_and_clear_device_error(&e3) != cudaSuccess)
+      quant_read_error(&e4) != cudaSuccess || read_and_clear_device_error(&e3) != cudaSuccess)
     return SA_ERR_CUDA;
-  const int e = e1 ? e1 : (e2 ? e2 : e3);
+  const int e = e1 ? e1 : (e2 ? e2 : (e4 ? e4 : e3));
   return e ? static_cast<sa_status>(e) : SA_OK;
 }
 
