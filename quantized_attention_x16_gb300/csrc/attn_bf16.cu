@@ -420,6 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // every output of this CTA is stored: a combine launch queued behind this
+  // one (programmatic dependent launch) may be scheduled
+  pdl_launch_dependents();
   if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);

@@ -23,6 +23,7 @@
 #include <type_traits>
 
 #include "internal.h"
+#include "sm100.cuh"
 #include "work.cuh"
 
 namespace sa {
@@ -31,6 +32,26 @@ namespace {
 constexpr int kLanesPerRow = 8;                       // lanes sharing one output row
 constexpr int kRowsPerCta = 256 / kLanesPerRow;          // 256 threads, 32 rows
 constexpr int kSegBatch = 2;                             // partial rows whose loads are issued together
+
+// Launch configuration of a combine kernel: a programmatic dependent launch
+// behind the attention kernel, so that its launch is processed while the
+// attention CTAs finish; the kernel waits (pdl_wait) before it reads.
+cudaLaunchAttribute g_pdl_attr = [] {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}();
+cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, cudaStream_t s) {
+  cudaLaunchConfig_t c = {};
+  c.gridDim = grid;
+  c.blockDim = block;
+  c.dynamicSmemBytes = 0;
+  c.stream = s;
+  c.attrs = &g_pdl_attr;
+  c.numAttrs = 1;
+  return c;
+}
 
 // Merges the nseg partial rows seg(0), seg(1), ... of one output row; called
 // by the kLanesPerRow lanes of the row, lane i of them holding columns
@@ -141,6 +162,7 @@ __global__ void __launch_bounds__(kRowsPerCta * kLanesPerRow) splitkv_combine_ke
                                                                          long long nrows, int L, int Lp,
                                                                          long long split_rows, int H,
                                                                          const Strides so, void* out) {
+  pdl_wait();                                        // the partial results are written
   const long long row = (long long)blockIdx.x * kRowsPerCta + threadIdx.x / kLanesPerRow;
   if (row >= nrows) return;
   const int sub = threadIdx.x % kLanesPerRow;
@@ -158,9 +180,9 @@ cudaError_t launch(const SplitOut& part, int nsplit, const Dims& dm, void* o, co
   const int Lp = padded_len(dm.Lq);
   const long long split_rows = (long long)dm.B * dm.H * Lp;
   const long long ctas = (nrows + kRowsPerCta - 1) / kRowsPerCta;
-  splitkv_combine_kernel<D, OUT32><<<(unsigned)ctas, kRowsPerCta * kLanesPerRow, 0, s>>>(part, nsplit, nrows, dm.Lq, Lp,
-                                                                              split_rows, dm.H, so, o);
-  return cudaGetLastError();
+  const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)ctas), dim3(kRowsPerCta * kLanesPerRow), s);
+  return cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<D, OUT32>, part, nsplit, nrows, dm.Lq, Lp, split_rows, dm.H,
+                            so, o);
 }
 
 // Stream-K: CTAs (k, y) for cut pair k and y in 0..7, 32 rows each, so the
@@ -171,6 +193,7 @@ template <int D, bool OUT32>
 __global__ void __launch_bounds__(kRowsPerCta * kLanesPerRow) streamk_combine_kernel(const __grid_constant__ StreamKCuts cuts,
                                                                          const SplitOut part, int L, int H,
                                                                          const Strides so, void* out) {
+  pdl_wait();                                        // the partial results are written
   const int* e = cuts.e[blockIdx.x];
   const int bh = e[0], qt0 = e[1], nq = e[2], cta0 = e[3], nseg = e[4] - e[3] + 1, first_last = e[5];
   const int rr = blockIdx.y * kRowsPerCta + threadIdx.x / kLanesPerRow;   // row of the pair (query tile rr / 128)
@@ -192,9 +215,8 @@ cudaError_t launch_sk(const AttnWork& w, int ctas, const SplitOut& part, const D
   StreamKCuts cuts;
   make_streamk_cuts(w, ctas, &cuts);
   if (cuts.n == 0) return cudaSuccess;               // no pair was cut
-  streamk_combine_kernel<D, OUT32><<<dim3(cuts.n, 256 / kRowsPerCta), kRowsPerCta * kLanesPerRow, 0, s>>>(cuts, part, dm.Lq,
-                                                                                                dm.H, so, o);
-  return cudaGetLastError();
+  const cudaLaunchConfig_t cfg = pdl_config(dim3(cuts.n, 256 / kRowsPerCta), dim3(kRowsPerCta * kLanesPerRow), s);
+  return cudaLaunchKernelEx(&cfg, streamk_combine_kernel<D, OUT32>, cuts, part, dm.Lq, dm.H, so, o);
 }
 
 }  // namespace
