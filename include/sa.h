@@ -71,6 +71,18 @@ typedef enum { SA_MODE_BF16 = 0, SA_MODE_NVFP4 = 1 } sa_mode;
  * sa_quantize_static_scratch. */
 #define SA_LAYOUT_BLHD 32
 
+/* Scheduling flag of sa_attn_fwd_host, OR-ed into `mode`: the host inputs q,
+ * k, v already hold their final values when the call is made (no work
+ * enqueued on `stream` before the call writes them), so the call's
+ * host -> device copies may start before that work completes; each waits only
+ * until the previous sa_attn_fwd_host call on this device has finished
+ * computing on the workspace slot it refills (and its compute until that
+ * call's copy-out from the slot is done).  Back-to-back calls on one
+ * workspace then overlap one call's first copy-ins with the previous call's
+ * last compute and copy-out.  Results are unchanged.  Accepted by
+ * sa_attn_fwd_host (and its workspace-size query) only. */
+#define SA_HOST_OVERLAP 64
+
 /*
  * Quantised operands produced by sa_quantize (device pointers, caller-owned).
  * Every layout holds Lp = L rounded up to a multiple of 128 tokens per head;

@@ -28,6 +28,7 @@ SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA, SA_ERR_TIMEOUT = ran
 SA_MODE_BF16, SA_MODE_NVFP4 = 0, 1
 SA_OUT_FP32 = 16
 SA_LAYOUT_BLHD = 32
+SA_HOST_OVERLAP = 64
 
 #: every symbol include/sa.h declares
 EXPORTS = ("sa_fp4_qkv_bytes", "sa_fp4_qkv_from_blob", "sa_quantize", "sa_quantize_ex", "sa_quantize_static_scratch",
@@ -304,12 +305,14 @@ def sa_attn_fwd_host_workspace_bytes(B, H, Hkv, L, d, mode="nvfp4", out_dtype=No
 
 
 def sa_attn_fwd_host(q, k, v, o=None, causal=False, mode="nvfp4", out_dtype=None, workspace=None, chunk_pairs=0,
-                     stream=None):
+                     stream=None, overlap=False):
     """The path of sa_attn_fwd on pinned host tensors (see sa.h): q, k, v bf16
     BHLD pinned CPU tensors; o (allocated pinned if None) receives the output
     once ``stream`` has finished.  workspace: a uint8 CUDA tensor of at least
     sa_attn_fwd_host_workspace_bytes(...) bytes (allocated on the current
-    device if None).  Returns o."""
+    device if None).  overlap: SA_HOST_OVERLAP (q, k, v are final when the
+    call is made, so its copies may overlap the previous call's tail).
+    Returns o."""
     import torch
     _bf16_pinned(q, "q"), _bf16_pinned(k, "k"), _bf16_pinned(v, "v")
     B, H, L, d = q.shape
@@ -331,8 +334,9 @@ def sa_attn_fwd_host(q, k, v, o=None, causal=False, mode="nvfp4", out_dtype=None
         workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
     if not (workspace.is_cuda and workspace.dtype == torch.uint8 and workspace.is_contiguous()):
         raise ValueError("workspace must be a contiguous uint8 CUDA tensor")
-    _check(lib.sa_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Hkv, L, d, int(bool(causal)), m,
-                                _ptr(workspace), workspace.numel(), int(chunk_pairs), _stream(stream)),
+    _check(lib.sa_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Hkv, L, d, int(bool(causal)),
+                                m | (SA_HOST_OVERLAP if overlap else 0), _ptr(workspace), workspace.numel(),
+                                int(chunk_pairs), _stream(stream)),
            "sa_attn_fwd_host")
     return o
 

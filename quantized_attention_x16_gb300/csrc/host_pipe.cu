@@ -192,7 +192,7 @@ bool pinned_host(const void* p) {
 sa_status check_host_args(int B, int H, int Hkv, int L, int d, int causal, int mode_flags, int chunk_pairs) {
   if (B < 0 || H <= 0 || Hkv <= 0 || L < 0 || d <= 0 || H % Hkv != 0) return SA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
-  if (mode_flags & ~(0xF | SA_OUT_FP32)) return SA_ERR_INVALID_ARG;
+  if (mode_flags & ~(0xF | SA_OUT_FP32 | SA_HOST_OVERLAP)) return SA_ERR_INVALID_ARG;
   const int mode = mode_flags & 0xF;
   if (mode != SA_MODE_BF16 && mode != SA_MODE_NVFP4) return SA_ERR_INVALID_ARG;
   if (chunk_pairs < 0) return SA_ERR_INVALID_ARG;
@@ -245,10 +245,15 @@ sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,
   bool ok = true;
   auto cu = [&ok](cudaError_t e) { ok = ok && e == cudaSuccess; };
 
-  // both copy streams start after the work already on the caller's stream
-  // (an earlier call on the same workspace, for one)
+  // Both copy streams start after the work already on the caller's stream
+  // (an earlier call on the same workspace, for one) -- with SA_HOST_OVERLAP
+  // the copy-in stream does not: the first kSlots chunks wait instead for the
+  // slot events of the previous call on this device, like later chunks for
+  // those of this call (an event never recorded is no wait).
+  const bool overlap = (mode_flags & SA_HOST_OVERLAP) != 0;
+  const int dev_mode = mode_flags & ~SA_HOST_OVERLAP;   // the mode of the device-buffer calls
   cu(cudaEventRecord(p->start, s));
-  cu(cudaStreamWaitEvent(p->cin, p->start, 0));
+  if (!overlap) cu(cudaStreamWaitEvent(p->cin, p->start, 0));
   cu(cudaStreamWaitEvent(p->cout, p->start, 0));
   const int nchunks = (int)plan.size();
   size_t p0 = 0;
@@ -256,15 +261,16 @@ sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,
     const int slot = c % kSlots, nc = plan[c].n, nsplit = plan[c].nsplit;
     uint8_t* base = ws + slot * lay.slot.bytes;
     uint8_t *dq = base + lay.slot.q, *dk = base + lay.slot.k, *dv = base + lay.slot.v, *dout = base + lay.slot.o;
-    // copy in, once chunk c-3 is done reading this slot
-    if (c >= kSlots) cu(cudaStreamWaitEvent(p->cin, p->comp[slot], 0));
+    // copy in, once chunk c-3 (or the previous call's last chunk in this
+    // slot) is done reading this slot
+    if (c >= kSlots || overlap) cu(cudaStreamWaitEvent(p->cin, p->comp[slot], 0));
     cu(cudaMemcpyAsync(dq, hq + p0 * q_pair, nc * q_pair, cudaMemcpyHostToDevice, p->cin));
     cu(cudaMemcpyAsync(dk, hk + p0 * kv_pair, nc * kv_pair, cudaMemcpyHostToDevice, p->cin));
     cu(cudaMemcpyAsync(dv, hv + p0 * kv_pair, nc * kv_pair, cudaMemcpyHostToDevice, p->cin));
     cu(cudaEventRecord(p->in[slot], p->cin));
     // compute, once the inputs are in and chunk c-3's O has left the slot
     cu(cudaStreamWaitEvent(s, p->in[slot], 0));
-    if (c >= kSlots) cu(cudaStreamWaitEvent(s, p->out[slot], 0));
+    if (c >= kSlots || overlap) cu(cudaStreamWaitEvent(s, p->out[slot], 0));
     if (!ok) break;
     const void* aq = dq;
     const void* ak = dk;
@@ -277,9 +283,9 @@ sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,
       ak = av = nullptr;
     }
     if (st == SA_OK)
-      st = nsplit > 1 ? sa_attn_fwd_ws(aq, ak, av, dout, 1, nc * G, nc, L, d, causal, mode_flags, nsplit, split_ws,
+      st = nsplit > 1 ? sa_attn_fwd_ws(aq, ak, av, dout, 1, nc * G, nc, L, d, causal, dev_mode, nsplit, split_ws,
                                        lay.split_bytes, stream)
-                      : sa_attn_fwd(aq, ak, av, dout, 1, nc * G, nc, L, d, causal, mode_flags, stream);
+                      : sa_attn_fwd(aq, ak, av, dout, 1, nc * G, nc, L, d, causal, dev_mode, stream);
     if (st != SA_OK) return st;
     cu(cudaEventRecord(p->comp[slot], s));
     // copy out

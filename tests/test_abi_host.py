@@ -113,6 +113,10 @@ def test_argument_errors_launch_nothing(sa):
     assert need == 4 * (1 * 2 * 1024) * (64 + 2) * 4                       # partial O rows plus (m, l)
     assert lib.sa_attn_fwd_ws(p, p, p, p, 1, 2, 2, 1024, 64, 0, 0, 4, p, need - 16, None) == sa.SA_ERR_INVALID_ARG
     assert lib.sa_attn_fwd_workspace_bytes(1, 2, 2, 1024, 64, 0, 0, 1) == 0
+    # the host-overlap flag: sizes a host-path workspace, rejected by the device-buffer attention call
+    assert lib.sa_attn_fwd_host_workspace_bytes(1, 2, 2, 256, 64, 1 | sa.SA_HOST_OVERLAP, 0) == \
+        lib.sa_attn_fwd_host_workspace_bytes(1, 2, 2, 256, 64, 1, 0) > 0
+    assert lib.sa_attn_fwd(p, p, p, p, 1, 2, 2, 256, 64, 0, 1 | sa.SA_HOST_OVERLAP, None) == sa.SA_ERR_INVALID_ARG
     # the layout flag: accepted by the attention calls, not by the host-buffer path
     assert lib.sa_attn_fwd_host(p, p, p, p, 1, 2, 2, 256, 64, 0, 1 | sa.SA_LAYOUT_BLHD, p, 1 << 30, 0, None) == \
         sa.SA_ERR_INVALID_ARG

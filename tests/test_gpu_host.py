@@ -133,3 +133,28 @@ def test_host_path_rejects_bad_arguments(sa):
         sa.SA_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert sa.sa_last_device_error() == sa.SA_OK
+
+
+@pytest.mark.parametrize("mode", ["nvfp4", "bf16"])
+def test_host_path_overlapped_back_to_back_calls(sa, mode):
+    """SA_HOST_OVERLAP: calls queued back to back on one workspace, each on
+    other inputs, each copy-in free to start before the previous call ends;
+    every output must equal its own device-path result."""
+    ws_case = dict(W.spec("llm_prefill"), B=2, H=4, Hkv=2, L=1000)
+    xs = [W.make_inputs(dict(ws_case, seed=40 + i)) for i in range(4)]
+    refs = [device_path(sa, x, False, mode, torch.bfloat16) for x in xs]
+    need = sa.sa_attn_fwd_host_workspace_bytes(2, 4, 2, 1000, 128, mode)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    hs = [{n: x[n].pin_memory() for n in "qkv"} for x in xs]
+    outs = []
+    for _ in range(2):
+        for h in hs:
+            outs.append(sa.sa_attn_fwd_host(h["q"], h["k"], h["v"], mode=mode, workspace=ws, overlap=True))
+    torch.cuda.current_stream().synchronize()
+    assert sa.sa_last_device_error() == sa.SA_OK
+    for i, o in enumerate(outs):
+        ref = refs[i % len(refs)]
+        if mode == "bf16":
+            assert torch.equal(o.view(torch.int16), ref.view(torch.int16)), i
+        else:   # split-KV chunks of the library's chunking: float32 summation order only
+            assert (o.float() - ref.float()).abs().max().item() <= 2 ** -7 * ref.float().abs().max().item(), i
