@@ -93,11 +93,12 @@ __device__ __forceinline__ uint32_t quant_group16(const float* x, uint32_t* code
 //                    stored transposed.
 //   2. quant_qk_kernel -- persistent CTAs over tiles of 256 "quads" (a quad =
 //        64 consecutive channels of one row = four 1x16 groups = one 32-bit
-//        word of scale bytes) of one head: Q tiles first, then K tiles.  It is
-//        a programmatic dependent launch: its CTAs start while launch 1 drains
-//        and quantise Q, which launch 1 does not touch; before its first K
-//        tile each CTA waits for launch 1 to complete (mu), and K comes from
-//        L2, where launch 1 has just read it.  Tiles arrive by TMA in
+//        word of scale bytes) of one head: one round of Q tiles (one per CTA),
+//        then the K tiles, then the other Q tiles.  It is a programmatic
+//        dependent launch: its CTAs start while launch 1 drains and quantise
+//        Q, which launch 1 does not touch; before its first K tile each CTA
+//        waits for launch 1 to complete (mu), and K then comes from L2, where
+//        launch 1 has just read it.  Tiles arrive by TMA in
 //        128B-swizzled shared memory (boxes of 64 channels x 128 tokens of one
 //        head; tokens past L arrive as zeros) through a two-stage ring; each
 //        thread reads its quad with conflict-free 16-byte loads, subtracts mu
@@ -131,6 +132,7 @@ struct QuantArgs {
   Strides sq, skv;                  // element strides of the bf16 Q and K / V (BHLD or BLHD)
   int tph_q, tph_k;                 // Q / K tiles of kRows tokens per head
   int ntile_q, ntile_k, nblk_v;
+  int nq_first;                     // launch 2: Q tiles taken before the K tiles (the rest after)
   int nclu_mean, nclu_v;            // launch 1: mean clusters, V clusters
   uint64_t wait_ns;
 };
@@ -169,10 +171,15 @@ __device__ __forceinline__ void quant_quad(const uint4 (&w)[8], const float* mea
   *reinterpret_cast<uint32_t*>(sf_base + blk * 512 + (r % 32) * 16 + (r / 32) * 4) = sfw;
 }
 
-// Head and first token of Q/K tile `tile` (tiles [0, ntile_q) are Q, then K).
+// Whether tile `tile` of launch 2 is a K tile: tiles [0, nq_first) are Q
+// tiles, then come the K tiles, then the other Q tiles.
+__device__ __forceinline__ bool tile_is_k(const QuantArgs& a, int tile) {
+  return tile >= a.nq_first && tile < a.nq_first + a.ntile_k;
+}
+// Head and first token of Q/K tile `tile`.
 __device__ __forceinline__ void tile_head(const QuantArgs& a, int tile, int rows, bool& is_k, int& bh, int& t0) {
-  is_k = tile >= a.ntile_q;
-  const int u = is_k ? tile - a.ntile_q : tile;
+  is_k = tile_is_k(a, tile);
+  const int u = is_k ? tile - a.nq_first : (tile < a.nq_first ? tile : tile - a.ntile_k);
   const int tph = is_k ? a.tph_k : a.tph_q;
   bh = u / tph;
   t0 = (u % tph) * rows;
@@ -382,7 +389,7 @@ __global__ void __launch_bounds__(kThreadsQ, 3) quant_qk_kernel(const __grid_con
       ok = false;
       break;
     }
-    if (!waited && tile >= a.ntile_q) {
+    if (!waited && tile_is_k(a, tile)) {
       pdl_wait();                                       // mu is written by launch 1
       waited = true;
     }
@@ -453,6 +460,8 @@ cudaError_t launch_quantize_impl(const void* q, const void* k, const void* v, co
   const int ntiles = a.ntile_k + a.ntile_q;
   const int sms = device_sm_count() > 0 ? device_sm_count() : 148;
   const int grid = ntiles < 3 * sms ? ntiles : 3 * sms;    // three resident CTAs per SM
+  // one round of Q tiles runs beside launch 1; K follows while it is in L2
+  a.nq_first = a.ntile_q < grid ? a.ntile_q : grid;
   quant_v_mean_kernel<D><<<(a.nclu_mean + a.nclu_v) * kMeanCluster, kThreadsQ, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
