@@ -155,6 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmap_q);
         tma_prefetch_desc(&tmap_k);
         tma_prefetch_desc(&tmap_v);
+      }
+      pdl_wait();                                       // the inputs are written (programmatic launch)
+      if (leader) {
         mbar_arrive_expect_tx(bars.q_full, nq * C::kTileBytes);
         for (int q = 0; q < nq; ++q)
           for (int hh = 0; hh < D / 64; ++hh)
@@ -448,9 +451,12 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   }
   int ctas = 0;
   const AttnWork work = make_attn_work(dm.B, dm.H, dm.Lq, dm.Lkv, causal, device_sm_count(), &ctas, nsplit);
-  attn_bf16_kernel<D, OUT32><<<ctas, kThreads, C::kSmemBytes, s>>>(tq, tk, tv, o, dm.H, dm.Hkv, dm.Lq, dm.Lkv, causal,
-                                                                    work, part, so, kWaitLimitNs);
-  cudaError_t e = cudaGetLastError();
+  // a programmatic dependent launch: the CTAs' set-up overlaps the end of
+  // the kernel before; the producer waits for it before its first load
+  cudaLaunchAttribute attr;
+  const cudaLaunchConfig_t cfg = pdl_launch_config(dim3(ctas), dim3(kThreads), C::kSmemBytes, s, &attr);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_bf16_kernel<D, OUT32>, tq, tk, tv, o, dm.H, dm.Hkv, dm.Lq, dm.Lkv,
+                                     causal, work, part, so, kWaitLimitNs);
   if (e == cudaSuccess && work.nsplit > 1) e = launch_splitkv_combine(part, work.nsplit, dm, o, so, OUT32, s);
   return e;
 }

@@ -197,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmap_k);
         tma_prefetch_desc(&tmap_v);
       }
+      pdl_wait();                                       // the inputs are written (programmatic launch)
       // K and V tiles and Q units issued so far (over the whole list); the
       // counts also tell the abort path which copies may still be in flight
       int nk = 0, nv = 0, ug = 0;
@@ -652,10 +653,15 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   const AttnWork work = nsplit == kStreamK
                             ? make_streamk_work(dm.B, dm.H, dm.Lq, dm.Lkv, causal, device_sm_count(), &ctas)
                             : make_attn_work(dm.B, dm.H, dm.Lq, dm.Lkv, causal, device_sm_count(), &ctas, nsplit);
-  attn_nvfp4_kernel<D, OUT32><<<ctas, kThreads, C::kSmemBytes, s>>>(
-      tq, tk, tv, static_cast<const uint8_t*>(x.q_sf), static_cast<const uint8_t*>(x.k_sf),
-      static_cast<const uint8_t*>(x.v_sf), o, dm.H, dm.Hkv, dm.Lq, dm.Lkv, causal, work, part, so, kWaitLimitNs);
-  cudaError_t e = cudaGetLastError();
+  // a programmatic dependent launch: the CTAs' set-up overlaps the end of
+  // the kernel before (sa_quantize's last launch, as a rule); the producer
+  // waits for it before its first load
+  cudaLaunchAttribute attr;
+  const cudaLaunchConfig_t cfg = pdl_launch_config(dim3(ctas), dim3(kThreads), C::kSmemBytes, s, &attr);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_nvfp4_kernel<D, OUT32>, tq, tk, tv,
+                                     static_cast<const uint8_t*>(x.q_sf), static_cast<const uint8_t*>(x.k_sf),
+                                     static_cast<const uint8_t*>(x.v_sf), o, dm.H, dm.Hkv, dm.Lq, dm.Lkv, causal,
+                                     work, part, so, kWaitLimitNs);
   if (e == cudaSuccess && work.streamk) e = launch_streamk_combine(work, ctas, part, dm, o, so, OUT32, s);
   else if (e == cudaSuccess && work.nsplit > 1) e = launch_splitkv_combine(part, work.nsplit, dm, o, so, OUT32, s);
   return e;

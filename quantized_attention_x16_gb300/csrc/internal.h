@@ -41,6 +41,25 @@ inline int device_sm_count() {
   return n;
 }
 
+// Launch configuration of a programmatic dependent launch: the kernel may
+// start while the kernel before it in the stream finishes (once that one's
+// CTAs have all signalled griddepcontrol.launch_dependents or exited) and
+// must execute griddepcontrol.wait before it reads anything that kernel
+// writes.  `attr` is the caller's storage for the one launch attribute.
+inline cudaLaunchConfig_t pdl_launch_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                            cudaLaunchAttribute* attr) {
+  attr->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr->val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t c = {};
+  c.gridDim = grid;
+  c.blockDim = block;
+  c.dynamicSmemBytes = smem;
+  c.stream = s;
+  c.attrs = attr;
+  c.numAttrs = 1;
+  return c;
+}
+
 // Barrier-wait limit used by the attention kernels (nanoseconds).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 

@@ -356,6 +356,9 @@ __global__ void __launch_bounds__(kThreadsQ, 3) quant_qk_kernel(const __grid_con
                                                              const __grid_constant__ CUtensorMap tmap_k,
                                                              const QuantArgs a) {
   using T = TileQK<D>;
+  // the attention launch behind this one may start (it waits for this
+  // launch's completion before it reads the codes)
+  pdl_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t full[2];

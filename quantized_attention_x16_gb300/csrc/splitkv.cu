@@ -33,26 +33,6 @@ constexpr int kLanesPerRow = 8;                       // lanes sharing one outpu
 constexpr int kRowsPerCta = 256 / kLanesPerRow;          // 256 threads, 32 rows
 constexpr int kSegBatch = 2;                             // partial rows whose loads are issued together
 
-// Launch configuration of a combine kernel: a programmatic dependent launch
-// behind the attention kernel, so that its launch is processed while the
-// attention CTAs finish; the kernel waits (pdl_wait) before it reads.
-cudaLaunchAttribute g_pdl_attr = [] {
-  cudaLaunchAttribute a;
-  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  a.val.programmaticStreamSerializationAllowed = 1;
-  return a;
-}();
-cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, cudaStream_t s) {
-  cudaLaunchConfig_t c = {};
-  c.gridDim = grid;
-  c.blockDim = block;
-  c.dynamicSmemBytes = 0;
-  c.stream = s;
-  c.attrs = &g_pdl_attr;
-  c.numAttrs = 1;
-  return c;
-}
-
 // Merges the nseg partial rows seg(0), seg(1), ... of one output row; called
 // by the kLanesPerRow lanes of the row, lane i of them holding columns
 // [i*V, i*V + V), V = D / kLanesPerRow.  The loads of kSegBatch segments
@@ -180,7 +160,10 @@ cudaError_t launch(const SplitOut& part, int nsplit, const Dims& dm, void* o, co
   const int Lp = padded_len(dm.Lq);
   const long long split_rows = (long long)dm.B * dm.H * Lp;
   const long long ctas = (nrows + kRowsPerCta - 1) / kRowsPerCta;
-  const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)ctas), dim3(kRowsPerCta * kLanesPerRow), s);
+  // a programmatic dependent launch behind the attention kernel: its launch
+  // is processed while the attention CTAs finish
+  cudaLaunchAttribute attr;
+  const cudaLaunchConfig_t cfg = pdl_launch_config(dim3((unsigned)ctas), dim3(kRowsPerCta * kLanesPerRow), 0, s, &attr);
   return cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<D, OUT32>, part, nsplit, nrows, dm.Lq, Lp, split_rows, dm.H,
                             so, o);
 }
@@ -215,7 +198,9 @@ cudaError_t launch_sk(const AttnWork& w, int ctas, const SplitOut& part, const D
   StreamKCuts cuts;
   make_streamk_cuts(w, ctas, &cuts);
   if (cuts.n == 0) return cudaSuccess;               // no pair was cut
-  const cudaLaunchConfig_t cfg = pdl_config(dim3(cuts.n, 256 / kRowsPerCta), dim3(kRowsPerCta * kLanesPerRow), s);
+  cudaLaunchAttribute attr;
+  const cudaLaunchConfig_t cfg =
+      pdl_launch_config(dim3(cuts.n, 256 / kRowsPerCta), dim3(kRowsPerCta * kLanesPerRow), 0, s, &attr);
   return cudaLaunchKernelEx(&cfg, streamk_combine_kernel<D, OUT32>, cuts, part, dm.Lq, dm.H, so, o);
 }
 
