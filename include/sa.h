@@ -243,8 +243,8 @@ sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o,
  * boundary is computed in segments and merged the same way.
  *
  * sa_attn_fwd_workspace_bytes: device workspace bytes sa_attn_fwd_ws needs
- *   for the given sizes and `nsplit`: 0 = the library's choice (NVFP4:
- *   stream-K once the pairs fill the SMs; split-KV while the units leave at
+ *   for the given sizes and `nsplit`: 0 = the library's choice (NVFP4,
+ *   non-causal: stream-K once the pairs fill the SMs; split-KV while the units leave at
  *   least half of the SMs idle and every share keeps 16 key tiles or more, at
  *   most 16 shares; else neither); 1 = one unit per CTA; n > 1 = n shares, at
  *   most one per key tile; -1 = stream-K (NVFP4 only).  0 when neither would
