@@ -105,7 +105,8 @@ def cpu_oracle_sample(w, heads, nrows, seed=0):
     import numpy as np
     from oracle import attention as A
     x = W.make_inputs(w)
-    rows = np.array(W.sample_rows(w["L"], nrows, seed=seed))
+    Lq, L = W.lq(w), w["L"]
+    rows = np.array(W.sample_rows(Lq, nrows, seed=seed))
     G = w["H"] // w["Hkv"]
     t0 = time.perf_counter()
     for h in range(heads):
@@ -115,10 +116,20 @@ def cpu_oracle_sample(w, heads, nrows, seed=0):
         (qd, kd, vd), _ = A.dequantized_operands(q, k, v)
         A.sa3_emulated_attention(qd, kd, vd, w["causal"], rows=rows)
     dt = time.perf_counter() - t0
-    fl = 4.0 * heads * len(rows) * w["L"] * w["d"] / (2 if w["causal"] else 1)
+    if w["causal"] and Lq == L:
+        fl = 4.0 * heads * len(rows) * L * w["d"] / 2          # the halved count of the metric
+    elif w["causal"]:
+        fl = 4.0 * heads * w["d"] * sum(int(r) + L - Lq + 1 for r in rows)
+    else:
+        fl = 4.0 * heads * len(rows) * L * w["d"]
     desc = (f"{heads} head(s) x {len(rows)} query rows of {w['name']} (full-length keys): NumPy oracle "
             "quantiser (K mean, Q/K/V NVFP4) + SA3 tile-by-tile emulation")
     return dt, fl, desc
+
+
+def workload_str(w):
+    lens = f"L={w['L']}" if W.lq(w) == w["L"] else f"Lq={W.lq(w)} Lkv={w['L']}"
+    return f"{w['name']}: B={w['B']} H={w['H']} Hkv={w['Hkv']} {lens} d={w['d']}"
 
 
 def host_cores():
@@ -141,8 +152,8 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64/f32 (CPU oracle)", "data": "synthetic",
-            "config": {"workload": f"{w['name']}: B={w['B']} H={w['H']} Hkv={w['Hkv']} L={w['L']} d={w['d']} "
-                                   f"{'causal' if w['causal'] else 'non-causal'}", "sample": desc},
+            "config": {"workload": f"{workload_str(w)} {'causal' if w['causal'] else 'non-causal'}",
+                       "sample": desc},
             "cpu_baseline": {"value": v, "unit": "TOPS", "cores": host_cores(), "kind": "oracle", "sample": desc},
             "e2e": {"value": v, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -158,9 +169,10 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     w = W.spec(args.workload, seed=W.spec(args.workload)["seed"] + 1000 * rank)   # independent batch per rank
     B, H, Hkv, L, d = w["B"], w["H"], w["Hkv"], w["L"], w["d"]
+    Lq = W.lq(w)                                   # query rows (L: keys)
     x = W.make_inputs(w)
     q, k, v = (x[n].to(dev) for n in "qkv")
-    fq = sa.FP4QKV(B, H, Hkv, L, d, device=dev)
+    fq = sa.FP4QKV(B, H, Hkv, Lq, d, device=dev, Lkv=L)
     o4 = torch.empty_like(q)
     o16 = torch.empty_like(q)
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
@@ -170,8 +182,8 @@ def run_ours(args, rank, world, local_rank):
     # the library's work split (stream-K for the NVFP4 path once the pairs
     # fill the SMs, split-KV for problems too small to); the workspace is
     # allocated once, outside the timed region
-    ws4 = sa.sa_attn_fwd_workspace_bytes(B, H, Hkv, L, d, causal, "nvfp4", 0)
-    ws16 = sa.sa_attn_fwd_workspace_bytes(B, H, Hkv, L, d, causal, "bf16", 0)
+    ws4 = sa.sa_attn_fwd_workspace_bytes(B, H, Hkv, Lq, d, causal, "nvfp4", 0, Lkv=L)
+    ws16 = sa.sa_attn_fwd_workspace_bytes(B, H, Hkv, Lq, d, causal, "bf16", 0, Lkv=L)
     nsplit_ws = max(ws4, ws16)
     ws = torch.empty(max(nsplit_ws, 16), dtype=torch.uint8, device=dev)
 
@@ -236,30 +248,37 @@ def run_ours(args, rank, world, local_rank):
     # ---- end to end through the public API with host buffers (same metric)
     # sa_attn_fwd_host: pinned host Q, K, V in, pinned host O out; the library
     # chunks the problem by (batch, kv head) and overlaps its copies with the
-    # quantiser and attention kernels of neighbouring chunks
-    hq, hk, hv = (x[n].pin_memory() for n in "qkv")
-    ho = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h = ho.numel() * ho.element_size()
-    ws = torch.empty(sa.sa_attn_fwd_host_workspace_bytes(B, H, Hkv, L, d, "nvfp4"), dtype=torch.uint8, device=dev)
-    del fq
+    # quantiser and attention kernels of neighbouring chunks.  It takes one
+    # length for queries and keys, so a workload with Lq != L has no e2e.
+    e2e = None
+    if Lq == L:
+        hq, hk, hv = (x[n].pin_memory() for n in "qkv")
+        ho = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        d2h = ho.numel() * ho.element_size()
+        ws = torch.empty(sa.sa_attn_fwd_host_workspace_bytes(B, H, Hkv, L, d, "nvfp4"), dtype=torch.uint8,
+                         device=dev)
+        del fq
 
-    # SA_HOST_OVERLAP: each step's inputs are final when it is called, so its
-    # first copies may run beside the previous step's last compute and
-    # copy-out (every step still copies its own inputs in and its O out)
-    def e2e_step():
-        sa.sa_attn_fwd_host(hq, hk, hv, o=ho, causal=causal, mode="nvfp4", workspace=ws, overlap=True)
+        # SA_HOST_OVERLAP: each step's inputs are final when it is called, so
+        # its first copies may run beside the previous step's last compute and
+        # copy-out (every step still copies its own inputs in and its O out)
+        def e2e_step():
+            sa.sa_attn_fwd_host(hq, hk, hv, o=ho, causal=causal, mode="nvfp4", workspace=ws, overlap=True)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record()
-    torch.cuda.synchronize()
-    t_e2e = shard.max_over_ranks(e0.elapsed_time(e1) * 1e-3 / args.steps, device=dev)
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        t_e2e = shard.max_over_ranks(e0.elapsed_time(e1) * 1e-3 / args.steps, device=dev)
+        e2e = {"value": world * fl / t_e2e / 1e12, "unit": "TOPS", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
+               "api": "sa_attn_fwd_host (nvfp4, SA_HOST_OVERLAP)"}
 
     if rank != 0:
         return
@@ -268,6 +287,7 @@ def run_ours(args, rank, world, local_rank):
     a4 = fl / t_4 / 1e12
     a16 = fl / t_16 / 1e12
     qbytes = quant_bytes(w)
+    attn_bytes = attn_nvfp4_bytes(w)
     clocks = clk.summary()
     prof = load_profile_traffic()
     cpu = None
@@ -288,12 +308,12 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "nvfp4 (e2m1 x e4m3-scaled, fp32 accumulate); bf16 path alongside",
         "data": "synthetic (seeded torch.Generator, bf16)",
-        "config": {"workload": f"{w['name']}: B={B} H={H} Hkv={Hkv} L={L} d={d} "
-                               f"{'causal' if causal else 'non-causal'} ({w['kind']} inputs)",
-                   "B": B, "H": H, "Hkv": Hkv, "L": L, "d": d, "causal": causal,
+        "config": {"workload": f"{workload_str(w)} {'causal' if causal else 'non-causal'} ({w['kind']} inputs)",
+                   "B": B, "H": H, "Hkv": Hkv, "L": L, "Lq": Lq, "d": d, "causal": causal,
                    "l2": "flushed by a 256 MB write before every step",
-                   "value_def": "4*B*H*L^2*d / (sa_quantize + NVFP4 sa_attn_fwd, back to back in one "
-                                "CUDA-event interval) per GPU, summed over GPUs",
+                   "value_def": "4*B*H*L^2*d (halved for causal; with Lq != L, 4*B*H*d x the (query, key) "
+                                "pairs the mask leaves) / (sa_quantize + NVFP4 sa_attn_fwd, back to back in "
+                                "one CUDA-event interval) per GPU, summed over GPUs",
                    "parallelism": f"independent batch per GPU ({world} GPU)",
                    "work_split": "library choice (sa_attn_fwd_ws, nsplit=0): nvfp4 "
                                  + ("stream-K/split" if ws4 > 0 else "one unit per CTA") + ", bf16 "
@@ -322,9 +342,14 @@ def run_ours(args, rank, world, local_rank):
                               "peak": pk["hbm"], "unit": "GB/s", "frac": qbytes / t_q / 1e9 / pk["hbm"],
                               "traffic": None, "algorithmic_bytes": qbytes,
                               "traffic_kernels": {k: prof.get(k) for k in ("quant_v_mean_kernel", "quant_qk_kernel")}},
+        "roofline_hbm_attn": {"kernel": f"attn_nvfp4_kernel<{d}>", "bound": "hbm (context: the bound of few-query "
+                              "shapes such as decode)", "achieved": attn_bytes / t_4 / 1e9, "peak": pk["hbm"],
+                              "unit": "GB/s", "frac": attn_bytes / t_4 / 1e9 / pk["hbm"],
+                              "algorithmic_bytes": attn_bytes},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * fl / t_e2e / 1e12, "unit": "TOPS", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3, "api": "sa_attn_fwd_host (nvfp4, SA_HOST_OVERLAP)"},
+        "e2e": e2e if e2e is not None else {"value": None, "unit": "TOPS", "h2d_bytes_per_step": 0,
+                                            "d2h_bytes_per_step": 0,
+                                            "note": "sa_attn_fwd_host takes equal query and key lengths"},
         "gpu_launches": launches,
         "clocks": clocks,
         "wall_s_timed_region": wall,
@@ -355,10 +380,21 @@ def quant_bytes(w):
     """Algorithmic HBM bytes of sa_quantize: read Q, K, V (bf16) + K again for the
     mean, write codes (0.5 B/elem) and scales (1/16 B/elem), the mean and its partials."""
     B, H, Hkv, L, d = w["B"], w["H"], w["Hkv"], w["L"], w["d"]
-    nq, nk = B * H * L * d, B * Hkv * L * d
+    nq, nk = B * H * W.lq(w) * d, B * Hkv * L * d
     reads = 2 * nq + 2 * nk * 2 + 2 * nk
     writes = (nq + 2 * nk) * (0.5 + 1 / 16)
     return reads + writes
+
+
+def attn_nvfp4_bytes(w):
+    """Algorithmic HBM bytes of one NVFP4 attention call: read the FP4 codes and
+    e4m3 scales of Q, K, V (0.5 + 1/16 B per element, padded lengths), write O
+    (bf16)."""
+    B, H, Hkv, L, d = w["B"], w["H"], w["Hkv"], w["L"], w["d"]
+    Lq = W.lq(w)
+    pad = lambda n: (n + 127) // 128 * 128   # noqa: E731
+    fp4 = 0.5 + 1 / 16
+    return (B * H * pad(Lq) * d + 2 * B * Hkv * pad(L) * d) * fp4 + 2 * B * H * Lq * d
 
 
 def load_profile_traffic():

@@ -6,7 +6,9 @@ oracle can both be fed the same inputs while sharing no method code.
 
 Every tensor is drawn on the CPU in float32 from ``torch.Generator`` seeded
 per workload, then rounded to bfloat16 (the operand type of the library).
-Layout is BHLD: Q [B, H, L, d], K and V [B, Hkv, L, d].
+Layout is BHLD: Q [B, H, Lq, d], K and V [B, Hkv, L, d]; Lq = L unless the
+workload sets "Lq", and then Q is drawn by the same recipe at length Lq with
+the seed + 1 (K and V are the workload's at length L).
 
 Workloads (named by what they are):
 
@@ -21,6 +23,8 @@ Workloads (named by what they are):
                     bias ~ N(0,1) per (head, channel), drawn independently for
                     Q and K; V ~ N(0,1).
 * ``sweep_<causal|full>_d<64|128>_L<n>``  B1 H8, L in 1k..32k, N(0,1).
+* ``decode_gqa``    B16 Hq32 Hkv8, one query token against L = 8192 keys,
+                    d128, N(0,1): a decode step (split over the key range).
 """
 
 import math
@@ -32,6 +36,7 @@ WORKLOADS = {
     "llm_prefill": dict(B=2, H=16, Hkv=16, L=4096, d=128, causal=False, seed=2, kind="kbias"),
     "causal_gqa":  dict(B=1, H=32, Hkv=8, L=8192,  d=128, causal=True,  seed=3, kind="outlier"),
     "dit_video":   dict(B=1, H=24, Hkv=24, L=16384, d=128, causal=False, seed=4, kind="qkbias"),
+    "decode_gqa":  dict(B=16, H=32, Hkv=8, L=8192, Lq=1, d=128, causal=False, seed=6, kind="iid"),
 }
 SWEEP_L = (1024, 2048, 4096, 8192, 16384, 32768)
 _i = 0
@@ -43,10 +48,21 @@ for _d in (64, 128):
             _i += 1
 
 
+def lq(w):
+    """Query length of a workload (the key length L unless it sets Lq)."""
+    return w.get("Lq", w["L"])
+
+
 def flops(w):
-    """Counted attention work 4*B*H*L^2*d, halved for causal."""
-    f = 4.0 * w["B"] * w["H"] * w["L"] * w["L"] * w["d"]
-    return f / 2 if w["causal"] else f
+    """Counted attention work 4*B*H*L^2*d, halved for causal; with Lq != L,
+    4*B*H*d times the (query, key) pairs the mask leaves (all Lq*L, or under
+    the bottom-right causal mask sum over rows i of i + L - Lq + 1)."""
+    L, Lq = w["L"], lq(w)
+    if Lq == L:
+        f = 4.0 * w["B"] * w["H"] * L * L * w["d"]
+        return f / 2 if w["causal"] else f
+    pairs = Lq * (L - Lq) + Lq * (Lq + 1) / 2 if w["causal"] else Lq * L
+    return 4.0 * w["B"] * w["H"] * w["d"] * pairs
 
 
 def spec(name, **over):
@@ -67,6 +83,11 @@ def make_inputs(w):
 
     ``w`` may override B/H/Hkv/L/d/seed/kind of a named workload (used for
     the small parity cases); the recipe depends only on ``kind``."""
+    if lq(w) != w["L"]:
+        base = {k: v for k, v in w.items() if k != "Lq"}
+        x = make_inputs(base)
+        x["q"] = make_inputs(dict(base, L=lq(w), seed=int(w["seed"]) + 1))["q"]
+        return x
     B, H, Hkv, L, d = w["B"], w["H"], w["Hkv"], w["L"], w["d"]
     g = torch.Generator().manual_seed(int(w["seed"]))
     kind = w["kind"]
@@ -110,7 +131,7 @@ def sample_rows(L, n, seed=1234):
 
 
 def describe(w):
-    return {k: w[k] for k in ("B", "H", "Hkv", "L", "d", "causal", "seed", "kind")}
+    return {k: w[k] for k in ("B", "H", "Hkv", "L", "Lq", "d", "causal", "seed", "kind") if k in w}
 
 
-__all__ = ["WORKLOADS", "spec", "make_inputs", "flops", "sample_rows", "describe", "math"]
+__all__ = ["WORKLOADS", "spec", "make_inputs", "lq", "flops", "sample_rows", "describe", "math"]
