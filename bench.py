@@ -172,12 +172,21 @@ def run_ours(args, rank, world, local_rank):
     Lq = W.lq(w)                                   # query rows (L: keys)
     x = W.make_inputs(w)
     q, k, v = (x[n].to(dev) for n in "qkv")
+    fl = W.flops(w)
+    causal = w["causal"]
+    # A one-token query (decode) against a GQA cache: the G query heads of a
+    # kv head read the same keys and values, and with one row per head no mask
+    # tells them apart (under the bottom-right causal mask the row sees every
+    # key), so Q [B, H, 1, d] goes to the library as [B, Hkv, G, d] -- the
+    # same BHLD memory, G query rows per kv head, the same O -- with G times
+    # fewer 128-row query tiles.
+    fold = Lq == 1 and H > Hkv
+    if fold:
+        q, H, Lq, causal = q.view(B, Hkv, H // Hkv, d), Hkv, H // Hkv, False
     fq = sa.FP4QKV(B, H, Hkv, Lq, d, device=dev, Lkv=L)
     o4 = torch.empty_like(q)
     o16 = torch.empty_like(q)
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
-    fl = W.flops(w)
-    causal = w["causal"]
 
     # the library's work split (stream-K for the NVFP4 path once the pairs
     # fill the SMs, split-KV for problems too small to); the workspace is
@@ -309,7 +318,9 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "nvfp4 (e2m1 x e4m3-scaled, fp32 accumulate); bf16 path alongside",
         "data": "synthetic (seeded torch.Generator, bf16)",
         "config": {"workload": f"{workload_str(w)} {'causal' if causal else 'non-causal'} ({w['kind']} inputs)",
-                   "B": B, "H": H, "Hkv": Hkv, "L": L, "Lq": Lq, "d": d, "causal": causal,
+                   "B": w["B"], "H": w["H"], "Hkv": w["Hkv"], "L": L, "Lq": W.lq(w), "d": d, "causal": w["causal"],
+                   "gqa_fold": ("Q [B, H, 1, d] passed as [B, Hkv, H/Hkv, d]: the query heads of a kv head as "
+                                "its query rows") if fold else None,
                    "l2": "flushed by a 256 MB write before every step",
                    "value_def": "4*B*H*L^2*d (halved for causal; with Lq != L, 4*B*H*d x the (query, key) "
                                 "pairs the mask leaves) / (sa_quantize + NVFP4 sa_attn_fwd, back to back in "

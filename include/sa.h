@@ -127,6 +127,11 @@ typedef struct {
  * entry points take this struct; the others are the special case Lq = Lkv =
  * L.  With Lq != Lkv the quantised layouts below have Lq rows for Q and Lkv
  * rows (or token columns) for K and V, each rounded up to 128.
+ * Decode with grouped heads: a one-token query (Lq = 1) sees every key, so
+ * the G = H / Hkv query heads of a kv head differ only in their query
+ * vectors; in BHLD, Q [B, H, 1, d] is the same memory as [B, Hkv, G, d], and
+ * calling with {B, Hkv, Hkv, G, Lkv, d}, non-causal, gives the same O with G
+ * query rows per 128-row tile instead of one (G times fewer tiles).
  */
 typedef struct {
   int B, H, Hkv;   /* batch, query heads, key/value heads (H % Hkv == 0) */

@@ -301,3 +301,27 @@ def test_query_length_differs_from_key_length(sa, case, mode, causal, nsplit):
     o32 = run_qk(sa, x, causal, mode, nsplit, torch.float32) if mode == "nvfp4" else None
     heads = [(b, h) for b in range(w["B"]) for h in range(w["H"])]
     check(o, x, causal, heads, np.arange(Lq), mode, o32)
+
+
+@pytest.mark.parametrize("mode", ["bf16", "nvfp4"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_decode_grouped_heads_fold(sa, mode, causal):
+    """A one-token query sees every key, so Q [B, H, 1, d] passed as
+    [B, Hkv, G, d] (the G query heads of a kv head as its query rows, the
+    same memory) must give the same O bit for bit: every row's arithmetic
+    (its Q quantisation, its softmax, its P) is its own, and the K'/V
+    quantisation is per kv head either way."""
+    w = dict(W.spec("causal_gqa"), B=3, H=8, Hkv=2, seed=87)
+    x = qk_inputs(w, 1, 1500)
+    q, k, v = (x[n].cuda() for n in "qkv")
+    B, H, Hkv, d = 3, 8, 2, q.shape[-1]
+    qf = q.view(B, Hkv, H // Hkv, d)
+    if mode == "bf16":
+        o = sa.sa_attn_fwd(q, k, v, causal=causal, mode="bf16", nsplit=0)
+        of = sa.sa_attn_fwd(qf, k, v, causal=False, mode="bf16", nsplit=0)
+    else:
+        o = sa.sa_attn_fwd(sa.sa_quantize(q, k, v), causal=causal, mode="nvfp4", nsplit=0)
+        of = sa.sa_attn_fwd(sa.sa_quantize(qf, k, v), causal=False, mode="nvfp4", nsplit=0)
+    torch.cuda.synchronize()
+    assert sa.sa_last_device_error() == 0
+    assert torch.equal(of.view(B, H, 1, d).view(torch.int16), o.view(torch.int16))
