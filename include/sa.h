@@ -163,7 +163,13 @@ sa_status sa_fp4_qkv_from_blob_s(void* blob, const sa_shape* shape, sa_fp4_qkv* 
  *   code_i = e2m1_rne_satfinite(x_i / decode(s8)); all codes +0 if s8 == 0
  * with K' = float32(k) - k_mean[c].  Results are bit-exact functions of the
  * inputs.  q, k, v: bf16 BHLD device tensors; out: buffers as documented
- * above (all eight pointers required).  Enqueues 4 kernels on `stream`.
+ * above (all eight pointers required).  Enqueues 2 kernels on `stream`, the
+ * second a programmatic dependent launch of the first (it starts while the
+ * first drains and waits for it before it reads the K means); the second
+ * also lets a programmatic dependent launch behind it (sa_attn_fwd's) start
+ * early.  Ordering on `stream` is unchanged: work enqueued after the call
+ * that is not itself such a launch starts after both kernels complete, and
+ * such a launch reads nothing before they have.
  */
 sa_status sa_quantize(const void* q, const void* k, const void* v,
                       int B, int H, int Hkv, int L, int d,
@@ -260,7 +266,9 @@ sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o,
  *   workspace means one unit per CTA; with nsplit > 1 or -1 it is
  *   SA_ERR_INVALID_ARG; -1 with the BF16 path is SA_ERR_UNSUPPORTED.
  *   Enqueues the attention kernel and, when work is split, the combine
- *   kernel, on `stream`.
+ *   kernel, on `stream`; both are programmatic dependent launches (each may
+ *   start its set-up while the kernel before it finishes and reads its
+ *   inputs only after that kernel has completed), so stream order holds.
  */
 size_t sa_attn_fwd_workspace_bytes(int B, int H, int Hkv, int L, int d, int causal, int mode, int nsplit);
 sa_status sa_attn_fwd_ws(const void* q, const void* k, const void* v, void* o,
