@@ -32,6 +32,7 @@
 #include <mutex>
 #include <vector>
 
+#include "host_plan.h"
 #include "internal.h"
 
 namespace sa {
@@ -39,7 +40,6 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kSlots = 3;
-constexpr int kTailMinShareTiles = 8;   // split-KV shares of the shrinking last chunks
 
 // Two copy streams and the events that order the slots, per device; created
 // on first use and kept for the life of the process.
@@ -73,67 +73,6 @@ HostPipe* pipe_for_current_device() {
 }
 
 size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
-
-// Attention CTAs of one (batch, kv head) pair: its G heads' query-tile pairs.
-long long units_per_pair(int G, int L) { return (long long)G * (((L + 127) / 128 + 1) / 2); }
-
-// Pairs per chunk: the most whose attention CTAs fit in one wave on the SMs
-// (a chunk's kernels then take about one CTA lifetime), and at least two
-// chunks when there are two pairs or more.
-int default_chunk_pairs(int B, int H, int Hkv, int L) {
-  const int G = H / Hkv, pairs = B * Hkv;
-  const long long units = units_per_pair(G, L);
-  long long n = device_sm_count() / (units > 0 ? units : 1);
-  if (n < 1) n = 1;
-  if (pairs >= 2 && n > (pairs + 1) / 2) n = (pairs + 1) / 2;
-  return (int)n;
-}
-
-// Split-KV shares for a chunk of n pairs in the library's chunking: enough to
-// fill the SMs when its CTAs would leave half of them idle, each share keeping
-// kTailMinShareTiles key tiles, at most 16.
-int chunk_nsplit(int n, int G, int L) {
-  const int sms = device_sm_count(), nkt = (L + 127) / 128;
-  const long long units = (long long)n * units_per_pair(G, L);
-  if (sms <= 0 || units <= 0 || 2 * units > sms) return 1;
-  long long sp = sms / units;
-  if (sp > nkt / kTailMinShareTiles) sp = nkt / kTailMinShareTiles;
-  if (sp > 16) sp = 16;
-  return sp > 1 ? (int)sp : 1;
-}
-
-struct Chunk {
-  int n, nsplit;
-};
-
-// The chunks in order.  A caller's chunk size, or the BF16 path: chunks of
-// chunk_pairs (default n; the last one ragged), no split-KV.  The library's
-// chunking of the NVFP4 path: chunks of n pairs, the last ones shrinking by
-// halves down to min(2, n) pairs (built from the end: 2, 4, 8, ... capped at
-// n), split-KV where chunk_nsplit says so.
-std::vector<Chunk> chunk_plan(int B, int H, int Hkv, int L, int chunk_pairs, bool fp4) {
-  const int pairs = B * Hkv, G = H / Hkv;
-  const int n = default_chunk_pairs(B, H, Hkv, L);
-  std::vector<Chunk> plan;
-  if (chunk_pairs > 0 || !fp4) {
-    const int m = chunk_pairs > 0 ? chunk_pairs : n;
-    for (int p0 = 0; p0 < pairs; p0 += m) plan.push_back(Chunk{pairs - p0 < m ? pairs - p0 : m, 1});
-    return plan;
-  }
-  int rem = pairs, size = n < 2 ? n : 2;
-  while (rem > 0) {
-    const int t = size < rem ? size : rem;
-    plan.push_back(Chunk{t, chunk_nsplit(t, G, L)});
-    rem -= t;
-    size = 2 * size < n ? 2 * size : n;
-  }
-  for (size_t i = 0, j = plan.size() - 1; i < j; ++i, --j) {
-    const Chunk c = plan[i];
-    plan[i] = plan[j];
-    plan[j] = c;
-  }
-  return plan;
-}
 
 // Byte layout of one slot for chunks of up to n pairs.
 struct SlotLayout {
@@ -213,7 +152,7 @@ size_t sa_attn_fwd_host_workspace_bytes(int B, int H, int Hkv, int L, int d, int
   if (check_host_args(B, H, Hkv, L, d, 0, mode_flags, chunk_pairs) != SA_OK || B == 0 || L == 0) return 0;
   const bool fp4 = (mode_flags & 0xF) == SA_MODE_NVFP4;
   const size_t osz = (mode_flags & SA_OUT_FP32) ? 4 : 2;
-  return pipe_layout(chunk_plan(B, H, Hkv, L, chunk_pairs, fp4), H / Hkv, L, d, fp4, osz).bytes;
+  return pipe_layout(chunk_plan(B, H, Hkv, L, chunk_pairs, fp4, device_sm_count()), H / Hkv, L, d, fp4, osz).bytes;
 }
 
 sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int L, int d,
@@ -227,7 +166,7 @@ sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,
   if (!pinned_host(q) || !pinned_host(k) || !pinned_host(v) || !pinned_host(o)) return SA_ERR_INVALID_ARG;
   const int G = H / Hkv;
   const bool fp4 = (mode_flags & 0xF) == SA_MODE_NVFP4;
-  const std::vector<Chunk> plan = chunk_plan(B, H, Hkv, L, chunk_pairs, fp4);
+  const std::vector<Chunk> plan = chunk_plan(B, H, Hkv, L, chunk_pairs, fp4, device_sm_count());
   const size_t osz = (mode_flags & SA_OUT_FP32) ? 4 : 2;
   const PipeLayout lay = pipe_layout(plan, G, L, d, fp4, osz);
   if (workspace_bytes < lay.bytes) return SA_ERR_INVALID_ARG;
