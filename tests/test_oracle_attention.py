@@ -349,3 +349,30 @@ def test_emulation_without_quantisers_is_exact_lq_lkv(causal):
     for bc in (32, 128):
         e = A.sa3_emulated_attention(q, k, v, causal, bc=bc, quantize_p=False)
         assert np.allclose(e, A.exact_attention(q, k, v, causal), atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_decode_grouped_heads_fold_on_the_oracle(causal):
+    """A one-token query sees every key (bottom-right causal mask: j <= 0 +
+    Lkv - 1), so the G query heads of a kv head may be passed as G query rows
+    of one head: the exact and the emulated outputs of Q [B, H, 1, d] equal
+    those of Q viewed as [B, Hkv, G, d] (non-causal), row for row, up to the
+    float64 rounding of the oracle's blocked products (its Q quantisation is
+    per row, so the dequantised Q is the same exactly).  This is the
+    reformulation the decode bench and the header's note rely on."""
+    rng = np.random.default_rng(31)
+    B, H, Hkv, Lkv, d = 2, 6, 2, 300, 64
+    G = H // Hkv
+    q = rng.standard_normal((B, H, 1, d)).astype(np.float32)
+    k = rng.standard_normal((B, Hkv, Lkv, d)).astype(np.float32)
+    v = rng.standard_normal((B, Hkv, Lkv, d)).astype(np.float32)
+    qf = q.reshape(B, Hkv, G, d)
+    ex = A.exact_attention(q, k, v, causal)
+    exf = A.exact_attention(qf, k, v, False)
+    np.testing.assert_allclose(exf.reshape(B, H, 1, d), ex, rtol=1e-12, atol=1e-14)
+    (qd, kd, vd), _ = A.dequantized_operands(q, k, v)
+    (qdf, kdf, vdf), _ = A.dequantized_operands(qf, k, v)
+    np.testing.assert_array_equal(qdf.reshape(B, H, 1, d), qd)      # per-row Q quantisation
+    em = A.sa3_emulated_attention(qd, kd, vd, causal)
+    emf = A.sa3_emulated_attention(qdf, kdf, vdf, False)
+    np.testing.assert_allclose(emf.reshape(B, H, 1, d), em, rtol=1e-12, atol=1e-14)
