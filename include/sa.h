@@ -77,9 +77,12 @@ typedef enum { SA_MODE_BF16 = 0, SA_MODE_NVFP4 = 1 } sa_mode;
  * host -> device copies may start before that work completes; each waits only
  * until the previous sa_attn_fwd_host call on this device has finished
  * computing on the workspace slot it refills (and its compute until that
- * call's copy-out from the slot is done).  Back-to-back calls on one
- * workspace then overlap one call's first copy-ins with the previous call's
- * last compute and copy-out.  Results are unchanged.  Accepted by
+ * call's copy-out from the slot is done).  This applies when the previous
+ * call used the same workspace pointer and sizes that give the same slots;
+ * otherwise the call waits for the work before it, as without the flag.
+ * Back-to-back calls on one workspace then overlap one call's first copy-ins
+ * with the previous call's last compute and copy-out.  Results are
+ * unchanged.  Accepted by
  * sa_attn_fwd_host (and its workspace-size query) only. */
 #define SA_HOST_OVERLAP 64
 

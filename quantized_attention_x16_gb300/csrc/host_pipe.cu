@@ -47,6 +47,11 @@ struct HostPipe {
   bool ready = false;
   cudaStream_t cin = nullptr, cout = nullptr;
   cudaEvent_t start = nullptr, in[kSlots] = {}, comp[kSlots] = {}, out[kSlots] = {};
+  // the slots of the last call (its workspace and slot size): the slot events
+  // order a call after the previous one only when both cut the same memory
+  // into the same slots
+  const void* last_ws = nullptr;
+  size_t last_slot_bytes = 0;
 };
 HostPipe g_pipe[kMaxDevices];
 std::mutex g_pipe_mu;
@@ -188,8 +193,13 @@ sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,
   // (an earlier call on the same workspace, for one) -- with SA_HOST_OVERLAP
   // the copy-in stream does not: the first kSlots chunks wait instead for the
   // slot events of the previous call on this device, like later chunks for
-  // those of this call (an event never recorded is no wait).
-  const bool overlap = (mode_flags & SA_HOST_OVERLAP) != 0;
+  // those of this call (an event never recorded is no wait).  That is only
+  // sound when the previous call used the same slots (same workspace, same
+  // slot size); otherwise this call waits for everything before it.
+  const bool overlap = (mode_flags & SA_HOST_OVERLAP) != 0 && p->last_ws == workspace &&
+                       p->last_slot_bytes == lay.slot.bytes;
+  p->last_ws = workspace;
+  p->last_slot_bytes = lay.slot.bytes;
   const int dev_mode = mode_flags & ~SA_HOST_OVERLAP;   // the mode of the device-buffer calls
   cu(cudaEventRecord(p->start, s));
   if (!overlap) cu(cudaStreamWaitEvent(p->cin, p->start, 0));
