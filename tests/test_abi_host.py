@@ -32,6 +32,19 @@ def header_functions():
     return sorted(set(re.findall(r"\b(sa_[a-z0-9_]+)\s*\(", text)))
 
 
+def test_binding_constants_match_the_header(sa):
+    """The binding's copies of the header's #defines and enumerators."""
+    text = open(os.path.join(ROOT, "include", "sa.h")).read()
+    defines = dict((m.group(1), int(m.group(2))) for m in re.finditer(r"#define\s+(SA_[A-Z0-9_]+)\s+(\d+)", text))
+    assert defines, "no #defines found"
+    for name, value in defines.items():
+        assert getattr(sa, name) == value, name
+    enums = dict((m.group(1), int(m.group(2))) for m in re.finditer(r"\b(SA_[A-Z0-9_]+)\s*=\s*(\d+)", text))
+    assert len(enums) >= 7
+    for name, value in enums.items():
+        assert getattr(sa, name) == value, name
+
+
 def test_exports_every_declared_symbol(sa):
     declared = header_functions()
     assert declared, "no declarations found"
