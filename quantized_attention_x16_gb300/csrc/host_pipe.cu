@@ -198,8 +198,9 @@ sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,
   // slot size); otherwise this call waits for everything before it.
   const bool overlap = (mode_flags & SA_HOST_OVERLAP) != 0 && p->last_ws == workspace &&
                        p->last_slot_bytes == lay.slot.bytes;
-  p->last_ws = workspace;
-  p->last_slot_bytes = lay.slot.bytes;
+  // until this call has enqueued all of its work, the next one must not rely
+  // on its slot events (an error below returns with the record cleared)
+  p->last_ws = nullptr;
   const int dev_mode = mode_flags & ~SA_HOST_OVERLAP;   // the mode of the device-buffer calls
   cu(cudaEventRecord(p->start, s));
   if (!overlap) cu(cudaStreamWaitEvent(p->cin, p->start, 0));
@@ -247,7 +248,10 @@ sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,
   // stream is in order, so its last event covers every chunk)
   const int last = (nchunks - 1) % kSlots;
   cu(cudaStreamWaitEvent(s, p->out[last], 0));
-  return ok ? SA_OK : SA_ERR_CUDA;
+  if (!ok) return SA_ERR_CUDA;
+  p->last_ws = workspace;
+  p->last_slot_bytes = lay.slot.bytes;
+  return SA_OK;
 }
 
 }  // extern "C"
