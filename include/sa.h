@@ -80,6 +80,10 @@ typedef enum { SA_MODE_BF16 = 0, SA_MODE_NVFP4 = 1 } sa_mode;
  * call's copy-out from the slot is done).  This applies when the previous
  * call used the same workspace pointer and sizes that give the same slots;
  * otherwise the call waits for the work before it, as without the flag.
+ * The call's compute (on `stream`) also waits until the previous call's last
+ * compute has finished, whichever stream that call used: the split-KV region
+ * of the workspace is shared by all slots, so no chunk of this call may use
+ * it while a chunk of the previous call still does.
  * Back-to-back calls on one workspace then overlap one call's first copy-ins
  * with the previous call's last compute and copy-out.  Results are
  * unchanged.  Accepted by
@@ -316,10 +320,12 @@ sa_status sa_attn_fwd_s(const void* q, const void* k, const void* v, void* o, co
  * is quantised per key tile, so split-KV changes nothing else).  The copies start after the work already enqueued on
  * `stream`, and `stream` reaches the end of the call's work only after O is
  * in host memory (synchronise on `stream` before reading o).  The two copy
- * streams and ten events are created on the first call on each device and
- * kept until the process exits; calls on one device must not be made
+ * streams and thirteen events are created on the first call on each device
+ * and kept until the process exits; calls on one device must not be made
  * concurrently from several host threads.  Errors as for sa_attn_fwd; a
- * failure after the first copy was enqueued leaves o partly written.
+ * failure after the first copy was enqueued leaves o partly written, and
+ * `stream` still waits for every copy the call enqueued (after synchronising
+ * it, no copy of the failed call touches q, k, v, o or the workspace).
  */
 size_t sa_attn_fwd_host_workspace_bytes(int B, int H, int Hkv, int L, int d, int mode, int chunk_pairs);
 sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,

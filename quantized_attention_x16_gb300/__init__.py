@@ -135,6 +135,14 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _keep_for_stream(t, stream):
+    """A temporary allocated here (on the current stream) and used by work
+    enqueued on another `stream`: the caching allocator must not hand its
+    memory out again before that work has finished."""
+    if stream is not None:
+        t.record_stream(stream)
+
+
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
@@ -285,6 +293,7 @@ def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=
     need = int(lib.sa_attn_fwd_workspace_bytes_s(ctypes.byref(shape), int(bool(causal)), m & 0xF, ns))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        _keep_for_stream(workspace, stream)
     ws, nbytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel())
     _check(lib.sa_attn_fwd_s(*args, _ptr(o), ctypes.byref(shape), int(bool(causal)), m, ns, ws, nbytes,
                              _stream(stream)), "sa_attn_fwd_s")
@@ -332,6 +341,7 @@ def sa_attn_fwd_host(q, k, v, o=None, causal=False, mode="nvfp4", out_dtype=None
         raise SaError(SA_ERR_UNSUPPORTED, "sa_attn_fwd_host_workspace_bytes")
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+        _keep_for_stream(workspace, stream)
     if not (workspace.is_cuda and workspace.dtype == torch.uint8 and workspace.is_contiguous()):
         raise ValueError("workspace must be a contiguous uint8 CUDA tensor")
     _check(lib.sa_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Hkv, L, d, int(bool(causal)),

@@ -436,26 +436,26 @@ template <int D, bool OUT32>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o, const Strides& so,
                      const Dims& dm, int causal, int nsplit, const SplitOut& part, cudaStream_t s) {
   using C = CfgBF16<D>;
-  static bool attr_done = false;   // the attribute is a property of the function, set once per process
-  if (!attr_done) {
+  // kernel attributes are per device: set them on the first launch on each
+  static std::atomic<bool> attr_done[kMaxDevices];
+  cudaError_t e = once_per_device(attr_done, [] {
     // The warpgroup register split assumes kLaunchRegs registers per thread at
     // launch; with fewer, a setmaxnreg increase could never be satisfied.
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, attn_bf16_kernel<D, OUT32>);
-    if (e != cudaSuccess) return e;
+    cudaError_t r = cudaFuncGetAttributes(&fa, attn_bf16_kernel<D, OUT32>);
+    if (r != cudaSuccess) return r;
     if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_bf16_kernel<D, OUT32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+    return cudaFuncSetAttribute(attn_bf16_kernel<D, OUT32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::kSmemBytes);
+  });
+  if (e != cudaSuccess) return e;
   int ctas = 0;
   const AttnWork work = make_attn_work(dm.B, dm.H, dm.Lq, dm.Lkv, causal, device_sm_count(), &ctas, nsplit);
   // a programmatic dependent launch: the CTAs' set-up overlaps the end of
   // the kernel before; the producer waits for it before its first load
   cudaLaunchAttribute attr;
   const cudaLaunchConfig_t cfg = pdl_launch_config(dim3(ctas), dim3(kThreads), C::kSmemBytes, s, &attr);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_bf16_kernel<D, OUT32>, tq, tk, tv, o, dm.H, dm.Hkv, dm.Lq, dm.Lkv,
+  e = cudaLaunchKernelEx(&cfg, attn_bf16_kernel<D, OUT32>, tq, tk, tv, o, dm.H, dm.Hkv, dm.Lq, dm.Lkv,
                                      causal, work, part, so, kWaitLimitNs);
   if (e == cudaSuccess && work.nsplit > 1) e = launch_splitkv_combine(part, work.nsplit, dm, o, so, OUT32, s);
   return e;

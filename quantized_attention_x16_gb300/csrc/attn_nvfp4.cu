@@ -89,7 +89,9 @@ struct CfgF4 {
   // Q/K rows of 64 bytes use the 64B swizzle, rows of 32 bytes the 32B one.
   static constexpr uint32_t kQKSwz = (D == 128) ? kSwizzle64B : kSwizzle32B;
   static constexpr uint32_t kQKSbo = 8 * kRowBytes;
-  // tensor-memory columns
+  // tensor-memory columns: one S region, which the two query tiles take in
+  // turns (separate regions at d = 64, where they fit, measured slower: the
+  // turns keep the two softmax warpgroups out of step)
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColO0 = 128;
   static constexpr uint32_t kColSf = 128 + 2 * D;
@@ -270,9 +272,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- S issuer
       // S0(0), S1(0), S0(1), S1(1), ... into the one S region; each waits
       // until the softmax warps have read the previous S (over the whole
-      // list).  A tile's K scales go to the buffer of its parity; the buffer
-      // was last read by the S MMAs two tiles earlier, complete once the S
-      // before the previous tile's has been read.
+      // list).  Scale-factor buffers in tensor memory are rewritten only once
+      // the MMAs that read them are complete (a tcgen05.cp is not ordered
+      // after them): a tile's K scales go to the buffer of its parity, last
+      // read by the S MMAs of tile gk - 2, whose commit is that stage's
+      // k_empty phase; a unit's Q scales to the buffer of its parity, last
+      // read by unit ug - 2, whose commit is q_empty.
       const bool leader = elect_one();
       const uint32_t sb = smem_u32(smem);
       const uint32_t tS = tbase + C::kColS;
@@ -289,10 +294,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nt = u.n[0] > u.n[1] ? u.n[0] : u.n[1];
         ok = mbar_wait_warp(bars.q_full + qb, (ug >> 1) & 1, abort_flag, wait_ns);
         if (!ok) break;
-        // Q scales of this unit to the columns of its parity, last read by
-        // the S MMAs of unit ug-2, complete before S of unit ug-1 was issued.
-        // (A unit without key tiles issues no MMA, and so no copy whose
-        // completion a commit would have to cover.)
+        // Q scales of this unit to the columns of its parity.  (A unit without
+        // key tiles issues no MMA, and so no copy whose completion a commit
+        // would have to cover.)
+        if (ok && nt > 0 && ug >= 2)
+          ok = mbar_wait_warp(bars.q_empty + qb, ((ug >> 1) - 1) & 1, abort_flag, wait_ns);
+        if (!ok) break;
         if (nt > 0) {
           tc_fence_after();
           if (leader)
@@ -303,6 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; ok && j < nt; ++j, ++gk) {
           const int s = gk % C::NS;
           ok = mbar_wait_warp(bars.k_full + s, (gk / C::NS) & 1, abort_flag, wait_ns);
+          if (ok && gk >= 2)
+            ok = mbar_wait_warp(bars.k_empty + (gk - 2) % C::NS, ((gk - 2) / C::NS) & 1, abort_flag, wait_ns);
           if (!ok) break;
           tc_fence_after();
           const uint32_t sfk = tbase + C::kColSfK + 8 * (gk & 1);
@@ -636,19 +645,19 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
                      void* o, const Strides& so, const Dims& dm, int causal, int nsplit, const SplitOut& part,
                      cudaStream_t s) {
   using C = CfgF4<D>;
-  static bool attr_done = false;
-  if (!attr_done) {
+  // kernel attributes are per device: set them on the first launch on each
+  static std::atomic<bool> attr_done[kMaxDevices];
+  cudaError_t e = once_per_device(attr_done, [] {
     // The warpgroup register split assumes kLaunchRegs registers per thread at
     // launch; with fewer, a setmaxnreg increase could never be satisfied.
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, attn_nvfp4_kernel<D, OUT32>);
-    if (e != cudaSuccess) return e;
+    cudaError_t r = cudaFuncGetAttributes(&fa, attn_nvfp4_kernel<D, OUT32>);
+    if (r != cudaSuccess) return r;
     if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_nvfp4_kernel<D, OUT32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+    return cudaFuncSetAttribute(attn_nvfp4_kernel<D, OUT32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::kSmemBytes);
+  });
+  if (e != cudaSuccess) return e;
   int ctas = 0;
   const AttnWork work = nsplit == kStreamK
                             ? make_streamk_work(dm.B, dm.H, dm.Lq, dm.Lkv, causal, device_sm_count(), &ctas)
@@ -658,7 +667,7 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   // waits for it before its first load
   cudaLaunchAttribute attr;
   const cudaLaunchConfig_t cfg = pdl_launch_config(dim3(ctas), dim3(kThreads), C::kSmemBytes, s, &attr);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_nvfp4_kernel<D, OUT32>, tq, tk, tv,
+  e = cudaLaunchKernelEx(&cfg, attn_nvfp4_kernel<D, OUT32>, tq, tk, tv,
                                      static_cast<const uint8_t*>(x.q_sf), static_cast<const uint8_t*>(x.k_sf),
                                      static_cast<const uint8_t*>(x.v_sf), o, dm.H, dm.Hkv, dm.Lq, dm.Lkv, causal,
                                      work, part, so, kWaitLimitNs);

@@ -38,7 +38,6 @@
 namespace sa {
 namespace {
 
-constexpr int kMaxDevices = 64;
 constexpr int kSlots = 3;
 
 // Two copy streams and the events that order the slots, per device; created
@@ -47,6 +46,11 @@ struct HostPipe {
   bool ready = false;
   cudaStream_t cin = nullptr, cout = nullptr;
   cudaEvent_t start = nullptr, in[kSlots] = {}, comp[kSlots] = {}, out[kSlots] = {};
+  // join: the end of each copy stream's work of a call, for the caller's
+  // stream to wait on; last_comp: the last compute of a call on the caller's
+  // stream (an overlapped call's compute, and so its use of the split-KV
+  // region that all slots share, starts after it)
+  cudaEvent_t join_in = nullptr, join_out = nullptr, last_comp = nullptr;
   // the slots of the last call (its workspace and slot size): the slot events
   // order a call after the previous one only when both cut the same memory
   // into the same slots
@@ -65,7 +69,10 @@ HostPipe* pipe_for_current_device() {
     const unsigned ef = cudaEventDisableTiming;
     if (cudaStreamCreateWithFlags(&p.cin, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&p.cout, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&p.start, ef) != cudaSuccess)
+        cudaEventCreateWithFlags(&p.start, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.join_in, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.join_out, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.last_comp, ef) != cudaSuccess)
       return nullptr;
     for (int i = 0; i < kSlots; ++i)
       if (cudaEventCreateWithFlags(&p.in[i], ef) != cudaSuccess ||
@@ -188,6 +195,17 @@ sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,
   uint8_t* split_ws = ws + lay.split;
   bool ok = true;
   auto cu = [&ok](cudaError_t e) { ok = ok && e == cudaSuccess; };
+  // Every exit after the first enqueue makes the caller's stream wait for all
+  // the work this call put on the two copy streams, so that synchronising the
+  // stream means every copy has finished -- also after an error (the copies
+  // already enqueued still read q, k, v and write o and the workspace).
+  auto join = [&]() {
+    bool j = cudaEventRecord(p->join_in, p->cin) == cudaSuccess;
+    j = cudaEventRecord(p->join_out, p->cout) == cudaSuccess && j;
+    j = cudaStreamWaitEvent(s, p->join_in, 0) == cudaSuccess && j;
+    j = cudaStreamWaitEvent(s, p->join_out, 0) == cudaSuccess && j;
+    return j;
+  };
 
   // Both copy streams start after the work already on the caller's stream
   // (an earlier call on the same workspace, for one) -- with SA_HOST_OVERLAP
@@ -205,6 +223,10 @@ sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,
   cu(cudaEventRecord(p->start, s));
   if (!overlap) cu(cudaStreamWaitEvent(p->cin, p->start, 0));
   cu(cudaStreamWaitEvent(p->cout, p->start, 0));
+  // an overlapped call may be on another stream than the previous one: its
+  // compute waits for the previous call's (the split-KV region is shared by
+  // all slots; the slot events cover the rest)
+  if (overlap) cu(cudaStreamWaitEvent(s, p->last_comp, 0));
   const int nchunks = (int)plan.size();
   size_t p0 = 0;
   for (int c = 0; ok && c < nchunks; ++c) {
@@ -236,7 +258,10 @@ sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,
       st = nsplit > 1 ? sa_attn_fwd_ws(aq, ak, av, dout, 1, nc * G, nc, L, d, causal, dev_mode, nsplit, split_ws,
                                        lay.split_bytes, stream)
                       : sa_attn_fwd(aq, ak, av, dout, 1, nc * G, nc, L, d, causal, dev_mode, stream);
-    if (st != SA_OK) return st;
+    if (st != SA_OK) {
+      join();
+      return st;
+    }
     cu(cudaEventRecord(p->comp[slot], s));
     // copy out
     cu(cudaStreamWaitEvent(p->cout, p->comp[slot], 0));
@@ -244,11 +269,11 @@ sa_status sa_attn_fwd_host(const void* q, const void* k, const void* v, void* o,
     cu(cudaEventRecord(p->out[slot], p->cout));
     p0 += nc;
   }
-  // the caller's stream completes after the last copy out (the copy-out
-  // stream is in order, so its last event covers every chunk)
-  const int last = (nchunks - 1) % kSlots;
-  cu(cudaStreamWaitEvent(s, p->out[last], 0));
-  if (!ok) return SA_ERR_CUDA;
+  // the caller's stream completes after the last copy out (and after every
+  // copy this call enqueued, also when a step above failed)
+  cu(cudaEventRecord(p->last_comp, s));
+  const bool joined = join();
+  if (!ok || !joined) return SA_ERR_CUDA;
   p->last_ws = workspace;
   p->last_slot_bytes = lay.slot.bytes;
   return SA_OK;

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/sa.h"
 
 namespace sa {
@@ -29,15 +31,33 @@ inline Strides layout_strides(bool blhd, int heads, int L, int d) {
               : Strides{(long long)heads * L * d, (long long)L * d, d};
 }
 
+// Per-device once-only set-up (kernel attributes such as the dynamic
+// shared-memory size are properties of a function on one device): run(), a
+// callable returning cudaError_t, on the first call for the current device;
+// later calls on that device return cudaSuccess.  Concurrent first calls may
+// both run it (the set-up is idempotent).
+constexpr int kMaxDevices = 64;
+template <typename F>
+inline cudaError_t once_per_device(std::atomic<bool> (&done)[kMaxDevices], F run) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = run();
+  if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
+  return e;
+}
+
 // Number of SMs of the current device (cached per device; 0 if unknown).
 inline int device_sm_count() {
-  static int cache[64] = {};
+  static std::atomic<int> cache[kMaxDevices] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  if (dev < kMaxDevices && cache[dev].load(std::memory_order_relaxed) > 0) return cache[dev].load();
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (dev < 64) cache[dev] = n;
+  if (dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -64,6 +84,13 @@ inline cudaLaunchConfig_t pdl_launch_config(dim3 grid, dim3 block, size_t smem, 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // quant.cu
+// The smooth-K mean is summed in chunks of kMeanChunk tokens (one float32
+// partial sum per chunk and channel, then the chunk sums in order); a problem
+// needs kmean_partial_floats(dm) floats of partial sums.
+constexpr int kMeanChunk = 128;
+inline size_t kmean_partial_floats(const Dims& dm) {
+  return (size_t)dm.B * dm.Hkv * (size_t)(padded_len(dm.Lkv) / kMeanChunk) * (size_t)dm.d;
+}
 // tq / tk: bf16 Q and K as [rows][d], boxes of 64 channels x 128 rows, 128B swizzle.
 cudaError_t launch_quantize(const void* q, const void* k, const void* v, const Dims& dm, bool blhd,
                             const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t s);

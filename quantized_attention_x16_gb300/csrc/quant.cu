@@ -22,7 +22,6 @@ namespace sa {
 
 namespace {
 
-constexpr int kMeanChunk = 128;   // tokens per sequential partial sum
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -454,12 +453,11 @@ cudaError_t launch_quantize_impl(const void* q, const void* k, const void* v, co
   a.nclu_v = (a.nblk_v + kMeanCluster - 1) / kMeanCluster;
   a.wait_ns = kWaitLimitNs;
   constexpr int kSmem = 2 * T::kSmemBytes + 1024;        // two stages + alignment slack
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(quant_qk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<bool> attr_done[kMaxDevices];   // kernel attributes are per device
+  cudaError_t ea = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(quant_qk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  });
+  if (ea != cudaSuccess) return ea;
   const int ntiles = a.ntile_k + a.ntile_q;
   const int sms = device_sm_count() > 0 ? device_sm_count() : 148;
   const int grid = ntiles < 3 * sms ? ntiles : 3 * sms;    // three resident CTAs per SM
@@ -504,7 +502,6 @@ namespace {
 
 static __device__ __align__(256) float g_quant_scratch[kStaticScratchFloats];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 float* g_scratch_addr[kMaxDevices] = {};
 
@@ -529,8 +526,8 @@ cudaError_t static_scratch_address(float** out) {
 cudaError_t launch_quantize_static_scratch(const void* q, const void* k, const void* v, const Dims& dm,
                                            const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk,
                                            cudaStream_t s) {
-  const size_t need = (size_t)dm.B * dm.Hkv * (padded_len(dm.Lkv) / kMeanChunk) * dm.d;
-  if (need > kStaticScratchFloats) return cudaErrorInvalidValue;
+  // (sa_quantize_static_scratch has checked kmean_partial_floats(dm) <=
+  // kStaticScratchFloats before calling)
   float* part = nullptr;
   cudaError_t e = static_scratch_address(&part);
   if (e != cudaSuccess) return e;

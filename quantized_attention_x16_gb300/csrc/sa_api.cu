@@ -103,7 +103,7 @@ void blob_sizes(const Dims& dm, size_t sz[8]) {
   sz[4] = nk * (d / 2);                                        // v_codes (transposed)
   sz[5] = (size_t)dm.B * dm.Hkv * (Lkvp / 64) * 512;           // v_sf
   sz[6] = (size_t)dm.B * dm.Hkv * d * sizeof(float);           // k_mean
-  sz[7] = (size_t)dm.B * dm.Hkv * (Lkvp / 128) * d * sizeof(float);   // K-mean partial sums
+  sz[7] = kmean_partial_floats(dm) * sizeof(float);   // K-mean partial sums
 }
 
 __global__ void wait_selftest_kernel(uint64_t limit_ns) {
@@ -223,7 +223,7 @@ sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v
   const sa_status st = check_dims(dm);
   if (st != SA_OK) return st;
   if (empty_problem(dm)) return SA_OK;
-  if ((size_t)B * Hkv * (padded_len(L) / 128) * d > (size_t)SA_STATIC_SCRATCH_FLOATS) return SA_ERR_UNSUPPORTED;
+  if (kmean_partial_floats(dm) > kStaticScratchFloats) return SA_ERR_UNSUPPORTED;   // before any pointer check
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !out || !aligned16(out->q_codes) ||
       !aligned16(out->q_sf) || !aligned16(out->k_codes) || !aligned16(out->k_sf) || !aligned16(out->v_codes) ||
       !aligned16(out->v_sf) || !aligned16(out->k_mean))
