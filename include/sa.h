@@ -354,6 +354,34 @@ sa_status sa_last_device_error(void);
  */
 sa_status sa_selftest_wait_timeout(uint64_t limit_ns, sa_stream_t stream);
 
+/*
+ * Self-test of the score step of the NVFP4 attention kernel (test support; the
+ * pages describe no such call): S = Q^ K^'^T for query tile qt (rows
+ * 128*qt .. 128*qt + 127, padded) of head (b, h) and key tile kt (keys
+ * 128*kt .. 128*kt + 127) of its kv head h / (H / Hkv), computed with the
+ * kernel's own block-scaled FP4 MMAs ("GPU kernel porting with AI agents",
+ * section "Sage Attention 3": Q and K' in 1x16 NVFP4 groups) and written as
+ * float32 [128][128] (row = query, column = key, unscaled: no 1/sqrt(d)) to
+ * the device buffer s_out.  x: operands from sa_quantize for `shape`
+ * (Lq and Lkv as there).  Lets a test measure how far the tensor core's
+ * float32 scores lie from the exact products of the dequantised operands.
+ * SA_ERR_INVALID_ARG for indices outside the padded tiles, null or
+ * misaligned pointers, or an empty problem.  Asynchronous on `stream`.
+ */
+sa_status sa_selftest_nvfp4_score_tile(const sa_fp4_qkv* x, const sa_shape* shape, int b, int h, int qt, int kt,
+                                       float* s_out, sa_stream_t stream);
+
+/*
+ * Self-test of the exponent path of the attention kernels' softmax (test
+ * support; the pages describe no such call): ex2_out[i] = 2^x[i] and
+ * lg2_out[i] = log2(y[i]) computed with the same approximate hardware
+ * instructions the softmax uses for P and for the e4m3 group-scale fold, so
+ * that a test can measure their error.  x, y, ex2_out, lg2_out: device
+ * buffers of n floats.  Asynchronous on `stream`.
+ */
+sa_status sa_selftest_exp_path(const float* x, const float* y, int n, float* ex2_out, float* lg2_out,
+                                sa_stream_t stream);
+
 /* Library version string. */
 const char* sa_version(void);
 

@@ -37,7 +37,8 @@ EXPORTS = ("sa_fp4_qkv_bytes", "sa_fp4_qkv_from_blob", "sa_quantize", "sa_quanti
            "sa_fp4_qkv_bytes_s", "sa_fp4_qkv_from_blob_s", "sa_quantize_s", "sa_attn_fwd_workspace_bytes_s",
            "sa_attn_fwd_s",
            "sa_attn_fwd_host_workspace_bytes", "sa_attn_fwd_host",
-           "sa_status_string", "sa_last_device_error", "sa_selftest_wait_timeout", "sa_version")
+           "sa_status_string", "sa_last_device_error", "sa_selftest_wait_timeout", "sa_selftest_nvfp4_score_tile",
+           "sa_selftest_exp_path", "sa_version")
 SA_STATIC_SCRATCH_FLOATS = 1 << 20
 
 
@@ -95,6 +96,10 @@ def _load():
     lib.sa_last_device_error.restype = i
     lib.sa_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.sa_selftest_wait_timeout.restype = i
+    lib.sa_selftest_nvfp4_score_tile.argtypes = [ctypes.POINTER(SaFp4Qkv), shp, i, i, i, i, vp, vp]
+    lib.sa_selftest_nvfp4_score_tile.restype = i
+    lib.sa_selftest_exp_path.argtypes = [vp, vp, i, vp, vp, vp]
+    lib.sa_selftest_exp_path.restype = i
     lib.sa_version.argtypes = []
     lib.sa_version.restype = ctypes.c_char_p
     return lib
@@ -357,3 +362,31 @@ def sa_last_device_error():
 
 def sa_selftest_wait_timeout(limit_ns, stream=None):
     _check(lib.sa_selftest_wait_timeout(int(limit_ns), _stream(stream)), "sa_selftest_wait_timeout")
+
+
+def sa_selftest_exp_path(x, y, stream=None):
+    """(2^x, log2 y) through the softmax's approximate instructions; x, y
+    float32 CUDA tensors of one size (test support)."""
+    import torch
+    if not (x.is_cuda and y.is_cuda and x.dtype == torch.float32 and y.dtype == torch.float32 and x.numel() == y.numel()
+            and x.is_contiguous() and y.is_contiguous()):
+        raise ValueError("x, y must be contiguous float32 CUDA tensors of one size")
+    e, l = torch.empty_like(x), torch.empty_like(y)
+    _check(lib.sa_selftest_exp_path(_ptr(x), _ptr(y), x.numel(), _ptr(e), _ptr(l), _stream(stream)),
+           "sa_selftest_exp_path")
+    return e, l
+
+
+def sa_selftest_nvfp4_score_tile(f, b, h, qt, kt, stream=None):
+    """The NVFP4 attention kernel's score tile S = Q^ K^'^T (float32 [128, 128],
+    unscaled) for query tile qt of head (b, h) and key tile kt, from the
+    operands of an FP4QKV (test support)."""
+    import torch
+    if not isinstance(f, FP4QKV):
+        raise ValueError("f must be an FP4QKV from sa_quantize")
+    B, H, Hkv, L, d = f.dims
+    out = torch.empty((128, 128), dtype=torch.float32, device=f.blob.device)
+    shape = SaShape(B, H, Hkv, L, f.Lkv, d)
+    _check(lib.sa_selftest_nvfp4_score_tile(ctypes.byref(f.struct), ctypes.byref(shape), int(b), int(h), int(qt),
+                                            int(kt), _ptr(out), _stream(stream)), "sa_selftest_nvfp4_score_tile")
+    return out

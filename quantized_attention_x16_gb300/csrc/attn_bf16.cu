@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = (warp % 4) * 32 + lane;                      // row within the query tile
     const uint32_t lane_addr = tbase + (((warp % 4) * 32) << 16);
     const int qt = qt0 + q;
-    const float c = 1.4426950408889634f * rsqrtf((float)D);
+    const float c = softmax_scale_log2<D>();
     const uint32_t ocol = C::kColO0 + q * D;
     float m_use = -INFINITY, l = 0.f;
     bool ok = true;

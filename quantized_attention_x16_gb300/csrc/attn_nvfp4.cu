@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp / 4;
     const int r = (warp % 4) * 32 + lane;
     const uint32_t lane_addr = tbase + (((warp % 4) * 32) << 16);
-    const float c = 1.4426950408889634f * rsqrtf((float)D);
+    const float c = softmax_scale_log2<D>();
     uint8_t* prow0 = smem + C::kOffP + 2 * q * C::kPBytes + r * 64;
     uint8_t* psf0 = smem + C::kOffPSf + 2 * q * C::kPSfBytes + (r % 32) * 16 + (r / 32) * 4;
     const uint32_t ocol = C::kColO0 + q * D;
@@ -676,7 +676,143 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   return e;
 }
 
+// Test support: the FP32 score tile S = Q^ K^'^T of one (query tile, key
+// tile) from the attention kernel's own S step -- the same tensor maps,
+// shared-memory descriptors, scale-factor copies and block-scaled MMAs -- read
+// back from tensor memory and written row-major [128][128] to `out`.  One CTA
+// of 128 threads (warp w reads lanes 32w..32w+31); every wait bounded.
+template <int D>
+__global__ void __launch_bounds__(128, 1)
+    nvfp4_score_tile_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                            const uint8_t* __restrict__ q_sf, const uint8_t* __restrict__ k_sf, int qrow, int krow,
+                            long long qsf_blk, long long ksf_blk, float* __restrict__ out, uint64_t wait_ns) {
+  using C = CfgF4<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sq = smem;
+  uint8_t* sk = smem + C::kQBytes;
+  uint8_t* sqsf = sk + C::kKBytes;
+  uint8_t* sksf = sqsf + C::kQSfBytes;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sksf + C::kKSfBytes);   // [0] loads, [1] MMA
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    mbar_init(bar + 1, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  constexpr uint32_t kColSfQ = 128, kColSfK = 128 + 4 * (D / 64);
+  bool ok = true;
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(bar, C::kQBytes + C::kKBytes + C::kQSfBytes + C::kKSfBytes);
+    tma_load_2d(sq, &tmap_q, bar, 0, qrow);
+    tma_load_2d(sk, &tmap_k, bar, 0, krow);
+    bulk_load(sqsf, q_sf + qsf_blk * C::kQSfBytes, C::kQSfBytes, bar);
+    bulk_load(sksf, k_sf + ksf_blk * C::kKSfBytes, C::kKSfBytes, bar);
+  }
+  if (warp == 0) {
+    ok = mbar_wait_warp(bar, 0, abort_flag, wait_ns);
+    if (ok) {
+      tc_fence_after();
+      if (elect_one()) {
+        const uint32_t sb = smem_u32(smem);
+        copy_sf(tbase + kColSfQ, smem_u32(sqsf), D / 64);
+        copy_sf(tbase + kColSfK, smem_u32(sksf), D / 64);
+#pragma unroll
+        for (int kk = 0; kk < D / 64; ++kk)
+          mma_nvf4(tbase, desc_qk(sb + kk * 32, C::kQKSbo, C::kQKSwz),
+                   desc_qk(sb + C::kQBytes + kk * 32, C::kQKSbo, C::kQKSwz), C::kIdescS, tbase + kColSfQ + 4 * kk,
+                   tbase + kColSfK + 4 * kk, kk > 0 ? 1u : 0u);
+        tc_commit(bar + 1);
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  ok = mbar_wait_warp(bar + 1, 0, abort_flag, wait_ns);
+  if (ok) {
+    tc_fence_after();
+    const uint32_t lane_addr = tbase + ((warp * 32) << 16);
+    const int r = warp * 32 + lane;
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+      uint32_t s[32];
+      tmem_ld32(lane_addr + 32 * cc, s);
+      tmem_ld_wait(s);
+      float4* dst = reinterpret_cast<float4*>(out + (long long)r * 128 + 32 * cc);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        dst[i] = make_float4(__uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1]), __uint_as_float(s[4 * i + 2]),
+                             __uint_as_float(s[4 * i + 3]));
+    }
+  } else {
+    // the MMA may still be in flight if only the wait gave up: let it land
+    // before the tensor memory goes away
+    mbar_wait_drain(bar + 1, 0, wait_ns);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 256);
+  }
+}
+
+// Test support: the exponent path's builtins as the softmax uses them,
+// ex2_out[i] = ex2_approx(x[i]), lg2_out[i] = lg2_approx(y[i]).
+__global__ void exp_path_selftest_kernel(const float* __restrict__ x, const float* __restrict__ y, int n,
+                                         float* __restrict__ ex2_out, float* __restrict__ lg2_out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) {
+    ex2_out[i] = ex2_approx(x[i]);
+    lg2_out[i] = lg2_approx(y[i]);
+  }
+}
+
+template <int D>
+cudaError_t launch_score_tile(const CUtensorMap& tq, const CUtensorMap& tk, const sa_fp4_qkv& x, const Dims& dm, int b,
+                              int h, int qt, int kt, float* out, cudaStream_t s) {
+  using C = CfgF4<D>;
+  const int smem = C::kQBytes + C::kKBytes + C::kQSfBytes + C::kKSfBytes + 32 + 1024;
+  static std::atomic<bool> attr_done[kMaxDevices];
+  cudaError_t e = once_per_device(attr_done, [smem] {
+    return cudaFuncSetAttribute(nvfp4_score_tile_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (e != cudaSuccess) return e;
+  const int Lqp = padded_len(dm.Lq), Lkvp = padded_len(dm.Lkv);
+  const long long bhq = (long long)b * dm.H + h;
+  const long long bhk = (long long)b * dm.Hkv + h / (dm.H / dm.Hkv);
+  nvfp4_score_tile_kernel<D><<<1, 128, smem, s>>>(tq, tk, static_cast<const uint8_t*>(x.q_sf),
+                                                  static_cast<const uint8_t*>(x.k_sf), (int)(bhq * Lqp + qt * 128),
+                                                  (int)(bhk * Lkvp + kt * 128), bhq * (Lqp / 128) + qt,
+                                                  bhk * (Lkvp / 128) + kt, out, kWaitLimitNs);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_nvfp4_score_tile(const CUtensorMap& tq, const CUtensorMap& tk, const sa_fp4_qkv& x,
+                                    const Dims& dm, int b, int h, int qt, int kt, float* out, cudaStream_t s) {
+  return dm.d == 64 ? launch_score_tile<64>(tq, tk, x, dm, b, h, qt, kt, out, s)
+                    : launch_score_tile<128>(tq, tk, x, dm, b, h, qt, kt, out, s);
+}
+
+cudaError_t launch_exp_path_selftest(const float* x, const float* y, int n, float* ex2_out, float* lg2_out,
+                                     cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  exp_path_selftest_kernel<<<(n + 255) / 256, 256, 0, s>>>(x, y, n, ex2_out, lg2_out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_attn_nvfp4(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const sa_fp4_qkv& qkv, void* o, const Strides& so, const Dims& dm, int causal,

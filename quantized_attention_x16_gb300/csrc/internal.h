@@ -80,6 +80,14 @@ inline cudaLaunchConfig_t pdl_launch_config(dim3 grid, dim3 block, size_t smem, 
   return c;
 }
 
+// The softmax scale in base-2 units, c = log2(e) / sqrt(d), rounded once to
+// float32 (d = 64: log2(e) / 8; d = 128: log2(e) * 2^-3.5).
+template <int D>
+__host__ __device__ constexpr float softmax_scale_log2() {
+  static_assert(D == 64 || D == 128, "head dimension");
+  return static_cast<float>(1.4426950408889634074 * (D == 64 ? 0.125 : 0.088388347648318440550));
+}
+
 // Barrier-wait limit used by the attention kernels (nanoseconds).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -125,6 +133,15 @@ cudaError_t launch_attn_bf16(const CUtensorMap& tq, const CUtensorMap& tk, const
 cudaError_t launch_attn_nvfp4(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const sa_fp4_qkv& qkv, void* o, const Strides& so, const Dims& dm, int causal,
                               bool out_f32, int nsplit, const SplitOut& part, cudaStream_t s);
+// Test support: the FP32 score tile of the NVFP4 attention kernel's S step for
+// query tile qt of head (b, h) and key tile kt of its kv head, [128][128] to
+// `out` (device); tq / tk as for launch_attn_nvfp4.
+cudaError_t launch_nvfp4_score_tile(const CUtensorMap& tq, const CUtensorMap& tk, const sa_fp4_qkv& x,
+                                    const Dims& dm, int b, int h, int qt, int kt, float* out, cudaStream_t s);
+// Test support: ex2_out[i] = the softmax's exp2 of x[i], lg2_out[i] = its
+// log2 of y[i] (device buffers of n floats).
+cudaError_t launch_exp_path_selftest(const float* x, const float* y, int n, float* ex2_out, float* lg2_out,
+                                     cudaStream_t s);
 // splitkv.cu: O from the nsplit partial results of every row t < L.
 cudaError_t launch_splitkv_combine(const SplitOut& part, int nsplit, const Dims& dm, void* o, const Strides& so,
                                    bool out_f32, cudaStream_t s);

@@ -379,6 +379,41 @@ sa_status sa_last_device_error(void) {
   return e ? static_cast<sa_status>(e) : SA_OK;
 }
 
+sa_status sa_selftest_nvfp4_score_tile(const sa_fp4_qkv* x, const sa_shape* shape, int b, int h, int qt, int kt,
+                                       float* s_out, sa_stream_t stream) {
+  if (!shape || !x || !s_out) return SA_ERR_INVALID_ARG;
+  const Dims dm = dims_of(shape);
+  const sa_status st = check_dims(dm);
+  if (st != SA_OK) return st;
+  if (empty_problem(dm)) return SA_ERR_INVALID_ARG;                 // no tile to compute
+  if (b < 0 || b >= dm.B || h < 0 || h >= dm.H || qt < 0 || qt >= padded_len(dm.Lq) / 128 || kt < 0 ||
+      kt >= padded_len(dm.Lkv) / 128)
+    return SA_ERR_INVALID_ARG;
+  if (!aligned16(x->q_codes) || !aligned16(x->q_sf) || !aligned16(x->k_codes) || !aligned16(x->k_sf) ||
+      !aligned16(s_out))
+    return SA_ERR_INVALID_ARG;
+  const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const int d = dm.d;
+  const CUtensorMapSwizzle qk_swz = d == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  const int Lqp = padded_len(dm.Lq), Lkvp = padded_len(dm.Lkv);
+  CUtensorMap tq, tk;
+  if (!make_map(&tq, u8, x->q_codes, d / 2, (uint64_t)dm.B * dm.H * Lqp, 1, d / 2, 128, qk_swz) ||
+      !make_map(&tk, u8, x->k_codes, d / 2, (uint64_t)dm.B * dm.Hkv * Lkvp, 1, d / 2, 128, qk_swz))
+    return SA_ERR_CUDA;
+  return launch_nvfp4_score_tile(tq, tk, *x, dm, b, h, qt, kt, s_out, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? SA_OK
+             : SA_ERR_CUDA;
+}
+
+sa_status sa_selftest_exp_path(const float* x, const float* y, int n, float* ex2_out, float* lg2_out,
+                                sa_stream_t stream) {
+  if (n < 0 || (n > 0 && (!x || !y || !ex2_out || !lg2_out))) return SA_ERR_INVALID_ARG;
+  return launch_exp_path_selftest(x, y, n, ex2_out, lg2_out, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SA_OK
+             : SA_ERR_CUDA;
+}
+
 sa_status sa_selftest_wait_timeout(uint64_t limit_ns, sa_stream_t stream) {
   if (limit_ns == 0 || limit_ns > 10000000000ull) return SA_ERR_INVALID_ARG;
   wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns);
