@@ -13,9 +13,11 @@ every host <-> device copy inside the timed region (the library overlaps the
 copies of one chunk of (batch, kv head) pairs with the compute of the next).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-For N > 1 launch with torch.distributed.run (one rank per GPU); every rank runs
-its own independent batch (weak scaling, no collective on the data path) and
-rank 0 prints the max-over-ranks time.
+For N > 1 launch with torch.distributed.run (one rank per GPU): the one
+problem is sharded by (batch, kv head) pairs -- each rank computes a
+contiguous range of pairs with all their query heads (shard.shard_qkv), which
+needs no exchange on the data path -- and `value` is the whole problem's
+counted work over the max-over-ranks time (strong scaling).
 """
 
 import argparse
@@ -167,13 +169,22 @@ def run_ours(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = W.spec(args.workload, seed=W.spec(args.workload)["seed"] + 1000 * rank)   # independent batch per rank
+    w = W.spec(args.workload)
     B, H, Hkv, L, d = w["B"], w["H"], w["Hkv"], w["L"], w["d"]
     Lq = W.lq(w)                                   # query rows (L: keys)
     x = W.make_inputs(w)
-    q, k, v = (x[n].to(dev) for n in "qkv")
-    fl = W.flops(w)
+    fl = W.flops(w)                                # the whole problem's counted work
     causal = w["causal"]
+    # this rank's share: a contiguous range of (batch, kv head) pairs with all
+    # their query heads, as a problem of its own (B = 1, H = n*G, Hkv = n)
+    p0, p1 = shard.pair_range(B, Hkv, world, rank)
+    if world > 1:
+        qs, ks, vs = shard.shard_qkv(x["q"], x["k"], x["v"], world, rank)
+        x = dict(q=qs.contiguous(), k=ks.contiguous(), v=vs.contiguous())
+        B, H, Hkv = 1, (p1 - p0) * (H // Hkv), p1 - p0
+    if p1 == p0:
+        raise SystemExit(f"rank {rank}: no (batch, kv head) pair to compute ({w['B'] * w['Hkv']} pairs, {world} ranks)")
+    q, k, v = (x[n].to(dev) for n in "qkv")
     # A one-token query (decode) against a GQA cache: the G query heads of a
     # kv head read the same keys and values, and with one row per head no mask
     # tells them apart (under the bottom-right causal mask the row sees every
@@ -250,7 +261,11 @@ def run_ours(args, rank, world, local_rank):
     tp = [a[0].elapsed_time(a[1]) * 1e-3 for a in evp]
     mean = lambda xs: sum(xs) / len(xs)   # noqa: E731
     t_q, t_4, t_16, t_path = mean(tq), mean(t4), mean(t16), mean(tp)
-    # the slowest rank sets each time (no-ops at N = 1)
+    # rank 0's own launches for the per-kernel rooflines (its share of the problem)
+    w_local = dict(w, B=B, H=H, Hkv=Hkv)
+    fl_local = W.flops(w_local)
+    lq_, l4_, l16_ = t_q, t_4, t_16
+    # the slowest rank sets each time of the whole problem (no-ops at N = 1)
     t_path, t_q, t_4, t_16 = (shard.max_over_ranks(t, device=dev) for t in (t_path, t_q, t_4, t_16))
     assert sa.sa_last_device_error() == sa.SA_OK
 
@@ -285,7 +300,7 @@ def run_ours(args, rank, world, local_rank):
         e1.record()
         torch.cuda.synchronize()
         t_e2e = shard.max_over_ranks(e0.elapsed_time(e1) * 1e-3 / args.steps, device=dev)
-        e2e = {"value": world * fl / t_e2e / 1e12, "unit": "TOPS", "h2d_bytes_per_step": h2d,
+        e2e = {"value": fl / t_e2e / 1e12, "unit": "TOPS", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
                "api": "sa_attn_fwd_host (nvfp4, SA_HOST_OVERLAP)"}
 
@@ -293,10 +308,10 @@ def run_ours(args, rank, world, local_rank):
         return
     pk = peaks()
     nvfp4_peak = pk["bf16"] * NVFP4_OVER_BF16
-    a4 = fl / t_4 / 1e12
-    a16 = fl / t_16 / 1e12
-    qbytes = quant_bytes(w)
-    attn_bytes = attn_nvfp4_bytes(w)
+    a4 = fl_local / l4_ / 1e12                     # rank 0's launch: its share over its own time
+    a16 = fl_local / l16_ / 1e12
+    qbytes = quant_bytes(w_local)
+    attn_bytes = attn_nvfp4_bytes(w_local)
     clocks = clk.summary()
     prof = load_profile_traffic()
     cpu = None
@@ -306,14 +321,14 @@ def run_ours(args, rank, world, local_rank):
                "sample": cpu_desc, "seconds": cpu_dt}
     line = {
         "metric": METRIC,
-        "value": world * fl / t_path / 1e12,
+        "value": fl / t_path / 1e12,
         "unit": "TOPS",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": t_path * 1e3,
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong",
         "vs_baseline": None,
         "dtype": "nvfp4 (e2m1 x e4m3-scaled, fp32 accumulate); bf16 path alongside",
         "data": "synthetic (seeded torch.Generator, bf16)",
@@ -322,10 +337,12 @@ def run_ours(args, rank, world, local_rank):
                    "gqa_fold": ("Q [B, H, 1, d] passed as [B, Hkv, H/Hkv, d]: the query heads of a kv head as "
                                 "its query rows") if fold else None,
                    "l2": "flushed by a 256 MB write before every step",
-                   "value_def": "4*B*H*L^2*d (halved for causal; with Lq != L, 4*B*H*d x the (query, key) "
-                                "pairs the mask leaves) / (sa_quantize + NVFP4 sa_attn_fwd, back to back in "
-                                "one CUDA-event interval) per GPU, summed over GPUs",
-                   "parallelism": f"independent batch per GPU ({world} GPU)",
+                   "value_def": "4*B*H*L^2*d of the whole problem (halved for causal; with Lq != L, 4*B*H*d x "
+                                "the (query, key) pairs the mask leaves) / the slowest rank's (sa_quantize + "
+                                "NVFP4 sa_attn_fwd, back to back in one CUDA-event interval)",
+                   "parallelism": (f"(batch, kv head) pairs sharded over {world} GPUs, {p1 - p0} of "
+                                   f"{w['B'] * w['Hkv']} on rank 0, no collective on the data path")
+                                  if world > 1 else "one GPU, the whole problem",
                    "work_split": "library choice (sa_attn_fwd_ws, nsplit=0): nvfp4 "
                                  + ("stream-K/split" if ws4 > 0 else "one unit per CTA") + ", bf16 "
                                  + ("split-KV" if ws16 > 0 else "one unit per CTA")},
@@ -333,7 +350,7 @@ def run_ours(args, rank, world, local_rank):
             "nvfp4_attn_only_tops": a4,
             "nvfp4_attn_us": t_4 * 1e6,
             "quantize_us": t_q * 1e6,
-            "quantize_gbs": qbytes / t_q / 1e9,
+            "quantize_gbs": qbytes / lq_ / 1e9,
             "path_us": t_path * 1e6,
             "quantize_plus_attn_timed_apart_us": (t_q + t_4) * 1e6,
             "nvfp4_end_to_end_tops": fl / t_path / 1e12,
@@ -349,13 +366,13 @@ def run_ours(args, rank, world, local_rank):
         "roofline_bf16": {"kernel": f"attn_bf16_kernel<{d}>", "bound": "tensor", "achieved": a16, "peak": pk["bf16"],
                           "unit": "TFLOP/s", "frac": a16 / pk["bf16"], "traffic": prof.get("attn_bf16"),
                           "peak_src": f"{pk['src']} bf16 burst"},
-        "roofline_quantize": {"kernel": "sa_quantize (2 kernels)", "bound": "hbm", "achieved": qbytes / t_q / 1e9,
-                              "peak": pk["hbm"], "unit": "GB/s", "frac": qbytes / t_q / 1e9 / pk["hbm"],
+        "roofline_quantize": {"kernel": "sa_quantize (2 kernels)", "bound": "hbm", "achieved": qbytes / lq_ / 1e9,
+                              "peak": pk["hbm"], "unit": "GB/s", "frac": qbytes / lq_ / 1e9 / pk["hbm"],
                               "traffic": None, "algorithmic_bytes": qbytes,
                               "traffic_kernels": {k: prof.get(k) for k in ("quant_v_mean_kernel", "quant_qk_kernel")}},
         "roofline_hbm_attn": {"kernel": f"attn_nvfp4_kernel<{d}>", "bound": "hbm (context: the bound of few-query "
-                              "shapes such as decode)", "achieved": attn_bytes / t_4 / 1e9, "peak": pk["hbm"],
-                              "unit": "GB/s", "frac": attn_bytes / t_4 / 1e9 / pk["hbm"],
+                              "shapes such as decode)", "achieved": attn_bytes / l4_ / 1e9, "peak": pk["hbm"],
+                              "unit": "GB/s", "frac": attn_bytes / l4_ / 1e9 / pk["hbm"],
                               "algorithmic_bytes": attn_bytes},
         "cpu_baseline": cpu,
         "e2e": e2e if e2e is not None else {"value": None, "unit": "TOPS", "h2d_bytes_per_step": 0,

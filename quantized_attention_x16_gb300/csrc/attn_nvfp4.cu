@@ -113,21 +113,29 @@ struct BarsF4 {
   uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *s_free, *p_full, *o_done, *drain;
 };
 
-// Descriptors are built at each use from a 32-bit shared address.  (Kernels
-// that kept precomputed 64-bit descriptors in registers and offset them were
-// observed to feed the first MMA of a CTA an all-zero A descriptor -- it read
-// the reserved head of the shared window -- while building them in place, as
-// here, gave exact results; the cause was not visible from the source.)
+// Shared-memory matrix descriptors: each issuing warp builds a base
+// descriptor per operand region once, after its register reallocation, and
+// adds a byte offset per use (the start-address field is the address / 16;
+// every offset here is a multiple of 16) -- the scheme of the BF16 kernel.
+// (An earlier build that issued its MMAs from a divergent single-lane branch
+// fed the first MMA of every CTA an all-zero A descriptor with this scheme;
+// since the issuing warps run converged and issue from an elected lane, the
+// precomputed descriptors give exact results, which the one-key-tile-per-CTA
+// parity test checks on every row.)
 __device__ __forceinline__ uint64_t desc_qk(uint32_t saddr, uint32_t sbo, uint32_t swz) {
   return sdesc(saddr, 16, sbo, swz);
 }
 __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) { return sdesc(saddr, 0, 128, kSwizzleNone); }
+__device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
 
 // Copies `nblk` consecutive 512-byte scale blocks at shared address `saddr` to
 // tensor memory columns [col, col + 4*nblk), replicated across the four lane
 // quarters.
 __device__ __forceinline__ void copy_sf(uint32_t tcol, uint32_t saddr, int nblk) {
   for (int i = 0; i < nblk; ++i) tmem_cp_32x128b_warpx4(tcol + 4 * i, desc_sf(saddr + 512 * i));
+}
+__device__ __forceinline__ void copy_sf_d(uint32_t tcol, uint64_t d0, uint32_t off, int nblk) {
+  for (int i = 0; i < nblk; ++i) tmem_cp_32x128b_warpx4(tcol + 4 * i, dadd(d0, off + 512 * i));
 }
 
 template <int D, bool OUT32>
@@ -281,6 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool leader = elect_one();
       const uint32_t sb = smem_u32(smem);
       const uint32_t tS = tbase + C::kColS;
+      const uint64_t dQ0 = desc_qk(sb + C::kOffQ, C::kQKSbo, C::kQKSwz);
+      const uint64_t dK0 = desc_qk(sb + C::kOffK, C::kQKSbo, C::kQKSwz);
+      const uint64_t dSf0 = desc_sf(sb);
       UnitIter it;
       unit_iter_init(work, it);
       AttnUnitRef u;
@@ -304,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (leader)
             for (int q = 0; q < u.nq; ++q)
-              copy_sf(tbase + C::kColSfQ + 16 * qb + 8 * q, sb + C::kOffQSf + (2 * qb + q) * C::kQSfBytes, D / 64);
+              copy_sf_d(tbase + C::kColSfQ + 16 * qb + 8 * q, dSf0, C::kOffQSf + (2 * qb + q) * C::kQSfBytes, D / 64);
           __syncwarp();
         }
         for (int j = 0; ok && j < nt; ++j, ++gk) {
@@ -315,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t sfk = tbase + C::kColSfK + 8 * (gk & 1);
-          if (leader) copy_sf(sfk, sb + C::kOffKSf + s * C::kKSfBytes, D / 64);
+          if (leader) copy_sf_d(sfk, dSf0, C::kOffKSf + s * C::kKSfBytes, D / 64);
           __syncwarp();
           for (int q = 0; ok && q < 2; ++q) {
             if (j >= (q ? u.n[1] : u.n[0])) continue;
@@ -326,8 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) {
 #pragma unroll
               for (int kk = 0; kk < D / 64; ++kk)
-                mma_nvf4(tS, desc_qk(sb + C::kOffQ + (2 * qb + q) * C::kQBytes + kk * 32, C::kQKSbo, C::kQKSwz),
-                         desc_qk(sb + C::kOffK + s * C::kKBytes + kk * 32, C::kQKSbo, C::kQKSwz), C::kIdescS,
+                mma_nvf4(tS, dadd(dQ0, (2 * qb + q) * C::kQBytes + kk * 32), dadd(dK0, s * C::kKBytes + kk * 32),
+                         C::kIdescS,
                          sfq + 4 * kk, sfk + 4 * kk, kk > 0 ? 1u : 0u);
               tc_commit(bars.s_full + q);
             }
@@ -359,6 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // before they release that P^.
       const bool leader = elect_one();
       const uint32_t sb = smem_u32(smem);
+      const uint64_t dP0 = desc_qk(sb + C::kOffP, 512, kSwizzle64B);
+      const uint64_t dV0 = desc_qk(sb + C::kOffV, 512, kSwizzle64B);
+      const uint64_t dSf0 = desc_sf(sb);
       UnitIter it;
       unit_iter_init(work, it);
       AttnUnitRef u;
@@ -373,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t sfv = tbase + C::kColSfV + 8 * (gk & 1);
-          if (leader) copy_sf(sfv, sb + C::kOffVSf + s * C::kVSfBytes, 2);
+          if (leader) copy_sf_d(sfv, dSf0, C::kOffVSf + s * C::kVSfBytes, 2);
           __syncwarp();
           for (int q = 0; ok && q < 2; ++q) {
             if (j >= (q ? u.n[1] : u.n[0])) continue;
@@ -384,11 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tO = tbase + C::kColO0 + q * D;
             if (leader) {
               const int pb = 2 * q + (cp[q] & 1);            // P^ buffer of this tile
-              copy_sf(sfp, sb + C::kOffPSf + pb * C::kPSfBytes, 2);
+              copy_sf_d(sfp, dSf0, C::kOffPSf + pb * C::kPSfBytes, 2);
 #pragma unroll
               for (int kk = 0; kk < BN / 64; ++kk)
-                mma_nvf4(tO, desc_qk(sb + C::kOffP + pb * C::kPBytes + kk * 32, 512, kSwizzle64B),
-                         desc_qk(sb + C::kOffV + s * C::kVBytes + kk * 32, 512, kSwizzle64B), C::kIdescPV,
+                mma_nvf4(tO, dadd(dP0, pb * C::kPBytes + kk * 32), dadd(dV0, s * C::kVBytes + kk * 32), C::kIdescPV,
                          sfp + 4 * kk, sfv + 4 * kk, (j > 0 || kk > 0) ? 1u : 0u);
               tc_commit(bars.o_done + q);
             }

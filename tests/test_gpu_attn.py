@@ -203,6 +203,29 @@ def test_attention_full_size_sampled_rows(sa, name, mode):
     check(o, x, w["causal"], heads, rows, mode, o32, label=f"{name} (stream-K cut pairs: {ncut})")
 
 
+# Every CTA computing exactly one key tile: the first S (and P.V) MMA of each
+# CTA is its only one, so a wrong operand descriptor on a CTA's first MMA
+# would show on every row.  One unit per CTA (L = 128, a single query and key
+# tile per head) and split-KV shares of one key tile.
+FIRST_TILE = [
+    (dict(W.spec("llm_prefill"), B=2, H=32, Hkv=32, L=128, seed=71), None),
+    (dict(W.spec("causal_gqa"), B=1, H=48, Hkv=16, L=100, d=64, seed=72), None),
+    (dict(W.spec("llm_prefill"), B=1, H=4, Hkv=4, L=512, seed=73), 4),
+    (dict(W.spec("dit_video"), B=1, H=4, Hkv=2, L=384, d=64, seed=74), 3),
+]
+
+
+@pytest.mark.parametrize("mode", ["bf16", "nvfp4"])
+@pytest.mark.parametrize("case", FIRST_TILE, ids=lambda c: _id(c[0]) + f"-s{c[1]}")
+def test_every_cta_single_key_tile_all_rows(sa, case, mode):
+    w, nsplit = case
+    x = W.make_inputs(w)
+    o = run_split(sa, x, w["causal"], mode, nsplit)
+    o32 = run_split(sa, x, w["causal"], mode, nsplit, torch.float32) if mode == "nvfp4" else None
+    heads = [(b, h) for b in range(w["B"]) for h in range(w["H"])]
+    check(o, x, w["causal"], heads, np.arange(w["L"]), mode, o32, label="one key tile per CTA " + _id(w))
+
+
 def test_wait_timeout_is_reported_and_context_survives(sa):
     sa.sa_selftest_wait_timeout(2_000_000)      # 2 ms wait on a barrier nothing completes
     assert sa.sa_last_device_error() == sa.SA_ERR_TIMEOUT
