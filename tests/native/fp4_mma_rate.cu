@@ -1,10 +1,11 @@
-// Throughput of the block-scaled FP4 MMA (tcgen05 kind::mxf4nvf4, M=128
-// N=128 K=64, the attention kernel's S-MMA shape and descriptors) with
-// operands resident in shared memory and the accumulator in tensor memory:
-// one CTA per SM, one thread issuing `iters` x 2 MMAs back to back.  The
-// operands and scales are zeros (the rate does not depend on the values).
-// Prints one line per run and "ok"; every wait is bounded (a timeout sets the
-// printed error flag).
+// Throughput of the block-scaled FP4 MMA (tcgen05 kind::mxf4nvf4, M=128,
+// K=64 per instruction, N = 128 -- the attention kernel's S-MMA shape and
+// descriptors -- and N = 256, the widest single-CTA shape) with operands
+// resident in shared memory and the accumulator in tensor memory: one CTA per
+// SM, one thread issuing `iters` x 2 MMAs back to back, no TMA.  The operands
+// and scales are zeros (the rate does not depend on the values).  Prints one
+// line per run and "ok"; every wait is bounded (a timeout sets the printed
+// error flag).
 #include <cstdio>
 #include <cstdint>
 #include <vector>
@@ -19,8 +20,15 @@ __device__ __forceinline__ void copy_sf(uint32_t tcol, uint32_t saddr, int nblk)
   for (int i = 0; i < nblk; ++i) tmem_cp_32x128b_warpx4(tcol + 4 * i, desc_sf(saddr + 512 * i));
 }
 
-constexpr int kSmem = 18 * 1024 + 1024;
+// A: 128 rows x 64 bytes (K = 128, two 64-deep chunks, 64B swizzle); B: N
+// rows likewise; scale blocks (512 bytes per 128 rows x 4 groups) after them.
+template <int N>
+struct Lay {
+  static constexpr int kA = 0, kB = 8192, kSfA = kB + N * 64, kSfB = kSfA + 1024, kBytes = kSfB + (N / 128) * 1024;
+};
+constexpr int kSmem = Lay<256>::kBytes + 1024;
 
+template <int N>
 __global__ void __launch_bounds__(128, 1) probe(int iters, unsigned long long* ns_out, unsigned long long* cyc_out,
                                                 int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -28,7 +36,8 @@ __global__ void __launch_bounds__(128, 1) probe(int iters, unsigned long long* n
   __shared__ uint64_t bar;
   __shared__ uint32_t slot;
   __shared__ int abort_flag;
-  for (int i = threadIdx.x; i < 18 * 1024 / 16; i += blockDim.x) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  using Y = Lay<N>;
+  for (int i = threadIdx.x; i < Y::kBytes / 16; i += blockDim.x) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     abort_flag = 0;
@@ -48,19 +57,21 @@ __global__ void __launch_bounds__(128, 1) probe(int iters, unsigned long long* n
   if (warp == 0) {
     const bool leader = elect_one();
     const uint32_t sb = smem_u32(smem);
-    const uint32_t sA = sb, sB = sb + 8192, sfA = sb + 16384, sfB = sb + 17408;
-    const uint32_t idesc = idesc_nvf4(128, 128);
+    const uint32_t sA = sb + Y::kA, sB = sb + Y::kB, sfA = sb + Y::kSfA, sfB = sb + Y::kSfB;
+    const uint32_t idesc = idesc_nvf4(128, N);
+    // tensor memory: the accumulator in columns [0, N), A scales at 256 (8
+    // columns), B scales at 272 (8 columns per 128 rows of B)
     unsigned long long t0 = 0, c0 = 0;
     if (leader) {
       copy_sf(tbase + 256, sfA, 2);
-      copy_sf(tbase + 264, sfB, 2);
+      copy_sf(tbase + 272, sfB, 2 * (N / 128));
       t0 = globaltimer_ns();
       c0 = clock64();
       for (int i = 0; i < iters; ++i) {
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk)
           mma_nvf4(tbase, desc_qk(sA + kk * 32, 512, kSwizzle64B), desc_qk(sB + kk * 32, 512, kSwizzle64B), idesc,
-                   tbase + 256 + 4 * kk, tbase + 264 + 4 * kk, (i | kk) ? 1u : 0u);
+                   tbase + 256 + 4 * kk, tbase + 272 + 4 * kk, (i | kk) ? 1u : 0u);
       }
       tc_commit(&bar);
     }
@@ -90,9 +101,12 @@ int main() {
   cudaMalloc(&cyc, sms * 8);
   cudaMalloc(&err, 4);
   cudaMemset(err, 0, 4);
-  cudaFuncSetAttribute(probe, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  cudaFuncSetAttribute(probe<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  cudaFuncSetAttribute(probe<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  for (int n : {128, 256})
   for (int iters : {2000, 20000, 40000}) {
-    probe<<<sms, 128, kSmem>>>(iters, ns, cyc, err);
+    if (n == 128) probe<128><<<sms, 128, kSmem>>>(iters, ns, cyc, err);
+    else probe<256><<<sms, 128, kSmem>>>(iters, ns, cyc, err);
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) { printf("cuda error %s\n", cudaGetErrorString(e)); return 1; }
     std::vector<unsigned long long> hn(sms), hc(sms);
@@ -102,10 +116,11 @@ int main() {
     cudaMemcpy(&he, err, 4, cudaMemcpyDeviceToHost);
     unsigned long long mx = 0, mc = 0;
     for (int i = 0; i < sms; ++i) { if (hn[i] > mx) mx = hn[i]; if (hc[i] > mc) mc = hc[i]; }
-    const double flops = (double)sms * iters * 2 * (2.0 * 128 * 128 * 64);
-    printf("iters %6d: %8.1f us  %8.1f TFLOP/s (whole GPU, slowest SM)  %.0f FLOP/clk/SM  clock %.0f MHz  err %d\n",
-           iters, mx / 1e3, flops / (mx * 1e-9) / 1e12, (double)iters * 2 * (2.0 * 128 * 128 * 64) / mc,
-           (double)mc / mx * 1e3, he);
+    const double per_mma = 2.0 * 128 * n * 64;
+    const double flops = (double)sms * iters * 2 * per_mma;
+    printf("M128 N%d K64 iters %6d: %8.1f us  %8.1f TFLOP/s (whole GPU, slowest SM)  %.0f FLOP/clk/SM  clock %.0f MHz  "
+           "err %d\n",
+           n, iters, mx / 1e3, flops / (mx * 1e-9) / 1e12, (double)iters * 2 * per_mma / mc, (double)mc / mx * 1e3, he);
   }
   printf("ok\n");
   return 0;

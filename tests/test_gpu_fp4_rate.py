@@ -1,7 +1,10 @@
-"""GPU: the rate of the block-scaled FP4 MMA in the attention kernel's own
-shape (tests/native/fp4_mma_rate.cu), the context figure beside the FP4
-roofline.  Checks that the probe runs, completes its waits, and reports a
-plausible rate; prints the figures (run with -s to see them)."""
+"""GPU: the rate of the block-scaled FP4 MMA (tests/native/fp4_mma_rate.cu):
+M128 N128 K64 (the attention kernel's S-MMA shape) and M128 N256 K64 (the
+widest single-CTA shape), operands resident in shared memory, no TMA -- the
+dense NVFP4 peak the bench's FP4 roofline takes (FLOP per clock per SM times
+the SM count and the maximum SM clock).  Checks that the probe runs,
+completes its waits, and reports a plausible rate; prints the figures (run
+with -s to see them)."""
 
 import os
 import re
@@ -28,3 +31,5 @@ def test_fp4_mma_rate(tmp_path):
     errs = [int(m) for m in re.findall(r"err (\d+)", out.stdout)]
     assert rates and all(e == 0 for e in errs)
     assert max(rates) > 2000.0, rates          # far below any working tensor pipe
+    per_clk = [float(m) for m in re.findall(r"([0-9]+) FLOP/clk/SM", out.stdout)]
+    assert max(per_clk) <= 1.05 * 32768, per_clk   # the figure the bench's FP4 roofline is built on
