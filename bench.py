@@ -36,7 +36,11 @@ import workloads as W  # noqa: E402
 
 WORKLOAD = "llm_prefill"
 METRIC = "attention fwd TOPS (4BHL^2d/time), NVFP4 and BF16 paths, 1 GB300; % of peak"
-NVFP4_OVER_BF16 = 6.0      # nominal dense FP4 : BF16 tensor ratio on GB300 (13.5 / 2.25 PFLOP/s)
+NVFP4_OVER_BF16 = 6.0      # nominal dense FP4 : BF16 tensor ratio on GB300 (13.5 / 2.25 PFLOP/s), for context
+# Dense NVFP4 rate measured on this GPU by tests/native/fp4_mma_rate.cu (the
+# block-scaled FP4 MMA, M128 x N128|N256 x K64, operands in shared memory):
+# FLOP per clock per SM; the FP4 roofline peak is this x SMs x max SM clock.
+NVFP4_FLOP_PER_CLK_SM = 32768
 # Oracle samples: the cpu_baseline (about 10-20 s of single-threaded NumPy) and
 # one step of the reference arm (about 0.2 s: quantising one head dominates).
 CPU_SAMPLE_HEADS, CPU_SAMPLE_ROWS = 16, 2048
@@ -307,7 +311,9 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     pk = peaks()
-    nvfp4_peak = pk["bf16"] * NVFP4_OVER_BF16
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    nvfp4_peak = NVFP4_FLOP_PER_CLK_SM * sms * pk["sm_max_mhz"] * 1e6 / 1e12
+    nvfp4_nominal_ratio_peak = pk["bf16"] * NVFP4_OVER_BF16
     a4 = fl_local / l4_ / 1e12                     # rank 0's launch: its share over its own time
     a16 = fl_local / l16_ / 1e12
     qbytes = quant_bytes(w_local)
@@ -361,7 +367,12 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"kernel": f"attn_nvfp4_kernel<{d}>", "bound": "tensor", "achieved": a4, "peak": nvfp4_peak,
                      "unit": "TFLOP/s", "frac": a4 / nvfp4_peak,
                      "traffic": prof.get("attn_nvfp4"),
-                     "peak_src": f"{pk['src']} bf16 burst {pk['bf16']} x nominal FP4:BF16 ratio {NVFP4_OVER_BF16}"},
+                     "peak_src": (f"measured NVFP4 MMA rate {NVFP4_FLOP_PER_CLK_SM} FLOP/clk/SM (fp4_mma_rate probe) x {sms} "
+                                  f"SMs x {pk['sm_max_mhz']} MHz max SM clock"),
+                     "peak_nominal_ratio": nvfp4_nominal_ratio_peak,
+                     "frac_of_nominal_ratio_peak": a4 / nvfp4_nominal_ratio_peak,
+                     "peak_nominal_ratio_src": f"{pk['src']} bf16 burst {pk['bf16']} x nominal FP4:BF16 ratio "
+                                               f"{NVFP4_OVER_BF16}"},
         "roofline_secondary": mufu_roofline(a4, d, pk),
         "roofline_bf16": {"kernel": f"attn_bf16_kernel<{d}>", "bound": "tensor", "achieved": a16, "peak": pk["bf16"],
                           "unit": "TFLOP/s", "frac": a16 / pk["bf16"], "traffic": prof.get("attn_bf16"),
