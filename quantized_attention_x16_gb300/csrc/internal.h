@@ -99,14 +99,14 @@ constexpr int kMeanChunk = 128;
 inline size_t kmean_partial_floats(const Dims& dm) {
   return (size_t)dm.B * dm.Hkv * (size_t)(padded_len(dm.Lkv) / kMeanChunk) * (size_t)dm.d;
 }
-// tq / tk: bf16 Q and K as [rows][d], boxes of 64 channels x 128 rows, 128B swizzle.
-cudaError_t launch_quantize(const void* q, const void* k, const void* v, const Dims& dm, bool blhd,
-                            const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t s);
+// tq / tk / tv: the bf16 Q, K and V heads (make_bf16_head_map: boxes of 64
+// channels x 128 tokens, 128B swizzle, zeros past L).
+cudaError_t launch_quantize(const Dims& dm, const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, cudaStream_t s);
 // Same kernels, K-mean partial sums in the library's fixed per-device array.
 constexpr size_t kStaticScratchFloats = SA_STATIC_SCRATCH_FLOATS;
-cudaError_t launch_quantize_static_scratch(const void* q, const void* k, const void* v, const Dims& dm,
-                                           const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk,
-                                           cudaStream_t s);
+cudaError_t launch_quantize_static_scratch(const Dims& dm, const sa_fp4_qkv& out, const CUtensorMap& tq,
+                                           const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s);
 
 // Split-KV partial results (device, caller's workspace): for split s and
 // padded row R = (b*H + h)*Lp + t, the unnormalised O row at o + (s*rows + R)*d

@@ -23,407 +23,509 @@ namespace sa {
 namespace {
 
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
+// ---------------------------------------------------------------------------
+// Group arithmetic.
+//
+// Every 1x16 group: s8 = e4m3_rne_sat(RN(max|x| / 6)), code_i =
+// e2m1_rne_sat(RN(x_i / s)) with s = decode(s8), all codes +0 when s8 == 0.
+// Neither quotient uses a divide instruction:
+//  * RN(max|x| / 6): Markstein's correction step.  With y = RN(1/6), q0 =
+//    RN(a*y) and the exact remainder r = a - q0*6 from one FMA, RN(q0 + r*y)
+//    = RN(a/6).
+//  * code_i from q = RN(x*yh + RN(x*yl)) (one product and one FMA), where
+//    yh = RD(1/s) and yl = RN((1 - s*yh) * yh): the residual 1 - s*yh is
+//    exact and >= 0, and yh + yl is 1/s to 2^-46, so q is x/s plus at most
+//    2^-45 |x/s| before its one rounding.  The code of q can differ from the
+//    code of RN(x/s) only where that rounding is decided differently next to
+//    an e2m1 boundary T, i.e. for x/s within 2^-45 of T or of a float32
+//    midpoint T +- ulp/2 beside it.  x/s = T exactly gives q = T.  A midpoint
+//    T +- ulp/2 has a 25-bit odd significand, so s (4 significant bits) times
+//    it is no float32 and x/s stays at least 2^-30 (relative) away from it.
+//    So the codes are those of the correctly rounded quotient, for bf16 x (Q,
+//    V) and float32 x (K' = K - mean) alike; this is checked on the host for
+//    every bf16 x and every e4m3 scale, and for every float32 significand
+//    near each boundary.  yl >= 0 keeps the sign of a zero x (+0 * yh + +0 =
+//    +0, -0 * yh + -0 = -0).  (yh, yl) is looked up by the scale byte in a
+//    128-entry shared-memory table.
+
+// max(|a|, |b|) per bf16 half (the result's sign bits are not used).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
-// Quantises one 1x16 group: returns the e4m3 scale byte, writes 2 words of codes.
-//
-// Both divisions are done as correctly rounded quotients without a divide
-// instruction (Markstein's correction step: with y = RN(1/b), q0 = RN(x*y)
-// and the exact remainder r = x - q0*b from one FMA, RN(q0 + r*y) = RN(x/b)).
-// This was checked exhaustively over all 2^23 significands against each
-// divisor significand 9/8 .. 15/8, which covers b = 6 (= 12/8 * 4) and every
-// e4m3 scale; exponents only shift the result.
-//  * scale: s = RN(max|x| / 6) with y = RN(1/6);
-//  * codes: the quotient is formed for the divisor -s, i.e. qn = RN(x / -s) =
-//    -RN(x / s) (rounding is symmetric), and the code sign bits are flipped
-//    afterwards (e2m1 is sign-magnitude).  This keeps the sign of a zero
-//    input: x = -0.0 gives qn = +0 and code 0x8, x = +0.0 gives code 0x0.
-__device__ __forceinline__ uint32_t quant_group16(const float* x, uint32_t* codes) {
-  float amax = 0.f;
+// Per-half maxima of |x| over n words -> (max of the low halves, max of the high halves) as floats.
+template <int N>
+__device__ __forceinline__ void absmax_halves(const uint32_t* w, float& lo, float& hi) {
+  uint32_t m[N];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  for (int i = 0; i < N; ++i) m[i] = w[i];
+#pragma unroll
+  for (int s = 1; s < N; s *= 2)
+#pragma unroll
+    for (int i = 0; i + s < N; i += 2 * s) m[i] = absmax_bf16x2(m[i], m[i + s]);
+  lo = __uint_as_float((m[0] & 0x7FFFu) << 16);
+  hi = __uint_as_float(m[0] & 0x7FFF0000u);
+}
+
+// RN(a / 6) for a >= 0 (Markstein step, exact).
+__device__ __forceinline__ float div6_rn(float a) {
   const float y6 = __uint_as_float(0x3E2AAAABu);        // RN(1/6)
-  const float q6 = amax * y6;
-  const float s = fmaf(fmaf(-q6, 6.0f, amax), y6, q6);
-  const uint32_t s8 = cvt_e4m3x2(s, 0.f) & 0xFFu;
-  if (s8 == 0u) {
-    codes[0] = 0u;
-    codes[1] = 0u;
-    return 0u;
-  }
-  float sf, unused;
-  e4m3x2_to_f32(s8, sf, unused);
-  const float ny = -__frcp_rn(sf);                      // RN(1 / -sf)
+  const float q6 = a * y6;
+  return fmaf(fmaf(-q6, 6.0f, a), y6, q6);
+}
+
+// The e4m3 scale bytes of two groups from their max |x| (low byte: a0).
+__device__ __forceinline__ uint32_t scale_pair(float a0, float a1) {
+  return cvt_e4m3x2(div6_rn(a0), div6_rn(a1));
+}
+
+// Codes of 16 values x[0..15] for scale byte s8: two words.
+__device__ __forceinline__ void codes_group(const float* x, uint32_t s8, const float2* rtab, uint32_t* codes) {
+  const float2 r = rtab[s8];
   float q[16];
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
-    float n0, n1, t0, t1;
-    mul2(n0, n1, x[i], x[i + 1], ny, ny);               // q0' = RN(x * y')
-    fma2(t0, t1, n0, n1, sf, sf, x[i], x[i + 1]);       // r' = x - q0' * (-sf), exact
-    fma2(q[i], q[i + 1], t0, t1, ny, ny, n0, n1);       // RN(q0' + r' * y')
+    float t0, t1;
+    mul2(t0, t1, x[i], x[i + 1], r.y, r.y);
+    fma2(q[i], q[i + 1], x[i], x[i + 1], r.x, r.x, t0, t1);
   }
-  codes[0] = cvt_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]) ^ 0x88888888u;
-  codes[1] = cvt_e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]) ^ 0x88888888u;
-  return s8;
+  const bool z = s8 == 0u;
+  codes[0] = z ? 0u : cvt_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
+  codes[1] = z ? 0u : cvt_e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]);
 }
 
-// ---------------------------------------------------------------------------
-// Two launches, 256 threads per CTA.
-//   1. quant_v_mean_kernel -- clusters of kMeanCluster CTAs, of two kinds:
-//        mean clusters (first in the grid, so that the latency-bound sums
-//                    start at once and run beside the bandwidth-bound V CTAs):
-//                    one per (b, kv head).  CTA r sums its share of the
-//                    head's 128-token chunks, one thread per channel pair and
-//                    chunk, token by token from 0 (the documented order), into
-//                    the scratch buffer.  After a cluster barrier
-//                    (release/acquire at cluster scope) CTA 0 adds the chunk
-//                    sums in chunk order and divides by L (bit-exact mu), and
-//                    writes mu;
-//        V clusters: eight independent CTAs, one thread per channel pair and
-//                    32 tokens: 32 4-byte loads (each warp load is one 128-byte
-//                    row segment), two 16-token groups per channel, codes
-//                    stored transposed.
-//   2. quant_qk_kernel -- persistent CTAs over tiles of 256 "quads" (a quad =
-//        64 consecutive channels of one row = four 1x16 groups = one 32-bit
-//        word of scale bytes) of one head: one round of Q tiles (one per CTA),
-//        then the K tiles, then the other Q tiles.  It is a programmatic
-//        dependent launch: its CTAs start while launch 1 drains and quantise
-//        Q, which launch 1 does not touch; before its first K tile each CTA
-//        waits for launch 1 to complete (mu), and K then comes from L2, where
-//        launch 1 has just read it.  Tiles arrive by TMA in
-//        128B-swizzled shared memory (boxes of 64 channels x 128 tokens of one
-//        head; tokens past L arrive as zeros) through a two-stage ring; each
-//        thread reads its quad with conflict-free 16-byte loads, subtracts mu
-//        for K (64 means through L1), and stores 32 bytes of codes and the
-//        scale word in the MMA scale layout.
-// Every layout holds Lp = L rounded up to 128 tokens per head; the tokens
-// past L are written as zero codes with zero scales (Q and K rows, V token
-// groups), and a V group that straddles L is quantised with zeros for its
-// missing tokens.
+// bf16 pair word -> two floats (channel/token 2i in the low half).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-constexpr int kThreadsQ = 256;
-constexpr int kMeanCluster = 8;                          // CTAs per head in the mean clusters
+// ---------------------------------------------------------------------------
+// Two launches of one persistent kernel body, each CTA a TMA producer warp and
+// kWorkers worker warps over a ring of kStages tiles.  A tile is 32 KB of one
+// bf16 head: two TMA boxes of 64 channels x 128 tokens, 128B-swizzled (16-byte
+// chunk c of box row rr at chunk c ^ (rr & 7)); d = 128: 128 tokens, the two
+// channel halves; d = 64: 256 tokens.  Tokens past L arrive as zeros.  Every
+// worker warp waits for every tile of its CTA in order, takes a fixed share
+// of it and releases the ring slot with one arrival; warps are not
+// synchronised with each other beyond that, so a warp with more work on one
+// tile (the mean sums) catches up on the next ones.
+//   pass 1: Q tiles alternating with K-mean tiles (an odd grid, so that each
+//     CTA alternates too):
+//     Q    one thread per quad (64 channels of one token = four 1x16 groups =
+//          one 32-bit scale word): eight conflict-free 16-byte shared loads,
+//          32 bytes of codes and the scale word stored in the MMA scale layout;
+//     mean two warps per tile (which two rotates from tile to tile), one
+//          thread per channel pair: the chunk sum of 128 tokens, token by
+//          token from 0, to the scratch buffer.
+//   pass 2 (a programmatic dependent launch of pass 1): V tiles and the K'
+//     tiles, each CTA over round-robin V tiles and a contiguous range of K'
+//     tiles, two V tiles first and then the two kinds alternating.  The V
+//     tiles and the K loads need nothing from pass 1; before its first K'
+//     tile each CTA waits for pass 1 (griddepcontrol.wait) and forms the
+//     means of its range's heads (chunk sums added in chunk order, divided by
+//     L).  K is then mostly in L2, where pass 1 has just read it.
+//     V    one thread per channel pair and 32 tokens (two 16-token groups per
+//          channel): 32 four-byte shared loads (a warp reads 32 words of one
+//          box row), 16 bytes of transposed codes per channel;
+//     K'   as Q, on K' = RN(k - mean) in float32.
+// Every layout holds Lp = L rounded up to 128 tokens per head; the tokens past
+// L are written as zero codes with zero scales (Q and K rows, V token groups),
+// and a V group that straddles L is quantised with zeros for its missing
+// tokens.
+
+constexpr int kWorkers = 8;                              // worker warps per CTA
+constexpr int kThreadsQ = (kWorkers + 1) * 32;           // + one TMA producer warp
+constexpr int kStages = 3;
+constexpr int kCtasPerSm = 2;
+constexpr int kBoxBytes = 128 * 64 * 2;                  // 128 tokens x 64 bf16 channels
+constexpr int kTileBytes = 2 * kBoxBytes;
+constexpr int kMaxMeanHeads = 8;                         // heads per pass-2 CTA range (at most)
+constexpr int kSmemQ = kStages * kTileBytes + 1024;      // ring + alignment slack
 
 template <int D>
-struct TileQK {
-  static constexpr int kRows = kThreadsQ / (D / 64);     // rows per tile: 128 (d = 128), 256 (d = 64)
-  static constexpr int kBoxes = 2;                       // 128-row x 64-channel boxes per tile
-  static constexpr int kBoxBytes = 128 * 64 * 2;
-  static constexpr int kSmemBytes = kBoxes * kBoxBytes;
+struct TileGeo {
+  static constexpr int kRows = D == 128 ? 128 : 256;    // tokens per tile
 };
 
+enum TileKind { kTileQ = 0, kTileV = 1, kTileMean = 2, kTileK = 3 };
+
 struct QuantArgs {
-  const __nv_bfloat16* q;
-  const __nv_bfloat16* k;
-  const __nv_bfloat16* v;
   uint8_t *qc, *qsf, *kc, *ksf, *vc, *vsf;
-  float* part;      // scratch: chunk sums [B*Hkv][Lp/128][D]
+  float* part;      // chunk sums [B*Hkv][Lkvp/128][D]
   float* kmean;     // [B*Hkv][D]
-  int Lq, Lqp, Lkv, Lkvp, nbh_q, nbh_kv, chunks_per_cta;   // Q and K/V tokens (and padded to 128)
-  int H, Hkv;                       // heads of Q and of K / V (bh = b * heads + h)
-  Strides sq, skv;                  // element strides of the bf16 Q and K / V (BHLD or BLHD)
-  int tph_q, tph_k;                 // Q / K tiles of kRows tokens per head
-  int ntile_q, ntile_k, nblk_v;
-  int nq_first;                     // launch 2: Q tiles taken before the K tiles (the rest after)
-  int nclu_mean, nclu_v;            // launch 1: mean clusters, V clusters
+  int Lkv, Lqp, Lkvp;
+  int H, Hkv;
+  int tph_q, tph_k;                 // tiles per head of Q and of K / V
+  uint32_t dq_m, dq_l, dk_m, dk_l;  // u / tph_q and u / tph_k as (umulhi(u, m) + u) >> l
+  int ntile_q, ntile_k;             // Q tiles; K tiles (= V tiles = mean tiles)
+  int range2;                       // pass 2: K' tiles per CTA (the last CTAs may have fewer)
   uint64_t wait_ns;
 };
 
-// Quantises one quad (minus the 64 means at `mean`, when given) and stores its
-// 32 bytes of codes and its scale word: token t of head bh (rows of Lp tokens
-// per head), `quad` the 64-channel block within the row.
+struct TileRef {
+  int kind, bh, t0;
+};
+
+// floor(u / d) for 0 <= u < 2^31 from (m, l) = (floor(2^32 (2^l - d) / d) + 1,
+// ceil(log2 d)) (Granlund and Montgomery's multiply-shift division).
+__host__ __device__ inline void fastdiv_params(uint32_t d, uint32_t& m, uint32_t& l) {
+  l = 0;
+  while ((1ull << l) < d) ++l;
+  m = (uint32_t)((((1ull << 32) * ((1ull << l) - d)) / d) + 1);
+}
+__device__ __forceinline__ int fastdiv(int u, uint32_t m, uint32_t l) {
+  return (int)((__umulhi((uint32_t)u, m) + (uint32_t)u) >> l);
+}
+
 template <int D>
-__device__ __forceinline__ void quant_quad(const uint4 (&w)[8], const float* mean, uint8_t* codes_base,
-                                           uint8_t* sf_base, long long bh, int t, int quad, int Lp) {
-  uint32_t codes[8];
-  uint32_t sfw = 0;
+__device__ __forceinline__ TileRef head_tile(int kind, int u, int tph, uint32_t m, uint32_t l) {
+  const int bh = fastdiv(u, m, l);
+  return TileRef{kind, bh, (u - bh * tph) * TileGeo<D>::kRows};
+}
+
+// Element j of two lists merged alternately (x first, then the rest of the
+// longer one): sets `second` (an element of y) and returns the index in its
+// list.
+__device__ __forceinline__ int merge_at(int nx, int ny, int j, bool& second) {
+  const int m = min(nx, ny);
+  if (j < 2 * m) {
+    second = (j & 1) != 0;
+    return j >> 1;
+  }
+  second = ny > nx;
+  return j - m;
+}
+
+// Pass 1, tile u of ntile_q + ntile_k: Q and mean tiles merged alternately.
+template <int D>
+__device__ __forceinline__ TileRef pass1_tile(const QuantArgs& a, int u) {
+  bool mean;
+  const int j = merge_at(a.ntile_q, a.ntile_k, u, mean);
+  return mean ? head_tile<D>(kTileMean, j, a.tph_k, a.dk_m, a.dk_l) : head_tile<D>(kTileQ, j, a.tph_q, a.dq_m, a.dq_l);
+}
+
+// Pass 2, CTA c of G: its V tiles c, c + G, ... (nv) and the K' tiles of its
+// contiguous range [k0, k0 + nk), in the order: the first nv0 = min(nv, 2) V
+// tiles (they need nothing from pass 1 and cover its wait), then K' and the
+// other V tiles merged alternately.
+template <int D>
+__device__ __forceinline__ TileRef pass2_tile(const QuantArgs& a, int c, int G, int nv, int k0, int nk, int i) {
+  const int nv0 = min(nv, 2);
+  if (i < nv0) return head_tile<D>(kTileV, c + i * G, a.tph_k, a.dk_m, a.dk_l);
+  bool v;
+  const int j = merge_at(nk, nv - nv0, i - nv0, v);
+  return v ? head_tile<D>(kTileV, c + (nv0 + j) * G, a.tph_k, a.dk_m, a.dk_l)
+           : head_tile<D>(kTileK, k0 + j, a.tph_k, a.dk_m, a.dk_l);
+}
+
+// Issues the two box copies of tile t into dst.
+template <int D>
+__device__ __forceinline__ void issue_tile(const TileRef& t, const CUtensorMap* tq, const CUtensorMap* tk,
+                                           const CUtensorMap* tv, const QuantArgs& a, uint8_t* dst, uint64_t* bar) {
+  const CUtensorMap* map = t.kind == kTileQ ? tq : (t.kind == kTileV ? tv : tk);
+  const int heads = t.kind == kTileQ ? a.H : a.Hkv;
+  mbar_arrive_expect_tx(bar, kTileBytes);
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    float x[16];
-    bf16x8_to_f32(w[2 * g], x);
-    bf16x8_to_f32(w[2 * g + 1], x + 8);
-    if (mean != nullptr) {
-      const float4* m4 = reinterpret_cast<const float4*>(mean + 16 * g);
+  for (int b = 0; b < 2; ++b) {
+    const int x = D == 128 ? 64 * b : 0;
+    const int y = D == 128 ? t.t0 : t.t0 + 128 * b;
+    tma_load_4d(dst + b * kBoxBytes, map, bar, x, y, t.bh % heads, t.bh / heads);
+  }
+}
+
+// Q (IS_K false) or K' (IS_K true: `nmean` = -mean of the head, in shared
+// memory) rows of a tile: one quad per thread.  d = 128: warp w takes box
+// w & 1 (the quad) and rows 32 (w >> 1) + lane; d = 64: rows 32 w + lane.  A
+// quarter-warp reads 8 consecutive rows of one box: 8 distinct chunks.
+template <int D, bool IS_K>
+__device__ __forceinline__ void quant_rows(const QuantArgs& a, const TileRef& t, const uint8_t* tile, int warp,
+                                           int lane, const float2* rtab, const float* nmean) {
+  const int tl = D == 128 ? 32 * (warp >> 1) + lane : 32 * warp + lane;
+  const int box = D == 128 ? (warp & 1) : (tl >> 7);
+  const int rr = tl & 127, quad = D == 128 ? box : 0;
+  const int tok = t.t0 + tl;
+  const int Lp = IS_K ? a.Lkvp : a.Lqp;
+  if (tok >= Lp) return;                               // (d = 64: warp-uniform)
+  const uint8_t* src = tile + box * kBoxBytes + rr * 128;
+  const uint32_t x7 = (uint32_t)(rr & 7) << 4;
+  uint32_t w[32];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src + (((uint32_t)i << 4) ^ x7));
+    w[4 * i] = v.x;
+    w[4 * i + 1] = v.y;
+    w[4 * i + 2] = v.z;
+    w[4 * i + 3] = v.w;
+  }
+  uint32_t codes[8];
+  uint32_t sfw;
+  if constexpr (!IS_K) {
+    float am[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      float lo, hi;
+      absmax_halves<8>(w + 8 * g, lo, hi);
+      am[g] = fmaxf(lo, hi);
+    }
+    sfw = scale_pair(am[0], am[1]) | (scale_pair(am[2], am[3]) << 16);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      float x[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        x[2 * i] = bf16_lo(w[8 * g + i]);
+        x[2 * i + 1] = bf16_hi(w[8 * g + i]);
+      }
+      codes_group(x, (sfw >> (8 * g)) & 0xFFu, rtab, codes + 2 * g);
+    }
+  } else {
+    // K' = RN(k - mean); a token past L arrived as zeros and K' there is kept
+    // zero (no mean subtracted)
+    const bool sub = tok < a.Lkv;
+    float x[4][16], am[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const float4* m4 = reinterpret_cast<const float4*>(nmean + quad * 64 + 16 * g);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float4 m = __ldg(m4 + i);
-        x[4 * i + 0] = __fsub_rn(x[4 * i + 0], m.x);
-        x[4 * i + 1] = __fsub_rn(x[4 * i + 1], m.y);
-        x[4 * i + 2] = __fsub_rn(x[4 * i + 2], m.z);
-        x[4 * i + 3] = __fsub_rn(x[4 * i + 3], m.w);
+        const float4 m = sub ? m4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        add2(x[g][4 * i], x[g][4 * i + 1], bf16_lo(w[8 * g + 2 * i]), bf16_hi(w[8 * g + 2 * i]), m.x, m.y);
+        add2(x[g][4 * i + 2], x[g][4 * i + 3], bf16_lo(w[8 * g + 2 * i + 1]), bf16_hi(w[8 * g + 2 * i + 1]), m.z,
+             m.w);
       }
+      float mx = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(x[g][i]));
+      am[g] = mx;
     }
-    sfw |= quant_group16(x, codes + 2 * g) << (8 * g);
+    sfw = scale_pair(am[0], am[1]) | (scale_pair(am[2], am[3]) << 16);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) codes_group(x[g], (sfw >> (8 * g)) & 0xFFu, rtab, codes + 2 * g);
   }
-  uint4* cdst = reinterpret_cast<uint4*>(codes_base + (bh * Lp + t) * (D / 2) + quad * 32);
+  uint8_t* cbase = IS_K ? a.kc : a.qc;
+  uint8_t* sbase = IS_K ? a.ksf : a.qsf;
+  uint4* cdst = reinterpret_cast<uint4*>(cbase + ((size_t)t.bh * Lp + tok) * (D / 2) + quad * 32);
   cdst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
   cdst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-  const int rb = t / 128, r = t % 128;
-  const long long blk = (bh * (Lp / 128) + rb) * (D / 64) + quad;
-  *reinterpret_cast<uint32_t*>(sf_base + blk * 512 + (r % 32) * 16 + (r / 32) * 4) = sfw;
+  const int r = tok & 127;
+  const size_t blk = ((size_t)t.bh * (Lp / 128) + (tok >> 7)) * (D / 64) + quad;
+  *reinterpret_cast<uint32_t*>(sbase + blk * 512 + (r & 31) * 16 + (r >> 5) * 4) = sfw;
 }
 
-// Whether tile `tile` of launch 2 is a K tile: tiles [0, nq_first) are Q
-// tiles, then come the K tiles, then the other Q tiles.
-__device__ __forceinline__ bool tile_is_k(const QuantArgs& a, int tile) {
-  return tile >= a.nq_first && tile < a.nq_first + a.ntile_k;
-}
-// Head and first token of Q/K tile `tile`.
-__device__ __forceinline__ void tile_head(const QuantArgs& a, int tile, int rows, bool& is_k, int& bh, int& t0) {
-  is_k = tile_is_k(a, tile);
-  const int u = is_k ? tile - a.nq_first : (tile < a.nq_first ? tile : tile - a.ntile_k);
-  const int tph = is_k ? a.tph_k : a.tph_q;
-  bh = u / tph;
-  t0 = (u % tph) * rows;
-}
-
-// Issues the TMA copies of Q/K tile `tile` into `dst`: tokens [t0, t0 + kRows)
-// of one head, boxes of 64 channels x 128 tokens (d = 128: the two channel
-// halves; d = 64: two token blocks).  Tokens past L (and a second box wholly
-// past Lp) arrive as zeros.
-template <int D>
-__device__ __forceinline__ void issue_tile_qk(const QuantArgs& a, const CUtensorMap* tq, const CUtensorMap* tk,
-                                              int tile, uint8_t* dst, uint64_t* bar) {
-  using T = TileQK<D>;
-  bool is_k;
-  int bh, t0;
-  tile_head(a, tile, T::kRows, is_k, bh, t0);
-  const CUtensorMap* map = is_k ? tk : tq;
-  const int heads = is_k ? a.Hkv : a.H;
-  mbar_arrive_expect_tx(bar, T::kBoxes * T::kBoxBytes);
+// Row offsets within a box row of the word of channel pair `lane` (0..31) for
+// the 8 swizzle phases: chunk (lane >> 2) ^ phase, word lane & 3.
+__device__ __forceinline__ void pair_offsets(int lane, uint32_t (&off)[8]) {
 #pragma unroll
-  for (int b = 0; b < T::kBoxes; ++b) {
-    const int x = D == 128 ? 64 * b : 0;
-    const int y = D == 128 ? t0 : t0 + 128 * b;
-    tma_load_4d(dst + b * T::kBoxBytes, map, bar, x, y, bh % heads, bh / heads);
-  }
+  for (int k = 0; k < 8; ++k) off[k] = ((((uint32_t)lane >> 2) ^ (uint32_t)k) << 4) | (((uint32_t)lane & 3u) << 2);
 }
 
-// Quantises the tile in `src` (128B swizzle: 16-byte chunk i of box row rr
-// sits at chunk i ^ (rr & 7)); one quad per thread.
+// V tile: one thread per channel pair and 32 tokens.  d = 128: warp w takes
+// box w & 1 and tokens 32 (w >> 1) ..; d = 64: tokens 32 w .. (box w / 4).
 template <int D>
-__device__ __forceinline__ void quant_tile_smem(const QuantArgs& a, int tile, const uint8_t* src) {
-  using T = TileQK<D>;
-  bool is_k;
-  int bh, t0;
-  tile_head(a, tile, T::kRows, is_k, bh, t0);
-  const int r = threadIdx.x / (D / 64), quad = threadIdx.x % (D / 64);
-  const int t = t0 + r;
-  if (t >= (is_k ? a.Lkvp : a.Lqp)) return;
-  const int box = D == 128 ? quad : r / 128, rr = D == 128 ? r : r % 128;
-  const uint8_t* base = src + box * T::kBoxBytes + rr * 128;
-  uint4 w[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) w[i] = *reinterpret_cast<const uint4*>(base + ((i ^ (rr & 7)) * 16));
-  // a token past L arrived as zeros; K' there is kept zero (no mean subtracted)
-  if (is_k)
-    quant_quad<D>(w, t < a.Lkv ? a.kmean + (size_t)bh * D + quad * 64 : nullptr, a.kc, a.ksf, bh, t, quad, a.Lkvp);
-  else
-    quant_quad<D>(w, nullptr, a.qc, a.qsf, bh, t, quad, a.Lqp);
-}
-
-// One thread per (channel pair, 32 tokens = two 16-token groups).  Items are
-// ordered channel pair fastest, so a warp covers 64 consecutive channels of
-// the same 32 tokens and each of its 32 loads reads one 128-byte segment of a
-// V row.  A channel's two scale bytes are one half of its 64-token scale word.
-template <int D>
-__device__ __forceinline__ void quant_v_cta(const QuantArgs& a, int blk) {
-  constexpr int kPairs = D / 2;
-  const long long item = (long long)blk * kThreadsQ + threadIdx.x;
-  const int npb = a.Lkvp / 32;                          // 32-token pieces per head (padded length)
-  if (item >= (long long)a.nbh_kv * npb * kPairs) return;
-  const int c = 2 * (int)(item % kPairs);
-  const long long piece = item / kPairs;                // over B*Hkv*npb
-  const long long bh = piece / npb;
-  const int tp = (int)(piece % npb);
-  const int nvalid = a.Lkv - tp * 32;                   // tokens of this piece below Lkv (may be <= 0)
-  const long long vb = bh / a.Hkv, vh = bh % a.Hkv;
-  const uint32_t* src =
-      reinterpret_cast<const uint32_t*>(a.v + vb * a.skv.b + vh * a.skv.h + (long long)tp * 32 * a.skv.t + c);
-  const size_t tstep = (size_t)(a.skv.t / 2);           // token stride in bf16 pairs
+__device__ __forceinline__ void quant_v(const QuantArgs& a, const TileRef& t, const uint8_t* tile, int warp, int lane,
+                                        const float2* rtab) {
+  const int box = D == 128 ? (warp & 1) : (warp >> 2);
+  const int tl0 = D == 128 ? 32 * (warp >> 1) : 32 * warp;
+  const int tok0 = t.t0 + tl0;
+  if (tok0 >= a.Lkvp) return;                           // (d = 64: warp-uniform)
+  const uint8_t* src = tile + box * kBoxBytes + (tl0 & 127) * 128;
+  uint32_t off[8];
+  pair_offsets(lane, off);
   uint32_t w[32];
-  if (nvalid >= 32) {
 #pragma unroll
-    for (int t = 0; t < 32; ++t) w[t] = __ldg(src + t * tstep);
-  } else {
-    // the ragged end of the head: tokens past L count as zeros
+  for (int j = 0; j < 32; ++j) w[j] = *reinterpret_cast<const uint32_t*>(src + j * 128 + off[j & 7]);
+  // per-channel maxima of the two 16-token groups (low halves: channel c)
+  float a0, a1, b0, b1;
+  absmax_halves<16>(w, a0, a1);
+  absmax_halves<16>(w + 16, b0, b1);
+  const uint32_t s01 = scale_pair(a0, a1);              // group 0: channel c (low byte), c + 1
+  const uint32_t s23 = scale_pair(b0, b1);              // group 1
+  const int c = (D == 128 ? 64 * box : 0) + 2 * lane;
+  uint8_t* sblk = a.vsf + ((size_t)t.bh * (a.Lkvp / 64) + (tok0 >> 6)) * 512 + ((tok0 & 63) >> 4);
 #pragma unroll
-    for (int t = 0; t < 32; ++t) w[t] = t < nvalid ? __ldg(src + t * tstep) : 0u;
-  }
-  uint8_t* sblk = a.vsf + ((size_t)bh * (a.Lkvp / 64) + tp / 2) * 512 + (tp % 2) * 2;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {                         // channel c + h
+  for (int h = 0; h < 2; ++h) {
     uint32_t codes[4];
-    uint32_t sfw = 0;
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
       float x[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        x[i] = __uint_as_float(h ? (w[16 * g + i] & 0xFFFF0000u) : (w[16 * g + i] << 16));
-      sfw |= quant_group16(x, codes + 2 * g) << (8 * g);
+      for (int i = 0; i < 16; ++i) x[i] = h ? bf16_hi(w[16 * g + i]) : bf16_lo(w[16 * g + i]);
+      codes_group(x, ((g ? s23 : s01) >> (8 * h)) & 0xFFu, rtab, codes + 2 * g);
     }
     const int ch = c + h;
-    *reinterpret_cast<uint4*>(a.vc + ((size_t)bh * D + ch) * (a.Lkvp / 2) + (size_t)tp * 16) =
+    *reinterpret_cast<uint4*>(a.vc + ((size_t)t.bh * D + ch) * (a.Lkvp / 2) + (tok0 >> 1)) =
         make_uint4(codes[0], codes[1], codes[2], codes[3]);
-    *reinterpret_cast<uint16_t*>(sblk + (ch % 32) * 16 + (ch / 32) * 4) = (uint16_t)sfw;
-    if (D == 64) *reinterpret_cast<uint16_t*>(sblk + (ch % 32) * 16 + (ch / 32 + 2) * 4) = 0;   // padding rows
+    const uint32_t sc = ((s01 >> (8 * h)) & 0xFFu) | (((s23 >> (8 * h)) & 0xFFu) << 8);
+    *reinterpret_cast<uint16_t*>(sblk + (ch & 31) * 16 + (ch >> 5) * 4) = (uint16_t)sc;
+    if (D == 64) *reinterpret_cast<uint16_t*>(sblk + (ch & 31) * 16 + ((ch >> 5) + 2) * 4) = 0;   // padding rows
   }
 }
 
-// mu[bh][c] = (chunk sums in chunk order) / L, chunk sum = the chunk's tokens
-// (128, fewer in a ragged last chunk) added token by token from 0.  Called by
-// all CTAs of one cluster.
+// K-mean tile, on the two warps `sel` (0 or 1 = box for d = 128, chunk half
+// for d = 64): thread = channel pair, the 128-token chunk sum token by token
+// from 0 (a token past L adds +0, which leaves a float32 sum unchanged: the
+// sum starts at +0 and never becomes -0).
 template <int D>
-__device__ __forceinline__ void mean_cluster(const QuantArgs& a, int bh) {
-  constexpr int kPairs = D / 2;
-  constexpr int kChunksAtOnce = kThreadsQ / kPairs;
-  const uint32_t rank = cluster_ctarank();
-  const int nchunk = a.Lkvp / kMeanChunk, cpc = a.chunks_per_cta;
-  const int first = (int)rank * cpc, last = min(nchunk, first + cpc);
-  const int c = 2 * (threadIdx.x % kPairs);
-  for (int ch = first + (int)threadIdx.x / kPairs; ch < last; ch += kChunksAtOnce) {
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(a.k + (long long)(bh / a.Hkv) * a.skv.b +
-                                                            (long long)(bh % a.Hkv) * a.skv.h +
-                                                            (long long)ch * kMeanChunk * a.skv.t + c);
-    const size_t tstep = (size_t)(a.skv.t / 2);         // token stride in bf16 pairs
-    float acc0 = 0.f, acc1 = 0.f;
-    const int nvalid = a.Lkv - ch * kMeanChunk;         // tokens of this chunk below Lkv
-#pragma unroll 1
-    for (int t0 = 0; t0 < kMeanChunk; t0 += 32) {
-      // a token past L adds +0, which leaves a float32 sum unchanged (the
-      // sum starts at +0 and never becomes -0)
-      uint32_t w[32];
+__device__ __forceinline__ void mean_chunk(const QuantArgs& a, const TileRef& t, const uint8_t* tile, int sel,
+                                           int lane) {
+  const int tok0 = D == 128 ? t.t0 : t.t0 + 128 * sel;
+  if (tok0 >= a.Lkvp) return;
+  const uint8_t* src = tile + sel * kBoxBytes;
+  uint32_t off[8];
+  pair_offsets(lane, off);
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll 2
+  for (int j0 = 0; j0 < 128; j0 += 8) {
+    uint32_t w[8];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) w[i] = t0 + i < nvalid ? __ldg(src + (t0 + i) * tstep) : 0u;
+    for (int k = 0; k < 8; ++k) w[k] = *reinterpret_cast<const uint32_t*>(src + (j0 + k) * 128 + off[k]);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        acc0 = __fadd_rn(acc0, __uint_as_float(w[i] << 16));
-        acc1 = __fadd_rn(acc1, __uint_as_float(w[i] & 0xFFFF0000u));
-      }
-    }
-    *reinterpret_cast<float2*>(a.part + ((size_t)bh * nchunk + ch) * D + c) = make_float2(acc0, acc1);
+    for (int k = 0; k < 8; ++k) add2(s0, s1, s0, s1, bf16_lo(w[k]), bf16_hi(w[k]));
   }
-  cluster_sync();                                       // every chunk sum of the head is written
-  if (rank == 0 && threadIdx.x < D) {
-    const int col = threadIdx.x;
-    float tot = 0.f;
-#pragma unroll 1
-    for (int c0 = 0; c0 < nchunk; c0 += 8) {
-      float v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int ch = c0 + j;
-        v[j] = ch < nchunk ? __ldcg(a.part + ((size_t)bh * nchunk + ch) * D + col) : 0.f;
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (c0 + j < nchunk) tot = __fadd_rn(tot, v[j]);
-    }
-    a.kmean[(size_t)bh * D + col] = __fdiv_rn(tot, (float)a.Lkv);
-  }
+  const int c = (D == 128 ? 64 * sel : 0) + 2 * lane;
+  const int nchunk = a.Lkvp / kMeanChunk;
+  *reinterpret_cast<float2*>(a.part + ((size_t)t.bh * nchunk + (tok0 / kMeanChunk)) * D + c) = make_float2(s0, s1);
 }
 
-// Clusters [0, nclu_mean) compute the means, the rest quantise V.  Every CTA
-// lets the dependent quant_qk_kernel launch at once (it waits for this
-// launch's completion before it reads mu).
-template <int D>
-__global__ void __cluster_dims__(kMeanCluster, 1, 1) __launch_bounds__(kThreadsQ)
-    quant_v_mean_kernel(const QuantArgs a) {
-  pdl_launch_dependents();
-  const int clu = blockIdx.x / kMeanCluster;
-  if (clu < a.nclu_mean) {
-    mean_cluster<D>(a, clu);
-    return;
-  }
-  const int blk = (clu - a.nclu_mean) * kMeanCluster + (int)(blockIdx.x % kMeanCluster);
-  if (blk < a.nblk_v) quant_v_cta<D>(a, blk);
-}
-
-// Persistent: CTA c takes tiles c, c + G, c + 2G, ... (G = grid size) through
-// a two-stage TMA ring, the next tile's copy in flight while the current one
-// is quantised.
-template <int D>
-__global__ void __launch_bounds__(kThreadsQ, 3) quant_qk_kernel(const __grid_constant__ CUtensorMap tmap_q,
-                                                             const __grid_constant__ CUtensorMap tmap_k,
-                                                             const QuantArgs a) {
-  using T = TileQK<D>;
-  // the attention launch behind this one may start (it waits for this
-  // launch's completion before it reads the codes)
+template <int D, int PASS>
+__global__ void __launch_bounds__(kThreadsQ, kCtasPerSm)
+    quant_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                 const __grid_constant__ CUtensorMap tmap_v, const QuantArgs a) {
+  // the launch behind this one (pass 2, or the attention) may be scheduled at
+  // once: it waits for this launch's completion before it reads its outputs
   pdl_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full[2];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t full[kStages], empty[kStages], mean_ready;
   __shared__ int abort_flag;
-  const int ntiles = a.ntile_k + a.ntile_q, G = gridDim.x;
+  __shared__ float2 rtab[128];
+  __shared__ __align__(16) float nmean[PASS == 2 ? kMaxMeanHeads * D : 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the tiles of this CTA: pass 1 c, c + G, ... of ntile_q + ntile_k; pass 2
+  // nv V tiles and the K' tiles [k0, k0 + nk)
+  const int G = gridDim.x, c = blockIdx.x;
+  const int n1 = a.ntile_q + a.ntile_k;
+  const int nv = c < a.ntile_k ? (a.ntile_k - c + G - 1) / G : 0;
+  const int k0 = min(a.ntile_k, c * a.range2), nk = min(a.ntile_k, k0 + a.range2) - k0;
+  const int kh0 = k0 / a.tph_k;                         // first head of the K' range
+  const int ntiles = PASS == 1 ? (c < n1 ? (n1 - c + G - 1) / G : 0) : nv + nk;
+  auto tile_at = [&](int i) {
+    return PASS == 1 ? pass1_tile<D>(a, c + i * G) : pass2_tile<D>(a, c, G, nv, k0, nk, i);
+  };
   if (threadIdx.x == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWorkers);
+    }
+    mbar_init(&mean_ready, D / 32);
     abort_flag = 0;
     fence_barrier_init();
   }
+  if (threadIdx.x < 128) {
+    // (yh, yl) of scale byte s8 (0 and the NaN code: unused)
+    const uint32_t s8 = threadIdx.x;
+    float2 r = make_float2(0.f, 0.f);
+    if (s8 != 0u && s8 != 0x7Fu) {
+      const float sf = e4m3_to_f32(s8);
+      const float yh = __frcp_rd(sf);
+      r = make_float2(yh, __fmul_rn(fmaf(-sf, yh, 1.0f), yh));
+    }
+    rtab[s8] = r;
+  }
   __syncthreads();
-  const bool leader = threadIdx.x == 0;
-  int tile = blockIdx.x;
-  int issued[2] = {0, 0};                               // loads issued per stage (leader's count)
-  if (leader) {
-    if (tile < ntiles) {
-      issue_tile_qk<D>(a, &tmap_q, &tmap_k, tile, smem, &full[0]);
-      issued[0] = 1;
+
+  if (warp == kWorkers) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int i = 0;
+      bool ok = true;
+      for (; i < ntiles; ++i) {
+        const int st = i % kStages;
+        if (i >= kStages && !mbar_wait_backoff(&empty[st], ((i / kStages) - 1) & 1, &abort_flag, a.wait_ns, 64)) {
+          ok = false;
+          break;
+        }
+        issue_tile<D>(tile_at(i), &tmap_q, &tmap_k, &tmap_v, a, ring + st * kTileBytes, &full[st]);
+      }
+      if (!ok) {
+        // never leave with a copy in flight: wait (bounded) for each stage's
+        // last load (tiles 0 .. i - 1 were issued, tile j to stage j % kStages;
+        // the n-th load of a stage completes its phase n - 1)
+        for (int st = 0; st < kStages; ++st) {
+          const int n = (i - st + kStages - 1) / kStages;
+          if (n > 0) mbar_wait_drain(&full[st], (n - 1) & 1, a.wait_ns);
+        }
+      }
     }
-    if (tile + G < ntiles) {
-      issue_tile_qk<D>(a, &tmap_q, &tmap_k, tile + G, smem + T::kSmemBytes, &full[1]);
-      issued[1] = 1;
+  } else {
+    // ----------------------------------------------------------------- workers
+    // one tile: wait for its copy, quantise this warp's share, release the
+    // slot (every warp sees every phase of every stage in order)
+    auto work = [&](int i) -> bool {
+      const int st = i % kStages;
+      if (!mbar_wait(&full[st], (i / kStages) & 1, &abort_flag, a.wait_ns)) return false;
+      const uint8_t* tile = ring + st * kTileBytes;
+      const TileRef t = tile_at(i);
+      if (t.kind == kTileQ) {
+        quant_rows<D, false>(a, t, tile, warp, lane, rtab, nullptr);
+      } else if (t.kind == kTileV) {
+        quant_v<D>(a, t, tile, warp, lane, rtab);
+      } else if (t.kind == kTileMean) {
+        const int w0 = 2 * (i & 3);                     // the two warps of this mean tile
+        if (warp == w0 || warp == w0 + 1) mean_chunk<D>(a, t, tile, warp - w0, lane);
+      } else {
+        quant_rows<D, true>(a, t, tile, warp, lane, rtab, nmean + (t.bh - kh0) * D);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+      return true;
+    };
+    // pass 2: the tiles before the first K' tile (all of them without K' tiles)
+    const int nfirst = PASS == 1 ? ntiles : (nk > 0 ? min(nv, 2) : ntiles);
+    bool ok = true;
+    for (int i = 0; ok && i < nfirst; ++i) ok = work(i);
+    if (PASS == 2 && ok && nk > 0) {
+      // before the first K' tile: the chunk sums are written by pass 1
+      pdl_wait();
+      // -mean of every head of the range (warps 0 .. D/32 - 1, one channel each)
+      if (threadIdx.x < D) {
+        const int ch = threadIdx.x;
+        const int nchunk = a.Lkvp / kMeanChunk;
+        const int h1 = (k0 + nk - 1) / a.tph_k;
+        for (int bh = kh0; bh <= h1; ++bh) {
+          const float* p = a.part + (size_t)bh * nchunk * D + ch;
+          float tot = 0.f;
+#pragma unroll 1
+          for (int c0 = 0; c0 < nchunk; c0 += 16) {
+            float v[16];                                // 16 loads in flight, then the adds in order
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = c0 + j < nchunk ? __ldcg(p + (size_t)(c0 + j) * D) : 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < nchunk) tot = __fadd_rn(tot, v[j]);
+          }
+          const float mu = __fdiv_rn(tot, (float)a.Lkv);
+          nmean[(bh - kh0) * D + ch] = -mu;
+          if (k0 <= bh * a.tph_k) a.kmean[(size_t)bh * D + ch] = mu;   // the range holding the head's first tile
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&mean_ready);
+      }
+      ok = mbar_wait(&mean_ready, 0, &abort_flag, a.wait_ns);
+      for (int i = nfirst; ok && i < ntiles; ++i) ok = work(i);
     }
   }
-  bool ok = true, waited = false;
-  int i = 0;
-  for (; tile < ntiles; ++i, tile += G) {
-    const int st = i & 1;
-    if (!mbar_wait(&full[st], (i >> 1) & 1, &abort_flag, a.wait_ns)) {
-      ok = false;
-      break;
-    }
-    if (!waited && tile_is_k(a, tile)) {
-      pdl_wait();                                       // mu is written by launch 1
-      waited = true;
-    }
-    quant_tile_smem<D>(a, tile, smem + st * T::kSmemBytes);
-    __syncthreads();                                    // stage st has been read by every thread
-    if (leader && tile + 2 * G < ntiles) {
-      issue_tile_qk<D>(a, &tmap_q, &tmap_k, tile + 2 * G, smem + st * T::kSmemBytes, &full[st]);
-      ++issued[st];
-    }
-  }
-  if (!ok && leader) {
-    // never leave with a copy in flight: wait (bounded) for each stage's last
-    // issued load, the use-th load of a stage completing phase use - 1
-    for (int st = 0; st < 2; ++st) {
-      const int consumed = (i + 1 - st) / 2;            // loads of stage st waited for so far
-      if (issued[st] > consumed) mbar_wait_drain(&full[st], (issued[st] - 1) & 1, a.wait_ns);
-    }
-  }
-  // this launch completes only after launch 1 has: what follows in the stream
-  // may then read every output of sa_quantize
-  if (!waited) pdl_wait();
+  // (pass 2 completes only after pass 1 has: the workers of every CTA with
+  // K' tiles waited for it, so what follows in the stream may then read
+  // every output of sa_quantize)
 }
 
 template <int D>
-cudaError_t launch_quantize_impl(const void* q, const void* k, const void* v, const Dims& dm, bool blhd,
-                                 const sa_fp4_qkv& out, float* partials, const CUtensorMap& tq,
-                                 const CUtensorMap& tk, cudaStream_t s) {
-  using T = TileQK<D>;
+cudaError_t launch_quantize_impl(const Dims& dm, const sa_fp4_qkv& out, float* partials, const CUtensorMap& tq,
+                                 const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
+  constexpr int R = TileGeo<D>::kRows;
   QuantArgs a;
-  a.q = static_cast<const __nv_bfloat16*>(q);
-  a.k = static_cast<const __nv_bfloat16*>(k);
-  a.v = static_cast<const __nv_bfloat16*>(v);
   a.qc = static_cast<uint8_t*>(out.q_codes);
   a.qsf = static_cast<uint8_t*>(out.q_sf);
   a.kc = static_cast<uint8_t*>(out.k_codes);
@@ -432,63 +534,57 @@ cudaError_t launch_quantize_impl(const void* q, const void* k, const void* v, co
   a.vsf = static_cast<uint8_t*>(out.v_sf);
   a.part = partials;
   a.kmean = out.k_mean;
-  a.Lq = dm.Lq;
-  a.Lqp = padded_len(dm.Lq);
   a.Lkv = dm.Lkv;
+  a.Lqp = padded_len(dm.Lq);
   a.Lkvp = padded_len(dm.Lkv);
   a.H = dm.H;
   a.Hkv = dm.Hkv;
-  a.sq = layout_strides(blhd, dm.H, dm.Lq, dm.d);
-  a.skv = layout_strides(blhd, dm.Hkv, dm.Lkv, dm.d);
-  a.nbh_q = dm.B * dm.H;
-  a.nbh_kv = dm.B * dm.Hkv;
-  const int nchunk = a.Lkvp / kMeanChunk;
-  a.chunks_per_cta = (nchunk + kMeanCluster - 1) / kMeanCluster;
-  a.tph_q = (a.Lqp + T::kRows - 1) / T::kRows;
-  a.tph_k = (a.Lkvp + T::kRows - 1) / T::kRows;
-  a.ntile_q = a.nbh_q * a.tph_q;
-  a.ntile_k = a.nbh_kv * a.tph_k;
-  a.nblk_v = (int)(((long long)a.nbh_kv * (a.Lkvp / 32) * (D / 2) + kThreadsQ - 1) / kThreadsQ);
-  a.nclu_mean = a.nbh_kv;
-  a.nclu_v = (a.nblk_v + kMeanCluster - 1) / kMeanCluster;
+  a.tph_q = (a.Lqp + R - 1) / R;
+  a.tph_k = (a.Lkvp + R - 1) / R;
+  a.ntile_q = dm.B * dm.H * a.tph_q;
+  a.ntile_k = dm.B * dm.Hkv * a.tph_k;
   a.wait_ns = kWaitLimitNs;
-  constexpr int kSmem = 2 * T::kSmemBytes + 1024;        // two stages + alignment slack
+  fastdiv_params((uint32_t)a.tph_q, a.dq_m, a.dq_l);
+  fastdiv_params((uint32_t)a.tph_k, a.dk_m, a.dk_l);
   static std::atomic<bool> attr_done[kMaxDevices];   // kernel attributes are per device
   cudaError_t ea = once_per_device(attr_done, [] {
-    return cudaFuncSetAttribute(quant_qk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = cudaFuncSetAttribute(quant_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemQ);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(quant_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemQ);
+    return e;
   });
   if (ea != cudaSuccess) return ea;
-  const int ntiles = a.ntile_k + a.ntile_q;
   const int sms = device_sm_count() > 0 ? device_sm_count() : 148;
-  const int grid = ntiles < 3 * sms ? ntiles : 3 * sms;    // three resident CTAs per SM
-  // one round of Q tiles runs beside launch 1; K follows while it is in L2
-  a.nq_first = a.ntile_q < grid ? a.ntile_q : grid;
-  quant_v_mean_kernel<D><<<(a.nclu_mean + a.nclu_v) * kMeanCluster, kThreadsQ, 0, s>>>(a);
+  const int slots = kCtasPerSm * sms;
+  const int n1 = a.ntile_q + a.ntile_k;
+  // an odd grid, so that CTA c (tiles c, c + G, ...) alternates between Q and
+  // mean tiles instead of taking only one kind
+  const int odd_slots = (slots & 1) ? slots : slots - 1;
+  const int grid1 = n1 < odd_slots ? n1 : odd_slots;
+  // pass 2: K' ranges spanning at most kMaxMeanHeads heads (a range of r
+  // tiles spans at most ceil((r - 1) / tph_k) + 1 heads); one per CTA
+  int range2 = (a.ntile_k + slots - 1) / slots;
+  if (range2 > (kMaxMeanHeads - 1) * a.tph_k + 1) range2 = (kMaxMeanHeads - 1) * a.tph_k + 1;
+  a.range2 = range2;
+  const int grid2 = (a.ntile_k + range2 - 1) / range2;
+  quant_kernel<D, 1><<<grid1, kThreadsQ, kSmemQ, s>>>(tq, tk, tv, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // launch 2 may start while launch 1 drains (programmatic dependent launch)
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreadsQ);
-  cfg.dynamicSmemBytes = kSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, quant_qk_kernel<D>, tq, tk, a);
+  // pass 2 may start while pass 1 drains (programmatic dependent launch)
+  cudaLaunchAttribute attr;
+  const cudaLaunchConfig_t cfg = pdl_launch_config(dim3(grid2), dim3(kThreadsQ), kSmemQ, s, &attr);
+  return cudaLaunchKernelEx(&cfg, quant_kernel<D, 2>, tq, tk, tv, a);
 }
 
 }  // namespace
 
 cudaError_t quant_read_error(int* out) { return read_and_clear_device_error(out); }
 
-cudaError_t launch_quantize(const void* q, const void* k, const void* v, const Dims& dm, bool blhd,
-                            const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t s) {
+cudaError_t launch_quantize(const Dims& dm, const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, cudaStream_t s) {
   float* part = static_cast<float*>(out.workspace);
-  return dm.d == 64 ? launch_quantize_impl<64>(q, k, v, dm, blhd, out, part, tq, tk, s)
-                    : launch_quantize_impl<128>(q, k, v, dm, blhd, out, part, tq, tk, s);
+  return dm.d == 64 ? launch_quantize_impl<64>(dm, out, part, tq, tk, tv, s)
+                    : launch_quantize_impl<128>(dm, out, part, tq, tk, tv, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -523,9 +619,8 @@ cudaError_t static_scratch_address(float** out) {
 
 }  // namespace
 
-cudaError_t launch_quantize_static_scratch(const void* q, const void* k, const void* v, const Dims& dm,
-                                           const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk,
-                                           cudaStream_t s) {
+cudaError_t launch_quantize_static_scratch(const Dims& dm, const sa_fp4_qkv& out, const CUtensorMap& tq,
+                                           const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
   // (sa_quantize_static_scratch has checked kmean_partial_floats(dm) <=
   // kStaticScratchFloats before calling)
   float* part = nullptr;
@@ -534,8 +629,8 @@ cudaError_t launch_quantize_static_scratch(const void* q, const void* k, const v
   // Every chunk sum read is written first by the same call (its first
   // launch), so earlier contents of the array never reach the outputs and
   // nothing needs clearing.
-  return dm.d == 64 ? launch_quantize_impl<64>(q, k, v, dm, false, out, part, tq, tk, s)
-                    : launch_quantize_impl<128>(q, k, v, dm, false, out, part, tq, tk, s);
+  return dm.d == 64 ? launch_quantize_impl<64>(dm, out, part, tq, tk, tv, s)
+                    : launch_quantize_impl<128>(dm, out, part, tq, tk, tv, s);
 }
 
 }  // namespace sa

@@ -62,9 +62,10 @@ bool make_bf16_head_map(CUtensorMap* m, const void* base, int heads, int L, cons
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_bf16_row_maps(const void* q, const void* k, const Dims& dm, bool blhd, CUtensorMap* tq,
-                        CUtensorMap* tk) {
-  return make_bf16_head_map(tq, q, dm.H, dm.Lq, dm, blhd) && make_bf16_head_map(tk, k, dm.Hkv, dm.Lkv, dm, blhd);
+bool make_bf16_maps(const void* q, const void* k, const void* v, const Dims& dm, bool blhd, CUtensorMap* tq,
+                    CUtensorMap* tk, CUtensorMap* tv) {
+  return make_bf16_head_map(tq, q, dm.H, dm.Lq, dm, blhd) && make_bf16_head_map(tk, k, dm.Hkv, dm.Lkv, dm, blhd) &&
+         make_bf16_head_map(tv, v, dm.Hkv, dm.Lkv, dm, blhd);
 }
 
 // SA_OK for sizes the kernels take, or the error to return.  B == 0 or Lq ==
@@ -198,9 +199,9 @@ sa_status sa_quantize_s(const void* q, const void* k, const void* v, const sa_sh
   if (dm.Lq == 0) return SA_ERR_INVALID_ARG;            // keys without queries: nothing to quantise them for
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !fp4_ptrs_ok(out)) return SA_ERR_INVALID_ARG;
   const bool blhd = (flags & SA_LAYOUT_BLHD) != 0;
-  CUtensorMap tq, tk;
-  if (!make_bf16_row_maps(q, k, dm, blhd, &tq, &tk)) return SA_ERR_CUDA;
-  return launch_quantize(q, k, v, dm, blhd, *out, tq, tk, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+  CUtensorMap tq, tk, tv;
+  if (!make_bf16_maps(q, k, v, dm, blhd, &tq, &tk, &tv)) return SA_ERR_CUDA;
+  return launch_quantize(dm, *out, tq, tk, tv, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? SA_OK
              : SA_ERR_CUDA;
 }
@@ -228,9 +229,9 @@ sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v
       !aligned16(out->q_sf) || !aligned16(out->k_codes) || !aligned16(out->k_sf) || !aligned16(out->v_codes) ||
       !aligned16(out->v_sf) || !aligned16(out->k_mean))
     return SA_ERR_INVALID_ARG;
-  CUtensorMap tq, tk;
-  if (!make_bf16_row_maps(q, k, dm, false, &tq, &tk)) return SA_ERR_CUDA;
-  return launch_quantize_static_scratch(q, k, v, dm, *out, tq, tk, reinterpret_cast<cudaStream_t>(stream)) ==
+  CUtensorMap tq, tk, tv;
+  if (!make_bf16_maps(q, k, v, dm, false, &tq, &tk, &tv)) return SA_ERR_CUDA;
+  return launch_quantize_static_scratch(dm, *out, tq, tk, tv, reinterpret_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? SA_OK
              : SA_ERR_CUDA;

@@ -93,6 +93,14 @@ def crafted_inputs(d=128, L=256):
         [1e30, -1e30, 3.0, -1e-30] + [0.0] * 12,
         [-1e-3, 6.0] + [-1e-6] * 14,
         [3e-38, -1e-38] + [0.0] * 14,
+        # scale 15/8 (amax 11.25) and every e2m1 tie x / s = 0.25 .. 5: the
+        # case a single rounded product with RN(1/s) gets wrong
+        [11.25, 2.34375, 4.6875, 9.375, -2.34375, -4.6875, -9.375, 1.40625, 3.28125, 6.5625, 0.46875,
+         -0.46875, 0.0, -0.0, 0.9375, -11.25],
+        [1.40625, 0.29296875, 0.5859375, 1.171875, -0.17578125, 0.41015625, 0.8203125, -0.05859375] + [0.0] * 8,
+        # scale 9/8 (amax 6.75) at the same ties
+        [6.75, 0.28125, 0.84375, 1.40625, 1.96875, 2.8125, 3.9375, 5.625, -0.28125, -0.84375, -1.40625,
+         -1.96875, -2.8125, -3.9375, -5.625, 0.0],
     ]
     for i, p in enumerate(pats):
         for rep in range(3):
