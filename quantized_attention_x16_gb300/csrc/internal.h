@@ -142,6 +142,15 @@ cudaError_t launch_nvfp4_score_tile(const CUtensorMap& tq, const CUtensorMap& tk
 // log2 of y[i] (device buffers of n floats).
 cudaError_t launch_exp_path_selftest(const float* x, const float* y, int n, float* ex2_out, float* lg2_out,
                                      cudaStream_t s);
+// attn_decode.cu: NVFP4 attention for problems with at most 16 query rows per
+// kv head ((H / Hkv) * Lq <= 16: decode steps), the rows of a kv head's query
+// heads taken together; tk / tv as for launch_attn_nvfp4.  nsplit key shares
+// per (batch, kv head) (partial results and splitkv.cu's combine when > 1).
+bool decode_eligible(const Dims& dm);
+int decode_nsplit(const Dims& dm, int sms);
+cudaError_t launch_attn_decode(const CUtensorMap& tk, const CUtensorMap& tv, const sa_fp4_qkv& x, void* o,
+                               const Strides& so, const Dims& dm, int causal, bool out_f32, int nsplit,
+                               const SplitOut& part, cudaStream_t s);
 // splitkv.cu: O from the nsplit partial results of every row t < L.
 cudaError_t launch_splitkv_combine(const SplitOut& part, int nsplit, const Dims& dm, void* o, const Strides& so,
                                    bool out_f32, cudaStream_t s);

@@ -250,6 +250,9 @@ static int resolve_nsplit(const Dims& dm, int causal, int mode, int requested) {
   if (requested == 1) return 1;
   if (requested == kStreamK) return kStreamK;
   const int sms = device_sm_count();
+  // few query rows per kv head (decode): the decode kernel, its key range
+  // split into shares so that the (batch, kv head) pairs fill the SMs twice
+  if (requested == 0 && mode == SA_MODE_NVFP4 && decode_eligible(dm)) return decode_nsplit(dm, sms);
   if (requested == 0) {
     const long long pairs = (long long)(((dm.Lq + 127) / 128 + 1) / 2) * dm.B * dm.H;
     // stream-K balances key tiles, not units: under the causal mask most
@@ -332,6 +335,11 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
       !make_map(&tk, u8, x->k_codes, d / 2, (uint64_t)dm.B * dm.Hkv * Lkvp, 1, d / 2, 128, qk_swz) ||
       !make_map(&tv, u8, x->v_codes, Lkvp / 2, (uint64_t)dm.B * dm.Hkv * d, 1, 64, d, CU_TENSOR_MAP_SWIZZLE_64B))
     return SA_ERR_CUDA;
+  // at most 16 query rows per kv head (decode): the decode kernel, unless
+  // stream-K was asked for
+  if (decode_eligible(dm) && nsplit != kStreamK)
+    return launch_attn_decode(tk, tv, *x, o, so, dm, causal, out_f32, nsplit, part, s) == cudaSuccess ? SA_OK
+                                                                                                      : SA_ERR_CUDA;
   return launch_attn_nvfp4(tq, tk, tv, *x, o, so, dm, causal, out_f32, nsplit, part, s) == cudaSuccess
              ? SA_OK
              : SA_ERR_CUDA;

@@ -343,6 +343,7 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
   asm volatile("" : SA_M8(r, 0), SA_M8(r, 8));
 }
+__device__ __forceinline__ void tmem_launder(uint32_t (&r)[16]) { asm volatile("" : SA_M8(r, 0), SA_M8(r, 8)); }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "

@@ -15,8 +15,8 @@
 // Eight lanes per row, four rows per warp; lane i of a row holds d/8
 // consecutive columns.  Small: it reads nsplit * d + 2 floats per row, from
 // L2 as a rule, so its cost is load latency and the per-row scalar work (the
-// weights 2^(m_s - M) and 1 / l); the loads of two partial rows are issued
-// together and the scalar work is shared by eight lanes instead of 32.
+// weights 2^(m_s - M) and 1 / l); the loads of up to four partial rows are
+// issued together and the scalar work is shared by eight lanes instead of 32.
 
 #include <cuda_bf16.h>
 
@@ -31,13 +31,13 @@ namespace {
 
 constexpr int kLanesPerRow = 8;                       // lanes sharing one output row
 constexpr int kRowsPerCta = 256 / kLanesPerRow;          // 256 threads, 32 rows
-constexpr int kSegBatch = 2;                             // partial rows whose loads are issued together
+constexpr int kSegBatch = 4;                             // partial rows whose loads are issued together
 
 // Merges the nseg partial rows seg(0), seg(1), ... of one output row; called
 // by the kLanesPerRow lanes of the row, lane i of them holding columns
 // [i*V, i*V + V), V = D / kLanesPerRow.  The loads of kSegBatch segments
 // (their (m, l) and their O rows) are issued before any is used, so a row
-// costs one memory round trip in the usual case of two segments; the
+// costs one memory round trip with up to four segments; the
 // arithmetic is the same in every case: M first, then the weighted sums in
 // segment order.
 template <int D, typename SegRow>
