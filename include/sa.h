@@ -260,13 +260,22 @@ sa_status sa_attn_fwd(const void* q, const void* k, const void* v, void* o,
  * range of (query-tile pair, key tile) items; a pair cut by a range
  * boundary is computed in segments and merged the same way.
  *
+ * Decode (NVFP4 path, at most 16 query rows per kv head: (H / Hkv) * Lq <=
+ * 16): a kernel laid out for few rows ("FlashAttention kernels" section 3,
+ * Flash-Decoding) takes the query rows of the G heads of a kv head together.
+ * Split-KV there cuts each (batch, kv head) pair's key range into shares;
+ * stream-K (-1) means equal ranges of all (pair, key tile) items, the pairs
+ * that ranges cut merged by a combine kernel.  The library's choice (0) is
+ * as many shares as let the pairs fill one wave of resident CTAs.
+ *
  * sa_attn_fwd_workspace_bytes: device workspace bytes sa_attn_fwd_ws needs
  *   for the given sizes and `nsplit`: 0 = the library's choice (NVFP4,
  *   non-causal: stream-K once the pairs fill the SMs; split-KV while the units leave at
  *   least half of the SMs idle and every share keeps 16 key tiles or more, at
- *   most 16 shares; else neither); 1 = one unit per CTA; n > 1 = n shares, at
- *   most one per key tile; -1 = stream-K (NVFP4 only).  0 when neither would
- *   be used, or for invalid or empty sizes.
+ *   most 16 shares; else neither; decode shapes: shares as above); 1 = one
+ *   unit per CTA; n > 1 = n shares, at most one per key tile; -1 = stream-K
+ *   (NVFP4 only).  0 when neither would be used, or for invalid or empty
+ *   sizes.
  * sa_attn_fwd_ws: sa_attn_fwd with split-KV or stream-K.  Arguments as
  *   sa_attn_fwd, plus nsplit as above and a caller-owned, 16-byte aligned
  *   device workspace of workspace_bytes.  With nsplit 0 a missing or short

@@ -146,8 +146,14 @@ cudaError_t launch_exp_path_selftest(const float* x, const float* y, int n, floa
 // kv head ((H / Hkv) * Lq <= 16: decode steps), the rows of a kv head's query
 // heads taken together; tk / tv as for launch_attn_nvfp4.  nsplit key shares
 // per (batch, kv head) (partial results and splitkv.cu's combine when > 1).
+// nsplit kStreamK: equal ranges of the (pair, key tile) items over
+// decode_range_ctas CTAs, partial results of cut pairs in a workspace of
+// decode_range_workspace_bytes (two slots of 16 rows per CTA).
 bool decode_eligible(const Dims& dm);
 int decode_nsplit(const Dims& dm, int sms);
+int decode_range_ctas(const Dims& dm, int sms);
+size_t decode_range_workspace_bytes(const Dims& dm, int sms);
+SplitOut decode_range_layout(void* ws, const Dims& dm, int sms);
 cudaError_t launch_attn_decode(const CUtensorMap& tk, const CUtensorMap& tv, const sa_fp4_qkv& x, void* o,
                                const Strides& so, const Dims& dm, int causal, bool out_f32, int nsplit,
                                const SplitOut& part, cudaStream_t s);

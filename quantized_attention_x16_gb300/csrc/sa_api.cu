@@ -250,8 +250,10 @@ static int resolve_nsplit(const Dims& dm, int causal, int mode, int requested) {
   if (requested == 1) return 1;
   if (requested == kStreamK) return kStreamK;
   const int sms = device_sm_count();
-  // few query rows per kv head (decode): the decode kernel, its key range
-  // split into shares so that the (batch, kv head) pairs fill the SMs twice
+  // few query rows per kv head (decode): the decode kernel, its key range cut
+  // into shares so that the (batch, kv head) pairs fill one wave of CTAs
+  // (equal ranges of (pair, key tile) items, kStreamK, measured slower:
+  // decode_gqa 60 against 45.6 us)
   if (requested == 0 && mode == SA_MODE_NVFP4 && decode_eligible(dm)) return decode_nsplit(dm, sms);
   if (requested == 0) {
     const long long pairs = (long long)(((dm.Lq + 127) / 128 + 1) / 2) * dm.B * dm.H;
@@ -269,6 +271,8 @@ static int resolve_nsplit(const Dims& dm, int causal, int mode, int requested) {
 }
 
 static size_t work_split_bytes(const Dims& dm, int causal, int nsplit) {
+  // (kStreamK is an NVFP4 schedule; for decode shapes, the decode kernel's ranges)
+  if (nsplit == kStreamK && decode_eligible(dm)) return decode_range_workspace_bytes(dm, device_sm_count());
   if (nsplit == kStreamK) {
     int ctas = 0;
     make_streamk_work(dm.B, dm.H, dm.Lq, dm.Lkv, causal, device_sm_count() > 0 ? device_sm_count() : 1, &ctas);
@@ -288,7 +292,8 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
   const int mode = mode_flags & 0xF;
   if (mode != SA_MODE_BF16 && mode != SA_MODE_NVFP4) return SA_ERR_INVALID_ARG;
   if (nsplit_req < kStreamK) return SA_ERR_INVALID_ARG;
-  if (nsplit_req == kStreamK && (mode != SA_MODE_NVFP4 || !streamk_fits(dm.B, dm.H, dm.Lq, dm.Lkv, causal)))
+  if (nsplit_req == kStreamK &&
+      (mode != SA_MODE_NVFP4 || (!decode_eligible(dm) && !streamk_fits(dm.B, dm.H, dm.Lq, dm.Lkv, causal))))
     return SA_ERR_UNSUPPORTED;
   if (empty_problem(dm)) return SA_OK;
   const bool out_f32 = (mode_flags & SA_OUT_FP32) != 0;
@@ -306,7 +311,9 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
   if (nsplit != 1 && !aligned16(workspace)) return SA_ERR_INVALID_ARG;
   SplitOut part{nullptr, nullptr};
   if (nsplit > 1) part = splitkv_layout(workspace, dm, nsplit);
-  if (nsplit == kStreamK) {
+  if (nsplit == kStreamK && decode_eligible(dm)) {
+    part = decode_range_layout(workspace, dm, device_sm_count());
+  } else if (nsplit == kStreamK) {
     int ctas = 0;
     make_streamk_work(dm.B, dm.H, dm.Lq, dm.Lkv, causal, device_sm_count() > 0 ? device_sm_count() : 1, &ctas);
     part = streamk_layout(workspace, dm, ctas);
@@ -335,9 +342,9 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
       !make_map(&tk, u8, x->k_codes, d / 2, (uint64_t)dm.B * dm.Hkv * Lkvp, 1, d / 2, 128, qk_swz) ||
       !make_map(&tv, u8, x->v_codes, Lkvp / 2, (uint64_t)dm.B * dm.Hkv * d, 1, 64, d, CU_TENSOR_MAP_SWIZZLE_64B))
     return SA_ERR_CUDA;
-  // at most 16 query rows per kv head (decode): the decode kernel, unless
-  // stream-K was asked for
-  if (decode_eligible(dm) && nsplit != kStreamK)
+  // at most 16 query rows per kv head (decode): the decode kernel (stream-K
+  // there means its balanced ranges)
+  if (decode_eligible(dm))
     return launch_attn_decode(tk, tv, *x, o, so, dm, causal, out_f32, nsplit, part, s) == cudaSuccess ? SA_OK
                                                                                                       : SA_ERR_CUDA;
   return launch_attn_nvfp4(tq, tk, tv, *x, o, so, dm, causal, out_f32, nsplit, part, s) == cudaSuccess

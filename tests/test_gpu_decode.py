@@ -7,8 +7,11 @@ NVFP4 path's (the same two-level P quantisation per row and key tile), so the
 bar is the NVFP4 parity bar of tests/test_gpu_attn.py.  Cases: GQA one-token
 decode with ragged caches, the 16-row maximum (G = 16, and G = 1 with 16
 tokens), a causal chunk whose rows see different key ranges, a cache of one
-key, forced key shares (one, two, more shares than fit evenly), and the full
-decode_gqa workload in both layouts (per head and folded).
+key, forced key shares (one, two, more shares than fit evenly), the balanced ranges
+(equal runs of (pair, key tile) items over the CTAs, nsplit -1 and the
+library's choice: a range may end inside one pair and start inside the next,
+or hold whole pairs), and the full decode_gqa workload in both layouts (per
+head and folded).
 """
 
 import numpy as np
@@ -42,7 +45,7 @@ def _id(c):
     return f"B{w['B']}H{w['H']}K{w['Hkv']}d{w['d']}-Lq{Lq}-Lkv{Lkv}"
 
 
-@pytest.mark.parametrize("nsplit", [None, 1, 2, 5])
+@pytest.mark.parametrize("nsplit", [None, -1, 1, 2, 5])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("case", DECODE, ids=_id)
 def test_decode_all_rows(sa, case, causal, nsplit):
@@ -90,3 +93,19 @@ def test_decode_full_size(sa, fold):
     heads = [(b, h) for b in (0, 7, 15) for h in (0, 5, 18, 31)]
     check(o.float().cpu().numpy(), x, False, heads, np.arange(1), "nvfp4", o32.float().cpu().numpy(),
           label=f"decode_gqa full {'folded' if fold else 'per head'}")
+
+
+@pytest.mark.parametrize("case", [
+    (dict(W.spec("causal_gqa"), B=16, H=32, Hkv=8, d=128, seed=208), 1, 1000),   # 1024 items: ranges of 1-2 tiles across pairs
+    (dict(W.spec("dit_video"), B=50, H=160, Hkv=40, d=64, seed=209), 1, 100),   # 2000 one-tile pairs: ranges of whole pairs
+], ids=lambda c: f"B{c[0]['B']}K{c[0]['Hkv']}d{c[0]['d']}-Lkv{c[2]}")
+def test_decode_ranges_across_pairs(sa, case):
+    """Ranges that end inside one pair and start inside the next, and ranges
+    of several whole pairs (written directly, no combine), on a sample of heads."""
+    w, Lq, Lkv = case
+    x = qk_inputs(w, Lq, Lkv)
+    o = run_qk(sa, x, False, "nvfp4", -1)
+    o32 = run_qk(sa, x, False, "nvfp4", -1, torch.float32)
+    B, H = w["B"], w["H"]
+    heads = sorted({(b, h) for b, h in [(0, 0), (0, H - 1), (B // 2, H // 3), (B - 1, 1), (B - 1, H - 1), (1, 7)]})
+    check(o, x, False, heads, np.arange(Lq), "nvfp4", o32, label=f"decode ranges {_id(case)}")
