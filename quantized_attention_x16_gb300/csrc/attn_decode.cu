@@ -140,14 +140,16 @@ struct DecSeg {
   bool direct;
 };
 __device__ __forceinline__ long long range_start(const DecArgs& a, int c) { return (long long)c * a.items / gridDim.x; }
+template <bool RANGES>
 __device__ __forceinline__ int dec_nseg(const DecArgs& a, int c) {
-  if (!a.ranges) return 1;
+  if constexpr (!RANGES) return 1;
   const long long i0 = range_start(a, c), i1 = range_start(a, c + 1);
   return i1 > i0 ? (int)((i1 - 1) / a.ntk - i0 / a.ntk + 1) : 0;
 }
+template <bool RANGES>
 __device__ __forceinline__ DecSeg dec_seg(const DecArgs& a, int c, int k) {
   DecSeg sg;
-  if (!a.ranges) {
+  if constexpr (!RANGES) {
     const int share = c % a.nsplit;
     sg.pair = c / a.nsplit;
     sg.j0 = (int)((long long)share * a.ntk / a.nsplit);
@@ -173,7 +175,7 @@ constexpr int dec_ctas_per_sm() {
   return NR <= 4 ? 4 : 2;
 }
 
-template <int D, int NR, bool OUT32>
+template <int D, int NR, bool OUT32, bool RANGES>
 __global__ void __launch_bounds__(kDecThreads, dec_ctas_per_sm<NR>())
     attn_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                        const DecArgs a) {
@@ -202,13 +204,13 @@ __global__ void __launch_bounds__(kDecThreads, dec_ctas_per_sm<NR>())
   const int Lqp = (a.Lq + 127) & ~127, Lkvp = (a.Lkv + 127) & ~127;
   const int G = a.H / a.Hkv;
   const int cta = blockIdx.x;
-  const int nseg = dec_nseg(a, cta);
+  const int nseg = dec_nseg<RANGES>(a, cta);
   const int nr = a.nr;                   // valid rows: r = g * Lq + t, query head kvh * G + g, token t
   // the segments' key tiles laid end to end: global tile g = gbase(k) + j
   // (barrier phases, stages and buffers count g over the whole list)
   int gtotal = 0;
   for (int k = 0; k < nseg; ++k) {
-    const DecSeg sg = dec_seg(a, cta, k);
+    const DecSeg sg = dec_seg<RANGES>(a, cta, k);
     gtotal += sg.j1 - sg.j0;
   }
 
@@ -255,7 +257,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_ctas_per_sm<NR>())
     pdl_wait();                                          // the codes are written (programmatic launch)
     int nk = 0, nv = 0, nq = 0;
     int kseg = 0, jseg = 0;                              // the segment and local tile of K step g
-    DecSeg sg = nseg > 0 ? dec_seg(a, cta, 0) : DecSeg{0, 0, 0, 0, true};
+    DecSeg sg = nseg > 0 ? dec_seg<RANGES>(a, cta, 0) : DecSeg{0, 0, 0, 0, true};
     int vseg = 0, vj = 0;                                // the segment and local tile of V step g - 1
     DecSeg vsg = sg;
     for (int g = 0; ok && g <= gtotal; ++g) {
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_ctas_per_sm<NR>())
         while (jseg >= sg.j1 - sg.j0) {                  // (segments have at least one tile)
           ++kseg;
           jseg = 0;
-          sg = dec_seg(a, cta, kseg);
+          sg = dec_seg<RANGES>(a, cta, kseg);
         }
         if (jseg == 0) {
           // Q^T of segment kseg: rows r < nr gathered from their heads' rows
@@ -321,7 +323,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_ctas_per_sm<NR>())
         while (vj >= vsg.j1 - vsg.j0) {
           ++vseg;
           vj = 0;
-          vsg = dec_seg(a, cta, vseg);
+          vsg = dec_seg<RANGES>(a, cta, vseg);
         }
         const int ja = vsg.j0 + vj;
         const long long bhk = vsg.pair;
@@ -373,7 +375,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_ctas_per_sm<NR>())
         if (jseg >= nseg_tiles) {
           ++kseg;
           jseg = 0;
-          const DecSeg sg = dec_seg(a, cta, kseg);
+          const DecSeg sg = dec_seg<RANGES>(a, cta, kseg);
           nseg_tiles = sg.j1 - sg.j0;
           const int qb = kseg & 1;
           ok = mbar_wait_warp(q_full + qb, (kseg >> 1) & 1, abort_flag, a.wait_ns);
@@ -410,7 +412,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_ctas_per_sm<NR>())
         if (pseg_j >= pseg_n) {
           ++pk;
           pseg_j = 0;
-          const DecSeg sg = dec_seg(a, cta, pk);
+          const DecSeg sg = dec_seg<RANGES>(a, cta, pk);
           pseg_n = sg.j1 - sg.j0;
         }
         ok = mbar_wait_warp(v_full + s, (gv / C::NSV) & 1, abort_flag, a.wait_ns) &&
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_ctas_per_sm<NR>())
     for (int r = 0; r < NR; ++r) lim[r] = r >= nr ? 0 : (a.causal ? r % a.Lq + a.Lkv - a.Lq + 1 : a.Lkv);
     int g = 0;                                           // global tile
     for (int kseg = 0; ok && kseg < nseg; ++kseg) {
-      const DecSeg sg = dec_seg(a, cta, kseg);
+      const DecSeg sg = dec_seg<RANGES>(a, cta, kseg);
       const int nt = sg.j1 - sg.j0;
       float m_run[NR], m_ref0[NR], m_ref1[NR], lam0[NR], lam1[NR];
       uint32_t href0 = 0u, href1 = 0u;                   // bit r: row r has had a live tile in that accumulator
@@ -630,7 +632,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_ctas_per_sm<NR>())
           } else {
             // shares: share `slot` of padded row (b * H + h) * Lqp + t;
             // ranges: row r of slot `slot`
-            const long long R = a.ranges ? (long long)sg.slot * kNR + r : (long long)sg.slot * a.rows + bhq * Lqp + t;
+            const long long R = RANGES ? (long long)sg.slot * kNR + r : (long long)sg.slot * a.rows + bhq * Lqp + t;
             a.part.o[R * D + k] = ov;
             if (k == 0) *reinterpret_cast<float2*>(a.part.ml + 2 * R) = make_float2(mm[r], l);
           }
@@ -730,7 +732,10 @@ cudaError_t launch_dec(const CUtensorMap& tk, const CUtensorMap& tv, const sa_fp
   using C = CfgDec<D>;
   static std::atomic<bool> attr_done[kMaxDevices];   // kernel attributes are per device
   cudaError_t e = once_per_device(attr_done, [] {
-    return cudaFuncSetAttribute(attn_decode_kernel<D, NR, OUT32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t r = cudaFuncSetAttribute(attn_decode_kernel<D, NR, OUT32, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (r != cudaSuccess) return r;
+    return cudaFuncSetAttribute(attn_decode_kernel<D, NR, OUT32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::kSmemBytes);
   });
   if (e != cudaSuccess) return e;
@@ -759,7 +764,9 @@ cudaError_t launch_dec(const CUtensorMap& tk, const CUtensorMap& tv, const sa_fp
   // the kernel before; the producer waits for it before its first load
   cudaLaunchAttribute attr;
   const cudaLaunchConfig_t cfg = pdl_launch_config(dim3(ctas), dim3(kDecThreads), C::kSmemBytes, s, &attr);
-  e = cudaLaunchKernelEx(&cfg, attn_decode_kernel<D, NR, OUT32>, tk, tv, a);
+  // (the shares' instantiation has the one-segment list folded in)
+  e = a.ranges ? cudaLaunchKernelEx(&cfg, attn_decode_kernel<D, NR, OUT32, true>, tk, tv, a)
+               : cudaLaunchKernelEx(&cfg, attn_decode_kernel<D, NR, OUT32, false>, tk, tv, a);
   if (e != cudaSuccess) return e;
   if (a.ranges) {
     cudaLaunchAttribute attr2;
