@@ -198,6 +198,12 @@ def run_ours(args, rank, world, local_rank):
     fold = Lq == 1 and H > Hkv
     if fold:
         q, H, Lq, causal = q.view(B, Hkv, H // Hkv, d), Hkv, H // Hkv, False
+    # at most 16 query rows per kv head: the library's decode kernel (4, 8 or
+    # 16 rows), HBM-bound by design; else the prefill kernel
+    nr = (H // Hkv) * Lq
+    decode = nr <= 16
+    kname4 = (f"attn_decode_kernel<{d}, {4 if nr <= 4 else 8 if nr <= 8 else 16}>" if decode
+              else f"attn_nvfp4_kernel<{d}>")
     fq = sa.FP4QKV(B, H, Hkv, Lq, d, device=dev, Lkv=L)
     o4 = torch.empty_like(q)
     o16 = torch.empty_like(q)
@@ -274,7 +280,8 @@ def run_ours(args, rank, world, local_rank):
     mean = lambda xs: sum(xs) / len(xs)   # noqa: E731
     t_q, t_4, t_16, t_path = mean(tq), mean(t4), mean(t16), mean(tp)
     # rank 0's own launches for the per-kernel rooflines (its share of the problem)
-    w_local = dict(w, B=B, H=H, Hkv=Hkv)
+    # (a folded decode: H = Hkv heads of Lq = G rows each, the same work)
+    w_local = dict(w, B=B, H=H, Hkv=Hkv, Lq=Lq, causal=causal)
     fl_local = W.flops(w_local)
     lq_, l4_, l16_ = t_q, t_4, t_16
     # the slowest rank sets each time of the whole problem (no-ops at N = 1)
@@ -372,9 +379,9 @@ def run_ours(args, rank, world, local_rank):
             "bf16_attn_us": t_16 * 1e6,
             "bf16_frac_of_measured_peak": a16 / pk["bf16"],
         },
-        "roofline": {"kernel": f"attn_nvfp4_kernel<{d}>", "bound": "tensor", "achieved": a4, "peak": nvfp4_peak,
+        "roofline": {"kernel": kname4, "bound": "tensor", "achieved": a4, "peak": nvfp4_peak,
                      "unit": "TFLOP/s", "frac": a4 / nvfp4_peak,
-                     "traffic": prof.get("attn_nvfp4"),
+                     "traffic": prof.get("attn_decode" if decode else "attn_nvfp4"),
                      "peak_src": (f"measured NVFP4 MMA rate {NVFP4_FLOP_PER_CLK_SM} FLOP/clk/SM (fp4_mma_rate probe) x {sms} "
                                   f"SMs x {pk['sm_max_mhz']} MHz max SM clock"),
                      "peak_nominal_ratio": nvfp4_nominal_ratio_peak,
@@ -385,13 +392,18 @@ def run_ours(args, rank, world, local_rank):
         "roofline_bf16": {"kernel": f"attn_bf16_kernel<{d}>", "bound": "tensor", "achieved": a16, "peak": pk["bf16"],
                           "unit": "TFLOP/s", "frac": a16 / pk["bf16"], "traffic": prof.get("attn_bf16"),
                           "peak_src": f"{pk['src']} bf16 burst"},
-        "roofline_quantize": {"kernel": "sa_quantize (2 kernels)", "bound": "hbm", "achieved": qbytes / lq_ / 1e9,
+        "roofline_quantize": {"kernel": f"sa_quantize (quant_kernel<{d}, 1> + quant_kernel<{d}, 2>)", "bound": "hbm",
+                              "achieved": qbytes / lq_ / 1e9,
                               "peak": pk["hbm"], "unit": "GB/s", "frac": qbytes / lq_ / 1e9 / pk["hbm"],
-                              "traffic": None, "algorithmic_bytes": qbytes,
-                              "traffic_kernels": {k: prof.get(k) for k in ("quant_v_mean_kernel", "quant_qk_kernel")}},
-        "roofline_hbm_attn": {"kernel": f"attn_nvfp4_kernel<{d}>", "bound": "hbm (context: the bound of few-query "
-                              "shapes such as decode)", "achieved": attn_bytes / l4_ / 1e9, "peak": pk["hbm"],
-                              "unit": "GB/s", "frac": attn_bytes / l4_ / 1e9 / pk["hbm"],
+                              "traffic": (prof["quant_pass1"] + prof["quant_pass2"]
+                                          if "quant_pass1" in prof and "quant_pass2" in prof else None),
+                              "algorithmic_bytes": qbytes,
+                              "traffic_kernels": {"pass 1 (Q, K mean)": prof.get("quant_pass1"),
+                                                  "pass 2 (V, K')": prof.get("quant_pass2")}},
+        "roofline_hbm_attn": {"kernel": kname4, "bound": "hbm" + ("" if decode else " (context: the bound of "
+                              "few-query shapes such as decode)"), "achieved": attn_bytes / l4_ / 1e9,
+                              "peak": pk["hbm"], "unit": "GB/s", "frac": attn_bytes / l4_ / 1e9 / pk["hbm"],
+                              "traffic": prof.get("attn_decode") if decode else None,
                               "algorithmic_bytes": attn_bytes},
         "cpu_baseline": cpu,
         "e2e": e2e if e2e is not None else {"value": None, "unit": "TOPS", "h2d_bytes_per_step": 0,
@@ -401,6 +413,11 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
+    if decode:
+        # the decode kernel reads the whole K/V cache once per call: its
+        # primary roofline is HBM; the tensor figure stays beside it
+        line["roofline_tensor"] = line["roofline"]
+        line["roofline"] = line.pop("roofline_hbm_attn")
     print(json.dumps(line), flush=True)
 
 
@@ -435,13 +452,12 @@ def quant_bytes(w):
 
 def attn_nvfp4_bytes(w):
     """Algorithmic HBM bytes of one NVFP4 attention call: read the FP4 codes and
-    e4m3 scales of Q, K, V (0.5 + 1/16 B per element, padded lengths), write O
-    (bf16)."""
+    e4m3 scales of Q, K, V once (0.5 + 1/16 B per element of the problem, no
+    tile padding), write O (bf16)."""
     B, H, Hkv, L, d = w["B"], w["H"], w["Hkv"], w["L"], w["d"]
     Lq = W.lq(w)
-    pad = lambda n: (n + 127) // 128 * 128   # noqa: E731
     fp4 = 0.5 + 1 / 16
-    return (B * H * pad(Lq) * d + 2 * B * Hkv * pad(L) * d) * fp4 + 2 * B * H * Lq * d
+    return (B * H * Lq * d + 2 * B * Hkv * L * d) * fp4 + 2 * B * H * Lq * d
 
 
 def load_profile_traffic():
