@@ -17,6 +17,14 @@ definition of exact attention); causal = top-left aligned square mask
 (key j visible to query i iff j <= i); the first-level P factor is taken per
 row and per KV tile, s1 = rowmax_tile(p~) / 2688; the row sum l adds the
 unquantised p~; the P.V products of a tile are multiplied by s1.
+
+Smooth-Q variant (page "kernel overview", evolution chain "Smooth-K ->
+Smooth-Q+K"): Q is quantised as Q' = Q - mean of its 128-token block
+(oracle/quant.py) and the scores get the block mean's share back, dS =
+qbar K^'^T.  Reading: dS uses the same dequantised smoothed keys K^' as the
+quantised product, so the scores are (Q^' + qbar) K^'^T -- only Q's
+representation changes -- and everything after the scores is the SA3 tile
+loop unchanged.
 """
 
 import numpy as np
@@ -190,6 +198,29 @@ def dequantized_operands(q, k, v):
     L = np.asarray(v).shape[-2]
     vd = np.swapaxes(dequantize_groups(vc, vs), -1, -2)[..., :L, :]     # drop V's zero completion
     return (qd, kd, vd), dict(mu=mu, qc=qc, qs=qs, kc=kc, ks=ks, vc=vc, vs=vs)
+
+
+def smooth_q_correction(qbar, kd):
+    """The score correction of smooth-Q for one head: dS[i, j] = qbar_i . K^'_j,
+    for block i of the queries and key j (float64).  qbar [nb, d], kd [L, d]
+    the dequantised smoothed keys.  With it the scores of a query row t are
+    Q^'_t K^'^T + dS[t // block] = (Q^'_t + qbar[t // block]) K^'^T."""
+    return np.asarray(qbar, np.float64) @ np.asarray(kd, np.float64).T
+
+
+def dequantized_operands_sq(q, k, v, block=None):
+    """``dequantized_operands`` for the smooth-Q variant: the query operand is
+    Q^' + qbar (float64, the block mean added back to the dequantised Q'
+    rows), so that the emulation's scores are Q^' K^'^T + dS.  The raw
+    results add ``qbar`` [B, H, nb, d] and the Q' codes and scales."""
+    from . import quant
+    block = quant.SQ_BLOCK if block is None else block
+    (_, kd, vd), raw = dequantized_operands(q, k, v)
+    qc, qs, qbar = quant.quantize_q_smooth(q, block)
+    blk = np.arange(np.asarray(q).shape[2]) // block
+    qd = dequantize_groups(qc, qs) + np.asarray(qbar, np.float64)[:, :, blk, :]
+    raw.update(qc=qc, qs=qs, qbar=qbar)
+    return (qd, kd, vd), raw
 
 
 def cosine_per_head(a, b):

@@ -16,6 +16,15 @@ Readings (the pages give no formulas):
 * the K mean is an FP32 sum in a fixed order -- 128-token chunks summed
   token by token, then the chunk sums summed chunk by chunk, then divided by
   L -- so that a kernel following the same order reproduces it bit for bit.
+
+Smooth-Q (the SageAttention2 step of the evolution chain on page "kernel
+overview": "Smooth-K -> Smooth-Q+K"; a labelled variant of the SA3 path).
+Readings (the pages give no formulas):
+* the Q block is the attention kernel's query tile: 128 consecutive tokens of
+  one head (the last block of a head may be shorter);
+* the block mean is an FP32 sum of the block's tokens, token by token from
+  0.0, divided by their count (IEEE float32), per channel;
+* Q' = fl32(q - mean) is quantised as Q is (1x16 groups along d).
 """
 
 import numpy as np
@@ -24,6 +33,7 @@ from .formats import E2M1_MAGNITUDES, e2m1_encode, e4m3_encode, e4m3_decode
 
 GROUP = 16
 KMEAN_CHUNK = 128
+SQ_BLOCK = 128
 
 
 def k_mean(k):
@@ -78,6 +88,38 @@ def dequantize_groups(codes, scales):
 def quantize_q(q):
     """Q [B,H,L,d] float32 -> (codes [B,H,L,d], scales [B,H,L,d/16]), groups along d."""
     return quantize_groups(q)
+
+
+def q_block_mean(q, block=SQ_BLOCK):
+    """Per-block mean of Q over tokens, per channel (smooth-Q), FP32.
+
+    q float32 [B, H, L, d] (exact bf16 values).  Block i holds tokens
+    [block*i, min(L, block*(i+1))); its tokens are summed token by token from
+    0.0 and the sum is divided by their count.  Returns float32
+    [B, H, ceil(L / block), d]."""
+    q = np.asarray(q, dtype=np.float32)
+    B, H, L, d = q.shape
+    nb = -(-L // block)
+    out = np.zeros((B, H, nb, d), dtype=np.float32)
+    for i in range(nb):
+        t0, t1 = i * block, min(L, (i + 1) * block)
+        part = np.zeros((B, H, d), dtype=np.float32)
+        for t in range(t0, t1):
+            part = part + q[:, :, t, :]
+        out[:, :, i, :] = part / np.float32(t1 - t0)
+    return out
+
+
+def quantize_q_smooth(q, block=SQ_BLOCK):
+    """Smooth-Q then quantise: Q' = fl32(q - mean of the token's block);
+    groups along d.  Returns (codes [B,H,L,d], scales [B,H,L,d/16], the block
+    means [B,H,nb,d])."""
+    q = np.asarray(q, dtype=np.float32)
+    qbar = q_block_mean(q, block)
+    blk = np.arange(q.shape[2]) // block
+    qp = (q - qbar[:, :, blk, :]).astype(np.float32)
+    codes, scales = quantize_groups(qp)
+    return codes, scales, qbar
 
 
 def quantize_k(k, mu):
