@@ -55,7 +55,9 @@ typedef enum {
   SA_ERR_TIMEOUT = 4
 } sa_status;
 
-typedef enum { SA_MODE_BF16 = 0, SA_MODE_NVFP4 = 1 } sa_mode;
+/* SA_MODE_NVFP4_SQ: the NVFP4 path with SageAttention2's smooth-Q added (a
+ * labelled variant; see sa_quantize_smooth_q). */
+typedef enum { SA_MODE_BF16 = 0, SA_MODE_NVFP4 = 1, SA_MODE_NVFP4_SQ = 2 } sa_mode;
 
 /* Output-format flag OR-ed into the `mode` argument of sa_attn_fwd: with it,
  * o is float32 [B, H, L, d] (the FP32 accumulator divided by the row sum,
@@ -226,6 +228,45 @@ sa_status sa_quantize_s(const void* q, const void* k, const void* v, const sa_sh
 sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v,
                                      int B, int H, int Hkv, int L, int d,
                                      const sa_fp4_qkv* out, sa_stream_t stream);
+
+/*
+ * Smooth-Q variant ("kernel overview", SageAttention evolution chain: "Smooth-K
+ * -> Smooth-Q+K"; the SageAttention2 step, kept beside the SA3 path as a
+ * labelled variant).  Q is quantised as Q' = Q - qbar_i, qbar_i the mean of
+ * its 128-token block i (the attention kernel's query tile of one head:
+ * float32 sum of the block's valid rows, row by row from 0, divided by their
+ * count; Q' = RN(q - qbar_i), then 1x16 NVFP4 as sa_quantize does), and the
+ * attention kernel adds the block mean's share of the scores back:
+ *   S = Q^' K^'^T + dS,  dS[i, j] = qbar_i . K^'_j  (= (Q^' + qbar_i) K^'^T)
+ * with K^' the dequantised smoothed keys.  dS is float32: per 1x16 group an
+ * FMA chain over its channels, then the group sums times the group scales in
+ * group order; the rest is the NVFP4 path unchanged.
+ *
+ * sa_fp4_sq: the sa_fp4_qkv buffers plus q_mean [B, H, Lqp/128, d] and ds
+ *   [B, H, Lqp/128, Lkvp] (float32; Lqp, Lkvp the lengths rounded up to 128).
+ * sa_smooth_q_bytes_s: device bytes of one blob holding q_mean and ds at
+ *   256-byte aligned offsets (offsets_out, may be NULL, receives 2); 0 for
+ *   invalid or empty sizes.  sa_smooth_q_from_blob_s sets out->q_mean and
+ *   out->ds into such a blob (out->fp4 is left as it is).
+ * sa_quantize_smooth_q: run after sa_quantize(_s) of the same q, k, v into
+ *   x->fp4 (it reads the K codes and scales): overwrites x->fp4.q_codes and
+ *   q_sf with those of Q', writes q_mean and ds.  flags: 0 or SA_LAYOUT_BLHD
+ *   (the layout of q).  Two kernels on `stream` (plain launches); bit-exact
+ *   codes, scales and means.
+ * sa_attn_fwd(_ws, _s) with mode SA_MODE_NVFP4_SQ: q points to a host
+ *   `const sa_fp4_sq*`; otherwise as SA_MODE_NVFP4 (the few-row decode kernel
+ *   is not used: such shapes run on the prefill kernel).  sa_attn_fwd_host
+ *   does not take it (SA_ERR_UNSUPPORTED).
+ */
+typedef struct {
+  sa_fp4_qkv fp4;
+  float* q_mean;
+  float* ds;
+} sa_fp4_sq;
+size_t sa_smooth_q_bytes_s(const sa_shape* shape, size_t offsets_out[2]);
+sa_status sa_smooth_q_from_blob_s(void* blob, const sa_shape* shape, sa_fp4_sq* out);
+sa_status sa_quantize_smooth_q(const void* q, const sa_shape* shape, int flags, const sa_fp4_sq* x,
+                               sa_stream_t stream);
 
 /*
  * sa_attn_fwd -- fused attention forward, O = softmax(Q K^T / sqrt(d)) V,

@@ -12,7 +12,9 @@ Names follow the C ABI:
 * ``sa_fp4_qkv_bytes`` / ``FP4QKV``   -- the caller-owned quantised-operand blob
 * ``sa_quantize(q, k, v, out=None)``  -- smooth-K + NVFP4 quantisation of Q, K, V
 * ``sa_quantize_static_scratch(...)`` -- the same without caller-provided scratch
-* ``sa_attn_fwd(q, k, v, o=None, causal=False, mode="bf16"|"nvfp4")``
+* ``sa_attn_fwd(q, k, v, o=None, causal=False, mode="bf16"|"nvfp4"|"nvfp4_sq")``
+* ``sa_quantize(..., smooth_q=True)`` -- also the smooth-Q variant's Q' codes,
+  block means and score corrections (``sa_quantize_smooth_q``), for mode "nvfp4_sq"
 * ``sa_attn_fwd_host(q, k, v, o=None, causal=False, mode=...)`` -- the same on
   pinned host tensors, copies overlapped with compute inside the library
 * ``sa_last_device_error()``, ``sa_selftest_wait_timeout(ns)``, ``sa_version()``
@@ -25,7 +27,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libsa.so")
 
 SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA, SA_ERR_TIMEOUT = range(5)
-SA_MODE_BF16, SA_MODE_NVFP4 = 0, 1
+SA_MODE_BF16, SA_MODE_NVFP4, SA_MODE_NVFP4_SQ = 0, 1, 2
+_MODES = {"bf16": SA_MODE_BF16, "nvfp4": SA_MODE_NVFP4, "nvfp4_sq": SA_MODE_NVFP4_SQ}
 SA_OUT_FP32 = 16
 SA_LAYOUT_BLHD = 32
 SA_HOST_OVERLAP = 64
@@ -37,6 +40,7 @@ EXPORTS = ("sa_fp4_qkv_bytes", "sa_fp4_qkv_from_blob", "sa_quantize", "sa_quanti
            "sa_fp4_qkv_bytes_s", "sa_fp4_qkv_from_blob_s", "sa_quantize_s", "sa_attn_fwd_workspace_bytes_s",
            "sa_attn_fwd_s",
            "sa_attn_fwd_host_workspace_bytes", "sa_attn_fwd_host",
+           "sa_smooth_q_bytes_s", "sa_smooth_q_from_blob_s", "sa_quantize_smooth_q",
            "sa_status_string", "sa_last_device_error", "sa_selftest_wait_timeout", "sa_selftest_nvfp4_score_tile",
            "sa_selftest_exp_path", "sa_version")
 SA_STATIC_SCRATCH_FLOATS = 1 << 20
@@ -46,6 +50,12 @@ class SaFp4Qkv(ctypes.Structure):
     """Mirror of ``sa_fp4_qkv`` (eight device pointers)."""
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("q_codes", "q_sf", "k_codes", "k_sf", "v_codes", "v_sf", "k_mean", "workspace")]
+
+
+class SaFp4Sq(ctypes.Structure):
+    """Mirror of ``sa_fp4_sq``: the sa_fp4_qkv plus the smooth-Q block means
+    and score corrections."""
+    _fields_ = [("fp4", SaFp4Qkv), ("q_mean", ctypes.c_void_p), ("ds", ctypes.c_void_p)]
 
 
 class SaShape(ctypes.Structure):
@@ -74,6 +84,12 @@ def _load():
     lib.sa_fp4_qkv_from_blob_s.restype = i
     lib.sa_quantize_s.argtypes = [vp, vp, vp, shp, i, ctypes.POINTER(SaFp4Qkv), vp]
     lib.sa_quantize_s.restype = i
+    lib.sa_smooth_q_bytes_s.argtypes = [shp, ctypes.POINTER(sz)]
+    lib.sa_smooth_q_bytes_s.restype = sz
+    lib.sa_smooth_q_from_blob_s.argtypes = [vp, shp, ctypes.POINTER(SaFp4Sq)]
+    lib.sa_smooth_q_from_blob_s.restype = i
+    lib.sa_quantize_smooth_q.argtypes = [vp, shp, i, ctypes.POINTER(SaFp4Sq), vp]
+    lib.sa_quantize_smooth_q.restype = i
     lib.sa_attn_fwd_workspace_bytes_s.argtypes = [shp, i, i, i]
     lib.sa_attn_fwd_workspace_bytes_s.restype = sz
     lib.sa_attn_fwd_s.argtypes = [vp, vp, vp, vp, shp, i, i, i, vp, sz, vp]
@@ -177,6 +193,33 @@ class FP4QKV:
         self.struct = SaFp4Qkv()
         _check(lib.sa_fp4_qkv_from_blob_s(_ptr(self.blob), ctypes.byref(self.shape), ctypes.byref(self.struct)),
                "sa_fp4_qkv_from_blob_s")
+        self.sq = None          # the smooth-Q buffers (sa_fp4_sq), once sa_quantize(smooth_q=True) made them
+
+    def _smooth_q_struct(self):
+        """Allocates the smooth-Q blob on first use; returns the sa_fp4_sq."""
+        import torch
+        if self.sq is None:
+            offs = (ctypes.c_size_t * 2)()
+            n = int(lib.sa_smooth_q_bytes_s(ctypes.byref(self.shape), offs))
+            if n == 0:
+                raise SaError(SA_ERR_UNSUPPORTED, "sa_smooth_q_bytes_s")
+            self.sq_offsets = [int(o) for o in offs]
+            self.sq_blob = torch.empty(n, dtype=torch.uint8, device=self.blob.device)
+            self.sq = SaFp4Sq()
+            _check(lib.sa_smooth_q_from_blob_s(_ptr(self.sq_blob), ctypes.byref(self.shape), ctypes.byref(self.sq)),
+                   "sa_smooth_q_from_blob_s")
+        self.sq.fp4 = self.struct
+        return self.sq
+
+    def sq_views(self):
+        """Torch views of the smooth-Q buffers: q_mean [B, H, Lqp/128, d] and
+        ds [B, H, Lqp/128, Lkvp] (float32)."""
+        import torch
+        B, H, Hkv, L, d = self.dims
+        nqt, Lkp = -(-L // 128), -(-self.Lkv // 128) * 128
+        qm = self.sq_blob[self.sq_offsets[0]:self.sq_offsets[0] + B * H * nqt * d * 4].view(torch.float32)
+        ds = self.sq_blob[self.sq_offsets[1]:self.sq_offsets[1] + B * H * nqt * Lkp * 4].view(torch.float32)
+        return dict(q_mean=qm.view(B, H, nqt, d), ds=ds.view(B, H, nqt, Lkp))
 
     def views(self):
         """Torch views of each region, shaped as documented in sa.h."""
@@ -215,9 +258,12 @@ def _dims(q, k, layout):
     raise ValueError(f"unknown layout {layout!r}")
 
 
-def sa_quantize(q, k, v, out=None, stream=None, layout="bhld"):
+def sa_quantize(q, k, v, out=None, stream=None, layout="bhld", smooth_q=False):
     """Smooth-K + NVFP4 quantisation of bf16 tensors (layout "bhld" or
-    "blhd"); returns an FP4QKV (the quantised layout is the same either way)."""
+    "blhd"); returns an FP4QKV (the quantised layout is the same either way).
+    smooth_q=True: then sa_quantize_smooth_q (Q re-quantised as Q minus its
+    128-token block means, the block means and the score corrections), for
+    sa_attn_fwd(mode="nvfp4_sq")."""
     _bf16_cuda(q, "q"), _bf16_cuda(k, "k"), _bf16_cuda(v, "v")
     (B, H, Hkv, L, Lkv, d), flag = _dims(q, k, layout)
     if out is None:
@@ -225,6 +271,10 @@ def sa_quantize(q, k, v, out=None, stream=None, layout="bhld"):
     shape = SaShape(B, H, Hkv, L, Lkv, d)
     _check(lib.sa_quantize_s(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shape), flag, ctypes.byref(out.struct),
                              _stream(stream)), "sa_quantize_s")
+    if smooth_q:
+        sq = out._smooth_q_struct()
+        _check(lib.sa_quantize_smooth_q(_ptr(q), ctypes.byref(shape), flag, ctypes.byref(sq), _stream(stream)),
+               "sa_quantize_smooth_q")
     return out
 
 
@@ -243,7 +293,7 @@ def sa_quantize_static_scratch(q, k, v, out=None, stream=None):
 
 
 def sa_attn_fwd_workspace_bytes(B, H, Hkv, L, d, causal=False, mode="bf16", nsplit=0, Lkv=None):
-    m = {"bf16": SA_MODE_BF16, "nvfp4": SA_MODE_NVFP4}[mode]
+    m = _MODES[mode]
     shape = SaShape(B, H, Hkv, L, L if Lkv is None else Lkv, d)
     return int(lib.sa_attn_fwd_workspace_bytes_s(ctypes.byref(shape), int(bool(causal)), m, int(nsplit)))
 
@@ -252,6 +302,8 @@ def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=
                 nsplit=None, workspace=None, layout="bhld"):
     """Fused attention forward.  mode "bf16": q, k, v bf16 BHLD tensors.
     mode "nvfp4": q is an FP4QKV from sa_quantize, k and v None.
+    mode "nvfp4_sq": the smooth-Q variant, q an FP4QKV from
+    sa_quantize(smooth_q=True).
     out_dtype: torch.bfloat16 (default) or torch.float32 (SA_OUT_FP32).
     nsplit None: sa_attn_fwd (no split-KV); otherwise sa_attn_fwd_ws with that
     nsplit (0 = the library's choice) and `workspace` (a uint8 CUDA tensor,
@@ -267,13 +319,18 @@ def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=
         args = (_ptr(q), _ptr(k), _ptr(v))
         m = SA_MODE_BF16
         dev = q.device
-    elif mode == "nvfp4":
+    elif mode in ("nvfp4", "nvfp4_sq"):
         if not isinstance(q, FP4QKV) or k is not None or v is not None:
-            raise ValueError("nvfp4 mode takes an FP4QKV as q and no k, v")
+            raise ValueError(f"{mode} mode takes an FP4QKV as q and no k, v")
         B, H, Hkv, L, d = q.dims
         Lkv = q.Lkv
-        args = (ctypes.cast(ctypes.pointer(q.struct), ctypes.c_void_p), None, None)
-        m = SA_MODE_NVFP4
+        if mode == "nvfp4_sq":
+            if q.sq is None:
+                raise ValueError("nvfp4_sq mode takes an FP4QKV from sa_quantize(..., smooth_q=True)")
+            args = (ctypes.cast(ctypes.pointer(q._smooth_q_struct()), ctypes.c_void_p), None, None)
+        else:
+            args = (ctypes.cast(ctypes.pointer(q.struct), ctypes.c_void_p), None, None)
+        m = _MODES[mode]
         dev = q.blob.device
     else:
         raise ValueError(f"unknown mode {mode!r}")

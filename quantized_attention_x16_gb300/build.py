@@ -15,7 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsa.so")
-SOURCES = ["sa_api.cu", "quant.cu", "attn_bf16.cu", "attn_nvfp4.cu", "attn_decode.cu", "splitkv.cu", "host_pipe.cu"]
+SOURCES = ["sa_api.cu", "quant.cu", "attn_bf16.cu", "attn_nvfp4.cu", "attn_decode.cu", "splitkv.cu", "host_pipe.cu",
+           "smooth_q.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-I" + os.path.join(os.path.dirname(HERE), "include")]

@@ -42,6 +42,14 @@
 // first K/V tiles load, and its first S is computed, while the softmax warps
 // finish the current one.  Q and its scales are double-buffered by unit
 // parity.
+//
+// Smooth-Q variant (SQ; page "kernel overview", evolution chain "Smooth-K ->
+// Smooth-Q+K"): Q' = Q - (its 128-row tile's mean) was quantised instead of
+// Q, and each score gets the tile mean's share back before the softmax:
+// S = Q^' K^'^T + dS[query tile][key], dS from smooth_q.cu.  The softmax
+// warpgroup of a query tile stages its 512-byte dS row of each key tile in
+// shared memory (a bulk copy issued by its thread 0 one tile ahead, three
+// buffers) and adds it to the scores; the rest is unchanged.
 
 #include <cuda_bf16.h>
 
@@ -60,6 +68,10 @@ constexpr int kSoftmaxRegs = 200;   // 8 softmax warps
 constexpr int kOtherRegs = 96;      // producer / MMA warpgroup
 constexpr int kLaunchRegs = 168;    // 65536 / 384 rounded down to a multiple of 8
 static_assert(8 * 32 * kSoftmaxRegs + 4 * 32 * kOtherRegs <= kThreads * kLaunchRegs, "register split");
+// smooth-Q: the softmax warps also stage and add the score corrections
+// (measured on llm_prefill: 296 -> 280 us with 8 more registers each)
+constexpr int kSoftmaxRegsSq = 208, kOtherRegsSq = 80;
+static_assert(8 * 32 * kSoftmaxRegsSq + 4 * 32 * kOtherRegsSq <= kThreads * kLaunchRegs, "register split");
 constexpr float kLog2PRange = 11.392317422778761f;   // log2(448 * 6)
 constexpr float kSkipBelow = 64.0f;                   // log2 units
 
@@ -83,8 +95,10 @@ struct CfgF4 {
   static constexpr int kOffKSf = kOffQSf + 4 * kQSfBytes;
   static constexpr int kOffVSf = kOffKSf + NS * kKSfBytes;
   static constexpr int kOffPSf = kOffVSf + NS * kVSfBytes;
-  static constexpr int kOffBar = kOffPSf + 4 * kPSfBytes;
-  static constexpr int kNumBars = 4 + 4 * NS + 8 + 2;
+  // smooth-Q: the score-correction rows of 128 keys, [query tile][3 buffers]
+  static constexpr int kOffDs = kOffPSf + 4 * kPSfBytes;
+  static constexpr int kOffBar = kOffDs + 2 * 3 * 512;
+  static constexpr int kNumBars = 4 + 4 * NS + 8 + 2 + 6;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   // Q/K rows of 64 bytes use the 64B swizzle, rows of 32 bytes the 32B one.
   static constexpr uint32_t kQKSwz = (D == 128) ? kSwizzle64B : kSwizzle32B;
@@ -110,7 +124,8 @@ struct CfgF4 {
 };
 
 struct BarsF4 {
-  uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *s_free, *p_full, *o_done, *drain;
+  uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *s_free, *p_full, *o_done, *drain,
+      *ds_full;
 };
 
 // Shared-memory matrix descriptors: each issuing warp builds a base
@@ -138,13 +153,20 @@ __device__ __forceinline__ void copy_sf_d(uint32_t tcol, uint64_t d0, uint32_t o
   for (int i = 0; i < nblk; ++i) tmem_cp_32x128b_warpx4(tcol + 4 * i, dadd(d0, off + 512 * i));
 }
 
-template <int D, bool OUT32>
+// One 512-byte smooth-Q correction row (128 keys) into shared memory,
+// completing on `bar`.
+__device__ __forceinline__ void ds_copy(uint8_t* dst, const float* src, uint64_t* bar) {
+  mbar_arrive_expect_tx(bar, 512);
+  bulk_load(dst, src, 512, bar);
+}
+
+template <int D, bool OUT32, bool SQ>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const uint8_t* __restrict__ q_sf,
                       const uint8_t* __restrict__ k_sf, const uint8_t* __restrict__ v_sf,
                       void* __restrict__ out_ptr, int H, int Hkv, int Lq, int Lkv, int causal, const AttnWork work,
-                      const SplitOut part, const Strides so, uint64_t wait_ns) {
+                      const SplitOut part, const Strides so, const float* __restrict__ ds, uint64_t wait_ns) {
   using C = CfgF4<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -161,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   bars.p_full = bars.s_free + 2;
   bars.o_done = bars.p_full + 2;
   bars.drain = bars.o_done + 2;
+  bars.ds_full = bars.drain + 2;          // [query tile][3]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_base + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -191,8 +214,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 8) {
     // Register split: the launch gives every thread kLaunchRegs; this
     // warpgroup (producer, MMA issuer, two idle warps) keeps kOtherRegs and the
-    // two softmax warpgroups take kSoftmaxRegs (sum checked above).
-    reg_dealloc<kOtherRegs>();
+    // two softmax warpgroups take kSoftmaxRegs (the SQ pair for the smooth-Q
+    // variant; sums checked above).
+    reg_dealloc<SQ ? kOtherRegsSq : kOtherRegs>();
     // The producer and MMA warps run their loops with all 32 lanes (waits are
     // warp-wide, addresses and descriptors warp-uniform); one elected lane
     // issues each TMA copy, tcgen05 instruction and commit.
@@ -419,9 +443,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    reg_alloc<kSoftmaxRegs>();
+    reg_alloc<SQ ? kSoftmaxRegsSq : kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax + P quantisation
+    // (smooth-Q: these threads copy the score corrections written by the
+    // launch before, so they wait for it too)
+    if constexpr (SQ) pdl_wait();
     const int q = warp / 4;
+    // Smooth-Q: the correction row of each (query tile, key tile) reaches
+    // shared memory by a bulk copy issued by thread 0 of the warpgroup one
+    // tile ahead, into buffer t % 3 for this slot's tile t (t = cq over the
+    // whole list).  Buffer (t + 1) % 3 last held tile t - 2, which every
+    // thread of the warpgroup has finished: thread 0 reaches tile t once S(t)
+    // is complete, issued after every thread loaded S(t - 1).
+    const bool ds_issuer = (threadIdx.x % 128) == 0;
+    int ds_hi = 0;                                      // tiles of this slot whose copy is issued (issuer only)
     const int r = (warp % 4) * 32 + lane;
     const uint32_t lane_addr = tbase + (((warp % 4) * 32) << 16);
     const float c = softmax_scale_log2<D>();
@@ -457,9 +492,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         float sv[128];
 #pragma unroll
         for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i / 32][i % 32]);
+        const int ja = u.jb + j;
+        if constexpr (SQ) {
+          // smooth-Q: S = Q^' K^'^T + dS, dS the query tile's correction of
+          // these 128 keys (the same for every row: broadcast reads)
+          if (ds_issuer) {
+            // this slot's correction rows of the unit are contiguous: the
+            // whole range is prefetched into L2 when the unit starts
+            const float* row0 = ds + (((long long)u.bh * (Lqp / BM) + qt) * Lkvp + (long long)u.jb * BN);
+            if (j == 0) {
+              bulk_prefetch_l2(row0, (uint32_t)nq * 512u);
+              ds_copy(smem + C::kOffDs + (3 * q + cq % 3) * 512, row0, bars.ds_full + 3 * q + cq % 3);
+            }
+            if (j + 1 < nq) {
+              const int t = (cq + 1) % 3;
+              ds_copy(smem + C::kOffDs + (3 * q + t) * 512, row0 + (j + 1) * BN, bars.ds_full + 3 * q + t);
+            }
+            ds_hi = j + 1 < nq ? cq + 2 : cq + 1;
+          }
+          if (!mbar_wait_warp(bars.ds_full + 3 * q + cq % 3, (cq / 3) & 1, abort_flag, wait_ns)) {
+            ok = false;
+            break;
+          }
+          // (shared-window loads, four in flight before their adds)
+          const uint32_t dsa = smem_u32(smem + C::kOffDs + (3 * q + cq % 3) * 512);
+#pragma unroll
+          for (int i0 = 0; i0 < 32; i0 += 4) {
+            float4 t[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) t[i] = lds_f4(dsa + 16 * (i0 + i));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int e = 4 * (i0 + i);
+              add2(sv[e], sv[e + 1], sv[e], sv[e + 1], t[i].x, t[i].y);
+              add2(sv[e + 2], sv[e + 3], sv[e + 2], sv[e + 3], t[i].z, t[i].w);
+            }
+          }
+        }
         // keys this row may not see: past Lkv (the zero padding of a ragged
         // last tile) and, causal, past its position qt*128 + r + Lkv - Lq
-        const int ja = u.jb + j;
         int lim = Lkv - ja * BN;
         if (causal) lim = min(lim, qt * BM + r + work.coff - ja * BN + 1);
         lim = min(lim, BN);
@@ -640,6 +711,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // p_full arrival)
       }
     }
+    if constexpr (SQ) {
+      // after an abort, let the correction copies still in flight land
+      // before the shared memory goes away (the last copy into each buffer)
+      if (ds_issuer && !ok)
+        for (int t = ds_hi > 3 ? ds_hi - 3 : 0; t < ds_hi; ++t)
+          mbar_wait_drain(bars.ds_full + 3 * q + t % 3, (t / 3) & 1, wait_ns);
+    }
   }
 
   tc_fence_before();
@@ -653,10 +731,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool OUT32>
+template <int D, bool OUT32, bool SQ>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const sa_fp4_qkv& x,
                      void* o, const Strides& so, const Dims& dm, int causal, int nsplit, const SplitOut& part,
-                     cudaStream_t s) {
+                     const float* ds, cudaStream_t s) {
   using C = CfgF4<D>;
   // kernel attributes are per device: set them on the first launch on each
   static std::atomic<bool> attr_done[kMaxDevices];
@@ -664,10 +742,10 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     // The warpgroup register split assumes kLaunchRegs registers per thread at
     // launch; with fewer, a setmaxnreg increase could never be satisfied.
     cudaFuncAttributes fa;
-    cudaError_t r = cudaFuncGetAttributes(&fa, attn_nvfp4_kernel<D, OUT32>);
+    cudaError_t r = cudaFuncGetAttributes(&fa, attn_nvfp4_kernel<D, OUT32, SQ>);
     if (r != cudaSuccess) return r;
     if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
-    return cudaFuncSetAttribute(attn_nvfp4_kernel<D, OUT32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(attn_nvfp4_kernel<D, OUT32, SQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::kSmemBytes);
   });
   if (e != cudaSuccess) return e;
@@ -680,10 +758,10 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   // waits for it before its first load
   cudaLaunchAttribute attr;
   const cudaLaunchConfig_t cfg = pdl_launch_config(dim3(ctas), dim3(kThreads), C::kSmemBytes, s, &attr);
-  e = cudaLaunchKernelEx(&cfg, attn_nvfp4_kernel<D, OUT32>, tq, tk, tv,
+  e = cudaLaunchKernelEx(&cfg, attn_nvfp4_kernel<D, OUT32, SQ>, tq, tk, tv,
                                      static_cast<const uint8_t*>(x.q_sf), static_cast<const uint8_t*>(x.k_sf),
                                      static_cast<const uint8_t*>(x.v_sf), o, dm.H, dm.Hkv, dm.Lq, dm.Lkv, causal,
-                                     work, part, so, kWaitLimitNs);
+                                     work, part, so, ds, kWaitLimitNs);
   if (e == cudaSuccess && work.streamk) e = launch_streamk_combine(work, ctas, part, dm, o, so, OUT32, s);
   else if (e == cudaSuccess && work.nsplit > 1) e = launch_splitkv_combine(part, work.nsplit, dm, o, so, OUT32, s);
   return e;
@@ -827,13 +905,22 @@ cudaError_t launch_exp_path_selftest(const float* x, const float* y, int n, floa
   return cudaGetLastError();
 }
 
+template <int D, bool SQ>
+cudaError_t launch_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const sa_fp4_qkv& qkv,
+                      void* o, const Strides& so, const Dims& dm, int causal, bool out_f32, int nsplit,
+                      const SplitOut& part, const float* ds, cudaStream_t s) {
+  return out_f32 ? launch_d<D, true, SQ>(tq, tk, tv, qkv, o, so, dm, causal, nsplit, part, ds, s)
+                 : launch_d<D, false, SQ>(tq, tk, tv, qkv, o, so, dm, causal, nsplit, part, ds, s);
+}
+
 cudaError_t launch_attn_nvfp4(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const sa_fp4_qkv& qkv, void* o, const Strides& so, const Dims& dm, int causal,
-                              bool out_f32, int nsplit, const SplitOut& part, cudaStream_t s) {
-  if (dm.d == 64) return out_f32 ? launch_d<64, true>(tq, tk, tv, qkv, o, so, dm, causal, nsplit, part, s)
-                                 : launch_d<64, false>(tq, tk, tv, qkv, o, so, dm, causal, nsplit, part, s);
-  return out_f32 ? launch_d<128, true>(tq, tk, tv, qkv, o, so, dm, causal, nsplit, part, s)
-                 : launch_d<128, false>(tq, tk, tv, qkv, o, so, dm, causal, nsplit, part, s);
+                              bool out_f32, int nsplit, const SplitOut& part, cudaStream_t s, const float* ds) {
+  if (dm.d == 64)
+    return ds ? launch_dq<64, true>(tq, tk, tv, qkv, o, so, dm, causal, out_f32, nsplit, part, ds, s)
+              : launch_dq<64, false>(tq, tk, tv, qkv, o, so, dm, causal, out_f32, nsplit, part, ds, s);
+  return ds ? launch_dq<128, true>(tq, tk, tv, qkv, o, so, dm, causal, out_f32, nsplit, part, ds, s)
+            : launch_dq<128, false>(tq, tk, tv, qkv, o, so, dm, causal, out_f32, nsplit, part, ds, s);
 }
 
 cudaError_t attn_nvfp4_read_error(int* out) { return read_and_clear_device_error(out); }

@@ -129,10 +129,19 @@ inline SplitOut splitkv_layout(void* ws, const Dims& dm, int nsplit) {
 cudaError_t launch_attn_bf16(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o,
                              const Strides& so, const Dims& dm, int causal, bool out_f32, int nsplit,
                              const SplitOut& part, cudaStream_t s);
-// attn_nvfp4.cu
+// attn_nvfp4.cu.  ds: the smooth-Q score corrections ([B*H][Lqp/128][Lkvp]
+// float32, added to every score of its query tile and key before the
+// softmax), or nullptr for the plain SA3 path.
 cudaError_t launch_attn_nvfp4(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const sa_fp4_qkv& qkv, void* o, const Strides& so, const Dims& dm, int causal,
-                              bool out_f32, int nsplit, const SplitOut& part, cudaStream_t s);
+                              bool out_f32, int nsplit, const SplitOut& part, cudaStream_t s,
+                              const float* ds = nullptr);
+// smooth_q.cu: after sa_quantize, Q re-quantised as Q' = Q - its 128-token
+// block mean (x.q_codes / x.q_sf overwritten, the means to qmean
+// [B*H][Lqp/128][d]) and the score corrections ds [B*H][Lqp/128][Lkvp] from
+// the means and x.k_codes / x.k_sf.  q: bf16 with element strides sq.
+cudaError_t launch_smooth_q(const void* q, const Strides& sq, const Dims& dm, const sa_fp4_qkv& x, float* qmean,
+                            float* ds, cudaStream_t s);
 // Test support: the FP32 score tile of the NVFP4 attention kernel's S step for
 // query tile qt of head (b, h) and key tile kt of its kv head, [128][128] to
 // `out` (device); tq / tk as for launch_attn_nvfp4.

@@ -237,6 +237,56 @@ sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v
              : SA_ERR_CUDA;
 }
 
+static void smooth_q_sizes(const Dims& dm, size_t sz[2]) {
+  const size_t tiles = (size_t)dm.B * dm.H * (padded_len(dm.Lq) / 128);
+  sz[0] = tiles * dm.d * sizeof(float);                         // q_mean
+  sz[1] = tiles * padded_len(dm.Lkv) * sizeof(float);           // ds
+}
+
+size_t sa_smooth_q_bytes_s(const sa_shape* shape, size_t offsets_out[2]) {
+  if (!shape) return 0;
+  const Dims dm = dims_of(shape);
+  if (check_dims(dm) != SA_OK || dm.B == 0 || dm.Lq == 0 || dm.Lkv == 0) return 0;
+  size_t sz[2];
+  smooth_q_sizes(dm, sz);
+  if (offsets_out) {
+    offsets_out[0] = 0;
+    offsets_out[1] = align256(sz[0]);
+  }
+  return align256(align256(sz[0]) + sz[1]);
+}
+
+sa_status sa_smooth_q_from_blob_s(void* blob, const sa_shape* shape, sa_fp4_sq* out) {
+  if (!out || !blob || !shape || (reinterpret_cast<uintptr_t>(blob) & 255u)) return SA_ERR_INVALID_ARG;
+  size_t off[2];
+  if (sa_smooth_q_bytes_s(shape, off) == 0) {
+    const sa_status st = check_dims(dims_of(shape));
+    return st != SA_OK ? st : SA_ERR_INVALID_ARG;
+  }
+  uint8_t* p = static_cast<uint8_t*>(blob);
+  out->q_mean = reinterpret_cast<float*>(p + off[0]);
+  out->ds = reinterpret_cast<float*>(p + off[1]);
+  return SA_OK;
+}
+
+sa_status sa_quantize_smooth_q(const void* q, const sa_shape* shape, int flags, const sa_fp4_sq* x,
+                               sa_stream_t stream) {
+  if (!shape || !x) return SA_ERR_INVALID_ARG;
+  const Dims dm = dims_of(shape);
+  const sa_status st = check_dims(dm);
+  if (st != SA_OK) return st;
+  if (flags & ~SA_LAYOUT_BLHD) return SA_ERR_INVALID_ARG;
+  if (empty_problem(dm)) return SA_OK;
+  if (dm.Lkv == 0) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(x->fp4.q_codes) || !aligned16(x->fp4.q_sf) || !aligned16(x->fp4.k_codes) ||
+      !aligned16(x->fp4.k_sf) || !aligned16(x->q_mean) || !aligned16(x->ds))
+    return SA_ERR_INVALID_ARG;
+  const Strides sq = layout_strides((flags & SA_LAYOUT_BLHD) != 0, dm.H, dm.Lq, dm.d);
+  return launch_smooth_q(q, sq, dm, x->fp4, x->q_mean, x->ds, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SA_OK
+             : SA_ERR_CUDA;
+}
+
 // The work split: `requested` 0 = the library's choice, 1 = one unit per CTA,
 // n > 1 = split-KV with n shares (at most one per key tile), -1 = stream-K.
 // The library chooses stream-K for the NVFP4 path when the pairs alone can
@@ -246,6 +296,11 @@ sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v
 // quantiser; 201.4 / 197.3 / 195.2 us after an L2 flush), split-KV when the
 // pairs leave half of the SMs idle and the shares stay long, else one unit
 // per CTA.
+// NVFP4 calls that run on the few-row decode kernel (the smooth-Q variant
+// always runs on the prefill kernel).
+static bool use_decode(const Dims& dm, int mode) { return mode == SA_MODE_NVFP4 && decode_eligible(dm); }
+static bool is_fp4(int mode) { return mode == SA_MODE_NVFP4 || mode == SA_MODE_NVFP4_SQ; }
+
 static int resolve_nsplit(const Dims& dm, int causal, int mode, int requested) {
   if (requested == 1) return 1;
   if (requested == kStreamK) return kStreamK;
@@ -254,14 +309,14 @@ static int resolve_nsplit(const Dims& dm, int causal, int mode, int requested) {
   // into shares so that the (batch, kv head) pairs fill one wave of CTAs
   // (equal ranges of (pair, key tile) items, kStreamK, measured slower:
   // decode_gqa 60 against 45.6 us)
-  if (requested == 0 && mode == SA_MODE_NVFP4 && decode_eligible(dm)) return decode_nsplit(dm, sms);
+  if (requested == 0 && use_decode(dm, mode)) return decode_nsplit(dm, sms);
   if (requested == 0) {
     const long long pairs = (long long)(((dm.Lq + 127) / 128 + 1) / 2) * dm.B * dm.H;
     // stream-K balances key tiles, not units: under the causal mask most
     // pairs are short, the per-unit fixed cost (~6 us) dominates the ranges
     // that hold them, and the heaviest-first work list is faster (causal GQA
     // B1 H32 L8192: 366 us against 533 us)
-    if (mode == SA_MODE_NVFP4 && !causal && sms > 0 && pairs >= sms &&
+    if (is_fp4(mode) && !causal && sms > 0 && pairs >= sms &&
         streamk_fits(dm.B, dm.H, dm.Lq, dm.Lkv, causal))
       return kStreamK;
     return choose_nsplit(dm.B, dm.H, dm.Lq, dm.Lkv, sms);
@@ -270,9 +325,9 @@ static int resolve_nsplit(const Dims& dm, int causal, int mode, int requested) {
   return requested < nkt ? requested : nkt;
 }
 
-static size_t work_split_bytes(const Dims& dm, int causal, int nsplit) {
+static size_t work_split_bytes(const Dims& dm, int causal, int mode, int nsplit) {
   // (kStreamK is an NVFP4 schedule; for decode shapes, the decode kernel's ranges)
-  if (nsplit == kStreamK && decode_eligible(dm)) return decode_range_workspace_bytes(dm, device_sm_count());
+  if (nsplit == kStreamK && use_decode(dm, mode)) return decode_range_workspace_bytes(dm, device_sm_count());
   if (nsplit == kStreamK) {
     int ctas = 0;
     make_streamk_work(dm.B, dm.H, dm.Lq, dm.Lkv, causal, device_sm_count() > 0 ? device_sm_count() : 1, &ctas);
@@ -290,10 +345,10 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
   if (causal && dm.Lkv < dm.Lq) return SA_ERR_INVALID_ARG;   // the first queries would see no key
   if (mode_flags & ~(0xF | SA_OUT_FP32 | SA_LAYOUT_BLHD)) return SA_ERR_INVALID_ARG;
   const int mode = mode_flags & 0xF;
-  if (mode != SA_MODE_BF16 && mode != SA_MODE_NVFP4) return SA_ERR_INVALID_ARG;
+  if (mode != SA_MODE_BF16 && !is_fp4(mode)) return SA_ERR_INVALID_ARG;
   if (nsplit_req < kStreamK) return SA_ERR_INVALID_ARG;
   if (nsplit_req == kStreamK &&
-      (mode != SA_MODE_NVFP4 || (!decode_eligible(dm) && !streamk_fits(dm.B, dm.H, dm.Lq, dm.Lkv, causal))))
+      (!is_fp4(mode) || (!use_decode(dm, mode) && !streamk_fits(dm.B, dm.H, dm.Lq, dm.Lkv, causal))))
     return SA_ERR_UNSUPPORTED;
   if (empty_problem(dm)) return SA_OK;
   const bool out_f32 = (mode_flags & SA_OUT_FP32) != 0;
@@ -305,13 +360,13 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
   // own choice then falls back to one unit per CTA)
   int nsplit = resolve_nsplit(dm, causal, mode, nsplit_req);
   const bool needs_ws = nsplit > 1 || nsplit == kStreamK;
-  const bool ws_ok = workspace != nullptr && workspace_bytes >= work_split_bytes(dm, causal, nsplit);
+  const bool ws_ok = workspace != nullptr && workspace_bytes >= work_split_bytes(dm, causal, mode, nsplit);
   if (needs_ws && !ws_ok && nsplit_req != 0) return SA_ERR_INVALID_ARG;
   if (needs_ws && !ws_ok) nsplit = 1;
   if (nsplit != 1 && !aligned16(workspace)) return SA_ERR_INVALID_ARG;
   SplitOut part{nullptr, nullptr};
   if (nsplit > 1) part = splitkv_layout(workspace, dm, nsplit);
-  if (nsplit == kStreamK && decode_eligible(dm)) {
+  if (nsplit == kStreamK && use_decode(dm, mode)) {
     part = decode_range_layout(workspace, dm, device_sm_count());
   } else if (nsplit == kStreamK) {
     int ctas = 0;
@@ -329,7 +384,10 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
                                                                                                     : SA_ERR_CUDA;
   }
   if (k != nullptr || v != nullptr || q == nullptr) return SA_ERR_INVALID_ARG;
-  const sa_fp4_qkv* x = static_cast<const sa_fp4_qkv*>(q);
+  // SA_MODE_NVFP4_SQ: q is an sa_fp4_sq, whose first member is the sa_fp4_qkv
+  const sa_fp4_sq* xs = mode == SA_MODE_NVFP4_SQ ? static_cast<const sa_fp4_sq*>(q) : nullptr;
+  const sa_fp4_qkv* x = xs ? &xs->fp4 : static_cast<const sa_fp4_qkv*>(q);
+  if (xs && !aligned16(xs->ds)) return SA_ERR_INVALID_ARG;
   if (!aligned16(x->q_codes) || !aligned16(x->q_sf) || !aligned16(x->k_codes) || !aligned16(x->k_sf) ||
       !aligned16(x->v_codes) || !aligned16(x->v_sf))
     return SA_ERR_INVALID_ARG;
@@ -344,10 +402,11 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
     return SA_ERR_CUDA;
   // at most 16 query rows per kv head (decode): the decode kernel (stream-K
   // there means its balanced ranges)
-  if (decode_eligible(dm))
+  if (use_decode(dm, mode))
     return launch_attn_decode(tk, tv, *x, o, so, dm, causal, out_f32, nsplit, part, s) == cudaSuccess ? SA_OK
                                                                                                       : SA_ERR_CUDA;
-  return launch_attn_nvfp4(tq, tk, tv, *x, o, so, dm, causal, out_f32, nsplit, part, s) == cudaSuccess
+  return launch_attn_nvfp4(tq, tk, tv, *x, o, so, dm, causal, out_f32, nsplit, part, s, xs ? xs->ds : nullptr) ==
+                 cudaSuccess
              ? SA_OK
              : SA_ERR_CUDA;
 }
@@ -363,8 +422,8 @@ size_t sa_attn_fwd_workspace_bytes_s(const sa_shape* shape, int causal, int mode
   const int m = mode & 0xF;
   if (check_dims(dm) != SA_OK || empty_problem(dm) || nsplit < kStreamK) return 0;
   if (causal != 0 && causal != 1) return 0;
-  if (nsplit == kStreamK && m != SA_MODE_NVFP4) return 0;
-  return work_split_bytes(dm, causal, resolve_nsplit(dm, causal, m, nsplit));
+  if (nsplit == kStreamK && !is_fp4(m)) return 0;
+  return work_split_bytes(dm, causal, m, resolve_nsplit(dm, causal, m, nsplit));
 }
 
 size_t sa_attn_fwd_workspace_bytes(int B, int H, int Hkv, int L, int d, int causal, int mode, int nsplit) {

@@ -30,6 +30,12 @@ from concurrent.futures import ProcessPoolExecutor
 
 NVFP4_TOL = 2e-3
 TIE_REL = 2e-5
+# The smooth-Q variant adds the float32 score correction dS before the
+# softmax: its error, (D/16 + 17) * 2^-24 * sum_c |qbar_c K^'_jc| (the FMA
+# chains of smooth_q.cu), and the rounding of S + dS widen the decision
+# window; tests/test_gpu_smooth_q.py checks that TIE_REL_SQ - TIE_REL covers
+# twice that extra relative error on every smooth-Q parity case.
+TIE_REL_SQ = 4e-5
 CLEAN_TOL = 1e-5
 COS_SLACK = 2e-3
 BF16_COS = 0.99999
@@ -53,13 +59,17 @@ def oracle_pool():
 
 def head_oracle(args):
     """Exact FP64 attention of one head at the given rows and, for the NVFP4
-    path, the SA3 emulation with its decision-ambiguity bound (runs in a pool
+    path (mode "nvfp4", or "nvfp4_sq" for the smooth-Q variant's operands),
+    the SA3 emulation with its decision-ambiguity bound (runs in a pool
     worker).  q [1,1,Lq,d], k and v [1,1,Lkv,d] float32 (the head's kv head)."""
     q, k, v, causal, rows, mode, tie_rel = args
     from oracle import attention as A
     ex = A.exact_attention(q, k, v, causal, rows=rows)[0, 0]
-    if mode != "nvfp4":
+    if mode not in ("nvfp4", "nvfp4_sq"):
         return ex, None, None
-    (qd, kd, vd), _ = A.dequantized_operands(q, k, v)
+    if mode == "nvfp4_sq":
+        (qd, kd, vd), _ = A.dequantized_operands_sq(q, k, v)
+    else:
+        (qd, kd, vd), _ = A.dequantized_operands(q, k, v)
     em, bd = A.sa3_emulated_attention(qd, kd, vd, causal, rows=rows, tie_rel=tie_rel, return_bound=True)
     return ex, em[0, 0], bd[0, 0]

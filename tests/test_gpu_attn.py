@@ -42,9 +42,9 @@ def run_gpu(sa, x, causal, mode, out_dtype=torch.bfloat16):
     return o.float().cpu().numpy()
 
 
-def oracle_heads(x, causal, heads, rows, mode):
-    """Exact (and, for nvfp4, emulated with its bound) output of the given
-    (b, h) pairs at the given rows, one pool task per head."""
+def oracle_heads(x, causal, heads, rows, mode, tie_rel=TIE_REL):
+    """Exact (and, for nvfp4 / nvfp4_sq, emulated with its bound) output of
+    the given (b, h) pairs at the given rows, one pool task per head."""
     B, H, L, d = x["q"].shape
     G = H // x["k"].shape[1]
     tasks = []
@@ -52,10 +52,10 @@ def oracle_heads(x, causal, heads, rows, mode):
         q = x["q"][b:b + 1, h:h + 1].float().numpy()
         k = x["k"][b:b + 1, h // G:h // G + 1].float().numpy()
         v = x["v"][b:b + 1, h // G:h // G + 1].float().numpy()
-        tasks.append((q, k, v, causal, np.asarray(rows), mode, TIE_REL))
+        tasks.append((q, k, v, causal, np.asarray(rows), mode, tie_rel))
     res = list(oracle_pool().map(head_oracle, tasks))
     ex = np.stack([r[0] for r in res])
-    if mode == "nvfp4":
+    if mode in ("nvfp4", "nvfp4_sq"):
         return ex, np.stack([r[1] for r in res]), np.stack([r[2] for r in res])
     return ex, None, None
 
@@ -64,9 +64,9 @@ def _cos(a, b):
     return np.array([np.dot(g.ravel(), e.ravel()) / np.linalg.norm(g) / np.linalg.norm(e) for g, e in zip(a, b)])
 
 
-def check(o, x, causal, heads, rows, mode, o32=None, label=""):
+def check(o, x, causal, heads, rows, mode, o32=None, label="", tie_rel=TIE_REL, extra=None):
     got = np.stack([o[b, h][rows] for (b, h) in heads])
-    ex, em, bound = oracle_heads(x, causal, heads, rows, mode)
+    ex, em, bound = oracle_heads(x, causal, heads, rows, mode, tie_rel)
     assert np.all(np.isfinite(got))
     cos = _cos(got, ex)
     if mode == "bf16":
@@ -81,8 +81,9 @@ def check(o, x, causal, heads, rows, mode, o32=None, label=""):
     cos_em = _cos(em, ex)
     tol = NVFP4_TOL * M + bound
     clean = bound.max(axis=-1) == 0
-    rec = dict(test=label, mode=mode, heads=len(heads), rows=len(rows), tie_rel=TIE_REL,
+    rec = dict(test=label, mode=mode, heads=len(heads), rows=len(rows), tie_rel=tie_rel,
                ambiguous_row_frac=float(np.mean(~clean)), cos_emul=float(cos_em.mean()))
+    rec.update(extra or {})
     for name, g, extra in (("fp32", None if o32 is None else np.stack([o32[b, h][rows] for (b, h) in heads]), 0),
                            ("bf16", got, 2.0 ** -9 * (np.abs(em) + tol))):
         if g is None:
