@@ -146,6 +146,52 @@ def test_argument_errors_launch_nothing(sa):
     assert s.q_codes == (1 << 20) + off[0] and s.workspace == (1 << 20) + off[7]
 
 
+def test_smooth_q_entry_points_host_checks(sa):
+    """The smooth-Q variant's sizing, blob and argument checks (no GPU)."""
+    lib = sa.lib
+    p = ctypes.c_void_p(1 << 20)
+    bad = ctypes.c_void_p(1 << 20 | 8)
+    z = ctypes.c_void_p(0)
+    shape = sa.SaShape(1, 2, 2, 200, 300, 64)          # two query tiles, 384 padded keys
+    offs = (ctypes.c_size_t * 2)()
+    n = lib.sa_smooth_q_bytes_s(ctypes.byref(shape), offs)
+    q_mean, ds = 1 * 2 * 2 * 64 * 4, 1 * 2 * 2 * 384 * 4
+    assert offs[0] == 0 and offs[1] == q_mean and n == q_mean + ds      # 1024 and 6144: already 256-aligned
+    for bad_shape in (sa.SaShape(1, 2, 2, 200, 300, 80), sa.SaShape(0, 2, 2, 200, 300, 64),
+                      sa.SaShape(1, 2, 2, 0, 300, 64), sa.SaShape(1, 3, 2, 200, 300, 64)):
+        assert lib.sa_smooth_q_bytes_s(ctypes.byref(bad_shape), None) == 0
+    x = sa.SaFp4Sq()
+    assert lib.sa_smooth_q_from_blob_s(ctypes.c_void_p(1 << 20 | 128), ctypes.byref(shape), ctypes.byref(x)) == \
+        sa.SA_ERR_INVALID_ARG
+    assert lib.sa_smooth_q_from_blob_s(p, ctypes.byref(shape), ctypes.byref(x)) == sa.SA_OK
+    assert x.q_mean == (1 << 20) and x.ds == (1 << 20) + offs[1]
+    # sa_quantize_smooth_q: argument errors before anything is launched
+    assert lib.sa_quantize_smooth_q(p, None, 0, ctypes.byref(x), None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_quantize_smooth_q(p, ctypes.byref(shape), 0, None, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_quantize_smooth_q(p, ctypes.byref(shape), 64, ctypes.byref(x), None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_quantize_smooth_q(bad, ctypes.byref(shape), 0, ctypes.byref(x), None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_quantize_smooth_q(p, ctypes.byref(shape), 0, ctypes.byref(x), None) == sa.SA_ERR_INVALID_ARG  # fp4 unset
+    assert lib.sa_quantize_smooth_q(p, ctypes.byref(sa.SaShape(1, 2, 2, 200, 300, 80)), 0, ctypes.byref(x), None) == \
+        sa.SA_ERR_UNSUPPORTED
+    assert lib.sa_quantize_smooth_q(z, ctypes.byref(sa.SaShape(0, 2, 2, 200, 300, 64)), 0, ctypes.byref(x), None) == \
+        sa.SA_OK                                                        # an empty problem
+    # attention in the smooth-Q mode: the struct is required, k and v must be NULL
+    assert lib.sa_attn_fwd(z, z, z, p, 1, 2, 2, 256, 64, 0, sa.SA_MODE_NVFP4_SQ, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_attn_fwd(p, p, z, p, 1, 2, 2, 256, 64, 0, sa.SA_MODE_NVFP4_SQ, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_attn_fwd(z, z, z, z, 0, 2, 2, 256, 64, 0, sa.SA_MODE_NVFP4_SQ, None) == sa.SA_OK
+    # the host-buffer path does not take it
+    assert lib.sa_attn_fwd_host(p, p, p, p, 1, 2, 2, 256, 64, 0, sa.SA_MODE_NVFP4_SQ, p, 1 << 30, 0, None) == \
+        sa.SA_ERR_UNSUPPORTED
+    assert lib.sa_attn_fwd_host_workspace_bytes(1, 2, 2, 256, 64, sa.SA_MODE_NVFP4_SQ, 0) == 0
+    # its work split is the prefill kernel's, also for few query rows per kv head
+    big = sa.SaShape(2, 16, 16, 4096, 4096, 128)
+    assert lib.sa_attn_fwd_workspace_bytes_s(ctypes.byref(big), 0, sa.SA_MODE_NVFP4_SQ, -1) == \
+        lib.sa_attn_fwd_workspace_bytes_s(ctypes.byref(big), 0, sa.SA_MODE_NVFP4, -1) > 0
+    dec = sa.SaShape(16, 8, 2, 1, 8192, 128)                         # 4 query rows per kv head
+    assert lib.sa_attn_fwd_workspace_bytes_s(ctypes.byref(dec), 0, sa.SA_MODE_NVFP4_SQ, 4) == \
+        4 * (16 * 8 * 128) * (128 + 2) * 4                            # split-KV rows of the prefill kernel
+
+
 def test_product_path_has_no_oracle_dependency():
     pkg = os.path.join(ROOT, "quantized_attention_x16_gb300")
     for dirpath, _, files in os.walk(pkg):
