@@ -56,8 +56,9 @@ typedef enum {
 } sa_status;
 
 /* SA_MODE_NVFP4_SQ: the NVFP4 path with SageAttention2's smooth-Q added (a
- * labelled variant; see sa_quantize_smooth_q). */
-typedef enum { SA_MODE_BF16 = 0, SA_MODE_NVFP4 = 1, SA_MODE_NVFP4_SQ = 2 } sa_mode;
+ * labelled variant; see sa_quantize_smooth_q).  SA_MODE_NVFP4_FQ: the NVFP4
+ * path with Q quantised inside the attention kernel (see sa_quantize_kv_s). */
+typedef enum { SA_MODE_BF16 = 0, SA_MODE_NVFP4 = 1, SA_MODE_NVFP4_SQ = 2, SA_MODE_NVFP4_FQ = 3 } sa_mode;
 
 /* Output-format flag OR-ed into the `mode` argument of sa_attn_fwd: with it,
  * o is float32 [B, H, L, d] (the FP32 accumulator divided by the row sum,
@@ -228,6 +229,26 @@ sa_status sa_quantize_s(const void* q, const void* k, const void* v, const sa_sh
 sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v,
                                      int B, int H, int Hkv, int L, int d,
                                      const sa_fp4_qkv* out, sa_stream_t stream);
+
+/*
+ * Q quantised inside the attention kernel ("GPU kernel porting with AI
+ * agents", section "Sage Attention 3": the same 1x16 NVFP4 quantisation of
+ * Q, fused into the attention's load stage instead of a separate pass).
+ * sa_quantize_kv_s: sa_quantize_s for K and V only -- smooth-K mean, K' and V
+ *   codes and scales, bit-identical to sa_quantize_s's; out->q_codes and
+ *   out->q_sf are neither read nor written (may be NULL).  Arguments and
+ *   errors as sa_quantize_s without q.  Two kernels on `stream`.
+ * sa_attn_fwd(_ws, _s) with mode SA_MODE_NVFP4_FQ: q is the bf16 Q device
+ *   tensor (BHLD, or BLHD with SA_LAYOUT_BLHD), k points to a host `const
+ *   sa_fp4_qkv*` from sa_quantize_kv_s for the same sizes, v must be NULL.
+ *   The attention kernel loads each unit's bf16 Q tiles by TMA and one of its
+ *   warps quantises them with sa_quantize's arithmetic, so O is bit-identical
+ *   to sa_quantize + SA_MODE_NVFP4 on the same work split (the few-row decode
+ *   kernel is not used: such shapes run on the prefill kernel).
+ *   sa_attn_fwd_host does not take it (SA_ERR_UNSUPPORTED).
+ */
+sa_status sa_quantize_kv_s(const void* k, const void* v, const sa_shape* shape, int flags, const sa_fp4_qkv* out,
+                           sa_stream_t stream);
 
 /*
  * Smooth-Q variant ("kernel overview", SageAttention evolution chain: "Smooth-K

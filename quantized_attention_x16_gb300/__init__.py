@@ -13,6 +13,8 @@ Names follow the C ABI:
 * ``sa_quantize(q, k, v, out=None)``  -- smooth-K + NVFP4 quantisation of Q, K, V
 * ``sa_quantize_static_scratch(...)`` -- the same without caller-provided scratch
 * ``sa_attn_fwd(q, k, v, o=None, causal=False, mode="bf16"|"nvfp4"|"nvfp4_sq")``
+* ``sa_quantize_kv(k, v, H)`` -- K and V only, for mode "nvfp4_fq" (Q quantised
+  inside the attention kernel)
 * ``sa_quantize(..., smooth_q=True)`` -- also the smooth-Q variant's Q' codes,
   block means and score corrections (``sa_quantize_smooth_q``), for mode "nvfp4_sq"
 * ``sa_attn_fwd_host(q, k, v, o=None, causal=False, mode=...)`` -- the same on
@@ -27,8 +29,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libsa.so")
 
 SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA, SA_ERR_TIMEOUT = range(5)
-SA_MODE_BF16, SA_MODE_NVFP4, SA_MODE_NVFP4_SQ = 0, 1, 2
-_MODES = {"bf16": SA_MODE_BF16, "nvfp4": SA_MODE_NVFP4, "nvfp4_sq": SA_MODE_NVFP4_SQ}
+SA_MODE_BF16, SA_MODE_NVFP4, SA_MODE_NVFP4_SQ, SA_MODE_NVFP4_FQ = 0, 1, 2, 3
+_MODES = {"bf16": SA_MODE_BF16, "nvfp4": SA_MODE_NVFP4, "nvfp4_sq": SA_MODE_NVFP4_SQ, "nvfp4_fq": SA_MODE_NVFP4_FQ}
 SA_OUT_FP32 = 16
 SA_LAYOUT_BLHD = 32
 SA_HOST_OVERLAP = 64
@@ -40,7 +42,7 @@ EXPORTS = ("sa_fp4_qkv_bytes", "sa_fp4_qkv_from_blob", "sa_quantize", "sa_quanti
            "sa_fp4_qkv_bytes_s", "sa_fp4_qkv_from_blob_s", "sa_quantize_s", "sa_attn_fwd_workspace_bytes_s",
            "sa_attn_fwd_s",
            "sa_attn_fwd_host_workspace_bytes", "sa_attn_fwd_host",
-           "sa_smooth_q_bytes_s", "sa_smooth_q_from_blob_s", "sa_quantize_smooth_q",
+           "sa_smooth_q_bytes_s", "sa_smooth_q_from_blob_s", "sa_quantize_smooth_q", "sa_quantize_kv_s",
            "sa_status_string", "sa_last_device_error", "sa_selftest_wait_timeout", "sa_selftest_nvfp4_score_tile",
            "sa_selftest_exp_path", "sa_version")
 SA_STATIC_SCRATCH_FLOATS = 1 << 20
@@ -84,6 +86,8 @@ def _load():
     lib.sa_fp4_qkv_from_blob_s.restype = i
     lib.sa_quantize_s.argtypes = [vp, vp, vp, shp, i, ctypes.POINTER(SaFp4Qkv), vp]
     lib.sa_quantize_s.restype = i
+    lib.sa_quantize_kv_s.argtypes = [vp, vp, shp, i, ctypes.POINTER(SaFp4Qkv), vp]
+    lib.sa_quantize_kv_s.restype = i
     lib.sa_smooth_q_bytes_s.argtypes = [shp, ctypes.POINTER(sz)]
     lib.sa_smooth_q_bytes_s.restype = sz
     lib.sa_smooth_q_from_blob_s.argtypes = [vp, shp, ctypes.POINTER(SaFp4Sq)]
@@ -278,6 +282,29 @@ def sa_quantize(q, k, v, out=None, stream=None, layout="bhld", smooth_q=False):
     return out
 
 
+def sa_quantize_kv(k, v, H, Lq=None, out=None, stream=None, layout="bhld"):
+    """Smooth-K + NVFP4 quantisation of K and V only (sa_quantize_kv_s), for
+    sa_attn_fwd(q, f, mode="nvfp4_fq"), which quantises Q inside the
+    attention kernel.  H: query heads; Lq: query length (default the key
+    length).  Returns an FP4QKV whose Q buffers are unused."""
+    _bf16_cuda(k, "k"), _bf16_cuda(v, "v")
+    if layout == "bhld":
+        B, Hkv, Lkv, d = k.shape
+        flag = 0
+    elif layout == "blhd":
+        B, Lkv, Hkv, d = k.shape
+        flag = SA_LAYOUT_BLHD
+    else:
+        raise ValueError(f"unknown layout {layout!r}")
+    Lq = Lkv if Lq is None else Lq
+    if out is None:
+        out = FP4QKV(B, H, Hkv, Lq, d, device=k.device, Lkv=Lkv)
+    shape = SaShape(B, H, Hkv, Lq, Lkv, d)
+    _check(lib.sa_quantize_kv_s(_ptr(k), _ptr(v), ctypes.byref(shape), flag, ctypes.byref(out.struct),
+                                _stream(stream)), "sa_quantize_kv_s")
+    return out
+
+
 def sa_quantize_static_scratch(q, k, v, out=None, stream=None):
     """sa_quantize without caller-provided scratch (see sa.h): the K-mean partial
     sums live in the library's fixed per-device array.  Returns an FP4QKV."""
@@ -304,6 +331,8 @@ def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=
     mode "nvfp4": q is an FP4QKV from sa_quantize, k and v None.
     mode "nvfp4_sq": the smooth-Q variant, q an FP4QKV from
     sa_quantize(smooth_q=True).
+    mode "nvfp4_fq": Q quantised inside the attention kernel: q the bf16 Q
+    tensor, k an FP4QKV from sa_quantize_kv, v None.
     out_dtype: torch.bfloat16 (default) or torch.float32 (SA_OUT_FP32).
     nsplit None: sa_attn_fwd (no split-KV); otherwise sa_attn_fwd_ws with that
     nsplit (0 = the library's choice) and `workspace` (a uint8 CUDA tensor,
@@ -318,6 +347,18 @@ def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=
         (B, H, Hkv, L, Lkv, d), _ = _dims(q, k, layout)
         args = (_ptr(q), _ptr(k), _ptr(v))
         m = SA_MODE_BF16
+        dev = q.device
+    elif mode == "nvfp4_fq":
+        if not isinstance(k, FP4QKV) or v is not None:
+            raise ValueError("nvfp4_fq mode takes the bf16 Q as q, an FP4QKV from sa_quantize_kv as k, and no v")
+        _bf16_cuda(q, "q")
+        B, H, Hkv, L, d = k.dims
+        Lkv = k.Lkv
+        qshape = (B, L, H, d) if lflag else (B, H, L, d)
+        if tuple(q.shape) != qshape:
+            raise ValueError(f"q must have shape {qshape}")
+        args = (_ptr(q), ctypes.cast(ctypes.pointer(k.struct), ctypes.c_void_p), None)
+        m = SA_MODE_NVFP4_FQ
         dev = q.device
     elif mode in ("nvfp4", "nvfp4_sq"):
         if not isinstance(q, FP4QKV) or k is not None or v is not None:

@@ -30,7 +30,8 @@
 // per row: softmax, P quantisation, O correction, epilogue); warp 8 issues TMA
 // and bulk copies; warp 9 issues the S MMAs and warp 10 the P.V MMAs, each
 // with the scale-factor copies they need (the three warps run their loops with
-// all lanes and issue from one elected lane); warp 11 idles.  Tensor memory: S
+// all lanes and issue from one elected lane); warp 11 idles (fused Q: it
+// stages bf16 Q).  Tensor memory: S
 // (128 columns, shared by both query tiles), O0, O1 (d columns each), then
 // scale factors (4 columns per 64-deep K chunk, copied from SMEM with
 // tcgen05.cp, replicated to the four lane quarters).
@@ -50,10 +51,21 @@
 // warpgroup of a query tile stages its 512-byte dS row of each key tile in
 // shared memory (a bulk copy issued by its thread 0 one tile ahead, three
 // buffers) and adds it to the scores; the rest is unchanged.
+//
+// Fused-Q variant (FQ): the kernel reads bf16 Q and quantises it itself, with
+// the arithmetic of sa_quantize (quant_group.cuh), so the result is the same
+// bytes and the same O.  Warp 11 copies a unit's bf16 Q tiles by TMA into a
+// staging area (64-channel x 128-token boxes, 128B swizzle) once the previous
+// unit's were quantised; each softmax thread quantises its own row of its
+// query tile into the Q buffer of the unit's parity: the first unit's before
+// the loop, the next unit's when the current unit's tiles are done (before
+// its epilogue), so that the S MMAs of the next unit can start while the
+// epilogue runs.  Q's full barriers then count the eight softmax warps.
 
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "quant_group.cuh"
 #include "sm100.cuh"
 #include "work.cuh"
 
@@ -64,6 +76,7 @@ constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int kThreads = 384;
 constexpr uint32_t kProducerSleepNs = 256;   // poll interval of the TMA producer's waits
+constexpr uint32_t kStageSleepNs = 512;      // poll interval of the fused-Q staging warp's waits
 constexpr int kSoftmaxRegs = 200;   // 8 softmax warps
 constexpr int kOtherRegs = 96;      // producer / MMA warpgroup
 constexpr int kLaunchRegs = 168;    // 65536 / 384 rounded down to a multiple of 8
@@ -98,8 +111,15 @@ struct CfgF4 {
   // smooth-Q: the score-correction rows of 128 keys, [query tile][3 buffers]
   static constexpr int kOffDs = kOffPSf + 4 * kPSfBytes;
   static constexpr int kOffBar = kOffDs + 2 * 3 * 512;
-  static constexpr int kNumBars = 4 + 4 * NS + 8 + 2 + 6;
+  static constexpr int kNumBars = 4 + 4 * NS + 8 + 2 + 6 + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+  // fused Q (the kernel quantises bf16 Q itself): the unit's bf16 Q tiles as
+  // TMA boxes of 64 channels x 128 tokens (128B swizzle, 1024-byte aligned)
+  // and the reciprocal table of the quantiser's quotients
+  static constexpr int kStageBox = 128 * 64 * 2;
+  static constexpr int kOffQStage = (kOffBar + kNumBars * 8 + 16 + 1023) & ~1023;
+  static constexpr int kOffRtab = kOffQStage + 2 * (D / 64) * kStageBox;
+  static constexpr int kSmemBytesFq = kOffRtab + 128 * 8 + 1024;
   // Q/K rows of 64 bytes use the 64B swizzle, rows of 32 bytes the 32B one.
   static constexpr uint32_t kQKSwz = (D == 128) ? kSwizzle64B : kSwizzle32B;
   static constexpr uint32_t kQKSbo = 8 * kRowBytes;
@@ -125,7 +145,7 @@ struct CfgF4 {
 
 struct BarsF4 {
   uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *s_free, *p_full, *o_done, *drain,
-      *ds_full;
+      *ds_full, *qs_full;
 };
 
 // Shared-memory matrix descriptors: each issuing warp builds a base
@@ -160,7 +180,35 @@ __device__ __forceinline__ void ds_copy(uint8_t* dst, const float* src, uint64_t
   bulk_load(dst, src, 512, bar);
 }
 
-template <int D, bool OUT32, bool SQ>
+// Fused Q: row r (0..127) of one query tile, quantised from its staged bf16
+// boxes (D/64 boxes of 64 channels x 128 tokens, 128B swizzle) into a Q
+// buffer as the Q loads would leave sa_quantize's bytes there: codes in K-major
+// rows (64B swizzle for 64-byte rows: 16-byte chunk c at c ^ ((r >> 1) & 3);
+// 32B swizzle for 32-byte rows: c ^ ((r >> 2) & 1)), the scale word of each
+// 64-channel block at byte (r % 32) * 16 + (r / 32) * 4 of its 512-byte block.
+// (One out-of-line copy: the softmax warps reach it from three places, and
+// inlined copies of it next to their tile loop cost instruction fetch stalls.)
+template <int D>
+__device__ __noinline__ void fq_quant_row(const uint8_t* stage, const float2* rtab, uint8_t* qtile, uint8_t* qsf,
+                                          int r) {
+  using C = CfgF4<D>;
+#pragma unroll 1
+  for (int quad = 0; quad < D / 64; ++quad) {
+    uint32_t w[32], codes[8], sfw;
+    qg::load_box_row(stage + quad * C::kStageBox, r, w);
+    qg::quant_q_quad(w, rtab, codes, sfw);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int ch = 2 * quad + h;
+      const int phys = D == 128 ? (ch ^ ((r >> 1) & 3)) : (ch ^ ((r >> 2) & 1));
+      *reinterpret_cast<uint4*>(qtile + r * C::kRowBytes + phys * 16) =
+          make_uint4(codes[4 * h], codes[4 * h + 1], codes[4 * h + 2], codes[4 * h + 3]);
+    }
+    *reinterpret_cast<uint32_t*>(qsf + quad * 512 + (r & 31) * 16 + (r >> 5) * 4) = sfw;
+  }
+}
+
+template <int D, bool OUT32, bool SQ, bool FQ>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const uint8_t* __restrict__ q_sf,
@@ -184,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   bars.o_done = bars.p_full + 2;
   bars.drain = bars.o_done + 2;
   bars.ds_full = bars.drain + 2;          // [query tile][3]
+  bars.qs_full = bars.ds_full + 6;        // fused Q: the unit's bf16 Q tiles have landed in the staging
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_base + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -197,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int q = 0; q < 2; ++q) {
       mbar_init(bars.s_free + q, 128);
       mbar_init(bars.p_full + q, 128);
+      if constexpr (FQ) mbar_init(bars.q_full + q, 8);   // one arrival per softmax warp
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -204,6 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 8) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
+  }
+  if constexpr (FQ) {
+    if (threadIdx.x < 128)
+      reinterpret_cast<float2*>(smem + C::kOffRtab)[threadIdx.x] = qg::rtab_entry(threadIdx.x);
   }
   tc_fence_before();
   __syncthreads();
@@ -238,23 +292,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && unit_next(work, it, u)) {
         const int qb = ug & 1;
-        // Q of this unit into buffer qb, once the S MMAs of unit ug-2 (the
-        // last to read that buffer) are complete
-        if (ug >= 2 && !mbar_wait_backoff_warp(bars.q_empty + qb, ((ug >> 1) - 1) & 1, abort_flag, wait_ns,
-                                               kProducerSleepNs)) {
-          ok = false;
-          break;
-        }
         const long long bhq = u.bh;
         const long long bhk = (long long)(u.bh / H) * Hkv + (u.bh % H) / G;
-        if (leader) {
-          mbar_arrive_expect_tx(bars.q_full + qb, u.nq * (C::kQBytes + C::kQSfBytes));
-          for (int q = 0; q < u.nq; ++q) {
-            const int qt = u.qt0 + q;
-            tma_load_2d(smem + C::kOffQ + (2 * qb + q) * C::kQBytes, &tmap_q, bars.q_full + qb, 0,
-                        (int)(bhq * Lqp + (long long)qt * BM));
-            bulk_load(smem + C::kOffQSf + (2 * qb + q) * C::kQSfBytes,
-                      q_sf + (bhq * (Lqp / 128) + qt) * C::kQSfBytes, C::kQSfBytes, bars.q_full + qb);
+        if constexpr (!FQ) {
+          // Q of this unit into buffer qb, once the S MMAs of unit ug-2 (the
+          // last to read that buffer) are complete
+          if (ug >= 2 && !mbar_wait_backoff_warp(bars.q_empty + qb, ((ug >> 1) - 1) & 1, abort_flag, wait_ns,
+                                                 kProducerSleepNs)) {
+            ok = false;
+            break;
+          }
+          if (leader) {
+            mbar_arrive_expect_tx(bars.q_full + qb, u.nq * (C::kQBytes + C::kQSfBytes));
+            for (int q = 0; q < u.nq; ++q) {
+              const int qt = u.qt0 + q;
+              tma_load_2d(smem + C::kOffQ + (2 * qb + q) * C::kQBytes, &tmap_q, bars.q_full + qb, 0,
+                          (int)(bhq * Lqp + (long long)qt * BM));
+              bulk_load(smem + C::kOffQSf + (2 * qb + q) * C::kQSfBytes,
+                        q_sf + (bhq * (Lqp / 128) + qt) * C::kQSfBytes, C::kQSfBytes, bars.q_full + qb);
+            }
           }
         }
         ++ug;
@@ -294,7 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (*abort_flag) {
         // let every copy already issued land before the CTA (and its shared
         // memory) goes away: the last issue into each Q buffer and each stage
-        for (int g = (ug > 2 ? ug - 2 : 0); g < ug; ++g) mbar_wait_drain(bars.q_full + (g & 1), (g >> 1) & 1, wait_ns);
+        if constexpr (!FQ) {
+          for (int g = (ug > 2 ? ug - 2 : 0); g < ug; ++g)
+            mbar_wait_drain(bars.q_full + (g & 1), (g >> 1) & 1, wait_ns);
+        }
         for (int g = (nk > C::NS ? nk - C::NS : 0); g < nk; ++g)
           mbar_wait_drain(bars.k_full + g % C::NS, (g / C::NS) & 1, wait_ns);
         for (int g = (nv > C::NS ? nv - C::NS : 0); g < nv; ++g)
@@ -441,6 +500,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         mbar_wait_drain(bars.drain + 1, 0, wait_ns);
       }
+    } else if (FQ && warp == 11) {
+      // ------------------------------------------------- fused Q: staging
+      // A unit's bf16 Q tiles (tokens past Lq read as zeros) into the staging,
+      // once every softmax warp has quantised the previous unit's from it
+      // (that unit's Q full barrier).
+      const bool leader = elect_one();
+      UnitIter it;
+      unit_iter_init(work, it);
+      AttnUnitRef u;
+      pdl_wait();                                       // Q is written (programmatic launch)
+      int ug = 0;
+      bool ok = true;
+      while (ok && unit_next(work, it, u)) {
+        // (a wait of about one unit: polled with sleeps, so as not to take
+        // issue slots from the softmax warps of this SM sub-partition)
+        if (ug >= 1)
+          ok = mbar_wait_backoff_warp(bars.q_full + ((ug - 1) & 1), ((ug - 1) >> 1) & 1, abort_flag, wait_ns,
+                                      kStageSleepNs);
+        if (!ok) break;
+        if (leader) {
+          mbar_arrive_expect_tx(bars.qs_full, u.nq * (D / 64) * C::kStageBox);
+          for (int q = 0; q < u.nq; ++q)
+            for (int b = 0; b < D / 64; ++b)
+              tma_load_4d(smem + C::kOffQStage + (q * (D / 64) + b) * C::kStageBox, &tmap_q, bars.qs_full, 64 * b,
+                          (u.qt0 + q) * BM, (int)(u.bh % H), (int)(u.bh / H));
+        }
+        __syncwarp();
+        ++ug;
+      }
+      // the last copy has landed before the shared memory goes away (after
+      // an abort it may not have been waited for)
+      if (ug > 0) mbar_wait_drain(bars.qs_full, (ug - 1) & 1, wait_ns);
     }
   } else {
     reg_alloc<SQ ? kSoftmaxRegsSq : kSoftmaxRegs>();
@@ -468,9 +559,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     AttnUnitRef u;
     int cq = 0;               // tiles of this query-tile slot so far (over the whole list)
     bool ok = true;
+    // Fused Q: this thread's row of query tile q of unit g (index over the
+    // whole list) into Q buffer g & 1, once the unit's bf16 tiles are staged
+    // and the S MMAs of unit g - 2 (the buffer's last readers) are complete;
+    // every warp arrives on the buffer's full barrier, quantising or not.
+    auto fq_unit = [&](const AttnUnitRef& v, int g) -> bool {
+      const int qb = g & 1;
+      if (!mbar_wait_warp(bars.qs_full, g & 1, abort_flag, wait_ns)) return false;
+      if (g >= 2 && !mbar_wait_warp(bars.q_empty + qb, ((g >> 1) - 1) & 1, abort_flag, wait_ns)) return false;
+      if (q < v.nq)
+        fq_quant_row<D>(smem + C::kOffQStage + q * (D / 64) * C::kStageBox,
+                        reinterpret_cast<const float2*>(smem + C::kOffRtab), smem + C::kOffQ + (2 * qb + q) * C::kQBytes,
+                        smem + C::kOffQSf + (2 * qb + q) * C::kQSfBytes, r);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.q_full + qb);
+      return true;
+    };
+    // ... the unit after the current one (g + 1), if the list has one
+    auto fq_next = [&](int g) -> bool {
+      UnitIter t = it;
+      AttnUnitRef v;
+      return unit_next(work, t, v) ? fq_unit(v, g + 1) : true;
+    };
+    int us = -1;              // fused Q: index of the current unit over the whole list
+    if constexpr (FQ) ok = fq_next(-1);                // the first unit
     while (ok && unit_next(work, it, u)) {
       const int nq = q ? u.n[1] : u.n[0];
-      if (q >= u.nq) continue;                         // the unit has no second query tile
+      ++us;
+      if (q >= u.nq) {                                 // the unit has no second query tile
+        if constexpr (FQ) ok = fq_next(us);
+        continue;
+      }
       const int qt = u.qt0 + q;
       float m_run = -INFINITY, m_ref = 0.f, lam = 0.f;
       bool have_ref = false;
@@ -653,6 +773,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bars.p_full + q);
       }
       if (!ok) break;
+      // fused Q: the next unit's, so that its S MMAs overlap this epilogue
+      if constexpr (FQ) {
+        if (!fq_next(us)) {
+          ok = false;
+          break;
+        }
+      }
       // ---- the unit's result for this row: O, or a partial for the combine
       // pass (O unnormalised in units of 2^m_ref / 2688 as is lam, m_ref
       // (-inf if no key tile was live) and lam)
@@ -731,22 +858,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool OUT32, bool SQ>
+template <int D, bool OUT32, bool SQ, bool FQ>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const sa_fp4_qkv& x,
                      void* o, const Strides& so, const Dims& dm, int causal, int nsplit, const SplitOut& part,
                      const float* ds, cudaStream_t s) {
   using C = CfgF4<D>;
+  constexpr int kSmem = FQ ? C::kSmemBytesFq : C::kSmemBytes;
   // kernel attributes are per device: set them on the first launch on each
   static std::atomic<bool> attr_done[kMaxDevices];
   cudaError_t e = once_per_device(attr_done, [] {
     // The warpgroup register split assumes kLaunchRegs registers per thread at
     // launch; with fewer, a setmaxnreg increase could never be satisfied.
     cudaFuncAttributes fa;
-    cudaError_t r = cudaFuncGetAttributes(&fa, attn_nvfp4_kernel<D, OUT32, SQ>);
+    cudaError_t r = cudaFuncGetAttributes(&fa, attn_nvfp4_kernel<D, OUT32, SQ, FQ>);
     if (r != cudaSuccess) return r;
     if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
-    return cudaFuncSetAttribute(attn_nvfp4_kernel<D, OUT32, SQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                C::kSmemBytes);
+    return cudaFuncSetAttribute(attn_nvfp4_kernel<D, OUT32, SQ, FQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmem);
   });
   if (e != cudaSuccess) return e;
   int ctas = 0;
@@ -757,8 +885,8 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   // the kernel before (sa_quantize's last launch, as a rule); the producer
   // waits for it before its first load
   cudaLaunchAttribute attr;
-  const cudaLaunchConfig_t cfg = pdl_launch_config(dim3(ctas), dim3(kThreads), C::kSmemBytes, s, &attr);
-  e = cudaLaunchKernelEx(&cfg, attn_nvfp4_kernel<D, OUT32, SQ>, tq, tk, tv,
+  const cudaLaunchConfig_t cfg = pdl_launch_config(dim3(ctas), dim3(kThreads), kSmem, s, &attr);
+  e = cudaLaunchKernelEx(&cfg, attn_nvfp4_kernel<D, OUT32, SQ, FQ>, tq, tk, tv,
                                      static_cast<const uint8_t*>(x.q_sf), static_cast<const uint8_t*>(x.k_sf),
                                      static_cast<const uint8_t*>(x.v_sf), o, dm.H, dm.Hkv, dm.Lq, dm.Lkv, causal,
                                      work, part, so, ds, kWaitLimitNs);
@@ -905,22 +1033,31 @@ cudaError_t launch_exp_path_selftest(const float* x, const float* y, int n, floa
   return cudaGetLastError();
 }
 
-template <int D, bool SQ>
+template <int D, bool SQ, bool FQ>
 cudaError_t launch_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const sa_fp4_qkv& qkv,
                       void* o, const Strides& so, const Dims& dm, int causal, bool out_f32, int nsplit,
                       const SplitOut& part, const float* ds, cudaStream_t s) {
-  return out_f32 ? launch_d<D, true, SQ>(tq, tk, tv, qkv, o, so, dm, causal, nsplit, part, ds, s)
-                 : launch_d<D, false, SQ>(tq, tk, tv, qkv, o, so, dm, causal, nsplit, part, ds, s);
+  return out_f32 ? launch_d<D, true, SQ, FQ>(tq, tk, tv, qkv, o, so, dm, causal, nsplit, part, ds, s)
+                 : launch_d<D, false, SQ, FQ>(tq, tk, tv, qkv, o, so, dm, causal, nsplit, part, ds, s);
+}
+
+template <int D>
+cudaError_t launch_variant(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const sa_fp4_qkv& qkv, void* o, const Strides& so, const Dims& dm, int causal,
+                           bool out_f32, int nsplit, const SplitOut& part, cudaStream_t s, const float* ds,
+                           bool fuse_q) {
+  if (ds) return launch_dq<D, true, false>(tq, tk, tv, qkv, o, so, dm, causal, out_f32, nsplit, part, ds, s);
+  if (fuse_q) return launch_dq<D, false, true>(tq, tk, tv, qkv, o, so, dm, causal, out_f32, nsplit, part, ds, s);
+  return launch_dq<D, false, false>(tq, tk, tv, qkv, o, so, dm, causal, out_f32, nsplit, part, ds, s);
 }
 
 cudaError_t launch_attn_nvfp4(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const sa_fp4_qkv& qkv, void* o, const Strides& so, const Dims& dm, int causal,
-                              bool out_f32, int nsplit, const SplitOut& part, cudaStream_t s, const float* ds) {
-  if (dm.d == 64)
-    return ds ? launch_dq<64, true>(tq, tk, tv, qkv, o, so, dm, causal, out_f32, nsplit, part, ds, s)
-              : launch_dq<64, false>(tq, tk, tv, qkv, o, so, dm, causal, out_f32, nsplit, part, ds, s);
-  return ds ? launch_dq<128, true>(tq, tk, tv, qkv, o, so, dm, causal, out_f32, nsplit, part, ds, s)
-            : launch_dq<128, false>(tq, tk, tv, qkv, o, so, dm, causal, out_f32, nsplit, part, ds, s);
+                              bool out_f32, int nsplit, const SplitOut& part, cudaStream_t s, const float* ds,
+                              bool fuse_q) {
+  if (ds && fuse_q) return cudaErrorInvalidValue;          // (the two variants do not combine)
+  return dm.d == 64 ? launch_variant<64>(tq, tk, tv, qkv, o, so, dm, causal, out_f32, nsplit, part, s, ds, fuse_q)
+                    : launch_variant<128>(tq, tk, tv, qkv, o, so, dm, causal, out_f32, nsplit, part, s, ds, fuse_q);
 }
 
 cudaError_t attn_nvfp4_read_error(int* out) { return read_and_clear_device_error(out); }

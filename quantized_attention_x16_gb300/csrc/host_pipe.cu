@@ -145,7 +145,7 @@ sa_status check_host_args(int B, int H, int Hkv, int L, int d, int causal, int m
   if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
   if (mode_flags & ~(0xF | SA_OUT_FP32 | SA_HOST_OVERLAP)) return SA_ERR_INVALID_ARG;
   const int mode = mode_flags & 0xF;
-  if (mode == SA_MODE_NVFP4_SQ) return SA_ERR_UNSUPPORTED;
+  if (mode == SA_MODE_NVFP4_SQ || mode == SA_MODE_NVFP4_FQ) return SA_ERR_UNSUPPORTED;
   if (mode != SA_MODE_BF16 && mode != SA_MODE_NVFP4) return SA_ERR_INVALID_ARG;
   if (chunk_pairs < 0) return SA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return SA_ERR_UNSUPPORTED;

@@ -100,9 +100,11 @@ inline size_t kmean_partial_floats(const Dims& dm) {
   return (size_t)dm.B * dm.Hkv * (size_t)(padded_len(dm.Lkv) / kMeanChunk) * (size_t)dm.d;
 }
 // tq / tk / tv: the bf16 Q, K and V heads (make_bf16_head_map: boxes of 64
-// channels x 128 tokens, 128B swizzle, zeros past L).
+// channels x 128 tokens, 128B swizzle, zeros past L).  with_q false: K and V
+// only (out.q_codes / out.q_sf untouched, tq unused), for the attention
+// kernel that quantises Q itself.
 cudaError_t launch_quantize(const Dims& dm, const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, cudaStream_t s);
+                            const CUtensorMap& tv, cudaStream_t s, bool with_q = true);
 // Same kernels, K-mean partial sums in the library's fixed per-device array.
 constexpr size_t kStaticScratchFloats = SA_STATIC_SCRATCH_FLOATS;
 cudaError_t launch_quantize_static_scratch(const Dims& dm, const sa_fp4_qkv& out, const CUtensorMap& tq,
@@ -132,10 +134,13 @@ cudaError_t launch_attn_bf16(const CUtensorMap& tq, const CUtensorMap& tk, const
 // attn_nvfp4.cu.  ds: the smooth-Q score corrections ([B*H][Lqp/128][Lkvp]
 // float32, added to every score of its query tile and key before the
 // softmax), or nullptr for the plain SA3 path.
+// fuse_q: Q arrives in bf16 (tq a make_bf16_head_map of it) and the kernel
+// quantises it itself, with sa_quantize's arithmetic (qkv.q_codes / q_sf
+// unused).
 cudaError_t launch_attn_nvfp4(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const sa_fp4_qkv& qkv, void* o, const Strides& so, const Dims& dm, int causal,
                               bool out_f32, int nsplit, const SplitOut& part, cudaStream_t s,
-                              const float* ds = nullptr);
+                              const float* ds = nullptr, bool fuse_q = false);
 // smooth_q.cu: after sa_quantize, Q re-quantised as Q' = Q - its 128-token
 // block mean (x.q_codes / x.q_sf overwritten, the means to qmean
 // [B*H][Lqp/128][d]) and the score corrections ds [B*H][Lqp/128][Lkvp] from

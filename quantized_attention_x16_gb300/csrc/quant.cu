@@ -16,6 +16,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "quant_group.cuh"
 #include "sm100.cuh"
 
 namespace sa {
@@ -23,82 +24,7 @@ namespace sa {
 namespace {
 
 
-// ---------------------------------------------------------------------------
-// Group arithmetic.
-//
-// Every 1x16 group: s8 = e4m3_rne_sat(RN(max|x| / 6)), code_i =
-// e2m1_rne_sat(RN(x_i / s)) with s = decode(s8), all codes +0 when s8 == 0.
-// Neither quotient uses a divide instruction:
-//  * RN(max|x| / 6): Markstein's correction step.  With y = RN(1/6), q0 =
-//    RN(a*y) and the exact remainder r = a - q0*6 from one FMA, RN(q0 + r*y)
-//    = RN(a/6).
-//  * code_i from q = RN(x*yh + RN(x*yl)) (one product and one FMA), where
-//    yh = RD(1/s) and yl = RN((1 - s*yh) * yh): the residual 1 - s*yh is
-//    exact and >= 0, and yh + yl is 1/s to 2^-46, so q is x/s plus at most
-//    2^-45 |x/s| before its one rounding.  The code of q can differ from the
-//    code of RN(x/s) only where that rounding is decided differently next to
-//    an e2m1 boundary T, i.e. for x/s within 2^-45 of T or of a float32
-//    midpoint T +- ulp/2 beside it.  x/s = T exactly gives q = T.  A midpoint
-//    T +- ulp/2 has a 25-bit odd significand, so s (4 significant bits) times
-//    it is no float32 and x/s stays at least 2^-30 (relative) away from it.
-//    So the codes are those of the correctly rounded quotient, for bf16 x (Q,
-//    V) and float32 x (K' = K - mean) alike; this is checked on the host for
-//    every bf16 x and every e4m3 scale, and for every float32 significand
-//    near each boundary.  yl >= 0 keeps the sign of a zero x (+0 * yh + +0 =
-//    +0, -0 * yh + -0 = -0).  (yh, yl) is looked up by the scale byte in a
-//    128-entry shared-memory table.
-
-// max(|a|, |b|) per bf16 half (the result's sign bits are not used).
-__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-// Per-half maxima of |x| over n words -> (max of the low halves, max of the high halves) as floats.
-template <int N>
-__device__ __forceinline__ void absmax_halves(const uint32_t* w, float& lo, float& hi) {
-  uint32_t m[N];
-#pragma unroll
-  for (int i = 0; i < N; ++i) m[i] = w[i];
-#pragma unroll
-  for (int s = 1; s < N; s *= 2)
-#pragma unroll
-    for (int i = 0; i + s < N; i += 2 * s) m[i] = absmax_bf16x2(m[i], m[i + s]);
-  lo = __uint_as_float((m[0] & 0x7FFFu) << 16);
-  hi = __uint_as_float(m[0] & 0x7FFF0000u);
-}
-
-// RN(a / 6) for a >= 0 (Markstein step, exact).
-__device__ __forceinline__ float div6_rn(float a) {
-  const float y6 = __uint_as_float(0x3E2AAAABu);        // RN(1/6)
-  const float q6 = a * y6;
-  return fmaf(fmaf(-q6, 6.0f, a), y6, q6);
-}
-
-// The e4m3 scale bytes of two groups from their max |x| (low byte: a0).
-__device__ __forceinline__ uint32_t scale_pair(float a0, float a1) {
-  return cvt_e4m3x2(div6_rn(a0), div6_rn(a1));
-}
-
-// Codes of 16 values x[0..15] for scale byte s8: two words.
-__device__ __forceinline__ void codes_group(const float* x, uint32_t s8, const float2* rtab, uint32_t* codes) {
-  const float2 r = rtab[s8];
-  float q[16];
-#pragma unroll
-  for (int i = 0; i < 16; i += 2) {
-    float t0, t1;
-    mul2(t0, t1, x[i], x[i + 1], r.y, r.y);
-    fma2(q[i], q[i + 1], x[i], x[i + 1], r.x, r.x, t0, t1);
-  }
-  const bool z = s8 == 0u;
-  codes[0] = z ? 0u : cvt_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
-  codes[1] = z ? 0u : cvt_e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]);
-}
-
-// bf16 pair word -> two floats (channel/token 2i in the low half).
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+using namespace qg;   // the group arithmetic (quant_group.cuh)
 
 // ---------------------------------------------------------------------------
 // Two launches of one persistent kernel body, each CTA a TMA producer warp and
@@ -247,38 +173,12 @@ __device__ __forceinline__ void quant_rows(const QuantArgs& a, const TileRef& t,
   const int tok = t.t0 + tl;
   const int Lp = IS_K ? a.Lkvp : a.Lqp;
   if (tok >= Lp) return;                               // (d = 64: warp-uniform)
-  const uint8_t* src = tile + box * kBoxBytes + rr * 128;
-  const uint32_t x7 = (uint32_t)(rr & 7) << 4;
   uint32_t w[32];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint4 v = *reinterpret_cast<const uint4*>(src + (((uint32_t)i << 4) ^ x7));
-    w[4 * i] = v.x;
-    w[4 * i + 1] = v.y;
-    w[4 * i + 2] = v.z;
-    w[4 * i + 3] = v.w;
-  }
+  load_box_row(tile + box * kBoxBytes, rr, w);
   uint32_t codes[8];
   uint32_t sfw;
   if constexpr (!IS_K) {
-    float am[4];
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      float lo, hi;
-      absmax_halves<8>(w + 8 * g, lo, hi);
-      am[g] = fmaxf(lo, hi);
-    }
-    sfw = scale_pair(am[0], am[1]) | (scale_pair(am[2], am[3]) << 16);
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      float x[16];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        x[2 * i] = bf16_lo(w[8 * g + i]);
-        x[2 * i + 1] = bf16_hi(w[8 * g + i]);
-      }
-      codes_group(x, (sfw >> (8 * g)) & 0xFFu, rtab, codes + 2 * g);
-    }
+    quant_q_quad(w, rtab, codes, sfw);
   } else {
     // K' = RN(k - mean); a token past L arrived as zeros and K' there is kept
     // zero (no mean subtracted)
@@ -422,17 +322,7 @@ __global__ void __launch_bounds__(kThreadsQ, kCtasPerSm)
     abort_flag = 0;
     fence_barrier_init();
   }
-  if (threadIdx.x < 128) {
-    // (yh, yl) of scale byte s8 (0 and the NaN code: unused)
-    const uint32_t s8 = threadIdx.x;
-    float2 r = make_float2(0.f, 0.f);
-    if (s8 != 0u && s8 != 0x7Fu) {
-      const float sf = e4m3_to_f32(s8);
-      const float yh = __frcp_rd(sf);
-      r = make_float2(yh, __fmul_rn(fmaf(-sf, yh, 1.0f), yh));
-    }
-    rtab[s8] = r;
-  }
+  if (threadIdx.x < 128) rtab[threadIdx.x] = rtab_entry(threadIdx.x);   // (yh, yl) of each scale byte
   __syncthreads();
 
   if (warp == kWorkers) {
@@ -523,7 +413,7 @@ __global__ void __launch_bounds__(kThreadsQ, kCtasPerSm)
 
 template <int D>
 cudaError_t launch_quantize_impl(const Dims& dm, const sa_fp4_qkv& out, float* partials, const CUtensorMap& tq,
-                                 const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
+                                 const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s, bool with_q = true) {
   constexpr int R = TileGeo<D>::kRows;
   QuantArgs a;
   a.qc = static_cast<uint8_t*>(out.q_codes);
@@ -541,7 +431,7 @@ cudaError_t launch_quantize_impl(const Dims& dm, const sa_fp4_qkv& out, float* p
   a.Hkv = dm.Hkv;
   a.tph_q = (a.Lqp + R - 1) / R;
   a.tph_k = (a.Lkvp + R - 1) / R;
-  a.ntile_q = dm.B * dm.H * a.tph_q;
+  a.ntile_q = with_q ? dm.B * dm.H * a.tph_q : 0;       // (without Q: pass 1 takes the K-mean tiles only)
   a.ntile_k = dm.B * dm.Hkv * a.tph_k;
   a.wait_ns = kWaitLimitNs;
   fastdiv_params((uint32_t)a.tph_q, a.dq_m, a.dq_l);
@@ -581,10 +471,10 @@ cudaError_t launch_quantize_impl(const Dims& dm, const sa_fp4_qkv& out, float* p
 cudaError_t quant_read_error(int* out) { return read_and_clear_device_error(out); }
 
 cudaError_t launch_quantize(const Dims& dm, const sa_fp4_qkv& out, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, cudaStream_t s) {
+                            const CUtensorMap& tv, cudaStream_t s, bool with_q) {
   float* part = static_cast<float*>(out.workspace);
-  return dm.d == 64 ? launch_quantize_impl<64>(dm, out, part, tq, tk, tv, s)
-                    : launch_quantize_impl<128>(dm, out, part, tq, tk, tv, s);
+  return dm.d == 64 ? launch_quantize_impl<64>(dm, out, part, tq, tk, tv, s, with_q)
+                    : launch_quantize_impl<128>(dm, out, part, tq, tk, tv, s, with_q);
 }
 
 // ---------------------------------------------------------------------------

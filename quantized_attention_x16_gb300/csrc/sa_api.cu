@@ -206,6 +206,28 @@ sa_status sa_quantize_s(const void* q, const void* k, const void* v, const sa_sh
              : SA_ERR_CUDA;
 }
 
+sa_status sa_quantize_kv_s(const void* k, const void* v, const sa_shape* shape, int flags, const sa_fp4_qkv* out,
+                           sa_stream_t stream) {
+  if (!shape) return SA_ERR_INVALID_ARG;
+  const Dims dm = dims_of(shape);
+  const sa_status st = check_dims(dm);
+  if (st != SA_OK) return st;
+  if (flags & ~SA_LAYOUT_BLHD) return SA_ERR_INVALID_ARG;
+  if (dm.B == 0 || (dm.Lq == 0 && dm.Lkv == 0)) return SA_OK;
+  if (dm.Lq == 0) return SA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !out || !aligned16(out->k_codes) || !aligned16(out->k_sf) ||
+      !aligned16(out->v_codes) || !aligned16(out->v_sf) || !aligned16(out->k_mean) || !aligned16(out->workspace))
+    return SA_ERR_INVALID_ARG;
+  const bool blhd = (flags & SA_LAYOUT_BLHD) != 0;
+  CUtensorMap tk, tv;
+  if (!make_bf16_head_map(&tk, k, dm.Hkv, dm.Lkv, dm, blhd) || !make_bf16_head_map(&tv, v, dm.Hkv, dm.Lkv, dm, blhd))
+    return SA_ERR_CUDA;
+  // (the Q map is not read: pass 1 takes the K-mean tiles only)
+  return launch_quantize(dm, *out, tk, tk, tv, reinterpret_cast<cudaStream_t>(stream), false) == cudaSuccess
+             ? SA_OK
+             : SA_ERR_CUDA;
+}
+
 sa_status sa_quantize_ex(const void* q, const void* k, const void* v, int B, int H, int Hkv, int L, int d, int flags,
                          const sa_fp4_qkv* out, sa_stream_t stream) {
   const sa_shape s{B, H, Hkv, L, L, d};
@@ -299,7 +321,9 @@ sa_status sa_quantize_smooth_q(const void* q, const sa_shape* shape, int flags, 
 // NVFP4 calls that run on the few-row decode kernel (the smooth-Q variant
 // always runs on the prefill kernel).
 static bool use_decode(const Dims& dm, int mode) { return mode == SA_MODE_NVFP4 && decode_eligible(dm); }
-static bool is_fp4(int mode) { return mode == SA_MODE_NVFP4 || mode == SA_MODE_NVFP4_SQ; }
+static bool is_fp4(int mode) {
+  return mode == SA_MODE_NVFP4 || mode == SA_MODE_NVFP4_SQ || mode == SA_MODE_NVFP4_FQ;
+}
 
 static int resolve_nsplit(const Dims& dm, int causal, int mode, int requested) {
   if (requested == 1) return 1;
@@ -383,12 +407,17 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
     return launch_attn_bf16(tq, tk, tv, o, so, dm, causal, out_f32, nsplit, part, s) == cudaSuccess ? SA_OK
                                                                                                     : SA_ERR_CUDA;
   }
-  if (k != nullptr || v != nullptr || q == nullptr) return SA_ERR_INVALID_ARG;
-  // SA_MODE_NVFP4_SQ: q is an sa_fp4_sq, whose first member is the sa_fp4_qkv
+  // SA_MODE_NVFP4_FQ: q is the bf16 Q, k the sa_fp4_qkv of K and V (its Q
+  // buffers unused); otherwise q is the sa_fp4_qkv (SA_MODE_NVFP4) or the
+  // sa_fp4_sq, whose first member is the sa_fp4_qkv (SA_MODE_NVFP4_SQ)
+  const bool fq = mode == SA_MODE_NVFP4_FQ;
+  if (fq ? (q == nullptr || k == nullptr || v != nullptr || !aligned16(q))
+         : (k != nullptr || v != nullptr || q == nullptr))
+    return SA_ERR_INVALID_ARG;
   const sa_fp4_sq* xs = mode == SA_MODE_NVFP4_SQ ? static_cast<const sa_fp4_sq*>(q) : nullptr;
-  const sa_fp4_qkv* x = xs ? &xs->fp4 : static_cast<const sa_fp4_qkv*>(q);
+  const sa_fp4_qkv* x = fq ? static_cast<const sa_fp4_qkv*>(k) : (xs ? &xs->fp4 : static_cast<const sa_fp4_qkv*>(q));
   if (xs && !aligned16(xs->ds)) return SA_ERR_INVALID_ARG;
-  if (!aligned16(x->q_codes) || !aligned16(x->q_sf) || !aligned16(x->k_codes) || !aligned16(x->k_sf) ||
+  if ((!fq && (!aligned16(x->q_codes) || !aligned16(x->q_sf))) || !aligned16(x->k_codes) || !aligned16(x->k_sf) ||
       !aligned16(x->v_codes) || !aligned16(x->v_sf))
     return SA_ERR_INVALID_ARG;
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -396,7 +425,8 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
   const CUtensorMapSwizzle qk_swz = d == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
   // the quantised layouts hold whole 128-token tiles
   const int Lqp = padded_len(dm.Lq), Lkvp = padded_len(dm.Lkv);
-  if (!make_map(&tq, u8, x->q_codes, d / 2, (uint64_t)dm.B * dm.H * Lqp, 1, d / 2, 128, qk_swz) ||
+  if (!(fq ? make_bf16_head_map(&tq, q, dm.H, dm.Lq, dm, blhd)
+           : make_map(&tq, u8, x->q_codes, d / 2, (uint64_t)dm.B * dm.H * Lqp, 1, d / 2, 128, qk_swz)) ||
       !make_map(&tk, u8, x->k_codes, d / 2, (uint64_t)dm.B * dm.Hkv * Lkvp, 1, d / 2, 128, qk_swz) ||
       !make_map(&tv, u8, x->v_codes, Lkvp / 2, (uint64_t)dm.B * dm.Hkv * d, 1, 64, d, CU_TENSOR_MAP_SWIZZLE_64B))
     return SA_ERR_CUDA;
@@ -405,7 +435,7 @@ static sa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
   if (use_decode(dm, mode))
     return launch_attn_decode(tk, tv, *x, o, so, dm, causal, out_f32, nsplit, part, s) == cudaSuccess ? SA_OK
                                                                                                       : SA_ERR_CUDA;
-  return launch_attn_nvfp4(tq, tk, tv, *x, o, so, dm, causal, out_f32, nsplit, part, s, xs ? xs->ds : nullptr) ==
+  return launch_attn_nvfp4(tq, tk, tv, *x, o, so, dm, causal, out_f32, nsplit, part, s, xs ? xs->ds : nullptr, fq) ==
                  cudaSuccess
              ? SA_OK
              : SA_ERR_CUDA;
