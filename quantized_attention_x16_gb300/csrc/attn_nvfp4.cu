@@ -57,10 +57,9 @@
 // bytes and the same O.  Warp 11 copies a unit's bf16 Q tiles by TMA into a
 // staging area (64-channel x 128-token boxes, 128B swizzle) once the previous
 // unit's were quantised; each softmax thread quantises its own row of its
-// query tile into the Q buffer of the unit's parity: the first unit's before
-// the loop, the next unit's when the current unit's tiles are done (before
-// its epilogue), so that the S MMAs of the next unit can start while the
-// epilogue runs.  Q's full barriers then count the eight softmax warps.
+// query tile into the Q buffer of the unit's parity: the next unit's at the
+// start of each unit (the first unit's own as well), so that it is ready as early as
+// a loaded Q would be.  Q's full barriers then count the eight softmax warps.
 
 #include <cuda_bf16.h>
 
@@ -181,30 +180,38 @@ __device__ __forceinline__ void ds_copy(uint8_t* dst, const float* src, uint64_t
 }
 
 // Fused Q: row r (0..127) of one query tile, quantised from its staged bf16
-// boxes (D/64 boxes of 64 channels x 128 tokens, 128B swizzle) into a Q
-// buffer as the Q loads would leave sa_quantize's bytes there: codes in K-major
-// rows (64B swizzle for 64-byte rows: 16-byte chunk c at c ^ ((r >> 1) & 3);
-// 32B swizzle for 32-byte rows: c ^ ((r >> 2) & 1)), the scale word of each
-// 64-channel block at byte (r % 32) * 16 + (r / 32) * 4 of its 512-byte block.
-// (One out-of-line copy: the softmax warps reach it from three places, and
-// inlined copies of it next to their tile loop cost instruction fetch stalls.)
+// boxes (D/64 boxes of 64 channels x 128 tokens, 128B swizzle: 16-byte chunk
+// i of row r at chunk i ^ (r & 7)) into a Q buffer as the Q loads would leave
+// sa_quantize's bytes there: codes in K-major rows (64B swizzle for 64-byte
+// rows: 16-byte chunk c at c ^ ((r >> 1) & 3); 32B swizzle for 32-byte rows:
+// c ^ ((r >> 2) & 1)), the scale word of each 64-channel block at byte
+// (r % 32) * 16 + (r / 32) * 4 of its 512-byte block.  Arguments are
+// shared-memory addresses.
 template <int D>
-__device__ __noinline__ void fq_quant_row(const uint8_t* stage, const float2* rtab, uint8_t* qtile, uint8_t* qsf,
-                                          int r) {
+__device__ __forceinline__ void fq_quant_row(uint32_t stage, uint32_t rtab, uint32_t qtile, uint32_t qsf, int r) {
   using C = CfgF4<D>;
-#pragma unroll 1
+  const qg::SharedRtab tab{rtab};
+  const uint32_t x7 = (uint32_t)(r & 7) << 4;
+#pragma unroll
   for (int quad = 0; quad < D / 64; ++quad) {
     uint32_t w[32], codes[8], sfw;
-    qg::load_box_row(stage + quad * C::kStageBox, r, w);
-    qg::quant_q_quad(w, rtab, codes, sfw);
+    const uint32_t src = stage + quad * C::kStageBox + r * 128;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 v = lds_f4(src + (((uint32_t)i << 4) ^ x7));
+      w[4 * i] = __float_as_uint(v.x);
+      w[4 * i + 1] = __float_as_uint(v.y);
+      w[4 * i + 2] = __float_as_uint(v.z);
+      w[4 * i + 3] = __float_as_uint(v.w);
+    }
+    qg::quant_q_quad(w, tab, codes, sfw);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int ch = 2 * quad + h;
       const int phys = D == 128 ? (ch ^ ((r >> 1) & 3)) : (ch ^ ((r >> 2) & 1));
-      *reinterpret_cast<uint4*>(qtile + r * C::kRowBytes + phys * 16) =
-          make_uint4(codes[4 * h], codes[4 * h + 1], codes[4 * h + 2], codes[4 * h + 3]);
+      sts_u4(qtile + r * C::kRowBytes + phys * 16, codes[4 * h], codes[4 * h + 1], codes[4 * h + 2], codes[4 * h + 3]);
     }
-    *reinterpret_cast<uint32_t*>(qsf + quad * 512 + (r & 31) * 16 + (r >> 5) * 4) = sfw;
+    sts_u32(qsf + quad * 512 + (r & 31) * 16 + (r >> 5) * 4, sfw);
   }
 }
 
@@ -567,30 +574,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qb = g & 1;
       if (!mbar_wait_warp(bars.qs_full, g & 1, abort_flag, wait_ns)) return false;
       if (g >= 2 && !mbar_wait_warp(bars.q_empty + qb, ((g >> 1) - 1) & 1, abort_flag, wait_ns)) return false;
-      if (q < v.nq)
-        fq_quant_row<D>(smem + C::kOffQStage + q * (D / 64) * C::kStageBox,
-                        reinterpret_cast<const float2*>(smem + C::kOffRtab), smem + C::kOffQ + (2 * qb + q) * C::kQBytes,
-                        smem + C::kOffQSf + (2 * qb + q) * C::kQSfBytes, r);
+      if (q < v.nq) {
+        const uint32_t sb = smem_u32(smem);
+        fq_quant_row<D>(sb + C::kOffQStage + q * (D / 64) * C::kStageBox, sb + C::kOffRtab,
+                        sb + C::kOffQ + (2 * qb + q) * C::kQBytes, sb + C::kOffQSf + (2 * qb + q) * C::kQSfBytes, r);
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.q_full + qb);
       return true;
     };
-    // ... the unit after the current one (g + 1), if the list has one
-    auto fq_next = [&](int g) -> bool {
-      UnitIter t = it;
-      AttnUnitRef v;
-      return unit_next(work, t, v) ? fq_unit(v, g + 1) : true;
-    };
     int us = -1;              // fused Q: index of the current unit over the whole list
-    if constexpr (FQ) ok = fq_next(-1);                // the first unit
     while (ok && unit_next(work, it, u)) {
       const int nq = q ? u.n[1] : u.n[0];
       ++us;
-      if (q >= u.nq) {                                 // the unit has no second query tile
-        if constexpr (FQ) ok = fq_next(us);
-        continue;
+      if constexpr (FQ) {
+        // the next unit's Q (and, for the first unit, its own), so that the S
+        // MMAs find it ready when they reach the next unit
+        for (int k = us == 0 ? 0 : 1; ok && k < 2; ++k) {
+          AttnUnitRef v = u;
+          bool has = true;
+          if (k == 1) {
+            UnitIter t = it;
+            has = unit_next(work, t, v);
+          }
+          if (has) ok = fq_unit(v, us + k);
+        }
+        if (!ok) break;
       }
+      if (q >= u.nq) continue;                         // the unit has no second query tile
       const int qt = u.qt0 + q;
       float m_run = -INFINITY, m_ref = 0.f, lam = 0.f;
       bool have_ref = false;
@@ -773,13 +785,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bars.p_full + q);
       }
       if (!ok) break;
-      // fused Q: the next unit's, so that its S MMAs overlap this epilogue
-      if constexpr (FQ) {
-        if (!fq_next(us)) {
-          ok = false;
-          break;
-        }
-      }
       // ---- the unit's result for this row: O, or a partial for the combine
       // pass (O unnormalised in units of 2^m_ref / 2688 as is lam, m_ref
       // (-inf if no key tile was live) and lam)

@@ -72,8 +72,10 @@ __device__ __forceinline__ uint32_t scale_pair(float a0, float a1) {
   return cvt_e4m3x2(div6_rn(a0), div6_rn(a1));
 }
 
-// Codes of 16 values x[0..15] for scale byte s8: two words.
-__device__ __forceinline__ void codes_group(const float* x, uint32_t s8, const float2* rtab, uint32_t* codes) {
+// Codes of 16 values x[0..15] for scale byte s8: two words.  Tab: the
+// reciprocal table, indexed by the scale byte (a pointer, or SharedRtab).
+template <class Tab>
+__device__ __forceinline__ void codes_group(const float* x, uint32_t s8, const Tab& rtab, uint32_t* codes) {
   const float2 r = rtab[s8];
   float q[16];
 #pragma unroll
@@ -103,6 +105,17 @@ __device__ __forceinline__ float2 rtab_entry(uint32_t s8) {
   return r;
 }
 
+// The reciprocal table at a shared-memory address: lookups are shared-window
+// loads even where the compiler cannot see which window a pointer is in.
+struct SharedRtab {
+  uint32_t base;
+  __device__ __forceinline__ float2 operator[](uint32_t s8) const {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(base + 8u * s8));
+    return v;
+  }
+};
+
 // Row rr (0..127) of a 64-channel x 128-token bf16 box as TMA leaves it with
 // the 128B swizzle (16-byte chunk i of row rr at chunk i ^ (rr & 7)): 32
 // words, channel pair i in word i (channel 2i in the low half).
@@ -122,7 +135,8 @@ __device__ __forceinline__ void load_box_row(const uint8_t* box, int rr, uint32_
 // One quad of Q (64 channels of one token, four 1x16 groups): the codes (8
 // words, channel 8j + e in nibble e of word j) and the scale word (group g in
 // byte g).
-__device__ __forceinline__ void quant_q_quad(const uint32_t (&w)[32], const float2* rtab, uint32_t (&codes)[8],
+template <class Tab>
+__device__ __forceinline__ void quant_q_quad(const uint32_t (&w)[32], const Tab& rtab, uint32_t (&codes)[8],
                                              uint32_t& sfw) {
   float am[4];
 #pragma unroll
