@@ -245,16 +245,39 @@ def run_ours(args, rank, world, local_rank):
         sa.sa_attn_fwd(fq, o=o4, causal=causal, mode="nvfp4", nsplit=0, workspace=ws)
         ev[1].record()
 
+    # the fused-Q mode (Q quantised inside the attention kernel): K and V
+    # through sa_quantize_kv, bf16 Q straight into the attention kernel; the
+    # same work and the same O bytes as the path above (prefill shapes only)
+    fk = None if decode else sa.FP4QKV(B, H, Hkv, Lq, d, device=dev, Lkv=L)
+
+    def step_fq(ev):
+        # ev[0..2]: the two calls timed apart; ev[3..4]: back to back, after
+        # another L2 flush
+        ev[0].record()
+        sa.sa_quantize_kv(k, v, H, Lq=Lq, out=fk)
+        ev[1].record()
+        sa.sa_attn_fwd(q, fk, o=o4, causal=causal, mode="nvfp4_fq", nsplit=0, workspace=ws)
+        ev[2].record()
+        flush_l2()
+        ev[3].record()
+        sa.sa_quantize_kv(k, v, H, Lq=Lq, out=fk)
+        sa.sa_attn_fwd(q, fk, o=o4, causal=causal, mode="nvfp4_fq", nsplit=0, workspace=ws)
+        ev[4].record()
+
     for _ in range(args.warmup):
         flush_l2()
         step([torch.cuda.Event(enable_timing=True) for _ in range(4)])
         flush_l2()
         step_path([torch.cuda.Event(enable_timing=True) for _ in range(2)])
+        if fk is not None:
+            flush_l2()
+            step_fq([torch.cuda.Event(enable_timing=True) for _ in range(5)])
     torch.cuda.synchronize()
     assert sa.sa_last_device_error() == sa.SA_OK
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     evp = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    evf = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -265,6 +288,9 @@ def run_ours(args, rank, world, local_rank):
             step(evs[i])
             flush_l2()
             step_path(evp[i])
+            if fk is not None:
+                flush_l2()
+                step_fq(evf[i])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
     if world > 1:
@@ -272,13 +298,18 @@ def run_ours(args, rank, world, local_rank):
     # sa_quantize: 2 kernels; each attention call: 1, plus a combine kernel
     # when its work is split; per step the breakdown and the path
     n4 = 2 if ws4 > 0 else 1
-    launches = args.steps * ((2 + n4 + (2 if ws16 > 0 else 1)) + (2 + n4))
+    launches = args.steps * ((2 + n4 + (2 if ws16 > 0 else 1)) + (2 + n4) + (2 * (2 + n4) if fk is not None else 0))
     tq = [a[0].elapsed_time(a[1]) * 1e-3 for a in evs]
     t4 = [a[1].elapsed_time(a[2]) * 1e-3 for a in evs]
     t16 = [a[2].elapsed_time(a[3]) * 1e-3 for a in evs]
     tp = [a[0].elapsed_time(a[1]) * 1e-3 for a in evp]
     mean = lambda xs: sum(xs) / len(xs)   # noqa: E731
     t_q, t_4, t_16, t_path = mean(tq), mean(t4), mean(t16), mean(tp)
+    fq_times = None
+    if fk is not None:
+        fq_times = {"quantize_kv_us": mean([a[0].elapsed_time(a[1]) for a in evf]) * 1e3,
+                    "attn_us": mean([a[1].elapsed_time(a[2]) for a in evf]) * 1e3,
+                    "path_us": mean([a[3].elapsed_time(a[4]) for a in evf]) * 1e3}
     # rank 0's own launches for the per-kernel rooflines (its share of the problem)
     # (a folded decode: H = Hkv heads of Lq = G rows each, the same work)
     w_local = dict(w, B=B, H=H, Hkv=Hkv, Lq=Lq, causal=causal)
@@ -378,6 +409,9 @@ def run_ours(args, rank, world, local_rank):
             "bf16_tflops": a16,
             "bf16_attn_us": t_16 * 1e6,
             "bf16_frac_of_measured_peak": a16 / pk["bf16"],
+            "fused_q": (dict(fq_times, attn_traffic_bytes=prof.get("attn_nvfp4_fq"), note="mode nvfp4_fq: sa_quantize_kv + the attention kernel quantising "
+                             "bf16 Q itself (bit-identical O); path_us against path_us above, L2 flushed before "
+                             "each interval") if fq_times is not None else None),
         },
         "roofline": {"kernel": kname4, "bound": "tensor", "achieved": a4, "peak": nvfp4_peak,
                      "unit": "TFLOP/s", "frac": a4 / nvfp4_peak,
