@@ -192,6 +192,52 @@ def test_smooth_q_entry_points_host_checks(sa):
         4 * (16 * 8 * 128) * (128 + 2) * 4                            # split-KV rows of the prefill kernel
 
 
+def test_fused_q_entry_points_host_checks(sa):
+    """sa_quantize_kv_s and the fused-Q attention mode: argument errors before
+    anything is launched, the host path's refusal, the work split (no GPU)."""
+    lib = sa.lib
+    p = ctypes.c_void_p(1 << 20)
+    bad = ctypes.c_void_p(1 << 20 | 8)
+    z = ctypes.c_void_p(0)
+    shape = sa.SaShape(1, 2, 2, 200, 300, 64)
+    good = sa.SaFp4Qkv()
+    assert lib.sa_fp4_qkv_from_blob_s(p, ctypes.byref(shape), ctypes.byref(good)) == sa.SA_OK
+    unset = sa.SaFp4Qkv()
+    # sa_quantize_kv_s
+    assert lib.sa_quantize_kv_s(p, p, None, 0, ctypes.byref(good), None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_quantize_kv_s(p, p, ctypes.byref(shape), 64, ctypes.byref(good), None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_quantize_kv_s(bad, p, ctypes.byref(shape), 0, ctypes.byref(good), None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_quantize_kv_s(p, bad, ctypes.byref(shape), 0, ctypes.byref(good), None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_quantize_kv_s(p, p, ctypes.byref(shape), 0, None, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_quantize_kv_s(p, p, ctypes.byref(shape), 0, ctypes.byref(unset), None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_quantize_kv_s(p, p, ctypes.byref(sa.SaShape(1, 2, 2, 200, 300, 80)), 0, ctypes.byref(good),
+                                None) == sa.SA_ERR_UNSUPPORTED
+    assert lib.sa_quantize_kv_s(p, p, ctypes.byref(sa.SaShape(1, 3, 2, 200, 300, 64)), 0, ctypes.byref(good),
+                                None) == sa.SA_ERR_INVALID_ARG               # H not a multiple of Hkv
+    assert lib.sa_quantize_kv_s(z, z, ctypes.byref(sa.SaShape(0, 2, 2, 200, 300, 64)), 0, None, None) == sa.SA_OK
+    # attention in the fused-Q mode: q the bf16 Q (16-byte aligned), k the
+    # K/V struct, v NULL
+    kp = ctypes.cast(ctypes.pointer(good), ctypes.c_void_p)
+    up = ctypes.cast(ctypes.pointer(unset), ctypes.c_void_p)
+    fq = sa.SA_MODE_NVFP4_FQ
+    assert lib.sa_attn_fwd(z, kp, z, p, 1, 2, 2, 256, 64, 0, fq, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_attn_fwd(p, z, z, p, 1, 2, 2, 256, 64, 0, fq, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_attn_fwd(p, kp, p, p, 1, 2, 2, 256, 64, 0, fq, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_attn_fwd(bad, kp, z, p, 1, 2, 2, 256, 64, 0, fq, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_attn_fwd(p, up, z, p, 1, 2, 2, 256, 64, 0, fq, None) == sa.SA_ERR_INVALID_ARG
+    assert lib.sa_attn_fwd(z, z, z, z, 0, 2, 2, 256, 64, 0, fq, None) == sa.SA_OK           # an empty problem
+    # the host-buffer path does not take it
+    assert lib.sa_attn_fwd_host(p, p, p, p, 1, 2, 2, 256, 64, 0, fq, p, 1 << 30, 0, None) == sa.SA_ERR_UNSUPPORTED
+    assert lib.sa_attn_fwd_host_workspace_bytes(1, 2, 2, 256, 64, fq, 0) == 0
+    # the prefill kernel's work split, also for few query rows per kv head
+    big = sa.SaShape(2, 16, 16, 4096, 4096, 128)
+    assert lib.sa_attn_fwd_workspace_bytes_s(ctypes.byref(big), 0, fq, -1) == \
+        lib.sa_attn_fwd_workspace_bytes_s(ctypes.byref(big), 0, sa.SA_MODE_NVFP4, -1) > 0
+    dec = sa.SaShape(16, 8, 2, 1, 8192, 128)                         # 4 query rows per kv head
+    assert lib.sa_attn_fwd_workspace_bytes_s(ctypes.byref(dec), 0, fq, 4) == \
+        lib.sa_attn_fwd_workspace_bytes_s(ctypes.byref(dec), 0, sa.SA_MODE_NVFP4_SQ, 4)
+
+
 def test_product_path_has_no_oracle_dependency():
     pkg = os.path.join(ROOT, "quantized_attention_x16_gb300")
     for dirpath, _, files in os.walk(pkg):
