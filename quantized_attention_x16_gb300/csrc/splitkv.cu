@@ -12,8 +12,10 @@
 // The P quantisation is per key tile, and shares are whole key tiles, so the
 // split changes only the float32 summation order.
 //
-// Eight lanes per row, four rows per warp; lane i of a row holds d/8
-// consecutive columns.  Small: it reads nsplit * d + 2 floats per row, from
+// Eight lanes per row, four rows per warp; lane i of a row holds columns
+// 32j + 4i .. 32j + 4i + 3 (j < d/32), so that the eight lanes of a row read
+// 128 contiguous bytes of a partial row per load and write contiguous output
+// per store.  Small: it reads nsplit * d + 2 floats per row, from
 // L2 as a rule, so its cost is load latency and the per-row scalar work (the
 // weights 2^(m_s - M) and 1 / l); the loads of up to four partial rows are
 // issued together and the scalar work is shared by eight lanes instead of 32.
@@ -34,8 +36,8 @@ constexpr int kRowsPerCta = 256 / kLanesPerRow;          // 256 threads, 32 rows
 constexpr int kSegBatch = 4;                             // partial rows whose loads are issued together
 
 // Merges the nseg partial rows seg(0), seg(1), ... of one output row; called
-// by the kLanesPerRow lanes of the row, lane i of them holding columns
-// [i*V, i*V + V), V = D / kLanesPerRow.  The loads of kSegBatch segments
+// by the kLanesPerRow lanes of the row, lane i of them holding the columns
+// 32j + 4i + c (out[4j + c], j < D/32, c < 4).  The loads of kSegBatch segments
 // (their (m, l) and their O rows) are issued before any is used, so a row
 // costs one memory round trip with up to four segments; the
 // arithmetic is the same in every case: M first, then the weighted sums in
@@ -52,9 +54,9 @@ __device__ __forceinline__ void merge_partials(const SplitOut& part, int nseg, S
   auto load = [&](int k, float2& ml, float4 (&a)[V4]) {
     const long long r = seg(k);
     ml = *reinterpret_cast<const float2*>(part.ml + 2 * r);
-    const float4* src = reinterpret_cast<const float4*>(part.o + r * D + sub * V);
+    const float4* src = reinterpret_cast<const float4*>(part.o + r * D);
 #pragma unroll
-    for (int j = 0; j < V4; ++j) a[j] = src[j];
+    for (int j = 0; j < V4; ++j) a[j] = src[j * kLanesPerRow + sub];
   };
   auto accumulate = [&](const float2& ml, const float4 (&a)[V4]) {
     if (!(ml.y > 0.f)) return;                          // an empty segment (its O row is not read)
@@ -113,26 +115,25 @@ __device__ __forceinline__ void merge_partials(const SplitOut& part, int nseg, S
   for (int c = 0; c < V; ++c) out[c] = acc[c] * inv;
 }
 
-// Stores a lane's V = D / kLanesPerRow consecutive output columns (rows are
-// 16-byte aligned).
+// Stores a lane's columns 32j + 4i + c of the output row starting at element
+// idx (rows are 16-byte aligned; i = the lane's index within its row).
 template <int D, bool OUT32>
 __device__ __forceinline__ void store_row_part(void* out, long long idx, const float (&v)[D / kLanesPerRow]) {
-  constexpr int V = D / kLanesPerRow;
+  constexpr int V4 = D / kLanesPerRow / 4;
+  const int sub = threadIdx.x % kLanesPerRow;
   if constexpr (OUT32) {
     float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + idx);
 #pragma unroll
-    for (int j = 0; j < V / 4; ++j) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    for (int j = 0; j < V4; ++j)
+      o[j * kLanesPerRow + sub] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
   } else {
-    uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + idx);
+    uint2* o = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + idx);
 #pragma unroll
-    for (int j = 0; j < V / 8; ++j) {
-      uint32_t w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
-        w[i] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      o[j] = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int j = 0; j < V4; ++j) {
+      const __nv_bfloat162 h0 = __floats2bfloat162_rn(v[4 * j], v[4 * j + 1]);
+      const __nv_bfloat162 h1 = __floats2bfloat162_rn(v[4 * j + 2], v[4 * j + 3]);
+      o[j * kLanesPerRow + sub] =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
     }
   }
 }
@@ -145,13 +146,11 @@ __global__ void __launch_bounds__(kRowsPerCta * kLanesPerRow) splitkv_combine_ke
   pdl_wait();                                        // the partial results are written
   const long long row = (long long)blockIdx.x * kRowsPerCta + threadIdx.x / kLanesPerRow;
   if (row >= nrows) return;
-  const int sub = threadIdx.x % kLanesPerRow;
   const long long bh = row / L;
   const long long prow = bh * Lp + row % L;          // row in the padded partial layout
   float v[D / kLanesPerRow];
   merge_partials<D>(part, nsplit, [&](int s) { return s * split_rows + prow; }, v);
-  store_row_part<D, OUT32>(out, (bh / H) * so.b + (bh % H) * so.h + (row % L) * so.t + sub * (D / kLanesPerRow),
-                           v);
+  store_row_part<D, OUT32>(out, (bh / H) * so.b + (bh % H) * so.h + (row % L) * so.t, v);
 }
 
 template <int D, bool OUT32>
@@ -182,14 +181,10 @@ __global__ void __launch_bounds__(kRowsPerCta * kLanesPerRow) streamk_combine_ke
   const int rr = blockIdx.y * kRowsPerCta + threadIdx.x / kLanesPerRow;   // row of the pair (query tile rr / 128)
   const int t = qt0 * 128 + rr;                                  // its token
   if (rr >= nq * 128 || t >= L) return;
-  const int sub = threadIdx.x % kLanesPerRow;
   float v[D / kLanesPerRow];
   merge_partials<D>(
       part, nseg, [&](int k) { return (long long)(2 * (cta0 + k) + (k == 0 ? first_last : 0)) * 256 + rr; }, v);
-  store_row_part<D, OUT32>(out,
-                           (long long)(bh / H) * so.b + (long long)(bh % H) * so.h + (long long)t * so.t +
-                               sub * (D / kLanesPerRow),
-                           v);
+  store_row_part<D, OUT32>(out, (long long)(bh / H) * so.b + (long long)(bh % H) * so.h + (long long)t * so.t, v);
 }
 
 template <int D, bool OUT32>
