@@ -85,7 +85,6 @@ struct QuantArgs {
   int tph_q, tph_k;                 // tiles per head of Q and of K / V
   uint32_t dq_m, dq_l, dk_m, dk_l;  // u / tph_q and u / tph_k as (umulhi(u, m) + u) >> l
   int ntile_q, ntile_k;             // Q tiles; K tiles (= V tiles = mean tiles)
-  int range2;                       // pass 2: K' tiles per CTA (the last CTAs may have fewer)
   uint64_t wait_ns;
 };
 
@@ -307,7 +306,10 @@ __global__ void __launch_bounds__(kThreadsQ, kCtasPerSm)
   const int G = gridDim.x, c = blockIdx.x;
   const int n1 = a.ntile_q + a.ntile_k;
   const int nv = c < a.ntile_k ? (a.ntile_k - c + G - 1) / G : 0;
-  const int k0 = min(a.ntile_k, c * a.range2), nk = min(a.ntile_k, k0 + a.range2) - k0;
+  // pass 2: K' tiles cut into G near-equal contiguous ranges (the first
+  // ntile_k % G of them one tile longer)
+  const int kq = a.ntile_k / G, kr = a.ntile_k % G;
+  const int k0 = c * kq + min(c, kr), nk = kq + (c < kr ? 1 : 0);
   const int kh0 = k0 / a.tph_k;                         // first head of the K' range
   const int ntiles = PASS == 1 ? (c < n1 ? (n1 - c + G - 1) / G : 0) : nv + nk;
   auto tile_at = [&](int i) {
@@ -451,12 +453,14 @@ cudaError_t launch_quantize_impl(const Dims& dm, const sa_fp4_qkv& out, float* p
   // mean tiles instead of taking only one kind
   const int odd_slots = (slots & 1) ? slots : slots - 1;
   const int grid1 = n1 < odd_slots ? n1 : odd_slots;
-  // pass 2: K' ranges spanning at most kMaxMeanHeads heads (a range of r
-  // tiles spans at most ceil((r - 1) / tph_k) + 1 heads); one per CTA
-  int range2 = (a.ntile_k + slots - 1) / slots;
-  if (range2 > (kMaxMeanHeads - 1) * a.tph_k + 1) range2 = (kMaxMeanHeads - 1) * a.tph_k + 1;
-  a.range2 = range2;
-  const int grid2 = (a.ntile_k + range2 - 1) / range2;
+  // pass 2: one CTA per slot (fewer with fewer K tiles), each over a
+  // near-equal contiguous range of K' tiles (floor or ceil of ntile_k /
+  // grid2: every slot busy, no SM with twice the tiles of another) spanning
+  // at most kMaxMeanHeads heads (a range of r tiles spans at most
+  // ceil((r - 1) / tph_k) + 1 heads)
+  const int max_range = (kMaxMeanHeads - 1) * a.tph_k + 1;
+  int grid2 = a.ntile_k < slots ? a.ntile_k : slots;
+  if (grid2 < (a.ntile_k + max_range - 1) / max_range) grid2 = (a.ntile_k + max_range - 1) / max_range;
   quant_kernel<D, 1><<<grid1, kThreadsQ, kSmemQ, s>>>(tq, tk, tv, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
