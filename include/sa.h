@@ -239,13 +239,14 @@ sa_status sa_quantize_static_scratch(const void* q, const void* k, const void* v
  *   out->q_sf are neither read nor written (may be NULL).  Arguments and
  *   errors as sa_quantize_s without q.  Two kernels on `stream`.
  * sa_attn_fwd(_ws, _s) with mode SA_MODE_NVFP4_FQ: q is the bf16 Q device
- *   tensor (BHLD, or BLHD with SA_LAYOUT_BLHD), k points to a host `const
- *   sa_fp4_qkv*` from sa_quantize_kv_s for the same sizes, v must be NULL.
- *   The attention kernel loads each unit's bf16 Q tiles by TMA and one of its
- *   warps quantises them with sa_quantize's arithmetic, so O is bit-identical
- *   to sa_quantize + SA_MODE_NVFP4 on the same work split (the few-row decode
- *   kernel is not used: such shapes run on the prefill kernel).
- *   sa_attn_fwd_host does not take it (SA_ERR_UNSUPPORTED).
+ *   tensor (BHLD, or BLHD with SA_LAYOUT_BLHD; 16-byte aligned, else
+ *   SA_ERR_INVALID_ARG), k points to a host `const sa_fp4_qkv*` from
+ *   sa_quantize_kv_s for the same sizes, v must be NULL.  The attention
+ *   kernel copies each unit's bf16 Q tiles by TMA into shared memory and its
+ *   softmax threads quantise their own rows with sa_quantize's arithmetic,
+ *   so O is bit-identical to sa_quantize + SA_MODE_NVFP4 on the same work
+ *   split (the few-row decode kernel is not used: such shapes run on the
+ *   prefill kernel).  sa_attn_fwd_host does not take it (SA_ERR_UNSUPPORTED).
  */
 sa_status sa_quantize_kv_s(const void* k, const void* v, const sa_shape* shape, int flags, const sa_fp4_qkv* out,
                            sa_stream_t stream);
