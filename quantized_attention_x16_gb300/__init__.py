@@ -250,16 +250,29 @@ class FP4QKV:
         return out
 
 
-def _dims(q, k, layout):
+def _dims(q, k, layout, v=None):
     """(B, H, Hkv, Lq, Lkv, d) of q [B, H, Lq, d] / k [B, Hkv, Lkv, d] (layout
-    "bhld") or q [B, Lq, H, d] / k [B, Lkv, Hkv, d] ("blhd"), and the layout flag."""
+    "bhld") or q [B, Lq, H, d] / k [B, Lkv, Hkv, d] ("blhd"), and the layout
+    flag; v, when given, must have k's shape.  (The library reads every
+    tensor with these sizes, so a mismatch is refused here.)"""
     if layout == "bhld":
         B, H, L, d = q.shape
-        return (B, H, k.shape[1], L, k.shape[2], d), 0
-    if layout == "blhd":
+        dims, flag = (B, H, k.shape[1], L, k.shape[2], d), 0
+    elif layout == "blhd":
         B, L, H, d = q.shape
-        return (B, H, k.shape[2], L, k.shape[1], d), SA_LAYOUT_BLHD
-    raise ValueError(f"unknown layout {layout!r}")
+        dims, flag = (B, H, k.shape[2], L, k.shape[1], d), SA_LAYOUT_BLHD
+    else:
+        raise ValueError(f"unknown layout {layout!r}")
+    if k.shape[0] != B or k.shape[3] != d:
+        raise ValueError(f"k {tuple(k.shape)} does not match q {tuple(q.shape)} (batch and head size)")
+    if v is not None and tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"v {tuple(v.shape)} must have k's shape {tuple(k.shape)}")
+    return dims, flag
+
+
+def _check_out(out, B, H, Hkv, L, Lkv, d):
+    if not isinstance(out, FP4QKV) or out.dims != (B, H, Hkv, L, d) or out.Lkv != Lkv:
+        raise ValueError(f"out must be an FP4QKV for B={B} H={H} Hkv={Hkv} L={L} Lkv={Lkv} d={d}")
 
 
 def sa_quantize(q, k, v, out=None, stream=None, layout="bhld", smooth_q=False):
@@ -269,9 +282,10 @@ def sa_quantize(q, k, v, out=None, stream=None, layout="bhld", smooth_q=False):
     128-token block means, the block means and the score corrections), for
     sa_attn_fwd(mode="nvfp4_sq")."""
     _bf16_cuda(q, "q"), _bf16_cuda(k, "k"), _bf16_cuda(v, "v")
-    (B, H, Hkv, L, Lkv, d), flag = _dims(q, k, layout)
+    (B, H, Hkv, L, Lkv, d), flag = _dims(q, k, layout, v)
     if out is None:
         out = FP4QKV(B, H, Hkv, L, d, device=q.device, Lkv=Lkv)
+    _check_out(out, B, H, Hkv, L, Lkv, d)
     shape = SaShape(B, H, Hkv, L, Lkv, d)
     _check(lib.sa_quantize_s(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shape), flag, ctypes.byref(out.struct),
                              _stream(stream)), "sa_quantize_s")
@@ -296,9 +310,12 @@ def sa_quantize_kv(k, v, H, Lq=None, out=None, stream=None, layout="bhld"):
         flag = SA_LAYOUT_BLHD
     else:
         raise ValueError(f"unknown layout {layout!r}")
+    if tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"v {tuple(v.shape)} must have k's shape {tuple(k.shape)}")
     Lq = Lkv if Lq is None else Lq
     if out is None:
         out = FP4QKV(B, H, Hkv, Lq, d, device=k.device, Lkv=Lkv)
+    _check_out(out, B, H, Hkv, Lq, Lkv, d)
     shape = SaShape(B, H, Hkv, Lq, Lkv, d)
     _check(lib.sa_quantize_kv_s(_ptr(k), _ptr(v), ctypes.byref(shape), flag, ctypes.byref(out.struct),
                                 _stream(stream)), "sa_quantize_kv_s")
@@ -309,10 +326,12 @@ def sa_quantize_static_scratch(q, k, v, out=None, stream=None):
     """sa_quantize without caller-provided scratch (see sa.h): the K-mean partial
     sums live in the library's fixed per-device array.  Returns an FP4QKV."""
     _bf16_cuda(q, "q"), _bf16_cuda(k, "k"), _bf16_cuda(v, "v")
-    B, H, L, d = q.shape
-    Hkv = k.shape[1]
+    (B, H, Hkv, L, Lkv, d), _ = _dims(q, k, "bhld", v)
+    if Lkv != L:
+        raise ValueError("sa_quantize_static_scratch takes equal query and key lengths")
     if out is None:
         out = FP4QKV(B, H, Hkv, L, d, device=q.device)
+    _check_out(out, B, H, Hkv, L, L, d)
     _check(lib.sa_quantize_static_scratch(_ptr(q), _ptr(k), _ptr(v), B, H, Hkv, L, d, ctypes.byref(out.struct),
                                           _stream(stream)),
            "sa_quantize_static_scratch")
@@ -344,7 +363,7 @@ def sa_attn_fwd(q, k=None, v=None, o=None, causal=False, mode="bf16", out_dtype=
     lflag = SA_LAYOUT_BLHD if layout == "blhd" else 0
     if mode == "bf16":
         _bf16_cuda(q, "q"), _bf16_cuda(k, "k"), _bf16_cuda(v, "v")
-        (B, H, Hkv, L, Lkv, d), _ = _dims(q, k, layout)
+        (B, H, Hkv, L, Lkv, d), _ = _dims(q, k, layout, v)
         args = (_ptr(q), _ptr(k), _ptr(v))
         m = SA_MODE_BF16
         dev = q.device
@@ -429,6 +448,9 @@ def sa_attn_fwd_host(q, k, v, o=None, causal=False, mode="nvfp4", out_dtype=None
     _bf16_pinned(q, "q"), _bf16_pinned(k, "k"), _bf16_pinned(v, "v")
     B, H, L, d = q.shape
     Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, L, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"k and v must be [B, Hkv, L, d] with q's B, L and d (q {tuple(q.shape)}, "
+                         f"k {tuple(k.shape)}, v {tuple(v.shape)})")
     if out_dtype is None:
         out_dtype = o.dtype if o is not None else torch.bfloat16
     if out_dtype not in (torch.bfloat16, torch.float32):

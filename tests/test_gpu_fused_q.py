@@ -129,3 +129,27 @@ def test_fused_q_full_size_bit_identical(sa, name):
     torch.cuda.synchronize()
     assert sa.sa_last_device_error() == 0
     assert torch.equal(o2, of)
+
+
+def test_binding_refuses_mismatched_shapes(sa):
+    """The binding checks q, k, v and the output blob against each other before
+    any launch (the library reads every tensor with the sizes it is given)."""
+    x = W.make_inputs(dict(W.spec("tiny")))
+    q, k, v = (x[n].cuda() for n in "qkv")
+    short_v = v[:, :, :128].contiguous()
+    other_d = torch.zeros(1, 2, 256, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):
+        sa.sa_quantize(q, k, short_v)
+    with pytest.raises(ValueError):
+        sa.sa_quantize(q, other_d, other_d)
+    with pytest.raises(ValueError):
+        sa.sa_quantize_kv(k, short_v, 2)
+    with pytest.raises(ValueError):
+        sa.sa_attn_fwd(q, k, short_v, mode="bf16")
+    f_small = sa.FP4QKV(1, 2, 2, 128, 64, device="cuda")
+    with pytest.raises(ValueError):
+        sa.sa_quantize(q, k, v, out=f_small)
+    with pytest.raises(ValueError):
+        sa.sa_quantize_kv(k, v, 2, out=f_small)
+    torch.cuda.synchronize()
+    assert sa.sa_last_device_error() == 0
