@@ -397,3 +397,50 @@ def test_decode_grouped_heads_fold(sa, mode, causal):
     torch.cuda.synchronize()
     assert sa.sa_last_device_error() == 0
     assert torch.equal(of.view(B, H, 1, d).view(torch.int16), o.view(torch.int16))
+
+
+def _random_cases(n, seed=77):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        d = int(rng.choice([64, 128]))
+        Hkv = int(rng.choice([1, 2]))
+        G = int(rng.choice([1, 2, 4]))
+        B = int(rng.integers(1, 3))
+        Lkv = int(rng.integers(1, 1100))
+        Lq = int(rng.choice([Lkv, int(rng.integers(1, Lkv + 1))]))
+        out.append((B, Hkv * G, Hkv, Lq, Lkv, d, bool(rng.integers(0, 2)), str(rng.choice(["bhld", "blhd"])),
+                    [None, 0, 2, -1][int(rng.integers(0, 4))]))
+    return out
+
+
+@pytest.mark.parametrize("mode", ["bf16", "nvfp4"])
+@pytest.mark.parametrize("case", _random_cases(12), ids=lambda s: "B{}H{}K{}Lq{}Lkv{}d{}c{}{}s{}".format(*s))
+def test_random_shapes_all_rows(sa, case, mode):
+    """Seeded random shapes (ragged lengths, MQA/GQA, Lq <= Lkv, both masks and
+    layouts, every work split, decode shapes included) against the oracle,
+    every row of every head."""
+    B, H, Hkv, Lq, Lkv, d, causal, layout, nsplit = case
+    if nsplit == -1 and mode == "bf16":
+        nsplit = 0                                     # (stream-K is a schedule of the NVFP4 path)
+    g = torch.Generator().manual_seed(Lq * 7919 + Lkv)
+    x = dict(q=torch.randn(B, H, Lq, d, generator=g).to(torch.bfloat16),
+             k=torch.randn(B, Hkv, Lkv, d, generator=g).to(torch.bfloat16),
+             v=torch.randn(B, Hkv, Lkv, d, generator=g).to(torch.bfloat16))
+    tr = (lambda t: t.transpose(1, 2).contiguous()) if layout == "blhd" else (lambda t: t)
+    q, k, v = (tr(x[n]).cuda() for n in "qkv")
+
+    def run(dt):
+        if mode == "nvfp4":
+            f = sa.sa_quantize(q, k, v, layout=layout)
+            o = sa.sa_attn_fwd(f, causal=causal, mode="nvfp4", nsplit=nsplit, out_dtype=dt, layout=layout)
+        else:
+            o = sa.sa_attn_fwd(q, k, v, causal=causal, mode="bf16", nsplit=nsplit, out_dtype=dt, layout=layout)
+        torch.cuda.synchronize()
+        assert sa.sa_last_device_error() == 0
+        return tr(o).float().cpu().numpy()
+
+    o = run(torch.bfloat16)
+    o32 = run(torch.float32) if mode == "nvfp4" else None
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    check(o, x, causal, heads, np.arange(Lq), mode, o32, label="random B{}H{}K{}Lq{}Lkv{}d{}".format(*case[:6]))
