@@ -144,18 +144,22 @@ __device__ __forceinline__ TileRef pass2_tile(const QuantArgs& a, int c, int G, 
            : head_tile<D>(kTileK, k0 + j, a.tph_k, a.dk_m, a.dk_l);
 }
 
-// Issues the two box copies of tile t into dst.
+// Issues the two box copies of tile t into dst.  K read for its mean (pass
+// 1) is kept in L2 for pass 2's K' tiles (evict_last); every other read is
+// the data's last (evict_first), which leaves L2 to K and to the outputs the
+// attention kernel reads next.
 template <int D>
 __device__ __forceinline__ void issue_tile(const TileRef& t, const CUtensorMap* tq, const CUtensorMap* tk,
                                            const CUtensorMap* tv, const QuantArgs& a, uint8_t* dst, uint64_t* bar) {
   const CUtensorMap* map = t.kind == kTileQ ? tq : (t.kind == kTileV ? tv : tk);
   const int heads = t.kind == kTileQ ? a.H : a.Hkv;
+  const uint64_t pol = t.kind == kTileMean ? l2_policy_evict_last() : l2_policy_evict_first();
   mbar_arrive_expect_tx(bar, kTileBytes);
 #pragma unroll
   for (int b = 0; b < 2; ++b) {
     const int x = D == 128 ? 64 * b : 0;
     const int y = D == 128 ? t.t0 : t.t0 + 128 * b;
-    tma_load_4d(dst + b * kBoxBytes, map, bar, x, y, t.bh % heads, t.bh / heads);
+    tma_load_4d_hint(dst + b * kBoxBytes, map, bar, x, y, t.bh % heads, t.bh / heads, pol);
   }
 }
 
