@@ -527,11 +527,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       kStageSleepNs);
         if (!ok) break;
         if (leader) {
+          // (bf16 Q is read once: its lines go first when L2 needs room)
+          const uint64_t pol = l2_policy_evict_first();
           mbar_arrive_expect_tx(bars.qs_full, u.nq * (D / 64) * C::kStageBox);
           for (int q = 0; q < u.nq; ++q)
             for (int b = 0; b < D / 64; ++b)
-              tma_load_4d(smem + C::kOffQStage + (q * (D / 64) + b) * C::kStageBox, &tmap_q, bars.qs_full, 64 * b,
-                          (u.qt0 + q) * BM, (int)(u.bh % H), (int)(u.bh / H));
+              tma_load_4d_hint(smem + C::kOffQStage + (q * (D / 64) + b) * C::kStageBox, &tmap_q, bars.qs_full,
+                               64 * b, (u.qt0 + q) * BM, (int)(u.bh % H), (int)(u.bh / H), pol);
         }
         __syncwarp();
         ++ug;
