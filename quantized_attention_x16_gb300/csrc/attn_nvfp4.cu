@@ -824,12 +824,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
             continue;
           }
+          // (O is not read again here: streaming stores, so that its lines
+          // leave L2 before the K and V tiles other CTAs still read)
           if constexpr (OUT32) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_ptr) + obase + 32 * cc);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
-                                   __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+              __stcs(dst + i, make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                          __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l));
           } else {
             uint32_t w[16];
 #pragma unroll
@@ -837,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_ptr) + obase + 32 * cc);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            for (int i = 0; i < 4; ++i) __stcs(dst + i, make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]));
           }
         }
         // (the tensor-memory loads above are complete: the next unit's first
