@@ -156,7 +156,7 @@ def run_reference(args, rank, world):
             vals.append(fl / dt / 1e12)
     v = statistics.median(vals)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TOPS", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "strong",
             "vs_baseline": None, "dtype": "f64/f32 (CPU oracle)", "data": "synthetic",
             "config": {"workload": f"{workload_str(w)} {'causal' if w['causal'] else 'non-causal'}",
                        "sample": desc},
