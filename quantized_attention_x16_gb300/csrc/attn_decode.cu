@@ -49,7 +49,6 @@ constexpr int kDecNSV = 2;                   // V stages (released by P.V, a til
 constexpr int kKeys = 128;                   // keys per tile
 constexpr float kLog2PRangeDec = 11.392317422778761f;   // log2(448 * 6)
 constexpr float kSkipBelowDec = 64.0f;                   // log2 units
-constexpr uint32_t kPollPNs = 64;                        // the MMA warp's sleep between polls of P^T
 
 template <int D>
 struct CfgDec {
@@ -416,12 +415,8 @@ __global__ void __launch_bounds__(kDecThreads, dec_ctas_per_sm<NR>())
           const DecSeg sg = dec_seg<RANGES>(a, cta, pk);
           pseg_n = sg.j1 - sg.j0;
         }
-        // P^T(gv) takes the softmax warps a whole key tile; its P.V has a tile
-        // of slack (the accumulator is rescaled a tile later), so the wait
-        // sleeps between polls and leaves the issue slots of the scheduler it
-        // shares to the softmax warp there
         ok = mbar_wait_warp(v_full + s, (gv / C::NSV) & 1, abort_flag, a.wait_ns) &&
-             mbar_wait_backoff_warp(p_full + (gv & 1), (gv >> 1) & 1, abort_flag, a.wait_ns, kPollPNs);
+             mbar_wait_warp(p_full + (gv & 1), (gv >> 1) & 1, abort_flag, a.wait_ns);
         if (!ok) break;
         tc_fence_after();
         const uint32_t sfv = tbase + C::kColSfV + 8 * (gv & 1), sfp = tbase + C::kColSfP + 8 * (gv & 1);
